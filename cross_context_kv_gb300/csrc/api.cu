@@ -1,0 +1,376 @@
+// api.cu -- the C ABI of libkvfix: argument checks, error reporting, launches.
+// Every public call validates its arguments on the host, returns KVFIX_EINVAL with a
+// message before anything is enqueued, and otherwise enqueues kernels on `stream`.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "internal.h"
+
+namespace kvfix {
+
+static thread_local char g_last_error[512] = "";
+
+kvfix_status fail(kvfix_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+kvfix_status cuda_fail(cudaError_t err, const char* what) {
+    return fail(KVFIX_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
+}
+
+RopeTheta make_theta(double base, int head_dim) {
+    RopeTheta t;
+    memset(&t, 0, sizeof t);
+    for (int i = 0; i < head_dim / 2; ++i) t.theta[i] = pow(base, -2.0 * (double)i / (double)head_dim);
+    return t;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Checks one plane descriptor and its pointer.  `what` names the argument.
+static kvfix_status check_plane(const void* ptr, const kvfix_kv_desc& d, const char* what,
+                                bool allow_null = false) {
+    if (ptr == nullptr && !allow_null) return fail(KVFIX_EINVAL, "%s: null pointer", what);
+    if (d.chunks < 0 || d.layers < 0 || d.tokens < 0)
+        return fail(KVFIX_EINVAL, "%s: negative chunks/layers/tokens", what);
+    if (d.kv_heads < 1 || d.head_dim < 16 || d.head_dim > kMaxHeadDim || d.head_dim % 16 != 0)
+        return fail(KVFIX_EINVAL, "%s: kv_heads must be >= 1 and head_dim a multiple of 16 in [16, %d] (got %d heads x %d)",
+                    what, kMaxHeadDim, d.kv_heads, d.head_dim);
+    if (d.stride_chunk < 0 || d.stride_layer < 0 || d.stride_token < 0)
+        return fail(KVFIX_EINVAL, "%s: negative stride", what);
+    if (d.stride_chunk % 8 || d.stride_layer % 8 || d.stride_token % 8)
+        return fail(KVFIX_EINVAL, "%s: strides must be multiples of 8 elements (16 bytes)", what);
+    const long long row = (long long)d.kv_heads * d.head_dim;
+    if (d.tokens > 1 && d.stride_token < row)
+        return fail(KVFIX_EINVAL, "%s: stride_token %lld is smaller than a token row (%lld)", what,
+                    (long long)d.stride_token, row);
+    if (ptr && !aligned16(ptr)) return fail(KVFIX_EINVAL, "%s: pointer not 16-byte aligned", what);
+    return KVFIX_OK;
+}
+
+static bool same_shape(const kvfix_kv_desc& a, const kvfix_kv_desc& b) {
+    return a.layers == b.layers && a.tokens == b.tokens && a.kv_heads == b.kv_heads &&
+           a.head_dim == b.head_dim;
+}
+
+// Byte extent [lo, hi) touched by a plane view.
+static void extent(const void* p, const kvfix_kv_desc& d, uintptr_t* lo, uintptr_t* hi) {
+    const long long row = (long long)d.kv_heads * d.head_dim;
+    long long last = 0;
+    if (d.chunks > 0 && d.layers > 0 && d.tokens > 0)
+        last = (long long)(d.chunks - 1) * d.stride_chunk + (long long)(d.layers - 1) * d.stride_layer +
+               (long long)(d.tokens - 1) * d.stride_token + row;
+    *lo = (uintptr_t)p;
+    *hi = (uintptr_t)p + 2 * (uintptr_t)last;
+}
+
+static bool overlaps(const void* a, const kvfix_kv_desc& da, const void* b, const kvfix_kv_desc& db) {
+    if (!a || !b) return false;
+    uintptr_t a0, a1, b0, b1;
+    extent(a, da, &a0, &a1);
+    extent(b, db, &b0, &b1);
+    return a0 < b1 && b0 < a1;
+}
+
+static bool overlaps_bytes(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || !na || !nb) return false;
+    uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+static kvfix_status launched(cudaError_t e, const char* what) {
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return KVFIX_OK;
+}
+
+}  // namespace kvfix
+
+using namespace kvfix;
+
+extern "C" {
+
+int kvfix_version(void) { return 100; }
+
+const char* kvfix_last_error(void) { return g_last_error; }
+
+kvfix_status kvfix_check_status(void* stream) {
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "kvfix_check_status: stream synchronize");
+    unsigned bits = read_status_repair(s) | read_status_diff(s) | read_status_draft(s);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "kvfix_check_status: status read");
+    if (bits & 4u) return fail(KVFIX_ETIMEOUT, "a bounded device wait gave up");
+    if (bits & 2u) return fail(KVFIX_ENOSPACE, "diff payload entries beyond the capacity were skipped");
+    if (bits & 1u) return fail(KVFIX_EDEVICE, "an index in caller data was out of range and skipped");
+    g_last_error[0] = '\0';
+    return KVFIX_OK;
+}
+
+kvfix_status kvfix_rerope(const kvfix_bf16* k_in, kvfix_bf16* k_out, kvfix_kv_desc desc,
+                          const int32_t* delta, double rope_base, void* stream) {
+    kvfix_status st;
+    if ((st = check_plane(k_in, desc, "kvfix_rerope: k_in")) != KVFIX_OK) return st;
+    if ((st = check_plane(k_out, desc, "kvfix_rerope: k_out")) != KVFIX_OK) return st;
+    if (desc.chunks > 0 && delta == nullptr) return fail(KVFIX_EINVAL, "kvfix_rerope: delta is null");
+    if (!(rope_base > 1.0) || !isfinite(rope_base))
+        return fail(KVFIX_EINVAL, "kvfix_rerope: rope_base must be finite and > 1");
+    if (k_in != k_out && overlaps(k_in, desc, k_out, desc))
+        return fail(KVFIX_EINVAL, "kvfix_rerope: k_out partially overlaps k_in");
+    RopeTheta th = make_theta(rope_base, desc.head_dim);
+    return launched(launch_rerope(k_in, k_out, desc, delta, th, (cudaStream_t)stream), "kvfix_rerope");
+}
+
+kvfix_status kvfix_score_topk(const kvfix_bf16* k_reuse, const kvfix_bf16* v_reuse,
+                              kvfix_kv_desc reuse, const kvfix_bf16* k_fresh,
+                              const kvfix_bf16* v_fresh, kvfix_kv_desc fresh, int32_t agents,
+                              const int32_t* delta, double rope_base, int32_t b, float* d_k,
+                              float* d_v, float* w_k, float* w_v, int32_t* idx_k, int32_t* idx_v,
+                              uint32_t* mask_k, uint32_t* mask_v, uint32_t* mask_union,
+                              void* stream) {
+    kvfix_status st;
+    const char* fn = "kvfix_score_topk";
+    if ((st = check_plane(k_reuse, reuse, "kvfix_score_topk: k_reuse")) != KVFIX_OK) return st;
+    if ((st = check_plane(v_reuse, reuse, "kvfix_score_topk: v_reuse")) != KVFIX_OK) return st;
+    if ((st = check_plane(k_fresh, fresh, "kvfix_score_topk: k_fresh")) != KVFIX_OK) return st;
+    if ((st = check_plane(v_fresh, fresh, "kvfix_score_topk: v_fresh")) != KVFIX_OK) return st;
+    if (reuse.layers != 1 || fresh.layers != 1)
+        return fail(KVFIX_EINVAL, "%s: reuse and fresh must be check-layer views (layers == 1)", fn);
+    if (!same_shape(reuse, fresh)) return fail(KVFIX_EINVAL, "%s: reuse and fresh shapes differ", fn);
+    if (agents < 1) return fail(KVFIX_EINVAL, "%s: agents must be >= 1", fn);
+    const long long units = (long long)agents * reuse.chunks;
+    if (fresh.chunks != units)
+        return fail(KVFIX_EINVAL, "%s: fresh.chunks (%d) must equal agents*reuse.chunks (%lld)", fn,
+                    fresh.chunks, units);
+    if (units > 65535 || reuse.chunks > 65535) return fail(KVFIX_EINVAL, "%s: at most 65535 units", fn);
+    const int n = reuse.tokens;
+    if (n > 65536) return fail(KVFIX_EINVAL, "%s: tokens must be <= 65536", fn);
+    if (b < 0 || b > n) return fail(KVFIX_EINVAL, "%s: b must lie in [0, tokens]", fn);
+    if (!d_k || !d_v || !w_k || !w_v) return fail(KVFIX_EINVAL, "%s: d_k, d_v, w_k, w_v are required", fn);
+    if (b > 0 && (!idx_k || !idx_v)) return fail(KVFIX_EINVAL, "%s: idx_k and idx_v are required when b > 0", fn);
+    if (units > 0 && !delta) return fail(KVFIX_EINVAL, "%s: delta is null", fn);
+    if (!(rope_base > 1.0) || !isfinite(rope_base)) return fail(KVFIX_EINVAL, "%s: rope_base must be finite and > 1", fn);
+    cudaStream_t s = (cudaStream_t)stream;
+    RopeTheta th = make_theta(rope_base, reuse.head_dim);
+    cudaError_t e = launch_score(k_reuse, v_reuse, reuse, k_fresh, v_fresh, fresh, agents, delta, th,
+                                 d_k, d_v, w_k, w_v, s);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    e = launch_select_f32(d_k, d_v, (int)units, n, b, idx_k, idx_v, mask_k, mask_v, mask_union, s);
+    return launched(e, fn);
+}
+
+kvfix_status kvfix_mean_correct(const kvfix_bf16* k_reuse, const kvfix_bf16* v_reuse,
+                                kvfix_kv_desc reuse, const kvfix_bf16* k_fresh,
+                                const kvfix_bf16* v_fresh, kvfix_kv_desc fresh, kvfix_bf16* k_out,
+                                kvfix_bf16* v_out, kvfix_kv_desc out, int32_t agents,
+                                const int32_t* delta, double rope_base, const int32_t* idx_k,
+                                const int32_t* idx_v, int32_t b, const float* w_k,
+                                const float* w_v, float* mu_k, float* mu_v, void* stream) {
+    const char* fn = "kvfix_mean_correct";
+    if (agents < 1) return fail(KVFIX_EINVAL, "%s: agents must be >= 1", fn);
+    if (!same_shape(reuse, fresh) || !same_shape(reuse, out))
+        return fail(KVFIX_EINVAL, "%s: reuse, fresh and out shapes differ", fn);
+    const long long units = (long long)agents * reuse.chunks;
+    if (fresh.chunks != units || out.chunks != units)
+        return fail(KVFIX_EINVAL, "%s: fresh.chunks and out.chunks must equal agents*reuse.chunks", fn);
+    if (units > 65535 || reuse.layers > 65535 || reuse.chunks > 65535)
+        return fail(KVFIX_EINVAL, "%s: at most 65535 units and 65535 layers", fn);
+    if ((long long)reuse.kv_heads * reuse.head_dim > 4096)
+        return fail(KVFIX_EINVAL, "%s: kv_heads*head_dim must be <= 4096", fn);
+    if (b < 0 || b > reuse.tokens) return fail(KVFIX_EINVAL, "%s: b must lie in [0, tokens]", fn);
+    if (!(rope_base > 1.0) || !isfinite(rope_base)) return fail(KVFIX_EINVAL, "%s: rope_base must be finite and > 1", fn);
+    if (units > 0 && !delta) return fail(KVFIX_EINVAL, "%s: delta is null", fn);
+    struct PlaneArgs {
+        const kvfix_bf16* reuse;
+        const kvfix_bf16* fresh;
+        kvfix_bf16* out;
+        const int32_t* idx;
+        const float* w;
+        float* mu;
+        bool rotate;
+        const char* name;
+    } planes[2] = {{k_reuse, k_fresh, k_out, idx_k, w_k, mu_k, true, "K"},
+                   {v_reuse, v_fresh, v_out, idx_v, w_v, mu_v, false, "V"}};
+    kvfix_status st;
+    int active = 0;
+    for (auto& p : planes) {
+        if (!p.reuse && !p.fresh && !p.out) continue;
+        ++active;
+        char what[96];
+        snprintf(what, sizeof what, "%s: %s reuse", fn, p.name);
+        if ((st = check_plane(p.reuse, reuse, what)) != KVFIX_OK) return st;
+        snprintf(what, sizeof what, "%s: %s fresh", fn, p.name);
+        if ((st = check_plane(p.fresh, fresh, what)) != KVFIX_OK) return st;
+        snprintf(what, sizeof what, "%s: %s out", fn, p.name);
+        if ((st = check_plane(p.out, out, what)) != KVFIX_OK) return st;
+        if (!p.w || !p.mu || (b > 0 && !p.idx))
+            return fail(KVFIX_EINVAL, "%s: %s plane needs w, mu and (b > 0) idx", fn, p.name);
+        if (overlaps(p.out, out, p.reuse, reuse) || overlaps(p.out, out, p.fresh, fresh))
+            return fail(KVFIX_EINVAL, "%s: %s out overlaps an input", fn, p.name);
+        const size_t mu_bytes = sizeof(float) * (size_t)units * reuse.layers * reuse.kv_heads * reuse.head_dim;
+        if (overlaps_bytes(p.mu, mu_bytes, p.w, sizeof(float) * (size_t)units * reuse.tokens))
+            return fail(KVFIX_EINVAL, "%s: %s mu overlaps w", fn, p.name);
+    }
+    if (!active) return fail(KVFIX_EINVAL, "%s: no plane given", fn);
+    cudaStream_t s = (cudaStream_t)stream;
+    RopeTheta th = make_theta(rope_base, reuse.head_dim);
+    for (auto& p : planes) {
+        if (!p.reuse) continue;
+        cudaError_t e = launch_mean_correct(p.reuse, reuse, p.fresh, fresh, p.out, out, agents, delta,
+                                            th, p.rotate, p.idx, b, p.w, p.mu, s);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+    }
+    return KVFIX_OK;
+}
+
+kvfix_status kvfix_lowrank_apply(const kvfix_bf16* x, kvfix_kv_desc desc, const kvfix_bf16* A,
+                                 const kvfix_bf16* B, int32_t rank, kvfix_bf16* out,
+                                 void* stream) {
+    const char* fn = "kvfix_lowrank_apply";
+    kvfix_status st;
+    if ((st = check_plane(x, desc, "kvfix_lowrank_apply: x")) != KVFIX_OK) return st;
+    if ((st = check_plane(out, desc, "kvfix_lowrank_apply: out")) != KVFIX_OK) return st;
+    if (!A || !B) return fail(KVFIX_EINVAL, "%s: A and B are required", fn);
+    if (!aligned16(A) || !aligned16(B)) return fail(KVFIX_EINVAL, "%s: A and B must be 16-byte aligned", fn);
+    if (rank < 16 || rank > 64 || rank % 16) return fail(KVFIX_EINVAL, "%s: rank must be 16, 32, 48 or 64", fn);
+    if (desc.head_dim != 64 && desc.head_dim != 128) return fail(KVFIX_EINVAL, "%s: head_dim must be 64 or 128", fn);
+    if (x != out && overlaps(x, desc, out, desc)) return fail(KVFIX_EINVAL, "%s: out partially overlaps x", fn);
+    const size_t na = 2 * (size_t)desc.chunks * desc.layers * desc.kv_heads * desc.tokens * rank;
+    const size_t nb = 2 * (size_t)desc.chunks * desc.layers * desc.kv_heads * rank * desc.head_dim;
+    uintptr_t o0, o1;
+    extent(out, desc, &o0, &o1);
+    if (overlaps_bytes((const void*)o0, o1 - o0, A, na) || overlaps_bytes((const void*)o0, o1 - o0, B, nb))
+        return fail(KVFIX_EINVAL, "%s: out overlaps A or B", fn);
+    return launched(launch_lowrank(x, desc, A, B, rank, out, (cudaStream_t)stream), fn);
+}
+
+size_t kvfix_draft_rank_workspace_bytes(kvfix_kv_desc desc, int32_t layer_begin) {
+    return draft_workspace_bytes(desc, layer_begin);
+}
+
+kvfix_status kvfix_draft_rank(const kvfix_bf16* k, kvfix_kv_desc desc, const kvfix_bf16* q,
+                              int32_t draft_steps, int32_t q_heads, int32_t layer_begin,
+                              int32_t k_rows, int32_t* idx, double* scores,
+                              const kvfix_bf16* k_fresh, const kvfix_bf16* v_fresh,
+                              kvfix_kv_desc fresh_desc, kvfix_bf16* k_io, kvfix_bf16* v_io,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+    const char* fn = "kvfix_draft_rank";
+    kvfix_status st;
+    if ((st = check_plane(k, desc, "kvfix_draft_rank: k")) != KVFIX_OK) return st;
+    if (!q || !aligned16(q)) return fail(KVFIX_EINVAL, "%s: q must be a 16-byte aligned device pointer", fn);
+    if (desc.head_dim != 64 && desc.head_dim != 128) return fail(KVFIX_EINVAL, "%s: head_dim must be 64 or 128", fn);
+    if (draft_steps < 1 || q_heads < 1 || q_heads % desc.kv_heads)
+        return fail(KVFIX_EINVAL, "%s: q_heads must be a positive multiple of kv_heads, draft_steps >= 1", fn);
+    if ((q_heads / desc.kv_heads) * draft_steps > 16)
+        return fail(KVFIX_EINVAL, "%s: (q_heads/kv_heads)*draft_steps must be <= 16", fn);
+    if (layer_begin < 0 || layer_begin > desc.layers) return fail(KVFIX_EINVAL, "%s: layer_begin out of range", fn);
+    if (desc.tokens > 65536 || desc.chunks > 65535) return fail(KVFIX_EINVAL, "%s: tokens <= 65536, chunks <= 65535", fn);
+    if (k_rows < 0 || k_rows > desc.tokens) return fail(KVFIX_EINVAL, "%s: k_rows must lie in [0, tokens]", fn);
+    if (!scores || (k_rows > 0 && !idx)) return fail(KVFIX_EINVAL, "%s: scores and idx are required", fn);
+    if (workspace_bytes < draft_workspace_bytes(desc, layer_begin) || (!workspace && workspace_bytes))
+        return fail(KVFIX_EINVAL, "%s: workspace smaller than kvfix_draft_rank_workspace_bytes()", fn);
+    if (workspace && !aligned16(workspace)) return fail(KVFIX_EINVAL, "%s: workspace not 16-byte aligned", fn);
+    if (k_io || v_io) {
+        if ((k_io && !k_fresh) || (v_io && !v_fresh)) return fail(KVFIX_EINVAL, "%s: k_io/v_io need k_fresh/v_fresh", fn);
+        if (k_io && (st = check_plane(k_io, desc, "kvfix_draft_rank: k_io")) != KVFIX_OK) return st;
+        if (v_io && (st = check_plane(v_io, desc, "kvfix_draft_rank: v_io")) != KVFIX_OK) return st;
+        if (k_fresh && (st = check_plane(k_fresh, fresh_desc, "kvfix_draft_rank: k_fresh")) != KVFIX_OK) return st;
+        if (v_fresh && (st = check_plane(v_fresh, fresh_desc, "kvfix_draft_rank: v_fresh")) != KVFIX_OK) return st;
+        if (!same_shape(desc, fresh_desc) || fresh_desc.chunks != desc.chunks)
+            return fail(KVFIX_EINVAL, "%s: fresh_desc must match desc", fn);
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_draft(k, desc, q, draft_steps, q_heads, layer_begin, k_rows, idx, scores, workspace, s);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    if (k_io) {
+        if ((e = launch_row_repair(k_io, desc, k_fresh, fresh_desc, idx, k_rows, s)) != cudaSuccess) return cuda_fail(e, fn);
+    }
+    if (v_io) {
+        if ((e = launch_row_repair(v_io, desc, v_fresh, fresh_desc, idx, k_rows, s)) != cudaSuccess) return cuda_fail(e, fn);
+    }
+    return KVFIX_OK;
+}
+
+kvfix_status kvfix_diff_encode(const kvfix_bf16* master_k, const kvfix_bf16* master_v,
+                               kvfix_kv_desc master, const kvfix_bf16* sib_k,
+                               const kvfix_bf16* sib_v, kvfix_kv_desc sib, int32_t block_tokens,
+                               uint32_t* mask, int64_t* offsets, kvfix_bf16* payload,
+                               int64_t capacity_entries, int64_t* h_entries, void* stream) {
+    const char* fn = "kvfix_diff_encode";
+    kvfix_status st;
+    if ((st = check_plane(master_k, master, "kvfix_diff_encode: master_k")) != KVFIX_OK) return st;
+    if ((st = check_plane(master_v, master, "kvfix_diff_encode: master_v")) != KVFIX_OK) return st;
+    if ((st = check_plane(sib_k, sib, "kvfix_diff_encode: sib_k")) != KVFIX_OK) return st;
+    if ((st = check_plane(sib_v, sib, "kvfix_diff_encode: sib_v")) != KVFIX_OK) return st;
+    if (master.chunks != 1) return fail(KVFIX_EINVAL, "%s: master.chunks must be 1", fn);
+    if (!same_shape(master, sib)) return fail(KVFIX_EINVAL, "%s: master and sibling shapes differ", fn);
+    if (block_tokens < 1 || master.tokens % block_tokens)
+        return fail(KVFIX_EINVAL, "%s: block_tokens must divide tokens", fn);
+    if (!mask || !offsets) return fail(KVFIX_EINVAL, "%s: mask and offsets are required", fn);
+    if (capacity_entries < 0) return fail(KVFIX_EINVAL, "%s: negative capacity", fn);
+    if (capacity_entries > 0 && (!payload || !aligned16(payload)))
+        return fail(KVFIX_EINVAL, "%s: payload must be a 16-byte aligned device pointer", fn);
+    const long long per_sibling = (long long)master.layers * (master.tokens / block_tokens);
+    const long long entries = per_sibling * sib.chunks;
+    if (entries >= (1ll << 31)) return fail(KVFIX_EINVAL, "%s: too many entries", fn);
+    if (sib.chunks > 65535 || master.layers > 65535) return fail(KVFIX_EINVAL, "%s: at most 65535 siblings and layers", fn);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(mask, 0, sizeof(uint32_t) * (size_t)((entries + 31) / 32), s);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    if ((e = launch_diff_mask(master_k, master_v, master, sib_k, sib_v, sib, block_tokens, mask, s)) != cudaSuccess)
+        return cuda_fail(e, fn);
+    if ((e = launch_diff_scan(mask, sib.chunks, per_sibling, offsets, s)) != cudaSuccess) return cuda_fail(e, fn);
+    if (h_entries) {
+        int64_t total = 0;
+        if ((e = cudaMemcpyAsync(&total, offsets + entries, sizeof total, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+            return cuda_fail(e, fn);
+        if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, fn);
+        *h_entries = total;
+        if (total > capacity_entries)
+            return fail(KVFIX_ENOSPACE, "%s: %lld entries needed, capacity %lld", fn, (long long)total,
+                        (long long)capacity_entries);
+    }
+    if (capacity_entries == 0) return KVFIX_OK;
+    return launched(launch_diff_pack(sib_k, sib_v, sib, block_tokens, mask, offsets, payload,
+                                     capacity_entries, s), fn);
+}
+
+kvfix_status kvfix_diff_gather(const kvfix_bf16* master_k, const kvfix_bf16* master_v,
+                               kvfix_kv_desc master, const uint32_t* mask,
+                               const int64_t* offsets, const kvfix_bf16* payload,
+                               int64_t payload_entries, int32_t siblings, int32_t block_tokens,
+                               kvfix_bf16* out_k, kvfix_bf16* out_v, kvfix_kv_desc out,
+                               void* stream) {
+    const char* fn = "kvfix_diff_gather";
+    kvfix_status st;
+    if ((st = check_plane(master_k, master, "kvfix_diff_gather: master_k")) != KVFIX_OK) return st;
+    if ((st = check_plane(master_v, master, "kvfix_diff_gather: master_v")) != KVFIX_OK) return st;
+    if ((st = check_plane(out_k, out, "kvfix_diff_gather: out_k")) != KVFIX_OK) return st;
+    if ((st = check_plane(out_v, out, "kvfix_diff_gather: out_v")) != KVFIX_OK) return st;
+    if (master.chunks != 1) return fail(KVFIX_EINVAL, "%s: master.chunks must be 1", fn);
+    if (!same_shape(master, out) || out.chunks != siblings)
+        return fail(KVFIX_EINVAL, "%s: out must have `siblings` chunks of the master's shape", fn);
+    if (block_tokens < 1 || master.tokens % block_tokens)
+        return fail(KVFIX_EINVAL, "%s: block_tokens must divide tokens", fn);
+    if (siblings < 0 || siblings > 65535 || master.layers > 65535)
+        return fail(KVFIX_EINVAL, "%s: siblings and layers must be <= 65535", fn);
+    if (!mask || !offsets) return fail(KVFIX_EINVAL, "%s: mask and offsets are required", fn);
+    if (payload_entries < 0) return fail(KVFIX_EINVAL, "%s: negative payload_entries", fn);
+    if (payload_entries > 0 && (!payload || !aligned16(payload)))
+        return fail(KVFIX_EINVAL, "%s: payload must be a 16-byte aligned device pointer", fn);
+    if (overlaps(out_k, out, master_k, master) || overlaps(out_v, out, master_v, master) ||
+        overlaps(out_k, out, out_v, out))
+        return fail(KVFIX_EINVAL, "%s: outputs overlap the master or each other", fn);
+    return launched(launch_diff_gather(master_k, master_v, master, mask, offsets, payload,
+                                       payload_entries, siblings, block_tokens, out_k, out_v, out,
+                                       (cudaStream_t)stream), fn);
+}
+
+}  // extern "C"

@@ -1,0 +1,283 @@
+// diff.cu -- block-sparse sibling diffs against one master cache (kvfix_diff_encode,
+// kvfix_diff_gather).
+//
+// Method: TokenDance section 4.3 (master-mirror layout, block-sparse K/V diff) and
+// section 5 (touched block indices plus those blocks' K/V contents, one index list
+// shared by K and V); section 4.4, Algorithm 1 (restore = master block, overwritten
+// where the diff touches it).
+//
+// An entry i = (s*L + l)*nblk + blk is bt token rows x all heads x both planes.  The
+// master block is held in registers and compared with / written for every sibling, so
+// the master is read once per call.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace kvfix {
+
+static __device__ unsigned int g_status_diff;
+
+unsigned read_status_diff(cudaStream_t stream) {
+    unsigned h = 0, zero = 0;
+    cudaMemcpyFromSymbolAsync(&h, g_status_diff, sizeof h, 0, cudaMemcpyDeviceToHost, stream);
+    cudaMemcpyToSymbolAsync(g_status_diff, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, stream);
+    cudaStreamSynchronize(stream);
+    return h;
+}
+
+constexpr int kDiffThreads = 512;
+constexpr int kDiffVec = 8;                             // 16-byte vectors per thread per pass
+constexpr int kDiffPass = kDiffThreads * kDiffVec;      // vectors per pass
+
+// Vector q of an entry (K vectors first, then V) -> element offset within the plane.
+struct BlockMap {
+    int bt, row8;  // tokens per block, vectors per token row
+    long long vecs_per_plane;
+    __device__ __forceinline__ void locate(long long q, const Plane& p, int c, int l, int t0,
+                                           int* plane, long long* off) const {
+        *plane = q >= vecs_per_plane;
+        long long r = *plane ? q - vecs_per_plane : q;
+        int t = (int)(r / row8);
+        int c8 = (int)(r % row8);
+        *off = p.row(c, l, t0 + t) + 8ll * c8;
+    }
+};
+
+__device__ __forceinline__ bool vec_ne(const uint4& a, const uint4& b) {
+    return ((a.x ^ b.x) | (a.y ^ b.y) | (a.z ^ b.z) | (a.w ^ b.w)) != 0u;
+}
+
+// grid = (nblk, L).  Sets mask bits of dirty entries (mask pre-zeroed).
+__global__ void __launch_bounds__(kDiffThreads)
+diff_mask_kernel(const uint16_t* __restrict__ mk, const uint16_t* __restrict__ mv, Plane mp,
+                 const uint16_t* __restrict__ sk, const uint16_t* __restrict__ sv, Plane sp,
+                 int bt, uint32_t* mask) {
+    const int blk = blockIdx.x, l = blockIdx.y;
+    const int nblk = mp.tokens / bt;
+    BlockMap bm{bt, mp.heads * mp.dim / 8, (long long)bt * (mp.heads * mp.dim / 8)};
+    const long long total = 2 * bm.vecs_per_plane;
+    const int S = sp.chunks, L = mp.layers;
+    for (long long q0 = 0; q0 < total; q0 += kDiffPass) {
+        uint4 m[kDiffVec];
+        int pl[kDiffVec];
+        long long off[kDiffVec];
+#pragma unroll
+        for (int k = 0; k < kDiffVec; ++k) {
+            long long q = q0 + (long long)k * kDiffThreads + threadIdx.x;
+            pl[k] = -1;
+            if (q < total) {
+                long long o;
+                bm.locate(q, mp, 0, l, blk * bt, &pl[k], &o);
+                m[k] = *reinterpret_cast<const uint4*>((pl[k] ? mv : mk) + o);
+                bm.locate(q, sp, 0, l, blk * bt, &pl[k], &off[k]);  // sibling offset, chunk 0
+            }
+        }
+        for (int s = 0; s < S; ++s) {
+            bool ne = false;
+#pragma unroll
+            for (int k = 0; k < kDiffVec; ++k) {
+                if (pl[k] < 0) continue;
+                const uint16_t* base = (pl[k] ? sv : sk) + (long long)s * sp.sc;
+                uint4 x = ld_stream(reinterpret_cast<const uint4*>(base + off[k]));
+                ne |= vec_ne(x, m[k]);
+            }
+            if (__syncthreads_or(ne) && threadIdx.x == 0) {
+                const long long i = ((long long)s * L + l) * nblk + blk;
+                atomicOr(&mask[i >> 5], 1u << (i & 31));
+            }
+        }
+    }
+}
+
+cudaError_t launch_diff_mask(const uint16_t* mk, const uint16_t* mv, const kvfix_kv_desc& md,
+                             const uint16_t* sk, const uint16_t* sv, const kvfix_kv_desc& sd,
+                             int bt, uint32_t* mask, cudaStream_t s) {
+    Plane mp = plane_of(md), sp = plane_of(sd);
+    if (mp.layers == 0 || mp.tokens == 0 || sp.chunks == 0) return cudaSuccess;
+    dim3 grid(mp.tokens / bt, mp.layers);
+    diff_mask_kernel<<<grid, kDiffThreads, 0, s>>>(mk, mv, mp, sk, sv, sp, bt, mask);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------- scan
+constexpr int kScanThreads = 1024;
+
+__device__ __forceinline__ int mask_bit(const uint32_t* mask, long long i) {
+    return (mask[i >> 5] >> (i & 31)) & 1;
+}
+
+// Exclusive scan of one value per thread (long long), block total in *total.
+__device__ long long block_scan_ll(long long x, long long* ws, long long* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    long long inc = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        long long y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    __syncthreads();
+    if (lane == 31) ws[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        long long v = lane < nw ? ws[lane] : 0, vi = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            long long y = __shfl_up_sync(0xffffffffu, vi, o);
+            if (lane >= o) vi += y;
+        }
+        if (lane < nw) ws[lane] = vi - v;
+        if (lane == 31) ws[32] = vi;
+    }
+    __syncthreads();
+    long long ex = inc - x + ws[warp];
+    *total = ws[32];
+    __syncthreads();
+    return ex;
+}
+
+// grid = siblings.  offsets[s*P + k] = dirty entries before it (over all siblings).
+__global__ void __launch_bounds__(kScanThreads)
+diff_scan_kernel(const uint32_t* __restrict__ mask, long long P, int S, int64_t* offsets) {
+    __shared__ long long ws[33];
+    const int s = blockIdx.x;
+    const long long lo = (long long)s * P;  // first entry of this sibling
+    // dirty entries of earlier siblings: bits [0, lo)
+    long long before = 0;
+    const long long full_words = lo >> 5;
+    for (long long w = threadIdx.x; w < full_words; w += blockDim.x) before += __popc(mask[w]);
+    if (threadIdx.x == 0 && (lo & 31)) before += __popc(mask[full_words] & ((1u << (lo & 31)) - 1u));
+    long long tot;
+    block_scan_ll(before, ws, &tot);
+    const long long base = tot;
+    const long long seg = (P + blockDim.x - 1) / blockDim.x;
+    const long long i0 = min(P, (long long)threadIdx.x * seg), i1 = min(P, i0 + seg);
+    long long cnt = 0;
+    for (long long i = i0; i < i1; ++i) cnt += mask_bit(mask, lo + i);
+    long long run = base + block_scan_ll(cnt, ws, &tot);
+    for (long long i = i0; i < i1; ++i) {
+        offsets[lo + i] = run;
+        run += mask_bit(mask, lo + i);
+    }
+    if (s == S - 1 && threadIdx.x == 0) offsets[(long long)S * P] = base + tot;
+}
+
+cudaError_t launch_diff_scan(const uint32_t* mask, int siblings, long long per_sibling,
+                             int64_t* offsets, cudaStream_t s) {
+    if (siblings == 0) return cudaMemsetAsync(offsets, 0, sizeof(int64_t), s);
+    diff_scan_kernel<<<siblings, kScanThreads, 0, s>>>(mask, per_sibling, siblings, offsets);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------- pack
+constexpr int kPackThreads = 256;
+
+// grid = ceil(E/32): one CTA per mask word; copies each dirty entry to the payload.
+__global__ void __launch_bounds__(kPackThreads)
+diff_pack_kernel(const uint16_t* __restrict__ sk, const uint16_t* __restrict__ sv, Plane sp, int bt,
+                 const uint32_t* __restrict__ mask, const int64_t* __restrict__ offsets,
+                 long long E, uint16_t* payload, long long capacity) {
+    const long long wi = blockIdx.x;
+    uint32_t word = mask[wi];
+    const int L = sp.layers, nblk = sp.tokens / bt;
+    BlockMap bm{bt, sp.heads * sp.dim / 8, (long long)bt * (sp.heads * sp.dim / 8)};
+    const long long total = 2 * bm.vecs_per_plane;
+    while (word) {
+        const int bit = __ffs(word) - 1;
+        word &= word - 1;
+        const long long i = wi * 32 + bit;
+        if (i >= E) break;
+        const long long e = offsets[i];
+        if (e >= capacity) {
+            if (threadIdx.x == 0) atomicOr(&g_status_diff, FLAG_NOSPACE);
+            continue;
+        }
+        const int s = (int)(i / ((long long)L * nblk));
+        const int l = (int)((i / nblk) % L);
+        const int blk = (int)(i % nblk);
+        uint4* dst = reinterpret_cast<uint4*>(payload + e * total * 8);
+        for (long long q = threadIdx.x; q < total; q += kPackThreads) {
+            int pl;
+            long long off;
+            bm.locate(q, sp, s, l, blk * bt, &pl, &off);
+            uint4 v = ld_stream(reinterpret_cast<const uint4*>((pl ? sv : sk) + off));
+            st_stream(dst + q, v);
+        }
+    }
+}
+
+cudaError_t launch_diff_pack(const uint16_t* sk, const uint16_t* sv, const kvfix_kv_desc& sd,
+                             int bt, const uint32_t* mask, const int64_t* offsets,
+                             uint16_t* payload, long long capacity, cudaStream_t s) {
+    Plane sp = plane_of(sd);
+    const long long E = (long long)sp.chunks * sp.layers * (sp.tokens / bt);
+    if (E == 0) return cudaSuccess;
+    const long long words = (E + 31) / 32;
+    diff_pack_kernel<<<(unsigned)words, kPackThreads, 0, s>>>(sk, sv, sp, bt, mask, offsets, E,
+                                                              payload, capacity);
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------- gather
+
+// grid = (nblk, L).  Master block in registers, written to every sibling unless the
+// sibling's entry is dirty, in which case the payload block is copied instead.
+__global__ void __launch_bounds__(kDiffThreads)
+diff_gather_kernel(const uint16_t* __restrict__ mk, const uint16_t* __restrict__ mv, Plane mp,
+                   const uint32_t* __restrict__ mask, const int64_t* __restrict__ offsets,
+                   const uint16_t* __restrict__ payload, long long payload_entries, int S, int bt,
+                   uint16_t* ok, uint16_t* ov, Plane op) {
+    const int blk = blockIdx.x, l = blockIdx.y;
+    const int nblk = mp.tokens / bt, L = mp.layers;
+    BlockMap bm{bt, mp.heads * mp.dim / 8, (long long)bt * (mp.heads * mp.dim / 8)};
+    const long long total = 2 * bm.vecs_per_plane;
+    for (long long q0 = 0; q0 < total; q0 += kDiffPass) {
+        uint4 m[kDiffVec];
+        int pl[kDiffVec];
+        long long off[kDiffVec];
+#pragma unroll
+        for (int k = 0; k < kDiffVec; ++k) {
+            long long q = q0 + (long long)k * kDiffThreads + threadIdx.x;
+            pl[k] = -1;
+            if (q < total) {
+                long long o;
+                bm.locate(q, mp, 0, l, blk * bt, &pl[k], &o);
+                m[k] = *reinterpret_cast<const uint4*>((pl[k] ? mv : mk) + o);
+                bm.locate(q, op, 0, l, blk * bt, &pl[k], &off[k]);
+            }
+        }
+        for (int s = 0; s < S; ++s) {
+            const long long i = ((long long)s * L + l) * nblk + blk;
+            const bool dirty = mask_bit(mask, i);
+            long long e = dirty ? offsets[i] : -1;
+            if (dirty && e >= payload_entries) {
+                if (threadIdx.x == 0) atomicOr(&g_status_diff, FLAG_NOSPACE);
+                e = -1;
+            }
+            const uint4* src = e >= 0 ? reinterpret_cast<const uint4*>(payload + e * total * 8) : nullptr;
+#pragma unroll
+            for (int k = 0; k < kDiffVec; ++k) {
+                if (pl[k] < 0) continue;
+                const long long q = q0 + (long long)k * kDiffThreads + threadIdx.x;
+                uint4 v = src ? ld_stream(src + q) : m[k];
+                uint16_t* base = (pl[k] ? ov : ok) + (long long)s * op.sc;
+                st_stream(reinterpret_cast<uint4*>(base + off[k]), v);
+            }
+        }
+    }
+}
+
+cudaError_t launch_diff_gather(const uint16_t* mk, const uint16_t* mv, const kvfix_kv_desc& md,
+                               const uint32_t* mask, const int64_t* offsets,
+                               const uint16_t* payload, long long payload_entries, int siblings,
+                               int bt, uint16_t* ok, uint16_t* ov, const kvfix_kv_desc& od,
+                               cudaStream_t s) {
+    Plane mp = plane_of(md), op = plane_of(od);
+    if (mp.layers == 0 || mp.tokens == 0 || siblings == 0) return cudaSuccess;
+    dim3 grid(mp.tokens / bt, mp.layers);
+    diff_gather_kernel<<<grid, kDiffThreads, 0, s>>>(mk, mv, mp, mask, offsets, payload,
+                                                     payload_entries, siblings, bt, ok, ov, op);
+    return cudaGetLastError();
+}
+
+}  // namespace kvfix

@@ -1,0 +1,78 @@
+// internal.h -- declarations shared by the host-side translation units of libkvfix.
+// Not part of the public ABI (include/kvfix.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/kvfix.h"
+
+namespace kvfix {
+
+// Host-computed RoPE frequencies theta_i = base^(-2i/D), passed by value to kernels.
+constexpr int kMaxHeadDim = 256;
+struct RopeTheta {
+    double theta[kMaxHeadDim / 2];
+};
+RopeTheta make_theta(double base, int head_dim);
+
+// Records `msg` as the calling thread's last error and returns `st`.
+kvfix_status fail(kvfix_status st, const char* fmt, ...);
+// Maps a CUDA error (after a launch or runtime call) to KVFIX_ECUDA with a message.
+kvfix_status cuda_fail(cudaError_t err, const char* what);
+
+// Per-translation-unit device status words: read (and clear) on `stream`.
+unsigned read_status_repair(cudaStream_t stream);
+unsigned read_status_diff(cudaStream_t stream);
+unsigned read_status_draft(cudaStream_t stream);
+
+// ---- launchers (enqueue only; arguments already validated) -----------------------
+
+cudaError_t launch_rerope(const uint16_t* in, uint16_t* out, const kvfix_kv_desc& d,
+                          const int32_t* delta, const RopeTheta& th, cudaStream_t s);
+
+cudaError_t launch_score(const uint16_t* k_reuse, const uint16_t* v_reuse,
+                         const kvfix_kv_desc& reuse, const uint16_t* k_fresh,
+                         const uint16_t* v_fresh, const kvfix_kv_desc& fresh, int agents,
+                         const int32_t* delta, const RopeTheta& th, float* d_k, float* d_v,
+                         float* w_k, float* w_v, cudaStream_t s);
+
+// Top-b of float scores per unit for two planes (either may be skipped with NULL
+// scores), plus the optional union mask.
+cudaError_t launch_select_f32(const float* d_k, const float* d_v, int units, int n, int b,
+                              int32_t* idx_k, int32_t* idx_v, uint32_t* mask_k,
+                              uint32_t* mask_v, uint32_t* mask_union, cudaStream_t s);
+
+cudaError_t launch_mean_correct(const uint16_t* reuse, const kvfix_kv_desc& rd,
+                                const uint16_t* fresh, const kvfix_kv_desc& fd, uint16_t* out,
+                                const kvfix_kv_desc& od, int agents, const int32_t* delta,
+                                const RopeTheta& th, bool rotate, const int32_t* idx, int b,
+                                const float* w, float* mu, cudaStream_t s);
+
+cudaError_t launch_lowrank(const uint16_t* x, const kvfix_kv_desc& d, const uint16_t* A,
+                           const uint16_t* B, int rank, uint16_t* out, cudaStream_t s);
+
+size_t draft_workspace_bytes(const kvfix_kv_desc& d, int layer_begin);
+cudaError_t launch_draft(const uint16_t* k, const kvfix_kv_desc& d, const uint16_t* q,
+                         int steps, int q_heads, int layer_begin, int k_rows, int32_t* idx,
+                         double* scores, void* ws, cudaStream_t s);
+cudaError_t launch_row_repair(uint16_t* io, const kvfix_kv_desc& d, const uint16_t* fresh,
+                              const kvfix_kv_desc& fd, const int32_t* idx, int k_rows,
+                              cudaStream_t s);
+
+cudaError_t launch_diff_mask(const uint16_t* mk, const uint16_t* mv, const kvfix_kv_desc& md,
+                             const uint16_t* sk, const uint16_t* sv, const kvfix_kv_desc& sd,
+                             int bt, uint32_t* mask, cudaStream_t s);
+cudaError_t launch_diff_scan(const uint32_t* mask, int siblings, long long per_sibling,
+                             int64_t* offsets, cudaStream_t s);
+cudaError_t launch_diff_pack(const uint16_t* sk, const uint16_t* sv, const kvfix_kv_desc& sd,
+                             int bt, const uint32_t* mask, const int64_t* offsets,
+                             uint16_t* payload, long long capacity, cudaStream_t s);
+cudaError_t launch_diff_gather(const uint16_t* mk, const uint16_t* mv, const kvfix_kv_desc& md,
+                               const uint32_t* mask, const int64_t* offsets,
+                               const uint16_t* payload, long long payload_entries, int siblings,
+                               int bt, uint16_t* ok, uint16_t* ov, const kvfix_kv_desc& od,
+                               cudaStream_t s);
+
+}  // namespace kvfix

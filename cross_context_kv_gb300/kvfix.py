@@ -1,0 +1,273 @@
+"""ctypes binding of libkvfix (include/kvfix.h).
+
+Argument marshalling only: every function checks tensor dtypes/devices, builds the
+plane descriptors from tensor shapes and strides, allocates outputs with torch on the
+tensors' device and calls the C entry point of the same name on the current CUDA
+stream.  All arithmetic runs in the library's CUDA kernels.  If libkvfix.so is
+missing, importing this module raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvfix.so")
+
+OK, EINVAL, ENOSPACE, ECUDA, ETIMEOUT, EDEVICE = range(6)
+STATUS_NAMES = {0: "KVFIX_OK", 1: "KVFIX_EINVAL", 2: "KVFIX_ENOSPACE", 3: "KVFIX_ECUDA",
+                4: "KVFIX_ETIMEOUT", 5: "KVFIX_EDEVICE"}
+
+
+class KvfixError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class KvDesc(ctypes.Structure):
+    _fields_ = [("chunks", ctypes.c_int32), ("layers", ctypes.c_int32), ("tokens", ctypes.c_int32),
+                ("kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("stride_chunk", ctypes.c_int64), ("stride_layer", ctypes.c_int64),
+                ("stride_token", ctypes.c_int64)]
+
+
+# name -> (restype, argtypes); mirrors include/kvfix.h
+P, I32, I64, F64, SZ, D = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double,
+                           ctypes.c_size_t, KvDesc)
+SIGNATURES = {
+    "kvfix_version": (ctypes.c_int, []),
+    "kvfix_last_error": (ctypes.c_char_p, []),
+    "kvfix_check_status": (ctypes.c_int, [P]),
+    "kvfix_rerope": (ctypes.c_int, [P, P, D, P, F64, P]),
+    "kvfix_score_topk": (ctypes.c_int, [P, P, D, P, P, D, I32, P, F64, I32, P, P, P, P, P, P, P, P, P, P]),
+    "kvfix_mean_correct": (ctypes.c_int, [P, P, D, P, P, D, P, P, D, I32, P, F64, P, P, I32, P, P, P, P, P]),
+    "kvfix_lowrank_apply": (ctypes.c_int, [P, D, P, P, I32, P, P]),
+    "kvfix_draft_rank_workspace_bytes": (SZ, [D, I32]),
+    "kvfix_draft_rank": (ctypes.c_int, [P, D, P, I32, I32, I32, I32, P, P, P, P, D, P, P, P, SZ, P]),
+    "kvfix_diff_encode": (ctypes.c_int, [P, P, D, P, P, D, I32, P, P, P, I64, P, P]),
+    "kvfix_diff_gather": (ctypes.c_int, [P, P, D, P, P, P, I64, I32, I32, P, P, D, P]),
+}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it first "
+                          "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def _check(status: int):
+    if status != OK:
+        raise KvfixError(status, lib.kvfix_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _bf16(t, name):
+    if t is None:
+        return
+    if t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA bfloat16 tensor (got {t.dtype} on {t.device})")
+
+
+def plane_desc(t: torch.Tensor) -> KvDesc:
+    """Descriptor of a [chunks][layers][tokens][heads][dim] (or [chunks][tokens][heads][dim],
+    read as one layer) bf16 view whose heads and dims are contiguous."""
+    if t.dim() == 4:
+        t = t.unsqueeze(1)
+    if t.dim() != 5:
+        raise ValueError(f"KV plane must be 4-D or 5-D, got shape {tuple(t.shape)}")
+    C, L, n, H, Dh = t.shape
+    sc, sl, st, sh, sd = t.stride()
+    if (sd != 1 or sh != Dh) and H * Dh > 1:
+        raise ValueError("KV plane views need contiguous heads and dims (stride(-1) == 1, "
+                         "stride(-2) == head_dim)")
+    return KvDesc(C, L, n, H, Dh, sc if C > 1 else 0, sl if L > 1 else 0, st if n > 1 else H * Dh)
+
+
+def _i32(t, name):
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous CUDA int32 tensor")
+
+
+def _f32(t, name):
+    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous CUDA float32 tensor")
+
+
+def version() -> int:
+    return lib.kvfix_version()
+
+
+def check_status(stream_of: torch.Tensor | None = None) -> int:
+    """Synchronise the current stream and raise if the device flagged a condition."""
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    _check(lib.kvfix_check_status(s))
+    return OK
+
+
+# --------------------------------------------------------------------- calls
+
+def rerope(k: torch.Tensor, delta: torch.Tensor, rope_base: float, out: torch.Tensor | None = None):
+    _bf16(k, "k")
+    _i32(delta, "delta")
+    out = torch.empty_like(k) if out is None else out
+    _bf16(out, "out")
+    d = plane_desc(k)
+    if plane_desc(out).tokens != d.tokens:
+        raise ValueError("out must match k")
+    _check(lib.kvfix_rerope(_ptr(k), _ptr(out), d, _ptr(delta), float(rope_base), _stream(k)))
+    return out
+
+
+def score_topk(k_reuse, v_reuse, k_fresh, v_fresh, agents: int, delta, rope_base: float, b: int,
+               masks: bool = False):
+    """Check-layer views: reuse [R](1)[n][H][D], fresh [agents*R](1)[n][H][D]."""
+    for t, nm in ((k_reuse, "k_reuse"), (v_reuse, "v_reuse"), (k_fresh, "k_fresh"), (v_fresh, "v_fresh")):
+        _bf16(t, nm)
+    _i32(delta, "delta")
+    rd, fd = plane_desc(k_reuse), plane_desc(k_fresh)
+    units, n = fd.chunks, fd.tokens
+    dev = k_reuse.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {"d_k": torch.empty(units, n, **f32), "d_v": torch.empty(units, n, **f32),
+           "w_k": torch.empty(units, n, **f32), "w_v": torch.empty(units, n, **f32),
+           "idx_k": torch.empty(units, max(b, 0), dtype=torch.int32, device=dev),
+           "idx_v": torch.empty(units, max(b, 0), dtype=torch.int32, device=dev)}
+    words = (n + 31) // 32
+    if masks:
+        for nm in ("mask_k", "mask_v", "mask_union"):
+            out[nm] = torch.empty(units, words, dtype=torch.int32, device=dev)
+    _check(lib.kvfix_score_topk(_ptr(k_reuse), _ptr(v_reuse), rd, _ptr(k_fresh), _ptr(v_fresh), fd,
+                                int(agents), _ptr(delta), float(rope_base), int(b),
+                                _ptr(out["d_k"]), _ptr(out["d_v"]), _ptr(out["w_k"]), _ptr(out["w_v"]),
+                                _ptr(out["idx_k"]) if b > 0 else None, _ptr(out["idx_v"]) if b > 0 else None,
+                                _ptr(out.get("mask_k")), _ptr(out.get("mask_v")),
+                                _ptr(out.get("mask_union")), _stream(k_reuse)))
+    return out
+
+
+def mean_correct(k_reuse, v_reuse, k_fresh, v_fresh, agents: int, delta, rope_base: float,
+                 idx_k, idx_v, w_k, w_v, k_out=None, v_out=None, mu_k=None, mu_v=None):
+    """reuse [R][L][n][H][D]; fresh/out [agents*R][L][n][H][D]; idx [agents*R][b]."""
+    for t, nm in ((k_reuse, "k_reuse"), (v_reuse, "v_reuse"), (k_fresh, "k_fresh"), (v_fresh, "v_fresh")):
+        _bf16(t, nm)
+    _i32(delta, "delta")
+    _i32(idx_k, "idx_k")
+    _i32(idx_v, "idx_v")
+    _f32(w_k, "w_k")
+    _f32(w_v, "w_v")
+    if idx_k.shape != idx_v.shape:
+        raise ValueError("idx_k and idx_v must have the same shape")
+    b = idx_k.shape[-1] if idx_k.dim() else 0
+    k_out = torch.empty_like(k_fresh) if k_out is None else k_out
+    v_out = torch.empty_like(v_fresh) if v_out is None else v_out
+    rd, fd, od = plane_desc(k_reuse), plane_desc(k_fresh), plane_desc(k_out)
+    units, L, H, Dh = fd.chunks, fd.layers, fd.kv_heads, fd.head_dim
+    if mu_k is None:
+        mu_k = torch.empty(units, L, H * Dh, dtype=torch.float32, device=k_reuse.device)
+    if mu_v is None:
+        mu_v = torch.empty(units, L, H * Dh, dtype=torch.float32, device=k_reuse.device)
+    _check(lib.kvfix_mean_correct(_ptr(k_reuse), _ptr(v_reuse), rd, _ptr(k_fresh), _ptr(v_fresh), fd,
+                                  _ptr(k_out), _ptr(v_out), od, int(agents), _ptr(delta),
+                                  float(rope_base), _ptr(idx_k), _ptr(idx_v), int(b), _ptr(w_k),
+                                  _ptr(w_v), _ptr(mu_k), _ptr(mu_v), _stream(k_reuse)))
+    return k_out, v_out, mu_k, mu_v
+
+
+def lowrank_apply(x, A, B, out=None):
+    """x [C][L][n][H][D]; A [C][L][H][n][r]; B [C][L][H][r][D] (A, B contiguous)."""
+    _bf16(x, "x")
+    _bf16(A, "A")
+    _bf16(B, "B")
+    if not (A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("A and B must be contiguous")
+    out = torch.empty_like(x) if out is None else out
+    _bf16(out, "out")
+    d = plane_desc(x)
+    _check(lib.kvfix_lowrank_apply(_ptr(x), d, _ptr(A), _ptr(B), int(A.shape[-1]), _ptr(out), _stream(x)))
+    return out
+
+
+def draft_rank_workspace_bytes(k, layer_begin: int) -> int:
+    return int(lib.kvfix_draft_rank_workspace_bytes(plane_desc(k), int(layer_begin)))
+
+
+def draft_rank(k, q, layer_begin: int, k_rows: int, k_fresh=None, v_fresh=None, k_io=None,
+               v_io=None, workspace=None):
+    """k [C][L][n][Hkv][D]; q [C][L][T][Hq][D] contiguous.  Returns (idx, scores)."""
+    _bf16(k, "k")
+    _bf16(q, "q")
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    d = plane_desc(k)
+    C, n = d.chunks, d.tokens
+    ws_bytes = draft_rank_workspace_bytes(k, layer_begin)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=k.device)
+    idx = torch.empty(C, max(k_rows, 0), dtype=torch.int32, device=k.device)
+    scores = torch.empty(C, n, dtype=torch.float64, device=k.device)
+    fd = plane_desc(k_fresh) if k_fresh is not None else (plane_desc(v_fresh) if v_fresh is not None else d)
+    _check(lib.kvfix_draft_rank(_ptr(k), d, _ptr(q), int(q.shape[2]), int(q.shape[3]), int(layer_begin),
+                                int(k_rows), _ptr(idx), _ptr(scores), _ptr(k_fresh), _ptr(v_fresh), fd,
+                                _ptr(k_io), _ptr(v_io), _ptr(workspace), workspace.numel(), _stream(k)))
+    return idx, scores
+
+
+def diff_encode(master_k, master_v, sib_k, sib_v, block_tokens: int, capacity: int | None = None,
+                sync: bool = True):
+    """master [L][n][H][D] (or [1][L][n][H][D]); siblings [S][L][n][H][D].
+    Returns (mask int32 words, offsets int64, payload [cap][2][bt][H][D], entries or None)."""
+    for t, nm in ((master_k, "master_k"), (master_v, "master_v"), (sib_k, "sib_k"), (sib_v, "sib_v")):
+        _bf16(t, nm)
+    mk = master_k.unsqueeze(0) if master_k.dim() == 4 else master_k
+    mv = master_v.unsqueeze(0) if master_v.dim() == 4 else master_v
+    md, sd = plane_desc(mk), plane_desc(sib_k)
+    S, L, n, H, Dh = sd.chunks, sd.layers, sd.tokens, sd.kv_heads, sd.head_dim
+    bt = int(block_tokens)
+    E = S * L * (n // bt)
+    dev = sib_k.device
+    mask = torch.empty((E + 31) // 32, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int64, device=dev)
+    cap = E if capacity is None else int(capacity)
+    payload = torch.empty(max(cap, 1), 2, bt, H, Dh, dtype=torch.bfloat16, device=dev)
+    entries = ctypes.c_int64(-1)
+    st = lib.kvfix_diff_encode(_ptr(mk), _ptr(mv), md, _ptr(sib_k), _ptr(sib_v), sd, bt, _ptr(mask),
+                               _ptr(offsets), _ptr(payload), cap, ctypes.byref(entries) if sync else None,
+                               _stream(sib_k))
+    _check(st)
+    return mask, offsets, payload, (entries.value if sync else None)
+
+
+def diff_gather(master_k, master_v, mask, offsets, payload, siblings: int, block_tokens: int,
+                out_k=None, out_v=None, payload_entries: int | None = None):
+    _bf16(master_k, "master_k")
+    _bf16(master_v, "master_v")
+    mk = master_k.unsqueeze(0) if master_k.dim() == 4 else master_k
+    mv = master_v.unsqueeze(0) if master_v.dim() == 4 else master_v
+    md = plane_desc(mk)
+    shape = (int(siblings),) + tuple(mk.shape[1:])
+    out_k = torch.empty(shape, dtype=torch.bfloat16, device=mk.device) if out_k is None else out_k
+    out_v = torch.empty(shape, dtype=torch.bfloat16, device=mk.device) if out_v is None else out_v
+    pe = payload.shape[0] if payload_entries is None else int(payload_entries)
+    _check(lib.kvfix_diff_gather(_ptr(mk), _ptr(mv), md, _ptr(mask), _ptr(offsets), _ptr(payload), pe,
+                                 int(siblings), int(block_tokens), _ptr(out_k), _ptr(out_v),
+                                 plane_desc(out_k), _stream(mk)))
+    return out_k, out_v

@@ -1,0 +1,277 @@
+/*
+ * kvfix.h -- C ABI of libkvfix, the repair path for reused KV-cache chunks on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The library re-aligns, scores, selects, corrects and stores KV caches that one
+ * agent reuses from another context.  Every call enqueues hand-written CUDA kernels
+ * on the caller's stream; nothing runs on the host but argument checks.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - bf16 tensors are passed as `kvfix_bf16*`: raw IEEE bfloat16 bit patterns.
+ * - All tensor pointers are DEVICE pointers unless the name starts with `h_`.
+ * - A KV plane (the keys or the values of a cache) is described by kvfix_kv_desc:
+ *   element (c, l, t, h, e) -- chunk, layer, token, KV head, head dim -- lives at
+ *       c*stride_chunk + l*stride_layer + t*stride_token + h*head_dim + e
+ *   (strides in elements).  The heads of one token are contiguous (one token row is
+ *   kv_heads*head_dim elements).  head_dim must be a multiple of 16 in [16, 256]; the
+ *   base pointer must be 16-byte aligned and every stride a non-negative multiple of
+ *   8 elements, so that rows move as 16-byte vectors.
+ * - `stream` is a cudaStream_t cast to void* (NULL = the legacy default stream).
+ * - Ownership: the caller owns every buffer.  The library keeps no per-call state
+ *   and allocates no device memory; calls that need scratch take a workspace
+ *   buffer whose size a companion *_workspace_bytes() query returns.
+ * - Errors: arguments are checked on the host before anything is launched; a bad
+ *   argument returns KVFIX_EINVAL and launches nothing.  A launch failure returns
+ *   KVFIX_ECUDA.  kvfix_last_error() gives the message of the last non-OK status of
+ *   the calling thread.  Conditions only the GPU can see (an index in caller data
+ *   out of range, a payload overflow) set a device status word instead; the kernels
+ *   then skip the offending access.  kvfix_check_status() reads and clears it.
+ * - Calls are asynchronous: a KVFIX_OK return means "enqueued".
+ * - Outputs never alias inputs, except where a call says so.
+ *
+ * Citations name the page and section that define each operation:
+ *   [KVCMAS]  KVCMAS: Efficient KV cache Correction for Shared Context in Multi-Agent Systems
+ *   [AKS]     AgentKVShift: Correcting Reused KV (review)
+ *   [TD]      TokenDance: Scaling Multi-Agent LLM Serving via Collective KV Cache Sharing (summary)
+ *   [BCR]     Budgeted Cache Repair for Cross-Context KV-Cache Reuse
+ */
+#ifndef KVFIX_H
+#define KVFIX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVFIX_API __attribute__((visibility("default")))
+#else
+#define KVFIX_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kvfix_bf16;
+
+typedef enum {
+    KVFIX_OK = 0,
+    KVFIX_EINVAL = 1,   /* bad argument; nothing was launched */
+    KVFIX_ENOSPACE = 2, /* diff payload capacity too small (see kvfix_diff_encode) */
+    KVFIX_ECUDA = 3,    /* a CUDA runtime call or launch failed */
+    KVFIX_ETIMEOUT = 4, /* a bounded device-side wait gave up */
+    KVFIX_EDEVICE = 5   /* the device flagged bad caller data (index out of range) */
+} kvfix_status;
+
+typedef struct {
+    int32_t chunks;
+    int32_t layers;
+    int32_t tokens;
+    int32_t kv_heads;
+    int32_t head_dim;
+    int64_t stride_chunk;
+    int64_t stride_layer;
+    int64_t stride_token;
+} kvfix_kv_desc;
+
+/* Library version, major*10000 + minor*100 + patch. */
+KVFIX_API int kvfix_version(void);
+
+/* Message of the calling thread's last non-OK status ("" if none).  The pointer
+ * stays valid until the thread's next kvfix call. */
+KVFIX_API const char* kvfix_last_error(void);
+
+/* Synchronise `stream`, then read and clear the device status word.
+ * Returns KVFIX_OK, KVFIX_EDEVICE (an index out of range was skipped),
+ * KVFIX_ENOSPACE (a payload write was skipped), KVFIX_ETIMEOUT or KVFIX_ECUDA. */
+KVFIX_API kvfix_status kvfix_check_status(void* stream);
+
+/*
+ * kvfix_rerope -- re-align cached keys to new positions with rotary embeddings.
+ * [KVCMAS] section 2.2 and App. A.3 (keys are re-aligned to their target positions,
+ * values are not rotated); [TD] section 4.4, Algorithm 1 (RoPERecover(P_old, P_new));
+ * [BCR] App. A (one scalar position shift per reused segment).
+ *
+ * With rotate-half RoPE, theta_i = rope_base^(-2i/D) for i < D/2 and dimension i
+ * paired with i + D/2, a key encoded at position p and moved to p + delta is rotated
+ * once more by the angle delta*theta_i:
+ *     y_i       = x_i cos(delta theta_i) - x_{i+D/2} sin(delta theta_i)
+ *     y_{i+D/2} = x_{i+D/2} cos(delta theta_i) + x_i sin(delta theta_i)
+ * k_in, k_out : one KV plane, both described by `desc` (k_out may equal k_in).
+ * delta       : device int32[desc.chunks], the shift of each chunk (any sign).
+ * Arithmetic: angles reduced in double, cos/sin and the rotation in float, output
+ * rounded to nearest-even bf16.  delta = 0 reproduces the input bit for bit.
+ */
+KVFIX_API kvfix_status kvfix_rerope(const kvfix_bf16* k_in, kvfix_bf16* k_out, kvfix_kv_desc desc,
+                          const int32_t* delta, double rope_base, void* stream);
+
+/*
+ * kvfix_score_topk -- check-layer divergence and probe selection.
+ * [AKS] "Core idea and method", steps 1-2 and the displayed b, d and w equations;
+ * [TD] section 4.2 (one batched rotation and one batched check-layer comparison for
+ * all requests of a round).
+ *
+ * Units: unit u = a*R + r pairs agent a (of `agents`) with reused chunk r (of
+ * R = reuse.chunks).  For every unit and token j of the check layer:
+ *     d_k[u][j] = || k_fresh[u][j] - rerope(k_reuse[r][j], delta[u]) ||_2
+ *     d_v[u][j] = || v_fresh[u][j] - v_reuse[r][j] ||_2
+ * where the norm runs over the whole token row (all KV heads).  Then, for each plane,
+ * the b tokens with the largest d (ties to the lower index; d compared as float) are
+ * the probes: idx_*[u][0..b-1] in ascending order, bit j of mask_*[u] set for each
+ * (word j/32, bit j%32), w_*[u][j] = min(d[u][j], 1).  mask_union = mask_k | mask_v.
+ *
+ * k_reuse, v_reuse : check-layer views, `reuse` (layers == 1), R chunks.
+ * k_fresh, v_fresh : check-layer views, `fresh` (layers == 1, chunks == agents*R,
+ *                    same tokens/heads/head_dim as `reuse`).
+ * delta            : device int32[agents*R].
+ * b                : 0 <= b <= tokens (b = ceil(r n) for probe ratio r).
+ * d_k, d_v, w_k, w_v : device float[agents*R][tokens], required.
+ * idx_k, idx_v     : device int32[agents*R][b], required when b > 0.
+ * mask_k, mask_v, mask_union : device uint32[agents*R][ceil(tokens/32)], optional.
+ * Limits: tokens <= 65536.  All agents of a round are handled by one set of launches;
+ * each reused check-layer row is read once for all agents.
+ */
+KVFIX_API kvfix_status kvfix_score_topk(const kvfix_bf16* k_reuse, const kvfix_bf16* v_reuse,
+                              kvfix_kv_desc reuse, const kvfix_bf16* k_fresh,
+                              const kvfix_bf16* v_fresh, kvfix_kv_desc fresh, int32_t agents,
+                              const int32_t* delta, double rope_base, int32_t b, float* d_k,
+                              float* d_v, float* w_k, float* w_v, int32_t* idx_k, int32_t* idx_v,
+                              uint32_t* mask_k, uint32_t* mask_v, uint32_t* mask_union,
+                              void* stream);
+
+/*
+ * kvfix_mean_correct -- probe-mean residual correction of every layer.
+ * [AKS] "Core idea and method", steps 3-4 and the displayed mu-hat and K_corr
+ * equations; [TD] section 4.2 (only the per-request refresh differs between the
+ * requests of a group).
+ *
+ * For unit u = a*R + r, layer l, plane P in {K, V} with probe list S = idx_P[u][0..b-1]
+ * and weights w_P[u]:
+ *     mu_P[u][l][h*D+e] = (1/b) sum_{i<b} (fresh_P[u][l][S_i][h][e] - rot(reuse_P[r][l][S_i][h])[e])
+ *     out_P[u][l][j]    = fresh_P[u][l][j]                              if j in S (bit copy)
+ *                       = bf16(rot(reuse_P[r][l][j]) + w_P[u][j] * mu_P[u][l])   otherwise
+ * rot is the re-rope by delta[u] for keys and the identity for values; b == 0 gives
+ * mu = 0 and out = bf16(rot(reuse)).  The sum runs in a fixed order (probe i goes to
+ * partial sum i mod 32; partial sums are added in order), so a round of N agents in
+ * one call and N one-agent calls give the same bits.
+ *
+ * reuse, fresh, out : plane descriptors; reuse has R chunks, fresh and out agents*R,
+ *                     all with the same layers/tokens/heads/head_dim.
+ * k_* / v_*         : pass all NULL for a plane to skip it.
+ * idx_k, idx_v      : device int32[agents*R][b] (ascending not required; each entry
+ *                     must lie in [0, tokens) -- others are skipped and flagged).
+ * w_k, w_v          : device float[agents*R][tokens].
+ * mu_k, mu_v        : device float[agents*R][layers][kv_heads*head_dim], written.
+ * Each reused row is read once for all agents of the call.
+ */
+KVFIX_API kvfix_status kvfix_mean_correct(const kvfix_bf16* k_reuse, const kvfix_bf16* v_reuse,
+                                kvfix_kv_desc reuse, const kvfix_bf16* k_fresh,
+                                const kvfix_bf16* v_fresh, kvfix_kv_desc fresh, kvfix_bf16* k_out,
+                                kvfix_bf16* v_out, kvfix_kv_desc out, int32_t agents,
+                                const int32_t* delta, double rope_base, const int32_t* idx_k,
+                                const int32_t* idx_v, int32_t b, const float* w_k,
+                                const float* w_v, float* mu_k, float* mu_v, void* stream);
+
+/*
+ * kvfix_lowrank_apply -- add a rank-r factorised delta to a KV plane.
+ * [KVCMAS] Eq. 4 (corrected cache = reference + estimated delta), Eq. 7 (a delta
+ * stored as A B, A of size rows x r, B of size r x D), Eq. 8 with a single anchor.
+ *
+ *     out[c][l][j][h][e] = bf16( x[c][l][j][h][e] + sum_{k<r} A[c][l][h][j][k] B[c][l][h][k][e] )
+ * x, out : one KV plane described by `desc`; out may equal x (in place).
+ * A      : device bf16[chunks][layers][kv_heads][tokens][rank], contiguous.
+ * B      : device bf16[chunks][layers][kv_heads][rank][head_dim], contiguous.
+ * rank   : a multiple of 16, at most 64.  head_dim must be 64 or 128.
+ * Arithmetic: bf16 products on the tensor cores with float accumulation, then the add
+ * in float and one rounding to bf16.
+ */
+KVFIX_API kvfix_status kvfix_lowrank_apply(const kvfix_bf16* x, kvfix_kv_desc desc, const kvfix_bf16* A,
+                                 const kvfix_bf16* B, int32_t rank, kvfix_bf16* out,
+                                 void* stream);
+
+/*
+ * kvfix_draft_rank -- rank cached rows by the attention mass of draft queries, keep
+ * the best k_rows, and optionally repair them.
+ * [BCR] section 3 ("The repair": the row score a_j), App. B Algorithm 2 (draft
+ * scoring with grouped-query keys expanded to query heads) and Algorithm 1 step 6
+ * (selected rows' K and V overwritten with exact ones); [KVCMAS] Eq. 3.
+ *
+ *     scores[c][j] = sum_{l >= layer_begin} sum_{t < draft_steps} sum_{h < q_heads}
+ *                    softmax_j( q[c][l][t][h] . k[c][l][j][h / (q_heads/kv_heads)] / sqrt(D) )
+ * (summed over (t, h); the ranking equals the mean's).  idx[c] = the k_rows rows with
+ * the largest score (ties to the lower index), ascending.
+ * If k_io / v_io are non-NULL, then for every layer and KV head, rows idx[c] of k_io /
+ * v_io are overwritten with the same rows of k_fresh / v_fresh.  k_io may be the
+ * scored buffer `k` itself (the overwrite runs after scoring, in stream order).
+ *
+ * k              : the assembled keys, `desc` (heads = kv_heads).
+ * q              : device bf16[chunks][layers][draft_steps][q_heads][head_dim], contiguous.
+ * idx            : device int32[chunks][k_rows]; scores: device double[chunks][tokens].
+ * k_fresh, v_fresh, k_io, v_io : planes described by `fresh_desc` / `desc`, or NULL.
+ * workspace      : device buffer of kvfix_draft_rank_workspace_bytes(desc, layer_begin)
+ *                  bytes (16-byte aligned), contents irrelevant on entry.
+ * Limits: q_heads a multiple of kv_heads, q_heads/kv_heads * draft_steps <= 16,
+ * head_dim 64 or 128, tokens <= 65536, 0 <= k_rows <= tokens.
+ */
+KVFIX_API size_t kvfix_draft_rank_workspace_bytes(kvfix_kv_desc desc, int32_t layer_begin);
+KVFIX_API kvfix_status kvfix_draft_rank(const kvfix_bf16* k, kvfix_kv_desc desc, const kvfix_bf16* q,
+                              int32_t draft_steps, int32_t q_heads, int32_t layer_begin,
+                              int32_t k_rows, int32_t* idx, double* scores,
+                              const kvfix_bf16* k_fresh, const kvfix_bf16* v_fresh,
+                              kvfix_kv_desc fresh_desc, kvfix_bf16* k_io, kvfix_bf16* v_io,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * kvfix_diff_encode -- store sibling caches as block-sparse diffs against a master.
+ * [TD] section 4.3 (master-mirror layout, block-sparse K/V diff) and section 5 (a
+ * mirror keeps the touched block indices and those blocks' K/V contents; one index
+ * list shared by K and V).
+ *
+ * Entry i = (s*L + l)*nblk + blk covers tokens [bt*blk, bt*blk + bt) of layer l of
+ * sibling s, all heads, both planes (nblk = tokens / bt).  It is dirty iff some bf16
+ * word of K or V in it differs bitwise from the master's (so -0 differs from +0).
+ *     mask    : device uint32[ceil(S*L*nblk/32)], bit i%32 of word i/32 = dirty
+ *     offsets : device int64[S*L*nblk + 1], offsets[i] = dirty entries before i,
+ *               offsets[S*L*nblk] = total
+ *     payload : device bf16[capacity_entries][2][bt][kv_heads][head_dim]; dirty entry
+ *               i is stored at offsets[i]: the sibling's K block, then its V block.
+ * master_* : `master` (chunks == 1); sib_* : `sib` (chunks = S siblings, same shape).
+ * h_entries: optional HOST pointer.  If given, the call synchronises the stream after
+ *            the mask and offsets are built, stores the total there and returns
+ *            KVFIX_ENOSPACE without writing the payload if it exceeds
+ *            capacity_entries.  If NULL the call stays asynchronous and the device
+ *            skips (and flags) entries beyond capacity_entries.
+ * bt must divide tokens.
+ */
+KVFIX_API kvfix_status kvfix_diff_encode(const kvfix_bf16* master_k, const kvfix_bf16* master_v,
+                               kvfix_kv_desc master, const kvfix_bf16* sib_k,
+                               const kvfix_bf16* sib_v, kvfix_kv_desc sib, int32_t block_tokens,
+                               uint32_t* mask, int64_t* offsets, kvfix_bf16* payload,
+                               int64_t capacity_entries, int64_t* h_entries, void* stream);
+
+/*
+ * kvfix_diff_gather -- restore every sibling from the master and its diff.
+ * [TD] section 4.4, Algorithm 1 (load the master block, overwrite the blocks the diff
+ * touches with the diff's values); section 5 (paired K/V diff kernel).
+ *
+ *     out_P[s][l][block blk] = payload[offsets[i]].P   if mask bit i is set
+ *                            = master_P[l][block blk]   otherwise
+ * Each master block is read once for all siblings.
+ * mask, offsets, payload : as written by kvfix_diff_encode.
+ * payload_entries        : entries the payload buffer holds; a dirty entry whose offset
+ *                          lies beyond it is not read (its block gets the master's
+ *                          contents) and is flagged (KVFIX_ENOSPACE in kvfix_check_status).
+ * out_k, out_v           : `out` (chunks = siblings, same shape as master).
+ */
+KVFIX_API kvfix_status kvfix_diff_gather(const kvfix_bf16* master_k, const kvfix_bf16* master_v,
+                               kvfix_kv_desc master, const uint32_t* mask,
+                               const int64_t* offsets, const kvfix_bf16* payload,
+                               int64_t payload_entries, int32_t siblings, int32_t block_tokens,
+                               kvfix_bf16* out_k, kvfix_bf16* out_v, kvfix_kv_desc out,
+                               void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVFIX_H */

@@ -115,6 +115,10 @@ EXPORT void oracle_rope_theta(double base, int D, double* theta)
 static void rotate_row(const double* x, double* y, int D, double delta, const double* theta)
 {
     int h = D / 2;
+    if (delta == 0.0) { /* rotation by zero is the identity (also for signed zeros) */
+        memcpy(y, x, sizeof(double) * (size_t)D);
+        return;
+    }
     for (int i = 0; i < h; ++i) {
         double a = delta * theta[i];
         double c = cos(a), s = sin(a);

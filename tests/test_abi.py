@@ -1,0 +1,87 @@
+"""The C ABI: the library builds, loads and exports every entry point include/kvfix.h
+declares; host-side argument checks reject bad calls before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvfix.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from cross_context_kv_gb300 import build
+    build.build()
+    from cross_context_kv_gb300 import kvfix
+    return kvfix
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"KVFIX_API\s+[\w\s\*]+?\b(kvfix_\w+)\s*\(", text)
+
+
+def test_header_declares_the_seven_calls():
+    names = set(declared_symbols())
+    for call in ("kvfix_rerope", "kvfix_score_topk", "kvfix_draft_rank", "kvfix_mean_correct",
+                 "kvfix_lowrank_apply", "kvfix_diff_encode", "kvfix_diff_gather"):
+        assert call in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(lib.LIB_PATH)
+    missing = [n for n in declared_symbols() if not hasattr(raw, n)]
+    assert not missing, missing
+    assert set(declared_symbols()) == set(lib.SIGNATURES), "binding signatures out of sync with the header"
+
+
+def test_binding_argument_counts_match_header(lib):
+    text = open(HEADER).read()
+    for name in declared_symbols():
+        m = re.search(r"KVFIX_API[^;(]*\b" + name + r"\s*\(([^)]*)\)", text)
+        params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
+        assert len(params) == len(lib.SIGNATURES[name][1]), name
+
+
+def _desc(lib, C=1, L=1, n=16, H=1, D=64):
+    row = H * D
+    return lib.KvDesc(C, L, n, H, D, L * n * row, n * row, row)
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    L = lib.lib
+    fake = ctypes.c_void_p(1 << 20)      # never dereferenced: the checks fail first
+    odd = ctypes.c_void_p((1 << 20) + 2)  # not 16-byte aligned
+    bad_dim = _desc(lib, D=24)
+    assert L.kvfix_rerope(fake, fake, bad_dim, fake, 1e4, None) == lib.EINVAL
+    assert b"head_dim" in L.kvfix_last_error()
+    assert L.kvfix_rerope(odd, fake, _desc(lib), fake, 1e4, None) == lib.EINVAL
+    assert L.kvfix_rerope(fake, fake, _desc(lib), fake, 0.5, None) == lib.EINVAL
+    assert L.kvfix_rerope(None, fake, _desc(lib), fake, 1e4, None) == lib.EINVAL
+    d = _desc(lib)
+    # b out of range
+    assert L.kvfix_score_topk(fake, fake, d, fake, fake, d, 1, fake, 1e4, 17, fake, fake, fake, fake,
+                              fake, fake, None, None, None, None) == lib.EINVAL
+    # fresh chunks != agents * reuse chunks
+    assert L.kvfix_score_topk(fake, fake, d, fake, fake, d, 2, fake, 1e4, 3, fake, fake, fake, fake,
+                              fake, fake, None, None, None, None) == lib.EINVAL
+    # rank not a multiple of 16
+    assert L.kvfix_lowrank_apply(fake, _desc(lib, D=128), fake, fake, 8, ctypes.c_void_p(1 << 30), None) == lib.EINVAL
+    # block size must divide the tokens
+    dm = _desc(lib, n=40)
+    assert L.kvfix_diff_encode(fake, fake, dm, fake, fake, dm, 16, fake, fake, fake, 10, None, None) == lib.EINVAL
+    # workspace too small
+    dk = _desc(lib, C=1, L=2, n=64, H=1, D=128)
+    need = L.kvfix_draft_rank_workspace_bytes(dk, 1)
+    assert need > 0
+    assert L.kvfix_draft_rank(fake, dk, fake, 2, 8, 1, 4, fake, fake, None, None, dk, None, None,
+                              fake, need - 16, None) == lib.EINVAL
+    # grouped queries beyond 16 rows per KV head
+    assert L.kvfix_draft_rank(fake, dk, fake, 3, 8, 1, 4, fake, fake, None, None, dk, None, None,
+                              fake, need, None) == lib.EINVAL
+
+
+def test_version(lib):
+    assert lib.version() == 100
