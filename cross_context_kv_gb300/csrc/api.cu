@@ -114,18 +114,27 @@ kvfix_status kvfix_check_status(void* stream) {
     return KVFIX_OK;
 }
 
-kvfix_status kvfix_rerope(const kvfix_bf16* k_in, kvfix_bf16* k_out, kvfix_kv_desc desc,
-                          const int32_t* delta, double rope_base, void* stream) {
+static bool same_desc(const kvfix_kv_desc& a, const kvfix_kv_desc& b) {
+    return memcmp(&a, &b, sizeof a) == 0;
+}
+
+kvfix_status kvfix_rerope(const kvfix_bf16* k_in, kvfix_kv_desc in_desc, kvfix_bf16* k_out,
+                          kvfix_kv_desc out_desc, const int32_t* delta, double rope_base,
+                          void* stream) {
     kvfix_status st;
-    if ((st = check_plane(k_in, desc, "kvfix_rerope: k_in")) != KVFIX_OK) return st;
-    if ((st = check_plane(k_out, desc, "kvfix_rerope: k_out")) != KVFIX_OK) return st;
-    if (desc.chunks > 0 && delta == nullptr) return fail(KVFIX_EINVAL, "kvfix_rerope: delta is null");
+    if ((st = check_plane(k_in, in_desc, "kvfix_rerope: k_in")) != KVFIX_OK) return st;
+    if ((st = check_plane(k_out, out_desc, "kvfix_rerope: k_out")) != KVFIX_OK) return st;
+    if (!same_shape(in_desc, out_desc) || in_desc.chunks != out_desc.chunks)
+        return fail(KVFIX_EINVAL, "kvfix_rerope: k_in and k_out shapes differ");
+    if (in_desc.chunks > 0 && delta == nullptr) return fail(KVFIX_EINVAL, "kvfix_rerope: delta is null");
     if (!(rope_base > 1.0) || !isfinite(rope_base))
         return fail(KVFIX_EINVAL, "kvfix_rerope: rope_base must be finite and > 1");
-    if (k_in != k_out && overlaps(k_in, desc, k_out, desc))
-        return fail(KVFIX_EINVAL, "kvfix_rerope: k_out partially overlaps k_in");
-    RopeTheta th = make_theta(rope_base, desc.head_dim);
-    return launched(launch_rerope(k_in, k_out, desc, delta, th, (cudaStream_t)stream), "kvfix_rerope");
+    const bool in_place = (const void*)k_in == (const void*)k_out && same_desc(in_desc, out_desc);
+    if (!in_place && overlaps(k_in, in_desc, k_out, out_desc))
+        return fail(KVFIX_EINVAL, "kvfix_rerope: k_out overlaps k_in (only an exact in-place call is allowed)");
+    RopeTheta th = make_theta(rope_base, in_desc.head_dim);
+    return launched(launch_rerope(k_in, in_desc, k_out, out_desc, delta, th, (cudaStream_t)stream),
+                    "kvfix_rerope");
 }
 
 kvfix_status kvfix_score_topk(const kvfix_bf16* k_reuse, const kvfix_bf16* v_reuse,
@@ -232,23 +241,27 @@ kvfix_status kvfix_mean_correct(const kvfix_bf16* k_reuse, const kvfix_bf16* v_r
 
 kvfix_status kvfix_lowrank_apply(const kvfix_bf16* x, kvfix_kv_desc desc, const kvfix_bf16* A,
                                  const kvfix_bf16* B, int32_t rank, kvfix_bf16* out,
-                                 void* stream) {
+                                 kvfix_kv_desc out_desc, void* stream) {
     const char* fn = "kvfix_lowrank_apply";
     kvfix_status st;
     if ((st = check_plane(x, desc, "kvfix_lowrank_apply: x")) != KVFIX_OK) return st;
-    if ((st = check_plane(out, desc, "kvfix_lowrank_apply: out")) != KVFIX_OK) return st;
+    if ((st = check_plane(out, out_desc, "kvfix_lowrank_apply: out")) != KVFIX_OK) return st;
+    if (!same_shape(desc, out_desc) || desc.chunks != out_desc.chunks)
+        return fail(KVFIX_EINVAL, "%s: x and out shapes differ", fn);
     if (!A || !B) return fail(KVFIX_EINVAL, "%s: A and B are required", fn);
     if (!aligned16(A) || !aligned16(B)) return fail(KVFIX_EINVAL, "%s: A and B must be 16-byte aligned", fn);
     if (rank < 16 || rank > 64 || rank % 16) return fail(KVFIX_EINVAL, "%s: rank must be 16, 32, 48 or 64", fn);
     if (desc.head_dim != 64 && desc.head_dim != 128) return fail(KVFIX_EINVAL, "%s: head_dim must be 64 or 128", fn);
-    if (x != out && overlaps(x, desc, out, desc)) return fail(KVFIX_EINVAL, "%s: out partially overlaps x", fn);
+    const bool in_place = (const void*)x == (const void*)out && same_desc(desc, out_desc);
+    if (!in_place && overlaps(x, desc, out, out_desc))
+        return fail(KVFIX_EINVAL, "%s: out overlaps x (only an exact in-place call is allowed)", fn);
     const size_t na = 2 * (size_t)desc.chunks * desc.layers * desc.kv_heads * desc.tokens * rank;
     const size_t nb = 2 * (size_t)desc.chunks * desc.layers * desc.kv_heads * rank * desc.head_dim;
     uintptr_t o0, o1;
-    extent(out, desc, &o0, &o1);
+    extent(out, out_desc, &o0, &o1);
     if (overlaps_bytes((const void*)o0, o1 - o0, A, na) || overlaps_bytes((const void*)o0, o1 - o0, B, nb))
         return fail(KVFIX_EINVAL, "%s: out overlaps A or B", fn);
-    return launched(launch_lowrank(x, desc, A, B, rank, out, (cudaStream_t)stream), fn);
+    return launched(launch_lowrank(x, desc, A, B, rank, out, out_desc, (cudaStream_t)stream), fn);
 }
 
 size_t kvfix_draft_rank_workspace_bytes(kvfix_kv_desc desc, int32_t layer_begin) {

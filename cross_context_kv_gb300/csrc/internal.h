@@ -29,8 +29,9 @@ unsigned read_status_draft(cudaStream_t stream);
 
 // ---- launchers (enqueue only; arguments already validated) -----------------------
 
-cudaError_t launch_rerope(const uint16_t* in, uint16_t* out, const kvfix_kv_desc& d,
-                          const int32_t* delta, const RopeTheta& th, cudaStream_t s);
+cudaError_t launch_rerope(const uint16_t* in, const kvfix_kv_desc& d, uint16_t* out,
+                          const kvfix_kv_desc& od, const int32_t* delta, const RopeTheta& th,
+                          cudaStream_t s);
 
 cudaError_t launch_score(const uint16_t* k_reuse, const uint16_t* v_reuse,
                          const kvfix_kv_desc& reuse, const uint16_t* k_fresh,
@@ -51,7 +52,8 @@ cudaError_t launch_mean_correct(const uint16_t* reuse, const kvfix_kv_desc& rd,
                                 const float* w, float* mu, cudaStream_t s);
 
 cudaError_t launch_lowrank(const uint16_t* x, const kvfix_kv_desc& d, const uint16_t* A,
-                           const uint16_t* B, int rank, uint16_t* out, cudaStream_t s);
+                           const uint16_t* B, int rank, uint16_t* out, const kvfix_kv_desc& od,
+                           cudaStream_t s);
 
 size_t draft_workspace_bytes(const kvfix_kv_desc& d, int layer_begin);
 cudaError_t launch_draft(const uint16_t* k, const kvfix_kv_desc& d, const uint16_t* q,

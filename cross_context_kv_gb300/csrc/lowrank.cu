@@ -32,7 +32,7 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, cons
 template <int D>
 __global__ void __launch_bounds__(kLrWarps * 32)
 lowrank_mma_kernel(const uint16_t* x, Plane p, const uint16_t* __restrict__ A,
-                   const uint16_t* __restrict__ B, int rank, uint16_t* out) {
+                   const uint16_t* __restrict__ B, int rank, uint16_t* out, Plane op) {
     constexpr int kPitch = D + 8;            // bf16 elements per staged row
     constexpr int kNT = D / 8;               // n-tiles of 8 dims
     constexpr int kV = D / 8;                // 16-byte vectors per row
@@ -105,15 +105,16 @@ lowrank_mma_kernel(const uint16_t* x, Plane p, const uint16_t* __restrict__ A,
         for (int i = lane; i < rows * kV; i += 32) {
             int rr = i / kV, v = i % kV;
             uint4 val = *reinterpret_cast<const uint4*>(xs + rr * kPitch + 8 * v);
-            st_stream(reinterpret_cast<uint4*>(out + p.row(c, l, r0 + rr) + (long long)h * D + 8 * v), val);
+            st_stream(reinterpret_cast<uint4*>(out + op.row(c, l, r0 + rr) + (long long)h * D + 8 * v), val);
         }
         __syncwarp();
     }
 }
 
 cudaError_t launch_lowrank(const uint16_t* x, const kvfix_kv_desc& d, const uint16_t* A,
-                           const uint16_t* B, int rank, uint16_t* out, cudaStream_t s) {
-    Plane p = plane_of(d);
+                           const uint16_t* B, int rank, uint16_t* out, const kvfix_kv_desc& od,
+                           cudaStream_t s) {
+    Plane p = plane_of(d), op = plane_of(od);
     if (p.chunks == 0 || p.layers == 0 || p.tokens == 0) return cudaSuccess;
     const int rows_per_cta = kLrWarps * kLrRowsPerWarp * kLrTilesPerCta;
     dim3 grid((p.tokens + rows_per_cta - 1) / rows_per_cta, p.heads, p.chunks * p.layers);
@@ -123,11 +124,11 @@ cudaError_t launch_lowrank(const uint16_t* x, const kvfix_kv_desc& d, const uint
     if (p.dim == 128) {
         e = cudaFuncSetAttribute(lowrank_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        lowrank_mma_kernel<128><<<grid, kLrWarps * 32, smem, s>>>(x, p, A, B, rank, out);
+        lowrank_mma_kernel<128><<<grid, kLrWarps * 32, smem, s>>>(x, p, A, B, rank, out, op);
     } else {
         e = cudaFuncSetAttribute(lowrank_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        lowrank_mma_kernel<64><<<grid, kLrWarps * 32, smem, s>>>(x, p, A, B, rank, out);
+        lowrank_mma_kernel<64><<<grid, kLrWarps * 32, smem, s>>>(x, p, A, B, rank, out, op);
     }
     return cudaGetLastError();
 }

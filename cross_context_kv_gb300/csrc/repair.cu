@@ -54,7 +54,7 @@ constexpr int kRopeThreads = 256;
 constexpr int kRopeItems = 4;  // pair vectors per thread
 
 __global__ void __launch_bounds__(kRopeThreads)
-rerope_kernel(const uint16_t* __restrict__ in, uint16_t* out, Plane p,
+rerope_kernel(const uint16_t* in, Plane p, uint16_t* out, Plane op,
               const int32_t* __restrict__ delta, RopeTheta th) {
     __shared__ float2 tab[kMaxHeadDim / 2];
     const int c = blockIdx.y;
@@ -66,7 +66,7 @@ rerope_kernel(const uint16_t* __restrict__ in, uint16_t* out, Plane p,
     const long long items = (long long)p.layers * p.tokens * p.heads * v16;
     long long base = (long long)blockIdx.x * kRopeThreads * kRopeItems + threadIdx.x;
     uint4 lo[kRopeItems], hi[kRopeItems];
-    long long off[kRopeItems];
+    long long off[kRopeItems], oof[kRopeItems];
 #pragma unroll
     for (int k = 0; k < kRopeItems; ++k) {
         long long it = base + (long long)k * kRopeThreads;
@@ -79,6 +79,7 @@ rerope_kernel(const uint16_t* __restrict__ in, uint16_t* out, Plane p,
             int t = (int)(r % p.tokens);
             int l = (int)(r / p.tokens);
             off[k] = p.row(c, l, t) + (long long)h * p.dim + 8 * v;
+            oof[k] = op.row(c, l, t) + (long long)h * p.dim + 8 * v;
             lo[k] = ld_stream(reinterpret_cast<const uint4*>(in + off[k]));
             hi[k] = ld_stream(reinterpret_cast<const uint4*>(in + off[k] + half));
         }
@@ -95,24 +96,24 @@ rerope_kernel(const uint16_t* __restrict__ in, uint16_t* out, Plane p,
             lo[k] = pack8(a);
             hi[k] = pack8(b);
         }
-        st_stream(reinterpret_cast<uint4*>(out + off[k]), lo[k]);
-        st_stream(reinterpret_cast<uint4*>(out + off[k] + half), hi[k]);
+        st_stream(reinterpret_cast<uint4*>(out + oof[k]), lo[k]);
+        st_stream(reinterpret_cast<uint4*>(out + oof[k] + half), hi[k]);
     }
 }
 
-cudaError_t launch_rerope(const uint16_t* in, uint16_t* out, const kvfix_kv_desc& dd,
-                          const int32_t* delta, const RopeTheta& th, cudaStream_t s) {
-    Plane p = plane_of(dd);
+cudaError_t launch_rerope(const uint16_t* in, const kvfix_kv_desc& dd, uint16_t* out,
+                          const kvfix_kv_desc& od, const int32_t* delta, const RopeTheta& th,
+                          cudaStream_t s) {
+    Plane p = plane_of(dd), op = plane_of(od);
     long long items = (long long)p.layers * p.tokens * p.heads * (p.dim / 16);
     if (items == 0 || p.chunks == 0) return cudaSuccess;
     long long tiles = (items + kRopeThreads * kRopeItems - 1) / (kRopeThreads * kRopeItems);
     for (int c0 = 0; c0 < p.chunks; c0 += 65535) {
         int nc = p.chunks - c0 < 65535 ? p.chunks - c0 : 65535;
-        Plane q = p;
         const uint16_t* qin = in + (long long)c0 * p.sc;
-        uint16_t* qout = out + (long long)c0 * p.sc;
+        uint16_t* qout = out + (long long)c0 * op.sc;
         dim3 grid((unsigned)tiles, (unsigned)nc);
-        rerope_kernel<<<grid, kRopeThreads, 0, s>>>(qin, qout, q, delta + c0, th);
+        rerope_kernel<<<grid, kRopeThreads, 0, s>>>(qin, p, qout, op, delta + c0, th);
     }
     return cudaGetLastError();
 }

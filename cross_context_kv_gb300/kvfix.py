@@ -41,10 +41,10 @@ SIGNATURES = {
     "kvfix_version": (ctypes.c_int, []),
     "kvfix_last_error": (ctypes.c_char_p, []),
     "kvfix_check_status": (ctypes.c_int, [P]),
-    "kvfix_rerope": (ctypes.c_int, [P, P, D, P, F64, P]),
+    "kvfix_rerope": (ctypes.c_int, [P, D, P, D, P, F64, P]),
     "kvfix_score_topk": (ctypes.c_int, [P, P, D, P, P, D, I32, P, F64, I32, P, P, P, P, P, P, P, P, P, P]),
     "kvfix_mean_correct": (ctypes.c_int, [P, P, D, P, P, D, P, P, D, I32, P, F64, P, P, I32, P, P, P, P, P]),
-    "kvfix_lowrank_apply": (ctypes.c_int, [P, D, P, P, I32, P, P]),
+    "kvfix_lowrank_apply": (ctypes.c_int, [P, D, P, P, I32, P, D, P]),
     "kvfix_draft_rank_workspace_bytes": (SZ, [D, I32]),
     "kvfix_draft_rank": (ctypes.c_int, [P, D, P, I32, I32, I32, I32, P, P, P, P, D, P, P, P, SZ, P]),
     "kvfix_diff_encode": (ctypes.c_int, [P, P, D, P, P, D, I32, P, P, P, I64, P, P]),
@@ -130,10 +130,8 @@ def rerope(k: torch.Tensor, delta: torch.Tensor, rope_base: float, out: torch.Te
     _i32(delta, "delta")
     out = torch.empty_like(k) if out is None else out
     _bf16(out, "out")
-    d = plane_desc(k)
-    if plane_desc(out).tokens != d.tokens:
-        raise ValueError("out must match k")
-    _check(lib.kvfix_rerope(_ptr(k), _ptr(out), d, _ptr(delta), float(rope_base), _stream(k)))
+    _check(lib.kvfix_rerope(_ptr(k), plane_desc(k), _ptr(out), plane_desc(out), _ptr(delta),
+                            float(rope_base), _stream(k)))
     return out
 
 
@@ -201,8 +199,8 @@ def lowrank_apply(x, A, B, out=None):
         raise ValueError("A and B must be contiguous")
     out = torch.empty_like(x) if out is None else out
     _bf16(out, "out")
-    d = plane_desc(x)
-    _check(lib.kvfix_lowrank_apply(_ptr(x), d, _ptr(A), _ptr(B), int(A.shape[-1]), _ptr(out), _stream(x)))
+    _check(lib.kvfix_lowrank_apply(_ptr(x), plane_desc(x), _ptr(A), _ptr(B), int(A.shape[-1]), _ptr(out),
+                                   plane_desc(out), _stream(x)))
     return out
 
 

@@ -97,13 +97,15 @@ KVFIX_API kvfix_status kvfix_check_status(void* stream);
  * once more by the angle delta*theta_i:
  *     y_i       = x_i cos(delta theta_i) - x_{i+D/2} sin(delta theta_i)
  *     y_{i+D/2} = x_{i+D/2} cos(delta theta_i) + x_i sin(delta theta_i)
- * k_in, k_out : one KV plane, both described by `desc` (k_out may equal k_in).
- * delta       : device int32[desc.chunks], the shift of each chunk (any sign).
+ * k_in, k_out : one KV plane each, described by in_desc / out_desc (same shape; k_out
+ *               may be k_in itself with the same descriptor, for an in-place update).
+ * delta       : device int32[in_desc.chunks], the shift of each chunk (any sign).
  * Arithmetic: angles reduced in double, cos/sin and the rotation in float, output
  * rounded to nearest-even bf16.  delta = 0 reproduces the input bit for bit.
  */
-KVFIX_API kvfix_status kvfix_rerope(const kvfix_bf16* k_in, kvfix_bf16* k_out, kvfix_kv_desc desc,
-                          const int32_t* delta, double rope_base, void* stream);
+KVFIX_API kvfix_status kvfix_rerope(const kvfix_bf16* k_in, kvfix_kv_desc in_desc, kvfix_bf16* k_out,
+                                    kvfix_kv_desc out_desc, const int32_t* delta, double rope_base,
+                                    void* stream);
 
 /*
  * kvfix_score_topk -- check-layer divergence and probe selection.
@@ -178,7 +180,8 @@ KVFIX_API kvfix_status kvfix_mean_correct(const kvfix_bf16* k_reuse, const kvfix
  * stored as A B, A of size rows x r, B of size r x D), Eq. 8 with a single anchor.
  *
  *     out[c][l][j][h][e] = bf16( x[c][l][j][h][e] + sum_{k<r} A[c][l][h][j][k] B[c][l][h][k][e] )
- * x, out : one KV plane described by `desc`; out may equal x (in place).
+ * x, out : one KV plane each, described by desc / out_desc (same shape); out may be x
+ *          itself with the same descriptor (in place).
  * A      : device bf16[chunks][layers][kv_heads][tokens][rank], contiguous.
  * B      : device bf16[chunks][layers][kv_heads][rank][head_dim], contiguous.
  * rank   : a multiple of 16, at most 64.  head_dim must be 64 or 128.
@@ -186,8 +189,8 @@ KVFIX_API kvfix_status kvfix_mean_correct(const kvfix_bf16* k_reuse, const kvfix
  * in float and one rounding to bf16.
  */
 KVFIX_API kvfix_status kvfix_lowrank_apply(const kvfix_bf16* x, kvfix_kv_desc desc, const kvfix_bf16* A,
-                                 const kvfix_bf16* B, int32_t rank, kvfix_bf16* out,
-                                 void* stream);
+                                           const kvfix_bf16* B, int32_t rank, kvfix_bf16* out,
+                                           kvfix_kv_desc out_desc, void* stream);
 
 /*
  * kvfix_draft_rank -- rank cached rows by the attention mass of draft queries, keep

@@ -55,11 +55,14 @@ def test_host_validation_rejects_bad_arguments(lib):
     fake = ctypes.c_void_p(1 << 20)      # never dereferenced: the checks fail first
     odd = ctypes.c_void_p((1 << 20) + 2)  # not 16-byte aligned
     bad_dim = _desc(lib, D=24)
-    assert L.kvfix_rerope(fake, fake, bad_dim, fake, 1e4, None) == lib.EINVAL
+    assert L.kvfix_rerope(fake, bad_dim, fake, bad_dim, fake, 1e4, None) == lib.EINVAL
     assert b"head_dim" in L.kvfix_last_error()
-    assert L.kvfix_rerope(odd, fake, _desc(lib), fake, 1e4, None) == lib.EINVAL
-    assert L.kvfix_rerope(fake, fake, _desc(lib), fake, 0.5, None) == lib.EINVAL
-    assert L.kvfix_rerope(None, fake, _desc(lib), fake, 1e4, None) == lib.EINVAL
+    assert L.kvfix_rerope(odd, _desc(lib), fake, _desc(lib), fake, 1e4, None) == lib.EINVAL
+    assert L.kvfix_rerope(fake, _desc(lib), fake, _desc(lib), fake, 0.5, None) == lib.EINVAL
+    assert L.kvfix_rerope(None, _desc(lib), fake, _desc(lib), fake, 1e4, None) == lib.EINVAL
+    # partial overlap of input and output is refused
+    assert L.kvfix_rerope(fake, _desc(lib), ctypes.c_void_p((1 << 20) + 64), _desc(lib), fake, 1e4,
+                          None) == lib.EINVAL
     d = _desc(lib)
     # b out of range
     assert L.kvfix_score_topk(fake, fake, d, fake, fake, d, 1, fake, 1e4, 17, fake, fake, fake, fake,
@@ -68,7 +71,8 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert L.kvfix_score_topk(fake, fake, d, fake, fake, d, 2, fake, 1e4, 3, fake, fake, fake, fake,
                               fake, fake, None, None, None, None) == lib.EINVAL
     # rank not a multiple of 16
-    assert L.kvfix_lowrank_apply(fake, _desc(lib, D=128), fake, fake, 8, ctypes.c_void_p(1 << 30), None) == lib.EINVAL
+    assert L.kvfix_lowrank_apply(fake, _desc(lib, D=128), fake, fake, 8, ctypes.c_void_p(1 << 30),
+                                 _desc(lib, D=128), None) == lib.EINVAL
     # block size must divide the tokens
     dm = _desc(lib, n=40)
     assert L.kvfix_diff_encode(fake, fake, dm, fake, fake, dm, 16, fake, fake, fake, 10, None, None) == lib.EINVAL
