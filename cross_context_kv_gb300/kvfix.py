@@ -47,6 +47,7 @@ SIGNATURES = {
     "kvfix_lowrank_apply": (ctypes.c_int, [P, D, P, P, I32, P, D, P]),
     "kvfix_draft_rank_workspace_bytes": (SZ, [D, I32]),
     "kvfix_draft_rank": (ctypes.c_int, [P, D, P, I32, I32, I32, I32, P, P, P, P, D, P, P, P, SZ, P]),
+    "kvfix_draft_rank_noalloc": (ctypes.c_int, [P, D, P, I32, I32, I32, I32, P, P, P, P, D, P, P, P]),
     "kvfix_diff_encode": (ctypes.c_int, [P, P, D, P, P, D, I32, P, P, P, I64, P, P]),
     "kvfix_diff_gather": (ctypes.c_int, [P, P, D, P, P, P, I64, I32, I32, P, P, D, P]),
 }

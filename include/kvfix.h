@@ -225,6 +225,36 @@ KVFIX_API kvfix_status kvfix_draft_rank(const kvfix_bf16* k, kvfix_kv_desc desc,
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * kvfix_draft_rank_noalloc -- kvfix_draft_rank for callers that cannot allocate device
+ * memory.  The pages have no counterpart: this is a service of this library only.
+ *
+ * Who needs it: a serving engine that gives nearly all of HBM to its own KV-block
+ * pool at start-up (a later cudaMalloc fails or fragments the pool), or a
+ * latency-critical path that must not pay the device-wide synchronisation a
+ * cudaMalloc/cudaFree can imply.  Same arguments and results as kvfix_draft_rank,
+ * without the workspace: the scratch lives in a fixed buffer of
+ * KVFIX_DRAFT_NOALLOC_SCRATCH_BYTES that the library reserves on every GPU that loads
+ * it, until the process exits.  The call allocates nothing.
+ * - A problem that needs more scratch than the buffer holds
+ *   (kvfix_draft_rank_workspace_bytes(desc, layer_begin) > the constant) returns
+ *   KVFIX_EINVAL with a message and launches nothing.
+ * - All calls on a device share the buffer: calls whose kernels overlap on the GPU
+ *   race.  Order them (one stream, or events).
+ * - The buffer keeps the last call's contents; nothing in it needs to start at zero.
+ * - The first call on a device looks up the buffer's device address with that device
+ *   current; make that first call before any stream capture begins.
+ */
+#define KVFIX_DRAFT_NOALLOC_SCRATCH_BYTES (64u << 20)
+KVFIX_API kvfix_status kvfix_draft_rank_noalloc(const kvfix_bf16* k, kvfix_kv_desc desc,
+                                                const kvfix_bf16* q, int32_t draft_steps,
+                                                int32_t q_heads, int32_t layer_begin,
+                                                int32_t k_rows, int32_t* idx, double* scores,
+                                                const kvfix_bf16* k_fresh,
+                                                const kvfix_bf16* v_fresh,
+                                                kvfix_kv_desc fresh_desc, kvfix_bf16* k_io,
+                                                kvfix_bf16* v_io, void* stream);
+
+/*
  * kvfix_diff_encode -- store sibling caches as block-sparse diffs against a master.
  * [TD] section 4.3 (master-mirror layout, block-sparse K/V diff) and section 5 (a
  * mirror keeps the touched block indices and those blocks' K/V contents; one index

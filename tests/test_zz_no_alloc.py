@@ -1,0 +1,64 @@
+"""kvfix_draft_rank_noalloc: the draft-rank call for callers that cannot allocate device
+memory (an engine whose KV-block pool already holds nearly all of HBM, or a path that
+must not pay an allocation's synchronisation).  It uses a fixed scratch buffer owned by
+the library instead of a caller workspace.  This file is collected last on purpose:
+the check must hold in a fresh process and after every other test has run.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from cross_context_kv_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+CASES = [
+    synth.LOWRANK_70B.with_(name="noalloc_a", chunks=2, layers=3, tokens=300, kv_heads=2, q_heads=16, seed=60),
+    synth.LOWRANK_70B.with_(name="noalloc_b", chunks=1, layers=5, tokens=4096, kv_heads=8, q_heads=64, seed=61),
+]
+
+
+def _noalloc(kvfix, k, q, layer_begin, k_rows, k_fresh=None, v_fresh=None, k_io=None, v_io=None):
+    """Direct call through the C ABI; outputs are allocated here, by the caller."""
+    d = kvfix.plane_desc(k)
+    idx = torch.full((d.chunks, k_rows), -7, dtype=torch.int32, device=DEV)
+    scores = torch.full((d.chunks, d.tokens), float("nan"), dtype=torch.float64, device=DEV)
+    fd = kvfix.plane_desc(k_fresh) if k_fresh is not None else d
+    p = kvfix._ptr
+    st = kvfix.lib.kvfix_draft_rank_noalloc(p(k), d, p(q), int(q.shape[2]), int(q.shape[3]), int(layer_begin),
+                                            int(k_rows), p(idx), p(scores), p(k_fresh), p(v_fresh), fd, p(k_io),
+                                            p(v_io), kvfix._stream(k))
+    return st, idx, scores
+
+
+def test_noalloc_matches_draft_rank_on_consecutive_calls():
+    from cross_context_kv_gb300 import kvfix
+    for cfg in CASES:  # two calls in a row, different problems, one shared buffer
+        inp = synth.lowrank_inputs(cfg, DEV)
+        k, q = inp["x_k"], inp["q"]
+        ref_k, ref_v = k.clone(), inp["x_v"].clone()
+        ref_idx, ref_scores = kvfix.draft_rank(k, q, cfg.layer_begin, cfg.k_rows, inp["fresh_k"], inp["fresh_v"],
+                                               ref_k, ref_v)
+        got_k, got_v = k.clone(), inp["x_v"].clone()
+        st, idx, scores = _noalloc(kvfix, k, q, cfg.layer_begin, cfg.k_rows, inp["fresh_k"], inp["fresh_v"],
+                                   got_k, got_v)
+        assert st == kvfix.OK, kvfix.lib.kvfix_last_error()
+        kvfix.check_status()
+        assert torch.equal(idx, ref_idx)
+        np.testing.assert_allclose(scores.cpu().numpy(), ref_scores.cpu().numpy(), rtol=1e-5, atol=1e-9)
+        assert torch.equal(got_k.view(torch.int16), ref_k.view(torch.int16))
+        assert torch.equal(got_v.view(torch.int16), ref_v.view(torch.int16))
+
+
+def test_noalloc_rejects_problems_beyond_the_buffer():
+    from cross_context_kv_gb300 import kvfix
+    cfg = synth.LOWRANK_70B.with_(chunks=1, layers=3, tokens=65536, kv_heads=8, q_heads=64)
+    k = torch.zeros((1, 3, 65536, 8, 128), dtype=torch.bfloat16, device=DEV)
+    q = torch.zeros((1, 3, 2, 64, 128), dtype=torch.bfloat16, device=DEV)
+    assert kvfix.draft_rank_workspace_bytes(k, 1) > (64 << 20)
+    st, _, _ = _noalloc(kvfix, k, q, 1, 10)
+    assert st == kvfix.EINVAL
+    assert b"fixed buffer" in kvfix.lib.kvfix_last_error()
