@@ -457,7 +457,7 @@ def run_ours(args, world, rank, local):
                    "l2": "flushed between timed steps (512 MiB write); working set 1.6 GB > L2"},
         "tokens_per_s": round(world * by["tokens"] / ms * 1e3, 1),
         "algorithmic_bytes_per_step": by["step"],
-        "roofline": {"bound": "hbm", "kernel": "kvfix_mean_correct (probe-mean + correct, K and V)",
+        "roofline": {"bound": "hbm", "kernel": "mean_correct_kernel (kvfix_mean_correct: probe means + correction, K and V, one launch)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
                      "peak_kind": peak_kind + " (copy bandwidth)",
@@ -465,7 +465,7 @@ def run_ours(args, world, rank, local):
         "step_roofline_frac": round(by["step"] / ms / 1e6 / peak, 4),
         "e2e": {"value": round(world * by["corrected"] / e2e_ms / 1e6, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": 6 * args.steps,
+        "gpu_launches": 3 * args.steps,  # score, select, mean_correct per step
         "clocks": clocks,
     }
     del inp, fk, fv, reuse, flush

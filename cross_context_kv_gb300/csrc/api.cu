@@ -169,7 +169,7 @@ kvfix_status kvfix_score_topk(const kvfix_bf16* k_reuse, const kvfix_bf16* v_reu
     cudaStream_t s = (cudaStream_t)stream;
     RopeTheta th = make_theta(rope_base, reuse.head_dim);
     cudaError_t e = launch_score(k_reuse, v_reuse, reuse, k_fresh, v_fresh, fresh, agents, delta, th,
-                                 d_k, d_v, w_k, w_v, s);
+                                 d_k, d_v, w_k, w_v, mask_union, s);
     if (e != cudaSuccess) return cuda_fail(e, fn);
     e = launch_select_f32(d_k, d_v, (int)units, n, b, idx_k, idx_v, mask_k, mask_v, mask_union, s);
     return launched(e, fn);
@@ -230,13 +230,16 @@ kvfix_status kvfix_mean_correct(const kvfix_bf16* k_reuse, const kvfix_bf16* v_r
     if (!active) return fail(KVFIX_EINVAL, "%s: no plane given", fn);
     cudaStream_t s = (cudaStream_t)stream;
     RopeTheta th = make_theta(rope_base, reuse.head_dim);
-    for (auto& p : planes) {
-        if (!p.reuse) continue;
-        cudaError_t e = launch_mean_correct(p.reuse, reuse, p.fresh, fresh, p.out, out, agents, delta,
-                                            th, p.rotate, p.idx, b, p.w, p.mu, s);
-        if (e != cudaSuccess) return cuda_fail(e, fn);
+    McPlanes mp;
+    for (int q = 0; q < 2; ++q) {
+        mp.reuse[q] = planes[q].reuse;
+        mp.fresh[q] = planes[q].fresh;
+        mp.out[q] = planes[q].out;
+        mp.idx[q] = planes[q].idx;
+        mp.w[q] = planes[q].w;
+        mp.mu[q] = planes[q].mu;
     }
-    return KVFIX_OK;
+    return launched(launch_mean_correct(mp, reuse, fresh, out, agents, delta, th, b, s), fn);
 }
 
 kvfix_status kvfix_lowrank_apply(const kvfix_bf16* x, kvfix_kv_desc desc, const kvfix_bf16* A,

@@ -53,6 +53,17 @@ __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
     }
 }
 
+// acc[i] += the 8 bf16 values of v, in order.
+__device__ __forceinline__ void add8(const uint4& v, float* acc) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t = __bfloat1622float2(h[i]);
+        acc[2 * i] += t.x;
+        acc[2 * i + 1] += t.y;
+    }
+}
+
 __device__ __forceinline__ uint4 pack8(const float* f) {
     uint4 v;
     __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
@@ -105,4 +116,115 @@ __device__ __forceinline__ void rotate_pair(float* lo, float* hi, const float* c
     }
 }
 
+}  // namespace kvfix
+
+// ------------------------------------------------------------- async bulk copies
+// 1-D bulk copies global -> shared completed on an mbarrier (transaction bytes),
+// the TMA path for contiguous rows.  Waits are bounded in time: past the limit the
+// caller sets a timeout flag instead of spinning on.
+namespace kvfix {
+
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before later
+// async-proxy (bulk copy) accesses to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// One poll; the thread may be suspended (up to kSuspendNs) until the phase completes.
+constexpr unsigned kSuspendNs = 1000000;  // 1 ms per poll
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity; false once about kWaitCycles SM
+// clocks (~2 s) have passed without completion.
+constexpr long long kWaitCycles = 4000000000ll;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+}  // namespace kvfix
+
+namespace kvfix {
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+}  // namespace kvfix
+
+// ------------------------------------------------------------- 4-wide (8-byte) helpers
+namespace kvfix {
+__device__ __forceinline__ void unpack4(const uint2& v, float* f) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+    float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+    f[0] = a.x;
+    f[1] = a.y;
+    f[2] = b.x;
+    f[3] = b.y;
+}
+
+__device__ __forceinline__ uint2 pack4(const float* f) {
+    uint2 v;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+    h[0] = __floats2bfloat162_rn(f[0], f[1]);
+    h[1] = __floats2bfloat162_rn(f[2], f[3]);
+    return v;
+}
+
+__device__ __forceinline__ void add4(const uint2& v, float* acc) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+    float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+    acc[0] += a.x;
+    acc[1] += a.y;
+    acc[2] += b.x;
+    acc[3] += b.y;
+}
+
+__device__ __forceinline__ void rotate4(float* lo, float* hi, const float* c, const float* s) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float x0 = lo[k], x1 = hi[k];
+        lo[k] = x0 * c[k] - x1 * s[k];
+        hi[k] = x1 * c[k] + x0 * s[k];
+    }
+}
+
+__device__ __forceinline__ void st_stream2(uint2* p, const uint2& v) {
+    asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
 }  // namespace kvfix

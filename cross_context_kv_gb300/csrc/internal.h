@@ -37,7 +37,7 @@ cudaError_t launch_score(const uint16_t* k_reuse, const uint16_t* v_reuse,
                          const kvfix_kv_desc& reuse, const uint16_t* k_fresh,
                          const uint16_t* v_fresh, const kvfix_kv_desc& fresh, int agents,
                          const int32_t* delta, const RopeTheta& th, float* d_k, float* d_v,
-                         float* w_k, float* w_v, cudaStream_t s);
+                         float* w_k, float* w_v, uint32_t* mask_union, cudaStream_t s);
 
 // Top-b of float scores per unit for two planes (either may be skipped with NULL
 // scores), plus the optional union mask.
@@ -45,11 +45,19 @@ cudaError_t launch_select_f32(const float* d_k, const float* d_v, int units, int
                               int32_t* idx_k, int32_t* idx_v, uint32_t* mask_k,
                               uint32_t* mask_v, uint32_t* mask_union, cudaStream_t s);
 
-cudaError_t launch_mean_correct(const uint16_t* reuse, const kvfix_kv_desc& rd,
-                                const uint16_t* fresh, const kvfix_kv_desc& fd, uint16_t* out,
-                                const kvfix_kv_desc& od, int agents, const int32_t* delta,
-                                const RopeTheta& th, bool rotate, const int32_t* idx, int b,
-                                const float* w, float* mu, cudaStream_t s);
+// Both planes of one kvfix_mean_correct call (index 0 = K, rotated; 1 = V); a plane
+// whose reuse pointer is null is skipped.
+struct McPlanes {
+    const uint16_t* reuse[2];
+    const uint16_t* fresh[2];
+    uint16_t* out[2];
+    const int32_t* idx[2];
+    const float* w[2];
+    float* mu[2];
+};
+cudaError_t launch_mean_correct(const McPlanes& planes, const kvfix_kv_desc& rd,
+                                const kvfix_kv_desc& fd, const kvfix_kv_desc& od, int agents,
+                                const int32_t* delta, const RopeTheta& th, int b, cudaStream_t s);
 
 cudaError_t launch_lowrank(const uint16_t* x, const kvfix_kv_desc& d, const uint16_t* A,
                            const uint16_t* B, int rank, uint16_t* out, const kvfix_kv_desc& od,

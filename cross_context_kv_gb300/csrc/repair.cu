@@ -13,6 +13,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 
 namespace kvfix {
@@ -131,7 +133,8 @@ __global__ void __launch_bounds__(kScoreWarps * 32)
 score_kernel(const uint16_t* __restrict__ k_reuse, const uint16_t* __restrict__ v_reuse, Plane rp,
              const uint16_t* __restrict__ k_fresh, const uint16_t* __restrict__ v_fresh, Plane fp,
              int agents, const int32_t* __restrict__ delta, RopeTheta th, float* __restrict__ d_k,
-             float* __restrict__ d_v, float* __restrict__ w_k, float* __restrict__ w_v) {
+             float* __restrict__ d_v, float* __restrict__ w_k, float* __restrict__ w_v,
+             uint32_t* mask_union) {
     __shared__ float2 tab[kAgentGroup][kMaxHeadDim / 2];
     __shared__ int dl[kAgentGroup];
     const int R = rp.chunks;
@@ -143,6 +146,14 @@ score_kernel(const uint16_t* __restrict__ k_reuse, const uint16_t* __restrict__ 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t_base = blockIdx.x * (kScoreWarps * kScoreRowsPerWarp);
     const bool do_k = k_reuse != nullptr, do_v = v_reuse != nullptr;
+    if (mask_union) {  // the selection ORs both planes into it afterwards
+        const int words = (n + 31) / 32;
+        const int w0 = t_base / 32, w1 = min(words, (t_base + kScoreWarps * kScoreRowsPerWarp + 31) / 32);
+        for (int i = threadIdx.x; i < agents * (w1 - w0); i += blockDim.x) {
+            const int a = i / (w1 - w0), w = w0 + i % (w1 - w0);
+            mask_union[((long long)a * R + r) * words + w] = 0u;
+        }
+    }
 
     for (int a0 = 0; a0 < agents; a0 += kAgentGroup) {
         const int ag = agents - a0 < kAgentGroup ? agents - a0 : kAgentGroup;
@@ -221,13 +232,13 @@ cudaError_t launch_score(const uint16_t* k_reuse, const uint16_t* v_reuse,
                          const kvfix_kv_desc& reuse, const uint16_t* k_fresh,
                          const uint16_t* v_fresh, const kvfix_kv_desc& fresh, int agents,
                          const int32_t* delta, const RopeTheta& th, float* d_k, float* d_v,
-                         float* w_k, float* w_v, cudaStream_t s) {
+                         float* w_k, float* w_v, uint32_t* mask_union, cudaStream_t s) {
     Plane rp = plane_of(reuse), fp = plane_of(fresh);
     if (rp.tokens == 0 || rp.chunks == 0 || agents == 0) return cudaSuccess;
     const int rows = kScoreWarps * kScoreRowsPerWarp;
     dim3 grid((rp.tokens + rows - 1) / rows, rp.chunks);
     score_kernel<<<grid, kScoreWarps * 32, 0, s>>>(k_reuse, v_reuse, rp, k_fresh, v_fresh, fp,
-                                                   agents, delta, th, d_k, d_v, w_k, w_v);
+                                                   agents, delta, th, d_k, d_v, w_k, w_v, mask_union);
     return cudaGetLastError();
 }
 
@@ -307,9 +318,16 @@ __device__ void block_select(KeyAt key_at, int n, int b, uint32_t* bits, int32_t
         __syncthreads();
         const Key prefix = sm.prefix;
         const Key hi_mask = (shift + 8 >= kBits) ? Key(0) : ~((Key(1) << (shift + 8)) - Key(1));
-        for (int i = tid; i < n; i += blockDim.x) {
-            Key k = key_at(i);
-            if ((k & hi_mask) == (prefix & hi_mask)) atomicAdd(&sm.hist[(unsigned)(k >> shift) & 255u], 1u);
+        // warp-aggregated histogram: one atomic per distinct digit per warp
+        for (int i0 = 0; i0 < n; i0 += blockDim.x) {
+            const int i = i0 + tid;
+            unsigned dig = 256u;  // not counted
+            if (i < n) {
+                Key k = key_at(i);
+                if ((k & hi_mask) == (prefix & hi_mask)) dig = (unsigned)(k >> shift) & 255u;
+            }
+            const unsigned peers = __match_any_sync(0xffffffffu, dig);
+            if (dig < 256u && (tid & 31) == __ffs(peers) - 1) atomicAdd(&sm.hist[dig], (unsigned)__popc(peers));
         }
         __syncthreads();
         if (tid < 32) {
@@ -373,7 +391,8 @@ __device__ void block_select(KeyAt key_at, int n, int b, uint32_t* bits, int32_t
     __syncthreads();
 }
 
-// grid = units; dynamic smem: keys (when n fits) + 3 bitmaps.
+// grid = (units, 2 planes); dynamic smem: keys (when n fits) + one bitmap.  The union
+// mask (zeroed by the score kernel) receives both planes' bits with atomicOr.
 __global__ void __launch_bounds__(kSelThreads)
 select_f32_kernel(const float* __restrict__ d_k, const float* __restrict__ d_v, int n, int b,
                   int32_t* idx_k, int32_t* idx_v, uint32_t* mask_k, uint32_t* mask_v,
@@ -381,36 +400,28 @@ select_f32_kernel(const float* __restrict__ d_k, const float* __restrict__ d_v, 
     extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ SelectSmem<uint32_t> sm;
     const int words = (n + 31) / 32;
-    uint32_t* bk = reinterpret_cast<uint32_t*>(dyn);
-    uint32_t* bv = bk + words;
-    uint32_t* keys = bv + words;
+    uint32_t* bits = reinterpret_cast<uint32_t*>(dyn);
+    uint32_t* keys = bits + words;
     const bool cached = n <= kSelSmemKeys;
     const long long u = blockIdx.x;
-    for (int plane = 0; plane < 2; ++plane) {
-        const float* d = plane == 0 ? d_k : d_v;
-        uint32_t* bits = plane == 0 ? bk : bv;
-        if (d == nullptr) {
-            for (int w = threadIdx.x; w < words; w += blockDim.x) bits[w] = 0u;
-            __syncthreads();
-            continue;
-        }
-        const float* du = d + u * n;
-        if (cached) {
-            for (int i = threadIdx.x; i < n; i += blockDim.x) keys[i] = ordered_f32(du[i]);
-            __syncthreads();
-            block_select<uint32_t>([&](int i) { return keys[i]; }, n, b, bits,
-                                   (plane == 0 ? idx_k : idx_v) + u * b, sm);
-        } else {
-            block_select<uint32_t>([&](int i) { return ordered_f32(du[i]); }, n, b, bits,
-                                   (plane == 0 ? idx_k : idx_v) + u * b, sm);
-        }
-        uint32_t* m = plane == 0 ? mask_k : mask_v;
-        if (m)
-            for (int w = threadIdx.x; w < words; w += blockDim.x) m[u * words + w] = bits[w];
+    const int plane = blockIdx.y;
+    const float* d = plane == 0 ? d_k : d_v;
+    if (d == nullptr) return;
+    const float* du = d + u * n;
+    int32_t* idx_out = (plane == 0 ? idx_k : idx_v) + u * b;
+    if (cached) {
+        for (int i = threadIdx.x; i < n; i += blockDim.x) keys[i] = ordered_f32(du[i]);
         __syncthreads();
+        block_select<uint32_t>([&](int i) { return keys[i]; }, n, b, bits, idx_out, sm);
+    } else {
+        block_select<uint32_t>([&](int i) { return ordered_f32(du[i]); }, n, b, bits, idx_out, sm);
     }
+    uint32_t* m = plane == 0 ? mask_k : mask_v;
+    if (m)
+        for (int w = threadIdx.x; w < words; w += blockDim.x) m[u * words + w] = bits[w];
     if (mask_union)
-        for (int w = threadIdx.x; w < words; w += blockDim.x) mask_union[u * words + w] = bk[w] | bv[w];
+        for (int w = threadIdx.x; w < words; w += blockDim.x)
+            if (bits[w]) atomicOr(&mask_union[u * words + w], bits[w]);
 }
 
 cudaError_t launch_select_f32(const float* d_k, const float* d_v, int units, int n, int b,
@@ -418,194 +429,372 @@ cudaError_t launch_select_f32(const float* d_k, const float* d_v, int units, int
                               uint32_t* mask_v, uint32_t* mask_union, cudaStream_t s) {
     if (units == 0 || n == 0) return cudaSuccess;
     const int words = (n + 31) / 32;
-    size_t smem = sizeof(uint32_t) * (size_t)(2 * words + (n <= kSelSmemKeys ? n : 0));
+    size_t smem = sizeof(uint32_t) * (size_t)(words + (n <= kSelSmemKeys ? n : 0));
     cudaError_t e = cudaFuncSetAttribute(select_f32_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    select_f32_kernel<<<units, kSelThreads, smem, s>>>(d_k, d_v, n, b, idx_k, idx_v, mask_k,
-                                                       mask_v, mask_union);
+    select_f32_kernel<<<dim3(units, 2), kSelThreads, smem, s>>>(d_k, d_v, n, b, idx_k, idx_v, mask_k,
+                                                               mask_v, mask_union);
     return cudaGetLastError();
 }
 
 // =====================================================================================
-// Probe mean: one CTA per (unit, layer, head); 32 slots x (D/16) lanes.
-// Slot g sums probes i = g, g+32, ... in order; slots are then added in order.
-// The fresh probe rows are copied to the output on the way (they are the output).
+// Probe-mean correction, one launch for both planes.  One thread-block cluster of 8
+// CTAs per (reused chunk, layer, plane):
+//   phase 1, per agent: the 32 canonical partial sums P_s (s = probe index mod 32, each
+//     summed in probe-list order) are spread over the cluster, 4 per CTA; the fresh
+//     probe rows are copied to the output on the way.  The rotation is linear, so a
+//     slot sums fresh and reused rows separately and rotates the reused sum once:
+//     P_s = sum(fresh) - rot(sum(reuse)).  Cluster barrier; CTA k adds, for the row
+//     elements e with e % 4 == k % 4 in its half, the 32 partials in order 0..31 (read
+//     through distributed shared memory) and divides by b.  Cluster barrier; every CTA
+//     gathers the full mean.  Cluster barrier (the buffers are reused by the next agent).
+//   phase 2: CTA k streams 1/8 of the layer's rows through a 2-stage ring of 16 KB
+//     shared-memory tiles filled by bulk asynchronous copies (TMA, completion counted
+//     in bytes on a "full" mbarrier, release by every warp on an "empty" mbarrier).
+//     The first tiles are requested at kernel start, so they arrive during phase 1.
+//     Each reused row is read once and the corrected row of every agent of the group is
+//     written from it; probe rows are skipped (phase 1 wrote them).
+// Work unit of a thread: a "quad pair" -- dims [4v, 4v+4) of one head and their rotation
+// partners [D/2+4v, D/2+4v+4).  A thread keeps the same quad pair through phase 2, so
+// its cos/sin and mean values stay in registers.  Shared-memory vectors read 4 at a
+// time are stored by residue: element e sits at (e % 4) * (HD / 4) + e / 4.
+// The fixed summation order makes one call for N agents bit-identical to N calls.
 // =====================================================================================
-__global__ void probe_mean_kernel(const uint16_t* __restrict__ reuse, Plane rp,
-                                  const uint16_t* __restrict__ fresh, Plane fp, uint16_t* out,
-                                  Plane op, const int32_t* __restrict__ delta, RopeTheta th,
-                                  int rotate, const int32_t* __restrict__ idx, int b,
-                                  float* __restrict__ mu) {
-    extern __shared__ __align__(16) float part[];  // [32][D]
-    __shared__ float2 tab[kMaxHeadDim / 2];
-    const int h = blockIdx.x, l = blockIdx.y, u = blockIdx.z;
-    const int R = rp.chunks;
-    const int r = u % R;
-    const int D = rp.dim, half = D / 2, v16 = D / 16;
-    const int n = rp.tokens;
-    const int dlt = delta[u];
-    const bool rot = rotate && dlt != 0;
-    if (rot) build_table(tab, dlt, th, half, threadIdx.x, blockDim.x);
-    __syncthreads();
-    const int g = threadIdx.x / v16, v = threadIdx.x % v16;
-    float acc0[8], acc1[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) acc0[k] = acc1[k] = 0.f;
-    const int32_t* S = idx + (long long)u * b;
-    const long long eo = (long long)h * D + 8 * v;
-    for (int i = g; i < b; i += 32) {
-        const int j = S[i];
-        if (j < 0 || j >= n) {
-            atomicOr(&g_status_repair, FLAG_BOUNDS);
-            continue;
-        }
-        const long long ro = rp.row(r, l, j) + eo;
-        const long long fo = fp.row(u, l, j) + eo;
-        const long long oo = op.row(u, l, j) + eo;
-        uint4 x0v = *reinterpret_cast<const uint4*>(reuse + ro);
-        uint4 x1v = *reinterpret_cast<const uint4*>(reuse + ro + half);
-        uint4 f0v = *reinterpret_cast<const uint4*>(fresh + fo);
-        uint4 f1v = *reinterpret_cast<const uint4*>(fresh + fo + half);
-        st_stream(reinterpret_cast<uint4*>(out + oo), f0v);
-        st_stream(reinterpret_cast<uint4*>(out + oo + half), f1v);
-        float x0[8], x1[8], f0[8], f1[8];
-        unpack8(x0v, x0);
-        unpack8(x1v, x1);
-        unpack8(f0v, f0);
-        unpack8(f1v, f1);
-        if (rot) rotate_with(x0, x1, tab, 8 * v);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            acc0[k] += f0[k] - x0[k];
-            acc1[k] += f1[k] - x1[k];
-        }
-    }
-    float* mine = part + g * D;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        mine[8 * v + k] = acc0[k];
-        mine[half + 8 * v + k] = acc1[k];
-    }
-    __syncthreads();
-    float* mu_row = mu + ((long long)u * rp.layers + l) * ((long long)rp.heads * D) + (long long)h * D;
-    for (int e = threadIdx.x; e < D; e += blockDim.x) {
-        float s = 0.f;
-        for (int q = 0; q < 32; ++q) s += part[q * D + e];
-        mu_row[e] = b > 0 ? s / (float)b : 0.f;
-    }
+namespace cg = cooperative_groups;
+
+constexpr int kMcCluster = 8;
+constexpr int kMcThreads = 256;
+constexpr int kMcWarps = kMcThreads / 32;
+constexpr int kMcSlotsPerCta = 32 / kMcCluster;
+constexpr int kMcLanesPerSlot = kMcThreads / kMcSlotsPerCta;  // 64
+constexpr int kMcStages = 2;
+constexpr int kMcTileBytes = 16384;
+
+struct McArgs {
+    const uint16_t* reuse[2];
+    const uint16_t* fresh[2];
+    uint16_t* out[2];
+    const int32_t* idx[2];
+    const float* w[2];
+    float* mu[2];
+    Plane rp, fp, op;
+    int agents, b, rows_per_cta, tile_rows;
+    const int32_t* delta;
+    RopeTheta th;
+};
+
+struct McLayout {  // byte offsets into the dynamic shared memory
+    int ps, slice, ring, mu_all, cs, member, total, words_member;
+};
+
+__host__ __device__ inline int align128(int x) { return (x + 127) / 128 * 128; }
+
+__host__ __device__ inline McLayout mc_layout(int HD, int half, int ag, int rows_per_cta, int tile_rows) {
+    McLayout m;
+    m.ps = 0;
+    m.slice = m.ps + 4 * kMcSlotsPerCta * HD;
+    m.ring = align128(m.slice + 4 * (HD / kMcCluster));
+    m.mu_all = align128(m.ring + kMcStages * tile_rows * HD * 2);
+    m.cs = m.mu_all + 4 * ag * HD;
+    m.member = m.cs + 4 * 2 * ag * half;
+    m.words_member = (rows_per_cta + 31) / 32;
+    m.total = m.member + 4 * ag * m.words_member;
+    return m;
 }
 
-// =====================================================================================
-// Correction of the non-probe rows: one CTA per (token tile, layer, reused chunk).
-// The reused tile is read once; every agent's corrected rows are written from it.
-// =====================================================================================
-constexpr int kCorrThreads = 256;
-constexpr int kCorrTile = 64;  // tokens per CTA
-
-__global__ void __launch_bounds__(kCorrThreads)
-correct_kernel(const uint16_t* __restrict__ reuse, Plane rp, uint16_t* out, Plane op, int agents,
-               const int32_t* __restrict__ delta, RopeTheta th, int rotate,
-               const int32_t* __restrict__ idx, int b, const float* __restrict__ w,
-               const float* __restrict__ mu) {
-    extern __shared__ __align__(16) float smu[];  // [kAgentGroup][H*D]
-    __shared__ float2 tab[kAgentGroup][kMaxHeadDim / 2];
-    __shared__ uint32_t member[kAgentGroup][kCorrTile / 32];
-    __shared__ float sw[kAgentGroup][kCorrTile];
+__global__ void __cluster_dims__(kMcCluster, 1, 1) __launch_bounds__(kMcThreads, 4)
+mean_correct_kernel(McArgs args) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full[kMcStages];
+    __shared__ __align__(8) uint64_t empty[kMcStages];
     __shared__ int rot_on[kAgentGroup];
-    const int t0 = blockIdx.x * kCorrTile, l = blockIdx.y, r = blockIdx.z;
-    const int R = rp.chunks, n = rp.tokens;
-    const int D = rp.dim, half = D / 2, v16 = D / 16, HD = rp.heads * D;
-    const int P = rp.heads * v16;
-    const int tt = min(kCorrTile, n - t0);
-    const int items = tt * P;
+    __shared__ int abort_flag;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int plane = blockIdx.y & 1, l = blockIdx.y >> 1, r = blockIdx.z;
+    const uint16_t* reuse = args.reuse[plane];
+    if (reuse == nullptr) return;  // plane not requested: the whole cluster leaves
+    const uint16_t* fresh = args.fresh[plane];
+    uint16_t* out = args.out[plane];
+    const int32_t* idx = args.idx[plane];
+    const float* wgt = args.w[plane];
+    float* mu = args.mu[plane];
+    const Plane& rp = args.rp;
+    const Plane& fp = args.fp;
+    const Plane& op = args.op;
+    const int R = rp.chunks, n = rp.tokens, L = rp.layers;
+    const int D = rp.dim, half = D / 2, v8 = D / 8;       // quads per half-head
+    const int HD = rp.heads * D, P = rp.heads * v8, G = HD / 4;
+    const int SL = HD / kMcCluster;                       // mean elements reduced per CTA
+    const int b = args.b;
+    const bool keys = plane == 0;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int t_lo = min(n, rank * args.rows_per_cta), t_hi = min(n, t_lo + args.rows_per_cta);
+    const int TR = args.tile_rows;
+    const int ag_max = min(args.agents, kAgentGroup);
+    const McLayout lay = mc_layout(HD, half, ag_max, args.rows_per_cta, TR);
+    float* ps = reinterpret_cast<float*>(smem + lay.ps);                // [4 slots][HD] by residue
+    float* mu_slice = reinterpret_cast<float*>(smem + lay.slice);      // [SL]
+    uint16_t* ring = reinterpret_cast<uint16_t*>(smem + lay.ring);
+    float* mu_all = reinterpret_cast<float*>(smem + lay.mu_all);      // [ag][HD] by residue
+    float* cos_t = reinterpret_cast<float*>(smem + lay.cs);           // [ag][4][D/8]
+    float* sin_t = cos_t + ag_max * half;                             // [ag][4][D/8]
+    uint32_t* member = reinterpret_cast<uint32_t*>(smem + lay.member);
+    const bool rows_contig = rp.st == HD;
+    const unsigned row_bytes = (unsigned)HD * 2u;
+    const int groups = (args.agents + kAgentGroup - 1) / kAgentGroup;
+    const int tiles = (t_hi - t_lo + TR - 1) / TR;   // per agent group
+    const int total_tiles = groups * tiles;
+    int issued = 0;                                  // thread 0 only
 
-    for (int a0 = 0; a0 < agents; a0 += kAgentGroup) {
-        const int ag = min(kAgentGroup, agents - a0);
+    auto issue = [&](int k) {  // thread 0: bulk-copy global tile k into its stage
+        const int slot = k % kMcStages;
+        const int t0 = t_lo + (k % tiles) * TR;
+        const int tt = min(TR, t_hi - t0);
+        uint16_t* dst = ring + (size_t)slot * TR * HD;
+        mbar_arrive_expect_tx(&full[slot], row_bytes * tt);
+        if (rows_contig) {
+            bulk_g2s(dst, reuse + rp.row(r, l, t0), row_bytes * tt, &full[slot]);
+        } else {
+            for (int q = 0; q < tt; ++q) bulk_g2s(dst + q * HD, reuse + rp.row(r, l, t0 + q), row_bytes, &full[slot]);
+        }
+    };
+
+    if (tid == 0) {
+        for (int q = 0; q < kMcStages; ++q) {
+            mbar_init(&full[q], 1);
+            mbar_init(&empty[q], kMcWarps);
+        }
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    __syncthreads();
+    if (tid == 0)  // the first tiles stream in while phase 1 runs
+        for (; issued < min(kMcStages, total_tiles); ++issued) issue(issued);
+
+    for (int grp = 0; grp < groups; ++grp) {
+        const int a0 = grp * kAgentGroup;
+        const int ag = min(kAgentGroup, args.agents - a0);
         __syncthreads();
-        for (int i = threadIdx.x; i < ag * (kCorrTile / 32); i += blockDim.x)
-            member[i / (kCorrTile / 32)][i % (kCorrTile / 32)] = 0u;
-        for (int i = threadIdx.x; i < ag * half; i += blockDim.x) {
-            int a = i / half, e = i % half;
+        for (int i = tid; i < ag * half; i += kMcThreads) {
+            const int a = i / half, e = i % half;  // angle index e = 4 * vq + k
             float c = 1.f, s = 0.f;
-            if (rotate) rope_cos_sin(delta[(a0 + a) * R + r], th.theta[e], &c, &s);
-            tab[a][e] = make_float2(c, s);
+            if (keys) rope_cos_sin(args.delta[(a0 + a) * R + r], args.th.theta[e], &c, &s);
+            const int o = (a * 4 + (e % 4)) * v8 + e / 4;
+            cos_t[o] = c;
+            sin_t[o] = s;
         }
-        if (threadIdx.x < ag) rot_on[threadIdx.x] = rotate && delta[(a0 + threadIdx.x) * R + r] != 0;
-        for (int i = threadIdx.x; i < ag * HD; i += blockDim.x) {
-            int a = i / HD, e = i % HD;
-            const long long u = (long long)(a0 + a) * R + r;
-            smu[i] = b > 0 ? mu[(u * rp.layers + l) * HD + e] : 0.f;
-        }
-        for (int i = threadIdx.x; i < ag * tt; i += blockDim.x) {
-            int a = i / tt, t = i % tt;
-            const long long u = (long long)(a0 + a) * R + r;
-            sw[a][t] = w[u * n + t0 + t];
-        }
+        if (tid < ag) rot_on[tid] = keys && args.delta[(a0 + tid) * R + r] != 0;
+        for (int i = tid; i < ag * lay.words_member; i += kMcThreads) member[i] = 0u;
         __syncthreads();
-        for (int i = threadIdx.x; i < ag * b; i += blockDim.x) {
-            int a = i / b, q = i % b;
+
+        // ---------------- phase 1: probe means, one agent at a time
+        for (int a = 0; a < ag; ++a) {
             const long long u = (long long)(a0 + a) * R + r;
-            int j = idx[u * b + q];
-            if (j >= t0 && j < t0 + tt) atomicOr(&member[a][(j - t0) >> 5], 1u << ((j - t0) & 31));
-        }
-        __syncthreads();
-        for (int it = threadIdx.x; it < items; it += kCorrThreads) {
-            const int t = it / P, pv = it % P;
-            const int h = pv / v16, v = pv % v16;
-            const long long eo = (long long)h * D + 8 * v;
-            const long long ro = rp.row(r, l, t0 + t) + eo;
-            const uint4 x0v = ld_stream(reinterpret_cast<const uint4*>(reuse + ro));
-            const uint4 x1v = ld_stream(reinterpret_cast<const uint4*>(reuse + ro + half));
-            for (int a = 0; a < ag; ++a) {
-                if (member[a][t >> 5] >> (t & 31) & 1u) continue;
-                float x0[8], x1[8];
-                unpack8(x0v, x0);
-                unpack8(x1v, x1);
-                if (rot_on[a]) rotate_with(x0, x1, tab[a], 8 * v);
-                if (b > 0) {
-                    const float wt = sw[a][t];
-                    const float* m = smu + a * HD + h * D + 8 * v;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        x0[k] = fmaf(wt, m[k], x0[k]);
-                        x1[k] = fmaf(wt, m[half + k], x1[k]);
-                    }
+            float* mu_g = mu + (u * L + l) * (long long)HD;
+            if (b == 0) {
+                for (int e = tid; e < HD; e += kMcThreads) mu_all[a * HD + e] = 0.f;
+                for (int e = tid; e < SL; e += kMcThreads) {
+                    const int ri = rank * SL + e;  // residue-major index
+                    mu_g[4 * (ri % G) + ri / G] = 0.f;
                 }
+                continue;
+            }
+            const int32_t* S = idx + u * b;
+            const int ls = tid / kMcLanesPerSlot;
+            const int s = rank * kMcSlotsPerCta + ls;
+            for (int pq = tid % kMcLanesPerSlot; pq < P; pq += kMcLanesPerSlot) {
+                const int h = pq / v8, v = pq % v8;
+                const long long eo = (long long)h * D + 4 * v;
+                const int g_lo = h * (D / 4) + v, g_hi = g_lo + v8;
+                float fs0[4], fs1[4], xs0[4], xs1[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) fs0[k] = fs1[k] = xs0[k] = xs1[k] = 0.f;
+                for (int i = s; i < b; i += 32) {
+                    const int j = S[i];
+                    if (j < 0 || j >= n) {
+                        atomicOr(&g_status_repair, FLAG_BOUNDS);
+                        continue;
+                    }
+                    const long long ro = rp.row(r, l, j) + eo;
+                    const long long fo = fp.row((int)u, l, j) + eo;
+                    const uint2 x0v = *reinterpret_cast<const uint2*>(reuse + ro);
+                    const uint2 x1v = *reinterpret_cast<const uint2*>(reuse + ro + half);
+                    const uint2 f0v = *reinterpret_cast<const uint2*>(fresh + fo);
+                    const uint2 f1v = *reinterpret_cast<const uint2*>(fresh + fo + half);
+                    const long long oo = op.row((int)u, l, j) + eo;
+                    st_stream2(reinterpret_cast<uint2*>(out + oo), f0v);
+                    st_stream2(reinterpret_cast<uint2*>(out + oo + half), f1v);
+                    add4(x0v, xs0);
+                    add4(x1v, xs1);
+                    add4(f0v, fs0);
+                    add4(f1v, fs1);
+                }
+                if (rot_on[a]) {
+                    float c[4], sn[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        c[k] = cos_t[(a * 4 + k) * v8 + v];
+                        sn[k] = sin_t[(a * 4 + k) * v8 + v];
+                    }
+                    rotate4(xs0, xs1, c, sn);
+                }
+                float* mine = ps + ls * HD;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    mine[k * G + g_lo] = fs0[k] - xs0[k];
+                    mine[k * G + g_hi] = fs1[k] - xs1[k];
+                }
+            }
+            cluster.sync();
+            // residue-major elements [rank*SL, rank*SL + SL): 32 partials added in order
+            for (int e = tid; e < SL; e += kMcThreads) {
+                const int ri = rank * SL + e;
+                float sum = 0.f;
+                for (int q = 0; q < 32; ++q) {
+                    const float* rps = cluster.map_shared_rank(ps, q / kMcSlotsPerCta);
+                    sum += rps[(q % kMcSlotsPerCta) * HD + ri];
+                }
+                const float m = sum / (float)b;
+                mu_slice[e] = m;
+                mu_g[4 * (ri % G) + ri / G] = m;
+            }
+            cluster.sync();
+            for (int i = tid; i < HD; i += kMcThreads) {
+                const float* rsl = cluster.map_shared_rank(mu_slice, i / SL);
+                mu_all[a * HD + i] = rsl[i % SL];
+            }
+            cluster.sync();
+        }
+
+        // ---------------- phase 2: stream this CTA's rows for every agent of the group
+        if (b > 0) {
+            for (int i = tid; i < ag * b; i += kMcThreads) {
+                const int a = i / b;
                 const long long u = (long long)(a0 + a) * R + r;
-                const long long oo = op.row((int)u, l, t0 + t) + eo;
-                st_stream(reinterpret_cast<uint4*>(out + oo), pack8(x0));
-                st_stream(reinterpret_cast<uint4*>(out + oo + half), pack8(x1));
+                const int j = idx[u * b + (i % b)];
+                if (j >= t_lo && j < t_hi)
+                    atomicOr(&member[a * lay.words_member + ((j - t_lo) >> 5)], 1u << ((j - t_lo) & 31));
             }
         }
+        __syncthreads();
+        const int rpp = kMcThreads / P;  // rows per pass (P <= 256 quad pairs per row)
+        const bool active = tid < rpp * P;
+        const int pq = tid % P, row_off = tid / P;
+        const int h = pq / v8, v = pq % v8;
+        const int eo = h * D + 4 * v;
+        const int g_lo = h * (D / 4) + v, g_hi = g_lo + v8;
+        float c[4], sn[4], m0[4], m1[4];
+        int cached = -1;  // agent whose cos/sin/mean sit in c, sn, m0, m1
+        for (int kl = 0; kl < tiles; ++kl) {
+            const int k = grp * tiles + kl;
+            const int slot = k % kMcStages;
+            const unsigned parity = (unsigned)(k / kMcStages) & 1u;
+            if (abort_flag) break;
+            if (!mbar_wait(&full[slot], parity)) {
+                atomicOr(&g_status_repair, FLAG_TIMEOUT);
+                abort_flag = 1;
+                break;
+            }
+            const uint16_t* tb = ring + (size_t)slot * TR * HD + eo;
+            const int t0 = t_lo + kl * TR;
+            const int tt = min(TR, t_hi - t0);
+            if (active) {
+                for (int a = 0; a < ag; ++a) {
+                    const bool rot = rot_on[a];
+                    if (a != cached) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            c[q] = rot ? cos_t[(a * 4 + q) * v8 + v] : 1.f;
+                            sn[q] = rot ? sin_t[(a * 4 + q) * v8 + v] : 0.f;
+                            m0[q] = mu_all[a * HD + q * G + g_lo];
+                            m1[q] = mu_all[a * HD + q * G + g_hi];
+                        }
+                        cached = a;
+                    }
+                    const long long u = (long long)(a0 + a) * R + r;
+                    uint16_t* ob = out + op.row((int)u, l, 0) + eo;
+                    const float* wb = wgt + u * n;
+                    const uint32_t* mem = member + a * lay.words_member;
+                    for (int row = row_off; row < tt; row += rpp) {
+                        const int t = t0 + row, tl = t - t_lo;
+                        if (mem[tl >> 5] >> (tl & 31) & 1u) continue;
+                        float x0[4], x1[4];
+                        unpack4(*reinterpret_cast<const uint2*>(tb + row * HD), x0);
+                        unpack4(*reinterpret_cast<const uint2*>(tb + row * HD + half), x1);
+                        if (rot) rotate4(x0, x1, c, sn);
+                        if (b > 0) {
+                            const float wt = __ldg(wb + t);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                x0[q] = fmaf(wt, m0[q], x0[q]);
+                                x1[q] = fmaf(wt, m1[q], x1[q]);
+                            }
+                        }
+                        uint16_t* o = ob + (long long)t * op.st;
+                        st_stream2(reinterpret_cast<uint2*>(o), pack4(x0));
+                        st_stream2(reinterpret_cast<uint2*>(o + half), pack4(x1));
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (tid == 0 && issued < total_tiles) {
+                // the stage is free once every warp released it; then refill it
+                if (!mbar_wait(&empty[slot], parity)) {
+                    atomicOr(&g_status_repair, FLAG_TIMEOUT);
+                    abort_flag = 1;
+                } else {
+                    issue(issued);
+                    ++issued;
+                }
+            }
+        }
+        __syncthreads();
+        if (abort_flag) {
+            // wait (bounded) for every copy still in flight, then leave
+            if (tid == 0)
+                for (int k = max(0, issued - kMcStages); k < issued; ++k)
+                    mbar_wait(&full[k % kMcStages], (unsigned)(k / kMcStages) & 1u);
+            __syncthreads();
+            return;
+        }
     }
 }
 
-cudaError_t launch_mean_correct(const uint16_t* reuse, const kvfix_kv_desc& rd,
-                                const uint16_t* fresh, const kvfix_kv_desc& fd, uint16_t* out,
+cudaError_t launch_mean_correct(const McPlanes& pl, const kvfix_kv_desc& rd, const kvfix_kv_desc& fd,
                                 const kvfix_kv_desc& od, int agents, const int32_t* delta,
-                                const RopeTheta& th, bool rotate, const int32_t* idx, int b,
-                                const float* w, float* mu, cudaStream_t s) {
-    Plane rp = plane_of(rd), fp = plane_of(fd), op = plane_of(od);
-    const int units = agents * rp.chunks;
-    if (units == 0 || rp.layers == 0 || rp.tokens == 0) return cudaSuccess;
-    const size_t mu_bytes = sizeof(float) * (size_t)units * rp.layers * rp.heads * rp.dim;
-    cudaError_t e;
-    if (b > 0) {
-        dim3 grid(rp.heads, rp.layers, units);
-        size_t smem = sizeof(float) * 32 * (size_t)rp.dim;
-        probe_mean_kernel<<<grid, 2 * rp.dim, smem, s>>>(reuse, rp, fresh, fp, out, op, delta, th,
-                                                         rotate ? 1 : 0, idx, b, mu);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    } else {
-        if ((e = cudaMemsetAsync(mu, 0, mu_bytes, s)) != cudaSuccess) return e;
+                                const RopeTheta& th, int b, cudaStream_t s) {
+    McArgs a;
+    for (int q = 0; q < 2; ++q) {
+        a.reuse[q] = pl.reuse[q];
+        a.fresh[q] = pl.fresh[q];
+        a.out[q] = pl.out[q];
+        a.idx[q] = pl.idx[q];
+        a.w[q] = pl.w[q];
+        a.mu[q] = pl.mu[q];
     }
-    dim3 grid((rp.tokens + kCorrTile - 1) / kCorrTile, rp.layers, rp.chunks);
-    size_t smem = sizeof(float) * kAgentGroup * (size_t)rp.heads * rp.dim;
-    e = cudaFuncSetAttribute(correct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    a.rp = plane_of(rd);
+    a.fp = plane_of(fd);
+    a.op = plane_of(od);
+    a.agents = agents;
+    a.b = b;
+    a.delta = delta;
+    a.th = th;
+    const int n = a.rp.tokens;
+    if (agents == 0 || a.rp.chunks == 0 || a.rp.layers == 0 || n == 0) return cudaSuccess;
+    a.rows_per_cta = (n + kMcCluster - 1) / kMcCluster;
+    const int HD = a.rp.heads * a.rp.dim;
+    a.tile_rows = kMcTileBytes / (2 * HD) > 0 ? kMcTileBytes / (2 * HD) : 1;
+    const int ag = agents < kAgentGroup ? agents : kAgentGroup;
+    const McLayout lay = mc_layout(HD, a.rp.dim / 2, ag, a.rows_per_cta, a.tile_rows);
+    const size_t smem = (size_t)lay.total;
+    cudaError_t e = cudaFuncSetAttribute(mean_correct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
-    correct_kernel<<<grid, kCorrThreads, smem, s>>>(reuse, rp, out, op, agents, delta, th,
-                                                    rotate ? 1 : 0, idx, b, w, mu);
+    dim3 grid(kMcCluster, 2 * a.rp.layers, a.rp.chunks);
+    mean_correct_kernel<<<grid, kMcThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
