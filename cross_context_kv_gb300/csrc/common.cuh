@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "internal.h"
 
 namespace kvfix {
@@ -226,5 +228,33 @@ __device__ __forceinline__ void rotate4(float* lo, float* hi, const float* c, co
 
 __device__ __forceinline__ void st_stream2(uint2* p, const uint2& v) {
     asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+}  // namespace kvfix
+
+// ------------------------------------------------------------- programmatic launch
+// Kernels of one call chain (score -> select -> mean correction) are launched with
+// programmatic stream serialisation: the next kernel may start once every CTA of the
+// previous one has called pdl_trigger(), and must call pdl_wait() before it reads
+// anything the previous kernel writes.  Before pdl_wait() a kernel only reads inputs
+// that no kernel of the chain writes.  Launched without the attribute (or after a
+// kernel that never triggers), pdl_wait() returns at once and order is as usual.
+namespace kvfix {
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... Exp, typename... Act>
+inline cudaError_t launch_chained(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t s, Act&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...);
 }
 }  // namespace kvfix

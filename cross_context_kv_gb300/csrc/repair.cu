@@ -146,6 +146,7 @@ score_kernel(const uint16_t* __restrict__ k_reuse, const uint16_t* __restrict__ 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t_base = blockIdx.x * (kScoreWarps * kScoreRowsPerWarp);
     const bool do_k = k_reuse != nullptr, do_v = v_reuse != nullptr;
+    pdl_trigger();  // the selection may launch; it waits for these scores
     if (mask_union) {  // the selection ORs both planes into it afterwards
         const int words = (n + 31) / 32;
         const int w0 = t_base / 32, w1 = min(words, (t_base + kScoreWarps * kScoreRowsPerWarp + 31) / 32);
@@ -405,6 +406,8 @@ select_f32_kernel(const float* __restrict__ d_k, const float* __restrict__ d_v, 
     const bool cached = n <= kSelSmemKeys;
     const long long u = blockIdx.x;
     const int plane = blockIdx.y;
+    pdl_wait();     // scores of the score kernel
+    pdl_trigger();  // the correction may launch; it waits for these probe sets
     const float* d = plane == 0 ? d_k : d_v;
     if (d == nullptr) return;
     const float* du = d + u * n;
@@ -433,9 +436,8 @@ cudaError_t launch_select_f32(const float* d_k, const float* d_v, int units, int
     cudaError_t e = cudaFuncSetAttribute(select_f32_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    select_f32_kernel<<<dim3(units, 2), kSelThreads, smem, s>>>(d_k, d_v, n, b, idx_k, idx_v, mask_k,
-                                                               mask_v, mask_union);
-    return cudaGetLastError();
+    return launch_chained(select_f32_kernel, dim3(units, 2), dim3(kSelThreads), smem, s, d_k, d_v, n, b,
+                          idx_k, idx_v, mask_k, mask_v, mask_union);
 }
 
 // =====================================================================================
@@ -572,6 +574,7 @@ mean_correct_kernel(McArgs args) {
     __syncthreads();
     if (tid == 0)  // the first tiles stream in while phase 1 runs
         for (; issued < min(kMcStages, total_tiles); ++issued) issue(issued);
+    pdl_wait();  // probe sets and weights of the selection kernel
 
     for (int grp = 0; grp < groups; ++grp) {
         const int a0 = grp * kAgentGroup;
@@ -794,8 +797,7 @@ cudaError_t launch_mean_correct(const McPlanes& pl, const kvfix_kv_desc& rd, con
                                          (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(kMcCluster, 2 * a.rp.layers, a.rp.chunks);
-    mean_correct_kernel<<<grid, kMcThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_chained(mean_correct_kernel, grid, dim3(kMcThreads), smem, s, a);
 }
 
 }  // namespace kvfix
