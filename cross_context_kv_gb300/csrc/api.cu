@@ -104,7 +104,7 @@ kvfix_status kvfix_check_status(void* stream) {
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "kvfix_check_status: stream synchronize");
-    unsigned bits = read_status_repair(s) | read_status_diff(s) | read_status_draft(s);
+    unsigned bits = read_status_repair(s) | read_status_diff(s) | read_status_draft(s) | read_status_lowrank(s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kvfix_check_status: status read");
     if (bits & 4u) return fail(KVFIX_ETIMEOUT, "a bounded device wait gave up");
@@ -253,7 +253,9 @@ kvfix_status kvfix_lowrank_apply(const kvfix_bf16* x, kvfix_kv_desc desc, const 
         return fail(KVFIX_EINVAL, "%s: x and out shapes differ", fn);
     if (!A || !B) return fail(KVFIX_EINVAL, "%s: A and B are required", fn);
     if (!aligned16(A) || !aligned16(B)) return fail(KVFIX_EINVAL, "%s: A and B must be 16-byte aligned", fn);
-    if (rank < 16 || rank > 64 || rank % 16) return fail(KVFIX_EINVAL, "%s: rank must be 16, 32, 48 or 64", fn);
+    if (rank != 16 && rank != 32 && rank != 64) return fail(KVFIX_EINVAL, "%s: rank must be 16, 32 or 64", fn);
+    if (desc.tokens > 0 && ((long long)desc.chunks * desc.layers * desc.kv_heads * desc.tokens >= (1ll << 31)))
+        return fail(KVFIX_EINVAL, "%s: at most 2^31 factor rows", fn);
     if (desc.head_dim != 64 && desc.head_dim != 128) return fail(KVFIX_EINVAL, "%s: head_dim must be 64 or 128", fn);
     const bool in_place = (const void*)x == (const void*)out && same_desc(desc, out_desc);
     if (!in_place && overlaps(x, desc, out, out_desc))

@@ -26,6 +26,7 @@ kvfix_status cuda_fail(cudaError_t err, const char* what);
 unsigned read_status_repair(cudaStream_t stream);
 unsigned read_status_diff(cudaStream_t stream);
 unsigned read_status_draft(cudaStream_t stream);
+unsigned read_status_lowrank(cudaStream_t stream);
 
 // ---- launchers (enqueue only; arguments already validated) -----------------------
 

@@ -487,10 +487,11 @@ struct McArgs {
 };
 
 struct McLayout {  // byte offsets into the dynamic shared memory
-    int ps, slice, ring, mu_all, cs, member, total, words_member;
+    int ps, slice, ring, mu_all, cs, member, wts, total, words_member;
 };
 
 __host__ __device__ inline int align128(int x) { return (x + 127) / 128 * 128; }
+__host__ __device__ inline bool mc_stage_weights(int ag, int rows_per_cta) { return ag * rows_per_cta <= 2048; }
 
 __host__ __device__ inline McLayout mc_layout(int HD, int half, int ag, int rows_per_cta, int tile_rows) {
     McLayout m;
@@ -501,7 +502,9 @@ __host__ __device__ inline McLayout mc_layout(int HD, int half, int ag, int rows
     m.cs = m.mu_all + 4 * ag * HD;
     m.member = m.cs + 4 * 2 * ag * half;
     m.words_member = (rows_per_cta + 31) / 32;
-    m.total = m.member + 4 * ag * m.words_member;
+    m.wts = m.member + 4 * ag * m.words_member;
+    // weights of this CTA's rows, per agent, when they fit in 8 KB
+    m.total = m.wts + (mc_stage_weights(ag, rows_per_cta) ? 4 * ag * rows_per_cta : 0);
     return m;
 }
 
@@ -543,6 +546,7 @@ mean_correct_kernel(McArgs args) {
     float* cos_t = reinterpret_cast<float*>(smem + lay.cs);           // [ag][4][D/8]
     float* sin_t = cos_t + ag_max * half;                             // [ag][4][D/8]
     uint32_t* member = reinterpret_cast<uint32_t*>(smem + lay.member);
+    float* wts = reinterpret_cast<float*>(smem + lay.wts);              // [ag][rows_per_cta]
     const bool rows_contig = rp.st == HD;
     const unsigned row_bytes = (unsigned)HD * 2u;
     const int groups = (args.agents + kAgentGroup - 1) / kAgentGroup;
@@ -654,11 +658,15 @@ mean_correct_kernel(McArgs args) {
             // residue-major elements [rank*SL, rank*SL + SL): 32 partials added in order
             for (int e = tid; e < SL; e += kMcThreads) {
                 const int ri = rank * SL + e;
-                float sum = 0.f;
+                float part[32];
+#pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     const float* rps = cluster.map_shared_rank(ps, q / kMcSlotsPerCta);
-                    sum += rps[(q % kMcSlotsPerCta) * HD + ri];
+                    part[q] = rps[(q % kMcSlotsPerCta) * HD + ri];
                 }
+                float sum = 0.f;
+#pragma unroll
+                for (int q = 0; q < 32; ++q) sum += part[q];
                 const float m = sum / (float)b;
                 mu_slice[e] = m;
                 mu_g[4 * (ri % G) + ri / G] = m;
@@ -679,6 +687,12 @@ mean_correct_kernel(McArgs args) {
                 const int j = idx[u * b + (i % b)];
                 if (j >= t_lo && j < t_hi)
                     atomicOr(&member[a * lay.words_member + ((j - t_lo) >> 5)], 1u << ((j - t_lo) & 31));
+            }
+            const int rows = mc_stage_weights(ag_max, args.rows_per_cta) ? t_hi - t_lo : 0;
+            for (int i = tid; i < ag * rows; i += kMcThreads) {
+                const int a = i / rows, t = i % rows;
+                const long long u = (long long)(a0 + a) * R + r;
+                wts[a * args.rows_per_cta + t] = wgt[u * n + t_lo + t];
             }
         }
         __syncthreads();
@@ -718,7 +732,8 @@ mean_correct_kernel(McArgs args) {
                     }
                     const long long u = (long long)(a0 + a) * R + r;
                     uint16_t* ob = out + op.row((int)u, l, 0) + eo;
-                    const float* wb = wgt + u * n;
+                    const bool staged = mc_stage_weights(ag_max, args.rows_per_cta);
+                    const float* wb = staged ? wts + a * args.rows_per_cta - t_lo : wgt + u * n;
                     const uint32_t* mem = member + a * lay.words_member;
                     for (int row = row_off; row < tt; row += rpp) {
                         const int t = t0 + row, tl = t - t_lo;
@@ -728,7 +743,7 @@ mean_correct_kernel(McArgs args) {
                         unpack4(*reinterpret_cast<const uint2*>(tb + row * HD + half), x1);
                         if (rot) rotate4(x0, x1, c, sn);
                         if (b > 0) {
-                            const float wt = __ldg(wb + t);
+                            const float wt = wb[t];
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
                                 x0[q] = fmaf(wt, m0[q], x0[q]);
@@ -793,6 +808,7 @@ cudaError_t launch_mean_correct(const McPlanes& pl, const kvfix_kv_desc& rd, con
     const int ag = agents < kAgentGroup ? agents : kAgentGroup;
     const McLayout lay = mc_layout(HD, a.rp.dim / 2, ag, a.rows_per_cta, a.tile_rows);
     const size_t smem = (size_t)lay.total;
+    if (smem > 220 * 1024) return cudaErrorInvalidValue;  // shape beyond the kernel's shared memory
     cudaError_t e = cudaFuncSetAttribute(mean_correct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;

@@ -184,9 +184,9 @@ KVFIX_API kvfix_status kvfix_mean_correct(const kvfix_bf16* k_reuse, const kvfix
  *          itself with the same descriptor (in place).
  * A      : device bf16[chunks][layers][kv_heads][tokens][rank], contiguous.
  * B      : device bf16[chunks][layers][kv_heads][rank][head_dim], contiguous.
- * rank   : a multiple of 16, at most 64.  head_dim must be 64 or 128.
- * Arithmetic: bf16 products on the tensor cores with float accumulation, then the add
- * in float and one rounding to bf16.
+ * rank   : 16, 32 or 64.  head_dim must be 64 or 128.
+ * Arithmetic: bf16 products on the tensor cores (tcgen05, accumulator in tensor memory)
+ * with float accumulation, then the add in float and one rounding to bf16.
  */
 KVFIX_API kvfix_status kvfix_lowrank_apply(const kvfix_bf16* x, kvfix_kv_desc desc, const kvfix_bf16* A,
                                            const kvfix_bf16* B, int32_t rank, kvfix_bf16* out,
