@@ -44,6 +44,27 @@ L2_FLUSH_BYTES = 512 << 20
 
 # ------------------------------------------------------------------ helpers
 
+def profiled_traffic(profile: str):
+    """dram read + write bytes per launch from a committed ncu summary, or None when the
+    kernel source has changed since that capture (hash mismatch)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", profile)
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and line.startswith("    "):
+                    k, v = line.strip().split(":", 1)
+                    fields[k.strip()] = v.strip()
+        src = os.path.join(ROOT, fields["kernel_source"])
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != fields["kernel_source_sha256"]:
+                return None
+        return int(fields["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -364,8 +385,10 @@ def stage_lowrank(kvfix, peak, steps=3, warmup=2):
     plane = C * L * n * H * D * 2
     lr_bytes = 2 * (2 * plane + C * L * H * n * r * 2 + C * L * H * r * D * 2)
     nl = L - cfg.layer_begin
-    ws_bytes = C * nl * H * 16 * n * 4
-    dr_bytes = (C * nl * n * H * D * 2) + 2 * ws_bytes + 2 * 2 * (C * L * cfg.k_rows * H * D * 2)
+    # scored keys read once; per-unit key masses written and read back; the repaired
+    # rows of both planes read from the fresh planes and written
+    contrib_bytes = C * nl * H * n * 4
+    dr_bytes = (C * nl * n * H * D * 2) + 2 * contrib_bytes + 2 * 2 * (C * L * cfg.k_rows * H * D * 2)
     lr, dr = statistics.mean(lr_ms), statistics.mean(dr_ms)
     flops = 2 * 2 * C * L * H * n * r * D + 2 * C * nl * H * 16 * n * D
     res = {"workload": "lowrank_70b: 4 chunks x 16384 tokens, 80 layers, 8 KV / 64 query heads x 128, rank 16, top 5% rows",
@@ -459,7 +482,8 @@ def run_ours(args, world, rank, local):
         "algorithmic_bytes_per_step": by["step"],
         "roofline": {"bound": "hbm", "kernel": "mean_correct_kernel (kvfix_mean_correct: probe means + correction, K and V, one launch)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic("mean_correct_kernel_repair_llama8b.md"),
                      "peak_kind": peak_kind + " (copy bandwidth)",
                      "launch_ms": round(mc, 5), "algorithmic_bytes_per_launch": by["mean_correct"]},
         "step_roofline_frac": round(by["step"] / ms / 1e6 / peak, 4),
@@ -509,6 +533,55 @@ def run_reference(args, world, rank):
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+PROFILE_CASES = {
+    # reduced workloads for profiler captures: inputs larger than L2, a few GB at most
+    "repair": lambda: synth.REPAIR_LLAMA8B.with_(layers=8),
+    "round": lambda: synth.ROUND_QWEN14B.with_(layers=8),
+    "diff": lambda: synth.SIBLINGS_8B.with_(layers=4),
+    "lowrank": lambda: synth.LOWRANK_70B.with_(chunks=1, layers=8),
+}
+
+
+def run_profile_case(name: str, iters: int = 3):
+    """A few launches of one stage on a reduced workload, for ncu (prints one JSON line)."""
+    from cross_context_kv_gb300 import kvfix
+    cfg = PROFILE_CASES[name]()
+    times = []
+    if name in ("repair", "round"):
+        reuse = synth.repair_reuse(cfg, "cuda")
+        fk, fv = compose_fresh_gpu(kvfix, cfg, reuse, range(cfg.units))
+        inp = {"k_reuse": reuse["k_reuse"], "v_reuse": reuse["v_reuse"], "delta": reuse["delta"],
+               "k_fresh": fk, "v_fresh": fv}
+        out = {"k": torch.empty_like(fk), "v": torch.empty_like(fv),
+               "mu_k": torch.empty(cfg.units, cfg.layers, cfg.kv_heads * cfg.head_dim, device="cuda"),
+               "mu_v": torch.empty(cfg.units, cfg.layers, cfg.kv_heads * cfg.head_dim, device="cuda")}
+        step = lambda: run_repair_step(kvfix, cfg, inp, out)  # noqa: E731
+    elif name == "diff":
+        inp = synth.diff_inputs(cfg, "cuda")
+        mask, offsets, payload, entries = kvfix.diff_encode(inp["master_k"], inp["master_v"], inp["sib_k"],
+                                                            inp["sib_v"], cfg.block_tokens)
+        def step():
+            m, o, pl, _ = kvfix.diff_encode(inp["master_k"], inp["master_v"], inp["sib_k"], inp["sib_v"],
+                                            cfg.block_tokens, capacity=payload.shape[0], sync=False)
+            kvfix.diff_gather(inp["master_k"], inp["master_v"], m, o, pl, cfg.siblings, cfg.block_tokens,
+                              payload_entries=entries)
+    else:
+        inp = synth.lowrank_inputs(cfg, "cuda")
+        kt = torch.empty_like(inp["x_k"])
+        def step():
+            kvfix.lowrank_apply(inp["x_k"], inp["a_k"], inp["b_k"], out=kt)
+            kvfix.draft_rank(kt, inp["q"], cfg.layer_begin, cfg.k_rows)
+    for _ in range(iters):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        step()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    kvfix.check_status()
+    print(json.dumps({"profile_case": name, "workload": repr(cfg), "ms": [round(t, 4) for t in times]}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -516,7 +589,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-stages", action="store_true")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
+                    help="run a few launches of one stage on a reduced workload (for ncu) and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case)
+        return
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -289,7 +289,9 @@ kvfix_status kvfix_draft_rank(const kvfix_bf16* k, kvfix_kv_desc desc, const kvf
     if ((q_heads / desc.kv_heads) * draft_steps > 16)
         return fail(KVFIX_EINVAL, "%s: (q_heads/kv_heads)*draft_steps must be <= 16", fn);
     if (layer_begin < 0 || layer_begin > desc.layers) return fail(KVFIX_EINVAL, "%s: layer_begin out of range", fn);
-    if (desc.tokens > 65536 || desc.chunks > 65535) return fail(KVFIX_EINVAL, "%s: tokens <= 65536, chunks <= 65535", fn);
+    if (desc.tokens > 16384 || desc.chunks > 65535) return fail(KVFIX_EINVAL, "%s: tokens <= 16384, chunks <= 65535", fn);
+    if ((long long)desc.chunks * (desc.layers - layer_begin) * desc.kv_heads > 65535)
+        return fail(KVFIX_EINVAL, "%s: at most 65535 (chunk, layer, head) units", fn);
     if (k_rows < 0 || k_rows > desc.tokens) return fail(KVFIX_EINVAL, "%s: k_rows must lie in [0, tokens]", fn);
     if (!scores || (k_rows > 0 && !idx)) return fail(KVFIX_EINVAL, "%s: scores and idx are required", fn);
     if (workspace_bytes < draft_workspace_bytes(desc, layer_begin) || (!workspace && workspace_bytes))

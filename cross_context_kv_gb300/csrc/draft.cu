@@ -20,7 +20,11 @@
 #include <math.h>
 #include <stdint.h>
 
-#include "common.cuh"
+#include <cooperative_groups.h>
+
+#include "tc.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace kvfix {
 
@@ -34,181 +38,271 @@ unsigned read_status_draft(cudaStream_t stream) {
     return h;
 }
 
-constexpr int kDrWarps = 8;
-constexpr int kDrTile = kDrWarps * 16;  // keys per CTA in the logits pass
-constexpr int kDrQ = 16;                // query rows per unit (padded)
+// One unit = (chunk, layer >= layer_begin, KV head): its G <= 16 query rows (draft steps
+// x query heads of the group) and its n keys.  A cluster of 8 CTAs takes a unit; CTA k
+// takes key tiles [k*tpc, (k+1)*tpc) of 128 keys:
+//   warp 0      TMA producer: key tiles (128 keys x D, two 64-column boxes, 128-byte
+//               swizzle) into a 3-stage ring;
+//   warp 1      tcgen05.mma M=128 (keys) x N=16 (queries) x K=D; the logits of tile t stay
+//               in tensor memory, columns [16t, 16t+16), so no logit goes to HBM;
+//   warps 2..5  softmax: per query, max and sum of exp over the CTA's keys (read back
+//               from TMEM), combined over the cluster through distributed shared memory
+//               in rank order; then each key's mass sum_q exp(z - max_q) / sum_q.
+// The per-key masses go to the workspace [unit][n]; a second kernel adds them over the
+// units of a chunk (layer-major, then head) in double and in a fixed order.
+constexpr int kDcCluster = 8;
+constexpr int kDcThreads = 192;
+constexpr int kDcStages = 3;
+constexpr int kDcRows = 128;   // keys per tile (MMA M)
+constexpr int kDcQ = 16;       // query rows per unit, padded (MMA N)
 
-struct DraftWs {
-    float* logits;   // [units][16][n]
-    float2* part;    // [units][tiles][16]  (max, sum exp) of a key tile
-    float2* stats;   // [units][16]         (max, 1 / sum exp)
-};
-
-static DraftWs carve(void* ws, long long units, int n) {
-    const long long tiles = (n + kDrTile - 1) / kDrTile;
-    char* p = static_cast<char*>(ws);
-    DraftWs w;
-    w.logits = reinterpret_cast<float*>(p);
-    p += ((sizeof(float) * units * kDrQ * n + 255) / 256) * 256;
-    w.part = reinterpret_cast<float2*>(p);
-    p += ((sizeof(float2) * units * tiles * kDrQ + 255) / 256) * 256;
-    w.stats = reinterpret_cast<float2*>(p);
-    return w;
+static long long dc_units(const kvfix_kv_desc& d, int layer_begin) {
+    const long long nl = d.layers > layer_begin ? d.layers - layer_begin : 0;
+    return (long long)d.chunks * nl * d.kv_heads;
 }
 
 size_t draft_workspace_bytes(const kvfix_kv_desc& d, int layer_begin) {
-    const long long nl = d.layers > layer_begin ? d.layers - layer_begin : 0;
-    const long long units = (long long)d.chunks * nl * d.kv_heads;
-    const long long n = d.tokens;
-    const long long tiles = (n + kDrTile - 1) / kDrTile;
-    size_t b = ((sizeof(float) * units * kDrQ * n + 255) / 256) * 256;
-    b += ((sizeof(float2) * units * tiles * kDrQ + 255) / 256) * 256;
-    b += ((sizeof(float2) * units * kDrQ + 255) / 256) * 256;
-    return b;
+    return ((sizeof(float) * (size_t)dc_units(d, layer_begin) * (size_t)d.tokens + 255) / 256) * 256;
 }
 
-__device__ __forceinline__ void mma_16816(float* d, const uint32_t* a, const uint32_t* b) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+// Tiles per CTA such that the CTA's logits fit the 512 TMEM columns.
+static int dc_tiles_per_cta(int n) {
+    const int tiles = (n + kDcRows - 1) / kDcRows;
+    return (tiles + kDcCluster - 1) / kDcCluster;
 }
 
-// ---- 1. logits: grid = (tiles, units) ------------------------------------------
+static int pow2_at_least(int x) {
+    int c = 32;
+    while (c < x) c <<= 1;
+    return c;
+}
+
+struct DcArgs {
+    const uint16_t* q;   // [C][L][steps][Hq][D]
+    float* contrib;      // [units][n]
+    int L, n, H, steps, q_heads, layer_begin, G, tpc, tmem_cols;
+};
+
+// Shared memory is padded to at least 80 KB so that at most two CTAs share an SM: each
+// holds up to 256 TMEM columns, and two never exceed the SM's 512 (an allocation that
+// had to wait for another cluster's CTA could otherwise deadlock the clusters).
 template <int D>
-__global__ void __launch_bounds__(kDrWarps * 32)
-draft_logits_kernel(const uint16_t* __restrict__ k, Plane p, const uint16_t* __restrict__ q,
-                    int steps, int q_heads, int layer_begin, int G, DraftWs ws) {
-    constexpr int kPitch = D + 8;
-    constexpr int kV = D / 8;
-    __shared__ __align__(16) uint16_t qs[kDrQ * kPitch];
-    __shared__ __align__(16) uint16_t ks[kDrWarps][16 * kPitch];
-    __shared__ float2 red[kDrWarps][kDrQ];
+struct DcCfg {
+    static constexpr int kTile = kDcRows * D * 2;
+    static constexpr int kQBytes = kDcQ * D * 2;
+    static constexpr int kNeed = 1024 + kDcStages * kTile + kQBytes;
+    static constexpr int kSmem = kNeed > 80 * 1024 ? kNeed : 80 * 1024;
+};
+
+template <int D>
+__global__ void __cluster_dims__(kDcCluster, 1, 1) __launch_bounds__(kDcThreads, 1)
+draft_cluster_kernel(const __grid_constant__ CUtensorMap tm_k, DcArgs args) {
+    using C = DcCfg<D>;
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t full[kDcStages], empty[kDcStages], done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    __shared__ float red_m[4][kDcQ], red_s[4][kDcQ];
+    __shared__ float cta_m[kDcQ], cta_s[kDcQ], fin_m[kDcQ], fin_inv[kDcQ];
+    cg::cluster_group cluster = cg::this_cluster();
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* qsm = smem + kDcStages * C::kTile;  // Q, K-major canonical, no swizzle
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, qd = lane & 3;
-    const int n = p.tokens, H = p.heads;
-    const int nl = p.layers - layer_begin;
+    const int rank = (int)cluster.block_rank();
     const long long unit = blockIdx.y;
-    const int kvh = (int)(unit % H);
-    const int l = layer_begin + (int)((unit / H) % nl);
-    const int c = (int)(unit / ((long long)H * nl));
-    const int group = q_heads / H;
-    // queries of this unit: row i = t*group + m  <->  q[c][l][t][kvh*group + m]
-    for (int i = threadIdx.x; i < kDrQ * kV; i += blockDim.x) {
-        int row = i / kV, v = i % kV;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (row < G) {
-            int t = row / group, m = row % group;
-            const uint16_t* src = q + ((((long long)c * p.layers + l) * steps + t) * q_heads + kvh * group + m) * D;
-            val = *reinterpret_cast<const uint4*>(src + 8 * v);
+    const int nl = args.L - args.layer_begin;
+    const int kvh = (int)(unit % args.H);
+    const int l = args.layer_begin + (int)((unit / args.H) % nl);
+    const int c = (int)(unit / ((long long)args.H * nl));
+    const int n = args.n;
+    const int tiles = (n + kDcRows - 1) / kDcRows;
+    const int tile0 = rank * args.tpc;
+    const int ntiles = max(0, min(args.tpc, tiles - tile0));
+    const int group = args.q_heads / args.H;
+
+    // Q rows i = t*group + m  <->  q[c][l][t][kvh*group + m], zero-padded to 16 rows;
+    // element (i, e) at (i%8)*16 + (i/8)*SBO + (e/8)*128 + (e%8)*2 with SBO = (D/8)*128.
+    for (int idx = threadIdx.x; idx < kDcQ * D; idx += kDcThreads) {
+        const int i = idx / D, e = idx % D;
+        uint16_t v = 0;
+        if (i < args.G) {
+            const int t = i / group, m = i % group;
+            v = args.q[((((long long)c * args.L + l) * args.steps + t) * args.q_heads + kvh * group + m) * D + e];
         }
-        *reinterpret_cast<uint4*>(qs + row * kPitch + 8 * v) = val;
+        *reinterpret_cast<uint16_t*>(qsm + (i % 8) * 16 + (i / 8) * (D / 8) * 128 + (e / 8) * 128 + (e % 8) * 2) = v;
     }
-    const int j0 = blockIdx.x * kDrTile + warp * 16;
-    uint16_t* kw = ks[warp];
-    for (int i = lane; i < 16 * kV; i += 32) {
-        int rr = i / kV, v = i % kV;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (j0 + rr < n)
-            val = ld_stream(reinterpret_cast<const uint4*>(k + p.row(c, l, j0 + rr) + (long long)kvh * D + 8 * v));
-        *reinterpret_cast<uint4*>(kw + rr * kPitch + 8 * v) = val;
+    fence_proxy_async_smem();
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kDcStages; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], 1);
+        }
+        mbar_init(&done, 1);
+        fence_mbar_init();
+        abort_flag = 0;
+        prefetch_tensormap(&tm_k);
     }
+    if (warp == 1) {
+        tmem_alloc(&tmem_slot, (uint32_t)args.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
     __syncthreads();
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-    for (int k0 = 0; k0 < D; k0 += 16) {
-        uint32_t a[4];
-        a[0] = *reinterpret_cast<const uint32_t*>(kw + g * kPitch + k0 + 2 * qd);
-        a[1] = *reinterpret_cast<const uint32_t*>(kw + (g + 8) * kPitch + k0 + 2 * qd);
-        a[2] = *reinterpret_cast<const uint32_t*>(kw + g * kPitch + k0 + 8 + 2 * qd);
-        a[3] = *reinterpret_cast<const uint32_t*>(kw + (g + 8) * kPitch + k0 + 8 + 2 * qd);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            uint32_t b[2];
-            const uint16_t* qrow = qs + (t * 8 + g) * kPitch + k0 + 2 * qd;
-            b[0] = *reinterpret_cast<const uint32_t*>(qrow);
-            b[1] = *reinterpret_cast<const uint32_t*>(qrow + 8);
-            mma_16816(acc[t], a, b);
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int i = 0; i < ntiles; ++i) {
+                const int st = i % kDcStages;
+                if (i >= kDcStages && !mbar_wait(&empty[st], (unsigned)(i / kDcStages - 1) & 1u)) {
+                    atomicOr(&abort_flag, 1);
+                    break;
+                }
+                unsigned char* dst = smem + st * C::kTile;
+                mbar_arrive_expect_tx(&full[st], C::kTile);
+                for (int half = 0; half < D / 64; ++half)
+                    tma_load_4d(dst + half * (kDcRows * 128), &tm_k, kvh * D + 64 * half, (tile0 + i) * kDcRows, l,
+                                c, &full[st]);
+            }
         }
-    }
-    const float scale = rsqrtf((float)D);
-    // acc[t][0,1]: key j0+g, queries t*8+2qd, +1; acc[t][2,3]: key j0+g+8.
-    const int ja = j0 + g, jb = j0 + g + 8;
-    float* lg = ws.logits + unit * kDrQ * (long long)n;
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc_idesc_bf16(kDcRows, kDcQ);
+            bool ok = true;
+            for (int i = 0; i < ntiles; ++i) {
+                const int st = i % kDcStages;
+                if (!mbar_wait(&full[st], (unsigned)(i / kDcStages) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const unsigned char* kt = smem + st * C::kTile;
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int qi = t * 8 + 2 * qd + e;
-            float za = acc[t][e] * scale, zb = acc[t][2 + e] * scale;
-            if (ja < n) lg[(long long)qi * n + ja] = za;
-            if (jb < n) lg[(long long)qi * n + jb] = zb;
-            // tile partial: max and sum exp over this warp's 16 keys (lanes sharing qd)
-            float m = fmaxf(ja < n ? za : -INFINITY, jb < n ? zb : -INFINITY);
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            float s = (ja < n ? expf(za - m) : 0.f) + (jb < n ? expf(zb - m) : 0.f);
-            if (m == -INFINITY) s = 0.f;
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (g == 0) red[warp][qi] = make_float2(m, s);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t adesc = tc_smem_desc(kt + (kk / 4) * (kDcRows * 128) + 32 * (kk % 4), 16, 1024, 2);
+                    const uint64_t bdesc = tc_smem_desc(qsm + 256 * kk, 128, (D / 8) * 128, 0);
+                    tc_mma_bf16(tmem + kDcQ * i, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(&empty[st]);  // the stage is free once these MMAs have read it
+            }
+            if (!ok) atomicOr(&abort_flag, 1);
+            tc_commit(&done);  // every logit of this CTA is in TMEM
         }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int wq = warp & 3, ew = warp - 2;
+        const int key_in_tile = 32 * wq + lane;
+        const float scale = rsqrtf((float)D);
+        const bool ok = mbar_wait(&done, 0u);
+        if (!ok) atomicOr(&abort_flag, 1);
+        tc_fence_after();
+        const int G = args.G;
+        float mx[kDcQ];
+#pragma unroll
+        for (int q = 0; q < kDcQ; ++q) mx[q] = -INFINITY;
+        for (int i = 0; i < ntiles && ok; ++i) {
+            const int key = (tile0 + i) * kDcRows + key_in_tile;
+            uint32_t v[16];
+            tmem_ld16(tmem + ((uint32_t)(32 * wq) << 16) + kDcQ * i, v);
+            tmem_wait_ld();
+            if (key < n) {
+#pragma unroll
+                for (int q = 0; q < kDcQ; ++q) mx[q] = fmaxf(mx[q], __uint_as_float(v[q]) * scale);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kDcQ; ++q) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], o));
+        }
+        if (lane == 0)
+#pragma unroll
+            for (int q = 0; q < kDcQ; ++q) red_m[ew][q] = mx[q];
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (threadIdx.x - 64 < kDcQ) {
+            const int q = threadIdx.x - 64;
+            cta_m[q] = fmaxf(fmaxf(red_m[0][q], red_m[1][q]), fmaxf(red_m[2][q], red_m[3][q]));
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        float sm[kDcQ];
+#pragma unroll
+        for (int q = 0; q < kDcQ; ++q) sm[q] = 0.f;
+        for (int i = 0; i < ntiles && ok; ++i) {
+            const int key = (tile0 + i) * kDcRows + key_in_tile;
+            uint32_t v[16];
+            tmem_ld16(tmem + ((uint32_t)(32 * wq) << 16) + kDcQ * i, v);
+            tmem_wait_ld();
+            if (key < n) {
+#pragma unroll
+                for (int q = 0; q < kDcQ; ++q) sm[q] += expf(__uint_as_float(v[q]) * scale - cta_m[q]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kDcQ; ++q) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sm[q] += __shfl_xor_sync(0xffffffffu, sm[q], o);
+        }
+        if (lane == 0)
+#pragma unroll
+            for (int q = 0; q < kDcQ; ++q) red_s[ew][q] = sm[q];
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (threadIdx.x - 64 < kDcQ) {
+            const int q = threadIdx.x - 64;
+            cta_s[q] = ((red_s[0][q] + red_s[1][q]) + red_s[2][q]) + red_s[3][q];
+        }
+        (void)G;
     }
-    __syncthreads();
-    if (threadIdx.x < kDrQ) {
-        const int qi = threadIdx.x;
+    // ---------------- cluster: combine the 8 CTAs' (max, sum) in rank order
+    cluster.sync();
+    if (threadIdx.x < kDcQ) {
+        const int q = threadIdx.x;
         float m = -INFINITY;
-        for (int w = 0; w < kDrWarps; ++w) m = fmaxf(m, red[w][qi].x);
-        float s = 0.f;
-        if (m != -INFINITY)
-            for (int w = 0; w < kDrWarps; ++w)
-                if (red[w][qi].x != -INFINITY) s += red[w][qi].y * expf(red[w][qi].x - m);
-        ws.part[(unit * gridDim.x + blockIdx.x) * kDrQ + qi] = make_float2(m, s);
+        for (int k = 0; k < kDcCluster; ++k) m = fmaxf(m, cluster.map_shared_rank(cta_m, k)[q]);
+        float ssum = 0.f;
+        for (int k = 0; k < kDcCluster; ++k) {
+            const float mk = cluster.map_shared_rank(cta_m, k)[q];
+            const float sk = cluster.map_shared_rank(cta_s, k)[q];
+            if (mk != -INFINITY) ssum += sk * expf(mk - m);
+        }
+        fin_m[q] = m;
+        fin_inv[q] = ssum > 0.f ? 1.0f / ssum : 0.f;
     }
+    cluster.sync();  // also: no CTA leaves while others still read its shared memory
+    if (warp >= 2) {
+        const int wq = warp & 3;
+        const int key_in_tile = 32 * wq + lane;
+        const float scale = rsqrtf((float)D);
+        float* out = args.contrib + unit * (long long)n;
+        for (int i = 0; i < ntiles && !abort_flag; ++i) {
+            const int key = (tile0 + i) * kDcRows + key_in_tile;
+            uint32_t v[16];
+            tmem_ld16(tmem + ((uint32_t)(32 * wq) << 16) + kDcQ * i, v);
+            tmem_wait_ld();
+            float acc = 0.f;
+            for (int q = 0; q < args.G; ++q) acc += expf(__uint_as_float(v[q]) * scale - fin_m[q]) * fin_inv[q];
+            if (key < n) out[key] = acc;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (abort_flag && threadIdx.x == 0) atomicOr(&g_status_draft, FLAG_TIMEOUT);
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, (uint32_t)args.tmem_cols);
 }
 
-// ---- 2. stats: grid = units, 16 threads x ... ------------------------------------
-__global__ void draft_stats_kernel(DraftWs ws, int tiles) {
-    const long long unit = blockIdx.x;
-    const int qi = threadIdx.x;
-    if (qi >= kDrQ) return;
-    float m = -INFINITY;
-    for (int t = 0; t < tiles; ++t) m = fmaxf(m, ws.part[(unit * tiles + t) * kDrQ + qi].x);
-    float s = 0.f;
-    for (int t = 0; t < tiles; ++t) {
-        float2 pt = ws.part[(unit * tiles + t) * kDrQ + qi];
-        if (pt.x != -INFINITY) s += pt.y * expf(pt.x - m);
-    }
-    ws.stats[unit * kDrQ + qi] = make_float2(m, s > 0.f ? 1.0f / s : 0.f);
-}
-
-// ---- 3. accumulate: grid = (ceil(n/256), chunks) -----------------------------------
+// ---- sum of the per-unit masses: grid = (ceil(n/256), chunks) ----------------------------
 constexpr int kAccThreads = 256;
 
 __global__ void __launch_bounds__(kAccThreads)
-draft_accum_kernel(DraftWs ws, int n, long long units_per_chunk, int G, double* scores) {
-    __shared__ float2 st[64][kDrQ];
+draft_accum_kernel(const float* __restrict__ contrib, int n, long long units_per_chunk, double* scores) {
     const int c = blockIdx.y;
     const int j = blockIdx.x * kAccThreads + threadIdx.x;
+    if (j >= n) return;
+    const float* p = contrib + (long long)c * units_per_chunk * n + j;
     double acc = 0.0;
-    for (long long u0 = 0; u0 < units_per_chunk; u0 += 64) {
-        const int nu = (int)min(64ll, units_per_chunk - u0);
-        __syncthreads();
-        for (int i = threadIdx.x; i < nu * kDrQ; i += blockDim.x)
-            st[i / kDrQ][i % kDrQ] = ws.stats[((long long)c * units_per_chunk + u0 + i / kDrQ) * kDrQ + i % kDrQ];
-        __syncthreads();
-        if (j < n) {
-            for (int uu = 0; uu < nu; ++uu) {
-                const long long unit = (long long)c * units_per_chunk + u0 + uu;
-                const float* lg = ws.logits + unit * kDrQ * (long long)n + j;
-                float f = 0.f;
-                for (int qi = 0; qi < G; ++qi) f += expf(lg[(long long)qi * n] - st[uu][qi].x) * st[uu][qi].y;
-                acc += (double)f;
-            }
-        }
-    }
-    if (j < n) scores[(long long)c * n + j] = acc;
+    for (long long u = 0; u < units_per_chunk; ++u) acc += (double)__ldg(p + u * n);
+    scores[(long long)c * n + j] = acc;
 }
 
 // ---- 4. select (double keys) --------------------------------------------------------
@@ -343,6 +437,23 @@ select_f64_kernel(const double* __restrict__ scores, int n, int kk, int32_t* idx
         if ((bits[i >> 5] >> (i & 31) & 1u) && ob < kk) out[ob++] = i;
 }
 
+static cudaError_t encode_keys(CUtensorMap* map, const uint16_t* base, const Plane& p) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const long long row = (long long)p.heads * p.dim;
+    cuuint64_t dims[4] = {(cuuint64_t)row, (cuuint64_t)p.tokens, (cuuint64_t)p.layers, (cuuint64_t)p.chunks};
+    long long st = p.tokens > 1 ? p.st : row;
+    long long sl = p.layers > 1 ? p.sl : st * p.tokens;
+    long long sc = p.chunks > 1 ? p.sc : sl * p.layers;
+    cuuint64_t strides[3] = {(cuuint64_t)(2 * st), (cuuint64_t)(2 * sl), (cuuint64_t)(2 * sc)};
+    cuuint32_t box[4] = {64, (cuuint32_t)kDcRows, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(base), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_draft(const uint16_t* k, const kvfix_kv_desc& d, const uint16_t* q, int steps,
                          int q_heads, int layer_begin, int k_rows, int32_t* idx, double* scores,
                          void* ws_ptr, cudaStream_t s) {
@@ -351,26 +462,43 @@ cudaError_t launch_draft(const uint16_t* k, const kvfix_kv_desc& d, const uint16
     const int nl = p.layers - layer_begin;
     const long long units_per_chunk = (long long)nl * p.heads;
     const long long units = units_per_chunk * p.chunks;
-    const int G = steps * (q_heads / p.heads);
     cudaError_t e;
     if (p.chunks == 0 || n == 0) return cudaSuccess;
     if (units == 0) {
         e = cudaMemsetAsync(scores, 0, sizeof(double) * (size_t)p.chunks * n, s);
         if (e != cudaSuccess) return e;
     } else {
-        DraftWs ws = carve(ws_ptr, units, n);
-        const int tiles = (n + kDrTile - 1) / kDrTile;
         if (units > 65535) return cudaErrorInvalidValue;
-        dim3 g1(tiles, (unsigned)units);
-        if (p.dim == 128)
-            draft_logits_kernel<128><<<g1, kDrWarps * 32, 0, s>>>(k, p, q, steps, q_heads, layer_begin, G, ws);
-        else
-            draft_logits_kernel<64><<<g1, kDrWarps * 32, 0, s>>>(k, p, q, steps, q_heads, layer_begin, G, ws);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        draft_stats_kernel<<<(unsigned)units, 32, 0, s>>>(ws, tiles);
+        CUtensorMap tk;
+        if ((e = encode_keys(&tk, k, p)) != cudaSuccess) return e;
+        DcArgs a;
+        a.q = q;
+        a.contrib = static_cast<float*>(ws_ptr);
+        a.L = p.layers;
+        a.n = n;
+        a.H = p.heads;
+        a.steps = steps;
+        a.q_heads = q_heads;
+        a.layer_begin = layer_begin;
+        a.G = steps * (q_heads / p.heads);
+        a.tpc = dc_tiles_per_cta(n);
+        a.tmem_cols = pow2_at_least(kDcQ * a.tpc);
+        if (a.tmem_cols > 256) return cudaErrorInvalidValue;  // n <= 16384
+        dim3 grid(kDcCluster, (unsigned)units);
+        if (p.dim == 128) {
+            e = cudaFuncSetAttribute(draft_cluster_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     DcCfg<128>::kSmem);
+            if (e != cudaSuccess) return e;
+            draft_cluster_kernel<128><<<grid, kDcThreads, DcCfg<128>::kSmem, s>>>(tk, a);
+        } else {
+            e = cudaFuncSetAttribute(draft_cluster_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     DcCfg<64>::kSmem);
+            if (e != cudaSuccess) return e;
+            draft_cluster_kernel<64><<<grid, kDcThreads, DcCfg<64>::kSmem, s>>>(tk, a);
+        }
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         dim3 g3((n + kAccThreads - 1) / kAccThreads, p.chunks);
-        draft_accum_kernel<<<g3, kAccThreads, 0, s>>>(ws, n, units_per_chunk, G, scores);
+        draft_accum_kernel<<<g3, kAccThreads, 0, s>>>(a.contrib, n, units_per_chunk, scores);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (k_rows > 0) {

@@ -214,7 +214,11 @@ KVFIX_API kvfix_status kvfix_lowrank_apply(const kvfix_bf16* x, kvfix_kv_desc de
  * workspace      : device buffer of kvfix_draft_rank_workspace_bytes(desc, layer_begin)
  *                  bytes (16-byte aligned), contents irrelevant on entry.
  * Limits: q_heads a multiple of kv_heads, q_heads/kv_heads * draft_steps <= 16,
- * head_dim 64 or 128, tokens <= 65536, 0 <= k_rows <= tokens.
+ * head_dim 64 or 128, tokens <= 16384 per chunk, chunks * (layers - layer_begin) *
+ * kv_heads <= 65535, 0 <= k_rows <= tokens.
+ * Arithmetic: the logits are a bf16 tensor-core contraction (tcgen05) with float
+ * accumulation kept in tensor memory; softmax statistics in float; per-unit masses in
+ * float, summed over units in double.
  */
 KVFIX_API size_t kvfix_draft_rank_workspace_bytes(kvfix_kv_desc desc, int32_t layer_begin);
 KVFIX_API kvfix_status kvfix_draft_rank(const kvfix_bf16* k, kvfix_kv_desc desc, const kvfix_bf16* q,

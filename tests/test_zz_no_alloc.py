@@ -54,11 +54,19 @@ def test_noalloc_matches_draft_rank_on_consecutive_calls():
 
 
 def test_noalloc_rejects_problems_beyond_the_buffer():
+    """A problem whose scratch exceeds the fixed buffer is refused before anything is
+    read or launched, so the descriptor may describe more rows than the buffers hold."""
     from cross_context_kv_gb300 import kvfix
-    cfg = synth.LOWRANK_70B.with_(chunks=1, layers=3, tokens=65536, kv_heads=8, q_heads=64)
-    k = torch.zeros((1, 3, 65536, 8, 128), dtype=torch.bfloat16, device=DEV)
-    q = torch.zeros((1, 3, 2, 64, 128), dtype=torch.bfloat16, device=DEV)
-    assert kvfix.draft_rank_workspace_bytes(k, 1) > (64 << 20)
-    st, _, _ = _noalloc(kvfix, k, q, 1, 10)
+    C, L, n, H, D = 2, 81, 16384, 8, 128
+    row = H * D
+    big = kvfix.KvDesc(C, L, n, H, D, L * n * row, n * row, row)
+    assert kvfix.lib.kvfix_draft_rank_workspace_bytes(big, 1) > (64 << 20)
+    k = torch.zeros(64, dtype=torch.bfloat16, device=DEV)
+    q = torch.zeros(64, dtype=torch.bfloat16, device=DEV)
+    idx = torch.zeros(16, dtype=torch.int32, device=DEV)
+    scores = torch.zeros(16, dtype=torch.float64, device=DEV)
+    p = kvfix._ptr
+    st = kvfix.lib.kvfix_draft_rank_noalloc(p(k), big, p(q), 2, 64, 1, 10, p(idx), p(scores), None, None, big,
+                                            None, None, kvfix._stream(k))
     assert st == kvfix.EINVAL
     assert b"fixed buffer" in kvfix.lib.kvfix_last_error()
