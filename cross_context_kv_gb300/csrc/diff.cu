@@ -6,9 +6,10 @@
 // shared by K and V); section 4.4, Algorithm 1 (restore = master block, overwritten
 // where the diff touches it).
 //
-// An entry i = (s*L + l)*nblk + blk is bt token rows x all heads x both planes.  The
-// master block is held in registers and compared with / written for every sibling, so
-// the master is read once per call.
+// An entry i = (s*L + l)*nblk + blk is bt token rows x all heads x both planes.  Encode
+// compares each master block (staged in shared memory by TMA) with every sibling's block
+// streaming through a TMA ring; gather holds the master block in registers and writes
+// it (or the payload block) for every sibling.  Either way the master is read once.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -48,44 +49,126 @@ __device__ __forceinline__ bool vec_ne(const uint4& a, const uint4& b) {
     return ((a.x ^ b.x) | (a.y ^ b.y) | (a.z ^ b.z) | (a.w ^ b.w)) != 0u;
 }
 
-// grid = (nblk, L).  Sets mask bits of dirty entries (mask pre-zeroed).
-__global__ void __launch_bounds__(kDiffThreads)
-diff_mask_kernel(const uint16_t* __restrict__ mk, const uint16_t* __restrict__ mv, Plane mp,
-                 const uint16_t* __restrict__ sk, const uint16_t* __restrict__ sv, Plane sp,
-                 int bt, uint32_t* mask) {
+// grid = (nblk, L), one CTA per (layer, block).  Sets the mask bits of dirty entries
+// (mask pre-zeroed).  The block is cut into "pieces" (a run of rows of one plane, at most
+// 32 KB).  The master's piece is bulk-copied (TMA) into one of two master buffers and
+// compared with the same piece of every sibling, which stream through a 3-stage ring of
+// bulk copies; a sibling's entry is dirty if any piece differs.  The master is read once.
+constexpr int kDmThreads = 512;
+constexpr int kDmStages = 3;
+constexpr int kDmPieceBytes = 32768;
+
+struct DmArgs {
+    const uint16_t* mk;
+    const uint16_t* mv;
+    const uint16_t* sk;
+    const uint16_t* sv;
+    Plane mp, sp;
+    int bt, piece_rows, pieces_per_plane;
+    uint32_t* mask;
+};
+
+__global__ void __launch_bounds__(kDmThreads, 1) diff_mask_kernel(DmArgs a) {
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __shared__ __align__(8) uint64_t mfull[2], full[kDmStages];
+    __shared__ int abort_flag;
     const int blk = blockIdx.x, l = blockIdx.y;
-    const int nblk = mp.tokens / bt;
-    BlockMap bm{bt, mp.heads * mp.dim / 8, (long long)bt * (mp.heads * mp.dim / 8)};
-    const long long total = 2 * bm.vecs_per_plane;
-    const int S = sp.chunks, L = mp.layers;
-    for (long long q0 = 0; q0 < total; q0 += kDiffPass) {
-        uint4 m[kDiffVec];
-        int pl[kDiffVec];
-        long long off[kDiffVec];
-#pragma unroll
-        for (int k = 0; k < kDiffVec; ++k) {
-            long long q = q0 + (long long)k * kDiffThreads + threadIdx.x;
-            pl[k] = -1;
-            if (q < total) {
-                long long o;
-                bm.locate(q, mp, 0, l, blk * bt, &pl[k], &o);
-                m[k] = *reinterpret_cast<const uint4*>((pl[k] ? mv : mk) + o);
-                bm.locate(q, sp, 0, l, blk * bt, &pl[k], &off[k]);  // sibling offset, chunk 0
-            }
+    const int S = a.sp.chunks, L = a.mp.layers, nblk = a.mp.tokens / a.bt;
+    const int HD = a.mp.heads * a.mp.dim;
+    const unsigned row_bytes = (unsigned)HD * 2u;
+    const int P = 2 * a.pieces_per_plane;  // pieces per block (K pieces, then V pieces)
+    const int units = P * S;               // (piece, sibling) pairs, piece-major
+    unsigned char* mbuf = dsm;                                 // [2][kDmPieceBytes]
+    unsigned char* ring = dsm + 2 * kDmPieceBytes;             // [kDmStages][kDmPieceBytes]
+    uint32_t* flags = reinterpret_cast<uint32_t*>(ring + kDmStages * kDmPieceBytes);  // [ceil(S/32)]
+    const int tid = threadIdx.x;
+    const bool contig_m = a.mp.st == HD, contig_s = a.sp.st == HD;
+
+    // piece p: plane p / pieces_per_plane, rows [r0, r0 + rows) of the block
+    auto piece_rows = [&](int p, int* r0) {
+        const int q = p % a.pieces_per_plane;
+        *r0 = q * a.piece_rows;
+        return min(a.piece_rows, a.bt - *r0);
+    };
+    auto copy_rows = [&](unsigned char* dst, const uint16_t* base, const Plane& pl, int chunk, int t0, int rows,
+                         bool contig, uint64_t* bar) {
+        if (contig) {
+            bulk_g2s(dst, base + pl.row(chunk, l, t0), row_bytes * rows, bar);
+        } else {
+            for (int q = 0; q < rows; ++q) bulk_g2s(dst + q * row_bytes, base + pl.row(chunk, l, t0 + q), row_bytes, bar);
         }
-        for (int s = 0; s < S; ++s) {
-            bool ne = false;
-#pragma unroll
-            for (int k = 0; k < kDiffVec; ++k) {
-                if (pl[k] < 0) continue;
-                const uint16_t* base = (pl[k] ? sv : sk) + (long long)s * sp.sc;
-                uint4 x = ld_stream(reinterpret_cast<const uint4*>(base + off[k]));
-                ne |= vec_ne(x, m[k]);
-            }
-            if (__syncthreads_or(ne) && threadIdx.x == 0) {
-                const long long i = ((long long)s * L + l) * nblk + blk;
-                atomicOr(&mask[i >> 5], 1u << (i & 31));
-            }
+    };
+    auto issue_master = [&](int p) {
+        int r0;
+        const int rows = piece_rows(p, &r0);
+        const bool vpl = p >= a.pieces_per_plane;
+        mbar_arrive_expect_tx(&mfull[p & 1], row_bytes * rows);
+        copy_rows(mbuf + (p & 1) * kDmPieceBytes, vpl ? a.mv : a.mk, a.mp, 0, blk * a.bt + r0, rows, contig_m,
+                  &mfull[p & 1]);
+    };
+    auto issue_unit = [&](int u) {
+        const int p = u / S, s = u % S;
+        int r0;
+        const int rows = piece_rows(p, &r0);
+        const bool vpl = p >= a.pieces_per_plane;
+        const int slot = u % kDmStages;
+        mbar_arrive_expect_tx(&full[slot], row_bytes * rows);
+        copy_rows(ring + slot * kDmPieceBytes, vpl ? a.sv : a.sk, a.sp, s, blk * a.bt + r0, rows, contig_s,
+                  &full[slot]);
+    };
+
+    for (int i = tid; i < (S + 31) / 32; i += kDmThreads) flags[i] = 0u;
+    if (tid == 0) {
+        mbar_init(&mfull[0], 1);
+        mbar_init(&mfull[1], 1);
+        for (int q = 0; q < kDmStages; ++q) mbar_init(&full[q], 1);
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        issue_master(0);
+        if (P > 1) issue_master(1);
+        for (int u = 0; u < min(kDmStages, units); ++u) issue_unit(u);
+    }
+    for (int u = 0; u < units; ++u) {
+        const int p = u / S, s = u % S;
+        int r0;
+        const int rows = piece_rows(p, &r0);
+        bool ok = true;
+        if (s == 0) ok = mbar_wait(&mfull[p & 1], (unsigned)(p >> 1) & 1u);
+        ok = ok && mbar_wait(&full[u % kDmStages], (unsigned)(u / kDmStages) & 1u);
+        if (!__syncthreads_and(ok)) {
+            if (tid == 0) abort_flag = 1;
+            break;
+        }
+        const uint4* m4 = reinterpret_cast<const uint4*>(mbuf + (p & 1) * kDmPieceBytes);
+        const uint4* s4 = reinterpret_cast<const uint4*>(ring + (u % kDmStages) * kDmPieceBytes);
+        const int vecs = rows * (int)(row_bytes / 16);
+        bool ne = false;
+        for (int v = tid; v < vecs; v += kDmThreads) ne |= vec_ne(m4[v], s4[v]);
+        if (__syncthreads_or(ne) && tid == 0) flags[s >> 5] |= 1u << (s & 31);
+        if (tid == 0) {  // every thread has passed the barrier: the stage (and, after the
+                         // last sibling of a piece, that piece's master buffer) may refill
+            fence_proxy_async_smem();
+            if (u + kDmStages < units) issue_unit(u + kDmStages);
+            if (s == S - 1 && p + 2 < P) issue_master(p + 2);
+        }
+    }
+    __syncthreads();
+    if (abort_flag) {
+        if (tid == 0) {
+            atomicOr(&g_status_diff, FLAG_TIMEOUT);
+            for (int q = 0; q < 2; ++q) mbar_wait(&mfull[q], 0u), mbar_wait(&mfull[q], 1u);
+            for (int q = 0; q < kDmStages; ++q) mbar_wait(&full[q], 0u), mbar_wait(&full[q], 1u);
+        }
+        __syncthreads();
+        return;
+    }
+    for (int s = tid; s < S; s += kDmThreads) {
+        if (flags[s >> 5] >> (s & 31) & 1u) {
+            const long long i = ((long long)s * L + l) * nblk + blk;
+            atomicOr(&a.mask[i >> 5], 1u << (i & 31));
         }
     }
 }
@@ -93,10 +176,25 @@ diff_mask_kernel(const uint16_t* __restrict__ mk, const uint16_t* __restrict__ m
 cudaError_t launch_diff_mask(const uint16_t* mk, const uint16_t* mv, const kvfix_kv_desc& md,
                              const uint16_t* sk, const uint16_t* sv, const kvfix_kv_desc& sd,
                              int bt, uint32_t* mask, cudaStream_t s) {
-    Plane mp = plane_of(md), sp = plane_of(sd);
-    if (mp.layers == 0 || mp.tokens == 0 || sp.chunks == 0) return cudaSuccess;
-    dim3 grid(mp.tokens / bt, mp.layers);
-    diff_mask_kernel<<<grid, kDiffThreads, 0, s>>>(mk, mv, mp, sk, sv, sp, bt, mask);
+    DmArgs a;
+    a.mk = mk;
+    a.mv = mv;
+    a.sk = sk;
+    a.sv = sv;
+    a.mp = plane_of(md);
+    a.sp = plane_of(sd);
+    a.bt = bt;
+    a.mask = mask;
+    if (a.mp.layers == 0 || a.mp.tokens == 0 || a.sp.chunks == 0) return cudaSuccess;
+    const int row_bytes = 2 * a.mp.heads * a.mp.dim;
+    a.piece_rows = kDmPieceBytes / row_bytes < bt ? kDmPieceBytes / row_bytes : bt;
+    if (a.piece_rows < 1) return cudaErrorInvalidValue;  // a token row above 32 KB
+    a.pieces_per_plane = (bt + a.piece_rows - 1) / a.piece_rows;
+    const size_t smem = (size_t)(2 + kDmStages) * kDmPieceBytes + 4 * (size_t)((a.sp.chunks + 31) / 32);
+    cudaError_t e = cudaFuncSetAttribute(diff_mask_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.mp.tokens / bt, a.mp.layers);
+    diff_mask_kernel<<<grid, kDmThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
