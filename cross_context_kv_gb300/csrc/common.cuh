@@ -113,8 +113,8 @@ __device__ __forceinline__ void rotate_pair(float* lo, float* hi, const float* c
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         float x0 = lo[k], x1 = hi[k];
-        lo[k] = x0 * c[k] - x1 * s[k];
-        hi[k] = x1 * c[k] + x0 * s[k];
+        lo[k] = __fmaf_rn(x0, c[k], __fmul_rn(x1, -s[k]));  // same rounding as the packed form
+        hi[k] = __fmaf_rn(x1, c[k], __fmul_rn(x0, s[k]));
     }
 }
 
@@ -221,8 +221,8 @@ __device__ __forceinline__ void rotate4(float* lo, float* hi, const float* c, co
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         float x0 = lo[k], x1 = hi[k];
-        lo[k] = x0 * c[k] - x1 * s[k];
-        hi[k] = x1 * c[k] + x0 * s[k];
+        lo[k] = __fmaf_rn(x0, c[k], __fmul_rn(x1, -s[k]));  // same rounding as the packed form
+        hi[k] = __fmaf_rn(x1, c[k], __fmul_rn(x0, s[k]));
     }
 }
 

@@ -44,8 +44,8 @@ __device__ __forceinline__ void rotate_with(float* lo, float* hi, const float2* 
     for (int k = 0; k < 8; ++k) {
         float2 cs = tab[i0 + k];
         float x0 = lo[k], x1 = hi[k];
-        lo[k] = x0 * cs.x - x1 * cs.y;
-        hi[k] = x1 * cs.x + x0 * cs.y;
+        lo[k] = __fmaf_rn(x0, cs.x, __fmul_rn(x1, -cs.y));  // same rounding as the packed form
+        hi[k] = __fmaf_rn(x1, cs.x, __fmul_rn(x0, cs.y));
     }
 }
 
@@ -702,8 +702,9 @@ mean_correct_kernel(McArgs args) {
         const int h = pq / v8, v = pq % v8;
         const int eo = h * D + 4 * v;
         const int g_lo = h * (D / 4) + v, g_hi = g_lo + v8;
-        float c[4], sn[4], m0[4], m1[4];
-        int cached = -1;  // agent whose cos/sin/mean sit in c, sn, m0, m1
+        // per-agent constants as float pairs (packed f32x2 arithmetic): cos, sin, -sin, mean
+        float2 c2[2], s2[2], ns2[2], m0[2], m1[2];
+        int cached = -1;  // agent whose constants sit in these registers
         for (int kl = 0; kl < tiles; ++kl) {
             const int k = grp * tiles + kl;
             const int slot = k % kMcStages;
@@ -722,11 +723,15 @@ mean_correct_kernel(McArgs args) {
                     const bool rot = rot_on[a];
                     if (a != cached) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            c[q] = rot ? cos_t[(a * 4 + q) * v8 + v] : 1.f;
-                            sn[q] = rot ? sin_t[(a * 4 + q) * v8 + v] : 0.f;
-                            m0[q] = mu_all[a * HD + q * G + g_lo];
-                            m1[q] = mu_all[a * HD + q * G + g_hi];
+                        for (int q = 0; q < 2; ++q) {
+                            const float* ct = cos_t + (a * 4 + 2 * q) * v8 + v;
+                            const float* st = sin_t + (a * 4 + 2 * q) * v8 + v;
+                            c2[q] = make_float2(ct[0], ct[v8]);
+                            s2[q] = make_float2(st[0], st[v8]);
+                            ns2[q] = make_float2(-s2[q].x, -s2[q].y);
+                            const float* mm = mu_all + a * HD + (2 * q) * G;
+                            m0[q] = make_float2(mm[g_lo], mm[G + g_lo]);
+                            m1[q] = make_float2(mm[g_hi], mm[G + g_hi]);
                         }
                         cached = a;
                     }
@@ -738,21 +743,39 @@ mean_correct_kernel(McArgs args) {
                     for (int row = row_off; row < tt; row += rpp) {
                         const int t = t0 + row, tl = t - t_lo;
                         if (mem[tl >> 5] >> (tl & 31) & 1u) continue;
-                        float x0[4], x1[4];
-                        unpack4(*reinterpret_cast<const uint2*>(tb + row * HD), x0);
-                        unpack4(*reinterpret_cast<const uint2*>(tb + row * HD + half), x1);
-                        if (rot) rotate4(x0, x1, c, sn);
-                        if (b > 0) {
-                            const float wt = wb[t];
+                        const uint2 lo_raw = *reinterpret_cast<const uint2*>(tb + row * HD);
+                        const uint2 hi_raw = *reinterpret_cast<const uint2*>(tb + row * HD + half);
+                        float2 x0[2], x1[2];
+                        x0[0] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo_raw.x));
+                        x0[1] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo_raw.y));
+                        x1[0] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi_raw.x));
+                        x1[1] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi_raw.y));
+                        if (rot) {
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                x0[q] = fmaf(wt, m0[q], x0[q]);
-                                x1[q] = fmaf(wt, m1[q], x1[q]);
+                            for (int q = 0; q < 2; ++q) {
+                                const float2 lo = __ffma2_rn(x0[q], c2[q], __fmul2_rn(x1[q], ns2[q]));
+                                const float2 hi = __ffma2_rn(x1[q], c2[q], __fmul2_rn(x0[q], s2[q]));
+                                x0[q] = lo;
+                                x1[q] = hi;
                             }
                         }
+                        if (b > 0) {
+                            const float wt = wb[t];
+                            const float2 w2 = make_float2(wt, wt);
+#pragma unroll
+                            for (int q = 0; q < 2; ++q) {
+                                x0[q] = __ffma2_rn(w2, m0[q], x0[q]);
+                                x1[q] = __ffma2_rn(w2, m1[q], x1[q]);
+                            }
+                        }
+                        uint2 lo_out, hi_out;
+                        *reinterpret_cast<__nv_bfloat162*>(&lo_out.x) = __float22bfloat162_rn(x0[0]);
+                        *reinterpret_cast<__nv_bfloat162*>(&lo_out.y) = __float22bfloat162_rn(x0[1]);
+                        *reinterpret_cast<__nv_bfloat162*>(&hi_out.x) = __float22bfloat162_rn(x1[0]);
+                        *reinterpret_cast<__nv_bfloat162*>(&hi_out.y) = __float22bfloat162_rn(x1[1]);
                         uint16_t* o = ob + (long long)t * op.st;
-                        st_stream2(reinterpret_cast<uint2*>(o), pack4(x0));
-                        st_stream2(reinterpret_cast<uint2*>(o + half), pack4(x1));
+                        st_stream2(reinterpret_cast<uint2*>(o), lo_out);
+                        st_stream2(reinterpret_cast<uint2*>(o + half), hi_out);
                     }
                 }
             }
