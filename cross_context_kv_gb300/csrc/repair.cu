@@ -122,12 +122,61 @@ cudaError_t launch_rerope(const uint16_t* in, const kvfix_kv_desc& dd, uint16_t*
 
 // =====================================================================================
 // Check-layer divergence for K and V of all agents: grid = (token tiles, R).
-// One warp per token row; each lane owns pair vectors p = lane, lane+32, ...
-// The reused row is loaded once and compared with every agent's fresh row.
+// One warp per (token row, plane): warps 2w and 2w+1 of a CTA take the K and V rows of
+// the same token.  Each lane owns pair vectors p = lane, lane+32, ... and loads two of
+// them at a time, so a row of up to 64 pair vectors costs one memory round trip.
 // =====================================================================================
 constexpr int kScoreWarps = 8;
-constexpr int kScoreRowsPerWarp = 2;
+constexpr int kScoreRowsPerCta = kScoreWarps / 2;
 constexpr int kAgentGroup = 8;
+
+__device__ __forceinline__ float sq_diff8(const uint4& x, const uint4& f, float acc) {
+    float xf[8], ff[8];
+    unpack8(x, xf);
+    unpack8(f, ff);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float e = ff[q] - xf[q];
+        acc = fmaf(e, e, acc);
+    }
+    return acc;
+}
+
+// Reused and fresh pieces of two pair vectors of one token row (the second may be absent).
+struct ScorePv2 {
+    uint4 x0a, x1a, f0a, f1a, x0b, x1b, f0b, f1b;
+};
+
+__device__ __forceinline__ ScorePv2 score_load(const uint16_t* reuse, long long ro, const uint16_t* fresh,
+                                               long long fo, long long e0, long long e1, int half) {
+    ScorePv2 v;
+    v.x0a = *reinterpret_cast<const uint4*>(reuse + ro + e0);
+    v.x1a = *reinterpret_cast<const uint4*>(reuse + ro + e0 + half);
+    v.f0a = *reinterpret_cast<const uint4*>(fresh + fo + e0);
+    v.f1a = *reinterpret_cast<const uint4*>(fresh + fo + e0 + half);
+    v.x0b = *reinterpret_cast<const uint4*>(reuse + ro + e1);
+    v.x1b = *reinterpret_cast<const uint4*>(reuse + ro + e1 + half);
+    v.f0b = *reinterpret_cast<const uint4*>(fresh + fo + e1);
+    v.f1b = *reinterpret_cast<const uint4*>(fresh + fo + e1 + half);
+    return v;
+}
+
+__device__ __forceinline__ float score_rot8(const uint4& x0v, const uint4& x1v, const uint4& f0v, const uint4& f1v,
+                                            const float2* tab, int i0, float ss) {
+    float x0[8], x1[8], f0[8], f1[8];
+    unpack8(x0v, x0);
+    unpack8(x1v, x1);
+    unpack8(f0v, f0);
+    unpack8(f1v, f1);
+    rotate_with(x0, x1, tab, i0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float e0 = f0[q] - x0[q], e1 = f1[q] - x1[q];
+        ss = fmaf(e0, e0, ss);
+        ss = fmaf(e1, e1, ss);
+    }
+    return ss;
+}
 
 __global__ void __launch_bounds__(kScoreWarps * 32)
 score_kernel(const uint16_t* __restrict__ k_reuse, const uint16_t* __restrict__ v_reuse, Plane rp,
@@ -144,12 +193,24 @@ score_kernel(const uint16_t* __restrict__ k_reuse, const uint16_t* __restrict__ 
     const int v16 = rp.dim / 16;
     const int P = rp.heads * v16;  // pair vectors per token row
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t_base = blockIdx.x * (kScoreWarps * kScoreRowsPerWarp);
-    const bool do_k = k_reuse != nullptr, do_v = v_reuse != nullptr;
+    const bool keys = (warp & 1) == 0;
+    const uint16_t* reuse = keys ? k_reuse : v_reuse;
+    const uint16_t* fresh = keys ? k_fresh : v_fresh;
+    float* d_out = keys ? d_k : d_v;
+    float* w_out = keys ? w_k : w_v;
+    const int t_base = blockIdx.x * kScoreRowsPerCta;
+    const int t = t_base + (warp >> 1);
+    const bool row_ok = reuse != nullptr && t < n;
+    const long long ro = row_ok ? rp.row(r, 0, t) : 0;
+    auto offs = [&](int p0, long long& e0, long long& e1) {  // element offsets of p0 and p0 + 32
+        const int p1 = p0 + 32 < P ? p0 + 32 : p0;
+        e0 = (long long)(p0 / v16) * rp.dim + 8 * (p0 % v16);
+        e1 = (long long)(p1 / v16) * rp.dim + 8 * (p1 % v16);
+    };
     pdl_trigger();  // the selection may launch; it waits for these scores
     if (mask_union) {  // the selection ORs both planes into it afterwards
         const int words = (n + 31) / 32;
-        const int w0 = t_base / 32, w1 = min(words, (t_base + kScoreWarps * kScoreRowsPerWarp + 31) / 32);
+        const int w0 = t_base / 32, w1 = min(words, (t_base + kScoreRowsPerCta + 31) / 32);
         for (int i = threadIdx.x; i < agents * (w1 - w0); i += blockDim.x) {
             const int a = i / (w1 - w0), w = w0 + i % (w1 - w0);
             mask_union[((long long)a * R + r) * words + w] = 0u;
@@ -159,71 +220,53 @@ score_kernel(const uint16_t* __restrict__ k_reuse, const uint16_t* __restrict__ 
     for (int a0 = 0; a0 < agents; a0 += kAgentGroup) {
         const int ag = agents - a0 < kAgentGroup ? agents - a0 : kAgentGroup;
         __syncthreads();
-        for (int i = threadIdx.x; i < ag * half; i += blockDim.x) {
-            int a = i / half, e = i % half;
-            float c, s;
-            rope_cos_sin(delta[(a0 + a) * R + r], th.theta[e], &c, &s);
-            tab[a][e] = make_float2(c, s);
+        // The first agent's first two pair vectors are requested before the angle table is
+        // built, so the table's arithmetic overlaps the memory round trip.
+        ScorePv2 v;
+        if (row_ok && lane < P) {
+            long long e0, e1;
+            offs(lane, e0, e1);
+            v = score_load(reuse, ro, fresh, fp.row(a0 * R + r, 0, t), e0, e1, half);
         }
+        if (k_reuse != nullptr)
+            for (int i = threadIdx.x; i < ag * half; i += blockDim.x) {
+                int a = i / half, e = i % half;
+                float c, s;
+                rope_cos_sin(delta[(a0 + a) * R + r], th.theta[e], &c, &s);
+                tab[a][e] = make_float2(c, s);
+            }
         if (threadIdx.x < ag) dl[threadIdx.x] = delta[(a0 + threadIdx.x) * R + r];
         __syncthreads();
-        for (int rr = 0; rr < kScoreRowsPerWarp; ++rr) {
-            const int t = t_base + rr * kScoreWarps + warp;
-            if (t >= n) continue;
-            const long long ro = rp.row(r, 0, t);
-            for (int a = 0; a < ag; ++a) {
-                const int u = (a0 + a) * R + r;
-                const long long fo = fp.row(u, 0, t);
-                float sk = 0.f, sv = 0.f;
-                for (int pv = lane; pv < P; pv += 32) {
-                    const int h = pv / v16, v = pv % v16;
-                    const long long eo = (long long)h * rp.dim + 8 * v;
-                    if (do_k) {
-                        float x0[8], x1[8], f0[8], f1[8];
-                        unpack8(*reinterpret_cast<const uint4*>(k_reuse + ro + eo), x0);
-                        unpack8(*reinterpret_cast<const uint4*>(k_reuse + ro + eo + half), x1);
-                        unpack8(*reinterpret_cast<const uint4*>(k_fresh + fo + eo), f0);
-                        unpack8(*reinterpret_cast<const uint4*>(k_fresh + fo + eo + half), f1);
-                        if (dl[a] != 0) rotate_with(x0, x1, tab[a], 8 * v);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            float e0 = f0[q] - x0[q], e1 = f1[q] - x1[q];
-                            sk = fmaf(e0, e0, sk);
-                            sk = fmaf(e1, e1, sk);
-                        }
-                    }
-                    if (do_v) {
-                        float x0[8], x1[8], f0[8], f1[8];
-                        unpack8(*reinterpret_cast<const uint4*>(v_reuse + ro + eo), x0);
-                        unpack8(*reinterpret_cast<const uint4*>(v_reuse + ro + eo + half), x1);
-                        unpack8(*reinterpret_cast<const uint4*>(v_fresh + fo + eo), f0);
-                        unpack8(*reinterpret_cast<const uint4*>(v_fresh + fo + eo + half), f1);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            float e0 = f0[q] - x0[q], e1 = f1[q] - x1[q];
-                            sv = fmaf(e0, e0, sv);
-                            sv = fmaf(e1, e1, sv);
-                        }
+        if (!row_ok) continue;
+        for (int a = 0; a < ag; ++a) {
+            const int u = (a0 + a) * R + r;
+            const long long fo = fp.row(u, 0, t);
+            const bool rot = keys && dl[a] != 0;
+            float ss = 0.f;
+            for (int p0 = lane; p0 < P; p0 += 64) {
+                const bool two = p0 + 32 < P;
+                long long e0, e1;
+                offs(p0, e0, e1);
+                if (a > 0 || p0 != lane) v = score_load(reuse, ro, fresh, fo, e0, e1, half);
+                if (rot) {
+                    ss = score_rot8(v.x0a, v.x1a, v.f0a, v.f1a, tab[a], 8 * (p0 % v16), ss);
+                    if (two) ss = score_rot8(v.x0b, v.x1b, v.f0b, v.f1b, tab[a], 8 * ((p0 + 32) % v16), ss);
+                } else {
+                    ss = sq_diff8(v.x0a, v.f0a, ss);
+                    ss = sq_diff8(v.x1a, v.f1a, ss);
+                    if (two) {
+                        ss = sq_diff8(v.x0b, v.f0b, ss);
+                        ss = sq_diff8(v.x1b, v.f1b, ss);
                     }
                 }
+            }
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    sk += __shfl_xor_sync(0xffffffffu, sk, o);
-                    sv += __shfl_xor_sync(0xffffffffu, sv, o);
-                }
-                if (lane == 0) {
-                    const long long oi = (long long)u * n + t;
-                    if (do_k) {
-                        float d = sqrtf(sk);
-                        d_k[oi] = d;
-                        w_k[oi] = fminf(d, 1.0f);
-                    }
-                    if (do_v) {
-                        float d = sqrtf(sv);
-                        d_v[oi] = d;
-                        w_v[oi] = fminf(d, 1.0f);
-                    }
-                }
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            if (lane == 0) {
+                const long long oi = (long long)u * n + t;
+                const float d = sqrtf(ss);
+                d_out[oi] = d;
+                w_out[oi] = fminf(d, 1.0f);
             }
         }
     }
@@ -236,8 +279,7 @@ cudaError_t launch_score(const uint16_t* k_reuse, const uint16_t* v_reuse,
                          float* w_k, float* w_v, uint32_t* mask_union, cudaStream_t s) {
     Plane rp = plane_of(reuse), fp = plane_of(fresh);
     if (rp.tokens == 0 || rp.chunks == 0 || agents == 0) return cudaSuccess;
-    const int rows = kScoreWarps * kScoreRowsPerWarp;
-    dim3 grid((rp.tokens + rows - 1) / rows, rp.chunks);
+    dim3 grid((rp.tokens + kScoreRowsPerCta - 1) / kScoreRowsPerCta, rp.chunks);
     score_kernel<<<grid, kScoreWarps * 32, 0, s>>>(k_reuse, v_reuse, rp, k_fresh, v_fresh, fp,
                                                    agents, delta, th, d_k, d_v, w_k, w_v, mask_union);
     return cudaGetLastError();
@@ -245,10 +287,14 @@ cudaError_t launch_score(const uint16_t* k_reuse, const uint16_t* v_reuse,
 
 // =====================================================================================
 // Block-wide top-b selection: the b largest keys, ties to the lower index.
-// Radix select (8-bit digits, most significant first) finds the b-th largest key T;
-// all keys > T are taken, and the lowest-index keys == T fill the rest.
+// Radix select, most significant bits first.  The bits above the highest bit in which
+// the block's smallest and largest keys differ are shared by every key and settled at
+// once; the rest are settled 8 at a time, each pass a histogram of the keys that still
+// match the settled prefix.  The result T is the b-th largest key: every key > T is
+// taken, and the lowest-index keys == T fill the rest.
 // =====================================================================================
 constexpr int kSelThreads = 1024;
+constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelSmemKeys = 16384;
 
 // Order-preserving map of a float to an unsigned key (larger float -> larger key).
@@ -257,137 +303,141 @@ __device__ __forceinline__ uint32_t ordered_f32(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive scan of one int per thread over the block; returns the block total in *total.
-__device__ int block_exclusive_scan(int x, int* warp_sums, int* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nw = blockDim.x >> 5;
-    int inc = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
-    }
-    __syncthreads();
-    if (lane == 31) warp_sums[warp] = inc;
-    __syncthreads();
-    if (warp == 0) {
-        int ws = lane < nw ? warp_sums[lane] : 0;
-        int wi = ws;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, wi, o);
-            if (lane >= o) wi += y;
-        }
-        if (lane < nw) warp_sums[lane] = wi - ws;
-        if (lane == 31) warp_sums[32] = wi;
-    }
-    __syncthreads();
-    int ex = inc - x + warp_sums[warp];
-    *total = warp_sums[32];
-    __syncthreads();
-    return ex;
-}
-
-template <typename Key>
 struct SelectSmem {
-    unsigned hist[256];
-    int warp_sums[33];
-    Key prefix;
-    int remaining;
+    unsigned hist[2][256];  // one histogram per pass parity
+    uint32_t wmin[kSelWarps], wmax[kSelWarps];
+    int wgt[kSelWarps], weq[kSelWarps];
+    uint32_t prefix[2];
+    int remaining[2];
 };
 
 // Select into `bits` (n-bit bitmap in shared memory, cleared here) and write the
-// ascending index list.  key_at(i) gives the key of index i.
-template <typename Key, typename KeyAt>
-__device__ void block_select(KeyAt key_at, int n, int b, uint32_t* bits, int32_t* idx_out,
-                             SelectSmem<Key>& sm) {
-    const int tid = threadIdx.x;
+// ascending index list.  key_at(i) gives the key of index i.  blockDim.x == kSelThreads.
+template <typename KeyAt>
+__device__ void block_select(KeyAt key_at, int n, int b, uint32_t* bits, int32_t* idx_out, SelectSmem& sm) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned full = 0xffffffffu;
     const int words = (n + 31) / 32;
-    for (int w = tid; w < words; w += blockDim.x) bits[w] = 0u;
-    if (b <= 0) {
-        __syncthreads();
-        return;
+    for (int w = tid; w < words; w += kSelThreads) bits[w] = 0u;
+    if (tid < 256) sm.hist[0][tid] = 0u;
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    for (int i = tid; i < n; i += kSelThreads) {
+        const uint32_t k = key_at(i);
+        kmin = min(kmin, k);
+        kmax = max(kmax, k);
     }
-    constexpr int kBits = sizeof(Key) * 8;
-    if (tid == 0) {
-        sm.prefix = 0;
-        sm.remaining = b;
+    kmin = __reduce_min_sync(full, kmin);
+    kmax = __reduce_max_sync(full, kmax);
+    if (lane == 0) {
+        sm.wmin[warp] = kmin;
+        sm.wmax[warp] = kmax;
     }
     __syncthreads();
-    for (int shift = kBits - 8; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += blockDim.x) sm.hist[i] = 0u;
-        __syncthreads();
-        const Key prefix = sm.prefix;
-        const Key hi_mask = (shift + 8 >= kBits) ? Key(0) : ~((Key(1) << (shift + 8)) - Key(1));
-        // warp-aggregated histogram: one atomic per distinct digit per warp
-        for (int i0 = 0; i0 < n; i0 += blockDim.x) {
+    if (b <= 0) return;
+    kmin = __reduce_min_sync(full, sm.wmin[lane]);
+    kmax = __reduce_max_sync(full, sm.wmax[lane]);
+    int hi = kmin == kmax ? 0 : 32 - __clz(kmin ^ kmax);  // bits [0, hi) are still open
+    uint32_t prefix = hi == 32 ? 0u : (kmax >> hi) << hi;
+    int remaining = b;  // keys still to take among those matching the prefix
+    for (int pass = 0; hi > 0; ++pass) {
+        const int wdt = hi < 8 ? hi : 8, shift = hi - wdt;
+        unsigned* h = sm.hist[pass & 1];
+        // warp-aggregated histogram: one shared-memory atomic per distinct digit per warp
+        for (int i0 = 0; i0 < n; i0 += kSelThreads) {
             const int i = i0 + tid;
             unsigned dig = 256u;  // not counted
             if (i < n) {
-                Key k = key_at(i);
-                if ((k & hi_mask) == (prefix & hi_mask)) dig = (unsigned)(k >> shift) & 255u;
+                const uint32_t k = key_at(i);
+                if (hi == 32 || (k >> hi) == (prefix >> hi)) dig = (k >> shift) & ((1u << wdt) - 1u);
             }
-            const unsigned peers = __match_any_sync(0xffffffffu, dig);
-            if (dig < 256u && (tid & 31) == __ffs(peers) - 1) atomicAdd(&sm.hist[dig], (unsigned)__popc(peers));
+            if (dig < 256u) atomicAdd(&h[dig], 1u);
         }
         __syncthreads();
-        if (tid < 32) {
+        if (warp == 0) {
             // lane l holds bins 255-8l .. 248-8l (descending digit order)
-            unsigned c[8];
-            unsigned lsum = 0;
+            unsigned c[8], lsum = 0;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                c[q] = sm.hist[255 - 8 * tid - q];
+                c[q] = h[255 - 8 * lane - q];
                 lsum += c[q];
             }
             unsigned inc = lsum;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                unsigned y = __shfl_up_sync(0xffffffffu, inc, o);
-                if (tid >= o) inc += y;
+                const unsigned y = __shfl_up_sync(full, inc, o);
+                if (lane >= o) inc += y;
             }
-            unsigned before = inc - lsum;  // keys with a larger digit than this lane's bins
-            const unsigned rem = (unsigned)sm.remaining;
+            const unsigned before = inc - lsum;  // keys with a larger digit than this lane's bins
+            const unsigned rem = (unsigned)remaining;
             if (before < rem && rem <= inc) {
                 unsigned acc = before;
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     if (acc < rem && rem <= acc + c[q]) {
-                        sm.prefix = prefix | (Key(255 - 8 * tid - q) << shift);
-                        sm.remaining = (int)(rem - acc);
+                        sm.prefix[pass & 1] = prefix | ((uint32_t)(255 - 8 * lane - q) << shift);
+                        sm.remaining[pass & 1] = (int)(rem - acc);
                     }
                     acc += c[q];
                 }
             }
+        } else if (tid - 32 < 256) {
+            sm.hist[(pass + 1) & 1][tid - 32] = 0u;  // the next pass's histogram
         }
         __syncthreads();
+        prefix = sm.prefix[pass & 1];
+        remaining = sm.remaining[pass & 1];
+        hi = shift;
     }
-    const Key T = sm.prefix;
-    const int need_eq = sm.remaining;
-    // Contiguous segment per thread, in index order.
-    const int seg = (n + blockDim.x - 1) / blockDim.x;
+    const uint32_t T = prefix;
+    // Keys > T and == T on this thread's contiguous segment, then one block scan of both.
+    const int seg = (n + kSelThreads - 1) / kSelThreads;
     const int i0 = min(n, tid * seg), i1 = min(n, i0 + seg);
-    int eq = 0;
-    for (int i = i0; i < i1; ++i) eq += (key_at(i) == T);
-    int tot;
-    int eq_before = block_exclusive_scan(eq, sm.warp_sums, &tot);
-    int cnt = 0;
+    int gt = 0, eq = 0;
     for (int i = i0; i < i1; ++i) {
-        Key k = key_at(i);
+        const uint32_t k = key_at(i);
+        gt += k > T;
+        eq += k == T;
+    }
+    int igt = gt, ieq = eq;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int yg = __shfl_up_sync(full, igt, o), ye = __shfl_up_sync(full, ieq, o);
+        if (lane >= o) {
+            igt += yg;
+            ieq += ye;
+        }
+    }
+    if (lane == 31) {
+        sm.wgt[warp] = igt;
+        sm.weq[warp] = ieq;
+    }
+    __syncthreads();
+    int wg = sm.wgt[lane], we = sm.weq[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int yg = __shfl_up_sync(full, wg, o), ye = __shfl_up_sync(full, we, o);
+        if (lane >= o) {
+            wg += yg;
+            we += ye;
+        }
+    }
+    // exclusive offsets of this warp
+    const int og = warp ? __shfl_sync(full, wg, warp - 1) : 0;
+    const int oe = warp ? __shfl_sync(full, we, warp - 1) : 0;
+    const int gt_before = og + igt - gt;
+    int eq_seen = oe + ieq - eq;
+    int out = gt_before + min(eq_seen, remaining);
+    for (int i = i0; i < i1; ++i) {
+        const uint32_t k = key_at(i);
         bool take = k > T;
         if (k == T) {
-            take = eq_before < need_eq;
-            ++eq_before;
+            take = eq_seen < remaining;
+            ++eq_seen;
         }
         if (take) {
+            idx_out[out++] = i;
             atomicOr(&bits[i >> 5], 1u << (i & 31));
-            ++cnt;
         }
-    }
-    int out_before = block_exclusive_scan(cnt, sm.warp_sums, &tot);
-    __syncthreads();
-    for (int i = i0; i < i1; ++i) {
-        if ((bits[i >> 5] >> (i & 31) & 1u) && out_before < b) idx_out[out_before++] = i;
     }
     __syncthreads();
 }
@@ -399,7 +449,7 @@ select_f32_kernel(const float* __restrict__ d_k, const float* __restrict__ d_v, 
                   int32_t* idx_k, int32_t* idx_v, uint32_t* mask_k, uint32_t* mask_v,
                   uint32_t* mask_union) {
     extern __shared__ __align__(16) unsigned char dyn[];
-    __shared__ SelectSmem<uint32_t> sm;
+    __shared__ SelectSmem sm;
     const int words = (n + 31) / 32;
     uint32_t* bits = reinterpret_cast<uint32_t*>(dyn);
     uint32_t* keys = bits + words;
@@ -415,9 +465,9 @@ select_f32_kernel(const float* __restrict__ d_k, const float* __restrict__ d_v, 
     if (cached) {
         for (int i = threadIdx.x; i < n; i += blockDim.x) keys[i] = ordered_f32(du[i]);
         __syncthreads();
-        block_select<uint32_t>([&](int i) { return keys[i]; }, n, b, bits, idx_out, sm);
+        block_select([&](int i) { return keys[i]; }, n, b, bits, idx_out, sm);
     } else {
-        block_select<uint32_t>([&](int i) { return ordered_f32(du[i]); }, n, b, bits, idx_out, sm);
+        block_select([&](int i) { return ordered_f32(du[i]); }, n, b, bits, idx_out, sm);
     }
     uint32_t* m = plane == 0 ? mask_k : mask_v;
     if (m)

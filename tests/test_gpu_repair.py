@@ -61,6 +61,12 @@ SMALL_REPAIR = [
                             delta_hi=9000),
     synth.ROUND_QWEN14B.with_(name="round_small", agents=3, chunks=2, layers=3, tokens=130,
                               kv_heads=2, head_dim=64, seed=8),
+    # more agents than one group of 8: probe rounds and tiles of two groups share the ring
+    synth.ROUND_QWEN14B.with_(name="round_two_groups", agents=10, chunks=1, layers=2, tokens=200,
+                              kv_heads=2, head_dim=64, seed=9),
+    # a token row wider than 1024 elements: probe rows are read straight from memory
+    synth.REPAIR_TINY.with_(name="wide_rows", tokens=90, kv_heads=9, head_dim=128, layers=2,
+                            r_num=1, r_den=3, seed=11),
 ]
 
 
