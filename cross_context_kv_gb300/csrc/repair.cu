@@ -520,7 +520,7 @@ constexpr int kMcThreads = 256;
 constexpr int kMcWarps = kMcThreads / 32;
 constexpr int kMcSlotsPerCta = 32 / kMcCluster;
 constexpr int kMcLanesPerSlot = kMcThreads / kMcSlotsPerCta;  // 64
-constexpr int kMcStages = 2;
+constexpr int kMcStages = 3;
 constexpr int kMcTileBytes = 16384;
 
 struct McArgs {
@@ -538,6 +538,7 @@ struct McArgs {
 
 struct McLayout {  // byte offsets into the dynamic shared memory
     int ps, slice, ring, mu_all, cs, member, wts, total, words_member;
+    int ps_alias;  // the phase-1 partials share the last ring stage
 };
 
 __host__ __device__ inline int align128(int x) { return (x + 127) / 128 * 128; }
@@ -545,10 +546,14 @@ __host__ __device__ inline bool mc_stage_weights(int ag, int rows_per_cta) { ret
 
 __host__ __device__ inline McLayout mc_layout(int HD, int half, int ag, int rows_per_cta, int tile_rows) {
     McLayout m;
-    m.ps = 0;
-    m.slice = m.ps + 4 * kMcSlotsPerCta * HD;
-    m.ring = align128(m.slice + 4 * (HD / kMcCluster));
-    m.mu_all = align128(m.ring + kMcStages * tile_rows * HD * 2);
+    // The partial sums of phase 1 are dead during phase 2: when they fit in one ring
+    // stage they live in the last one, which takes tiles only after phase 1.
+    const int stage = tile_rows * HD * 2, ps_bytes = 4 * kMcSlotsPerCta * HD;
+    m.ring = 0;
+    m.ps_alias = ps_bytes <= stage;
+    m.ps = m.ps_alias ? m.ring + (kMcStages - 1) * stage : m.ring + kMcStages * stage;
+    m.slice = align128(m.ps_alias ? m.ring + kMcStages * stage : m.ps + ps_bytes);
+    m.mu_all = align128(m.slice + 4 * (HD / kMcCluster));
     m.cs = m.mu_all + 4 * ag * HD;
     m.member = m.cs + 4 * 2 * ag * half;
     m.words_member = (rows_per_cta + 31) / 32;
@@ -626,8 +631,10 @@ mean_correct_kernel(McArgs args) {
         abort_flag = 0;
     }
     __syncthreads();
-    if (tid == 0)  // the first tiles stream in while phase 1 runs
-        for (; issued < min(kMcStages, total_tiles); ++issued) issue(issued);
+    // the first tiles stream in while phase 1 runs (not into the stage holding the partials)
+    const int ahead0 = lay.ps_alias ? kMcStages - 1 : kMcStages;
+    if (tid == 0)
+        for (; issued < min(ahead0, total_tiles); ++issued) issue(issued);
     pdl_wait();  // probe sets and weights of the selection kernel
 
     for (int grp = 0; grp < groups; ++grp) {
@@ -704,6 +711,7 @@ mean_correct_kernel(McArgs args) {
                     mine[k * G + g_hi] = fs1[k] - xs1[k];
                 }
             }
+            fence_proxy_async_smem();  // the partials' stage is refilled by bulk copies later
             cluster.sync();
             // residue-major elements [rank*SL, rank*SL + SL): 32 partials added in order
             for (int e = tid; e < SL; e += kMcThreads) {
@@ -746,6 +754,14 @@ mean_correct_kernel(McArgs args) {
             }
         }
         __syncthreads();
+        // Top the ring up to kMcStages tiles of this group.  When the partials share a
+        // stage, tiles of the next group wait for its phase 1: the ring is drained at
+        // each group's end.
+        const int tile_end = lay.ps_alias ? min(total_tiles, (grp + 1) * tiles) : total_tiles;
+        if (tid == 0 && !abort_flag) {
+            fence_proxy_async_smem();
+            for (; issued < min(grp * tiles + kMcStages, tile_end); ++issued) issue(issued);
+        }
         const int rpp = kMcThreads / P;  // rows per pass (P <= 256 quad pairs per row)
         const bool active = tid < rpp * P;
         const int pq = tid % P, row_off = tid / P;
@@ -831,7 +847,7 @@ mean_correct_kernel(McArgs args) {
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
-            if (tid == 0 && issued < total_tiles) {
+            if (tid == 0 && issued < tile_end && !abort_flag) {
                 // the stage is free once every warp released it; then refill it
                 if (!mbar_wait(&empty[slot], parity)) {
                     atomicOr(&g_status_repair, FLAG_TIMEOUT);
@@ -843,14 +859,15 @@ mean_correct_kernel(McArgs args) {
             }
         }
         __syncthreads();
-        if (abort_flag) {
-            // wait (bounded) for every copy still in flight, then leave
-            if (tid == 0)
-                for (int k = max(0, issued - kMcStages); k < issued; ++k)
-                    mbar_wait(&full[k % kMcStages], (unsigned)(k / kMcStages) & 1u);
-            __syncthreads();
-            return;
-        }
+    }
+    if (abort_flag) {
+        // A wait ran out (the status word says so).  From then on the tile loops skipped
+        // every wait while the CTA still passed each cluster barrier, so the other CTAs of
+        // the cluster were not held; copies still in flight are waited for (bounded).
+        if (tid == 0)
+            for (int k = max(0, issued - kMcStages); k < issued; ++k)
+                mbar_wait(&full[k % kMcStages], (unsigned)(k / kMcStages) & 1u);
+        __syncthreads();
     }
 }
 
