@@ -216,37 +216,75 @@ def run_repair_step(kvfix, cfg, inp, out):
     return sel
 
 
+HOST_LEAD_CYCLES = 1_000_000  # ~0.5 ms of device sleep before each timed step (untimed)
+
+
+def host_lead():
+    """Queue a short device-side sleep before a timed step, so the host has enqueued the
+    step's calls (about 70 us of binding overhead on the Grace host) before the device
+    reaches the first event: the events then bracket device work only, as in a stream of
+    back-to-back steps.  The sleep itself precedes the first event."""
+    torch.cuda._sleep(HOST_LEAD_CYCLES)
+
+
 def time_repair(kvfix, cfg, inp, steps, warmup, flush):
-    """Per-step CUDA events on the launching stream; L2 flushed (untimed) between steps.
+    """Per-step CUDA events on the launching stream around the whole step (score_topk and
+    mean_correct back to back, so the chained launches overlap as they do in use); L2
+    flushed (untimed) between steps.  Then `steps` launches of mean_correct alone, each
+    bracketed by events, for the correction kernel's own duration (an event between the
+    two calls would break the launch chaining, so the step loop has none).
     Returns (step times ms, mean_correct times ms)."""
     stream = torch.cuda.current_stream()
     out = {"k": torch.empty_like(inp["k_fresh"]), "v": torch.empty_like(inp["v_fresh"]),
            "mu_k": torch.empty(cfg.units, cfg.layers, cfg.kv_heads * cfg.head_dim, device="cuda"),
            "mu_v": torch.empty(cfg.units, cfg.layers, cfg.kv_heads * cfg.head_dim, device="cuda")}
-    cl = cfg.check_layer
     for _ in range(warmup):
         flush.zero_()
         run_repair_step(kvfix, cfg, inp, out)
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sel = None
     for s in range(steps):
         flush.zero_()
-        e0, e1, e2 = ev[s]
+        host_lead()
+        e0, e1 = ev[s]
         e0.record(stream)
-        sel = kvfix.score_topk(inp["k_reuse"][:, cl:cl + 1], inp["v_reuse"][:, cl:cl + 1],
-                               inp["k_fresh"][:, cl:cl + 1], inp["v_fresh"][:, cl:cl + 1], cfg.agents,
-                               inp["delta"], cfg.rope_base, cfg.b)
+        sel = run_repair_step(kvfix, cfg, inp, out)
         e1.record(stream)
+    torch.cuda.synchronize()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    for s in range(steps):
+        flush.zero_()
+        host_lead()
+        e0, e1 = ev[s]
+        e0.record(stream)
         kvfix.mean_correct(inp["k_reuse"], inp["v_reuse"], inp["k_fresh"], inp["v_fresh"], cfg.agents,
                            inp["delta"], cfg.rope_base, sel["idx_k"], sel["idx_v"], sel["w_k"], sel["w_v"],
                            k_out=out["k"], v_out=out["v"], mu_k=out["mu_k"], mu_v=out["mu_v"])
-        e2.record(stream)
+        e1.record(stream)
     torch.cuda.synchronize()
-    step_ms = [e0.elapsed_time(e2) for e0, _, e2 in ev]
-    mc_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev]
+    mc_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     kvfix.check_status()
     return step_ms, mc_ms
+
+
+def time_score(kvfix, cfg, inp, steps, flush):
+    """kvfix_score_topk alone (score + select kernels), events around the call, L2 flushed."""
+    stream = torch.cuda.current_stream()
+    cl = cfg.check_layer
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        host_lead()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        kvfix.score_topk(inp["k_reuse"][:, cl:cl + 1], inp["v_reuse"][:, cl:cl + 1],
+                         inp["k_fresh"][:, cl:cl + 1], inp["v_fresh"][:, cl:cl + 1], cfg.agents,
+                         inp["delta"], cfg.rope_base, cfg.b)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    return ms
 
 
 def time_e2e(kvfix, cfg, inp, steps, warmup):
@@ -323,12 +361,14 @@ def stage_diff(kvfix, peak, steps=5, warmup=2):
     out_v = torch.empty_like(inp["sib_v"])
     for s in range(warmup + steps):
         flush.zero_()
+        host_lead()
         e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         e0.record(stream)
         mask, offsets, payload, _ = kvfix.diff_encode(inp["master_k"], inp["master_v"], inp["sib_k"],
                                                       inp["sib_v"], cfg.block_tokens, capacity=cap, sync=False)
         e1.record(stream)
         flush.zero_()
+        host_lead()
         e1b = torch.cuda.Event(enable_timing=True)
         e1b.record(stream)
         kvfix.diff_gather(inp["master_k"], inp["master_v"], mask, offsets, payload, cfg.siblings,
@@ -368,6 +408,7 @@ def stage_lowrank(kvfix, peak, steps=3, warmup=2):
     lr_ms, dr_ms = [], []
     for s in range(warmup + steps):
         flush.zero_()
+        host_lead()
         e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         e0.record(stream)
         kvfix.lowrank_apply(inp["x_k"], inp["a_k"], inp["b_k"], out=kt)
@@ -465,6 +506,7 @@ def run_ours(args, world, rank, local):
     clocks = clk.summary()
     ms = barrier_max(statistics.mean(step_ms), world)
     mc = barrier_max(statistics.mean(mc_ms), world)
+    score_ms = statistics.mean(time_score(kvfix, cfg, inp, max(3, args.steps // 4), flush))
     e2e_ms, h2d, d2h = time_e2e(kvfix, cfg, inp, max(2, args.steps // 4), 1)
     e2e_ms = barrier_max(e2e_ms, world)
     value = world * by["corrected"] / ms / 1e6
@@ -472,6 +514,7 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "step_ms_spread": [round(min(step_ms), 5), round(statistics.median(step_ms), 5), round(max(step_ms), 5)],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded draws: reuse ~ N(0,1); fresh = rerope(reuse) + mu + xi)",
         "config": {"workload": "repair_llama8b: one 4096-token chunk, 32 layers, 8 KV heads x 128, bf16, "
@@ -487,9 +530,11 @@ def run_ours(args, world, rank, local):
                      "peak_kind": peak_kind + " (copy bandwidth)",
                      "launch_ms": round(mc, 5), "algorithmic_bytes_per_launch": by["mean_correct"]},
         "step_roofline_frac": round(by["step"] / ms / 1e6 / peak, 4),
+        "score_topk_ms": round(score_ms, 5),  # its own loop, after the timed region
         "e2e": {"value": round(world * by["corrected"] / e2e_ms / 1e6, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": 3 * args.steps,  # score, select, mean_correct per step
+        # timed steps: score, select, mean_correct each; then the timed mean_correct-alone loop
+        "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
     del inp, fk, fv, reuse, flush
