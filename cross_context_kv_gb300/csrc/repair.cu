@@ -493,15 +493,16 @@ cudaError_t launch_select_f32(const float* d_k, const float* d_v, int units, int
 // =====================================================================================
 // Probe-mean correction, one launch for both planes.  One thread-block cluster of 8
 // CTAs per (reused chunk, layer, plane):
-//   phase 1, per agent: the 32 canonical partial sums P_s (s = probe index mod 32, each
-//     summed in probe-list order) are spread over the cluster, 4 per CTA; the fresh
-//     probe rows are copied to the output on the way.  The rotation is linear, so a
-//     slot sums fresh and reused rows separately and rotates the reused sum once:
-//     P_s = sum(fresh) - rot(sum(reuse)).  Cluster barrier; CTA k adds, for the row
-//     elements e with e % 4 == k % 4 in its half, the 32 partials in order 0..31 (read
-//     through distributed shared memory) and divides by b.  Cluster barrier; every CTA
-//     gathers the full mean.  Cluster barrier (the buffers are reused by the next agent).
-//   phase 2: CTA k streams 1/8 of the layer's rows through a 2-stage ring of 16 KB
+//   phase 1, per agent: the 32 slot sums P_s (s = probe index mod 32, each summed in
+//     probe-list order) are spread over the cluster, 4 per CTA; the fresh probe rows are
+//     copied to the output on the way.  The rotation is linear, so a slot sums fresh and
+//     reused rows separately and rotates the reused sum once: P_s = sum(fresh) -
+//     rot(sum(reuse)).  CTA g folds its slots into the group sum
+//     Q_g = ((P_4g + P_4g+1) + P_4g+2) + P_4g+3.  Cluster barrier; CTA k adds, for the
+//     row elements e with e % 4 == k % 4 in its half, Q_0..Q_7 in order (read through
+//     distributed shared memory) and divides by b.  Cluster barrier; every CTA gathers
+//     the full mean.  Cluster barrier (the buffers are reused by the next agent).
+//   phase 2: CTA k streams 1/8 of the layer's rows through a 3-stage ring of 16 KB
 //     shared-memory tiles filled by bulk asynchronous copies (TMA, completion counted
 //     in bytes on a "full" mbarrier, release by every warp on an "empty" mbarrier).
 //     The first tiles are requested at kernel start, so they arrive during phase 1.
@@ -511,7 +512,9 @@ cudaError_t launch_select_f32(const float* d_k, const float* d_v, int units, int
 // partners [D/2+4v, D/2+4v+4).  A thread keeps the same quad pair through phase 2, so
 // its cos/sin and mean values stay in registers.  Shared-memory vectors read 4 at a
 // time are stored by residue: element e sits at (e % 4) * (HD / 4) + e / 4.
-// The fixed summation order makes one call for N agents bit-identical to N calls.
+// The summation order (slots, then groups of four, then the eight groups) is fixed, and
+// the multi-agent kernels below follow it too: one call for N agents is bit-identical
+// to N calls.
 // =====================================================================================
 namespace cg = cooperative_groups;
 
@@ -711,20 +714,20 @@ mean_correct_kernel(McArgs args) {
                     mine[k * G + g_hi] = fs1[k] - xs1[k];
                 }
             }
+            // Group sum of this CTA's four slots, in slot order: Q = ((P0 + P1) + P2) + P3.
+            __syncthreads();
+            for (int e = tid; e < HD; e += kMcThreads) ps[e] = ((ps[e] + ps[HD + e]) + ps[2 * HD + e]) + ps[3 * HD + e];
             fence_proxy_async_smem();  // the partials' stage is refilled by bulk copies later
             cluster.sync();
-            // residue-major elements [rank*SL, rank*SL + SL): 32 partials added in order
+            // residue-major elements [rank*SL, rank*SL + SL): the 8 group sums added in order
             for (int e = tid; e < SL; e += kMcThreads) {
                 const int ri = rank * SL + e;
-                float part[32];
+                float part[kMcCluster];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const float* rps = cluster.map_shared_rank(ps, q / kMcSlotsPerCta);
-                    part[q] = rps[(q % kMcSlotsPerCta) * HD + ri];
-                }
+                for (int q = 0; q < kMcCluster; ++q) part[q] = cluster.map_shared_rank(ps, q)[ri];
                 float sum = 0.f;
 #pragma unroll
-                for (int q = 0; q < 32; ++q) sum += part[q];
+                for (int q = 0; q < kMcCluster; ++q) sum += part[q];
                 const float m = sum / (float)b;
                 mu_slice[e] = m;
                 mu_g[4 * (ri % G) + ri / G] = m;
@@ -871,6 +874,263 @@ mean_correct_kernel(McArgs args) {
     }
 }
 
+// =====================================================================================
+// Rounds of several agents: two kernels instead of the per-agent phases above.
+//   round_mean_kernel: one CTA per (unit, layer, plane) computes that unit's probe mean
+//     into the mean output, all units at once.  Warp g takes slots 4g..4g+3 and folds
+//     them into the group sum Q_g; the CTA adds Q_0..Q_7 in order -- the arithmetic of
+//     the cluster kernel, element for element.  Fresh probe rows are copied to the output.
+//   round_stream_kernel: one CTA per (row block, layer, plane, reused chunk, agent group)
+//     reads each reused row once and writes the corrected row of every agent of the
+//     group.  A thread is one (agent, quad pair): its rotation and mean stay in
+//     registers for the whole row block.
+// =====================================================================================
+constexpr int kRmThreads = 256;
+constexpr int kRsThreads = 1024;
+constexpr int kRsRows = 128;  // rows per CTA of the stream kernel
+constexpr int kRsStages = 3;  // tiles of reused rows in flight per CTA
+
+__global__ void __launch_bounds__(kRmThreads, 4) round_mean_kernel(McArgs args) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ float ct[kMaxHeadDim / 2], st[kMaxHeadDim / 2];
+    const int u = blockIdx.x, plane = blockIdx.y & 1, l = blockIdx.y >> 1;
+    const uint16_t* reuse = args.reuse[plane];
+    if (reuse == nullptr) return;
+    const uint16_t* fresh = args.fresh[plane];
+    uint16_t* out = args.out[plane];
+    const Plane& rp = args.rp;
+    const Plane& fp = args.fp;
+    const Plane& op = args.op;
+    const int R = rp.chunks, r = u % R, n = rp.tokens, L = rp.layers;
+    const int D = rp.dim, half = D / 2, v8 = D / 8;
+    const int HD = rp.heads * D, P = rp.heads * v8;
+    const int b = args.b;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float* Qs = reinterpret_cast<float*>(smem);  // [8 groups][HD]
+    const int dlt = args.delta[u];
+    const bool rot = plane == 0 && dlt != 0;
+    if (rot)  // independent of the selection: before the wait
+        for (int e = tid; e < half; e += kRmThreads) rope_cos_sin(dlt, args.th.theta[e], &ct[e], &st[e]);
+    pdl_wait();  // probe sets of the selection kernel
+    // The stream kernel is released only at the end (its large CTAs would otherwise sit
+    // waiting on SMs this kernel's later CTAs need).
+    float* mu_g = args.mu[plane] + ((long long)u * L + l) * HD;
+    if (b == 0) {
+        for (int e = tid; e < HD; e += kRmThreads) mu_g[e] = 0.f;
+        return;
+    }
+    __syncthreads();
+    const int32_t* S = args.idx[plane] + (long long)u * b;
+    for (int pq = lane; pq < P; pq += 32) {
+        const int h = pq / v8, v = pq % v8;
+        const long long eo = (long long)h * D + 4 * v;
+        float q0[4], q1[4];
+#pragma unroll
+        for (int j4 = 0; j4 < kMcSlotsPerCta; ++j4) {
+            const int s = warp * kMcSlotsPerCta + j4;
+            float fs0[4], fs1[4], xs0[4], xs1[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) fs0[k] = fs1[k] = xs0[k] = xs1[k] = 0.f;
+            // two probe rows of the slot in flight at a time, summed in list order
+            for (int i = s; i < b; i += 64) {
+                const int j0 = __ldg(S + i), j1 = i + 32 < b ? __ldg(S + i + 32) : -2;
+                uint2 xv[2][2], fv[2][2];
+                bool ok[2];
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    const int j = w ? j1 : j0;
+                    ok[w] = j >= 0 && j < n;
+                    if (!ok[w] && j != -2) atomicOr(&g_status_repair, FLAG_BOUNDS);
+                    if (ok[w]) {
+                        const long long ro = rp.row(r, l, j) + eo;
+                        const long long fo = fp.row(u, l, j) + eo;
+                        xv[w][0] = __ldg(reinterpret_cast<const uint2*>(reuse + ro));
+                        xv[w][1] = __ldg(reinterpret_cast<const uint2*>(reuse + ro + half));
+                        fv[w][0] = __ldcs(reinterpret_cast<const uint2*>(fresh + fo));
+                        fv[w][1] = __ldcs(reinterpret_cast<const uint2*>(fresh + fo + half));
+                    }
+                }
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    if (!ok[w]) continue;
+                    const long long oo = op.row(u, l, w ? j1 : j0) + eo;
+                    __stcs(reinterpret_cast<uint2*>(out + oo), fv[w][0]);
+                    __stcs(reinterpret_cast<uint2*>(out + oo + half), fv[w][1]);
+                    add4(xv[w][0], xs0);
+                    add4(xv[w][1], xs1);
+                    add4(fv[w][0], fs0);
+                    add4(fv[w][1], fs1);
+                }
+            }
+            if (rot) {
+                float c[4], sn[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    c[k] = ct[4 * v + k];
+                    sn[k] = st[4 * v + k];
+                }
+                rotate4(xs0, xs1, c, sn);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float p0 = fs0[k] - xs0[k], p1 = fs1[k] - xs1[k];
+                q0[k] = j4 == 0 ? p0 : q0[k] + p0;
+                q1[k] = j4 == 0 ? p1 : q1[k] + p1;
+            }
+        }
+        float* Q = Qs + warp * HD + h * D + 4 * v;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            Q[k] = q0[k];
+            Q[half + k] = q1[k];
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < HD; e += kRmThreads) {
+        float sum = 0.f;
+#pragma unroll
+        for (int g = 0; g < kMcCluster; ++g) sum += Qs[g * HD + e];
+        mu_g[e] = sum / (float)b;
+    }
+    pdl_trigger();
+}
+
+__global__ void __launch_bounds__(kRsThreads) round_stream_kernel(McArgs args, int tile_rows) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int plane = blockIdx.y & 1, l = blockIdx.y >> 1;
+    const uint16_t* reuse = args.reuse[plane];
+    if (reuse == nullptr) return;
+    uint16_t* out = args.out[plane];
+    const Plane& rp = args.rp;
+    const Plane& op = args.op;
+    const int R = rp.chunks, n = rp.tokens, L = rp.layers;
+    const int r = blockIdx.z % R, a0 = (blockIdx.z / R) * kAgentGroup;
+    const int ag = min(kAgentGroup, args.agents - a0);
+    const int D = rp.dim, half = D / 2, v8 = D / 8;
+    const int HD = rp.heads * D, P = rp.heads * v8;
+    const int b = args.b;
+    const int tid = threadIdx.x;
+    const int t_lo = blockIdx.x * kRsRows, t_hi = min(n, t_lo + kRsRows);
+    const int words = kRsRows / 32;
+    const int TR = tile_rows;
+    uint16_t* ring = reinterpret_cast<uint16_t*>(smem);                         // [kRsStages][TR][HD]
+    float* cs = reinterpret_cast<float*>(ring + (size_t)kRsStages * TR * HD);   // [ag][half] cos, [ag][half] sin
+    uint32_t* member = reinterpret_cast<uint32_t*>(cs + 2 * kAgentGroup * half);  // [ag][words]
+    float* wts = reinterpret_cast<float*>(member + kAgentGroup * words);        // [ag][kRsRows]
+    const bool keys = plane == 0;
+    const int tiles = (t_hi - t_lo + TR - 1) / TR;
+    const int chunks_row = HD / 8;  // 16-byte pieces of a row
+    // every thread copies its 16-byte pieces of a tile; one commit group per tile
+    auto fetch = [&](int k) {
+        if (k < tiles) {
+            uint16_t* dst = ring + (size_t)(k % kRsStages) * TR * HD;
+            const int t0 = t_lo + k * TR, tt = min(TR, t_hi - t0);
+            for (int c = tid; c < tt * chunks_row; c += kRsThreads) {
+                const int q = c / chunks_row, o = (c % chunks_row) * 8;
+                cp_async16(dst + q * HD + o, reuse + rp.row(r, l, t0 + q) + o);
+            }
+        }
+        cp_async_commit();
+    };
+    for (int k = 0; k < kRsStages - 1; ++k) fetch(k);  // reused rows do not depend on the means
+    for (int i = tid; i < ag * half; i += kRsThreads) {
+        const int a = i / half, e = i % half;
+        const int dlt = args.delta[(a0 + a) * R + r];
+        float c = 1.f, s = 0.f;
+        if (keys && dlt != 0) rope_cos_sin(dlt, args.th.theta[e], &c, &s);
+        cs[a * half + e] = c;
+        cs[(kAgentGroup + a) * half + e] = s;
+    }
+    for (int i = tid; i < ag * words; i += kRsThreads) member[i] = 0u;
+    pdl_wait();  // the means (and, before them, the probe sets)
+    __syncthreads();
+    if (b > 0) {
+        for (int i = tid; i < ag * b; i += kRsThreads) {
+            const int a = i / b;
+            const int j = args.idx[plane][(long long)((a0 + a) * R + r) * b + i % b];
+            if (j >= t_lo && j < t_hi) atomicOr(&member[a * words + ((j - t_lo) >> 5)], 1u << ((j - t_lo) & 31));
+        }
+        for (int i = tid; i < ag * (t_hi - t_lo); i += kRsThreads) {
+            const int a = i / (t_hi - t_lo), t = i % (t_hi - t_lo);
+            wts[a * kRsRows + t] = args.w[plane][(long long)((a0 + a) * R + r) * n + t_lo + t];
+        }
+    }
+    __syncthreads();
+    const int per_row = ag * P, rpp = kRsThreads / per_row;
+    const bool active = tid < rpp * per_row;
+    const int a = (tid % per_row) / P, pq = tid % P, row_off = tid / per_row;
+    const int u = (a0 + a) * R + r;
+    const int h = pq / v8, v = pq % v8;
+    const int eo = h * D + 4 * v;
+    const bool rot = keys && args.delta[min(u, args.agents * R - 1)] != 0;
+    // the same float-pair constants and arithmetic as the cluster kernel's phase 2
+    float2 c2[2], s2[2], ns2[2], m0[2], m1[2];
+    if (active) {
+        const float* mu_g = args.mu[plane] + ((long long)u * L + l) * HD + eo;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const float* ct = cs + a * half + 4 * v + 2 * q;
+            const float* st = cs + (kAgentGroup + a) * half + 4 * v + 2 * q;
+            c2[q] = make_float2(ct[0], ct[1]);
+            s2[q] = make_float2(st[0], st[1]);
+            ns2[q] = make_float2(-s2[q].x, -s2[q].y);
+            m0[q] = make_float2(mu_g[2 * q], mu_g[2 * q + 1]);
+            m1[q] = make_float2(mu_g[half + 2 * q], mu_g[half + 2 * q + 1]);
+        }
+    }
+    const uint32_t* mem = member + a * words;
+    const float* wb = wts + a * kRsRows;
+    uint16_t* ob = out + op.row(u, l, 0) + eo;
+    for (int k = 0; k < tiles; ++k) {
+        fetch(k + kRsStages - 1);
+        cp_async_wait<kRsStages - 1>();  // this thread's pieces of tile k have landed
+        __syncthreads();                 // ... and everyone's
+        const uint16_t* tb = ring + (size_t)(k % kRsStages) * TR * HD + eo;
+        const int t0 = t_lo + k * TR, tt = min(TR, t_hi - t0);
+        if (active) {
+            for (int row = row_off; row < tt; row += rpp) {
+                const int tl = t0 + row - t_lo;
+                if (b > 0 && (mem[tl >> 5] >> (tl & 31) & 1u)) continue;  // probe row: written already
+                const uint2 lo_raw = *reinterpret_cast<const uint2*>(tb + row * HD);
+                const uint2 hi_raw = *reinterpret_cast<const uint2*>(tb + row * HD + half);
+                float2 x0[2], x1[2];
+                x0[0] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo_raw.x));
+                x0[1] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo_raw.y));
+                x1[0] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi_raw.x));
+                x1[1] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi_raw.y));
+                if (rot) {
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const float2 lo = __ffma2_rn(x0[q], c2[q], __fmul2_rn(x1[q], ns2[q]));
+                        const float2 hi = __ffma2_rn(x1[q], c2[q], __fmul2_rn(x0[q], s2[q]));
+                        x0[q] = lo;
+                        x1[q] = hi;
+                    }
+                }
+                if (b > 0) {
+                    const float wt = wb[tl];
+                    const float2 w2 = make_float2(wt, wt);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        x0[q] = __ffma2_rn(w2, m0[q], x0[q]);
+                        x1[q] = __ffma2_rn(w2, m1[q], x1[q]);
+                    }
+                }
+                uint2 lo_out, hi_out;
+                *reinterpret_cast<__nv_bfloat162*>(&lo_out.x) = __float22bfloat162_rn(x0[0]);
+                *reinterpret_cast<__nv_bfloat162*>(&lo_out.y) = __float22bfloat162_rn(x0[1]);
+                *reinterpret_cast<__nv_bfloat162*>(&hi_out.x) = __float22bfloat162_rn(x1[0]);
+                *reinterpret_cast<__nv_bfloat162*>(&hi_out.y) = __float22bfloat162_rn(x1[1]);
+                uint16_t* o = ob + (long long)(t0 + row) * op.st;
+                st_stream2(reinterpret_cast<uint2*>(o), lo_out);
+                st_stream2(reinterpret_cast<uint2*>(o + half), hi_out);
+            }
+        }
+        __syncthreads();  // tile k's stage is refilled by the next iteration's fetch
+    }
+    cp_async_wait<0>();
+}
+
 cudaError_t launch_mean_correct(const McPlanes& pl, const kvfix_kv_desc& rd, const kvfix_kv_desc& fd,
                                 const kvfix_kv_desc& od, int agents, const int32_t* delta,
                                 const RopeTheta& th, int b, cudaStream_t s) {
@@ -892,8 +1152,29 @@ cudaError_t launch_mean_correct(const McPlanes& pl, const kvfix_kv_desc& rd, con
     a.th = th;
     const int n = a.rp.tokens;
     if (agents == 0 || a.rp.chunks == 0 || a.rp.layers == 0 || n == 0) return cudaSuccess;
-    a.rows_per_cta = (n + kMcCluster - 1) / kMcCluster;
     const int HD = a.rp.heads * a.rp.dim;
+    if (agents > 1 && kAgentGroup * (HD / 8) <= kRsThreads) {
+        // a round of several agents: all probe means at once, then one fan-out stream
+        const size_t mean_smem = (size_t)kMcCluster * HD * sizeof(float);
+        cudaError_t e = cudaFuncSetAttribute(round_mean_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)mean_smem);
+        if (e != cudaSuccess) return e;
+        e = launch_chained(round_mean_kernel, dim3(agents * a.rp.chunks, 2 * a.rp.layers), dim3(kRmThreads),
+                           mean_smem, s, a);
+        if (e != cudaSuccess) return e;
+        const int half = a.rp.dim / 2;
+        const int tile_rows = max(1, min(32, kMcTileBytes / (2 * HD)));
+        const size_t stream_smem = (size_t)kRsStages * tile_rows * HD * 2 +
+                                   sizeof(float) * (2 * kAgentGroup * half + kAgentGroup * kRsRows) +
+                                   sizeof(uint32_t) * kAgentGroup * (kRsRows / 32);
+        e = cudaFuncSetAttribute(round_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stream_smem);
+        if (e != cudaSuccess) return e;
+        const int groups = (agents + kAgentGroup - 1) / kAgentGroup;
+        return launch_chained(round_stream_kernel, dim3((n + kRsRows - 1) / kRsRows, 2 * a.rp.layers,
+                                                        a.rp.chunks * groups),
+                              dim3(kRsThreads), stream_smem, s, a, tile_rows);
+    }
+    a.rows_per_cta = (n + kMcCluster - 1) / kMcCluster;
     a.tile_rows = kMcTileBytes / (2 * HD) > 0 ? kMcTileBytes / (2 * HD) : 1;
     const int ag = agents < kAgentGroup ? agents : kAgentGroup;
     const McLayout lay = mc_layout(HD, a.rp.dim / 2, ag, a.rows_per_cta, a.tile_rows);
