@@ -497,10 +497,10 @@ cudaError_t launch_select_f32(const float* d_k, const float* d_v, int units, int
 //     probe-list order) are spread over the cluster, 4 per CTA; the fresh probe rows are
 //     copied to the output on the way.  The rotation is linear, so a slot sums fresh and
 //     reused rows separately and rotates the reused sum once: P_s = sum(fresh) -
-//     rot(sum(reuse)).  CTA g folds its slots into the group sum
-//     Q_g = ((P_4g + P_4g+1) + P_4g+2) + P_4g+3.  Cluster barrier; CTA k adds, for the
-//     row elements e with e % 4 == k % 4 in its half, Q_0..Q_7 in order (read through
-//     distributed shared memory) and divides by b.  Cluster barrier; every CTA gathers
+//     rot(sum(reuse)).  Cluster barrier; CTA k reads, for the row elements e with
+//     e % 4 == k % 4 in its half, the 32 partials through distributed shared memory,
+//     adds the group sums Q_g = ((P_4g + P_4g+1) + P_4g+2) + P_4g+3 in order g = 0..7
+//     and divides by b.  Cluster barrier; every CTA gathers
 //     the full mean.  Cluster barrier (the buffers are reused by the next agent).
 //   phase 2: CTA k streams 1/8 of the layer's rows through a 3-stage ring of 16 KB
 //     shared-memory tiles filled by bulk asynchronous copies (TMA, completion counted
@@ -714,20 +714,22 @@ mean_correct_kernel(McArgs args) {
                     mine[k * G + g_hi] = fs1[k] - xs1[k];
                 }
             }
-            // Group sum of this CTA's four slots, in slot order: Q = ((P0 + P1) + P2) + P3.
-            __syncthreads();
-            for (int e = tid; e < HD; e += kMcThreads) ps[e] = ((ps[e] + ps[HD + e]) + ps[2 * HD + e]) + ps[3 * HD + e];
             fence_proxy_async_smem();  // the partials' stage is refilled by bulk copies later
             cluster.sync();
-            // residue-major elements [rank*SL, rank*SL + SL): the 8 group sums added in order
+            // residue-major elements [rank*SL, rank*SL + SL): the group sums
+            // Q_g = ((P_4g + P_4g+1) + P_4g+2) + P_4g+3 added in order g = 0..7
             for (int e = tid; e < SL; e += kMcThreads) {
                 const int ri = rank * SL + e;
-                float part[kMcCluster];
+                float part[32];
 #pragma unroll
-                for (int q = 0; q < kMcCluster; ++q) part[q] = cluster.map_shared_rank(ps, q)[ri];
+                for (int q = 0; q < 32; ++q) {
+                    const float* rps = cluster.map_shared_rank(ps, q / kMcSlotsPerCta);
+                    part[q] = rps[(q % kMcSlotsPerCta) * HD + ri];
+                }
                 float sum = 0.f;
 #pragma unroll
-                for (int q = 0; q < kMcCluster; ++q) sum += part[q];
+                for (int g = 0; g < kMcCluster; ++g)
+                    sum += ((part[4 * g] + part[4 * g + 1]) + part[4 * g + 2]) + part[4 * g + 3];
                 const float m = sum / (float)b;
                 mu_slice[e] = m;
                 mu_g[4 * (ri % G) + ri / G] = m;
