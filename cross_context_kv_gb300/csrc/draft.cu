@@ -8,13 +8,13 @@
 //
 // Pipeline (one unit = chunk, layer >= layer_begin, KV head; its G = steps x
 // q_heads/kv_heads <= 16 query rows share the unit's keys):
-//   1. logits:  tensor-core QK^T per 128-key tile -> logits in the workspace, plus the
-//               tile's per-query (max, sum exp) partials;
-//   2. stats:   per (unit, query) combine the tile partials into (max, sum exp);
-//   3. accum:   per key, sum over units (layer-major, then head) and queries of
-//               exp(z - max) / sum, float per unit, double across units;
-//   4. select:  top-k of the double scores (ties to the lower index);
-//   5. repair:  copy the selected rows of every layer and head from the fresh planes.
+//   1. rank:    one cluster per unit: tensor-core QK^T per 128-key tile with the logits
+//               kept in tensor memory, softmax statistics combined over the cluster,
+//               each key's mass sum_q exp(z - max_q) / sum_q to the workspace [unit][n];
+//   2. accum:   per key, the masses of the chunk's units added in double, layer-major
+//               then head;
+//   3. select:  top-k of the double scores (ties to the lower index);
+//   4. repair:  copy the selected rows of every layer and head from the fresh planes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -291,7 +291,7 @@ draft_cluster_kernel(const __grid_constant__ CUtensorMap tm_k, DcArgs args) {
     if (warp == 1) tmem_dealloc(tmem, (uint32_t)args.tmem_cols);
 }
 
-// ---- sum of the per-unit masses: grid = (ceil(n/256), chunks) ----------------------------
+// ---- 2. accum: sum of the per-unit masses, grid = (ceil(n/256), chunks) ----------------------------
 constexpr int kAccThreads = 256;
 
 __global__ void __launch_bounds__(kAccThreads)
@@ -305,7 +305,7 @@ draft_accum_kernel(const float* __restrict__ contrib, int n, long long units_per
     scores[(long long)c * n + j] = acc;
 }
 
-// ---- 4. select (double keys) --------------------------------------------------------
+// ---- 3. select (double keys) --------------------------------------------------------
 constexpr int kSelThreads2 = 1024;
 constexpr int kSelSmemKeys2 = 16384;
 
@@ -512,7 +512,7 @@ cudaError_t launch_draft(const uint16_t* k, const kvfix_kv_desc& d, const uint16
     return cudaSuccess;
 }
 
-// ---- 5. row repair: grid = (ceil(k/16), L, C) ----------------------------------------
+// ---- 4. row repair: grid = (ceil(k/16), L, C) ----------------------------------------
 constexpr int kRepThreads = 256;
 constexpr int kRepRows = 16;
 
