@@ -1044,19 +1044,22 @@ __global__ void __launch_bounds__(kRsThreads) round_stream_kernel(McArgs args, i
         cs[(kAgentGroup + a) * half + e] = s;
     }
     for (int i = tid; i < ag * words; i += kRsThreads) member[i] = 0u;
-    pdl_wait();  // the means (and, before them, the probe sets)
     __syncthreads();
+    // Probe sets and weights come from the selection, which completed before the mean
+    // kernel (this kernel's predecessor) passed its own wait: they are read before this
+    // kernel's wait, through L2.
     if (b > 0) {
         for (int i = tid; i < ag * b; i += kRsThreads) {
             const int a = i / b;
-            const int j = args.idx[plane][(long long)((a0 + a) * R + r) * b + i % b];
+            const int j = __ldcg(args.idx[plane] + (long long)((a0 + a) * R + r) * b + i % b);
             if (j >= t_lo && j < t_hi) atomicOr(&member[a * words + ((j - t_lo) >> 5)], 1u << ((j - t_lo) & 31));
         }
         for (int i = tid; i < ag * (t_hi - t_lo); i += kRsThreads) {
             const int a = i / (t_hi - t_lo), t = i % (t_hi - t_lo);
-            wts[a * kRsRows + t] = args.w[plane][(long long)((a0 + a) * R + r) * n + t_lo + t];
+            wts[a * kRsRows + t] = __ldcg(args.w[plane] + (long long)((a0 + a) * R + r) * n + t_lo + t);
         }
     }
+    pdl_wait();  // the means
     __syncthreads();
     const int per_row = ag * P, rpp = kRsThreads / per_row;
     const bool active = tid < rpp * per_row;
