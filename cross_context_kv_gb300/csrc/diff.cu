@@ -52,10 +52,10 @@ __device__ __forceinline__ bool vec_ne(const uint4& a, const uint4& b) {
 // grid = (nblk, L), one CTA per (layer, block).  Sets the mask bits of dirty entries
 // (mask pre-zeroed).  The block is cut into "pieces" (a run of rows of one plane, at most
 // 32 KB).  The master's piece is bulk-copied (TMA) into one of two master buffers and
-// compared with the same piece of every sibling, which stream through a 3-stage ring of
+// compared with the same piece of every sibling, which stream through a 4-stage ring of
 // bulk copies; a sibling's entry is dirty if any piece differs.  The master is read once.
 constexpr int kDmThreads = 512;
-constexpr int kDmStages = 3;
+constexpr int kDmStages = 4;
 constexpr int kDmPieceBytes = 32768;
 
 struct DmArgs {
