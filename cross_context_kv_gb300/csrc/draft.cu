@@ -11,8 +11,8 @@
 //   1. rank:    one cluster per unit: tensor-core QK^T per 128-key tile with the logits
 //               kept in tensor memory, softmax statistics combined over the cluster,
 //               each key's mass sum_q exp(z - max_q) / sum_q to the workspace [unit][n];
-//   2. accum:   per key, the masses of the chunk's units added in double, layer-major
-//               then head;
+//   2. accum:   per key, the masses of the chunk's units added in a fixed order
+//               (layer-major, then head) with compensated float sums;
 //   3. select:  top-k of the double scores (ties to the lower index);
 //   4. repair:  copy the selected rows of every layer and head from the fresh planes.
 #include <cuda_bf16.h>
@@ -292,7 +292,20 @@ draft_cluster_kernel(const __grid_constant__ CUtensorMap tm_k, DcArgs args) {
 }
 
 // ---- 2. accum: sum of the per-unit masses, grid = (ceil(n/256), chunks) ----------------------------
+// Units are added in order (layer-major, then head) as a compensated float pair: the
+// running sum and its rounding errors (Knuth's TwoSum), so the result carries about 48
+// significant bits, is the same on every run, and costs no double-precision arithmetic
+// (weak on this part).  Eight masses are loaded before they are added.
 constexpr int kAccThreads = 256;
+constexpr int kAccBatch = 8;
+
+__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float x) {
+    const float s = __fadd_rn(hi, x);
+    const float bb = __fsub_rn(s, hi);
+    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(x, bb));
+    hi = s;
+    lo = __fadd_rn(lo, err);
+}
 
 __global__ void __launch_bounds__(kAccThreads)
 draft_accum_kernel(const float* __restrict__ contrib, int n, long long units_per_chunk, double* scores) {
@@ -300,9 +313,17 @@ draft_accum_kernel(const float* __restrict__ contrib, int n, long long units_per
     const int j = blockIdx.x * kAccThreads + threadIdx.x;
     if (j >= n) return;
     const float* p = contrib + (long long)c * units_per_chunk * n + j;
-    double acc = 0.0;
-    for (long long u = 0; u < units_per_chunk; ++u) acc += (double)__ldg(p + u * n);
-    scores[(long long)c * n + j] = acc;
+    float hi = 0.f, lo = 0.f;
+    long long u = 0;
+    for (; u + kAccBatch <= units_per_chunk; u += kAccBatch) {
+        float v[kAccBatch];
+#pragma unroll
+        for (int q = 0; q < kAccBatch; ++q) v[q] = __ldg(p + (u + q) * n);
+#pragma unroll
+        for (int q = 0; q < kAccBatch; ++q) two_sum_acc(hi, lo, v[q]);
+    }
+    for (; u < units_per_chunk; ++u) two_sum_acc(hi, lo, __ldg(p + u * n));
+    scores[(long long)c * n + j] = (double)hi + (double)lo;
 }
 
 // ---- 3. select (double keys) --------------------------------------------------------
