@@ -1093,9 +1093,18 @@ __global__ void __launch_bounds__(kRsThreads) round_stream_kernel(McArgs args, i
         const uint16_t* tb = ring + (size_t)(k % kRsStages) * TR * HD + eo;
         const int t0 = t_lo + k * TR, tt = min(TR, t_hi - t0);
         if (active) {
-            for (int row = row_off; row < tt; row += rpp) {
-                const int tl = t0 + row - t_lo;
-                if (b > 0 && (mem[tl >> 5] >> (tl & 31) & 1u)) continue;  // probe row: written already
+            // probe bits of the tile's rows (TR <= 32: at most two bitmap words)
+            const int tl0 = t0 - t_lo;
+            uint64_t pbits = 0;
+            if (b > 0) {
+                pbits = mem[tl0 >> 5];
+                if ((tl0 & 31) + TR > 32) pbits |= (uint64_t)mem[(tl0 >> 5) + 1] << 32;
+                pbits >>= (tl0 & 31);
+            }
+            const long long ostep = (long long)rpp * op.st;
+            uint16_t* o = ob + (long long)(t0 + row_off) * op.st;
+            for (int row = row_off; row < tt; row += rpp, o += ostep) {
+                if ((pbits >> row) & 1u) continue;  // probe row: written already
                 const uint2 lo_raw = *reinterpret_cast<const uint2*>(tb + row * HD);
                 const uint2 hi_raw = *reinterpret_cast<const uint2*>(tb + row * HD + half);
                 float2 x0[2], x1[2];
@@ -1113,7 +1122,7 @@ __global__ void __launch_bounds__(kRsThreads) round_stream_kernel(McArgs args, i
                     }
                 }
                 if (b > 0) {
-                    const float wt = wb[tl];
+                    const float wt = wb[tl0 + row];
                     const float2 w2 = make_float2(wt, wt);
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
@@ -1126,7 +1135,6 @@ __global__ void __launch_bounds__(kRsThreads) round_stream_kernel(McArgs args, i
                 *reinterpret_cast<__nv_bfloat162*>(&lo_out.y) = __float22bfloat162_rn(x0[1]);
                 *reinterpret_cast<__nv_bfloat162*>(&hi_out.x) = __float22bfloat162_rn(x1[0]);
                 *reinterpret_cast<__nv_bfloat162*>(&hi_out.y) = __float22bfloat162_rn(x1[1]);
-                uint16_t* o = ob + (long long)(t0 + row) * op.st;
                 st_stream2(reinterpret_cast<uint2*>(o), lo_out);
                 st_stream2(reinterpret_cast<uint2*>(o + half), hi_out);
             }
