@@ -811,9 +811,14 @@ mean_correct_kernel(McArgs args) {
                     const bool staged = mc_stage_weights(ag_max, args.rows_per_cta);
                     const float* wb = staged ? wts + a * args.rows_per_cta - t_lo : wgt + u * n;
                     const uint32_t* mem = member + a * lay.words_member;
+                    // probe bits of the tile's rows (TR <= 32 here: at most two bitmap words)
+                    const int tl0 = t0 - t_lo;
+                    uint64_t pbits = mem[tl0 >> 5];
+                    if ((tl0 & 31) + tt > 32) pbits |= (uint64_t)mem[(tl0 >> 5) + 1] << 32;
+                    pbits >>= (tl0 & 31);
                     for (int row = row_off; row < tt; row += rpp) {
-                        const int t = t0 + row, tl = t - t_lo;
-                        if (mem[tl >> 5] >> (tl & 31) & 1u) continue;
+                        const int t = t0 + row;
+                        if ((pbits >> row) & 1u) continue;
                         const uint2 lo_raw = *reinterpret_cast<const uint2*>(tb + row * HD);
                         const uint2 hi_raw = *reinterpret_cast<const uint2*>(tb + row * HD + half);
                         float2 x0[2], x1[2];
@@ -1188,7 +1193,8 @@ cudaError_t launch_mean_correct(const McPlanes& pl, const kvfix_kv_desc& rd, con
                               dim3(kRsThreads), stream_smem, s, a, tile_rows);
     }
     a.rows_per_cta = (n + kMcCluster - 1) / kMcCluster;
-    a.tile_rows = kMcTileBytes / (2 * HD) > 0 ? kMcTileBytes / (2 * HD) : 1;
+    // at most 32 rows a tile: a tile's probe bits then fit one 64-bit window
+    a.tile_rows = max(1, min(32, kMcTileBytes / (2 * HD)));
     const int ag = agents < kAgentGroup ? agents : kAgentGroup;
     const McLayout lay = mc_layout(HD, a.rp.dim / 2, ag, a.rows_per_cta, a.tile_rows);
     const size_t smem = (size_t)lay.total;
