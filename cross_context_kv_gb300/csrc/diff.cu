@@ -294,12 +294,34 @@ diff_pack_kernel(const uint16_t* __restrict__ sk, const uint16_t* __restrict__ s
         const int l = (int)((i / nblk) % L);
         const int blk = (int)(i % nblk);
         uint4* dst = reinterpret_cast<uint4*>(payload + e * total * 8);
-        for (long long q = threadIdx.x; q < total; q += kPackThreads) {
-            int pl;
-            long long off;
-            bm.locate(q, sp, s, l, blk * bt, &pl, &off);
-            uint4 v = ld_stream(reinterpret_cast<const uint4*>((pl ? sv : sk) + off));
-            st_stream(dst + q, v);
+        const int row8 = bm.row8, rows_all = 2 * bt;  // the block's K rows, then its V rows
+        if (kPackThreads % row8 == 0) {
+            // a thread keeps one 16-byte column and walks rows; eight loads in flight
+            const int rpp = kPackThreads / row8, c8 = threadIdx.x % row8, r0 = threadIdx.x / row8;
+            const long long boff = sp.row(s, l, blk * bt) + 8 * c8;
+            for (int rb = 0; rb < rows_all; rb += 8 * rpp) {
+                uint4 v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int r = rb + r0 + j * rpp;
+                    if (r < rows_all)
+                        v[j] = ld_stream(reinterpret_cast<const uint4*>(
+                            (r < bt ? sk + boff + (long long)r * sp.st : sv + boff + (long long)(r - bt) * sp.st)));
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int r = rb + r0 + j * rpp;
+                    if (r < rows_all) st_stream(dst + (long long)r * row8 + c8, v[j]);
+                }
+            }
+        } else {
+            for (long long q = threadIdx.x; q < total; q += kPackThreads) {
+                int pl;
+                long long off;
+                bm.locate(q, sp, s, l, blk * bt, &pl, &off);
+                uint4 v = ld_stream(reinterpret_cast<const uint4*>((pl ? sv : sk) + off));
+                st_stream(dst + q, v);
+            }
         }
     }
 }
