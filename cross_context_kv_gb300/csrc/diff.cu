@@ -54,7 +54,12 @@ __device__ __forceinline__ bool vec_ne(const uint4& a, const uint4& b) {
 // 32 KB).  The master's piece is bulk-copied (TMA) into one of two master buffers and
 // compared with the same piece of every sibling, which stream through a 4-stage ring of
 // bulk copies; a sibling's entry is dirty if any piece differs.  The master is read once.
+// Warp 15 (one lane) issues the copies; warps 0..14 compare.  A comparing warp ORs its
+// verdict into the sibling's flag and releases the stage (and, after a piece's last
+// sibling, the master buffer) by an arrive on an "empty" mbarrier, so the warps never
+// wait for one another between pieces.
 constexpr int kDmThreads = 512;
+constexpr int kDmCmpWarps = kDmThreads / 32 - 1;  // comparing warps
 constexpr int kDmStages = 4;
 constexpr int kDmPieceBytes = 32768;
 
@@ -70,7 +75,7 @@ struct DmArgs {
 
 __global__ void __launch_bounds__(kDmThreads, 1) diff_mask_kernel(DmArgs a) {
     extern __shared__ __align__(128) unsigned char dsm[];
-    __shared__ __align__(8) uint64_t mfull[2], full[kDmStages];
+    __shared__ __align__(8) uint64_t mfull[2], mempty[2], full[kDmStages], empty[kDmStages];
     __shared__ int abort_flag;
     const int blk = blockIdx.x, l = blockIdx.y;
     const int S = a.sp.chunks, L = a.mp.layers, nblk = a.mp.tokens / a.bt;
@@ -81,7 +86,7 @@ __global__ void __launch_bounds__(kDmThreads, 1) diff_mask_kernel(DmArgs a) {
     unsigned char* mbuf = dsm;                                 // [2][kDmPieceBytes]
     unsigned char* ring = dsm + 2 * kDmPieceBytes;             // [kDmStages][kDmPieceBytes]
     uint32_t* flags = reinterpret_cast<uint32_t*>(ring + kDmStages * kDmPieceBytes);  // [ceil(S/32)]
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool contig_m = a.mp.st == HD, contig_s = a.sp.st == HD;
 
     // piece p: plane p / pieces_per_plane, rows [r0, r0 + rows) of the block
@@ -98,76 +103,90 @@ __global__ void __launch_bounds__(kDmThreads, 1) diff_mask_kernel(DmArgs a) {
             for (int q = 0; q < rows; ++q) bulk_g2s(dst + q * row_bytes, base + pl.row(chunk, l, t0 + q), row_bytes, bar);
         }
     };
-    auto issue_master = [&](int p) {
-        int r0;
-        const int rows = piece_rows(p, &r0);
-        const bool vpl = p >= a.pieces_per_plane;
-        mbar_arrive_expect_tx(&mfull[p & 1], row_bytes * rows);
-        copy_rows(mbuf + (p & 1) * kDmPieceBytes, vpl ? a.mv : a.mk, a.mp, 0, blk * a.bt + r0, rows, contig_m,
-                  &mfull[p & 1]);
-    };
-    auto issue_unit = [&](int u) {
-        const int p = u / S, s = u % S;
-        int r0;
-        const int rows = piece_rows(p, &r0);
-        const bool vpl = p >= a.pieces_per_plane;
-        const int slot = u % kDmStages;
-        mbar_arrive_expect_tx(&full[slot], row_bytes * rows);
-        copy_rows(ring + slot * kDmPieceBytes, vpl ? a.sv : a.sk, a.sp, s, blk * a.bt + r0, rows, contig_s,
-                  &full[slot]);
-    };
 
     for (int i = tid; i < (S + 31) / 32; i += kDmThreads) flags[i] = 0u;
     if (tid == 0) {
-        mbar_init(&mfull[0], 1);
-        mbar_init(&mfull[1], 1);
-        for (int q = 0; q < kDmStages; ++q) mbar_init(&full[q], 1);
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(&mfull[q], 1);
+            mbar_init(&mempty[q], kDmCmpWarps);
+        }
+        for (int q = 0; q < kDmStages; ++q) {
+            mbar_init(&full[q], 1);
+            mbar_init(&empty[q], kDmCmpWarps);
+        }
         fence_mbar_init();
         abort_flag = 0;
     }
     __syncthreads();
-    if (tid == 0) {
-        issue_master(0);
-        if (P > 1) issue_master(1);
-        for (int u = 0; u < min(kDmStages, units); ++u) issue_unit(u);
-    }
-    for (int u = 0; u < units; ++u) {
-        const int p = u / S, s = u % S;
-        int r0;
-        const int rows = piece_rows(p, &r0);
-        bool ok = true;
-        if (s == 0) ok = mbar_wait(&mfull[p & 1], (unsigned)(p >> 1) & 1u);
-        ok = ok && mbar_wait(&full[u % kDmStages], (unsigned)(u / kDmStages) & 1u);
-        if (!__syncthreads_and(ok)) {
-            if (tid == 0) abort_flag = 1;
-            break;
+
+    if (warp == kDmCmpWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            for (int g = 0; g < units; ++g) {
+                const int p = g / S, s = g % S;
+                int r0;
+                const int rows = piece_rows(p, &r0);
+                const bool vpl = p >= a.pieces_per_plane;
+                if (s == 0) {  // the piece's master, once its buffer's previous piece is done
+                    if (p >= 2 && !mbar_wait(&mempty[p & 1], (unsigned)((p >> 1) - 1) & 1u)) {
+                        atomicOr(&abort_flag, 1);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&mfull[p & 1], row_bytes * rows);
+                    copy_rows(mbuf + (p & 1) * kDmPieceBytes, vpl ? a.mv : a.mk, a.mp, 0, blk * a.bt + r0, rows,
+                              contig_m, &mfull[p & 1]);
+                }
+                const int slot = g % kDmStages;
+                if (g >= kDmStages && !mbar_wait(&empty[slot], (unsigned)(g / kDmStages - 1) & 1u)) {
+                    atomicOr(&abort_flag, 1);
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[slot], row_bytes * rows);
+                copy_rows(ring + slot * kDmPieceBytes, vpl ? a.sv : a.sk, a.sp, s, blk * a.bt + r0, rows, contig_s,
+                          &full[slot]);
+            }
         }
-        const uint4* m4 = reinterpret_cast<const uint4*>(mbuf + (p & 1) * kDmPieceBytes);
-        const uint4* s4 = reinterpret_cast<const uint4*>(ring + (u % kDmStages) * kDmPieceBytes);
-        const int vecs = rows * (int)(row_bytes / 16);
-        bool ne = false;
-        for (int v = tid; v < vecs; v += kDmThreads) ne |= vec_ne(m4[v], s4[v]);
-        if (__syncthreads_or(ne) && tid == 0) flags[s >> 5] |= 1u << (s & 31);
-        if (tid == 0) {  // every thread has passed the barrier: the stage (and, after the
-                         // last sibling of a piece, that piece's master buffer) may refill
-            fence_proxy_async_smem();
-            if (u + kDmStages < units) issue_unit(u + kDmStages);
-            if (s == S - 1 && p + 2 < P) issue_master(p + 2);
+    } else {
+        // ------------------------------------------------------------ compare
+        const int ct = tid;  // 0 .. 32*kDmCmpWarps - 1
+        for (int g = 0; g < units; ++g) {
+            const int p = g / S, s = g % S;
+            int r0;
+            const int rows = piece_rows(p, &r0);
+            bool ok = !abort_flag;
+            if (ok && s == 0) ok = mbar_wait(&mfull[p & 1], (unsigned)(p >> 1) & 1u);
+            ok = ok && mbar_wait(&full[g % kDmStages], (unsigned)(g / kDmStages) & 1u);
+            if (!ok) {
+                atomicOr(&abort_flag, 1);
+                break;
+            }
+            const uint4* m4 = reinterpret_cast<const uint4*>(mbuf + (p & 1) * kDmPieceBytes);
+            const uint4* s4 = reinterpret_cast<const uint4*>(ring + (g % kDmStages) * kDmPieceBytes);
+            const int vecs = rows * (int)(row_bytes / 16);
+            bool ne = false;
+            for (int v = ct; v < vecs; v += 32 * kDmCmpWarps) ne |= vec_ne(m4[v], s4[v]);
+            if (__any_sync(0xffffffffu, ne) && lane == 0) atomicOr(&flags[s >> 5], 1u << (s & 31));
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&empty[g % kDmStages]);
+                if (s == S - 1) mbar_arrive(&mempty[p & 1]);
+            }
         }
     }
     __syncthreads();
     if (abort_flag) {
         if (tid == 0) {
             atomicOr(&g_status_diff, FLAG_TIMEOUT);
+            // copies possibly in flight: wait (bounded) on both phases of every barrier
             for (int q = 0; q < 2; ++q) mbar_wait(&mfull[q], 0u), mbar_wait(&mfull[q], 1u);
             for (int q = 0; q < kDmStages; ++q) mbar_wait(&full[q], 0u), mbar_wait(&full[q], 1u);
         }
         __syncthreads();
         return;
     }
-    for (int s = tid; s < S; s += kDmThreads) {
-        if (flags[s >> 5] >> (s & 31) & 1u) {
-            const long long i = ((long long)s * L + l) * nblk + blk;
+    for (int q = tid; q < S; q += kDmThreads) {
+        if (flags[q >> 5] >> (q & 31) & 1u) {
+            const long long i = ((long long)q * L + l) * nblk + blk;
             atomicOr(&a.mask[i >> 5], 1u << (i & 31));
         }
     }
