@@ -55,6 +55,9 @@ constexpr int kDcThreads = 192;
 constexpr int kDcStages = 3;
 constexpr int kDcRows = 128;   // keys per tile (MMA M)
 constexpr int kDcQ = 16;       // query rows per unit, padded (MMA N)
+// The softmax works in base 2: exp(z - m) = 2^((z - m) log2 e), with the logits scaled by
+// log2 e once, so each term is one exp2f.
+constexpr float kLog2e = 1.4426950408889634f;
 
 static long long dc_units(const kvfix_kv_desc& d, int layer_begin) {
     const long long nl = d.layers > layer_begin ? d.layers - layer_begin : 0;
@@ -193,7 +196,7 @@ draft_cluster_kernel(const __grid_constant__ CUtensorMap tm_k, DcArgs args) {
         // ------------------------------------------------------------ softmax
         const int wq = warp & 3, ew = warp - 2;
         const int key_in_tile = 32 * wq + lane;
-        const float scale = rsqrtf((float)D);
+        const float scale = rsqrtf((float)D) * kLog2e;  // logits in base-2 units
         const bool ok = mbar_wait(&done, 0u);
         if (!ok) atomicOr(&abort_flag, 1);
         tc_fence_after();
@@ -235,7 +238,7 @@ draft_cluster_kernel(const __grid_constant__ CUtensorMap tm_k, DcArgs args) {
             tmem_wait_ld();
             if (key < n) {
 #pragma unroll
-                for (int q = 0; q < kDcQ; ++q) sm[q] += expf(__uint_as_float(v[q]) * scale - cta_m[q]);
+                for (int q = 0; q < kDcQ; ++q) sm[q] += exp2f(__uint_as_float(v[q]) * scale - cta_m[q]);
             }
         }
 #pragma unroll
@@ -263,7 +266,7 @@ draft_cluster_kernel(const __grid_constant__ CUtensorMap tm_k, DcArgs args) {
         for (int k = 0; k < kDcCluster; ++k) {
             const float mk = cluster.map_shared_rank(cta_m, k)[q];
             const float sk = cluster.map_shared_rank(cta_s, k)[q];
-            if (mk != -INFINITY) ssum += sk * expf(mk - m);
+            if (mk != -INFINITY) ssum += sk * exp2f(mk - m);
         }
         fin_m[q] = m;
         fin_inv[q] = ssum > 0.f ? 1.0f / ssum : 0.f;
@@ -272,7 +275,7 @@ draft_cluster_kernel(const __grid_constant__ CUtensorMap tm_k, DcArgs args) {
     if (warp >= 2) {
         const int wq = warp & 3;
         const int key_in_tile = 32 * wq + lane;
-        const float scale = rsqrtf((float)D);
+        const float scale = rsqrtf((float)D) * kLog2e;  // logits in base-2 units
         float* out = args.contrib + unit * (long long)n;
         for (int i = 0; i < ntiles && !abort_flag; ++i) {
             const int key = (tile0 + i) * kDcRows + key_in_tile;
@@ -280,7 +283,7 @@ draft_cluster_kernel(const __grid_constant__ CUtensorMap tm_k, DcArgs args) {
             tmem_ld16(tmem + ((uint32_t)(32 * wq) << 16) + kDcQ * i, v);
             tmem_wait_ld();
             float acc = 0.f;
-            for (int q = 0; q < args.G; ++q) acc += expf(__uint_as_float(v[q]) * scale - fin_m[q]) * fin_inv[q];
+            for (int q = 0; q < args.G; ++q) acc += exp2f(__uint_as_float(v[q]) * scale - fin_m[q]) * fin_inv[q];
             if (key < n) out[key] = acc;
         }
     }
