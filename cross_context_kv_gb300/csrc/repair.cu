@@ -342,7 +342,7 @@ __device__ void block_select(KeyAt key_at, int n, int b, uint32_t* bits, int32_t
     for (int pass = 0; hi > 0; ++pass) {
         const int wdt = hi < 8 ? hi : 8, shift = hi - wdt;
         unsigned* h = sm.hist[pass & 1];
-        // warp-aggregated histogram: one shared-memory atomic per distinct digit per warp
+        // histogram of the digits of the keys that match the prefix (plain shared atomics)
         for (int i0 = 0; i0 < n; i0 += kSelThreads) {
             const int i = i0 + tid;
             unsigned dig = 256u;  // not counted
