@@ -288,35 +288,51 @@ def time_score(kvfix, cfg, inp, steps, flush):
 
 
 def time_e2e(kvfix, cfg, inp, steps, warmup):
-    """Same step through the public API with HOST buffers: pinned host inputs copied in,
-    corrected K/V copied out, inside the timed region."""
+    """Same step through the public API with HOST buffers: every step copies its inputs in
+    from pinned host memory and its corrected K/V out to pinned host memory, inside the
+    timed region.  Consecutive steps alternate between two streams and two buffer sets, so
+    one step's copy out overlaps the next step's copy in (the link is full duplex), as a
+    serving loop would run them."""
     host = {k: inp[k].cpu().pin_memory() for k in ("k_reuse", "v_reuse", "k_fresh", "v_fresh", "delta")}
-    dev = {k: torch.empty_like(inp[k]) for k in host}
-    out = {"k": torch.empty_like(inp["k_fresh"]), "v": torch.empty_like(inp["v_fresh"]),
-           "mu_k": torch.empty(cfg.units, cfg.layers, cfg.kv_heads * cfg.head_dim, device="cuda"),
-           "mu_v": torch.empty(cfg.units, cfg.layers, cfg.kv_heads * cfg.head_dim, device="cuda")}
-    hk = torch.empty(out["k"].shape, dtype=torch.bfloat16).pin_memory()
-    hv = torch.empty(out["v"].shape, dtype=torch.bfloat16).pin_memory()
+    sets = []
+    for _ in range(2):
+        dev = {k: torch.empty_like(inp[k]) for k in host}
+        out = {"k": torch.empty_like(inp["k_fresh"]), "v": torch.empty_like(inp["v_fresh"]),
+               "mu_k": torch.empty(cfg.units, cfg.layers, cfg.kv_heads * cfg.head_dim, device="cuda"),
+               "mu_v": torch.empty(cfg.units, cfg.layers, cfg.kv_heads * cfg.head_dim, device="cuda")}
+        hk = torch.empty(out["k"].shape, dtype=torch.bfloat16).pin_memory()
+        hv = torch.empty(out["v"].shape, dtype=torch.bfloat16).pin_memory()
+        sets.append((torch.cuda.Stream(), dev, out, hk, hv))
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = hk.numel() * 2 + hv.numel() * 2
-    stream = torch.cuda.current_stream()
+    d2h = sets[0][3].numel() * 2 + sets[0][4].numel() * 2
+    main = torch.cuda.current_stream()
 
-    def one():
-        for k in host:
-            dev[k].copy_(host[k], non_blocking=True)
-        run_repair_step(kvfix, cfg, dev, out)
-        hk.copy_(out["k"], non_blocking=True)
-        hv.copy_(out["v"], non_blocking=True)
+    def one(i):
+        st, dev, out, hk, hv = sets[i % 2]
+        with torch.cuda.stream(st):
+            for k in host:
+                dev[k].copy_(host[k], non_blocking=True)
+            run_repair_step(kvfix, cfg, dev, out)
+            hk.copy_(out["k"], non_blocking=True)
+            hv.copy_(out["v"], non_blocking=True)
 
-    for _ in range(warmup):
-        one()
+    def join():
+        for st, *_ in sets:
+            main.wait_stream(st)
+
+    for i in range(warmup):
+        one(i)
+    join()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(steps):
-        one()
-    t1.record(stream)
+    t0.record(main)
+    for st, *_ in sets:
+        st.wait_stream(main)
+    for i in range(steps):
+        one(i)
+    join()
+    t1.record(main)
     torch.cuda.synchronize()
     return t0.elapsed_time(t1) / steps, h2d, d2h
 
