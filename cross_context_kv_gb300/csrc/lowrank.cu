@@ -5,7 +5,7 @@
 //
 // Blackwell path: one CTA per (unit = chunk, layer, head; range of 128-row tiles).
 //   warp 0      TMA producer: x tile (128 rows x D, two 64-column boxes, 128-byte
-//               swizzle) and A tile (128 rows x r, r*2-byte swizzle) into a 3-stage ring;
+//               swizzle) and A tile (128 rows x r, r*2-byte swizzle) into a ring of up to 5 stages;
 //   warp 1      allocates tensor memory and issues tcgen05.mma: one M=128 x N=D x K=16
 //               MMA per 16 ranks, float accumulator in TMEM (two buffers);
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, + x (read from the same
@@ -47,7 +47,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 constexpr int kLtThreads = 192;  // warp 0 producer, warp 1 MMA, warps 2..5 epilogue
-constexpr int kLtStages = 3;
+constexpr int kLtMaxStages = 5;  // ring depth, as far as shared memory allows
+constexpr int kLtSmemLimit = 227 * 1024;
 constexpr int kLtRows = 128;     // rows per tile (MMA M)
 constexpr int kLtTilesPerCta = 64;
 
@@ -57,7 +58,10 @@ struct LtCfg {
     static constexpr int kABytes = kLtRows * RANK * 2;         // A tile
     static constexpr int kStage = ((kXBytes + kABytes) + 1023) / 1024 * 1024;
     static constexpr int kBBytes = D * RANK * 2;
-    static constexpr int kSmem = 1024 /*alignment slack*/ + kLtStages * kStage + kBBytes;
+    // as many stages (up to kLtMaxStages) as fit: the ring is what keeps bytes in flight
+    static constexpr int kFit = (kLtSmemLimit - 1024 - kBBytes) / kStage;
+    static constexpr int kStages = kFit < kLtMaxStages ? kFit : kLtMaxStages;
+    static constexpr int kSmem = 1024 /*alignment slack*/ + kStages * kStage + kBBytes;
     static constexpr int kCols = 2 * D;                        // two accumulators (power of 2)
     static constexpr int kASwizzleBytes = RANK * 2;            // 32, 64 or 128
     static constexpr uint32_t kALayout = RANK == 16 ? 6u : RANK == 32 ? 4u : 2u;
@@ -74,6 +78,7 @@ lowrank_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
                   const __grid_constant__ CUtensorMap tm_a, LtArgs args) {
     using C = LtCfg<D, RANK>;
     extern __shared__ unsigned char smem_raw[];
+    constexpr int kLtStages = C::kStages;
     __shared__ __align__(8) uint64_t full[kLtStages], empty[kLtStages], tfull[2], tempty[2];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
