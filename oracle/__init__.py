@@ -64,6 +64,7 @@ def _load():
             "oracle_row_overwrite": (None, [P, P, I, I, I, I, I, P, I]),
             "oracle_diff_encode": (I64, [P, P, P, P, I, I, I, I, I, I, P, P, P, I64]),
             "oracle_diff_gather": (None, [P, P, P, P, P, I, I, I, I, I, I, P, P]),
+            "oracle_diff_restore": (None, [P, P, P, P, P, I, I, I, I, I, I, P, D, P, I64, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -284,3 +285,25 @@ def diff_gather(master_k, master_v, mask, offsets, payload, siblings: int, block
     _load().oracle_diff_gather(_p(mk), _p(mv), _p(mask), _p(offsets), _p(payload), S, L, n, H, D,
                                int(block_tokens), _p(ok), _p(ov))
     return ok, ov
+
+
+def diff_restore(master_k, master_v, mask, offsets, payload, siblings: int, block_tokens: int, delta,
+                 rope_base: float, slot_map, pool_k, pool_v):
+    """Restore every mirror into the paged pool (pool_k/pool_v [L][slots][H][D], updated in
+    place and returned): token t of mirror s goes to slot slot_map[s][t] (< 0: skipped),
+    keys rotated by delta[s]."""
+    mk, mv = _u16(master_k), _u16(master_v)
+    L, n, H, D = mk.shape
+    S = int(siblings)
+    mask = np.ascontiguousarray(mask, dtype=np.uint32)
+    offsets = np.ascontiguousarray(offsets, dtype=np.int64)
+    payload = _u16(payload) if payload.size else np.zeros((1,), np.uint16)
+    delta = np.ascontiguousarray(delta, dtype=np.int32)
+    slot_map = np.ascontiguousarray(slot_map, dtype=np.int32).reshape(S, n)
+    pk = np.array(pool_k, dtype=np.uint16, order="C", copy=True)
+    pv = np.array(pool_v, dtype=np.uint16, order="C", copy=True)
+    assert pk.shape[0] == L and pk.shape[2:] == (H, D) and pv.shape == pk.shape
+    _load().oracle_diff_restore(_p(mk), _p(mv), _p(mask), _p(offsets), _p(payload), S, L, n, H, D,
+                                int(block_tokens), _p(delta), float(rope_base), _p(slot_map),
+                                int(pk.shape[1]), _p(pk), _p(pv))
+    return pk, pv

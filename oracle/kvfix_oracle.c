@@ -537,3 +537,49 @@ EXPORT void oracle_diff_gather(const uint16_t* mk, const uint16_t* mv, const uin
         }
     }
 }
+
+/*
+ * Fused restore of mirrored caches into a paged KV pool (TokenDance, section 4.4,
+ * Algorithm 1: per layer, the master block, overwritten where the mirror's block-sparse
+ * diff touches it, keys re-aligned from the old to the new positions (RoPERecover), rows
+ * written to the paged cache through the slot mapping).  Readings: re-aligning mirror s
+ * is one rotation by delta[s] = P_new - P_old (one shift per mirror, as for a reused
+ * chunk); values are not rotated; token t of mirror s goes to row slot_map[s][t] of the
+ * pool in every layer, and a negative (or out-of-range) slot means the token is not
+ * restored.  Pool planes are [L][slots][H][D]; rows not written keep their contents.
+ */
+EXPORT void oracle_diff_restore(const uint16_t* mk, const uint16_t* mv, const uint32_t* mask,
+                                const int64_t* offsets, const uint16_t* payload, int S, int L,
+                                int n, int H, int D, int bt, const int32_t* delta, double base,
+                                const int32_t* slot_map, int64_t slots, uint16_t* pk, uint16_t* pv)
+{
+    double theta[1024];
+    oracle_rope_theta(base, D, theta);
+    int nblk = n / bt;
+    int64_t row = (int64_t)H * D;
+    int64_t blk_elems = (int64_t)bt * row;
+#pragma omp parallel for schedule(static)
+    for (int64_t st = 0; st < (int64_t)S * L * n; ++st) {
+        int64_t s = st / ((int64_t)L * n), l = (st / n) % L, t = st % n;
+        int32_t slot = slot_map[s * n + t];
+        if (slot < 0 || slot >= slots) continue;
+        int64_t i = (s * L + l) * nblk + t / bt;
+        const uint16_t *kr, *vr;
+        if (mask[i / 32] >> (i % 32) & 1u) {
+            const uint16_t* e = payload + offsets[i] * 2 * blk_elems + (t % bt) * row;
+            kr = e;
+            vr = e + blk_elems;
+        } else {
+            kr = mk + (l * n + t) * row;
+            vr = mv + (l * n + t) * row;
+        }
+        int64_t po = (l * slots + slot) * row;
+        double x[1024], y[1024];
+        for (int h = 0; h < H; ++h) {
+            for (int e = 0; e < D; ++e) x[e] = bf16_decode(kr[h * D + e]);
+            rotate_row(x, y, D, (double)delta[s], theta);
+            for (int e = 0; e < D; ++e) pk[po + h * D + e] = bf16_encode(y[e]);
+        }
+        memcpy(pv + po, vr, sizeof(uint16_t) * (size_t)row);
+    }
+}

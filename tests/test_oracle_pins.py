@@ -504,3 +504,56 @@ def test_diff_capacity_reports_need():
     _, offs, _, total = oracle.diff_encode(mk, mv, sk, sv, 16)
     _, offs2, payload, total2 = oracle.diff_encode(mk, mv, sk, sv, 16, capacity_entries=total - 1)
     assert total2 == total and np.array_equal(offs, offs2)
+
+
+# ------------------------------------------------------------ fused diff restore
+
+def _restore_case(rng, S=3, L=2, n=64, H=2, D=16, bt=16, slots=250, skip=0.1):
+    mk, mv, sk, sv = _siblings(rng, S=S, L=L, n=n, H=H, D=D, bt=bt, frac=0.5)
+    mask, offs, payload, _ = oracle.diff_encode(mk, mv, sk, sv, bt)
+    slot_map = rng.permutation(slots)[: S * n].reshape(S, n).astype(np.int32)
+    slot_map[rng.random((S, n)) < skip] = -1
+    slot_map[0, 1] = slots          # past the pool: not restored either
+    pool = np.full((L, slots, H, D), 0x1234, np.uint16)
+    return mk, mv, sk, sv, mask, offs, payload, slot_map, pool
+
+
+def test_diff_restore_zero_shift_places_each_mirror_row():
+    """Zero shift: pool row slot_map[s][t] of layer l holds mirror s's token t bit for bit
+    (keys and values); skipped and unmapped rows keep their contents."""
+    rng = np.random.default_rng(31)
+    mk, mv, sk, sv, mask, offs, payload, smap, pool = _restore_case(rng)
+    S, L, n = sk.shape[:3]
+    pk, pv = oracle.diff_restore(mk, mv, mask, offs, payload, S, 16, np.zeros(S), 1e4, smap, pool, pool)
+    hit = np.zeros(pool.shape[1], bool)
+    for s in range(S):
+        for t in range(n):
+            slot = smap[s, t]
+            if 0 <= slot < pool.shape[1]:
+                hit[slot] = True
+                assert np.array_equal(pk[:, slot], sk[s, :, t]) and np.array_equal(pv[:, slot], sv[s, :, t])
+    assert (pk[:, ~hit] == 0x1234).all() and (pv[:, ~hit] == 0x1234).all()
+    assert hit.sum() < S * n        # some tokens were skipped
+
+
+def test_diff_restore_rotates_keys_by_the_mirror_shift():
+    """Keys of mirror s are rotated by delta[s] (complex multiplication by exp(i delta theta)),
+    values are copied unrotated."""
+    rng = np.random.default_rng(32)
+    mk, mv, sk, sv, mask, offs, payload, smap, pool = _restore_case(rng, skip=0.0)
+    S, L, n, H, D = sk.shape
+    delta = np.array([0, 137, -4000], np.int32)
+    base = 5e5
+    pk, pv = oracle.diff_restore(mk, mv, mask, offs, payload, S, 16, delta, base, smap, pool, pool)
+    rot = oracle.rerope(sk, delta, base)
+    th = np.power(base, -2.0 * np.arange(D // 2) / D)
+    for s in range(S):
+        ok = smap[s] < pool.shape[1]
+        got_k = pk[:, smap[s, ok]]
+        assert np.array_equal(got_k, rot[s][:, ok])
+        assert np.array_equal(pv[:, smap[s, ok]], sv[s][:, ok])
+        x = oracle.bf16_decode(sk[s][:, ok])
+        z = (x[..., : D // 2] + 1j * x[..., D // 2:]) * np.exp(1j * float(delta[s]) * th)
+        y = oracle.bf16_decode(got_k)
+        tol = np.abs(np.concatenate([z.real, z.imag], -1)) * 2.0 ** -8 + 1e-30
+        assert (np.abs(y - np.concatenate([z.real, z.imag], -1)) <= tol).all()
