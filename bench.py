@@ -15,7 +15,7 @@ collective: weak scaling); the step time is the max over ranks.
 --impl reference times the CPU oracle (plain C, double precision) on the host cores
 on a bounded sample of the same workload, with the same metric.
 The "stages" object times the other rows of the path on their own workloads: the
-collective 8-agent round, the 16-sibling diff encode/gather, and the 70B-shaped
+collective 8-agent round, the 16-sibling diff encode/gather/restore, and the 70B-shaped
 low-rank + draft-ranked row repair.
 """
 from __future__ import annotations
@@ -372,9 +372,13 @@ def stage_diff(kvfix, peak, steps=5, warmup=2):
     mask, offsets, payload, entries = kvfix.diff_encode(inp["master_k"], inp["master_v"], inp["sib_k"],
                                                         inp["sib_v"], cfg.block_tokens)
     cap = payload.shape[0]
-    enc_ms, gat_ms = [], []
+    enc_ms, gat_ms, res_ms = [], [], []
     out_k = torch.empty_like(inp["sib_k"])
     out_v = torch.empty_like(inp["sib_v"])
+    tgt = synth.restore_inputs(cfg, "cuda")
+    pool_k = torch.empty((cfg.layers, tgt["slots"], cfg.kv_heads, cfg.head_dim), dtype=torch.bfloat16,
+                         device="cuda")
+    pool_v = torch.empty_like(pool_k)
     for s in range(warmup + steps):
         flush.zero_()
         host_lead()
@@ -390,16 +394,26 @@ def stage_diff(kvfix, peak, steps=5, warmup=2):
         kvfix.diff_gather(inp["master_k"], inp["master_v"], mask, offsets, payload, cfg.siblings,
                           cfg.block_tokens, out_k, out_v, payload_entries=entries)
         e2.record(stream)
+        flush.zero_()
+        host_lead()
+        e3, e4 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e3.record(stream)
+        kvfix.diff_restore(inp["master_k"], inp["master_v"], mask, offsets, payload, cfg.siblings,
+                           cfg.block_tokens, tgt["delta"], cfg.rope_base, tgt["slot_mapping"], pool_k,
+                           pool_v, payload_entries=entries)
+        e4.record(stream)
         torch.cuda.synchronize()
         if s >= warmup:
             enc_ms.append(e0.elapsed_time(e1))
             gat_ms.append(e1b.elapsed_time(e2))
+            res_ms.append(e3.elapsed_time(e4))
     kvfix.check_status()
     plane = inp["master_k"].numel() * 2
     blk = 2 * cfg.block_tokens * cfg.kv_heads * cfg.head_dim * 2
     enc_bytes = 2 * plane + 2 * plane * cfg.siblings + entries * blk + E // 8 + 8 * (E + 1)
     gat_bytes = 2 * plane + entries * blk + 2 * plane * cfg.siblings + E // 8 + 8 * (E + 1)
-    enc, gat = statistics.mean(enc_ms), statistics.mean(gat_ms)
+    res_bytes = gat_bytes + cfg.siblings * (cfg.tokens + 1) * 4
+    enc, gat, rst = statistics.mean(enc_ms), statistics.mean(gat_ms), statistics.mean(res_ms)
     full = 2 * plane * cfg.siblings
     stored = entries * blk + E // 8 + 8 * (E + 1)
     res = {"workload": "siblings_8b: 16 siblings of a 32-layer 8192-token 8x128 cache, 16-token blocks",
@@ -407,8 +421,11 @@ def stage_diff(kvfix, peak, steps=5, warmup=2):
            "encode": {"ms": round(enc, 4), "algorithmic_bytes": enc_bytes,
                       "GBps": round(enc_bytes / enc / 1e6, 1), "frac": round(enc_bytes / enc / 1e6 / peak, 4)},
            "gather": {"ms": round(gat, 4), "algorithmic_bytes": gat_bytes,
-                      "GBps": round(gat_bytes / gat / 1e6, 1), "frac": round(gat_bytes / gat / 1e6 / peak, 4)}}
-    del inp, mask, offsets, payload, out_k, out_v, flush
+                      "GBps": round(gat_bytes / gat / 1e6, 1), "frac": round(gat_bytes / gat / 1e6 / peak, 4)},
+           "restore": {"ms": round(rst, 4), "algorithmic_bytes": res_bytes,
+                       "GBps": round(res_bytes / rst / 1e6, 1), "frac": round(res_bytes / rst / 1e6 / peak, 4),
+                       "pool": f"{tgt['slots']} slots of 16-token pages, keys re-aligned per sibling"}}
+    del inp, mask, offsets, payload, out_k, out_v, flush, pool_k, pool_v, tgt
     torch.cuda.empty_cache()
     return res
 
@@ -621,11 +638,18 @@ def run_profile_case(name: str, iters: int = 3):
         inp = synth.diff_inputs(cfg, "cuda")
         mask, offsets, payload, entries = kvfix.diff_encode(inp["master_k"], inp["master_v"], inp["sib_k"],
                                                             inp["sib_v"], cfg.block_tokens)
+        tgt = synth.restore_inputs(cfg, "cuda")
+        pk = torch.empty((cfg.layers, tgt["slots"], cfg.kv_heads, cfg.head_dim), dtype=torch.bfloat16,
+                         device="cuda")
+        pv = torch.empty_like(pk)
         def step():
             m, o, pl, _ = kvfix.diff_encode(inp["master_k"], inp["master_v"], inp["sib_k"], inp["sib_v"],
                                             cfg.block_tokens, capacity=payload.shape[0], sync=False)
             kvfix.diff_gather(inp["master_k"], inp["master_v"], m, o, pl, cfg.siblings, cfg.block_tokens,
                               payload_entries=entries)
+            kvfix.diff_restore(inp["master_k"], inp["master_v"], m, o, pl, cfg.siblings, cfg.block_tokens,
+                               tgt["delta"], cfg.rope_base, tgt["slot_mapping"], pk, pv,
+                               payload_entries=entries)
     else:
         inp = synth.lowrank_inputs(cfg, "cuda")
         kt = torch.empty_like(inp["x_k"])

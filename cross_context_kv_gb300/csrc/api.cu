@@ -393,4 +393,45 @@ kvfix_status kvfix_diff_gather(const kvfix_bf16* master_k, const kvfix_bf16* mas
                                        (cudaStream_t)stream), fn);
 }
 
+kvfix_status kvfix_diff_restore(const kvfix_bf16* master_k, const kvfix_bf16* master_v,
+                                kvfix_kv_desc master, const uint32_t* mask,
+                                const int64_t* offsets, const kvfix_bf16* payload,
+                                int64_t payload_entries, int32_t siblings, int32_t block_tokens,
+                                const int32_t* delta, double rope_base,
+                                const int32_t* slot_mapping, kvfix_bf16* pool_k,
+                                kvfix_bf16* pool_v, kvfix_kv_desc pool, void* stream) {
+    const char* fn = "kvfix_diff_restore";
+    kvfix_status st;
+    if ((st = check_plane(master_k, master, "kvfix_diff_restore: master_k")) != KVFIX_OK) return st;
+    if ((st = check_plane(master_v, master, "kvfix_diff_restore: master_v")) != KVFIX_OK) return st;
+    if ((st = check_plane(pool_k, pool, "kvfix_diff_restore: pool_k")) != KVFIX_OK) return st;
+    if ((st = check_plane(pool_v, pool, "kvfix_diff_restore: pool_v")) != KVFIX_OK) return st;
+    if (master.chunks != 1 || pool.chunks != 1)
+        return fail(KVFIX_EINVAL, "%s: master.chunks and pool.chunks must be 1", fn);
+    if (pool.layers != master.layers || pool.kv_heads != master.kv_heads ||
+        pool.head_dim != master.head_dim)
+        return fail(KVFIX_EINVAL, "%s: the pool must have the master's layers, heads and head_dim", fn);
+    if (block_tokens < 1 || master.tokens % block_tokens)
+        return fail(KVFIX_EINVAL, "%s: block_tokens must divide tokens", fn);
+    if (siblings < 0 || siblings > 65535 || master.layers > 65535)
+        return fail(KVFIX_EINVAL, "%s: siblings and layers must be <= 65535", fn);
+    if (!mask || !offsets) return fail(KVFIX_EINVAL, "%s: mask and offsets are required", fn);
+    if (siblings > 0 && (!delta || (master.tokens > 0 && !slot_mapping)))
+        return fail(KVFIX_EINVAL, "%s: delta and slot_mapping are required", fn);
+    if (!(rope_base > 1.0) || !isfinite(rope_base))
+        return fail(KVFIX_EINVAL, "%s: rope_base must be finite and > 1", fn);
+    if (payload_entries < 0) return fail(KVFIX_EINVAL, "%s: negative payload_entries", fn);
+    if (payload_entries > 0 && (!payload || !aligned16(payload)))
+        return fail(KVFIX_EINVAL, "%s: payload must be a 16-byte aligned device pointer", fn);
+    if (overlaps(pool_k, pool, master_k, master) || overlaps(pool_v, pool, master_v, master) ||
+        overlaps(pool_k, pool, master_v, master) || overlaps(pool_v, pool, master_k, master) ||
+        overlaps(pool_k, pool, pool_v, pool))
+        return fail(KVFIX_EINVAL, "%s: pool planes overlap the master or each other", fn);
+    RopeTheta th = make_theta(rope_base, master.head_dim);
+    return launched(launch_diff_restore(master_k, master_v, master, mask, offsets, payload,
+                                        payload_entries, siblings, block_tokens, delta, th,
+                                        slot_mapping, pool_k, pool_v, pool, (cudaStream_t)stream),
+                    fn);
+}
+
 }  // extern "C"

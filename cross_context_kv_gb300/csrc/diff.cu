@@ -1,15 +1,17 @@
 // diff.cu -- block-sparse sibling diffs against one master cache (kvfix_diff_encode,
-// kvfix_diff_gather).
+// kvfix_diff_gather, kvfix_diff_restore).
 //
 // Method: TokenDance section 4.3 (master-mirror layout, block-sparse K/V diff) and
 // section 5 (touched block indices plus those blocks' K/V contents, one index list
 // shared by K and V); section 4.4, Algorithm 1 (restore = master block, overwritten
-// where the diff touches it).
+// where the diff touches it, keys re-aligned by RoPERecover, rows written to a paged
+// pool through a slot mapping).
 //
 // An entry i = (s*L + l)*nblk + blk is bt token rows x all heads x both planes.  Encode
 // compares each master block (staged in shared memory by TMA) with every sibling's block
 // streaming through a TMA ring; gather holds the master block in registers and writes
-// it (or the payload block) for every sibling.  Either way the master is read once.
+// it (or the payload block) for every sibling; restore does the same with the keys
+// rotated per sibling and the rows scattered to pool slots.  The master is read once.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -416,6 +418,186 @@ cudaError_t launch_diff_gather(const uint16_t* mk, const uint16_t* mv, const kvf
     dim3 grid(mp.tokens / bt, mp.layers);
     diff_gather_kernel<<<grid, kDiffThreads, 0, s>>>(mk, mv, mp, mask, offsets, payload,
                                                      payload_entries, siblings, bt, ok, ov, op);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------- restore
+
+constexpr int kRestoreThreads = 512;
+constexpr int kRestoreSibChunk = 16;                 // siblings per staged chunk
+constexpr int kRestoreSlotStage = 4096;              // staged (sibling, token) slots
+
+// Rotate (x_i, x_{i+D/2}) for the 8 dims of one pair item: (lo, hi) bf16 vectors; c, s,
+// m hold (cos, sin, -sin) of the 8 angles as float pairs.  Per element the same operations,
+// and so the same rounding, as kvfix_rerope (fma(x0, c, x1 * -s), fma(x1, c, x0 * s)), two
+// lanes at a time.
+__device__ __forceinline__ void restore_rotate8(uint4& lo, uint4& hi, const float2* c,
+                                                const float2* s, const float2* m) {
+    __nv_bfloat162* l2 = reinterpret_cast<__nv_bfloat162*>(&lo);
+    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&hi);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 x0 = __bfloat1622float2(l2[q]), x1 = __bfloat1622float2(h2[q]);
+        l2[q] = __float22bfloat162_rn(__ffma2_rn(x0, c[q], __fmul2_rn(x1, m[q])));
+        h2[q] = __float22bfloat162_rn(__ffma2_rn(x1, c[q], __fmul2_rn(x0, s[q])));
+    }
+}
+
+// grid = (nblk, L).  A thread owns one pair column r of the token row (the 8-wide K
+// vectors at dims 8j and D/2 + 8j of one head, which rotate together, j = r mod D/16) and
+// two V vector columns, for two rows of the block at a time; the master's pieces stay in
+// registers while every sibling is written.  Since the column is fixed, the sibling's
+// (cos, sin, -sin) of the column's 8 angles are read once for both rows.  Siblings go in
+// chunks of up to 16: per chunk the CTA stages in shared memory each sibling's payload
+// entry (or -1), its angle tables and the pool slots of the pass's rows, so the
+// per-sibling loop issues its stores without waiting on global memory.
+__global__ void __launch_bounds__(kRestoreThreads, 1)
+diff_restore_kernel(const uint16_t* __restrict__ mk, const uint16_t* __restrict__ mv, Plane mp,
+                    const uint32_t* __restrict__ mask, const int64_t* __restrict__ offsets,
+                    const uint16_t* __restrict__ payload, long long payload_entries, int S, int bt,
+                    const int32_t* __restrict__ delta, RopeTheta th,
+                    const int32_t* __restrict__ slot_map, uint16_t* pk, uint16_t* pv, Plane pp) {
+    __shared__ __align__(16) float cos_s[kRestoreSibChunk][kMaxHeadDim / 2];
+    __shared__ __align__(16) float sin_s[kRestoreSibChunk][kMaxHeadDim / 2];
+    __shared__ __align__(16) float nsin_s[kRestoreSibChunk][kMaxHeadDim / 2];
+    __shared__ int slot_s[kRestoreSlotStage];
+    __shared__ long long ent_s[kRestoreSibChunk];
+    __shared__ int rot_s[kRestoreSibChunk];
+    const int blk = blockIdx.x, l = blockIdx.y;
+    const int n = mp.tokens, nblk = n / bt, L = mp.layers;
+    const int D = mp.dim, half = D / 2, hp = D / 16;
+    const int rowe = mp.heads * D;                           // elements per token row
+    const int P = rowe / 16;                                 // pair columns per row
+    const int Pc = min(P, kRestoreThreads);                  // pair columns per segment
+    const int rpp = kRestoreThreads / Pc;                    // row slots per segment
+    const int rc = threadIdx.x % Pc, trow = threadIdx.x / Pc;
+    const bool active = trow < rpp;
+    const long long blk_elems = (long long)bt * rowe;        // elements per plane of a block
+    const int t0 = blk * bt;
+    const int slots = pp.tokens;
+    uint16_t* pkl = pk + (long long)l * pp.sl;
+    uint16_t* pvl = pv + (long long)l * pp.sl;
+    for (int c0 = 0; c0 < P; c0 += Pc) {
+        const int r = c0 + rc;
+        const bool k_ok = active && r < P;
+        const int ki = 8 * (r % hp), ke = (r / hp) * D + ki;   // angle index, element offset
+        int vo[2];
+        bool v_ok[2];
+        vo[0] = 8 * (2 * c0 + rc);
+        vo[1] = vo[0] + 8 * Pc;
+        v_ok[0] = active && vo[0] < rowe;
+        v_ok[1] = active && vo[1] < rowe;
+        for (int row0 = 0; row0 < bt; row0 += 2 * rpp) {
+            const int tpn = min(2 * rpp, bt - row0);
+            const int chunk = max(1, min(kRestoreSibChunk, kRestoreSlotStage / tpn));
+            int row[2];
+            row[0] = trow;            // rows of the pass, relative to row0
+            row[1] = trow + rpp;
+            uint4 klo[2], khi[2], vv[2][2];
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                if (!active || row[x] >= tpn) {
+                    row[x] = -1;
+                    continue;
+                }
+                const long long base = mp.row(0, l, t0 + row0 + row[x]);
+                if (k_ok) {
+                    klo[x] = ld_stream(reinterpret_cast<const uint4*>(mk + base + ke));
+                    khi[x] = ld_stream(reinterpret_cast<const uint4*>(mk + base + ke + half));
+                }
+#pragma unroll
+                for (int y = 0; y < 2; ++y)
+                    if (v_ok[y]) vv[x][y] = ld_stream(reinterpret_cast<const uint4*>(mv + base + vo[y]));
+            }
+            for (int s0 = 0; s0 < S; s0 += chunk) {
+                const int sc = min(chunk, S - s0);
+                __syncthreads();  // the previous chunk's stage is no longer read
+                for (int x = threadIdx.x; x < sc * half; x += kRestoreThreads) {
+                    const int ss = x / half, i = x % half;
+                    float c, sn;
+                    rope_cos_sin(delta[s0 + ss], th.theta[i], &c, &sn);
+                    cos_s[ss][i] = c;
+                    sin_s[ss][i] = sn;
+                    nsin_s[ss][i] = -sn;
+                }
+                for (int x = threadIdx.x; x < sc * tpn; x += kRestoreThreads) {
+                    const int ss = x / tpn, tt = x % tpn;
+                    int slot = __ldg(slot_map + (long long)(s0 + ss) * n + t0 + row0 + tt);
+                    if (slot >= slots) {
+                        atomicOr(&g_status_diff, FLAG_BOUNDS);
+                        slot = -1;
+                    }
+                    slot_s[x] = slot;
+                }
+                if (threadIdx.x < sc) {
+                    const int s = s0 + threadIdx.x;
+                    const long long i = ((long long)s * L + l) * nblk + blk;
+                    long long e = mask_bit(mask, i) ? offsets[i] : -1;
+                    if (e >= payload_entries) {
+                        atomicOr(&g_status_diff, FLAG_NOSPACE);
+                        e = -1;
+                    }
+                    ent_s[threadIdx.x] = e;
+                    rot_s[threadIdx.x] = delta[s] != 0;
+                }
+                __syncthreads();
+                for (int ss = 0; ss < sc; ++ss) {
+                    const long long e = ent_s[ss];
+                    const uint16_t* src = e >= 0 ? payload + e * 2 * blk_elems : nullptr;
+                    const bool rotate = rot_s[ss] != 0 && k_ok;
+                    float2 cc[4], sn[4], ns[4];
+                    if (rotate) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            cc[q] = reinterpret_cast<const float2*>(&cos_s[ss][ki])[q];
+                            sn[q] = reinterpret_cast<const float2*>(&sin_s[ss][ki])[q];
+                            ns[q] = reinterpret_cast<const float2*>(&nsin_s[ss][ki])[q];
+                        }
+                    }
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        if (row[x] < 0) continue;
+                        const int slot = slot_s[ss * tpn + row[x]];
+                        if (slot < 0) continue;
+                        const long long prow = (long long)slot * pp.st;
+                        const long long srow = (long long)(row0 + row[x]) * rowe;
+                        if (k_ok) {
+                            uint4 a = klo[x], b = khi[x];
+                            if (src) {
+                                a = ld_stream(reinterpret_cast<const uint4*>(src + srow + ke));
+                                b = ld_stream(reinterpret_cast<const uint4*>(src + srow + ke + half));
+                            }
+                            if (rotate) restore_rotate8(a, b, cc, sn, ns);
+                            st_stream(reinterpret_cast<uint4*>(pkl + prow + ke), a);
+                            st_stream(reinterpret_cast<uint4*>(pkl + prow + ke + half), b);
+                        }
+#pragma unroll
+                        for (int y = 0; y < 2; ++y) {
+                            if (!v_ok[y]) continue;
+                            uint4 v = vv[x][y];
+                            if (src)
+                                v = ld_stream(reinterpret_cast<const uint4*>(src + blk_elems + srow + vo[y]));
+                            st_stream(reinterpret_cast<uint4*>(pvl + prow + vo[y]), v);
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+cudaError_t launch_diff_restore(const uint16_t* mk, const uint16_t* mv, const kvfix_kv_desc& md,
+                                const uint32_t* mask, const int64_t* offsets,
+                                const uint16_t* payload, long long payload_entries, int siblings,
+                                int bt, const int32_t* delta, const RopeTheta& th,
+                                const int32_t* slot_map, uint16_t* pk, uint16_t* pv,
+                                const kvfix_kv_desc& pd, cudaStream_t s) {
+    Plane mp = plane_of(md), pp = plane_of(pd);
+    if (mp.layers == 0 || mp.tokens == 0 || siblings == 0) return cudaSuccess;
+    dim3 grid(mp.tokens / bt, mp.layers);
+    diff_restore_kernel<<<grid, kRestoreThreads, 0, s>>>(mk, mv, mp, mask, offsets, payload,
+                                                         payload_entries, siblings, bt, delta, th,
+                                                         slot_map, pk, pv, pp);
     return cudaGetLastError();
 }
 

@@ -86,4 +86,11 @@ cudaError_t launch_diff_gather(const uint16_t* mk, const uint16_t* mv, const kvf
                                int bt, uint16_t* ok, uint16_t* ov, const kvfix_kv_desc& od,
                                cudaStream_t s);
 
+cudaError_t launch_diff_restore(const uint16_t* mk, const uint16_t* mv, const kvfix_kv_desc& md,
+                                const uint32_t* mask, const int64_t* offsets,
+                                const uint16_t* payload, long long payload_entries, int siblings,
+                                int bt, const int32_t* delta, const RopeTheta& th,
+                                const int32_t* slot_map, uint16_t* pk, uint16_t* pv,
+                                const kvfix_kv_desc& pd, cudaStream_t s);
+
 }  // namespace kvfix

@@ -50,6 +50,7 @@ SIGNATURES = {
     "kvfix_draft_rank_noalloc": (ctypes.c_int, [P, D, P, I32, I32, I32, I32, P, P, P, P, D, P, P, P]),
     "kvfix_diff_encode": (ctypes.c_int, [P, P, D, P, P, D, I32, P, P, P, I64, P, P]),
     "kvfix_diff_gather": (ctypes.c_int, [P, P, D, P, P, P, I64, I32, I32, P, P, D, P]),
+    "kvfix_diff_restore": (ctypes.c_int, [P, P, D, P, P, P, I64, I32, I32, P, F64, P, P, P, D, P]),
 }
 
 
@@ -270,3 +271,30 @@ def diff_gather(master_k, master_v, mask, offsets, payload, siblings: int, block
                                  int(siblings), int(block_tokens), _ptr(out_k), _ptr(out_v),
                                  plane_desc(out_k), _stream(mk)))
     return out_k, out_v
+
+
+def diff_restore(master_k, master_v, mask, offsets, payload, siblings: int, block_tokens: int,
+                 delta, rope_base: float, slot_mapping, pool_k, pool_v,
+                 payload_entries: int | None = None):
+    """Restore every sibling into the paged pool pool_k/pool_v [layers][slots][heads][dim]
+    (written in place): token t of sibling s goes to row slot_mapping[s][t] (< 0: not
+    restored), keys rotated by delta[s]."""
+    _bf16(master_k, "master_k")
+    _bf16(master_v, "master_v")
+    _bf16(pool_k, "pool_k")
+    _bf16(pool_v, "pool_v")
+    _i32(delta, "delta")
+    _i32(slot_mapping, "slot_mapping")
+    mk = master_k.unsqueeze(0) if master_k.dim() == 4 else master_k
+    mv = master_v.unsqueeze(0) if master_v.dim() == 4 else master_v
+    if pool_k.dim() != 4 or pool_v.shape != pool_k.shape:
+        raise ValueError("pool_k and pool_v must both be [layers][slots][heads][dim]")
+    if delta.numel() != int(siblings) or slot_mapping.numel() != int(siblings) * mk.shape[2]:
+        raise ValueError("delta must hold one shift per sibling and slot_mapping one slot per "
+                         "(sibling, token)")
+    pe = payload.shape[0] if payload_entries is None else int(payload_entries)
+    _check(lib.kvfix_diff_restore(_ptr(mk), _ptr(mv), plane_desc(mk), _ptr(mask), _ptr(offsets),
+                                  _ptr(payload), pe, int(siblings), int(block_tokens), _ptr(delta),
+                                  float(rope_base), _ptr(slot_mapping), _ptr(pool_k), _ptr(pool_v),
+                                  plane_desc(pool_k.unsqueeze(0)), _stream(mk)))
+    return pool_k, pool_v

@@ -87,6 +87,8 @@ class DiffConfig:
     frac_hi: float
     noise_std: float
     seed: int
+    rope_base: float = 5e5
+    page_tokens: int = 16
 
     @property
     def blocks(self) -> int:
@@ -241,6 +243,26 @@ def diff_inputs(cfg: DiffConfig, device) -> dict:
                 (sel.float() + noise).to(BF16)
     return {"master_k": mk, "master_v": mv, "sib_k": sk, "sib_v": sv,
             "dirty_blocks": dirty_blocks}
+
+
+def restore_inputs(cfg: DiffConfig, device, skip: float = 0.0, spare_pages: int = 0) -> dict:
+    """Restore targets of the siblings: a shift delta[s] per sibling (sibling 0 keeps its
+    positions, the others ~ U{1 .. 4n}) and a paged slot mapping [S][n]: the pool holds
+    S*n/page + spare_pages pages of `page_tokens` rows, every (sibling, page) gets a
+    distinct pool page drawn at random, token t sits at row t % page of its page.  A
+    fraction `skip` of the tokens is left unmapped (slot -1)."""
+    S, n, pg = cfg.siblings, cfg.tokens, cfg.page_tokens
+    g = _gen(cfg.seed, 500, "cpu")
+    delta = torch.randint(1, 4 * n + 1, (S,), generator=g, dtype=torch.int64)
+    delta[0] = 0
+    pages = S * ((n + pg - 1) // pg) + spare_pages
+    perm = torch.randperm(pages, generator=g)[: S * ((n + pg - 1) // pg)].view(S, -1)
+    t = torch.arange(n)
+    slot = perm[:, t // pg] * pg + (t % pg)
+    if skip > 0:
+        slot[torch.rand((S, n), generator=g) < skip] = -1
+    return {"delta": delta.to(torch.int32).to(device), "slot_mapping": slot.to(torch.int32).to(device),
+            "slots": pages * pg}
 
 
 def lowrank_inputs(cfg: LowRankConfig, device, planes=("k", "v")) -> dict:

@@ -307,6 +307,38 @@ KVFIX_API kvfix_status kvfix_diff_gather(const kvfix_bf16* master_k, const kvfix
                                kvfix_bf16* out_k, kvfix_bf16* out_v, kvfix_kv_desc out,
                                void* stream);
 
+/*
+ * kvfix_diff_restore -- fused restore of every sibling into a paged KV pool.
+ * [TD] section 4.4, Algorithm 1 (per layer: load the master block, overwrite it where
+ * the sibling's block-sparse diff touches it, re-align the keys from the old to the new
+ * positions with RoPERecover, write the rows to the paged cache through the slot
+ * mapping); section 5 (the restore is one fused kernel, no intermediate full copy).
+ *
+ * Re-alignment of sibling s is one rotary shift by delta[s] = P_new - P_old (as in
+ * kvfix_rerope; values are not rotated).  Token t of sibling s is written, in every
+ * layer, to pool row slot_mapping[s*tokens + t]:
+ *     pool_k[l][slot] = rotate(delta[s], restored K row),  pool_v[l][slot] = restored V row
+ * where the restored row is the payload's if the entry is dirty, else the master's.
+ * A negative slot means the token is not restored; a slot >= pool.tokens is skipped
+ * and flagged (KVFIX_EDEVICE in kvfix_check_status).  Pool rows no slot names are left
+ * unchanged.  Slots must be distinct (two tokens naming one row race).
+ * master_*, mask, offsets, payload, payload_entries, siblings, block_tokens: as for
+ *                  kvfix_diff_gather.
+ * delta          : device int32[siblings].
+ * rope_base      : as for kvfix_rerope.
+ * slot_mapping   : device int32[siblings][tokens].
+ * pool_k, pool_v : `pool` -- chunks == 1, layers and heads x head_dim as the master's,
+ *                  tokens = the pool's rows per layer; neither may overlap the master.
+ * delta[s] = 0 copies sibling s's keys bit for bit.
+ */
+KVFIX_API kvfix_status kvfix_diff_restore(const kvfix_bf16* master_k, const kvfix_bf16* master_v,
+                                kvfix_kv_desc master, const uint32_t* mask,
+                                const int64_t* offsets, const kvfix_bf16* payload,
+                                int64_t payload_entries, int32_t siblings, int32_t block_tokens,
+                                const int32_t* delta, double rope_base,
+                                const int32_t* slot_mapping, kvfix_bf16* pool_k,
+                                kvfix_bf16* pool_v, kvfix_kv_desc pool, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,10 +23,10 @@ def declared_symbols():
     return re.findall(r"KVFIX_API\s+[\w\s\*]+?\b(kvfix_\w+)\s*\(", text)
 
 
-def test_header_declares_the_seven_calls():
+def test_header_declares_the_seven_calls_and_the_restore():
     names = set(declared_symbols())
     for call in ("kvfix_rerope", "kvfix_score_topk", "kvfix_draft_rank", "kvfix_mean_correct",
-                 "kvfix_lowrank_apply", "kvfix_diff_encode", "kvfix_diff_gather"):
+                 "kvfix_lowrank_apply", "kvfix_diff_encode", "kvfix_diff_gather", "kvfix_diff_restore"):
         assert call in names
 
 
@@ -85,6 +85,19 @@ def test_host_validation_rejects_bad_arguments(lib):
     # grouped queries beyond 16 rows per KV head
     assert L.kvfix_draft_rank(fake, dk, fake, 3, 8, 1, 4, fake, fake, None, None, dk, None, None,
                               fake, need, None) == lib.EINVAL
+    # restore: the pool must match the master's layers and lie apart from it
+    dm, far = _desc(lib, L=2, n=32), ctypes.c_void_p(1 << 30)
+    far_v = ctypes.c_void_p((1 << 30) + (1 << 24))
+    pool = _desc(lib, L=2, n=100)
+    assert L.kvfix_diff_restore(fake, fake, dm, fake, fake, None, 0, 2, 16, fake, 1e4, fake, far, far_v,
+                                _desc(lib, L=3, n=100), None) == lib.EINVAL
+    assert b"layers" in L.kvfix_last_error()
+    assert L.kvfix_diff_restore(fake, fake, dm, fake, fake, None, 0, 2, 16, fake, 1e4, fake, fake, far_v,
+                                pool, None) == lib.EINVAL
+    assert L.kvfix_diff_restore(fake, fake, dm, fake, fake, None, 0, 2, 16, None, 1e4, fake, far, far_v,
+                                pool, None) == lib.EINVAL
+    assert L.kvfix_diff_restore(fake, fake, dm, fake, fake, None, 0, 2, 16, fake, 1.0, fake, far, far_v,
+                                pool, None) == lib.EINVAL
 
 
 def test_version(lib):

@@ -96,3 +96,133 @@ def test_full_size_diff_bit_exact():
     full = 2 * inp["sib_k"].numel() * 2
     stored = entries * 2 * cfg.block_tokens * cfg.kv_heads * cfg.head_dim * 2 + mask.numel() * 4 + offsets.numel() * 8
     print(f"siblings_8b: {entries} dirty entries, compression {full / stored:.1f}x")
+
+
+# ------------------------------------------------------------ fused diff restore
+
+def _restore_setup(cfg, skip=0.1, spare_pages=3):
+    inp = synth.diff_inputs(cfg, DEV)
+    mask, offsets, payload, entries = kvfix().diff_encode(inp["master_k"], inp["master_v"], inp["sib_k"],
+                                                          inp["sib_v"], cfg.block_tokens)
+    tgt = synth.restore_inputs(cfg, DEV, skip=skip, spare_pages=spare_pages)
+    shape = (cfg.layers, tgt["slots"], cfg.kv_heads, cfg.head_dim)
+    g = torch.Generator(device=DEV).manual_seed(cfg.seed + 7)
+    pool0 = torch.randn(shape, generator=g, device=DEV).to(torch.bfloat16)  # rows not restored keep this
+    return inp, (mask, offsets, payload, entries), tgt, pool0
+
+
+def _assert_k_rotation_close(got, ref, src, delta, base, what):
+    """fp32 rotation against the oracle's fp64 one: within the K tolerance, at most 1e-3 of
+    the words differ from the oracle's, and every word lies within half a bf16 unit of the
+    exact rotation plus a float32 bound on the computation (2^-20 (|x_i| + |x_{i+D/2}|))."""
+    from helpers import assert_close_kv
+    assert_close_kv(got, ref, what)
+    ne = got != ref
+    assert ne.mean() < 1e-3, f"{what}: {ne.mean():.2e} of the words differ"
+    x = oracle.bf16_decode(src)
+    exact = oracle.rotate_f64(x, float(delta), base)
+    D = x.shape[-1]
+    mag = np.abs(x[..., : D // 2]) + np.abs(x[..., D // 2:])
+    mag = np.concatenate([mag, mag], -1)
+    y = oracle.bf16_decode(got)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(y), 1e-38))) - 7)
+    assert (np.abs(y - exact) <= 0.5 * ulp + 2.0 ** -20 * mag).all(), f"{what}: a word is outside the bound"
+
+
+@pytest.mark.parametrize("cfg", SMALL_DIFF, ids=lambda c: c.name)
+def test_diff_restore_matches_oracle(cfg):
+    inp, (mask, offsets, payload, entries), tgt, pool0 = _restore_setup(cfg)
+    pk, pv = pool0.clone(), pool0.clone()
+    kvfix().diff_restore(inp["master_k"], inp["master_v"], mask, offsets, payload, cfg.siblings,
+                         cfg.block_tokens, tgt["delta"], cfg.rope_base, tgt["slot_mapping"], pk, pv,
+                         payload_entries=entries)
+    kvfix().check_status()
+    ok, ov = oracle.diff_restore(synth.bits(inp["master_k"]), synth.bits(inp["master_v"]),
+                                 mask.cpu().numpy().view(np.uint32), offsets.cpu().numpy(),
+                                 synth.bits(payload[:max(entries, 1)]), cfg.siblings, cfg.block_tokens,
+                                 tgt["delta"].cpu().numpy(), cfg.rope_base,
+                                 tgt["slot_mapping"].cpu().numpy(), synth.bits(pool0), synth.bits(pool0))
+    assert np.array_equal(synth.bits(pv), ov)
+    gk = synth.bits(pk)
+    smap = tgt["slot_mapping"].cpu().numpy()
+    delta = tgt["delta"].cpu().numpy()
+    exact = np.ones(tgt["slots"], bool)      # unrestored rows and rows of unshifted siblings
+    sib_k = synth.bits(inp["sib_k"])
+    for s in range(cfg.siblings):
+        if delta[s] != 0:
+            on = smap[s] >= 0
+            exact[smap[s][on]] = False
+            _assert_k_rotation_close(gk[:, smap[s][on]], ok[:, smap[s][on]], sib_k[s][:, on], delta[s],
+                                     cfg.rope_base, f"{cfg.name} sibling {s}")
+    assert (smap < 0).any() and (delta == 0).any() and (delta != 0).any()
+    assert np.array_equal(gk[:, exact], ok[:, exact])
+
+
+@pytest.mark.parametrize("cfg", SMALL_DIFF, ids=lambda c: c.name)
+def test_diff_restore_equals_rerope_of_gather(cfg):
+    """Restore fuses gather, rerope and the slot scatter: the same words as those three
+    kernels run one after another."""
+    inp, (mask, offsets, payload, entries), tgt, pool0 = _restore_setup(cfg, skip=0.0, spare_pages=0)
+    pk, pv = pool0.clone(), pool0.clone()
+    kvfix().diff_restore(inp["master_k"], inp["master_v"], mask, offsets, payload, cfg.siblings,
+                         cfg.block_tokens, tgt["delta"], cfg.rope_base, tgt["slot_mapping"], pk, pv,
+                         payload_entries=entries)
+    gk, gv = kvfix().diff_gather(inp["master_k"], inp["master_v"], mask, offsets, payload, cfg.siblings,
+                                 cfg.block_tokens, payload_entries=entries)
+    rk = kvfix().rerope(gk, tgt["delta"], cfg.rope_base)
+    kvfix().check_status()
+    slot = tgt["slot_mapping"].long()
+    for s in range(cfg.siblings):
+        assert torch.equal(pk[:, slot[s]].view(torch.int16), rk[s].view(torch.int16))
+        assert torch.equal(pv[:, slot[s]].view(torch.int16), inp["sib_v"][s].view(torch.int16))
+
+
+def test_diff_restore_out_of_range_slot_is_flagged_and_skipped():
+    cfg = SMALL_DIFF[0]
+    inp, (mask, offsets, payload, entries), tgt, pool0 = _restore_setup(cfg, skip=0.0, spare_pages=0)
+    smap = tgt["slot_mapping"].clone()
+    smap[1, 5] = tgt["slots"]
+    pk, pv = pool0.clone(), pool0.clone()
+    kvfix().diff_restore(inp["master_k"], inp["master_v"], mask, offsets, payload, cfg.siblings,
+                         cfg.block_tokens, tgt["delta"], cfg.rope_base, smap, pk, pv, payload_entries=entries)
+    with pytest.raises(kvfix().KvfixError) as e:
+        kvfix().check_status()
+    assert e.value.status == kvfix().EDEVICE
+    missed = int(tgt["slot_mapping"][1, 5])
+    assert torch.equal(pk[:, missed].view(torch.int16), pool0[:, missed].view(torch.int16))
+    assert torch.equal(pv[:, missed].view(torch.int16), pool0[:, missed].view(torch.int16))
+
+
+@pytest.mark.slow
+def test_full_size_diff_restore():
+    """16 siblings at 8B shape into a paged pool, the benchmark's launch configuration:
+    every row equals the gather + rerope composition bit for bit, and sampled rows match
+    the oracle's rotation of the synthetic siblings."""
+    cfg = synth.SIBLINGS_8B
+    inp = synth.diff_inputs(cfg, DEV)
+    mask, offsets, payload, entries = kvfix().diff_encode(inp["master_k"], inp["master_v"], inp["sib_k"],
+                                                          inp["sib_v"], cfg.block_tokens)
+    tgt = synth.restore_inputs(cfg, DEV)
+    shape = (cfg.layers, tgt["slots"], cfg.kv_heads, cfg.head_dim)
+    pk = torch.empty(shape, dtype=torch.bfloat16, device=DEV)
+    pv = torch.empty_like(pk)
+    kvfix().diff_restore(inp["master_k"], inp["master_v"], mask, offsets, payload, cfg.siblings,
+                         cfg.block_tokens, tgt["delta"], cfg.rope_base, tgt["slot_mapping"], pk, pv,
+                         payload_entries=entries)
+    kvfix().check_status()
+    slot = tgt["slot_mapping"].long()
+    delta_h = tgt["delta"].cpu().numpy()
+    rng = np.random.default_rng(5)
+    for s in range(cfg.siblings):
+        rk = kvfix().rerope(inp["sib_k"][s:s + 1], tgt["delta"][s:s + 1], cfg.rope_base)
+        assert torch.equal(pk[:, slot[s]].view(torch.int16), rk[0].view(torch.int16))
+        assert torch.equal(pv[:, slot[s]].view(torch.int16), inp["sib_v"][s].view(torch.int16))
+        del rk
+        ts = np.sort(rng.choice(cfg.tokens, 24, replace=False))
+        sib = synth.bits(inp["sib_k"][s][:, ts])                      # [L][24][H][D]
+        ref = oracle.rerope(sib[None], delta_h[s:s + 1], cfg.rope_base)[0]
+        got = synth.bits(pk[:, slot[s, torch.as_tensor(ts, device=DEV)]])
+        if delta_h[s] == 0:
+            assert np.array_equal(got, sib)
+        else:
+            _assert_k_rotation_close(got, ref, sib, delta_h[s], cfg.rope_base, f"sibling {s}")
