@@ -65,6 +65,9 @@ def _load():
             "oracle_diff_encode": (I64, [P, P, P, P, I, I, I, I, I, I, P, P, P, I64]),
             "oracle_diff_gather": (None, [P, P, P, P, P, I, I, I, I, I, I, P, P]),
             "oracle_diff_restore": (None, [P, P, P, P, P, I, I, I, I, I, I, P, D, P, I64, P, P]),
+            "oracle_anchor_gate": (None, [P, P, P, I, I, I, I, I, I, I, D, D, P, P, P, P]),
+            "oracle_anchor_weights": (None, [P, P, P, I, I, I, I, I, I, D, P]),
+            "oracle_anchor_correct": (None, [P, P, P, P, I, I, I, I, I, I, I, P, D, I, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -307,3 +310,49 @@ def diff_restore(master_k, master_v, mask, offsets, payload, siblings: int, bloc
                                 int(block_tokens), _p(delta), float(rope_base), _p(slot_map),
                                 int(pk.shape[1]), _p(pk), _p(pv))
     return pk, pv
+
+
+# ------------------------------------------------------------ anchor-pool correction
+
+def anchor_gate(v_src, a_c, b_ct, k: int, T: float = 1.0, tau: float = 0.5):
+    """v_src [C][L][n][F] uint16; a_c [C][V][L][n][r]; b_ct [C][V][L][F][r] ->
+    (d [C][V], g [C][V], hbar [C], accept [C] bool)."""
+    x, a, b = _u16(v_src), _u16(a_c), _u16(b_ct)
+    C, L, n, F = x.shape
+    V, r = a.shape[1], a.shape[-1]
+    assert a.shape == (C, V, L, n, r) and b.shape == (C, V, L, F, r)
+    d = np.empty((C, V), np.float64)
+    g = np.empty_like(d)
+    hbar = np.empty(C, np.float64)
+    acc = np.empty(C, np.int32)
+    _load().oracle_anchor_gate(_p(x), _p(a), _p(b), C, V, L, n, F, r, int(k), float(T), float(tau),
+                               _p(d), _p(g), _p(hbar), _p(acc))
+    return d, g, hbar, acc.astype(bool)
+
+
+def anchor_weights(x, a_c, b_ct, T: float = 1.0):
+    """x [C][L][n][F] uint16 (one plane); a_c [C][V][L][n][r]; b_ct [C][V][L][F][r] ->
+    w [C][L][n][V] float64."""
+    x, a, b = _u16(x), _u16(a_c), _u16(b_ct)
+    C, L, n, F = x.shape
+    V, r = a.shape[1], a.shape[-1]
+    assert a.shape == (C, V, L, n, r) and b.shape == (C, V, L, F, r)
+    w = np.empty((C, L, n, V), np.float64)
+    _load().oracle_anchor_weights(_p(x), _p(a), _p(b), C, V, L, n, F, r, float(T), _p(w))
+    return w
+
+
+def anchor_correct(x, a_d, b_dt, w, heads: int, delta, rope_base: float, rotate: bool):
+    """x [C][L][n][H*D] uint16; a_d [C][V][L][n][r]; b_dt [C][V][L][H*D][r]; w [C][L][n][V]
+    -> out uint16 like x."""
+    x, a, b = _u16(x), _u16(a_d), _u16(b_dt)
+    C, L, n, F = x.shape
+    V, r = a.shape[1], a.shape[-1]
+    H = int(heads)
+    assert F % H == 0 and a.shape == (C, V, L, n, r) and b.shape == (C, V, L, F, r)
+    w = np.ascontiguousarray(w, dtype=np.float64).reshape(C, L, n, V)
+    dl = np.ascontiguousarray(delta, dtype=np.int32).reshape(C)
+    out = np.empty_like(x)
+    _load().oracle_anchor_correct(_p(x), _p(a), _p(b), _p(w), C, V, L, n, H, F // H, r, _p(dl),
+                                  float(rope_base), int(bool(rotate)), _p(out))
+    return out

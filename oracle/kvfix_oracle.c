@@ -583,3 +583,137 @@ EXPORT void oracle_diff_restore(const uint16_t* mk, const uint16_t* mv, const ui
         memcpy(pv + po, vr, sizeof(uint16_t) * (size_t)row);
     }
 }
+
+/* ------------------------------------------------------------ anchor-pool correction */
+
+/*
+ * One reconstructed row of an anchor's low-rank state (KVCMAS, section 3.3, Eq. 7: a
+ * state Z of a segment is kept as factors A_Z [n x r] and B_Z [r x F]).  The second
+ * factor is stored transposed, bt[f][c] = B_Z[c][f], so that each feature's r weights
+ * are contiguous.  rec[f] = sum_c a[c] * bt[f][c].
+ */
+static void anchor_row(const uint16_t* a, const uint16_t* bt, int F, int r, double* rec)
+{
+    for (int f = 0; f < F; ++f) {
+        double s = 0.0;
+        for (int c = 0; c < r; ++c) s += bf16_decode(a[c]) * bf16_decode(bt[(int64_t)f * r + c]);
+        rec[f] = s;
+    }
+}
+
+/*
+ * Reliability gate (KVCMAS, App. A.3 "Reliability Gate", Eq. 9-11): for each segment c,
+ *   d_v = ( sum_l || V_src^(l)[:k] - V~^(v,l)[:k] ||_F^2 )^(1/2),
+ *   g_v = exp(-d_v / T) / sum_u exp(-d_u / T),
+ *   Hbar = -sum_v g_v log2 g_v / log2 V,  accepted iff V >= 2 and Hbar <= tau.
+ * v_src [C][L][n][F] (the source value plane), ac [C][V][L][n][r], bct [C][V][L][F][r].
+ * The softmax is evaluated with the smallest distance subtracted (the same ratios);
+ * 0 log 0 = 0.  Writes d, g [C][V], hbar [C] (NaN when V < 2) and accept [C].
+ */
+EXPORT void oracle_anchor_gate(const uint16_t* v_src, const uint16_t* ac, const uint16_t* bct, int C,
+                               int V, int L, int n, int F, int r, int k, double T, double tau,
+                               double* d, double* g, double* hbar, int32_t* accept)
+{
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t cv = 0; cv < (int64_t)C * V; ++cv) {
+        int64_t c = cv / V, v = cv % V;
+        double* rec = (double*)malloc(sizeof(double) * (size_t)F);
+        double s = 0.0;
+        for (int l = 0; l < L; ++l)
+            for (int t = 0; t < k; ++t) {
+                const uint16_t* a = ac + (((c * V + v) * L + l) * (int64_t)n + t) * r;
+                const uint16_t* bt = bct + ((c * V + v) * L + l) * (int64_t)F * r;
+                const uint16_t* x = v_src + ((c * L + l) * (int64_t)n + t) * F;
+                anchor_row(a, bt, F, r, rec);
+                for (int f = 0; f < F; ++f) {
+                    double e = bf16_decode(x[f]) - rec[f];
+                    s += e * e;
+                }
+            }
+        d[cv] = sqrt(s);
+        free(rec);
+    }
+    for (int c = 0; c < C; ++c) {
+        const double* dc = d + (int64_t)c * V;
+        double* gc = g + (int64_t)c * V;
+        double dmin = dc[0], z = 0.0, h = 0.0;
+        for (int v = 1; v < V; ++v)
+            if (dc[v] < dmin) dmin = dc[v];
+        for (int v = 0; v < V; ++v) z += (gc[v] = exp(-(dc[v] - dmin) / T));
+        for (int v = 0; v < V; ++v) {
+            gc[v] /= z;
+            if (gc[v] > 0.0) h -= gc[v] * log2(gc[v]);
+        }
+        hbar[c] = V >= 2 ? h / log2((double)V) : NAN;
+        accept[c] = V >= 2 && hbar[c] <= tau;
+    }
+}
+
+/*
+ * Token-wise interpolation weights (KVCMAS, App. A.3 "Correction Weighting and Positional
+ * Alignment"): for each segment c, layer l, token t of one plane (keys in their canonical
+ * positions, as stored),
+ *   m_v = (1/F) sum_f | x[f] - (A_C,v[t] B_C,v)[f] |,   w_v = exp(-m_v / T) / sum_u exp(-m_u / T).
+ * x [C][L][n][F], ac [C][V][L][n][r], bct [C][V][L][F][r]; writes w [C][L][n][V].
+ */
+EXPORT void oracle_anchor_weights(const uint16_t* x, const uint16_t* ac, const uint16_t* bct, int C,
+                                  int V, int L, int n, int F, int r, double T, double* w)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t clt = 0; clt < (int64_t)C * L * n; ++clt) {
+        int64_t c = clt / ((int64_t)L * n), l = (clt / n) % L, t = clt % n;
+        double* rec = (double*)malloc(sizeof(double) * (size_t)F);
+        double* m = w + clt * V;
+        const uint16_t* xr = x + clt * F;
+        double mmin = 0.0, z = 0.0;
+        for (int v = 0; v < V; ++v) {
+            anchor_row(ac + (((c * V + v) * L + l) * (int64_t)n + t) * r,
+                       bct + ((c * V + v) * L + l) * (int64_t)F * r, F, r, rec);
+            double s = 0.0;
+            for (int f = 0; f < F; ++f) s += fabs(bf16_decode(xr[f]) - rec[f]);
+            m[v] = s / F;
+            if (v == 0 || m[v] < mmin) mmin = m[v];
+        }
+        for (int v = 0; v < V; ++v) z += (m[v] = exp(-(m[v] - mmin) / T));
+        for (int v = 0; v < V; ++v) m[v] /= z;
+        free(rec);
+    }
+}
+
+/*
+ * Anchor-weighted low-rank correction of the aligned source (KVCMAS Eq. 4 and Eq. 8 with
+ * the token-wise weights of App. A.3; keys re-aligned to their target positions, values
+ * not rotated):
+ *   out[t] = bf16( Align(x[t]) + sum_v w[t][v] (A_D,v[t] B_D,v) ),
+ * Align = rotate-half RoPE by delta[c] over each head (rotate != 0), else the identity.
+ * x [C][L][n][H*D], ad [C][V][L][n][r], bdt [C][V][L][H*D][r], w [C][L][n][V].
+ */
+EXPORT void oracle_anchor_correct(const uint16_t* x, const uint16_t* ad, const uint16_t* bdt,
+                                  const double* w, int C, int V, int L, int n, int H, int D, int r,
+                                  const int32_t* delta, double base, int rotate, uint16_t* out)
+{
+    double theta[1024];
+    oracle_rope_theta(base, D, theta);
+    const int F = H * D;
+#pragma omp parallel for schedule(static)
+    for (int64_t clt = 0; clt < (int64_t)C * L * n; ++clt) {
+        int64_t c = clt / ((int64_t)L * n), l = (clt / n) % L, t = clt % n;
+        double* y = (double*)malloc(sizeof(double) * (size_t)F * 3);
+        double* rec = y + F;
+        double* xd = y + 2 * F;
+        const uint16_t* xr = x + clt * F;
+        for (int f = 0; f < F; ++f) xd[f] = bf16_decode(xr[f]);
+        for (int h = 0; h < H; ++h) {
+            if (rotate) rotate_row(xd + h * D, y + h * D, D, (double)delta[c], theta);
+            else memcpy(y + h * D, xd + h * D, sizeof(double) * (size_t)D);
+        }
+        for (int v = 0; v < V; ++v) {
+            double wv = w[clt * V + v];
+            anchor_row(ad + (((c * V + v) * L + l) * (int64_t)n + t) * r,
+                       bdt + ((c * V + v) * L + l) * (int64_t)F * r, F, r, rec);
+            for (int f = 0; f < F; ++f) y[f] += wv * rec[f];
+        }
+        for (int f = 0; f < F; ++f) out[clt * F + f] = bf16_encode(y[f]);
+        free(y);
+    }
+}

@@ -557,3 +557,117 @@ def test_diff_restore_rotates_keys_by_the_mirror_shift():
         y = oracle.bf16_decode(got_k)
         tol = np.abs(np.concatenate([z.real, z.imag], -1)) * 2.0 ** -8 + 1e-30
         assert (np.abs(y - np.concatenate([z.real, z.imag], -1)) <= tol).all()
+
+
+# ------------------------------------------------------------ anchor-pool correction
+
+def _anchor_case(rng, C=2, V=3, L=2, n=7, F=16, r=4, a_std=0.5):
+    x = _bf16_bits(rng.standard_normal((C, L, n, F)))
+    a = _bf16_bits(a_std * rng.standard_normal((C, V, L, n, r)))
+    b = _bf16_bits(rng.standard_normal((C, V, L, F, r)))
+    return x, a, b
+
+
+def _recon(a, b):
+    """numpy: A [.., n, r] @ B^T for b stored [.., F, r]."""
+    return np.matmul(oracle.bf16_decode(a), np.swapaxes(oracle.bf16_decode(b), -1, -2))
+
+
+def test_anchor_gate_matches_frobenius_softmax_and_entropy():
+    """d_v against numpy's Frobenius norm of the prefix residual over layers, g against
+    scipy's softmax, the normalised entropy against scipy's entropy in bits."""
+    from scipy.special import softmax
+    from scipy.stats import entropy
+    rng = np.random.default_rng(41)
+    x, a, b = _anchor_case(rng, a_std=0.05)
+    k = 5
+    d, g, hbar, acc = oracle.anchor_gate(x, a, b, k, T=1.0, tau=0.6)
+    C, V = d.shape
+    for c in range(C):
+        res = oracle.bf16_decode(x[c])[None, :, :k] - _recon(a[c], b[c])[:, :, :k]  # [V][L][k][F]
+        dn = np.linalg.norm(res.reshape(V, -1), axis=1)
+        np.testing.assert_allclose(d[c], dn, rtol=1e-12)
+        np.testing.assert_allclose(g[c], softmax(-dn), rtol=1e-10)
+        h = entropy(g[c], base=2) / np.log2(V)
+        assert abs(hbar[c] - h) < 1e-12 and acc[c] == (h <= 0.6)
+
+
+def test_anchor_gate_special_cases():
+    rng = np.random.default_rng(42)
+    x, a, b = _anchor_case(rng, C=1, V=4)
+    same_a, same_b = np.repeat(a[:, :1], 4, 1), np.repeat(b[:, :1], 4, 1)
+    d, g, hbar, acc = oracle.anchor_gate(x, same_a, same_b, 3, tau=0.999)
+    assert np.all(g == 0.25) and abs(hbar[0] - 1.0) < 1e-15 and not acc[0]     # flat: no reuse
+    assert oracle.anchor_gate(x, same_a, same_b, 3, tau=1.0)[3][0]
+    d, g, hbar, acc = oracle.anchor_gate(x, a[:, :1], b[:, :1], 3, tau=1.0)
+    assert np.isnan(hbar[0]) and not acc[0]                                    # one anchor: dense
+    # two anchors on x = 0 reconstructing 0 and the constant e: d = (0, |e| sqrt(L k F)),
+    # g = (1, exp(-d1)) / (1 + exp(-d1)), Hbar = the binary entropy of g_0 (log2 2 = 1)
+    L, n, F, k = 1, 1, 1, 1
+    x0 = np.zeros((1, L, n, F), np.uint16)
+    aa = _bf16_bits(np.array([0.0, 1.0]).reshape(1, 2, 1, 1, 1))
+    bb = _bf16_bits(np.array([1.0, np.log(3.0)]).reshape(1, 2, 1, 1, 1))
+    d, g, hbar, acc = oracle.anchor_gate(x0, aa, bb, k, tau=0.9)
+    e = float(oracle.bf16_decode(bb)[0, 1, 0, 0, 0])
+    g0 = 1.0 / (1.0 + math.exp(-e))
+    assert d[0, 0] == 0.0 and d[0, 1] == e
+    assert abs(g[0, 0] - g0) < 1e-15
+    hb = -(g0 * math.log2(g0) + (1 - g0) * math.log2(1 - g0))
+    assert abs(hbar[0] - hb) < 1e-12 and acc[0] == (hb <= 0.9)
+    # a far anchor set against one exact match: the distribution is one-hot, entropy 0
+    xs = _bf16_bits(np.full((1, 1, 2, 4), 2.0))
+    a3 = _bf16_bits(np.array([1.0, 40.0, -40.0]).reshape(1, 3, 1, 1, 1).repeat(2, 3))
+    b3 = _bf16_bits(np.full((1, 3, 1, 4, 1), 2.0))
+    d, g, hbar, acc = oracle.anchor_gate(xs, a3, b3, 2, tau=0.01)
+    assert d[0, 0] == 0.0 and g[0, 0] == 1.0 and hbar[0] < 1e-80 and acc[0]
+
+
+def test_anchor_weights_match_library_softmax():
+    """w = softmax(-mean|x - A B|) per token, against numpy + scipy; one anchor -> 1,
+    identical anchors -> 1/V."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(43)
+    x, a, b = _anchor_case(rng, C=2, V=4, n=9, F=32, r=8)
+    w = oracle.anchor_weights(x, a, b)
+    for c in range(2):
+        m = np.abs(oracle.bf16_decode(x[c])[None] - _recon(a[c], b[c])).mean(-1)  # [V][L][n]
+        ref = softmax(-np.moveaxis(m, 0, -1), axis=-1)
+        np.testing.assert_allclose(w[c], ref, rtol=1e-12)
+    assert np.all(oracle.anchor_weights(x, a[:, :1], b[:, :1]) == 1.0)
+    w4 = oracle.anchor_weights(x, np.repeat(a[:, :1], 4, 1), np.repeat(b[:, :1], 4, 1))
+    assert np.all(w4 == 0.25)
+
+
+def test_anchor_correct_special_cases():
+    """Zero deltas give the aligned source (rerope for keys, the source for values) bit
+    for bit; one anchor of weight 1 without alignment is x + A B, against numpy."""
+    rng = np.random.default_rng(44)
+    C, V, L, n, H, D, r = 2, 3, 2, 6, 2, 16, 4
+    x = _bf16_bits(rng.standard_normal((C, L, n, H * D)))
+    ad = np.zeros((C, V, L, n, r), np.uint16)
+    bd = _bf16_bits(rng.standard_normal((C, V, L, H * D, r)))
+    w = rng.dirichlet(np.ones(V), (C, L, n))
+    delta = np.array([300, -7])
+    out = oracle.anchor_correct(x, ad, bd, w, H, delta, 1e4, rotate=True)
+    assert np.array_equal(out, oracle.rerope(x.reshape(C, L, n, H, D), delta, 1e4).reshape(x.shape))
+    assert np.array_equal(oracle.anchor_correct(x, ad, bd, w, H, delta, 1e4, rotate=False), x)
+    a1 = _bf16_bits(0.3 * rng.standard_normal((C, 1, L, n, r)))
+    out = oracle.anchor_correct(x, a1, bd[:, :1], np.ones((C, L, n, 1)), H, delta, 1e4, rotate=False)
+    ref = oracle.bf16_decode(x) + _recon(a1, bd[:, :1])[:, 0]
+    assert np.mean(out == _bf16_bits(ref)) > 0.999
+    np.testing.assert_allclose(oracle.bf16_decode(out), ref, rtol=2.0 ** -8, atol=1e-6)
+
+
+def test_anchor_correct_is_weighted_sum_of_anchor_deltas():
+    """Weights put the anchors' deltas together linearly: against the numpy sum of
+    w_v (A_v B_v) added to the rotated source."""
+    rng = np.random.default_rng(45)
+    C, V, L, n, H, D, r = 1, 4, 2, 5, 2, 16, 8
+    x = _bf16_bits(rng.standard_normal((C, L, n, H * D)))
+    ad = _bf16_bits(0.2 * rng.standard_normal((C, V, L, n, r)))
+    bd = _bf16_bits(rng.standard_normal((C, V, L, H * D, r)))
+    w = rng.dirichlet(np.ones(V), (C, L, n))
+    out = oracle.anchor_correct(x, ad, bd, w, H, [55], 5e5, rotate=True)
+    rot = oracle.rotate_f64(oracle.bf16_decode(x).reshape(C, L, n, H, D), 55, 5e5).reshape(x.shape)
+    ref = rot + np.einsum("clnv,cvlnf->clnf", w, _recon(ad, bd))
+    np.testing.assert_allclose(oracle.bf16_decode(out), ref, rtol=2.0 ** -8, atol=1e-6)
