@@ -1,0 +1,809 @@
+// anchor.cu -- anchor-pool correction of a reused segment (kvfix_anchor_gate,
+// kvfix_anchor_correct).
+//
+// Method: KVCMAS section 3.3 (anchors keep their base cache and delta corrections as
+// low-rank factors, Eq. 7; the transition correction is the weighted sum of the anchors'
+// deltas, Eq. 8, applied to the aligned source cache, Eq. 4) and App. A.3 (reliability
+// gate on the value states over a prefix, Eq. 9-11; token-wise interpolation weights
+// from the mean absolute source-to-anchor distance, keys and values separately, softmax
+// with T = 1; keys matched in canonical positions and then aligned to their targets).
+//
+// Factor layout (one plane): A [segment][anchor][layer][token][r], and the second factor
+// stored transposed, Bt [segment][anchor][layer][feature][r] (feature = head*D + dim),
+// so that both MMA operands are K-major with K = r.
+//
+// Blackwell path, three kernels:
+//   anchor_dist_kernel   per (128-row tile, layer, plane and segment): the anchors' base
+//                        rows A_v B_v are built 16 features at a time by tcgen05.mma
+//                        (M = 128 rows, N = 16, K = r) into tensor memory, while eight
+//                        epilogue warps fold |x - rec| (token weights) or (x - rec)^2 (gate)
+//                        into per-row, per-anchor sums; x and Bt stream through a TMA ring.
+//   anchor_gate_kernel   per segment: the gate's distances, softmax, normalised entropy.
+//   anchor_apply_kernel  per (tile, layer, plane and segment): the anchors' delta factors
+//                        are scaled by the token weights in shared memory and multiplied by
+//                        the stacked Bt (K = V*r) head by head into tensor memory; the
+//                        epilogue adds the aligned source (keys rotated) and stores by TMA.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tc.cuh"
+
+namespace kvfix {
+
+static __device__ unsigned int g_status_anchor;
+
+unsigned read_status_anchor(cudaStream_t stream) {
+    unsigned h = 0, zero = 0;
+    cudaMemcpyFromSymbolAsync(&h, g_status_anchor, sizeof h, 0, cudaMemcpyDeviceToHost, stream);
+    cudaMemcpyToSymbolAsync(g_status_anchor, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, stream);
+    cudaStreamSynchronize(stream);
+    return h;
+}
+
+__device__ __forceinline__ int anchor_vload(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
+
+// Named barrier over the epilogue warps that also ORs a predicate across them, so that a
+// failed wait in any of them stops all of them at the same step.
+template <int ID, int N>
+__device__ __forceinline__ bool bar_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+        " barrier.cta.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "n"(ID), "n"(N)
+        : "memory");
+    return r != 0;
+}
+
+constexpr int kAnRows = 128;          // rows per tile (MMA M)
+constexpr int kAnMaxAnchors = 16;
+constexpr int kAnSmemLimit = 227 * 1024;
+
+// ------------------------------------------------------------------ distances
+
+constexpr int kAdThreads = 320;       // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kAdCols = 16;           // features per chunk (MMA N)
+constexpr int kAdMaxStages = 8;
+constexpr int kAdXBytes = kAnRows * kAdCols * 2;  // x chunk, unswizzled
+
+enum { kAdWeights = 0, kAdGate = 1 };
+
+struct AdArgs {
+    int V, L, n, F, C;
+    int rows;            // rows of the tile range: n (weights) or the gate prefix k
+    int tiles;           // ceil(rows / 128)
+    int stages, slots;   // ring depth, tensor-memory buffers
+    int stage_bytes, bbox_bytes;
+    int tmem_cols;       // power of two >= slots * V * 16
+    float inv_T;
+    float* w[2];         // weights mode: [C][L][n][V] per plane
+    float* partial;      // gate mode: [C][L][tiles][V]
+    const int32_t* accept;  // weights mode: [C] or null; rejected segments are skipped
+};
+
+template <int R>
+struct AdCfg {
+    static constexpr int kRowBytes = R * 2;                       // 32, 64 or 128
+    static constexpr uint32_t kLayout = R == 16 ? 6u : R == 32 ? 4u : 2u;
+    static constexpr int kABytes = kAnRows * kRowBytes;           // one anchor's A tile
+    static constexpr int kBBytes = kAdCols * kRowBytes;           // one anchor's Bt chunk
+    static constexpr int kBBox = kBBytes < 1024 ? 1024 : kBBytes; // swizzle-atom aligned slot
+};
+
+// grid = (tiles, L, planes * C).  MODE kAdWeights: both planes (z = plane * C + c), every
+// row; writes the softmax of -mean|x - rec_v| / T per row.  MODE kAdGate: the value plane,
+// rows < k; writes per-tile sums of (x - rec_v)^2.
+template <int R, int MODE>
+__global__ void __launch_bounds__(kAdThreads, 1)
+anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CUtensorMap tm_x1,
+                   const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+                   const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_b1,
+                   AdArgs args) {
+    using K = AdCfg<R>;
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t full[kAdMaxStages], empty[kAdMaxStages], tfull[4], tempty[4], afull;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    __shared__ float red[kAnRows][kAnMaxAnchors + 1];
+    __shared__ float gsum[4][kAnMaxAnchors];
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int V = args.V;
+    unsigned char* asm_ = smem;                             // V A tiles
+    unsigned char* ring = smem + V * K::kABytes;            // stages: x chunk, then V Bt chunks
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x, l = blockIdx.y;
+    const int plane = MODE == kAdGate ? 0 : (int)blockIdx.z / args.C;
+    const int c = (int)blockIdx.z % args.C;
+    const CUtensorMap* mx = plane ? &tm_x1 : &tm_x0;
+    const CUtensorMap* ma = plane ? &tm_a1 : &tm_a0;
+    const CUtensorMap* mb = plane ? &tm_b1 : &tm_b0;
+    if (MODE == kAdWeights && args.accept && args.accept[c] == 0) return;
+    const int t0 = tile * kAnRows;
+    const int chunks = args.F / kAdCols;
+    const int S = args.stages, NS = args.slots;
+    const uint32_t slot_cols = (uint32_t)(V * kAdCols);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1 + 8);  // the MMA's commit and the eight epilogue warps
+        }
+        for (int a = 0; a < NS; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 8);
+        }
+        mbar_init(&afull, 1);
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_slot, (uint32_t)args.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&afull, (unsigned)(V * K::kABytes));
+            for (int v = 0; v < V; ++v)
+                tma_load_2d(asm_ + v * K::kABytes, ma, 0, ((c * V + v) * args.L + l) * args.n + t0, &afull);
+            for (int i = 0; i < chunks && !anchor_vload(&abort_flag); ++i) {
+                const int s = i % S;
+                if (i >= S && !mbar_wait(&empty[s], (unsigned)(i / S - 1) & 1u)) {
+                    atomicOr(&abort_flag, 1);
+                    break;
+                }
+                unsigned char* st = ring + s * args.stage_bytes;
+                mbar_arrive_expect_tx(&full[s], (unsigned)(kAdXBytes + V * K::kBBytes));
+                tma_load_4d(st, mx, i * kAdCols, t0, l, c, &full[s]);
+                for (int v = 0; v < V; ++v)
+                    tma_load_2d(st + kAdXBytes + v * args.bbox_bytes, mb, 0,
+                                ((c * V + v) * args.L + l) * args.F + i * kAdCols, &full[s]);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc_idesc_bf16(kAnRows, kAdCols);
+            bool ok = mbar_wait(&afull, 0u);
+            if (!ok) atomicOr(&abort_flag, 1);
+            tc_fence_after();
+            for (int i = 0; ok && i < chunks && !anchor_vload(&abort_flag); ++i) {
+                const int s = i % S, a = i % NS;
+                if (!mbar_wait(&full[s], (unsigned)(i / S) & 1u) ||
+                    (i >= NS && !mbar_wait(&tempty[a], (unsigned)(i / NS - 1) & 1u))) {
+                    atomicOr(&abort_flag, 1);
+                    break;
+                }
+                tc_fence_after();
+                const unsigned char* bt = ring + s * args.stage_bytes + kAdXBytes;
+                for (int v = 0; v < V; ++v) {
+#pragma unroll
+                    for (int kk = 0; kk < R / 16; ++kk) {
+                        const uint64_t adesc = tc_smem_desc(asm_ + v * K::kABytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
+                        const uint64_t bdesc = tc_smem_desc(bt + v * args.bbox_bytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
+                        tc_mma_bf16(tmem + a * slot_cols + v * kAdCols, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+                    }
+                }
+                tc_commit(&tfull[a]);
+                tc_commit(&empty[s]);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - 2;              // 0..7
+        const int wq = warp & 3;              // TMEM lane quarter this warp may read
+        const int half = ew >> 2;             // which 8 of the chunk's 16 features
+        const int m = 32 * wq + lane;         // tile row of this thread
+        const bool row_ok = t0 + m < args.rows;
+        float acc[kAnMaxAnchors];
+#pragma unroll
+        for (int v = 0; v < kAnMaxAnchors; ++v) acc[v] = 0.f;
+        for (int i = 0; i < chunks; ++i) {
+            const int s = i % S, a = i % NS;
+            bool ok = !anchor_vload(&abort_flag) && mbar_wait(&tfull[a], (unsigned)(i / NS) & 1u) &&
+                      mbar_wait(&full[s], (unsigned)(i / S) & 1u);
+            if (!ok) {
+                atomicOr(&abort_flag, 1);
+                break;
+            }
+            tc_fence_after();
+            const uint4 xv = *reinterpret_cast<const uint4*>(ring + s * args.stage_bytes + m * (kAdCols * 2) + half * 16);
+            float xf[8];
+            unpack8(xv, xf);
+            const uint32_t tbase = tmem + ((uint32_t)(32 * wq) << 16) + a * slot_cols + half * 8;
+#pragma unroll
+            for (int v = 0; v < kAnMaxAnchors; v += 2) {
+                if (v >= V) break;
+                uint32_t r0[8], r1[8];
+                tmem_ld8(tbase + v * kAdCols, r0);
+                if (v + 1 < V) tmem_ld8(tbase + (v + 1) * kAdCols, r1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float d0 = xf[e] - __uint_as_float(r0[e]);
+                    if (MODE == kAdGate) acc[v] = fmaf(d0, d0, acc[v]);
+                    else acc[v] += fabsf(d0);
+                }
+                if (v + 1 < V) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float d1 = xf[e] - __uint_as_float(r1[e]);
+                        if (MODE == kAdGate) acc[v + 1] = fmaf(d1, d1, acc[v + 1]);
+                        else acc[v + 1] += fabsf(d1);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&tempty[a]);
+                mbar_arrive(&empty[s]);
+            }
+        }
+        // both halves of a row: the second half adds its sums into the first's (the loops
+        // run to the fixed bound so that the sums stay in registers)
+        if (half == 1) {
+#pragma unroll
+            for (int v = 0; v < kAnMaxAnchors; ++v)
+                if (v < V) red[m][v] = acc[v];
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (half == 0 && !anchor_vload(&abort_flag)) {
+#pragma unroll
+            for (int v = 0; v < kAnMaxAnchors; ++v)
+                if (v < V) acc[v] += red[m][v];
+            if (MODE == kAdWeights) {
+                if (row_ok) {
+                    const float invF = 1.f / (float)args.F;
+                    float mmin = acc[0] * invF;
+#pragma unroll
+                    for (int v = 1; v < kAnMaxAnchors; ++v)
+                        if (v < V) mmin = fminf(mmin, acc[v] * invF);
+                    float z = 0.f;
+#pragma unroll
+                    for (int v = 0; v < kAnMaxAnchors; ++v)
+                        if (v < V) {
+                            acc[v] = expf(-(acc[v] * invF - mmin) * args.inv_T);
+                            z += acc[v];
+                        }
+                    const float iz = 1.f / z;
+                    float* wr = (plane ? args.w[1] : args.w[0]) + (((long long)c * args.L + l) * args.n + t0 + m) * V;
+#pragma unroll
+                    for (int v = 0; v < kAnMaxAnchors; ++v)
+                        if (v < V) wr[v] = acc[v] * iz;
+                }
+            } else {
+                // per-tile sums over the rows, in a fixed order: lanes, then the four warps
+#pragma unroll
+                for (int v = 0; v < kAnMaxAnchors; ++v) {
+                    if (v < V) {
+                        float x = row_ok ? acc[v] : 0.f;
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                        if (lane == 0) gsum[wq][v] = x;
+                    }
+                }
+            }
+        }
+        if (MODE == kAdGate) {
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (ew == 0 && lane < V && !anchor_vload(&abort_flag)) {
+                const float x = ((gsum[0][lane] + gsum[1][lane]) + gsum[2][lane]) + gsum[3][lane];
+                args.partial[(((long long)c * args.L + l) * args.tiles + tile) * V + lane] = x;
+            }
+        }
+    }
+    __syncthreads();
+    if (abort_flag && threadIdx.x == 0) atomicOr(&g_status_anchor, FLAG_TIMEOUT);
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, (uint32_t)args.tmem_cols);
+}
+
+// ------------------------------------------------------------------ gate
+
+// One warp per segment: d_v = sqrt(sum over layers and tiles of the per-tile sums, in
+// that order, in double), g = softmax(-d / T), Hbar = -sum g log2 g / log2 V, accepted
+// iff V >= 2 and Hbar <= tau.
+__global__ void anchor_gate_kernel(const float* __restrict__ partial, int V, int L, int tiles, double T,
+                                   double tau, double* d, double* g, double* hbar, int32_t* accept) {
+    const int c = blockIdx.x, v = threadIdx.x;
+    double dv = 0.0;
+    if (v < V) {
+        double s = 0.0;
+        for (int lt = 0; lt < L * tiles; ++lt) s += (double)partial[((long long)c * L * tiles + lt) * V + v];
+        dv = sqrt(s);
+        d[(long long)c * V + v] = dv;
+    }
+    double dmin = v < V ? dv : 1e308;
+    for (int o = 16; o > 0; o >>= 1) dmin = fmin(dmin, __shfl_xor_sync(0xffffffffu, dmin, o));
+    const double e = v < V ? exp(-(dv - dmin) / T) : 0.0;
+    double z = e;
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    const double gv = e / z;
+    if (v < V) g[(long long)c * V + v] = gv;
+    double h = (v < V && gv > 0.0) ? -gv * log2(gv) : 0.0;
+    for (int o = 16; o > 0; o >>= 1) h += __shfl_xor_sync(0xffffffffu, h, o);
+    if (v == 0) {
+        const double hb = V >= 2 ? h / log2((double)V) : __longlong_as_double(0x7ff8000000000000ll);
+        hbar[c] = hb;
+        accept[c] = (V >= 2 && hb <= tau) ? 1 : 0;
+    }
+}
+
+// ------------------------------------------------------------------ apply
+
+constexpr int kApThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kApMaxB = 8;            // Bt ring entries (one anchor's head slab each)
+constexpr int kApMaxX = 3;            // x head slabs
+
+struct ApArgs {
+    int V, L, n, H, C;
+    int nb, nx;                       // Bt ring entries and x slabs in use
+    const float* w[2];                // [C][L][n][V] per plane
+    const int32_t* accept;            // [C] or null
+    const int32_t* delta;             // [C]
+    uint16_t* out[2];                 // only to skip a missing plane
+};
+
+template <int D, int R>
+struct ApCfg {
+    static constexpr int kRowBytes = R * 2;
+    static constexpr uint32_t kLayout = R == 16 ? 6u : R == 32 ? 4u : 2u;
+    static constexpr int kABytes = kAnRows * kRowBytes;   // one anchor's A tile
+    static constexpr int kXBytes = kAnRows * D * 2;       // one head slab of x (64-feature boxes)
+    static constexpr int kBBytes = D * kRowBytes;         // one anchor's Bt rows of one head
+    static constexpr int kBSlot = kBBytes < 1024 ? 1024 : kBBytes;
+};
+
+// grid = (tiles, L, 2 * C), z = plane * C + c (plane 0 keys, rotated; 1 values).
+template <int D, int R>
+__global__ void __launch_bounds__(kApThreads, 1)
+anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CUtensorMap tm_x1,
+                    const __grid_constant__ CUtensorMap tm_o0, const __grid_constant__ CUtensorMap tm_o1,
+                    const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+                    const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_b1,
+                    ApArgs args, RopeTheta th) {
+    using K = ApCfg<D, R>;
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t afull, ascaled, xfull[kApMaxX], xempty[kApMaxX], bfull[kApMaxB], bempty[kApMaxB],
+        tfull[2], tempty[2];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    __shared__ float2 tab[D / 2];
+    const int tile = blockIdx.x, l = blockIdx.y;
+    const int plane = (int)blockIdx.z / args.C, c = (int)blockIdx.z % args.C;
+    if ((plane ? args.out[1] : args.out[0]) == nullptr) return;
+    if (args.accept && args.accept[c] == 0) return;  // rejected segment: left to a dense prefill
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int V = args.V, H = args.H, NB = args.nb, NX = args.nx;
+    unsigned char* asm_ = smem;                                  // V scaled A tiles
+    unsigned char* xs = asm_ + V * K::kABytes;                   // NX head slabs of x
+    unsigned char* bs = xs + NX * K::kXBytes;                    // Bt ring
+    const CUtensorMap* mx = plane ? &tm_x1 : &tm_x0;
+    const CUtensorMap* mo = plane ? &tm_o1 : &tm_o0;
+    const CUtensorMap* ma = plane ? &tm_a1 : &tm_a0;
+    const CUtensorMap* mb = plane ? &tm_b1 : &tm_b0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = tile * kAnRows;
+    const int F = H * D;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&afull, 1);
+        mbar_init(&ascaled, 4);
+        for (int i = 0; i < NX; ++i) {
+            mbar_init(&xfull[i], 1);
+            mbar_init(&xempty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 4);
+        }
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(&bfull[i], 1);
+            mbar_init(&bempty[i], 1);
+        }
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_slot, 2 * D);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&afull, (unsigned)(V * K::kABytes));
+            for (int v = 0; v < V; ++v)
+                tma_load_2d(asm_ + v * K::kABytes, ma, 0, ((c * V + v) * args.L + l) * args.n + t0, &afull);
+            for (int h = 0; h < H && !anchor_vload(&abort_flag); ++h) {
+                const int xi = h % NX;
+                if (h >= NX && !mbar_wait(&xempty[xi], (unsigned)(h / NX - 1) & 1u)) {
+                    atomicOr(&abort_flag, 1);
+                    break;
+                }
+                mbar_arrive_expect_tx(&xfull[xi], (unsigned)K::kXBytes);
+                for (int b = 0; b < D / 64; ++b)
+                    tma_load_4d(xs + xi * K::kXBytes + b * (kAnRows * 128), mx, h * D + 64 * b, t0, l, c, &xfull[xi]);
+                bool ok = true;
+                for (int v = 0; v < V; ++v) {
+                    const int q = h * V + v, e = q % NB;
+                    if (q >= NB && !mbar_wait(&bempty[e], (unsigned)(q / NB - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bfull[e], (unsigned)K::kBBytes);
+                    tma_load_2d(bs + e * K::kBSlot, mb, 0, ((c * V + v) * args.L + l) * F + h * D, &bfull[e]);
+                }
+                if (!ok) {
+                    atomicOr(&abort_flag, 1);
+                    break;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc_idesc_bf16(kAnRows, D);
+            bool ok = mbar_wait(&ascaled, 0u);
+            for (int h = 0; ok && h < H && !anchor_vload(&abort_flag); ++h) {
+                const int a = h & 1;
+                if (h >= 2 && !mbar_wait(&tempty[a], (unsigned)(h / 2 - 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int v = 0; v < V; ++v) {
+                    const int q = h * V + v, e = q % NB;
+                    if (!mbar_wait(&bfull[e], (unsigned)(q / NB) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < R / 16; ++kk) {
+                        const uint64_t adesc = tc_smem_desc(asm_ + v * K::kABytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
+                        const uint64_t bdesc = tc_smem_desc(bs + e * K::kBSlot + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
+                        tc_mma_bf16(tmem + a * D, adesc, bdesc, idesc, (v > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&bempty[e]);
+                }
+                if (ok) tc_commit(&tfull[a]);
+            }
+            if (!ok) atomicOr(&abort_flag, 1);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int wq = warp & 3;
+        const int m = 32 * wq + lane;        // tile row
+        const int et = threadIdx.x - 64;     // 0..127
+        const bool row_ok = t0 + m < args.n;
+        if (plane == 0)
+            for (int i = et; i < D / 2; i += 128) {
+                float cs, sn;
+                rope_cos_sin(args.delta[c], th.theta[i], &cs, &sn);
+                tab[i] = make_float2(cs, sn);
+            }
+        // scale row m of every anchor's A tile by the token's weight (bf16, in place: the
+        // swizzle only permutes 16-byte pieces within the row)
+        bool ok = mbar_wait(&afull, 0u);
+        if (ok) {
+            const float* wr = (plane ? args.w[1] : args.w[0]) + (((long long)c * args.L + l) * args.n + (row_ok ? t0 + m : 0)) * V;
+            for (int v = 0; v < V; ++v) {
+                const float wv = row_ok ? wr[v] : 0.f;
+                uint4* p = reinterpret_cast<uint4*>(asm_ + v * K::kABytes + m * K::kRowBytes);
+#pragma unroll
+                for (int q = 0; q < K::kRowBytes / 16; ++q) {
+                    float f[8];
+                    unpack8(p[q], f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] *= wv;
+                    p[q] = pack8(f);
+                }
+            }
+        } else {
+            atomicOr(&abort_flag, 1);
+        }
+        fence_proxy_async_smem();  // generic writes of A -> read by the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ascaled);
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the angle table is complete
+        for (int h = 0; h < H; ++h) {
+            const int a = h & 1, xi = h % NX;
+            ok = ok && !anchor_vload(&abort_flag) && mbar_wait(&tfull[a], (unsigned)(h / 2) & 1u) &&
+                 mbar_wait(&xfull[xi], (unsigned)(h / NX) & 1u);
+            if (!ok) atomicOr(&abort_flag, 1);
+            tc_fence_after();
+            unsigned char* slab = xs + xi * K::kXBytes;
+            if (ok) {
+                const uint32_t tb = tmem + ((uint32_t)(32 * wq) << 16) + a * D;
+#pragma unroll
+                for (int j = 0; j < D / 64; ++j) {
+                    // dims [32j, 32j + 32) and their partners [D/2 + 32j, D/2 + 32j + 32)
+                    uint32_t lo[32], hi[32];
+                    tmem_ld32(tb + 32 * j, lo);
+                    tmem_ld32(tb + D / 2 + 32 * j, hi);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int f0 = 32 * j + 8 * q, f1 = D / 2 + f0;  // first dims of the two pieces
+                        uint4* p0 = reinterpret_cast<uint4*>(slab + (f0 / 64) * (kAnRows * 128) + m * 128 +
+                                                             ((((f0 % 64) / 8) ^ (m & 7)) << 4));
+                        uint4* p1 = reinterpret_cast<uint4*>(slab + (f1 / 64) * (kAnRows * 128) + m * 128 +
+                                                             ((((f1 % 64) / 8) ^ (m & 7)) << 4));
+                        float x0[8], x1[8];
+                        unpack8(*p0, x0);
+                        unpack8(*p1, x1);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            float y0 = x0[e], y1 = x1[e];
+                            if (plane == 0) {
+                                const float2 cs = tab[f0 + e];
+                                y0 = __fmaf_rn(x0[e], cs.x, __fmul_rn(x1[e], -cs.y));
+                                y1 = __fmaf_rn(x1[e], cs.x, __fmul_rn(x0[e], cs.y));
+                            }
+                            x0[e] = y0 + __uint_as_float(lo[8 * q + e]);
+                            x1[e] = y1 + __uint_as_float(hi[8 * q + e]);
+                        }
+                        *p0 = pack8(x0);
+                        *p1 = pack8(x1);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[a]);
+            fence_proxy_async_smem();  // epilogue writes -> TMA store reads
+            if (bar_any<1, 128>(!ok || anchor_vload(&abort_flag))) ok = false;  // same verdict in all
+            if (et == 0) {
+                if (ok)
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_store_4d(mo, slab + b * (kAnRows * 128), h * D + 64 * b, t0, l, c);
+                bulk_commit();
+                bulk_wait_read<1>();  // the previous head's store has read its slab
+                if (h >= 1) mbar_arrive(&xempty[(h - 1) % NX]);
+            }
+            if (!ok) break;
+        }
+        if (et == 0) bulk_wait<0>();
+    }
+    __syncthreads();
+    if (abort_flag && threadIdx.x == 0) atomicOr(&g_status_anchor, FLAG_TIMEOUT);
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 2 * D);
+}
+
+// ------------------------------------------------------------------ host side
+
+// Tensor map of a bf16 plane view (dims: row elements, tokens, layers, chunks) with a
+// (box_inner x 128 rows) box.
+static cudaError_t anchor_plane_map(CUtensorMap* map, const void* base, const Plane& p, uint32_t box_inner,
+                                    CUtensorMapSwizzle sw) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const long long row = (long long)p.heads * p.dim;
+    cuuint64_t dims[4] = {(cuuint64_t)row, (cuuint64_t)p.tokens, (cuuint64_t)p.layers, (cuuint64_t)p.chunks};
+    long long st = p.tokens > 1 ? p.st : row;
+    long long sl = p.layers > 1 ? p.sl : st * p.tokens;
+    long long sc = p.chunks > 1 ? p.sc : sl * p.layers;
+    cuuint64_t strides[3] = {(cuuint64_t)(2 * st), (cuuint64_t)(2 * sl), (cuuint64_t)(2 * sc)};
+    cuuint32_t box[4] = {box_inner, (cuuint32_t)kAnRows, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Tensor map of a factor viewed as [rows][r] bf16 with an (r x box_rows) box, swizzled
+// by the row's byte length.
+static cudaError_t anchor_factor_map(CUtensorMap* map, const void* base, long long rows, int r, uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)r, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)r * 2};
+    cuuint32_t box[2] = {(cuuint32_t)r, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult res = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(r * 2), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+static int round_up(int x, int a) { return (x + a - 1) / a * a; }
+
+// Static shared memory of the kernels, kept out of the dynamic budget.
+constexpr int kAdStaticBytes = 12 * 1024;
+constexpr int kApStaticBytes = 2 * 1024;
+
+struct AdShape {
+    int stages, slots, stage_bytes, bbox, smem, cols;
+};
+
+static bool ad_shape(int V, int r, AdShape* s) {
+    const int row = 2 * r;
+    const int abytes = kAnRows * row, bbytes = kAdCols * row;
+    s->bbox = bbytes < 1024 ? 1024 : bbytes;
+    s->stage_bytes = round_up(kAdXBytes + V * s->bbox, 1024);
+    const int budget = kAnSmemLimit - kAdStaticBytes - 1024 - V * abytes;
+    s->stages = budget / s->stage_bytes;
+    if (s->stages > kAdMaxStages) s->stages = kAdMaxStages;
+    s->slots = 512 / (V * kAdCols);
+    if (s->slots > 4) s->slots = 4;
+    s->smem = 1024 + V * abytes + s->stages * s->stage_bytes;
+    s->cols = 32;
+    while (s->cols < s->slots * V * kAdCols) s->cols *= 2;
+    return V >= 1 && V <= kAnMaxAnchors && s->stages >= 2 && s->slots >= 1;
+}
+
+struct ApShape {
+    int nb, nx, smem;
+};
+
+static bool ap_shape(int V, int r, int D, ApShape* s) {
+    const int row = 2 * r;
+    const int abytes = kAnRows * row, xbytes = kAnRows * D * 2;
+    const int bslot = D * row < 1024 ? 1024 : D * row;
+    for (s->nx = kApMaxX; s->nx >= 2; --s->nx) {
+        const int budget = kAnSmemLimit - kApStaticBytes - 1024 - V * abytes - s->nx * xbytes;
+        s->nb = budget / bslot;
+        if (s->nb > kApMaxB) s->nb = kApMaxB;
+        if (s->nb >= 2) break;
+    }
+    s->smem = 1024 + V * abytes + s->nx * xbytes + s->nb * bslot;
+    return V >= 1 && V <= kAnMaxAnchors && s->nx >= 2 && s->nb >= 2;
+}
+
+bool anchor_shape_ok(int anchors, int rank, int head_dim) {
+    AdShape a;
+    ApShape b;
+    return ad_shape(anchors, rank, &a) && (head_dim <= 0 || ap_shape(anchors, rank, head_dim, &b));
+}
+
+size_t anchor_gate_workspace_bytes(const kvfix_kv_desc& d, int anchors, int prefix) {
+    const long long tiles = (prefix + kAnRows - 1) / kAnRows;
+    return (size_t)d.chunks * d.layers * tiles * anchors * sizeof(float);
+}
+
+template <int R, int MODE>
+static cudaError_t launch_dist(const CUtensorMap* mx, const CUtensorMap* ma, const CUtensorMap* mb, AdArgs& args,
+                               int planes, cudaStream_t s) {
+    AdShape sh;
+    if (!ad_shape(args.V, R, &sh)) return cudaErrorInvalidValue;
+    args.stages = sh.stages;
+    args.slots = sh.slots;
+    args.stage_bytes = sh.stage_bytes;
+    args.bbox_bytes = sh.bbox;
+    args.tmem_cols = sh.cols;
+    cudaError_t e = cudaFuncSetAttribute(anchor_dist_kernel<R, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, sh.smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(args.tiles, args.L, planes * args.C);
+    anchor_dist_kernel<R, MODE><<<grid, kAdThreads, sh.smem, s>>>(mx[0], mx[1], ma[0], ma[1], mb[0], mb[1], args);
+    return cudaGetLastError();
+}
+
+template <int R, int MODE>
+static cudaError_t dist_maps_and_launch(const uint16_t* const* x, const Plane& p, const uint16_t* const* ac,
+                                        const uint16_t* const* bct, AdArgs& args, int planes, cudaStream_t s) {
+    CUtensorMap mx[2], ma[2], mb[2];
+    cudaError_t e;
+    const long long arows = (long long)args.C * args.V * args.L * args.n;
+    const long long brows = (long long)args.C * args.V * args.L * args.F;
+    for (int q = 0; q < 2; ++q) {
+        const int src = q < planes ? q : 0;
+        if ((e = anchor_plane_map(&mx[q], x[src], p, kAdCols, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
+        if ((e = anchor_factor_map(&ma[q], ac[src], arows, R, kAnRows)) != cudaSuccess) return e;
+        if ((e = anchor_factor_map(&mb[q], bct[src], brows, R, kAdCols)) != cudaSuccess) return e;
+    }
+    return launch_dist<R, MODE>(mx, ma, mb, args, planes, s);
+}
+
+cudaError_t launch_anchor_gate(const uint16_t* v_src, const kvfix_kv_desc& d, const uint16_t* ac,
+                               const uint16_t* bct, int V, int r, int k, double T, double tau, double* dist,
+                               double* g, double* hbar, int32_t* accept, void* workspace, cudaStream_t s) {
+    Plane p = plane_of(d);
+    if (p.chunks == 0) return cudaSuccess;
+    AdArgs args = {};
+    args.V = V;
+    args.L = p.layers;
+    args.n = p.tokens;
+    args.F = p.heads * p.dim;
+    args.C = p.chunks;
+    args.rows = k;
+    args.tiles = (k + kAnRows - 1) / kAnRows;
+    args.inv_T = (float)(1.0 / T);
+    args.partial = static_cast<float*>(workspace);
+    const uint16_t* xs[1] = {v_src};
+    const uint16_t* as[1] = {ac};
+    const uint16_t* bs[1] = {bct};
+    cudaError_t e;
+    if (r == 16) e = dist_maps_and_launch<16, kAdGate>(xs, p, as, bs, args, 1, s);
+    else if (r == 32) e = dist_maps_and_launch<32, kAdGate>(xs, p, as, bs, args, 1, s);
+    else e = dist_maps_and_launch<64, kAdGate>(xs, p, as, bs, args, 1, s);
+    if (e != cudaSuccess) return e;
+    anchor_gate_kernel<<<p.chunks, 32, 0, s>>>(args.partial, V, p.layers, args.tiles, T, tau, dist, g, hbar, accept);
+    return cudaGetLastError();
+}
+
+template <int D, int R>
+static cudaError_t launch_apply(const uint16_t* const* x, const Plane& p, uint16_t* const* out, const Plane& op,
+                                const uint16_t* const* ad, const uint16_t* const* bdt, ApArgs& args,
+                                const RopeTheta& th, cudaStream_t s) {
+    ApShape sh;
+    if (!ap_shape(args.V, R, D, &sh)) return cudaErrorInvalidValue;
+    args.nb = sh.nb;
+    args.nx = sh.nx;
+    CUtensorMap mx[2], mo[2], ma[2], mb[2];
+    cudaError_t e;
+    const long long arows = (long long)args.C * args.V * args.L * args.n;
+    const long long brows = (long long)args.C * args.V * args.L * args.H * D;
+    for (int q = 0; q < 2; ++q) {
+        if ((e = anchor_plane_map(&mx[q], x[q], p, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+        if ((e = anchor_plane_map(&mo[q], out[q], op, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+        if ((e = anchor_factor_map(&ma[q], ad[q], arows, R, kAnRows)) != cudaSuccess) return e;
+        if ((e = anchor_factor_map(&mb[q], bdt[q], brows, R, D)) != cudaSuccess) return e;
+    }
+    e = cudaFuncSetAttribute(anchor_apply_kernel<D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, sh.smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.tokens + kAnRows - 1) / kAnRows, p.layers, 2 * p.chunks);
+    anchor_apply_kernel<D, R><<<grid, kApThreads, sh.smem, s>>>(mx[0], mx[1], mo[0], mo[1], ma[0], ma[1], mb[0],
+                                                                 mb[1], args, th);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_anchor_correct(const AnchorPlanes& pl, const kvfix_kv_desc& d, const kvfix_kv_desc& od, int V,
+                                  int r, double T, const int32_t* delta, const RopeTheta& th,
+                                  const int32_t* accept, cudaStream_t s) {
+    Plane p = plane_of(d), op = plane_of(od);
+    if (p.chunks == 0 || p.layers == 0 || p.tokens == 0) return cudaSuccess;
+    AdArgs args = {};
+    args.V = V;
+    args.L = p.layers;
+    args.n = p.tokens;
+    args.F = p.heads * p.dim;
+    args.C = p.chunks;
+    args.rows = p.tokens;
+    args.tiles = (p.tokens + kAnRows - 1) / kAnRows;
+    args.inv_T = (float)(1.0 / T);
+    args.w[0] = pl.w[0];
+    args.w[1] = pl.w[1];
+    args.accept = accept;
+    cudaError_t e;
+    if (r == 16) e = dist_maps_and_launch<16, kAdWeights>(pl.src, p, pl.ac, pl.bct, args, 2, s);
+    else if (r == 32) e = dist_maps_and_launch<32, kAdWeights>(pl.src, p, pl.ac, pl.bct, args, 2, s);
+    else e = dist_maps_and_launch<64, kAdWeights>(pl.src, p, pl.ac, pl.bct, args, 2, s);
+    if (e != cudaSuccess) return e;
+    ApArgs ap = {};
+    ap.V = V;
+    ap.L = p.layers;
+    ap.n = p.tokens;
+    ap.H = p.heads;
+    ap.C = p.chunks;
+    ap.w[0] = pl.w[0];
+    ap.w[1] = pl.w[1];
+    ap.accept = accept;
+    ap.delta = delta;
+    ap.out[0] = pl.out[0];
+    ap.out[1] = pl.out[1];
+    if (p.dim == 128) {
+        if (r == 16) return launch_apply<128, 16>(pl.src, p, pl.out, op, pl.ad, pl.bdt, ap, th, s);
+        if (r == 32) return launch_apply<128, 32>(pl.src, p, pl.out, op, pl.ad, pl.bdt, ap, th, s);
+        return launch_apply<128, 64>(pl.src, p, pl.out, op, pl.ad, pl.bdt, ap, th, s);
+    }
+    if (r == 16) return launch_apply<64, 16>(pl.src, p, pl.out, op, pl.ad, pl.bdt, ap, th, s);
+    if (r == 32) return launch_apply<64, 32>(pl.src, p, pl.out, op, pl.ad, pl.bdt, ap, th, s);
+    return launch_apply<64, 64>(pl.src, p, pl.out, op, pl.ad, pl.bdt, ap, th, s);
+}
+
+}  // namespace kvfix

@@ -104,7 +104,8 @@ kvfix_status kvfix_check_status(void* stream) {
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "kvfix_check_status: stream synchronize");
-    unsigned bits = read_status_repair(s) | read_status_diff(s) | read_status_draft(s) | read_status_lowrank(s);
+    unsigned bits = read_status_repair(s) | read_status_diff(s) | read_status_draft(s) | read_status_lowrank(s) |
+                    read_status_anchor(s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kvfix_check_status: status read");
     if (bits & 4u) return fail(KVFIX_ETIMEOUT, "a bounded device wait gave up");
@@ -431,6 +432,108 @@ kvfix_status kvfix_diff_restore(const kvfix_bf16* master_k, const kvfix_bf16* ma
     return launched(launch_diff_restore(master_k, master_v, master, mask, offsets, payload,
                                         payload_entries, siblings, block_tokens, delta, th,
                                         slot_mapping, pool_k, pool_v, pool, (cudaStream_t)stream),
+                    fn);
+}
+
+static kvfix_status check_factor(const void* p, const char* fn, const char* name) {
+    if (!p) return fail(KVFIX_EINVAL, "%s: %s is null", fn, name);
+    if (!aligned16(p)) return fail(KVFIX_EINVAL, "%s: %s not 16-byte aligned", fn, name);
+    return KVFIX_OK;
+}
+
+static kvfix_status check_anchor_shape(const kvfix_kv_desc& d, int32_t anchors, int32_t rank, int head_dim,
+                                       const char* fn) {
+    if (anchors < 1 || anchors > 16) return fail(KVFIX_EINVAL, "%s: anchors must be in [1, 16]", fn);
+    if (rank != 16 && rank != 32 && rank != 64) return fail(KVFIX_EINVAL, "%s: rank must be 16, 32 or 64", fn);
+    if (!anchor_shape_ok(anchors, rank, head_dim))
+        return fail(KVFIX_EINVAL, "%s: %d anchors of rank %d do not fit in shared memory", fn, anchors, rank);
+    const long long rows = (long long)d.chunks * anchors * d.layers *
+                           (long long)(d.tokens > d.kv_heads * d.head_dim ? d.tokens : d.kv_heads * d.head_dim);
+    if (rows >= (1ll << 31)) return fail(KVFIX_EINVAL, "%s: factor rows exceed 2^31", fn);
+    if (d.layers > 65535 || d.chunks > 32767) return fail(KVFIX_EINVAL, "%s: too many layers or segments", fn);
+    return KVFIX_OK;
+}
+
+size_t kvfix_anchor_gate_workspace_bytes(kvfix_kv_desc src, int32_t anchors, int32_t prefix) {
+    if (anchors < 1 || prefix < 1 || src.chunks < 0 || src.layers < 0) return 0;
+    return anchor_gate_workspace_bytes(src, anchors, prefix);
+}
+
+kvfix_status kvfix_anchor_gate(const kvfix_bf16* v_src, kvfix_kv_desc src, const kvfix_bf16* a_c,
+                               const kvfix_bf16* b_ct, int32_t anchors, int32_t rank, int32_t prefix,
+                               double temperature, double tau, double* d, double* g, double* hbar,
+                               int32_t* accept, void* workspace, size_t workspace_bytes, void* stream) {
+    const char* fn = "kvfix_anchor_gate";
+    kvfix_status st;
+    if ((st = check_plane(v_src, src, "kvfix_anchor_gate: v_src")) != KVFIX_OK) return st;
+    if ((st = check_anchor_shape(src, anchors, rank, 0, fn)) != KVFIX_OK) return st;
+    if (prefix < 1 || prefix > src.tokens) return fail(KVFIX_EINVAL, "%s: prefix must be in [1, tokens]", fn);
+    if (!(temperature > 0.0) || !isfinite(temperature) || isnan(tau))
+        return fail(KVFIX_EINVAL, "%s: temperature must be finite and > 0, tau a number", fn);
+    if ((st = check_factor(a_c, fn, "a_c")) != KVFIX_OK) return st;
+    if ((st = check_factor(b_ct, fn, "b_ct")) != KVFIX_OK) return st;
+    if (!d || !g || !hbar || !accept) return fail(KVFIX_EINVAL, "%s: d, g, hbar and accept are required", fn);
+    if (src.chunks > 0 && src.layers > 0) {
+        if (!workspace || workspace_bytes < anchor_gate_workspace_bytes(src, anchors, prefix))
+            return fail(KVFIX_EINVAL, "%s: workspace smaller than kvfix_anchor_gate_workspace_bytes()", fn);
+        if (!aligned16(workspace)) return fail(KVFIX_EINVAL, "%s: workspace not 16-byte aligned", fn);
+    }
+    if (src.layers == 0) return fail(KVFIX_EINVAL, "%s: no layers", fn);
+    return launched(launch_anchor_gate(v_src, src, a_c, b_ct, anchors, rank, prefix, temperature, tau, d, g, hbar,
+                                       accept, workspace, (cudaStream_t)stream),
+                    fn);
+}
+
+kvfix_status kvfix_anchor_correct(const kvfix_bf16* k_src, const kvfix_bf16* v_src, kvfix_kv_desc src,
+                                  const kvfix_bf16* a_c_k, const kvfix_bf16* b_ct_k, const kvfix_bf16* a_c_v,
+                                  const kvfix_bf16* b_ct_v, const kvfix_bf16* a_d_k, const kvfix_bf16* b_dt_k,
+                                  const kvfix_bf16* a_d_v, const kvfix_bf16* b_dt_v, int32_t anchors,
+                                  int32_t rank, double temperature, const int32_t* delta, double rope_base,
+                                  const int32_t* accept, float* w_k, float* w_v, kvfix_bf16* k_out,
+                                  kvfix_bf16* v_out, kvfix_kv_desc out, void* stream) {
+    const char* fn = "kvfix_anchor_correct";
+    kvfix_status st;
+    if ((st = check_plane(k_src, src, "kvfix_anchor_correct: k_src")) != KVFIX_OK) return st;
+    if ((st = check_plane(v_src, src, "kvfix_anchor_correct: v_src")) != KVFIX_OK) return st;
+    if ((st = check_plane(k_out, out, "kvfix_anchor_correct: k_out")) != KVFIX_OK) return st;
+    if ((st = check_plane(v_out, out, "kvfix_anchor_correct: v_out")) != KVFIX_OK) return st;
+    if (!same_shape(src, out) || src.chunks != out.chunks)
+        return fail(KVFIX_EINVAL, "%s: out must have the shape of src", fn);
+    if (src.head_dim != 64 && src.head_dim != 128) return fail(KVFIX_EINVAL, "%s: head_dim must be 64 or 128", fn);
+    if ((st = check_anchor_shape(src, anchors, rank, src.head_dim, fn)) != KVFIX_OK) return st;
+    if (!(temperature > 0.0) || !isfinite(temperature))
+        return fail(KVFIX_EINVAL, "%s: temperature must be finite and > 0", fn);
+    if (!(rope_base > 1.0) || !isfinite(rope_base))
+        return fail(KVFIX_EINVAL, "%s: rope_base must be finite and > 1", fn);
+    const void* f[8] = {a_c_k, b_ct_k, a_c_v, b_ct_v, a_d_k, b_dt_k, a_d_v, b_dt_v};
+    const char* names[8] = {"a_c_k", "b_ct_k", "a_c_v", "b_ct_v", "a_d_k", "b_dt_k", "a_d_v", "b_dt_v"};
+    for (int i = 0; i < 8; ++i)
+        if ((st = check_factor(f[i], fn, names[i])) != KVFIX_OK) return st;
+    if (src.chunks > 0 && (!delta || !w_k || !w_v))
+        return fail(KVFIX_EINVAL, "%s: delta, w_k and w_v are required", fn);
+    const bool k_in_place = (const void*)k_src == (const void*)k_out && same_desc(src, out);
+    const bool v_in_place = (const void*)v_src == (const void*)v_out && same_desc(src, out);
+    if ((!k_in_place && overlaps(k_out, out, k_src, src)) || (!v_in_place && overlaps(v_out, out, v_src, src)) ||
+        overlaps(k_out, out, v_src, src) || overlaps(v_out, out, k_src, src) || overlaps(k_out, out, v_out, out))
+        return fail(KVFIX_EINVAL, "%s: outputs overlap the sources (other than exactly in place) or each other", fn);
+    AnchorPlanes pl;
+    pl.src[0] = k_src;
+    pl.src[1] = v_src;
+    pl.ac[0] = a_c_k;
+    pl.ac[1] = a_c_v;
+    pl.bct[0] = b_ct_k;
+    pl.bct[1] = b_ct_v;
+    pl.ad[0] = a_d_k;
+    pl.ad[1] = a_d_v;
+    pl.bdt[0] = b_dt_k;
+    pl.bdt[1] = b_dt_v;
+    pl.w[0] = w_k;
+    pl.w[1] = w_v;
+    pl.out[0] = k_out;
+    pl.out[1] = v_out;
+    RopeTheta th = make_theta(rope_base, src.head_dim);
+    return launched(launch_anchor_correct(pl, src, out, anchors, rank, temperature, delta, th, accept,
+                                          (cudaStream_t)stream),
                     fn);
 }
 

@@ -93,4 +93,26 @@ cudaError_t launch_diff_restore(const uint16_t* mk, const uint16_t* mv, const kv
                                 const int32_t* slot_map, uint16_t* pk, uint16_t* pv,
                                 const kvfix_kv_desc& pd, cudaStream_t s);
 
+// Anchor-pool correction (both planes: index 0 = keys, rotated; 1 = values).
+struct AnchorPlanes {
+    const uint16_t* src[2];
+    const uint16_t* ac[2];
+    const uint16_t* bct[2];
+    const uint16_t* ad[2];
+    const uint16_t* bdt[2];
+    float* w[2];
+    uint16_t* out[2];
+};
+unsigned read_status_anchor(cudaStream_t stream);
+bool anchor_shape_ok(int anchors, int rank, int head_dim);
+size_t anchor_gate_workspace_bytes(const kvfix_kv_desc& d, int anchors, int prefix);
+cudaError_t launch_anchor_gate(const uint16_t* v_src, const kvfix_kv_desc& d, const uint16_t* ac,
+                               const uint16_t* bct, int V, int r, int k, double T, double tau,
+                               double* dist, double* g, double* hbar, int32_t* accept,
+                               void* workspace, cudaStream_t s);
+cudaError_t launch_anchor_correct(const AnchorPlanes& pl, const kvfix_kv_desc& d,
+                                  const kvfix_kv_desc& od, int V, int r, double T,
+                                  const int32_t* delta, const RopeTheta& th, const int32_t* accept,
+                                  cudaStream_t s);
+
 }  // namespace kvfix

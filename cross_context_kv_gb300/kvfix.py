@@ -51,6 +51,10 @@ SIGNATURES = {
     "kvfix_diff_encode": (ctypes.c_int, [P, P, D, P, P, D, I32, P, P, P, I64, P, P]),
     "kvfix_diff_gather": (ctypes.c_int, [P, P, D, P, P, P, I64, I32, I32, P, P, D, P]),
     "kvfix_diff_restore": (ctypes.c_int, [P, P, D, P, P, P, I64, I32, I32, P, F64, P, P, P, D, P]),
+    "kvfix_anchor_gate_workspace_bytes": (SZ, [D, I32, I32]),
+    "kvfix_anchor_gate": (ctypes.c_int, [P, D, P, P, I32, I32, I32, F64, F64, P, P, P, P, P, SZ, P]),
+    "kvfix_anchor_correct": (ctypes.c_int, [P, P, D, P, P, P, P, P, P, P, P, I32, I32, F64, P, F64, P, P, P, P, P,
+                                            D, P]),
 }
 
 
@@ -298,3 +302,61 @@ def diff_restore(master_k, master_v, mask, offsets, payload, siblings: int, bloc
                                   float(rope_base), _ptr(slot_mapping), _ptr(pool_k), _ptr(pool_v),
                                   plane_desc(pool_k.unsqueeze(0)), _stream(mk)))
     return pool_k, pool_v
+
+
+def _factor(t, name, shape):
+    _bf16(t, name)
+    if not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be a contiguous tensor of shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def anchor_gate(v_src, a_c, b_ct, prefix: int, temperature: float = 1.0, tau: float = 0.5):
+    """Reliability gate per segment.  v_src [C][L][n][H][D]; a_c [C][V][L][n][r];
+    b_ct [C][V][L][H*D][r].  Returns (d [C][V] f64, g [C][V] f64, hbar [C] f64, accept [C] i32)."""
+    _bf16(v_src, "v_src")
+    x = v_src if v_src.dim() == 5 else v_src.unsqueeze(0)
+    C, L, n, H, Dh = x.shape
+    V, r = a_c.shape[1], a_c.shape[-1]
+    _factor(a_c, "a_c", (C, V, L, n, r))
+    _factor(b_ct, "b_ct", (C, V, L, H * Dh, r))
+    dev = x.device
+    d = torch.empty((C, V), dtype=torch.float64, device=dev)
+    g = torch.empty_like(d)
+    hbar = torch.empty(C, dtype=torch.float64, device=dev)
+    acc = torch.empty(C, dtype=torch.int32, device=dev)
+    desc = plane_desc(x)
+    nbytes = lib.kvfix_anchor_gate_workspace_bytes(desc, V, int(prefix))
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    _check(lib.kvfix_anchor_gate(_ptr(x), desc, _ptr(a_c), _ptr(b_ct), V, r, int(prefix), float(temperature),
+                                 float(tau), _ptr(d), _ptr(g), _ptr(hbar), _ptr(acc), _ptr(ws), ws.numel(),
+                                 _stream(x)))
+    return d, g, hbar, acc
+
+
+def anchor_correct(k_src, v_src, factors: dict, delta, rope_base: float, temperature: float = 1.0,
+                   accept=None, out_k=None, out_v=None, w_k=None, w_v=None):
+    """Token-weighted anchor correction of both planes.  k_src/v_src [C][L][n][H][D];
+    factors: a_c_k, b_ct_k, a_c_v, b_ct_v, a_d_k, b_dt_k, a_d_v, b_dt_v ([C][V][L][n][r] and
+    [C][V][L][H*D][r]).  Returns (out_k, out_v, w_k, w_v); w_* [C][L][n][V] float32."""
+    _bf16(k_src, "k_src")
+    _bf16(v_src, "v_src")
+    _i32(delta, "delta")
+    C, L, n, H, Dh = k_src.shape
+    V, r = factors["a_c_k"].shape[1], factors["a_c_k"].shape[-1]
+    names = ("a_c_k", "b_ct_k", "a_c_v", "b_ct_v", "a_d_k", "b_dt_k", "a_d_v", "b_dt_v")
+    for nm in names:
+        _factor(factors[nm], nm, (C, V, L, n, r) if nm.startswith("a_") else (C, V, L, H * Dh, r))
+    dev = k_src.device
+    out_k = torch.empty_like(k_src) if out_k is None else out_k
+    out_v = torch.empty_like(v_src) if out_v is None else out_v
+    w_k = torch.empty((C, L, n, V), dtype=torch.float32, device=dev) if w_k is None else w_k
+    w_v = torch.empty((C, L, n, V), dtype=torch.float32, device=dev) if w_v is None else w_v
+    _f32(w_k, "w_k")
+    _f32(w_v, "w_v")
+    if accept is not None:
+        _i32(accept, "accept")
+    _check(lib.kvfix_anchor_correct(_ptr(k_src), _ptr(v_src), plane_desc(k_src),
+                                    *[_ptr(factors[nm]) for nm in names], V, r, float(temperature), _ptr(delta),
+                                    float(rope_base), _ptr(accept), _ptr(w_k), _ptr(w_v), _ptr(out_k), _ptr(out_v),
+                                    plane_desc(out_k), _stream(k_src)))
+    return out_k, out_v, w_k, w_v

@@ -125,6 +125,26 @@ class LowRankConfig:
         return dataclasses.replace(self, **kw)
 
 
+@dataclass(frozen=True)
+class AnchorConfig:
+    name: str
+    segments: int
+    anchors: int
+    layers: int
+    tokens: int
+    kv_heads: int
+    head_dim: int
+    rank: int
+    rope_base: float
+    tau: float           # reliability threshold
+    noise_std: float     # source = the matching anchor's base state + N(0, noise_std^2)
+    delta_std: float     # scale of the delta factor A_d
+    seed: int
+
+    def with_(self, **kw) -> "AnchorConfig":
+        return dataclasses.replace(self, **kw)
+
+
 REPAIR_TINY = RepairConfig("repair_tiny", agents=1, chunks=1, layers=2, tokens=256, kv_heads=4,
                            head_dim=64, rope_base=1e4, r_num=1, r_den=10, check_layer=1,
                            heavy_frac=0.05, heavy_kind="normal", delta_kind="fixed",
@@ -143,6 +163,12 @@ SIBLINGS_8B = DiffConfig("siblings_8b", siblings=16, layers=32, tokens=8192, kv_
 LOWRANK_70B = LowRankConfig("lowrank_70b", chunks=4, layers=80, tokens=16384, kv_heads=8,
                             q_heads=64, head_dim=128, rank=16, draft_steps=2, layer_begin=1,
                             budget_num=5, budget_den=100, a_std=0.1, fresh_std=0.5, seed=4)
+
+# Anchor-pool correction on Llama-3.1-8B-shaped caches: 2 shared segments of 4096 tokens,
+# V = 10 anchors of rank 32 per layer and plane, tau = 0.32 (KVCMAS's GSM8K threshold).
+ANCHOR_8B = AnchorConfig("anchor_8b", segments=2, anchors=10, layers=32, tokens=4096, kv_heads=8,
+                         head_dim=128, rank=32, rope_base=5e5, tau=0.32, noise_std=0.3,
+                         delta_std=0.1, seed=6)
 
 CONFIGS = {c.name: c for c in (REPAIR_TINY, REPAIR_LLAMA8B, ROUND_QWEN14B, SIBLINGS_8B,
                                LOWRANK_70B)}
@@ -263,6 +289,31 @@ def restore_inputs(cfg: DiffConfig, device, skip: float = 0.0, spare_pages: int 
         slot[torch.rand((S, n), generator=g) < skip] = -1
     return {"delta": delta.to(torch.int32).to(device), "slot_mapping": slot.to(torch.int32).to(device),
             "slots": pages * pg}
+
+
+def anchor_inputs(cfg: AnchorConfig, device) -> dict:
+    """Draws per segment c and plane p: anchors' base factors a_c_p ~ N(0,1) [C][V][L][n][r]
+    and b_ct_p ~ N(0, 1/r) [C][V][L][F][r] (base rows of unit variance); delta factors
+    a_d_p ~ N(0, delta_std^2), b_dt_p ~ N(0, 1/r); noise_p ~ N(0, noise_std^2) [C][L][n][H][D]
+    (bf16); the anchor each segment resembles, match[c] = c mod V (the source rows are
+    composed from these draws by the caller: the base state of anchor match[c] plus the
+    noise); key shifts delta ~ U{500..8000}."""
+    C, V, L, n, r = cfg.segments, cfg.anchors, cfg.layers, cfg.tokens, cfg.rank
+    F = cfg.kv_heads * cfg.head_dim
+    out = {}
+    bstd = 1.0 / float(r) ** 0.5
+    for pi, p in enumerate(("k", "v")):
+        base = 100 * (pi + 1)
+        out[f"a_c_{p}"] = _normal((C, V, L, n, r), 1.0, _gen(cfg.seed, base + 1, device), device, BF16)
+        out[f"b_ct_{p}"] = _normal((C, V, L, F, r), bstd, _gen(cfg.seed, base + 2, device), device, BF16)
+        out[f"a_d_{p}"] = _normal((C, V, L, n, r), cfg.delta_std, _gen(cfg.seed, base + 3, device), device, BF16)
+        out[f"b_dt_{p}"] = _normal((C, V, L, F, r), bstd, _gen(cfg.seed, base + 4, device), device, BF16)
+        out[f"noise_{p}"] = _normal((C, L, n, cfg.kv_heads, cfg.head_dim), cfg.noise_std,
+                                    _gen(cfg.seed, base + 5, device), device, BF16)
+    out["match"] = [c % V for c in range(C)]
+    gd = _gen(cfg.seed, 99, "cpu")
+    out["delta"] = torch.randint(500, 8001, (C,), generator=gd, dtype=torch.int64).to(torch.int32).to(device)
+    return out
 
 
 def lowrank_inputs(cfg: LowRankConfig, device, planes=("k", "v")) -> dict:

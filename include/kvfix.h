@@ -339,6 +339,69 @@ KVFIX_API kvfix_status kvfix_diff_restore(const kvfix_bf16* master_k, const kvfi
                                 const int32_t* slot_mapping, kvfix_bf16* pool_k,
                                 kvfix_bf16* pool_v, kvfix_kv_desc pool, void* stream);
 
+/*
+ * Anchor-pool correction.  [KVCMAS] section 3.3 (each anchor keeps its base cache and its
+ * delta correction as low-rank factors, Eq. 7; the correction is the weighted sum of the
+ * anchors' deltas, Eq. 8, applied to the aligned source cache, Eq. 4) and App. A.3
+ * (reliability gate, Eq. 9-11; token-wise weights; keys matched in canonical positions).
+ *
+ * Factor layout, per plane, for C segments (src.chunks), V anchors, L layers, n tokens,
+ * F = kv_heads * head_dim features and rank r:
+ *     A  : device bf16 [C][V][L][n][r]        (first factor, row t of the segment)
+ *     Bt : device bf16 [C][V][L][F][r]        (second factor, stored transposed)
+ * so that anchor v's state of layer l is A[c][v][l] * Bt[c][v][l]^T ([n x F]).
+ * anchors: 1..16; rank: 16, 32 or 64 (anchors * rank limited by shared memory: the call
+ * returns KVFIX_EINVAL for shapes that do not fit).
+ */
+
+/* Bytes of device workspace kvfix_anchor_gate needs for `src`, `anchors` and `prefix`. */
+KVFIX_API size_t kvfix_anchor_gate_workspace_bytes(kvfix_kv_desc src, int32_t anchors,
+                                                   int32_t prefix);
+
+/*
+ * kvfix_anchor_gate -- [KVCMAS] App. A.3 "Reliability Gate", Eq. 9-11, per segment c:
+ *     d_v  = ( sum_l || V_src^(l)[:k] - (A_v Bt_v^T)^(l)[:k] ||_F^2 )^(1/2)
+ *     g_v  = softmax_v(-d_v / T),   Hbar = -sum_v g_v log2 g_v / log2 V
+ *     accept = V >= 2 && Hbar <= tau
+ * v_src      : `src`, the source value plane (chunks = segments).
+ * a_c, b_ct  : base-state factors of the value plane (layout above).
+ * prefix k   : 1..tokens; temperature T > 0.
+ * d, g       : device double [C][V];  hbar : device double [C] (NaN if V < 2);
+ * accept     : device int32 [C].  Distances are summed per 128-row tile in float and
+ *              across tiles and layers in double, in a fixed order.
+ * workspace  : device, at least kvfix_anchor_gate_workspace_bytes(), 16-byte aligned.
+ */
+KVFIX_API kvfix_status kvfix_anchor_gate(const kvfix_bf16* v_src, kvfix_kv_desc src,
+                                         const kvfix_bf16* a_c, const kvfix_bf16* b_ct,
+                                         int32_t anchors, int32_t rank, int32_t prefix,
+                                         double temperature, double tau, double* d, double* g,
+                                         double* hbar, int32_t* accept, void* workspace,
+                                         size_t workspace_bytes, void* stream);
+
+/*
+ * kvfix_anchor_correct -- token-weighted anchor correction of both planes:
+ *     m_v[t] = (1/F) sum_f | x[t][f] - (A_c,v Bt_c,v^T)[t][f] |   (x: keys in canonical positions)
+ *     w[t]   = softmax_v(-m_v[t] / T)                            (per plane, layer, token)
+ *     out[t] = Align(x[t]) + sum_v w_v[t] (A_d,v Bt_d,v^T)[t]     (bf16)
+ * Align rotates keys by delta[c] (as kvfix_rerope) and leaves values unchanged.
+ * k_src, v_src : `src` (chunks = segments); head_dim 64 or 128.
+ * a_c_*, b_ct_*: base-state factors; a_d_*, b_dt_*: delta-correction factors (layout above).
+ * delta        : device int32 [C]; rope_base as for kvfix_rerope.
+ * accept       : optional device int32 [C] (e.g. kvfix_anchor_gate's): segments with 0 are
+ *                skipped entirely (outputs and weights untouched).  NULL corrects all.
+ * w_k, w_v     : device float [C][L][n][V], written with the token weights.
+ * k_out, v_out : `out`, the shape of src; may be exactly src (in place), no other overlap.
+ * The delta term is formed on the tensor cores from bf16(w_v * A_d,v) (the weight is
+ * folded into the first factor, rounded once to bf16) with float accumulation.
+ */
+KVFIX_API kvfix_status kvfix_anchor_correct(
+    const kvfix_bf16* k_src, const kvfix_bf16* v_src, kvfix_kv_desc src, const kvfix_bf16* a_c_k,
+    const kvfix_bf16* b_ct_k, const kvfix_bf16* a_c_v, const kvfix_bf16* b_ct_v,
+    const kvfix_bf16* a_d_k, const kvfix_bf16* b_dt_k, const kvfix_bf16* a_d_v,
+    const kvfix_bf16* b_dt_v, int32_t anchors, int32_t rank, double temperature,
+    const int32_t* delta, double rope_base, const int32_t* accept, float* w_k, float* w_v,
+    kvfix_bf16* k_out, kvfix_bf16* v_out, kvfix_kv_desc out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
