@@ -15,8 +15,8 @@ collective: weak scaling); the step time is the max over ranks.
 --impl reference times the CPU oracle (plain C, double precision) on the host cores
 on a bounded sample of the same workload, with the same metric.
 The "stages" object times the other rows of the path on their own workloads: the
-collective 8-agent round, the 16-sibling diff encode/gather/restore, and the 70B-shaped
-low-rank + draft-ranked row repair.
+collective 8-agent round, the 16-sibling diff encode/gather/restore, the 70B-shaped
+low-rank + draft-ranked row repair, and the anchor-pool gate + correction.
 """
 from __future__ import annotations
 
@@ -574,7 +574,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.empty_cache()
     if not args.no_stages and rank == 0:
         stages = {}
-        for name, fn in (("collective_round", stage_round), ("diff", stage_diff), ("lowrank_draft", stage_lowrank)):
+        for name, fn in (("collective_round", stage_round), ("diff", stage_diff), ("lowrank_draft", stage_lowrank),
+                         ("anchor", stage_anchor)):
             try:
                 stages[name] = fn(kvfix, peak)
             except Exception as exc:  # report, do not hide
@@ -611,12 +612,84 @@ def run_reference(args, world, rank):
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def compose_anchor_sources(cfg, inp):
+    """Source planes of the anchor workload: the matching anchor's base state plus the
+    noise draw (input construction, float32 matmul on the device, untimed)."""
+    out = {}
+    for p in ("k", "v"):
+        src = torch.empty_like(inp[f"noise_{p}"])
+        for c in range(cfg.segments):
+            v = inp["match"][c]
+            rec = torch.matmul(inp[f"a_c_{p}"][c, v].float(), inp[f"b_ct_{p}"][c, v].float().transpose(-1, -2))
+            src[c] = (rec.view(src[c].shape) + inp[f"noise_{p}"][c].float()).to(torch.bfloat16)
+            del rec
+        out[p] = src
+    return out
+
+
+ANCHOR_FACTORS = ("a_c_k", "b_ct_k", "a_c_v", "b_ct_v", "a_d_k", "b_dt_k", "a_d_v", "b_dt_v")
+
+
+def stage_anchor(kvfix, peak, steps=5, warmup=3):
+    cfg = synth.ANCHOR_8B
+    inp = synth.anchor_inputs(cfg, "cuda")
+    src = compose_anchor_sources(cfg, inp)
+    fac = {k: inp[k] for k in ANCHOR_FACTORS}
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    C, V, L, n, r = cfg.segments, cfg.anchors, cfg.layers, cfg.tokens, cfg.rank
+    F = cfg.kv_heads * cfg.head_dim
+    ok, ov = torch.empty_like(src["k"]), torch.empty_like(src["v"])
+    wk = torch.empty((C, L, n, V), dtype=torch.float32, device="cuda")
+    wv = torch.empty_like(wk)
+    gate_ms, cor_ms = [], []
+    accepted = None
+    for s in range(warmup + steps):
+        flush.zero_()
+        host_lead()
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        _, _, _, acc = kvfix.anchor_gate(src["v"], inp["a_c_v"], inp["b_ct_v"], n, tau=cfg.tau)
+        e1.record(stream)
+        kvfix.anchor_correct(src["k"], src["v"], fac, inp["delta"], cfg.rope_base, accept=acc, out_k=ok, out_v=ov,
+                             w_k=wk, w_v=wv)
+        e2.record(stream)
+        torch.cuda.synchronize()
+        accepted = int(acc.sum().item())
+        if s >= warmup:
+            gate_ms.append(e0.elapsed_time(e1))
+            cor_ms.append(e1.elapsed_time(e2))
+    kvfix.check_status()
+    plane = C * L * n * F * 2
+    a_bytes = C * V * L * n * r * 2
+    b_bytes = C * V * L * F * r * 2
+    w_bytes = C * L * n * V * 4
+    gate_bytes = plane + a_bytes + b_bytes
+    cor_bytes = 2 * (plane + a_bytes + b_bytes + w_bytes) + 2 * (2 * plane + a_bytes + b_bytes + w_bytes)
+    mac = C * V * L * n * F * r
+    gate, cor = statistics.mean(gate_ms), statistics.mean(cor_ms)
+    res = {"workload": "anchor_8b: 2 segments x 4096 tokens, 32 layers, 8 x 128, 10 anchors of rank 32, tau 0.32",
+           "accepted_segments": accepted,
+           "ms_per_step": round(gate + cor, 4),
+           "corrected_GBps": round(2 * plane / (gate + cor) / 1e6, 1),
+           "tensor_tflops": round(5 * 2 * mac / (gate + cor) / 1e9, 1),
+           "gate": {"ms": round(gate, 4), "algorithmic_bytes": gate_bytes,
+                    "GBps": round(gate_bytes / gate / 1e6, 1), "frac": round(gate_bytes / gate / 1e6 / peak, 4)},
+           "correct": {"ms": round(cor, 4), "algorithmic_bytes": cor_bytes,
+                       "GBps": round(cor_bytes / cor / 1e6, 1), "frac": round(cor_bytes / cor / 1e6 / peak, 4),
+                       "tflops": round(4 * 2 * mac / cor / 1e9, 1)}}
+    del inp, src, fac, ok, ov, wk, wv, flush
+    torch.cuda.empty_cache()
+    return res
+
+
 PROFILE_CASES = {
     # reduced workloads for profiler captures: inputs larger than L2, a few GB at most
     "repair": lambda: synth.REPAIR_LLAMA8B.with_(layers=8),
     "round": lambda: synth.ROUND_QWEN14B.with_(layers=8),
     "diff": lambda: synth.SIBLINGS_8B.with_(layers=4),
     "lowrank": lambda: synth.LOWRANK_70B.with_(chunks=1, layers=8),
+    "anchor": lambda: synth.ANCHOR_8B.with_(layers=8),
 }
 
 
@@ -650,6 +723,13 @@ def run_profile_case(name: str, iters: int = 3):
             kvfix.diff_restore(inp["master_k"], inp["master_v"], m, o, pl, cfg.siblings, cfg.block_tokens,
                                tgt["delta"], cfg.rope_base, tgt["slot_mapping"], pk, pv,
                                payload_entries=entries)
+    elif name == "anchor":
+        inp = synth.anchor_inputs(cfg, "cuda")
+        src = compose_anchor_sources(cfg, inp)
+        fac = {k: inp[k] for k in ANCHOR_FACTORS}
+        def step():
+            _, _, _, acc = kvfix.anchor_gate(src["v"], inp["a_c_v"], inp["b_ct_v"], cfg.tokens, tau=cfg.tau)
+            kvfix.anchor_correct(src["k"], src["v"], fac, inp["delta"], cfg.rope_base, accept=acc)
     else:
         inp = synth.lowrank_inputs(cfg, "cuda")
         kt = torch.empty_like(inp["x_k"])

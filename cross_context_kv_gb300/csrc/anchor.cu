@@ -14,10 +14,11 @@
 //
 // Blackwell path, three kernels:
 //   anchor_dist_kernel   per (128-row tile, layer, plane and segment): the anchors' base
-//                        rows A_v B_v are built 16 features at a time by tcgen05.mma
-//                        (M = 128 rows, N = 16, K = r) into tensor memory, while eight
-//                        epilogue warps fold |x - rec| (token weights) or (x - rec)^2 (gate)
-//                        into per-row, per-anchor sums; x and Bt stream through a TMA ring.
+//                        rows A_v B_v are built 128 features at a time by tcgen05.mma
+//                        (M = 128 rows, N = 128, K = r) into four tensor-memory buffers,
+//                        while eight epilogue warps fold |x - rec| (token weights) or
+//                        (x - rec)^2 (gate) into per-row, per-anchor sums; x chunks and Bt
+//                        stream through TMA rings fed by two producer lanes.
 //   anchor_gate_kernel   per segment: the gate's distances, softmax, normalised entropy.
 //   anchor_apply_kernel  per (tile, layer, plane and segment): the anchors' delta factors
 //                        are scaled by the token weights in shared memory and multiplied by
@@ -64,9 +65,10 @@ constexpr int kAnSmemLimit = 227 * 1024;
 // ------------------------------------------------------------------ distances
 
 constexpr int kAdThreads = 320;       // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
-constexpr int kAdCols = 16;           // features per chunk (MMA N)
-constexpr int kAdMaxStages = 8;
-constexpr int kAdXBytes = kAnRows * kAdCols * 2;  // x chunk, unswizzled
+constexpr int kAdCols = 128;          // features per chunk (MMA N)
+constexpr int kAdSlots = 4;           // tensor-memory accumulators of 128 columns
+constexpr int kAdMaxB = 16;           // Bt ring entries (one anchor's chunk each)
+constexpr int kAdXBytes = kAnRows * kAdCols * 2;  // x chunk: two 64-feature boxes, 128-byte swizzle
 
 enum { kAdWeights = 0, kAdGate = 1 };
 
@@ -74,9 +76,7 @@ struct AdArgs {
     int V, L, n, F, C;
     int rows;            // rows of the tile range: n (weights) or the gate prefix k
     int tiles;           // ceil(rows / 128)
-    int stages, slots;   // ring depth, tensor-memory buffers
-    int stage_bytes, bbox_bytes;
-    int tmem_cols;       // power of two >= slots * V * 16
+    int nb;              // Bt ring entries
     float inv_T;
     float* w[2];         // weights mode: [C][L][n][V] per plane
     float* partial;      // gate mode: [C][L][tiles][V]
@@ -89,12 +89,15 @@ struct AdCfg {
     static constexpr uint32_t kLayout = R == 16 ? 6u : R == 32 ? 4u : 2u;
     static constexpr int kABytes = kAnRows * kRowBytes;           // one anchor's A tile
     static constexpr int kBBytes = kAdCols * kRowBytes;           // one anchor's Bt chunk
-    static constexpr int kBBox = kBBytes < 1024 ? 1024 : kBBytes; // swizzle-atom aligned slot
 };
 
-// grid = (tiles, L, planes * C).  MODE kAdWeights: both planes (z = plane * C + c), every
-// row; writes the softmax of -mean|x - rec_v| / T per row.  MODE kAdGate: the value plane,
-// rows < k; writes per-tile sums of (x - rec_v)^2.
+// grid = (tiles, L, planes * C).  For each 128-feature chunk the x tile is staged once;
+// the anchors' base rows of the chunk (M = 128 rows, N = 128 features, K = r) go through
+// four tensor-memory accumulators while the epilogue folds them against x, which each
+// thread holds in registers (its row, 64 of the chunk's features) for all anchors.
+// MODE kAdWeights: both planes (z = plane * C + c), every row; writes the softmax of
+// -mean|x - rec_v| / T per row.  MODE kAdGate: the value plane, rows < k; writes per-tile
+// sums of (x - rec_v)^2.
 template <int R, int MODE>
 __global__ void __launch_bounds__(kAdThreads, 1)
 anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CUtensorMap tm_x1,
@@ -103,34 +106,39 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
                    AdArgs args) {
     using K = AdCfg<R>;
     extern __shared__ unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t full[kAdMaxStages], empty[kAdMaxStages], tfull[4], tempty[4], afull;
+    __shared__ __align__(8) uint64_t xfull[2], xempty[2], bfull[kAdMaxB], bempty[kAdMaxB], tfull[kAdSlots],
+        tempty[kAdSlots], afull;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ float red[kAnRows][kAnMaxAnchors + 1];
     __shared__ float gsum[4][kAnMaxAnchors];
-    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int V = args.V;
-    unsigned char* asm_ = smem;                             // V A tiles
-    unsigned char* ring = smem + V * K::kABytes;            // stages: x chunk, then V Bt chunks
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x, l = blockIdx.y;
     const int plane = MODE == kAdGate ? 0 : (int)blockIdx.z / args.C;
     const int c = (int)blockIdx.z % args.C;
+    if (MODE == kAdWeights && args.accept && args.accept[c] == 0) return;
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int V = args.V, NB = args.nb;
+    unsigned char* asm_ = smem;                             // V A tiles
+    unsigned char* xs = smem + V * K::kABytes;              // two x chunks
+    unsigned char* bs = xs + 2 * kAdXBytes;                 // Bt ring
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const CUtensorMap* mx = plane ? &tm_x1 : &tm_x0;
     const CUtensorMap* ma = plane ? &tm_a1 : &tm_a0;
     const CUtensorMap* mb = plane ? &tm_b1 : &tm_b0;
-    if (MODE == kAdWeights && args.accept && args.accept[c] == 0) return;
     const int t0 = tile * kAnRows;
     const int chunks = args.F / kAdCols;
-    const int S = args.stages, NS = args.slots;
-    const uint32_t slot_cols = (uint32_t)(V * kAdCols);
+    const int total = chunks * V;                           // (chunk, anchor) steps
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + 8);  // the MMA's commit and the eight epilogue warps
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&xfull[i], 1);
+            mbar_init(&xempty[i], 8);   // the eight epilogue warps
         }
-        for (int a = 0; a < NS; ++a) {
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(&bfull[i], 1);
+            mbar_init(&bempty[i], 1);
+        }
+        for (int a = 0; a < kAdSlots; ++a) {
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], 8);
         }
@@ -139,7 +147,7 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
         abort_flag = 0;
     }
     if (warp == 1) {
-        tmem_alloc(&tmem_slot, (uint32_t)args.tmem_cols);
+        tmem_alloc(&tmem_slot, kAdSlots * kAdCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -149,22 +157,34 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // lane 0 streams A and the x chunks, lane 1 the Bt ring (independent waits)
         if (lane == 0) {
+            prefetch_tensormap(mx);
+            prefetch_tensormap(ma);
+            prefetch_tensormap(mb);
             mbar_arrive_expect_tx(&afull, (unsigned)(V * K::kABytes));
             for (int v = 0; v < V; ++v)
                 tma_load_2d(asm_ + v * K::kABytes, ma, 0, ((c * V + v) * args.L + l) * args.n + t0, &afull);
-            for (int i = 0; i < chunks && !anchor_vload(&abort_flag); ++i) {
-                const int s = i % S;
-                if (i >= S && !mbar_wait(&empty[s], (unsigned)(i / S - 1) & 1u)) {
+            for (int j = 0; j < chunks && !anchor_vload(&abort_flag); ++j) {
+                const int xi = j & 1;
+                if (j >= 2 && !mbar_wait(&xempty[xi], (unsigned)(j / 2 - 1) & 1u)) {
                     atomicOr(&abort_flag, 1);
                     break;
                 }
-                unsigned char* st = ring + s * args.stage_bytes;
-                mbar_arrive_expect_tx(&full[s], (unsigned)(kAdXBytes + V * K::kBBytes));
-                tma_load_4d(st, mx, i * kAdCols, t0, l, c, &full[s]);
-                for (int v = 0; v < V; ++v)
-                    tma_load_2d(st + kAdXBytes + v * args.bbox_bytes, mb, 0,
-                                ((c * V + v) * args.L + l) * args.F + i * kAdCols, &full[s]);
+                mbar_arrive_expect_tx(&xfull[xi], (unsigned)kAdXBytes);
+                for (int b = 0; b < 2; ++b)
+                    tma_load_4d(xs + xi * kAdXBytes + b * (kAnRows * 128), mx, j * kAdCols + 64 * b, t0, l, c,
+                                &xfull[xi]);
+            }
+        } else if (lane == 1) {
+            for (int q = 0; q < total && !anchor_vload(&abort_flag); ++q) {
+                const int j = q / V, v = q % V, e = q % NB;
+                if (q >= NB && !mbar_wait(&bempty[e], (unsigned)(q / NB - 1) & 1u)) {
+                    atomicOr(&abort_flag, 1);
+                    break;
+                }
+                mbar_arrive_expect_tx(&bfull[e], (unsigned)K::kBBytes);
+                tma_load_2d(bs + e * K::kBBytes, mb, 0, ((c * V + v) * args.L + l) * args.F + j * kAdCols, &bfull[e]);
             }
         }
     } else if (warp == 1) {
@@ -172,81 +192,107 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
         if (lane == 0) {
             constexpr uint32_t idesc = tc_idesc_bf16(kAnRows, kAdCols);
             bool ok = mbar_wait(&afull, 0u);
-            if (!ok) atomicOr(&abort_flag, 1);
             tc_fence_after();
-            for (int i = 0; ok && i < chunks && !anchor_vload(&abort_flag); ++i) {
-                const int s = i % S, a = i % NS;
-                if (!mbar_wait(&full[s], (unsigned)(i / S) & 1u) ||
-                    (i >= NS && !mbar_wait(&tempty[a], (unsigned)(i / NS - 1) & 1u))) {
-                    atomicOr(&abort_flag, 1);
+            for (int q = 0; ok && q < total && !anchor_vload(&abort_flag); ++q) {
+                const int v = q % V, e = q % NB, a = q % kAdSlots;
+                if ((q >= kAdSlots && !mbar_wait(&tempty[a], (unsigned)(q / kAdSlots - 1) & 1u)) ||
+                    !mbar_wait(&bfull[e], (unsigned)(q / NB) & 1u)) {
+                    ok = false;
                     break;
                 }
                 tc_fence_after();
-                const unsigned char* bt = ring + s * args.stage_bytes + kAdXBytes;
-                for (int v = 0; v < V; ++v) {
 #pragma unroll
-                    for (int kk = 0; kk < R / 16; ++kk) {
-                        const uint64_t adesc = tc_smem_desc(asm_ + v * K::kABytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
-                        const uint64_t bdesc = tc_smem_desc(bt + v * args.bbox_bytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
-                        tc_mma_bf16(tmem + a * slot_cols + v * kAdCols, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
-                    }
+                for (int kk = 0; kk < R / 16; ++kk) {
+                    const uint64_t adesc = tc_smem_desc(asm_ + v * K::kABytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
+                    const uint64_t bdesc = tc_smem_desc(bs + e * K::kBBytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
+                    tc_mma_bf16(tmem + a * kAdCols, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
                 }
+                tc_commit(&bempty[e]);
                 tc_commit(&tfull[a]);
-                tc_commit(&empty[s]);
             }
+            if (!ok) atomicOr(&abort_flag, 1);
         }
     } else {
         // ------------------------------------------------------------ epilogue
         const int ew = warp - 2;              // 0..7
         const int wq = warp & 3;              // TMEM lane quarter this warp may read
-        const int half = ew >> 2;             // which 8 of the chunk's 16 features
+        const int half = ew >> 2;             // which 64 of the chunk's 128 features
         const int m = 32 * wq + lane;         // tile row of this thread
         const bool row_ok = t0 + m < args.rows;
         float acc[kAnMaxAnchors];
 #pragma unroll
         for (int v = 0; v < kAnMaxAnchors; ++v) acc[v] = 0.f;
-        for (int i = 0; i < chunks; ++i) {
-            const int s = i % S, a = i % NS;
-            bool ok = !anchor_vload(&abort_flag) && mbar_wait(&tfull[a], (unsigned)(i / NS) & 1u) &&
-                      mbar_wait(&full[s], (unsigned)(i / S) & 1u);
-            if (!ok) {
-                atomicOr(&abort_flag, 1);
+        bool ok = true;
+        for (int j = 0; ok && j < chunks; ++j) {
+            const int xi = j & 1;
+            if (anchor_vload(&abort_flag) || !mbar_wait(&xfull[xi], (unsigned)(j / 2) & 1u)) {
+                ok = false;
                 break;
             }
-            tc_fence_after();
-            const uint4 xv = *reinterpret_cast<const uint4*>(ring + s * args.stage_bytes + m * (kAdCols * 2) + half * 16);
-            float xf[8];
-            unpack8(xv, xf);
-            const uint32_t tbase = tmem + ((uint32_t)(32 * wq) << 16) + a * slot_cols + half * 8;
+            // this row's 64 features of the chunk, as float pairs
+            float2 x2[32];
+            const unsigned char* xrow = xs + xi * kAdXBytes + half * (kAnRows * 128) + m * 128;
 #pragma unroll
-            for (int v = 0; v < kAnMaxAnchors; v += 2) {
-                if (v >= V) break;
-                uint32_t r0[8], r1[8];
-                tmem_ld8(tbase + v * kAdCols, r0);
-                if (v + 1 < V) tmem_ld8(tbase + (v + 1) * kAdCols, r1);
-                tmem_wait_ld();
+            for (int q = 0; q < 8; ++q) {
+                const uint4 u = *reinterpret_cast<const uint4*>(xrow + ((q ^ (m & 7)) << 4));
+                const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float d0 = xf[e] - __uint_as_float(r0[e]);
-                    if (MODE == kAdGate) acc[v] = fmaf(d0, d0, acc[v]);
-                    else acc[v] += fabsf(d0);
-                }
-                if (v + 1 < V) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float d1 = xf[e] - __uint_as_float(r1[e]);
-                        if (MODE == kAdGate) acc[v + 1] = fmaf(d1, d1, acc[v + 1]);
-                        else acc[v + 1] += fabsf(d1);
-                    }
-                }
+                for (int e = 0; e < 4; ++e) x2[4 * q + e] = __bfloat1622float2(h2[e]);
             }
-            tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&tempty[a]);
-                mbar_arrive(&empty[s]);
+            if (lane == 0) mbar_arrive(&xempty[xi]);  // x is in registers now
+#pragma unroll
+            for (int v = 0; v < kAnMaxAnchors; ++v) {
+                if (v >= V) break;
+                const int q = j * V + v, a = q % kAdSlots;
+                if (!mbar_wait(&tfull[a], (unsigned)(q / kAdSlots) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t r0[32], r1[32];
+                const uint32_t tb = tmem + ((uint32_t)(32 * wq) << 16) + a * kAdCols + 64 * half;
+                tmem_ld32(tb, r0);
+                tmem_ld32(tb + 32, r1);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[a]);
+                const float2 neg = make_float2(-1.f, -1.f);
+                if (MODE == kAdGate) {
+                    float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 d = __ffma2_rn(make_float2(__uint_as_float(r0[2 * e]), __uint_as_float(r0[2 * e + 1])),
+                                                    neg, x2[e]);
+                        s2 = __ffma2_rn(d, d, s2);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 d = __ffma2_rn(make_float2(__uint_as_float(r1[2 * e]), __uint_as_float(r1[2 * e + 1])),
+                                                    neg, x2[16 + e]);
+                        s2 = __ffma2_rn(d, d, s2);
+                    }
+                    acc[v] += s2.x + s2.y;
+                } else {
+                    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 d = __ffma2_rn(make_float2(__uint_as_float(r0[2 * e]), __uint_as_float(r0[2 * e + 1])),
+                                                    neg, x2[e]);
+                        s0 += fabsf(d.x) + fabsf(d.y);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 d = __ffma2_rn(make_float2(__uint_as_float(r1[2 * e]), __uint_as_float(r1[2 * e + 1])),
+                                                    neg, x2[16 + e]);
+                        s1 += fabsf(d.x) + fabsf(d.y);
+                    }
+                    acc[v] += s0 + s1;
+                }
             }
         }
+        if (!ok) atomicOr(&abort_flag, 1);
         // both halves of a row: the second half adds its sums into the first's (the loops
         // run to the fixed bound so that the sums stay in registers)
         if (half == 1) {
@@ -303,24 +349,35 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
     __syncthreads();
     if (abort_flag && threadIdx.x == 0) atomicOr(&g_status_anchor, FLAG_TIMEOUT);
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, (uint32_t)args.tmem_cols);
+    if (warp == 1) tmem_dealloc(tmem, kAdSlots * kAdCols);
 }
 
 // ------------------------------------------------------------------ gate
 
-// One warp per segment: d_v = sqrt(sum over layers and tiles of the per-tile sums, in
-// that order, in double), g = softmax(-d / T), Hbar = -sum g log2 g / log2 V, accepted
-// iff V >= 2 and Hbar <= tau.
-__global__ void anchor_gate_kernel(const float* __restrict__ partial, int V, int L, int tiles, double T,
-                                   double tau, double* d, double* g, double* hbar, int32_t* accept) {
-    const int c = blockIdx.x, v = threadIdx.x;
-    double dv = 0.0;
-    if (v < V) {
+// One CTA per segment, one warp per anchor: d_v = sqrt(sum of the per-tile sums over
+// layers and tiles, lane j taking every 32nd in double, lanes folded by a fixed tree);
+// then warp 0: g = softmax(-d / T), Hbar = -sum g log2 g / log2 V, accepted iff V >= 2 and
+// Hbar <= tau.
+__global__ void __launch_bounds__(32 * kAnMaxAnchors)
+anchor_gate_kernel(const float* __restrict__ partial, int V, int L, int tiles, double T, double tau, double* d,
+                   double* g, double* hbar, int32_t* accept) {
+    __shared__ double ds[kAnMaxAnchors];
+    const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = L * tiles;
+    if (warp < V) {
         double s = 0.0;
-        for (int lt = 0; lt < L * tiles; ++lt) s += (double)partial[((long long)c * L * tiles + lt) * V + v];
-        dv = sqrt(s);
-        d[(long long)c * V + v] = dv;
+        for (int lt = lane; lt < n; lt += 32) s += (double)partial[((long long)c * n + lt) * V + warp];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) {
+            ds[warp] = sqrt(s);
+            d[(long long)c * V + warp] = ds[warp];
+        }
     }
+    __syncthreads();
+    if (warp != 0) return;
+    const int v = lane;
+    const double dv = v < V ? ds[v] : 0.0;
     double dmin = v < V ? dv : 1e308;
     for (int o = 16; o > 0; o >>= 1) dmin = fmin(dmin, __shfl_xor_sync(0xffffffffu, dmin, o));
     const double e = v < V ? exp(-(dv - dmin) / T) : 0.0;
@@ -340,8 +397,8 @@ __global__ void anchor_gate_kernel(const float* __restrict__ partial, int V, int
 // ------------------------------------------------------------------ apply
 
 constexpr int kApThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kApMaxB = 8;            // Bt ring entries (one anchor's head slab each)
-constexpr int kApMaxX = 3;            // x head slabs
+constexpr int kApMaxB = 16;           // Bt ring entries (one anchor's head slab each)
+constexpr int kApMaxX = 2;            // x head slabs
 
 struct ApArgs {
     int V, L, n, H, C;
@@ -423,7 +480,12 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // lane 0 streams A and the x slabs, lane 1 the Bt ring (independent waits)
         if (lane == 0) {
+            prefetch_tensormap(mx);
+            prefetch_tensormap(mo);
+            prefetch_tensormap(ma);
+            prefetch_tensormap(mb);
             mbar_arrive_expect_tx(&afull, (unsigned)(V * K::kABytes));
             for (int v = 0; v < V; ++v)
                 tma_load_2d(asm_ + v * K::kABytes, ma, 0, ((c * V + v) * args.L + l) * args.n + t0, &afull);
@@ -436,20 +498,16 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
                 mbar_arrive_expect_tx(&xfull[xi], (unsigned)K::kXBytes);
                 for (int b = 0; b < D / 64; ++b)
                     tma_load_4d(xs + xi * K::kXBytes + b * (kAnRows * 128), mx, h * D + 64 * b, t0, l, c, &xfull[xi]);
-                bool ok = true;
-                for (int v = 0; v < V; ++v) {
-                    const int q = h * V + v, e = q % NB;
-                    if (q >= NB && !mbar_wait(&bempty[e], (unsigned)(q / NB - 1) & 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&bfull[e], (unsigned)K::kBBytes);
-                    tma_load_2d(bs + e * K::kBSlot, mb, 0, ((c * V + v) * args.L + l) * F + h * D, &bfull[e]);
-                }
-                if (!ok) {
+            }
+        } else if (lane == 1) {
+            for (int q = 0; q < H * V && !anchor_vload(&abort_flag); ++q) {
+                const int h = q / V, v = q % V, e = q % NB;
+                if (q >= NB && !mbar_wait(&bempty[e], (unsigned)(q / NB - 1) & 1u)) {
                     atomicOr(&abort_flag, 1);
                     break;
                 }
+                mbar_arrive_expect_tx(&bfull[e], (unsigned)K::kBBytes);
+                tma_load_2d(bs + e * K::kBSlot, mb, 0, ((c * V + v) * args.L + l) * F + h * D, &bfull[e]);
             }
         }
     } else if (warp == 1) {
@@ -624,27 +682,21 @@ static cudaError_t anchor_factor_map(CUtensorMap* map, const void* base, long lo
 static int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
 // Static shared memory of the kernels, kept out of the dynamic budget.
-constexpr int kAdStaticBytes = 12 * 1024;
+constexpr int kAdStaticBytes = 10 * 1024;
 constexpr int kApStaticBytes = 2 * 1024;
 
 struct AdShape {
-    int stages, slots, stage_bytes, bbox, smem, cols;
+    int nb, smem;
 };
 
 static bool ad_shape(int V, int r, AdShape* s) {
     const int row = 2 * r;
     const int abytes = kAnRows * row, bbytes = kAdCols * row;
-    s->bbox = bbytes < 1024 ? 1024 : bbytes;
-    s->stage_bytes = round_up(kAdXBytes + V * s->bbox, 1024);
-    const int budget = kAnSmemLimit - kAdStaticBytes - 1024 - V * abytes;
-    s->stages = budget / s->stage_bytes;
-    if (s->stages > kAdMaxStages) s->stages = kAdMaxStages;
-    s->slots = 512 / (V * kAdCols);
-    if (s->slots > 4) s->slots = 4;
-    s->smem = 1024 + V * abytes + s->stages * s->stage_bytes;
-    s->cols = 32;
-    while (s->cols < s->slots * V * kAdCols) s->cols *= 2;
-    return V >= 1 && V <= kAnMaxAnchors && s->stages >= 2 && s->slots >= 1;
+    const int budget = kAnSmemLimit - kAdStaticBytes - 1024 - V * abytes - 2 * kAdXBytes;
+    s->nb = budget / bbytes;
+    if (s->nb > kAdMaxB) s->nb = kAdMaxB;
+    s->smem = 1024 + V * abytes + 2 * kAdXBytes + s->nb * bbytes;
+    return V >= 1 && V <= kAnMaxAnchors && s->nb >= 2;
 }
 
 struct ApShape {
@@ -681,11 +733,7 @@ static cudaError_t launch_dist(const CUtensorMap* mx, const CUtensorMap* ma, con
                                int planes, cudaStream_t s) {
     AdShape sh;
     if (!ad_shape(args.V, R, &sh)) return cudaErrorInvalidValue;
-    args.stages = sh.stages;
-    args.slots = sh.slots;
-    args.stage_bytes = sh.stage_bytes;
-    args.bbox_bytes = sh.bbox;
-    args.tmem_cols = sh.cols;
+    args.nb = sh.nb;
     cudaError_t e = cudaFuncSetAttribute(anchor_dist_kernel<R, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, sh.smem);
     if (e != cudaSuccess) return e;
     dim3 grid(args.tiles, args.L, planes * args.C);
@@ -702,7 +750,7 @@ static cudaError_t dist_maps_and_launch(const uint16_t* const* x, const Plane& p
     const long long brows = (long long)args.C * args.V * args.L * args.F;
     for (int q = 0; q < 2; ++q) {
         const int src = q < planes ? q : 0;
-        if ((e = anchor_plane_map(&mx[q], x[src], p, kAdCols, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
+        if ((e = anchor_plane_map(&mx[q], x[src], p, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
         if ((e = anchor_factor_map(&ma[q], ac[src], arows, R, kAnRows)) != cudaSuccess) return e;
         if ((e = anchor_factor_map(&mb[q], bct[src], brows, R, kAdCols)) != cudaSuccess) return e;
     }
@@ -732,7 +780,7 @@ cudaError_t launch_anchor_gate(const uint16_t* v_src, const kvfix_kv_desc& d, co
     else if (r == 32) e = dist_maps_and_launch<32, kAdGate>(xs, p, as, bs, args, 1, s);
     else e = dist_maps_and_launch<64, kAdGate>(xs, p, as, bs, args, 1, s);
     if (e != cudaSuccess) return e;
-    anchor_gate_kernel<<<p.chunks, 32, 0, s>>>(args.partial, V, p.layers, args.tiles, T, tau, dist, g, hbar, accept);
+    anchor_gate_kernel<<<p.chunks, 32 * kAnMaxAnchors, 0, s>>>(args.partial, V, p.layers, args.tiles, T, tau, dist, g, hbar, accept);
     return cudaGetLastError();
 }
 

@@ -445,6 +445,8 @@ static kvfix_status check_anchor_shape(const kvfix_kv_desc& d, int32_t anchors, 
                                        const char* fn) {
     if (anchors < 1 || anchors > 16) return fail(KVFIX_EINVAL, "%s: anchors must be in [1, 16]", fn);
     if (rank != 16 && rank != 32 && rank != 64) return fail(KVFIX_EINVAL, "%s: rank must be 16, 32 or 64", fn);
+    if ((d.kv_heads * d.head_dim) % 128 != 0)
+        return fail(KVFIX_EINVAL, "%s: kv_heads * head_dim must be a multiple of 128", fn);
     if (!anchor_shape_ok(anchors, rank, head_dim))
         return fail(KVFIX_EINVAL, "%s: %d anchors of rank %d do not fit in shared memory", fn, anchors, rank);
     const long long rows = (long long)d.chunks * anchors * d.layers *

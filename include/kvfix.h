@@ -351,7 +351,7 @@ KVFIX_API kvfix_status kvfix_diff_restore(const kvfix_bf16* master_k, const kvfi
  *     Bt : device bf16 [C][V][L][F][r]        (second factor, stored transposed)
  * so that anchor v's state of layer l is A[c][v][l] * Bt[c][v][l]^T ([n x F]).
  * anchors: 1..16; rank: 16, 32 or 64 (anchors * rank limited by shared memory: the call
- * returns KVFIX_EINVAL for shapes that do not fit).
+ * returns KVFIX_EINVAL for shapes that do not fit); F must be a multiple of 128.
  */
 
 /* Bytes of device workspace kvfix_anchor_gate needs for `src`, `anchors` and `prefix`. */
