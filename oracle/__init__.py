@@ -66,6 +66,7 @@ def _load():
             "oracle_diff_gather": (None, [P, P, P, P, P, I, I, I, I, I, I, P, P]),
             "oracle_diff_restore": (None, [P, P, P, P, P, I, I, I, I, I, I, P, D, P, I64, P, P]),
             "oracle_anchor_gate": (None, [P, P, P, I, I, I, I, I, I, I, D, D, P, P, P, P]),
+            "oracle_repair_layout": (I, [P, I, I, I, I, I, I, D, I, P, I, P]),
             "oracle_anchor_weights": (None, [P, P, P, I, I, I, I, I, I, D, P]),
             "oracle_anchor_correct": (None, [P, P, P, P, I, I, I, I, I, I, I, P, D, I, P]),
         }
@@ -356,3 +357,23 @@ def anchor_correct(x, a_d, b_dt, w, heads: int, delta, rope_base: float, rotate:
     _load().oracle_anchor_correct(_p(x), _p(a), _p(b), _p(w), C, V, L, n, H, F // H, r, _p(dl),
                                   float(rope_base), int(bool(rotate)), _p(out))
     return out
+
+
+# ------------------------------------------------------------ repair layouts
+
+LAYOUT_SINGLE, LAYOUT_CHUNK, LAYOUT_GROW = 0, 1, 2
+
+
+def repair_layout(scores, layout: int, chunk_tokens: int = 64, budget=(1, 5), tau: float = 0.25,
+                  skip: bool = True, max_rows=None):
+    """scores [U][n] float64 -> (idx [U][max_rows] int32 ascending then -1, counts [U])."""
+    sc = np.ascontiguousarray(scores, dtype=np.float64)
+    if sc.ndim == 1:
+        sc = sc[None]
+    U, n = sc.shape
+    max_rows = n if max_rows is None else int(max_rows)
+    idx = np.empty((U, max(max_rows, 1)), np.int32)
+    counts = np.empty(U, np.int32)
+    _load().oracle_repair_layout(_p(sc), U, n, int(layout), int(chunk_tokens), int(budget[0]), int(budget[1]),
+                                 float(tau), int(bool(skip)), _p(idx), max(max_rows, 1), _p(counts))
+    return idx[:, :max_rows], counts

@@ -717,3 +717,95 @@ EXPORT void oracle_anchor_correct(const uint16_t* x, const uint16_t* ad, const u
         free(y);
     }
 }
+
+/* ------------------------------------------------------------ repair layouts */
+
+/* p / q rounded to the nearest integer, halves to even (p, q >= 0, q > 0). */
+static int64_t round_half_even(int64_t p, int64_t q)
+{
+    int64_t f = p / q, r = p - f * q;
+    if (2 * r > q || (2 * r == q && (f & 1))) ++f;
+    return f;
+}
+
+/*
+ * Rows to repair from per-row draft scores, in the three layouts of Budgeted Cache
+ * Repair (section 3 "The layouts"; App. A.2 "The policy" step 2 and Table 8; App. B,
+ * Algorithm 1 lines 1-2 and Algorithm 2 line 5), for each unit u of scores [U][n]:
+ *   layout 0 (single): the round(rho n) rows with the largest scores;
+ *   layout 1 (chunk):  B-token chunks (the last one may be short), each scored by the mean
+ *                      of its rows' scores; the max(1, round(rho n / B)) best chunks, all
+ *                      their rows; with skip != 0, no rows when n < 2B or rho n < B;
+ *   layout 2 (grow):   round(rho n) rows: the best unselected row seeds a span, which
+ *                      takes the better of its two unselected neighbours while that one
+ *                      scores at least tau times the seed, until neither qualifies or the
+ *                      budget is spent; then the next seed.
+ * Ties go to the lower index (rows, chunks, and left before right).  rho = num / den,
+ * rounding halves to even.  Writes the rows ascending into idx [U][max_rows] (then -1)
+ * and their number into counts [U]; returns the largest count.
+ */
+EXPORT int oracle_repair_layout(const double* scores, int U, int n, int layout, int B, int num, int den,
+                                double tau, int skip, int32_t* idx, int max_rows, int32_t* counts)
+{
+    int most = 0;
+    for (int u = 0; u < U; ++u) {
+        const double* s = scores + (int64_t)u * n;
+        unsigned char* sel = (unsigned char*)calloc((size_t)n + 1, 1);
+        int chosen = 0;
+        if (layout == 0 || layout == 2) {
+            int k = (int)round_half_even((int64_t)num * n, den);
+            if (k > n) k = n;
+            keyed* order = (keyed*)malloc(sizeof(keyed) * (size_t)(n > 0 ? n : 1));
+            for (int j = 0; j < n; ++j) order[j] = (keyed){s[j], j};
+            qsort(order, (size_t)n, sizeof(keyed), by_key_desc_idx_asc);
+            int p = 0;
+            while (chosen < k) {
+                while (sel[order[p].idx]) ++p;
+                int seed = order[p].idx, lo = seed, hi = seed;
+                sel[seed] = 1;
+                ++chosen;
+                if (layout == 0) continue;
+                double thr = tau * s[seed];
+                while (chosen < k) {
+                    int l_ok = lo > 0 && !sel[lo - 1] && s[lo - 1] >= thr;
+                    int r_ok = hi < n - 1 && !sel[hi + 1] && s[hi + 1] >= thr;
+                    if (!l_ok && !r_ok) break;
+                    if (l_ok && (!r_ok || s[lo - 1] >= s[hi + 1])) sel[--lo] = 1;
+                    else sel[++hi] = 1;
+                    ++chosen;
+                }
+            }
+            free(order);
+        } else {
+            int nch = (n + B - 1) / B;
+            int skipped = skip && (n < 2 * B || (int64_t)num * n < (int64_t)den * B);
+            int c = (int)round_half_even((int64_t)num * n, (int64_t)den * B);
+            if (c < 1) c = 1;
+            if (c > nch) c = nch;
+            if (!skipped && nch > 0) {
+                keyed* order = (keyed*)malloc(sizeof(keyed) * (size_t)nch);
+                for (int i = 0; i < nch; ++i) {
+                    int a = i * B, b = a + B < n ? a + B : n;
+                    double sum = 0.0;
+                    for (int j = a; j < b; ++j) sum += s[j];
+                    order[i] = (keyed){sum / (b - a), i};
+                }
+                qsort(order, (size_t)nch, sizeof(keyed), by_key_desc_idx_asc);
+                for (int t = 0; t < c; ++t) {
+                    int a = order[t].idx * B, b = a + B < n ? a + B : n;
+                    for (int j = a; j < b; ++j) sel[j] = 1;
+                    chosen += b - a;
+                }
+                free(order);
+            }
+        }
+        int w = 0;
+        for (int j = 0; j < n; ++j)
+            if (sel[j] && w < max_rows) idx[(int64_t)u * max_rows + w++] = j;
+        for (int t = w; t < max_rows; ++t) idx[(int64_t)u * max_rows + t] = -1;
+        counts[u] = chosen;
+        if (chosen > most) most = chosen;
+        free(sel);
+    }
+    return most;
+}

@@ -671,3 +671,101 @@ def test_anchor_correct_is_weighted_sum_of_anchor_deltas():
     rot = oracle.rotate_f64(oracle.bf16_decode(x).reshape(C, L, n, H, D), 55, 5e5).reshape(x.shape)
     ref = rot + np.einsum("clnv,cvlnf->clnf", w, _recon(ad, bd))
     np.testing.assert_allclose(oracle.bf16_decode(out), ref, rtol=2.0 ** -8, atol=1e-6)
+
+
+# ------------------------------------------------------------ repair layouts
+
+def test_chunk_budgets_reproduce_table8():
+    """The chunk budget max(1, round(rho n / B)) reproduces every printed budget of the
+    unit-of-choice table (no skip rule there: the whole-segment row is a single chunk)."""
+    rows = _golden("bcr_table8_budgets.txt")
+    rng = np.random.default_rng(51)
+    s = rng.random((1, 2048))
+    for key, (unit, pct) in rows.items():
+        _, counts = oracle.repair_layout(s, oracle.LAYOUT_CHUNK, chunk_tokens=int(unit), budget=(1, 5), skip=False)
+        assert round(100.0 * counts[0] / 2048, 1) == pct, key
+
+
+def test_chunk_skip_rule_and_short_last_chunk():
+    rng = np.random.default_rng(52)
+    s = rng.random((1, 200))
+    assert oracle.repair_layout(s, oracle.LAYOUT_CHUNK, 128, (1, 5))[1][0] == 0       # n < 2B
+    assert oracle.repair_layout(s, oracle.LAYOUT_CHUNK, 64, (1, 5))[1][0] == 0        # rho n < B
+    means = [s[0, a:a + 64].mean() for a in (0, 64, 128, 192)]
+    best = int(np.argmax(means))
+    assert oracle.repair_layout(s, oracle.LAYOUT_CHUNK, 64, (1, 3))[1][0] == (8 if best == 3 else 64)
+    # a short last chunk is scored by its own mean: make it the best
+    s2 = np.zeros((1, 200))
+    s2[0, 192:] = 1.0
+    s2[0, :64] = 0.9
+    idx, cnt = oracle.repair_layout(s2, oracle.LAYOUT_CHUNK, 64, (1, 2))
+    assert cnt[0] == 64 + 8 and list(idx[0, :cnt[0]]) == list(range(64)) + list(range(192, 200))
+
+
+def test_chunk_layout_is_best_subset_by_brute_force():
+    """Top chunks by mean = the chunk subset of the budget's size with the largest sum of
+    means (distinct means), found by enumeration."""
+    rng = np.random.default_rng(53)
+    for trial in range(20):
+        n, B = int(rng.integers(12, 40)), int(rng.integers(2, 7))
+        s = rng.random((1, n))
+        idx, cnt = oracle.repair_layout(s, oracle.LAYOUT_CHUNK, B, (1, 3), skip=False)
+        nch = (n + B - 1) // B
+        means = [s[0, i * B:min(n, i * B + B)].mean() for i in range(nch)]
+        c = max(1, int(round(n / (3 * B))))
+        c = min(c, nch)
+        best = max(itertools.combinations(range(nch), c), key=lambda sub: sum(means[i] for i in sub))
+        rows = sorted(j for i in best for j in range(i * B, min(n, i * B + B)))
+        assert list(idx[0, :cnt[0]]) == rows
+
+
+def test_single_layout_matches_lexsort():
+    rng = np.random.default_rng(54)
+    s = np.round(rng.random((3, 500)) * 50) / 50            # many ties
+    idx, cnt = oracle.repair_layout(s, oracle.LAYOUT_SINGLE, budget=(1, 10))
+    for u in range(3):
+        top = np.lexsort((np.arange(500), -s[u]))[:50]
+        assert cnt[u] == 50 and list(idx[u, :50]) == sorted(top)
+
+
+def _spans(rows):
+    rows = sorted(rows)
+    out, start = [], rows[0]
+    for a, b in zip(rows, rows[1:] + [None]):
+        if b != a + 1:
+            out.append((start, a))
+            start = b
+    return out
+
+
+def test_grow_layout_invariants_and_limits():
+    rng = np.random.default_rng(55)
+    n = 400
+    s = rng.random((2, n)) ** 3
+    k = 80
+    # tau > 1: nothing grows, the single layout
+    g, cg = oracle.repair_layout(s, oracle.LAYOUT_GROW, budget=(1, 5), tau=1.5)
+    t, ct = oracle.repair_layout(s, oracle.LAYOUT_SINGLE, budget=(1, 5))
+    assert np.array_equal(g, t) and np.array_equal(cg, ct)
+    # tau = 0: one span of k rows around the best row
+    g, cg = oracle.repair_layout(s, oracle.LAYOUT_GROW, budget=(1, 5), tau=0.0)
+    for u in range(2):
+        rows = list(g[u, :cg[u]])
+        assert cg[u] == k and _spans(rows) == [(rows[0], rows[-1])] and int(np.argmax(s[u])) in rows
+    # tau = 0.25: exactly k distinct rows, the best row among them, fewer spans than with
+    # no growth at all and more than with unlimited growth
+    g, cg = oracle.repair_layout(s, oracle.LAYOUT_GROW, budget=(1, 5), tau=0.25)
+    for u in range(2):
+        rows = list(g[u, :cg[u]])
+        assert cg[u] == k and len(set(rows)) == k and int(np.argmax(s[u])) in rows
+        assert 1 < len(_spans(rows)) < len(_spans(list(t[u, :ct[u]])))
+
+
+def test_grow_layout_small_case_by_hand():
+    """A worked case: scores 1 5 4 0.9 0.1 8 7 0.5, budget 4 of 8 rows (rho 1/2), tau 0.5.
+    Seed 5 (8): left 0.1 < 4, right 6 (7) >= 4 -> {5,6}; then 7 (0.5) < 4, 4 (0.1) < 4:
+    span ends.  Next seed 1 (5): neighbours 0 (1) < 2.5, 2 (4) >= 2.5 -> {1,2}: budget
+    spent.  Rows 1 2 5 6."""
+    s = np.array([[1, 5, 4, 0.9, 0.1, 8, 7, 0.5]], dtype=np.float64)
+    idx, cnt = oracle.repair_layout(s, oracle.LAYOUT_GROW, budget=(1, 2), tau=0.5)
+    assert cnt[0] == 4 and list(idx[0, :4]) == [1, 2, 5, 6]
