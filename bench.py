@@ -465,6 +465,31 @@ def stage_lowrank(kvfix, peak, steps=3, warmup=2):
     dr_bytes = (C * nl * n * H * D * 2) + 2 * contrib_bytes + 2 * 2 * (C * L * cfg.k_rows * H * D * 2)
     lr, dr = statistics.mean(lr_ms), statistics.mean(dr_ms)
     flops = 2 * 2 * C * L * H * n * r * D + 2 * C * nl * H * 16 * n * D
+    # the chunk and grow layouts of the same draft scores, each followed by the row repair
+    _, scores = kvfix.draft_rank(kt, inp["q"], cfg.layer_begin, 1, workspace=ws)
+    lay = {}
+    for name, lay_args in (("chunk64", (kvfix.LAYOUT_CHUNK, 64, (cfg.budget_num, cfg.budget_den), 0.25, True)),
+                           ("grow", (kvfix.LAYOUT_GROW, 1, (cfg.budget_num, cfg.budget_den), 0.25, True))):
+        sel_ms, rep_ms = [], []
+        for s in range(warmup + steps):
+            flush.zero_()
+            host_lead()
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            lidx, lcnt = kvfix.repair_layout(scores, *lay_args)
+            e1.record(stream)
+            kvfix.repair_rows(kt, vt, inp["fresh_k"], inp["fresh_v"], lidx, lcnt)
+            e2.record(stream)
+            torch.cuda.synchronize()
+            if s >= warmup:
+                sel_ms.append(e0.elapsed_time(e1))
+                rep_ms.append(e1.elapsed_time(e2))
+        rows = int(lcnt.sum().item())
+        rep_bytes = 2 * 2 * rows * L * H * D * 2
+        rep = statistics.mean(rep_ms)
+        lay[name] = {"select_ms": round(statistics.mean(sel_ms), 4), "rows": rows, "repair_ms": round(rep, 4),
+                     "repair_GBps": round(rep_bytes / rep / 1e6, 1), "repair_frac": round(rep_bytes / rep / 1e6 / peak, 4)}
+    kvfix.check_status()
     res = {"workload": "lowrank_70b: 4 chunks x 16384 tokens, 80 layers, 8 KV / 64 query heads x 128, rank 16, top 5% rows",
            "ms_per_step": round(lr + dr, 4),
            "corrected_GBps": round(2 * plane / (lr + dr) / 1e6, 1),
@@ -473,7 +498,8 @@ def stage_lowrank(kvfix, peak, steps=3, warmup=2):
            "lowrank_apply": {"ms": round(lr, 4), "algorithmic_bytes": lr_bytes,
                              "GBps": round(lr_bytes / lr / 1e6, 1), "frac": round(lr_bytes / lr / 1e6 / peak, 4)},
            "draft_rank": {"ms": round(dr, 4), "algorithmic_bytes": dr_bytes,
-                          "GBps": round(dr_bytes / dr / 1e6, 1), "frac": round(dr_bytes / dr / 1e6 / peak, 4)}}
+                          "GBps": round(dr_bytes / dr / 1e6, 1), "frac": round(dr_bytes / dr / 1e6 / peak, 4)},
+           "layouts": lay}
     del inp, kt, vt, ws, flush
     torch.cuda.empty_cache()
     return res

@@ -105,7 +105,7 @@ kvfix_status kvfix_check_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "kvfix_check_status: stream synchronize");
     unsigned bits = read_status_repair(s) | read_status_diff(s) | read_status_draft(s) | read_status_lowrank(s) |
-                    read_status_anchor(s);
+                    read_status_anchor(s) | read_status_layout(s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kvfix_check_status: status read");
     if (bits & 4u) return fail(KVFIX_ETIMEOUT, "a bounded device wait gave up");
@@ -537,6 +537,77 @@ kvfix_status kvfix_anchor_correct(const kvfix_bf16* k_src, const kvfix_bf16* v_s
     return launched(launch_anchor_correct(pl, src, out, anchors, rank, temperature, delta, th, accept,
                                           (cudaStream_t)stream),
                     fn);
+}
+
+// p / q rounded to the nearest integer, halves to even (p >= 0, q > 0).
+static long long round_half_even(long long p, long long q) {
+    long long f = p / q, r = p - f * q;
+    if (2 * r > q || (2 * r == q && (f & 1))) ++f;
+    return f;
+}
+
+kvfix_status kvfix_repair_layout(const double* scores, int32_t units, int32_t tokens, int32_t layout,
+                                 int32_t chunk_tokens, int32_t budget_num, int32_t budget_den, double tau,
+                                 int32_t skip_rule, int32_t* idx, int32_t max_rows, int32_t* counts,
+                                 void* stream) {
+    const char* fn = "kvfix_repair_layout";
+    if (units < 0 || units > 65535) return fail(KVFIX_EINVAL, "%s: units must be in [0, 65535]", fn);
+    if (tokens < 1 || tokens > 16384) return fail(KVFIX_EINVAL, "%s: tokens must be in [1, 16384]", fn);
+    if (layout < 0 || layout > 2) return fail(KVFIX_EINVAL, "%s: unknown layout %d", fn, layout);
+    if (layout == 1 && chunk_tokens < 1) return fail(KVFIX_EINVAL, "%s: chunk_tokens must be >= 1", fn);
+    if (budget_den < 1 || budget_num < 0 || budget_num > budget_den)
+        return fail(KVFIX_EINVAL, "%s: the budget must be a fraction in [0, 1]", fn);
+    if (!isfinite(tau)) return fail(KVFIX_EINVAL, "%s: tau must be finite", fn);
+    if (units > 0 && (!scores || !idx || !counts)) return fail(KVFIX_EINVAL, "%s: scores, idx and counts are required", fn);
+    const long long n = tokens;
+    int k = 0, c = 0, skipped = 0;
+    long long need;
+    if (layout == 1) {
+        const long long B = chunk_tokens, nch = (n + B - 1) / B;
+        skipped = skip_rule && (n < 2 * B || (long long)budget_num * n < (long long)budget_den * B);
+        long long cc = round_half_even((long long)budget_num * n, (long long)budget_den * B);
+        if (cc < 1) cc = 1;
+        if (cc > nch) cc = nch;
+        c = (int)cc;
+        need = skipped ? 0 : (cc * B < n ? cc * B : n);
+    } else {
+        k = (int)round_half_even((long long)budget_num * n, budget_den);
+        need = k;
+    }
+    if (max_rows < need || max_rows < 1)
+        return fail(KVFIX_EINVAL, "%s: max_rows %d is below the layout's %lld rows", fn, max_rows, need);
+    return launched(launch_repair_layout(scores, units, tokens, layout, chunk_tokens, k, c, skipped, tau, idx,
+                                         max_rows, counts, (cudaStream_t)stream),
+                    fn);
+}
+
+kvfix_status kvfix_repair_rows(kvfix_bf16* k_io, kvfix_bf16* v_io, kvfix_kv_desc desc, const kvfix_bf16* k_fresh,
+                               const kvfix_bf16* v_fresh, kvfix_kv_desc fresh_desc, const int32_t* idx,
+                               int32_t max_rows, const int32_t* counts, void* stream) {
+    const char* fn = "kvfix_repair_rows";
+    kvfix_status st;
+    if ((k_io == nullptr) != (k_fresh == nullptr) || (v_io == nullptr) != (v_fresh == nullptr))
+        return fail(KVFIX_EINVAL, "%s: each plane needs both its io and its fresh pointer, or neither", fn);
+    if (k_io && (st = check_plane(k_io, desc, "kvfix_repair_rows: k_io")) != KVFIX_OK) return st;
+    if (v_io && (st = check_plane(v_io, desc, "kvfix_repair_rows: v_io")) != KVFIX_OK) return st;
+    if (k_fresh && (st = check_plane(k_fresh, fresh_desc, "kvfix_repair_rows: k_fresh")) != KVFIX_OK) return st;
+    if (v_fresh && (st = check_plane(v_fresh, fresh_desc, "kvfix_repair_rows: v_fresh")) != KVFIX_OK) return st;
+    if (!same_shape(desc, fresh_desc) || desc.chunks != fresh_desc.chunks)
+        return fail(KVFIX_EINVAL, "%s: fresh planes must have the shape of desc", fn);
+    if (max_rows < 0) return fail(KVFIX_EINVAL, "%s: negative max_rows", fn);
+    if (max_rows > 0 && desc.chunks > 0 && (!idx || !counts)) return fail(KVFIX_EINVAL, "%s: idx and counts are required", fn);
+    if (desc.layers > 65535 || desc.chunks > 65535) return fail(KVFIX_EINVAL, "%s: too many layers or chunks", fn);
+    if ((k_io && (overlaps(k_io, desc, k_fresh, fresh_desc) || (v_fresh && overlaps(k_io, desc, v_fresh, fresh_desc)))) ||
+        (v_io && (overlaps(v_io, desc, v_fresh, fresh_desc) || (k_fresh && overlaps(v_io, desc, k_fresh, fresh_desc)))) ||
+        (k_io && v_io && overlaps(k_io, desc, v_io, desc)))
+        return fail(KVFIX_EINVAL, "%s: planes overlap", fn);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e;
+    if (k_io && (e = launch_row_repair(k_io, desc, k_fresh, fresh_desc, idx, max_rows, s, counts)) != cudaSuccess)
+        return cuda_fail(e, fn);
+    if (v_io && (e = launch_row_repair(v_io, desc, v_fresh, fresh_desc, idx, max_rows, s, counts)) != cudaSuccess)
+        return cuda_fail(e, fn);
+    return KVFIX_OK;
 }
 
 }  // extern "C"

@@ -540,13 +540,15 @@ cudaError_t launch_draft(const uint16_t* k, const kvfix_kv_desc& d, const uint16
 constexpr int kRepThreads = 256;
 constexpr int kRepRows = 16;
 
+// idx holds `kk` entries per chunk; with counts, only the first counts[c] are rows.
 __global__ void __launch_bounds__(kRepThreads)
 row_repair_kernel(uint16_t* io, Plane p, const uint16_t* __restrict__ fresh, Plane fp,
-                  const int32_t* __restrict__ idx, int kk) {
+                  const int32_t* __restrict__ idx, int kk, const int32_t* __restrict__ counts) {
     const int l = blockIdx.y, c = blockIdx.z;
     const int row8 = p.heads * p.dim / 8;
     const int i0 = blockIdx.x * kRepRows;
-    const int rows = min(kRepRows, kk - i0);
+    const int used = counts ? min(kk, counts[c]) : kk;
+    const int rows = min(kRepRows, used - i0);
     for (int it = threadIdx.x; it < rows * row8; it += kRepThreads) {
         const int i = i0 + it / row8, v = it % row8;
         const int j = idx[(long long)c * kk + i];
@@ -561,11 +563,11 @@ row_repair_kernel(uint16_t* io, Plane p, const uint16_t* __restrict__ fresh, Pla
 
 cudaError_t launch_row_repair(uint16_t* io, const kvfix_kv_desc& d, const uint16_t* fresh,
                               const kvfix_kv_desc& fd, const int32_t* idx, int k_rows,
-                              cudaStream_t s) {
+                              cudaStream_t s, const int32_t* counts) {
     Plane p = plane_of(d), fp = plane_of(fd);
     if (k_rows == 0 || p.layers == 0 || p.chunks == 0) return cudaSuccess;
     dim3 grid((k_rows + kRepRows - 1) / kRepRows, p.layers, p.chunks);
-    row_repair_kernel<<<grid, kRepThreads, 0, s>>>(io, p, fresh, fp, idx, k_rows);
+    row_repair_kernel<<<grid, kRepThreads, 0, s>>>(io, p, fresh, fp, idx, k_rows, counts);
     return cudaGetLastError();
 }
 

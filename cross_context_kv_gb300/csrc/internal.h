@@ -68,9 +68,18 @@ size_t draft_workspace_bytes(const kvfix_kv_desc& d, int layer_begin);
 cudaError_t launch_draft(const uint16_t* k, const kvfix_kv_desc& d, const uint16_t* q,
                          int steps, int q_heads, int layer_begin, int k_rows, int32_t* idx,
                          double* scores, void* ws, cudaStream_t s);
+// Rows idx[c][0 .. k_rows) (or the first counts[c] of them, counts non-null) of io are
+// overwritten with the same rows of fresh, every layer and head.
 cudaError_t launch_row_repair(uint16_t* io, const kvfix_kv_desc& d, const uint16_t* fresh,
                               const kvfix_kv_desc& fd, const int32_t* idx, int k_rows,
-                              cudaStream_t s);
+                              cudaStream_t s, const int32_t* counts = nullptr);
+
+// Repair layouts: one CTA per unit (tokens <= 16384).
+unsigned read_status_layout(cudaStream_t stream);
+size_t layout_smem_bytes(int n, int layout, int B, int k);
+cudaError_t launch_repair_layout(const double* scores, int units, int n, int layout, int B, int k, int c,
+                                 int skipped, double tau, int32_t* idx, int max_rows, int32_t* counts,
+                                 cudaStream_t s);
 
 cudaError_t launch_diff_mask(const uint16_t* mk, const uint16_t* mv, const kvfix_kv_desc& md,
                              const uint16_t* sk, const uint16_t* sv, const kvfix_kv_desc& sd,

@@ -51,6 +51,8 @@ SIGNATURES = {
     "kvfix_diff_encode": (ctypes.c_int, [P, P, D, P, P, D, I32, P, P, P, I64, P, P]),
     "kvfix_diff_gather": (ctypes.c_int, [P, P, D, P, P, P, I64, I32, I32, P, P, D, P]),
     "kvfix_diff_restore": (ctypes.c_int, [P, P, D, P, P, P, I64, I32, I32, P, F64, P, P, P, D, P]),
+    "kvfix_repair_layout": (ctypes.c_int, [P, I32, I32, I32, I32, I32, I32, F64, I32, P, I32, P, P]),
+    "kvfix_repair_rows": (ctypes.c_int, [P, P, D, P, P, D, P, I32, P, P]),
     "kvfix_anchor_gate_workspace_bytes": (SZ, [D, I32, I32]),
     "kvfix_anchor_gate": (ctypes.c_int, [P, D, P, P, I32, I32, I32, F64, F64, P, P, P, P, P, SZ, P]),
     "kvfix_anchor_correct": (ctypes.c_int, [P, P, D, P, P, P, P, P, P, P, P, I32, I32, F64, P, F64, P, P, P, P, P,
@@ -360,3 +362,48 @@ def anchor_correct(k_src, v_src, factors: dict, delta, rope_base: float, tempera
                                     float(rope_base), _ptr(accept), _ptr(w_k), _ptr(w_v), _ptr(out_k), _ptr(out_v),
                                     plane_desc(out_k), _stream(k_src)))
     return out_k, out_v, w_k, w_v
+
+
+LAYOUT_SINGLE, LAYOUT_CHUNK, LAYOUT_GROW = 0, 1, 2
+
+
+def _round_half_even(p: int, q: int) -> int:
+    f, r = divmod(p, q)
+    return f + (1 if 2 * r > q or (2 * r == q and f % 2) else 0)
+
+
+def layout_max_rows(tokens: int, layout: int, chunk_tokens: int = 64, budget=(1, 5)) -> int:
+    """The most rows a layout can choose (the size idx needs per unit)."""
+    num, den = budget
+    if layout == LAYOUT_CHUNK:
+        nch = -(-tokens // chunk_tokens)
+        c = min(nch, max(1, _round_half_even(num * tokens, den * chunk_tokens)))
+        return max(1, min(tokens, c * chunk_tokens))
+    return max(1, _round_half_even(num * tokens, den))
+
+
+def repair_layout(scores, layout: int, chunk_tokens: int = 64, budget=(1, 5), tau: float = 0.25,
+                  skip_rule: bool = True, max_rows: int | None = None):
+    """scores [units][tokens] float64 (CUDA) -> (idx [units][max_rows] int32, counts [units] int32)."""
+    if scores.dtype != torch.float64 or not scores.is_cuda or not scores.is_contiguous():
+        raise TypeError("scores must be a contiguous CUDA float64 tensor")
+    sc = scores if scores.dim() == 2 else scores.unsqueeze(0)
+    U, n = sc.shape
+    mr = layout_max_rows(n, layout, chunk_tokens, budget) if max_rows is None else int(max_rows)
+    idx = torch.empty((U, mr), dtype=torch.int32, device=sc.device)
+    counts = torch.empty(U, dtype=torch.int32, device=sc.device)
+    _check(lib.kvfix_repair_layout(_ptr(sc), U, n, int(layout), int(chunk_tokens), int(budget[0]), int(budget[1]),
+                                   float(tau), int(bool(skip_rule)), _ptr(idx), mr, _ptr(counts), _stream(sc)))
+    return idx, counts
+
+
+def repair_rows(k_io, v_io, k_fresh, v_fresh, idx, counts):
+    """Overwrite rows idx[c][:counts[c]] of k_io / v_io ([C][L][n][H][D]) with the fresh rows."""
+    for t, nm in ((k_io, "k_io"), (v_io, "v_io"), (k_fresh, "k_fresh"), (v_fresh, "v_fresh")):
+        _bf16(t, nm)
+    _i32(idx, "idx")
+    _i32(counts, "counts")
+    ref = k_io if k_io is not None else v_io
+    fref = k_fresh if k_fresh is not None else v_fresh
+    _check(lib.kvfix_repair_rows(_ptr(k_io), _ptr(v_io), plane_desc(ref), _ptr(k_fresh), _ptr(v_fresh),
+                                 plane_desc(fref), _ptr(idx), idx.shape[-1], _ptr(counts), _stream(ref)))

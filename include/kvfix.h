@@ -402,6 +402,50 @@ KVFIX_API kvfix_status kvfix_anchor_correct(
     const int32_t* delta, double rope_base, const int32_t* accept, float* w_k, float* w_v,
     kvfix_bf16* k_out, kvfix_bf16* v_out, kvfix_kv_desc out, void* stream);
 
+/*
+ * kvfix_repair_layout -- the rows a draft-scored repair recomputes, in one of the layouts
+ * of [BCR] section 3 "The layouts", App. A.2 ("The policy" step 2, Table 8) and App. B
+ * (Algorithm 1 lines 1-2, Algorithm 2 line 5).  For each unit u of scores [units][tokens]
+ * (e.g. kvfix_draft_rank's), with rho = budget_num / budget_den and rounding of halves
+ * to even:
+ *   KVFIX_LAYOUT_SINGLE: the round(rho n) rows with the largest scores;
+ *   KVFIX_LAYOUT_CHUNK : chunk_tokens-token chunks (the last may be short), each scored by
+ *                        the mean of its rows' scores (summed in index order, in double);
+ *                        the max(1, round(rho n / chunk_tokens)) best chunks, all their
+ *                        rows.  skip_rule != 0: no rows when n < 2 chunk_tokens or
+ *                        rho n < chunk_tokens (Algorithm 1 line 1);
+ *   KVFIX_LAYOUT_GROW  : round(rho n) rows: the best unselected row seeds a span, which
+ *                        takes the better of its two unselected neighbours (left on a tie)
+ *                        while that one scores at least tau times the seed, until neither
+ *                        does or the budget is spent; then the next seed.
+ * Ties go to the lower index.  Scores must be finite.
+ * idx      : device int32 [units][max_rows]: the rows, ascending, then -1.
+ * counts   : device int32 [units]: rows chosen (the same for every unit except when the
+ *            chunk layout's last, short chunk is chosen).
+ * max_rows : at least the layout's largest count (KVFIX_EINVAL otherwise): round(rho n)
+ *            for single and grow, (chunks chosen) * chunk_tokens (at most n) for chunk.
+ * tokens   : 1..16384.
+ */
+typedef enum { KVFIX_LAYOUT_SINGLE = 0, KVFIX_LAYOUT_CHUNK = 1, KVFIX_LAYOUT_GROW = 2 } kvfix_layout;
+KVFIX_API kvfix_status kvfix_repair_layout(const double* scores, int32_t units, int32_t tokens,
+                                           int32_t layout, int32_t chunk_tokens, int32_t budget_num,
+                                           int32_t budget_den, double tau, int32_t skip_rule,
+                                           int32_t* idx, int32_t max_rows, int32_t* counts,
+                                           void* stream);
+
+/*
+ * kvfix_repair_rows -- overwrite the chosen rows with exact ones ([BCR] App. B Algorithm 1
+ * line 6; [KVCMAS] Eq. 3): for every chunk c of `desc`, layer and KV head, rows
+ * idx[c][0 .. counts[c]) of k_io / v_io get the same rows of k_fresh / v_fresh
+ * (`fresh_desc`, the shape of desc).  idx holds max_rows entries per chunk; rows out of
+ * range are skipped and flagged (KVFIX_EDEVICE in kvfix_check_status).  Either plane may
+ * be skipped by passing NULL for both its pointers.
+ */
+KVFIX_API kvfix_status kvfix_repair_rows(kvfix_bf16* k_io, kvfix_bf16* v_io, kvfix_kv_desc desc,
+                                         const kvfix_bf16* k_fresh, const kvfix_bf16* v_fresh,
+                                         kvfix_kv_desc fresh_desc, const int32_t* idx,
+                                         int32_t max_rows, const int32_t* counts, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
