@@ -67,6 +67,9 @@ def _load():
             "oracle_diff_restore": (None, [P, P, P, P, P, I, I, I, I, I, I, P, D, P, I64, P, P]),
             "oracle_anchor_gate": (None, [P, P, P, I, I, I, I, I, I, I, D, D, P, P, P, P]),
             "oracle_repair_layout": (I, [P, I, I, I, I, I, I, D, I, P, I, P]),
+            "oracle_master_select": (I, [P, P, I, I, I, P]),
+            "oracle_diff_encode_split": (None, [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P]),
+            "oracle_diff_gather_split": (None, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P]),
             "oracle_anchor_weights": (None, [P, P, P, I, I, I, I, I, I, D, P]),
             "oracle_anchor_correct": (None, [P, P, P, P, I, I, I, I, I, I, I, P, D, I, P]),
         }
@@ -377,3 +380,52 @@ def repair_layout(scores, layout: int, chunk_tokens: int = 64, budget=(1, 5), ta
     _load().oracle_repair_layout(_p(sc), U, n, int(layout), int(chunk_tokens), int(budget[0]), int(budget[1]),
                                  float(tau), int(bool(skip)), _p(idx), max(max_rows, 1), _p(counts))
     return idx[:, :max_rows], counts
+
+
+# ------------------------------------------------------------ master selection, split diffs
+
+def master_select(d_k, d_v, agents: int):
+    """d_k, d_v [A*R][n] float32 (either may be None) -> (master, totals [A] float64)."""
+    ref = d_k if d_k is not None else d_v
+    ref = np.ascontiguousarray(ref, dtype=np.float32)
+    A = int(agents)
+    R = ref.shape[0] // A
+    n = ref.shape[-1]
+    dk = None if d_k is None else np.ascontiguousarray(d_k, dtype=np.float32)
+    dv = None if d_v is None else np.ascontiguousarray(d_v, dtype=np.float32)
+    tot = np.empty(A, np.float64)
+    m = _load().oracle_master_select(None if dk is None else _p(dk), None if dv is None else _p(dv), A, R, n,
+                                     _p(tot))
+    return int(m), tot
+
+
+def diff_encode_split(master_k, master_v, sib_k, sib_v, block_tokens: int):
+    """-> per plane (mask uint32, offsets int64 [E+1], payload [entries][bt][H][D]) for K and V."""
+    mk, mv, sk, sv = _u16(master_k), _u16(master_v), _u16(sib_k), _u16(sib_v)
+    S, L, n, H, D = sk.shape
+    bt = int(block_tokens)
+    E = S * L * (n // bt)
+    masks = [np.empty((E + 31) // 32, np.uint32) for _ in range(2)]
+    offs = [np.empty(E + 1, np.int64) for _ in range(2)]
+    pays = [np.empty((E, bt, H, D), np.uint16) for _ in range(2)]
+    cap = np.array([E, E], np.int64)
+    need = np.zeros(2, np.int64)
+    _load().oracle_diff_encode_split(_p(mk), _p(mv), _p(sk), _p(sv), S, L, n, H, D, bt, _p(masks[0]), _p(masks[1]),
+                                     _p(offs[0]), _p(offs[1]), _p(pays[0]), _p(pays[1]), _p(cap), _p(need))
+    return ((masks[0], offs[0], pays[0][:need[0]]), (masks[1], offs[1], pays[1][:need[1]]))
+
+
+def diff_gather_split(master_k, master_v, k_diff, v_diff, siblings: int, block_tokens: int):
+    mk, mv = _u16(master_k), _u16(master_v)
+    L, n, H, D = mk.shape
+    S = int(siblings)
+    parts = []
+    for mask, off, pay in (k_diff, v_diff):
+        pay = _u16(pay) if pay.size else np.zeros((1,), np.uint16)
+        parts.append((np.ascontiguousarray(mask, dtype=np.uint32), np.ascontiguousarray(off, dtype=np.int64), pay))
+    ok = np.empty((S, L, n, H, D), np.uint16)
+    ov = np.empty_like(ok)
+    (mk_, ok_, pk_), (mv_, ov_, pv_) = parts
+    _load().oracle_diff_gather_split(_p(mk), _p(mv), _p(mk_), _p(mv_), _p(ok_), _p(ov_), _p(pk_), _p(pv_), S, L, n,
+                                     H, D, int(block_tokens), _p(ok), _p(ov))
+    return ok, ov

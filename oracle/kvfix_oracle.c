@@ -809,3 +809,97 @@ EXPORT int oracle_repair_layout(const double* scores, int U, int n, int layout, 
     }
     return most;
 }
+
+/* ------------------------------------------------------------ master selection, split diffs */
+
+/*
+ * Master of a round's cache family (TokenDance, section 4.2 "reuse plan output": the reuse
+ * pass accumulates a deviation score per request, and the master is the request with the
+ * lowest total deviation from the shared blocks): for agent a,
+ *   total[a] = sum_{r < R} sum_{j < n} (d_k[a R + r][j] + d_v[a R + r][j]),
+ * summed in that order in double; master = the agent with the smallest total (ties to the
+ * lower index).  Either plane's scores may be NULL.
+ */
+EXPORT int oracle_master_select(const float* d_k, const float* d_v, int A, int R, int n, double* total)
+{
+    int best = 0;
+    for (int a = 0; a < A; ++a) {
+        double s = 0.0;
+        for (int64_t r = 0; r < R; ++r)
+            for (int64_t j = 0; j < n; ++j) {
+                int64_t o = ((int64_t)a * R + r) * n + j;
+                if (d_k) s += (double)d_k[o];
+                if (d_v) s += (double)d_v[o];
+            }
+        total[a] = s;
+        if (s < total[best]) best = a;
+    }
+    return best;
+}
+
+/*
+ * Block-sparse diff with one index list per plane (TokenDance, section 5: the K and V
+ * planes share one block list only when they touch the same blocks).  For plane P
+ * (K = 0, V = 1), entry i = (s L + l) nblk + blk is dirty iff some bf16 word of plane P in
+ * that block differs bitwise from the master's; offsets_P = exclusive counts (last =
+ * total); payload_P [entries_P][bt][H][D] holds the sibling's plane-P block.  Returns the
+ * totals in need[2]; payload entries beyond capacity[P] are not written.
+ */
+EXPORT void oracle_diff_encode_split(const uint16_t* mk, const uint16_t* mv, const uint16_t* sk,
+                                     const uint16_t* sv, int S, int L, int n, int H, int D, int bt,
+                                     uint32_t* mask_k, uint32_t* mask_v, int64_t* off_k,
+                                     int64_t* off_v, uint16_t* pay_k, uint16_t* pay_v,
+                                     const int64_t* capacity, int64_t* need)
+{
+    int nblk = n / bt;
+    int64_t E = (int64_t)S * L * nblk;
+    int64_t row = (int64_t)H * D, blk_elems = (int64_t)bt * row;
+    for (int p = 0; p < 2; ++p) {
+        const uint16_t* m = p ? mv : mk;
+        const uint16_t* sb = p ? sv : sk;
+        uint32_t* mask = p ? mask_v : mask_k;
+        int64_t* off = p ? off_v : off_k;
+        uint16_t* pay = p ? pay_v : pay_k;
+        memset(mask, 0, sizeof(uint32_t) * (size_t)((E + 31) / 32));
+        int64_t count = 0;
+        for (int64_t i = 0; i < E; ++i) {
+            int64_t s = i / ((int64_t)L * nblk), l = (i / nblk) % L, blk = i % nblk;
+            const uint16_t* a = m + (l * n + blk * bt) * row;
+            const uint16_t* b = sb + ((s * L + l) * n + blk * bt) * row;
+            off[i] = count;
+            if (memcmp(a, b, sizeof(uint16_t) * (size_t)blk_elems) != 0) {
+                mask[i >> 5] |= 1u << (i & 31);
+                if (count < capacity[p]) memcpy(pay + count * blk_elems, b, sizeof(uint16_t) * (size_t)blk_elems);
+                ++count;
+            }
+        }
+        off[E] = count;
+        need[p] = count;
+    }
+}
+
+/* Inverse of oracle_diff_encode_split: out_P[s] = the master's plane P, with each dirty
+ * block replaced from payload_P. */
+EXPORT void oracle_diff_gather_split(const uint16_t* mk, const uint16_t* mv, const uint32_t* mask_k,
+                                     const uint32_t* mask_v, const int64_t* off_k,
+                                     const int64_t* off_v, const uint16_t* pay_k,
+                                     const uint16_t* pay_v, int S, int L, int n, int H, int D,
+                                     int bt, uint16_t* ok, uint16_t* ov)
+{
+    int nblk = n / bt;
+    int64_t E = (int64_t)S * L * nblk;
+    int64_t row = (int64_t)H * D, blk_elems = (int64_t)bt * row;
+    for (int p = 0; p < 2; ++p) {
+        const uint16_t* m = p ? mv : mk;
+        const uint32_t* mask = p ? mask_v : mask_k;
+        const int64_t* off = p ? off_v : off_k;
+        const uint16_t* pay = p ? pay_v : pay_k;
+        uint16_t* out = p ? ov : ok;
+        for (int64_t i = 0; i < E; ++i) {
+            int64_t s = i / ((int64_t)L * nblk), l = (i / nblk) % L, blk = i % nblk;
+            const uint16_t* src = (mask[i >> 5] >> (i & 31) & 1u) ? pay + off[i] * blk_elems
+                                                                  : m + (l * n + blk * bt) * row;
+            memcpy(out + ((s * L + l) * n + blk * bt) * row, src, sizeof(uint16_t) * (size_t)blk_elems);
+        }
+    }
+}

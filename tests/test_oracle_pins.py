@@ -769,3 +769,98 @@ def test_grow_layout_small_case_by_hand():
     s = np.array([[1, 5, 4, 0.9, 0.1, 8, 7, 0.5]], dtype=np.float64)
     idx, cnt = oracle.repair_layout(s, oracle.LAYOUT_GROW, budget=(1, 2), tau=0.5)
     assert cnt[0] == 4 and list(idx[0, :4]) == [1, 2, 5, 6]
+
+
+# ------------------------------------------------------------ master selection, split diffs
+
+def test_master_select_matches_numpy():
+    rng = np.random.default_rng(61)
+    A, R, n = 5, 3, 70
+    dk = rng.random((A * R, n)).astype(np.float32)
+    dv = rng.random((A * R, n)).astype(np.float32)
+    m, tot = oracle.master_select(dk, dv, A)
+    ref = dk.astype(np.float64).reshape(A, -1).sum(1) + dv.astype(np.float64).reshape(A, -1).sum(1)
+    np.testing.assert_allclose(tot, ref, rtol=1e-12)
+    assert m == int(np.argmin(ref))
+    m1, tot1 = oracle.master_select(dk, None, A)
+    np.testing.assert_allclose(tot1, dk.astype(np.float64).reshape(A, -1).sum(1), rtol=1e-12)
+    same = np.tile(dk[:R], (A, 1))
+    assert oracle.master_select(same, same, A)[0] == 0          # ties to the lower index
+
+
+def test_master_by_deviation_minimises_diff_storage():
+    """Agents share content X and each changes a disjoint set of its blocks; the agent with
+    the smallest total deviation from X is the master whose diffs of the others take the
+    fewest payload entries (entries(m) = sum |M| + (S - 2) |M_m|)."""
+    rng = np.random.default_rng(62)
+    S, L, n, H, D, bt = 5, 2, 64, 2, 8, 8
+    X_k = _bf16_bits(rng.standard_normal((L, n, H, D)))
+    X_v = _bf16_bits(rng.standard_normal((L, n, H, D)))
+    nblk = n // bt
+    blocks = rng.permutation(L * nblk)
+    sizes = [3, 1, 4, 2, 5]
+    caches_k = np.repeat(X_k[None], S, 0)
+    caches_v = np.repeat(X_v[None], S, 0)
+    start = 0
+    for s in range(S):
+        for b in blocks[start:start + sizes[s]]:
+            l, blk = divmod(int(b), nblk)
+            noise = rng.standard_normal((bt, H, D))
+            caches_k[s, l, blk * bt:(blk + 1) * bt] = _bf16_bits(oracle.bf16_decode(X_k[l, blk * bt:(blk + 1) * bt]) + noise)
+        start += sizes[s]
+    dev = np.sqrt(((oracle.bf16_decode(caches_k) - oracle.bf16_decode(X_k)[None]) ** 2).sum(axis=(3, 4)))
+    d = dev.reshape(S * L, n).astype(np.float32)                     # [agent * layer][token]
+    m, _ = oracle.master_select(d, None, S)
+    entries = []
+    for cand in range(S):
+        _, _, _, total = oracle.diff_encode(caches_k[cand], caches_v[cand], caches_k, caches_v, bt)
+        entries.append(total)
+    assert m == int(np.argmin(entries)) == 1
+
+
+def _split_case(rng, S=3, L=2, n=48, H=2, D=8, bt=8):
+    mk = _bf16_bits(rng.standard_normal((L, n, H, D)))
+    mv = _bf16_bits(rng.standard_normal((L, n, H, D)))
+    sk = np.repeat(mk[None], S, 0)
+    sv = np.repeat(mv[None], S, 0)
+    return mk, mv, sk, sv, bt
+
+
+def test_split_diff_roundtrip_and_relation_to_joint():
+    rng = np.random.default_rng(63)
+    mk, mv, sk, sv, bt = _split_case(rng)
+    S, L, n = sk.shape[:3]
+    for s in range(S):
+        for l in range(L):
+            for blk in range(n // bt):
+                u = rng.random()
+                t = blk * bt + int(rng.integers(0, bt))
+                if u < 0.2:
+                    sk[s, l, t, 0, 0] ^= 1
+                elif u < 0.4:
+                    sv[s, l, t, 1, 3] ^= 1
+                elif u < 0.5:
+                    sk[s, l, t, 1, 1] ^= 1
+                    sv[s, l, t, 0, 2] ^= 1
+    kd, vd = oracle.diff_encode_split(mk, mv, sk, sv, bt)
+    ok, ov = oracle.diff_gather_split(mk, mv, kd, vd, S, bt)
+    assert np.array_equal(ok, sk) and np.array_equal(ov, sv)
+    jmask, joffs, jpay, jtotal = oracle.diff_encode(mk, mv, sk, sv, bt)
+    assert np.array_equal(kd[0] | vd[0], jmask)                     # joint dirty = K dirty or V dirty
+    nk, nv = int(kd[1][-1]), int(vd[1][-1])
+    assert max(nk, nv) <= jtotal <= nk + nv and nk + nv > jtotal    # some blocks touch one plane only
+
+
+def test_split_diff_equals_joint_when_planes_agree():
+    """When K and V touch the same blocks the two lists coincide with the joint one and the
+    split payloads are the joint payload's K and V halves."""
+    rng = np.random.default_rng(64)
+    mk, mv, sk, sv, bt = _split_case(rng)
+    for s, l, t in ((0, 0, 3), (1, 1, 40), (2, 0, 17), (2, 1, 9)):
+        sk[s, l, t, 0, 0] ^= 2
+        sv[s, l, t, 1, 1] ^= 2
+    kd, vd = oracle.diff_encode_split(mk, mv, sk, sv, bt)
+    jmask, joffs, jpay, jtotal = oracle.diff_encode(mk, mv, sk, sv, bt)
+    assert np.array_equal(kd[0], jmask) and np.array_equal(vd[0], jmask)
+    assert np.array_equal(kd[1], joffs) and np.array_equal(vd[1], joffs)
+    assert np.array_equal(kd[2], jpay[:, 0]) and np.array_equal(vd[2], jpay[:, 1])
