@@ -351,7 +351,24 @@ def stage_round(kvfix, peak, steps=5, warmup=2):
     ms = statistics.mean(step_ms)
     mc = statistics.mean(mc_ms)
     per_agent_extra = 2 * (cfg.agents - 1) * cfg.chunks * cfg.layers * cfg.tokens * cfg.kv_heads * cfg.head_dim * 2
+    # the round's master (lowest total deviation) from the same check-layer scores
+    cl = cfg.check_layer
+    sel = kvfix.score_topk(inp["k_reuse"][:, cl:cl + 1], inp["v_reuse"][:, cl:cl + 1], inp["k_fresh"][:, cl:cl + 1],
+                           inp["v_fresh"][:, cl:cl + 1], cfg.agents, inp["delta"], cfg.rope_base, cfg.b)
+    ms_ms = []
+    stream = torch.cuda.current_stream()
+    for s in range(warmup + steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        master, _ = kvfix.master_select(sel["d_k"], sel["d_v"], cfg.agents)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if s >= warmup:
+            ms_ms.append(e0.elapsed_time(e1))
+    res_master = {"ms": round(statistics.mean(ms_ms), 4), "master": int(master.item()),
+                  "score_bytes": 2 * sel["d_k"].numel() * 4}
     res = {"workload": "round_qwen14b: 8 agents x 8 shared 512-token blocks, 48 layers, 8x128 heads",
+           "master_select": res_master,
            "ms_per_step": round(ms, 4), "corrected_GBps": round(by["corrected"] / ms / 1e6, 1),
            "tokens_per_s": round(by["tokens"] / ms * 1e3, 1),
            "mean_correct": {"ms": round(mc, 4), "algorithmic_bytes": by["mean_correct"],
@@ -412,6 +429,32 @@ def stage_diff(kvfix, peak, steps=5, warmup=2):
     blk = 2 * cfg.block_tokens * cfg.kv_heads * cfg.head_dim * 2
     enc_bytes = 2 * plane + 2 * plane * cfg.siblings + entries * blk + E // 8 + 8 * (E + 1)
     gat_bytes = 2 * plane + entries * blk + 2 * plane * cfg.siblings + E // 8 + 8 * (E + 1)
+    # per-plane lists of the same siblings (the generator dirties K and V in the same
+    # blocks, so both lists equal the joint one): encode and gather
+    sp_enc, sp_gat = [], []
+    kl, vl, sent = kvfix.diff_encode_split(inp["master_k"], inp["master_v"], inp["sib_k"], inp["sib_v"],
+                                           cfg.block_tokens)
+    for s in range(warmup + steps):
+        flush.zero_()
+        host_lead()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        kl, vl, _ = kvfix.diff_encode_split(inp["master_k"], inp["master_v"], inp["sib_k"], inp["sib_v"],
+                                            cfg.block_tokens, capacity=sent, sync=False)
+        e1.record(stream)
+        flush.zero_()
+        host_lead()
+        e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2.record(stream)
+        kvfix.diff_gather_split(inp["master_k"], inp["master_v"], kl, vl, cfg.siblings, cfg.block_tokens, out_k,
+                                out_v, entries=sent)
+        e3.record(stream)
+        torch.cuda.synchronize()
+        if s >= warmup:
+            sp_enc.append(e0.elapsed_time(e1))
+            sp_gat.append(e2.elapsed_time(e3))
+    kvfix.check_status()
+    del kl, vl
     res_bytes = gat_bytes + cfg.siblings * (cfg.tokens + 1) * 4
     enc, gat, rst = statistics.mean(enc_ms), statistics.mean(gat_ms), statistics.mean(res_ms)
     full = 2 * plane * cfg.siblings
@@ -422,6 +465,10 @@ def stage_diff(kvfix, peak, steps=5, warmup=2):
                       "GBps": round(enc_bytes / enc / 1e6, 1), "frac": round(enc_bytes / enc / 1e6 / peak, 4)},
            "gather": {"ms": round(gat, 4), "algorithmic_bytes": gat_bytes,
                       "GBps": round(gat_bytes / gat / 1e6, 1), "frac": round(gat_bytes / gat / 1e6 / peak, 4)},
+           "split_lists": {"entries": list(sent), "encode_ms": round(statistics.mean(sp_enc), 4),
+                           "encode_frac": round((enc_bytes + 8 * (E + 1) + E // 8) / statistics.mean(sp_enc) / 1e6 / peak, 4),
+                           "gather_ms": round(statistics.mean(sp_gat), 4),
+                           "gather_frac": round((gat_bytes + 8 * (E + 1) + E // 8) / statistics.mean(sp_gat) / 1e6 / peak, 4)},
            "restore": {"ms": round(rst, 4), "algorithmic_bytes": res_bytes,
                        "GBps": round(res_bytes / rst / 1e6, 1), "frac": round(res_bytes / rst / 1e6 / peak, 4),
                        "pool": f"{tgt['slots']} slots of 16-token pages, keys re-aligned per sibling"}}

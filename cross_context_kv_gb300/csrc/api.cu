@@ -610,4 +610,103 @@ kvfix_status kvfix_repair_rows(kvfix_bf16* k_io, kvfix_bf16* v_io, kvfix_kv_desc
     return KVFIX_OK;
 }
 
+kvfix_status kvfix_master_select(const float* d_k, const float* d_v, int32_t agents, int32_t units_per_agent,
+                                 int32_t tokens, double* totals, int32_t* master, void* stream) {
+    const char* fn = "kvfix_master_select";
+    if (agents < 0 || agents > 65535 || units_per_agent < 1 || tokens < 1)
+        return fail(KVFIX_EINVAL, "%s: agents in [0, 65535], units_per_agent and tokens >= 1", fn);
+    if (agents > 0 && ((!d_k && !d_v) || !totals || !master))
+        return fail(KVFIX_EINVAL, "%s: a score plane, totals and master are required", fn);
+    return launched(launch_master_select(d_k, d_v, agents, units_per_agent, tokens, totals, master,
+                                         (cudaStream_t)stream),
+                    fn);
+}
+
+kvfix_status kvfix_diff_encode_split(const kvfix_bf16* master_k, const kvfix_bf16* master_v, kvfix_kv_desc master,
+                                     const kvfix_bf16* sib_k, const kvfix_bf16* sib_v, kvfix_kv_desc sib,
+                                     int32_t block_tokens, uint32_t* mask_k, uint32_t* mask_v, int64_t* offsets_k,
+                                     int64_t* offsets_v, kvfix_bf16* payload_k, kvfix_bf16* payload_v,
+                                     int64_t capacity_k, int64_t capacity_v, int64_t* h_entries, void* stream) {
+    const char* fn = "kvfix_diff_encode_split";
+    kvfix_status st;
+    if ((st = check_plane(master_k, master, "kvfix_diff_encode_split: master_k")) != KVFIX_OK) return st;
+    if ((st = check_plane(master_v, master, "kvfix_diff_encode_split: master_v")) != KVFIX_OK) return st;
+    if ((st = check_plane(sib_k, sib, "kvfix_diff_encode_split: sib_k")) != KVFIX_OK) return st;
+    if ((st = check_plane(sib_v, sib, "kvfix_diff_encode_split: sib_v")) != KVFIX_OK) return st;
+    if (master.chunks != 1) return fail(KVFIX_EINVAL, "%s: master.chunks must be 1", fn);
+    if (!same_shape(master, sib)) return fail(KVFIX_EINVAL, "%s: master and sibling shapes differ", fn);
+    if (block_tokens < 1 || master.tokens % block_tokens)
+        return fail(KVFIX_EINVAL, "%s: block_tokens must divide tokens", fn);
+    if (!mask_k || !mask_v || !offsets_k || !offsets_v)
+        return fail(KVFIX_EINVAL, "%s: both masks and both offset arrays are required", fn);
+    if (capacity_k < 0 || capacity_v < 0) return fail(KVFIX_EINVAL, "%s: negative capacity", fn);
+    if ((capacity_k > 0 && (!payload_k || !aligned16(payload_k))) || (capacity_v > 0 && (!payload_v || !aligned16(payload_v))))
+        return fail(KVFIX_EINVAL, "%s: payloads must be 16-byte aligned device pointers", fn);
+    const long long per_sibling = (long long)master.layers * (master.tokens / block_tokens);
+    const long long entries = per_sibling * sib.chunks;
+    if (entries >= (1ll << 31)) return fail(KVFIX_EINVAL, "%s: too many entries", fn);
+    if (sib.chunks > 65535 || master.layers > 65535) return fail(KVFIX_EINVAL, "%s: at most 65535 siblings and layers", fn);
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t mbytes = sizeof(uint32_t) * (size_t)((entries + 31) / 32);
+    cudaError_t e;
+    if ((e = cudaMemsetAsync(mask_k, 0, mbytes, s)) != cudaSuccess || (e = cudaMemsetAsync(mask_v, 0, mbytes, s)) != cudaSuccess)
+        return cuda_fail(e, fn);
+    if ((e = launch_diff_mask(master_k, master_v, master, sib_k, sib_v, sib, block_tokens, mask_k, s, mask_v)) != cudaSuccess)
+        return cuda_fail(e, fn);
+    if ((e = launch_diff_scan(mask_k, sib.chunks, per_sibling, offsets_k, s)) != cudaSuccess) return cuda_fail(e, fn);
+    if ((e = launch_diff_scan(mask_v, sib.chunks, per_sibling, offsets_v, s)) != cudaSuccess) return cuda_fail(e, fn);
+    if (h_entries) {
+        int64_t tot[2] = {0, 0};
+        if ((e = cudaMemcpyAsync(&tot[0], offsets_k + entries, sizeof(int64_t), cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(&tot[1], offsets_v + entries, sizeof(int64_t), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+            return cuda_fail(e, fn);
+        if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, fn);
+        h_entries[0] = tot[0];
+        h_entries[1] = tot[1];
+        if (tot[0] > capacity_k || tot[1] > capacity_v)
+            return fail(KVFIX_ENOSPACE, "%s: %lld + %lld entries needed, capacity %lld + %lld", fn, (long long)tot[0],
+                        (long long)tot[1], (long long)capacity_k, (long long)capacity_v);
+    }
+    if (capacity_k > 0 &&
+        (e = launch_diff_pack(sib_k, sib_v, sib, block_tokens, mask_k, offsets_k, payload_k, capacity_k, s, 1)) != cudaSuccess)
+        return cuda_fail(e, fn);
+    if (capacity_v > 0 &&
+        (e = launch_diff_pack(sib_k, sib_v, sib, block_tokens, mask_v, offsets_v, payload_v, capacity_v, s, 2)) != cudaSuccess)
+        return cuda_fail(e, fn);
+    return KVFIX_OK;
+}
+
+kvfix_status kvfix_diff_gather_split(const kvfix_bf16* master_k, const kvfix_bf16* master_v, kvfix_kv_desc master,
+                                     const uint32_t* mask_k, const uint32_t* mask_v, const int64_t* offsets_k,
+                                     const int64_t* offsets_v, const kvfix_bf16* payload_k,
+                                     const kvfix_bf16* payload_v, int64_t entries_k, int64_t entries_v,
+                                     int32_t siblings, int32_t block_tokens, kvfix_bf16* out_k, kvfix_bf16* out_v,
+                                     kvfix_kv_desc out, void* stream) {
+    const char* fn = "kvfix_diff_gather_split";
+    kvfix_status st;
+    if ((st = check_plane(master_k, master, "kvfix_diff_gather_split: master_k")) != KVFIX_OK) return st;
+    if ((st = check_plane(master_v, master, "kvfix_diff_gather_split: master_v")) != KVFIX_OK) return st;
+    if ((st = check_plane(out_k, out, "kvfix_diff_gather_split: out_k")) != KVFIX_OK) return st;
+    if ((st = check_plane(out_v, out, "kvfix_diff_gather_split: out_v")) != KVFIX_OK) return st;
+    if (master.chunks != 1) return fail(KVFIX_EINVAL, "%s: master.chunks must be 1", fn);
+    if (!same_shape(master, out) || out.chunks != siblings)
+        return fail(KVFIX_EINVAL, "%s: out must have `siblings` chunks of the master's shape", fn);
+    if (block_tokens < 1 || master.tokens % block_tokens)
+        return fail(KVFIX_EINVAL, "%s: block_tokens must divide tokens", fn);
+    if (siblings < 0 || siblings > 65535 || master.layers > 65535)
+        return fail(KVFIX_EINVAL, "%s: siblings and layers must be <= 65535", fn);
+    if (!mask_k || !mask_v || !offsets_k || !offsets_v)
+        return fail(KVFIX_EINVAL, "%s: both masks and both offset arrays are required", fn);
+    if (entries_k < 0 || entries_v < 0) return fail(KVFIX_EINVAL, "%s: negative payload entries", fn);
+    if ((entries_k > 0 && (!payload_k || !aligned16(payload_k))) || (entries_v > 0 && (!payload_v || !aligned16(payload_v))))
+        return fail(KVFIX_EINVAL, "%s: payloads must be 16-byte aligned device pointers", fn);
+    if (overlaps(out_k, out, master_k, master) || overlaps(out_v, out, master_v, master) ||
+        overlaps(out_k, out, out_v, out))
+        return fail(KVFIX_EINVAL, "%s: outputs overlap the master or each other", fn);
+    return launched(launch_diff_gather(master_k, master_v, master, mask_k, offsets_k, payload_k, entries_k, siblings,
+                                       block_tokens, out_k, out_v, out, (cudaStream_t)stream, mask_v, offsets_v,
+                                       payload_v, entries_v),
+                    fn);
+}
+
 }  // extern "C"

@@ -72,7 +72,8 @@ struct DmArgs {
     const uint16_t* sv;
     Plane mp, sp;
     int bt, piece_rows, pieces_per_plane;
-    uint32_t* mask;
+    uint32_t* mask;    // K and V together, or K alone when mask_v is set
+    uint32_t* mask_v;  // V alone (per-plane lists), or null
 };
 
 __global__ void __launch_bounds__(kDmThreads, 1) diff_mask_kernel(DmArgs a) {
@@ -87,7 +88,9 @@ __global__ void __launch_bounds__(kDmThreads, 1) diff_mask_kernel(DmArgs a) {
     const int units = P * S;               // (piece, sibling) pairs, piece-major
     unsigned char* mbuf = dsm;                                 // [2][kDmPieceBytes]
     unsigned char* ring = dsm + 2 * kDmPieceBytes;             // [kDmStages][kDmPieceBytes]
-    uint32_t* flags = reinterpret_cast<uint32_t*>(ring + kDmStages * kDmPieceBytes);  // [ceil(S/32)]
+    uint32_t* flags = reinterpret_cast<uint32_t*>(ring + kDmStages * kDmPieceBytes);  // [planes][ceil(S/32)]
+    const int fwords = (S + 31) / 32;
+    const bool split = a.mask_v != nullptr;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool contig_m = a.mp.st == HD, contig_s = a.sp.st == HD;
 
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(kDmThreads, 1) diff_mask_kernel(DmArgs a) {
         }
     };
 
-    for (int i = tid; i < (S + 31) / 32; i += kDmThreads) flags[i] = 0u;
+    for (int i = tid; i < (split ? 2 : 1) * fwords; i += kDmThreads) flags[i] = 0u;
     if (tid == 0) {
         for (int q = 0; q < 2; ++q) {
             mbar_init(&mfull[q], 1);
@@ -167,7 +170,8 @@ __global__ void __launch_bounds__(kDmThreads, 1) diff_mask_kernel(DmArgs a) {
             const int vecs = rows * (int)(row_bytes / 16);
             bool ne = false;
             for (int v = ct; v < vecs; v += 32 * kDmCmpWarps) ne |= vec_ne(m4[v], s4[v]);
-            if (__any_sync(0xffffffffu, ne) && lane == 0) atomicOr(&flags[s >> 5], 1u << (s & 31));
+            const int fp = split && p >= a.pieces_per_plane ? fwords : 0;  // the V plane's flags
+            if (__any_sync(0xffffffffu, ne) && lane == 0) atomicOr(&flags[fp + (s >> 5)], 1u << (s & 31));
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&empty[g % kDmStages]);
@@ -186,17 +190,18 @@ __global__ void __launch_bounds__(kDmThreads, 1) diff_mask_kernel(DmArgs a) {
         __syncthreads();
         return;
     }
-    for (int q = tid; q < S; q += kDmThreads) {
-        if (flags[q >> 5] >> (q & 31) & 1u) {
-            const long long i = ((long long)q * L + l) * nblk + blk;
-            atomicOr(&a.mask[i >> 5], 1u << (i & 31));
+    for (int q = tid; q < (split ? 2 : 1) * S; q += kDmThreads) {
+        const int pl = q / S, sq = q % S;
+        if (flags[pl * fwords + (sq >> 5)] >> (sq & 31) & 1u) {
+            const long long i = ((long long)sq * L + l) * nblk + blk;
+            atomicOr(&(pl ? a.mask_v : a.mask)[i >> 5], 1u << (i & 31));
         }
     }
 }
 
 cudaError_t launch_diff_mask(const uint16_t* mk, const uint16_t* mv, const kvfix_kv_desc& md,
                              const uint16_t* sk, const uint16_t* sv, const kvfix_kv_desc& sd,
-                             int bt, uint32_t* mask, cudaStream_t s) {
+                             int bt, uint32_t* mask, cudaStream_t s, uint32_t* mask_v) {
     DmArgs a;
     a.mk = mk;
     a.mv = mv;
@@ -206,12 +211,13 @@ cudaError_t launch_diff_mask(const uint16_t* mk, const uint16_t* mv, const kvfix
     a.sp = plane_of(sd);
     a.bt = bt;
     a.mask = mask;
+    a.mask_v = mask_v;
     if (a.mp.layers == 0 || a.mp.tokens == 0 || a.sp.chunks == 0) return cudaSuccess;
     const int row_bytes = 2 * a.mp.heads * a.mp.dim;
     a.piece_rows = kDmPieceBytes / row_bytes < bt ? kDmPieceBytes / row_bytes : bt;
     if (a.piece_rows < 1) return cudaErrorInvalidValue;  // a token row above 32 KB
     a.pieces_per_plane = (bt + a.piece_rows - 1) / a.piece_rows;
-    const size_t smem = (size_t)(2 + kDmStages) * kDmPieceBytes + 4 * (size_t)((a.sp.chunks + 31) / 32);
+    const size_t smem = (size_t)(2 + kDmStages) * kDmPieceBytes + 8 * (size_t)((a.sp.chunks + 31) / 32);
     cudaError_t e = cudaFuncSetAttribute(diff_mask_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.mp.tokens / bt, a.mp.layers);
@@ -295,12 +301,14 @@ constexpr int kPackThreads = 256;
 __global__ void __launch_bounds__(kPackThreads)
 diff_pack_kernel(const uint16_t* __restrict__ sk, const uint16_t* __restrict__ sv, Plane sp, int bt,
                  const uint32_t* __restrict__ mask, const int64_t* __restrict__ offsets,
-                 long long E, uint16_t* payload, long long capacity) {
+                 long long E, uint16_t* payload, long long capacity, int planes) {
     const long long wi = blockIdx.x;
     uint32_t word = mask[wi];
     const int L = sp.layers, nblk = sp.tokens / bt;
     BlockMap bm{bt, sp.heads * sp.dim / 8, (long long)bt * (sp.heads * sp.dim / 8)};
-    const long long total = 2 * bm.vecs_per_plane;
+    // planes: 0 = the block's K rows then its V rows, 1 = K rows only, 2 = V rows only
+    const long long total = (planes == 0 ? 2 : 1) * bm.vecs_per_plane;
+    const long long vbase = planes == 2 ? bm.vecs_per_plane : 0;
     while (word) {
         const int bit = __ffs(word) - 1;
         word &= word - 1;
@@ -315,7 +323,8 @@ diff_pack_kernel(const uint16_t* __restrict__ sk, const uint16_t* __restrict__ s
         const int l = (int)((i / nblk) % L);
         const int blk = (int)(i % nblk);
         uint4* dst = reinterpret_cast<uint4*>(payload + e * total * 8);
-        const int row8 = bm.row8, rows_all = 2 * bt;  // the block's K rows, then its V rows
+        const int row8 = bm.row8, rows_all = (planes == 0 ? 2 : 1) * bt;
+        const int rshift = planes == 2 ? bt : 0;  // first source row, counted over K then V
         if (kPackThreads % row8 == 0) {
             // a thread keeps one 16-byte column and walks rows; eight loads in flight
             const int rpp = kPackThreads / row8, c8 = threadIdx.x % row8, r0 = threadIdx.x / row8;
@@ -324,10 +333,10 @@ diff_pack_kernel(const uint16_t* __restrict__ sk, const uint16_t* __restrict__ s
                 uint4 v[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const int r = rb + r0 + j * rpp;
+                    const int r = rb + r0 + j * rpp, rr = r + rshift;
                     if (r < rows_all)
                         v[j] = ld_stream(reinterpret_cast<const uint4*>(
-                            (r < bt ? sk + boff + (long long)r * sp.st : sv + boff + (long long)(r - bt) * sp.st)));
+                            (rr < bt ? sk + boff + (long long)rr * sp.st : sv + boff + (long long)(rr - bt) * sp.st)));
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -339,7 +348,7 @@ diff_pack_kernel(const uint16_t* __restrict__ sk, const uint16_t* __restrict__ s
             for (long long q = threadIdx.x; q < total; q += kPackThreads) {
                 int pl;
                 long long off;
-                bm.locate(q, sp, s, l, blk * bt, &pl, &off);
+                bm.locate(q + vbase, sp, s, l, blk * bt, &pl, &off);
                 uint4 v = ld_stream(reinterpret_cast<const uint4*>((pl ? sv : sk) + off));
                 st_stream(dst + q, v);
             }
@@ -349,25 +358,46 @@ diff_pack_kernel(const uint16_t* __restrict__ sk, const uint16_t* __restrict__ s
 
 cudaError_t launch_diff_pack(const uint16_t* sk, const uint16_t* sv, const kvfix_kv_desc& sd,
                              int bt, const uint32_t* mask, const int64_t* offsets,
-                             uint16_t* payload, long long capacity, cudaStream_t s) {
+                             uint16_t* payload, long long capacity, cudaStream_t s, int planes) {
     Plane sp = plane_of(sd);
     const long long E = (long long)sp.chunks * sp.layers * (sp.tokens / bt);
     if (E == 0) return cudaSuccess;
     const long long words = (E + 31) / 32;
     diff_pack_kernel<<<(unsigned)words, kPackThreads, 0, s>>>(sk, sv, sp, bt, mask, offsets, E,
-                                                              payload, capacity);
+                                                              payload, capacity, planes);
     return cudaGetLastError();
 }
 
 // ----------------------------------------------------------------------- gather
 
+// The V plane's list when K and V keep separate ones (null mask: one list for both).
+struct SplitList {
+    const uint32_t* mask;
+    const int64_t* offsets;
+    const uint16_t* payload;
+    long long entries;
+};
+
+// Payload entry of sibling entry i in a list, or -1 (clean, or beyond the payload: flagged).
+__device__ __forceinline__ long long diff_entry(const uint32_t* mask, const int64_t* offsets, long long entries,
+                                               long long i) {
+    long long e = mask_bit(mask, i) ? offsets[i] : -1;
+    if (e >= entries) {
+        if (threadIdx.x == 0) atomicOr(&g_status_diff, FLAG_NOSPACE);
+        e = -1;
+    }
+    return e;
+}
+
 // grid = (nblk, L).  Master block in registers, written to every sibling unless the
-// sibling's entry is dirty, in which case the payload block is copied instead.
+// sibling's entry is dirty, in which case the payload block is copied instead.  With a
+// split list, K blocks come from (mask, offsets, payload) and V blocks from vl, each
+// payload entry holding one plane.
 __global__ void __launch_bounds__(kDiffThreads)
 diff_gather_kernel(const uint16_t* __restrict__ mk, const uint16_t* __restrict__ mv, Plane mp,
                    const uint32_t* __restrict__ mask, const int64_t* __restrict__ offsets,
                    const uint16_t* __restrict__ payload, long long payload_entries, int S, int bt,
-                   uint16_t* ok, uint16_t* ov, Plane op) {
+                   uint16_t* ok, uint16_t* ov, Plane op, SplitList vl) {
     const int blk = blockIdx.x, l = blockIdx.y;
     const int nblk = mp.tokens / bt, L = mp.layers;
     BlockMap bm{bt, mp.heads * mp.dim / 8, (long long)bt * (mp.heads * mp.dim / 8)};
@@ -387,20 +417,23 @@ diff_gather_kernel(const uint16_t* __restrict__ mk, const uint16_t* __restrict__
                 bm.locate(q, op, 0, l, blk * bt, &pl[k], &off[k]);
             }
         }
+        const bool split = vl.mask != nullptr;
+        const long long vpp = bm.vecs_per_plane, estride = split ? vpp : total;
         for (int s = 0; s < S; ++s) {
             const long long i = ((long long)s * L + l) * nblk + blk;
-            const bool dirty = mask_bit(mask, i);
-            long long e = dirty ? offsets[i] : -1;
-            if (dirty && e >= payload_entries) {
-                if (threadIdx.x == 0) atomicOr(&g_status_diff, FLAG_NOSPACE);
-                e = -1;
+            const long long e = diff_entry(mask, offsets, payload_entries, i);
+            const uint4* src = e >= 0 ? reinterpret_cast<const uint4*>(payload + e * estride * 8) : nullptr;
+            const uint4* srcv = src;  // joint entry: V vectors follow its K vectors
+            if (split) {
+                const long long ev = diff_entry(vl.mask, vl.offsets, vl.entries, i);
+                srcv = ev >= 0 ? reinterpret_cast<const uint4*>(vl.payload + ev * vpp * 8) : nullptr;
             }
-            const uint4* src = e >= 0 ? reinterpret_cast<const uint4*>(payload + e * total * 8) : nullptr;
 #pragma unroll
             for (int k = 0; k < kDiffVec; ++k) {
                 if (pl[k] < 0) continue;
                 const long long q = q0 + (long long)k * kDiffThreads + threadIdx.x;
-                uint4 v = src ? ld_stream(src + q) : m[k];
+                const uint4* sp = pl[k] ? srcv : src;
+                uint4 v = sp ? ld_stream(sp + (split && pl[k] ? q - vpp : q)) : m[k];
                 uint16_t* base = (pl[k] ? ov : ok) + (long long)s * op.sc;
                 st_stream(reinterpret_cast<uint4*>(base + off[k]), v);
             }
@@ -412,12 +445,67 @@ cudaError_t launch_diff_gather(const uint16_t* mk, const uint16_t* mv, const kvf
                                const uint32_t* mask, const int64_t* offsets,
                                const uint16_t* payload, long long payload_entries, int siblings,
                                int bt, uint16_t* ok, uint16_t* ov, const kvfix_kv_desc& od,
-                               cudaStream_t s) {
+                               cudaStream_t s, const uint32_t* mask_v, const int64_t* offsets_v,
+                               const uint16_t* payload_v, long long entries_v) {
     Plane mp = plane_of(md), op = plane_of(od);
     if (mp.layers == 0 || mp.tokens == 0 || siblings == 0) return cudaSuccess;
     dim3 grid(mp.tokens / bt, mp.layers);
+    SplitList vl{mask_v, offsets_v, payload_v, entries_v};
     diff_gather_kernel<<<grid, kDiffThreads, 0, s>>>(mk, mv, mp, mask, offsets, payload,
-                                                     payload_entries, siblings, bt, ok, ov, op);
+                                                     payload_entries, siblings, bt, ok, ov, op, vl);
+    return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- master selection
+
+constexpr int kMsThreads = 256;
+
+// grid = agents.  total[a] = sum over the agent's units and tokens of d_k + d_v, in double:
+// thread t takes every 256th value of the agent's range, then a fixed tree over threads.
+__global__ void __launch_bounds__(kMsThreads)
+master_total_kernel(const float* __restrict__ d_k, const float* __restrict__ d_v, long long per_agent,
+                    double* totals) {
+    __shared__ double part[kMsThreads];
+    const long long base = (long long)blockIdx.x * per_agent;
+    double s = 0.0;
+    for (long long i = threadIdx.x; i < per_agent; i += kMsThreads) {
+        if (d_k) s += (double)d_k[base + i];
+        if (d_v) s += (double)d_v[base + i];
+    }
+    part[threadIdx.x] = s;
+    __syncthreads();
+    for (int h = kMsThreads / 2; h > 0; h >>= 1) {
+        if (threadIdx.x < h) part[threadIdx.x] += part[threadIdx.x + h];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) totals[blockIdx.x] = part[0];
+}
+
+// One warp: the smallest total, ties to the lower agent.
+__global__ void master_argmin_kernel(const double* __restrict__ totals, int A, int32_t* master) {
+    double best = 0.0;
+    int bi = -1;
+    for (int a = threadIdx.x; a < A; a += 32)
+        if (bi < 0 || totals[a] < best) {
+            best = totals[a];
+            bi = a;
+        }
+    for (int o = 16; o > 0; o >>= 1) {
+        const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (oi >= 0 && (bi < 0 || ob < best || (ob == best && oi < bi))) {
+            best = ob;
+            bi = oi;
+        }
+    }
+    if (threadIdx.x == 0) *master = bi;
+}
+
+cudaError_t launch_master_select(const float* d_k, const float* d_v, int agents, int units_per_agent,
+                                 int tokens, double* totals, int32_t* master, cudaStream_t s) {
+    if (agents == 0) return cudaSuccess;
+    master_total_kernel<<<agents, kMsThreads, 0, s>>>(d_k, d_v, (long long)units_per_agent * tokens, totals);
+    master_argmin_kernel<<<1, 32, 0, s>>>(totals, agents, master);
     return cudaGetLastError();
 }
 

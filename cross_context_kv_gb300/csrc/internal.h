@@ -81,19 +81,26 @@ cudaError_t launch_repair_layout(const double* scores, int units, int n, int lay
                                  int skipped, double tau, int32_t* idx, int max_rows, int32_t* counts,
                                  cudaStream_t s);
 
+// mask_v non-null: K blocks are marked in mask and V blocks in mask_v (per-plane lists).
 cudaError_t launch_diff_mask(const uint16_t* mk, const uint16_t* mv, const kvfix_kv_desc& md,
                              const uint16_t* sk, const uint16_t* sv, const kvfix_kv_desc& sd,
-                             int bt, uint32_t* mask, cudaStream_t s);
+                             int bt, uint32_t* mask, cudaStream_t s, uint32_t* mask_v = nullptr);
 cudaError_t launch_diff_scan(const uint32_t* mask, int siblings, long long per_sibling,
                              int64_t* offsets, cudaStream_t s);
+// planes: 0 = entries hold the K block then the V block; 1 = K only; 2 = V only.
 cudaError_t launch_diff_pack(const uint16_t* sk, const uint16_t* sv, const kvfix_kv_desc& sd,
                              int bt, const uint32_t* mask, const int64_t* offsets,
-                             uint16_t* payload, long long capacity, cudaStream_t s);
+                             uint16_t* payload, long long capacity, cudaStream_t s, int planes = 0);
 cudaError_t launch_diff_gather(const uint16_t* mk, const uint16_t* mv, const kvfix_kv_desc& md,
                                const uint32_t* mask, const int64_t* offsets,
                                const uint16_t* payload, long long payload_entries, int siblings,
                                int bt, uint16_t* ok, uint16_t* ov, const kvfix_kv_desc& od,
-                               cudaStream_t s);
+                               cudaStream_t s, const uint32_t* mask_v = nullptr,
+                               const int64_t* offsets_v = nullptr, const uint16_t* payload_v = nullptr,
+                               long long entries_v = 0);
+// Per-agent total deviation (double) and the agent with the smallest one.
+cudaError_t launch_master_select(const float* d_k, const float* d_v, int agents, int units_per_agent,
+                                 int tokens, double* totals, int32_t* master, cudaStream_t s);
 
 cudaError_t launch_diff_restore(const uint16_t* mk, const uint16_t* mv, const kvfix_kv_desc& md,
                                 const uint32_t* mask, const int64_t* offsets,

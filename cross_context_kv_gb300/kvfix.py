@@ -52,6 +52,9 @@ SIGNATURES = {
     "kvfix_diff_gather": (ctypes.c_int, [P, P, D, P, P, P, I64, I32, I32, P, P, D, P]),
     "kvfix_diff_restore": (ctypes.c_int, [P, P, D, P, P, P, I64, I32, I32, P, F64, P, P, P, D, P]),
     "kvfix_repair_layout": (ctypes.c_int, [P, I32, I32, I32, I32, I32, I32, F64, I32, P, I32, P, P]),
+    "kvfix_master_select": (ctypes.c_int, [P, P, I32, I32, I32, P, P, P]),
+    "kvfix_diff_encode_split": (ctypes.c_int, [P, P, D, P, P, D, I32, P, P, P, P, P, P, I64, I64, P, P]),
+    "kvfix_diff_gather_split": (ctypes.c_int, [P, P, D, P, P, P, P, P, P, I64, I64, I32, I32, P, P, D, P]),
     "kvfix_repair_rows": (ctypes.c_int, [P, P, D, P, P, D, P, I32, P, P]),
     "kvfix_anchor_gate_workspace_bytes": (SZ, [D, I32, I32]),
     "kvfix_anchor_gate": (ctypes.c_int, [P, D, P, P, I32, I32, I32, F64, F64, P, P, P, P, P, SZ, P]),
@@ -407,3 +410,62 @@ def repair_rows(k_io, v_io, k_fresh, v_fresh, idx, counts):
     fref = k_fresh if k_fresh is not None else v_fresh
     _check(lib.kvfix_repair_rows(_ptr(k_io), _ptr(v_io), plane_desc(ref), _ptr(k_fresh), _ptr(v_fresh),
                                  plane_desc(fref), _ptr(idx), idx.shape[-1], _ptr(counts), _stream(ref)))
+
+
+def master_select(d_k, d_v, agents: int):
+    """d_k, d_v [agents*R][n] float32 (CUDA; either may be None) -> (master int32 [1], totals [agents] f64)."""
+    ref = d_k if d_k is not None else d_v
+    for t, nm in ((d_k, "d_k"), (d_v, "d_v")):
+        if t is not None:
+            _f32(t, nm)
+    A = int(agents)
+    R = ref.shape[0] // A
+    totals = torch.empty(A, dtype=torch.float64, device=ref.device)
+    master = torch.empty(1, dtype=torch.int32, device=ref.device)
+    _check(lib.kvfix_master_select(_ptr(d_k), _ptr(d_v), A, R, ref.shape[-1], _ptr(totals), _ptr(master),
+                                   _stream(ref)))
+    return master, totals
+
+
+def diff_encode_split(master_k, master_v, sib_k, sib_v, block_tokens: int, capacity=None, sync: bool = True):
+    """Per-plane block lists.  Returns ((mask_k, offsets_k, payload_k), (mask_v, offsets_v, payload_v),
+    (entries_k, entries_v) or None); payload_P [cap][bt][H][D]."""
+    for t, nm in ((master_k, "master_k"), (master_v, "master_v"), (sib_k, "sib_k"), (sib_v, "sib_v")):
+        _bf16(t, nm)
+    mk = master_k.unsqueeze(0) if master_k.dim() == 4 else master_k
+    mv = master_v.unsqueeze(0) if master_v.dim() == 4 else master_v
+    md, sd = plane_desc(mk), plane_desc(sib_k)
+    S, L, n, H, Dh = sd.chunks, sd.layers, sd.tokens, sd.kv_heads, sd.head_dim
+    bt = int(block_tokens)
+    E = S * L * (n // bt)
+    dev = sib_k.device
+    caps = (E, E) if capacity is None else tuple(int(c) for c in capacity)
+    lists = []
+    for cap in caps:
+        lists.append((torch.empty((E + 31) // 32, dtype=torch.int32, device=dev),
+                      torch.empty(E + 1, dtype=torch.int64, device=dev),
+                      torch.empty(max(cap, 1), bt, H, Dh, dtype=torch.bfloat16, device=dev)))
+    entries = (ctypes.c_int64 * 2)(-1, -1)
+    (mk_, ok_, pk_), (mv_, ov_, pv_) = lists
+    _check(lib.kvfix_diff_encode_split(_ptr(mk), _ptr(mv), md, _ptr(sib_k), _ptr(sib_v), sd, bt, _ptr(mk_), _ptr(mv_),
+                                       _ptr(ok_), _ptr(ov_), _ptr(pk_), _ptr(pv_), caps[0], caps[1],
+                                       entries if sync else None, _stream(sib_k)))
+    return lists[0], lists[1], ((entries[0], entries[1]) if sync else None)
+
+
+def diff_gather_split(master_k, master_v, k_list, v_list, siblings: int, block_tokens: int, out_k=None,
+                      out_v=None, entries=None):
+    _bf16(master_k, "master_k")
+    _bf16(master_v, "master_v")
+    mk = master_k.unsqueeze(0) if master_k.dim() == 4 else master_k
+    mv = master_v.unsqueeze(0) if master_v.dim() == 4 else master_v
+    md = plane_desc(mk)
+    shape = (int(siblings),) + tuple(mk.shape[1:])
+    out_k = torch.empty(shape, dtype=torch.bfloat16, device=mk.device) if out_k is None else out_k
+    out_v = torch.empty(shape, dtype=torch.bfloat16, device=mk.device) if out_v is None else out_v
+    ek, ev = (k_list[2].shape[0], v_list[2].shape[0]) if entries is None else entries
+    _check(lib.kvfix_diff_gather_split(_ptr(mk), _ptr(mv), md, _ptr(k_list[0]), _ptr(v_list[0]), _ptr(k_list[1]),
+                                       _ptr(v_list[1]), _ptr(k_list[2]), _ptr(v_list[2]), int(ek), int(ev),
+                                       int(siblings), int(block_tokens), _ptr(out_k), _ptr(out_v), plane_desc(out_k),
+                                       _stream(mk)))
+    return out_k, out_v

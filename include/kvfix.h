@@ -446,6 +446,56 @@ KVFIX_API kvfix_status kvfix_repair_rows(kvfix_bf16* k_io, kvfix_bf16* v_io, kvf
                                          kvfix_kv_desc fresh_desc, const int32_t* idx,
                                          int32_t max_rows, const int32_t* counts, void* stream);
 
+/*
+ * kvfix_master_select -- the master of a round's cache family.  [TD] section 4.2 ("reuse
+ * plan output": the reuse pass accumulates a deviation score per request; the master is
+ * the request with the lowest total deviation from the shared blocks, which keeps the
+ * mirrors' diffs small) and section 4.3 (master-mirror layout).
+ *     totals[a] = sum_{r < R} sum_{j < tokens} (d_k[a R + r][j] + d_v[a R + r][j])
+ *     *master   = the agent with the smallest total (ties to the lower index)
+ * d_k, d_v : device float [agents * R][tokens] as kvfix_score_topk writes them for a
+ *            collective round (unit a R + r); either may be NULL.
+ * totals   : device double [agents], summed in double in a fixed order (per agent: thread
+ *            t of 256 takes every 256th value, then a tree over threads).
+ * master   : device int32 [1].
+ */
+KVFIX_API kvfix_status kvfix_master_select(const float* d_k, const float* d_v, int32_t agents,
+                                           int32_t units_per_agent, int32_t tokens, double* totals,
+                                           int32_t* master, void* stream);
+
+/*
+ * kvfix_diff_encode_split -- block-sparse diffs with one block list per plane.  [TD]
+ * section 5 (the K and V planes share one block index list only when they touch the same
+ * blocks).  As kvfix_diff_encode, except that entry i is dirty in plane P iff some bf16
+ * word of plane P in it differs from the master's, and each plane has its own list:
+ *     mask_k / mask_v       : device uint32[ceil(S*L*nblk/32)]
+ *     offsets_k / offsets_v : device int64[S*L*nblk + 1]
+ *     payload_k / payload_v : device bf16[capacity_P][bt][kv_heads][head_dim] (one plane)
+ * h_entries: optional HOST int64[2] (K, V); if given, the call synchronises and returns
+ * KVFIX_ENOSPACE, writing no payload, when a plane's total exceeds its capacity.  If NULL,
+ * entries beyond a capacity are skipped and flagged.
+ */
+KVFIX_API kvfix_status kvfix_diff_encode_split(
+    const kvfix_bf16* master_k, const kvfix_bf16* master_v, kvfix_kv_desc master,
+    const kvfix_bf16* sib_k, const kvfix_bf16* sib_v, kvfix_kv_desc sib, int32_t block_tokens,
+    uint32_t* mask_k, uint32_t* mask_v, int64_t* offsets_k, int64_t* offsets_v,
+    kvfix_bf16* payload_k, kvfix_bf16* payload_v, int64_t capacity_k, int64_t capacity_v,
+    int64_t* h_entries, void* stream);
+
+/*
+ * kvfix_diff_gather_split -- restore every sibling from the master and its per-plane
+ * diffs (the lists kvfix_diff_encode_split writes): K blocks from (mask_k, offsets_k,
+ * payload_k), V blocks from (mask_v, offsets_v, payload_v); entries_* are the payloads'
+ * sizes (an offset beyond them is not read and is flagged).  Otherwise as
+ * kvfix_diff_gather.
+ */
+KVFIX_API kvfix_status kvfix_diff_gather_split(
+    const kvfix_bf16* master_k, const kvfix_bf16* master_v, kvfix_kv_desc master,
+    const uint32_t* mask_k, const uint32_t* mask_v, const int64_t* offsets_k,
+    const int64_t* offsets_v, const kvfix_bf16* payload_k, const kvfix_bf16* payload_v,
+    int64_t entries_k, int64_t entries_v, int32_t siblings, int32_t block_tokens,
+    kvfix_bf16* out_k, kvfix_bf16* out_v, kvfix_kv_desc out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -226,3 +226,89 @@ def test_full_size_diff_restore():
             assert np.array_equal(got, sib)
         else:
             _assert_k_rotation_close(got, ref, sib, delta_h[s], cfg.rope_base, f"sibling {s}")
+
+
+# ------------------------------------------------------------ per-plane lists, master
+
+def _planes_differ(inp, cfg, seed):
+    """Make the K and V planes touch different blocks: flip V words in extra blocks and
+    restore K in some of the dirty ones."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    S, L, n = cfg.siblings, cfg.layers, cfg.tokens
+    bt = cfg.block_tokens
+    sk, sv = inp["sib_k"], inp["sib_v"]
+    for s in range(S):
+        for _ in range(3):
+            l = int(torch.randint(L, (1,), generator=g))
+            t = int(torch.randint(n, (1,), generator=g))
+            sv[s, l, t, 0, 0] = -sv[s, l, t, 0, 0] + 1.0
+        blocks = inp["dirty_blocks"][s]
+        if len(blocks):
+            b = int(blocks[0])
+            sk[s, :, b * bt:(b + 1) * bt] = inp["master_k"][:, b * bt:(b + 1) * bt]
+
+
+def _split_check(cfg, inp):
+    kl, vl, ent = kvfix().diff_encode_split(inp["master_k"], inp["master_v"], inp["sib_k"], inp["sib_v"],
+                                            cfg.block_tokens)
+    kvfix().check_status()
+    okd, ovd = oracle.diff_encode_split(synth.bits(inp["master_k"]), synth.bits(inp["master_v"]),
+                                        synth.bits(inp["sib_k"]), synth.bits(inp["sib_v"]), cfg.block_tokens)
+    for got, ref, e in ((kl, okd, ent[0]), (vl, ovd, ent[1])):
+        assert e == ref[1][-1]
+        assert np.array_equal(got[0].cpu().numpy().view(np.uint32), ref[0])
+        assert np.array_equal(got[1].cpu().numpy(), ref[1])
+        assert np.array_equal(synth.bits(got[2][:e]), ref[2])
+    ok, ov = kvfix().diff_gather_split(inp["master_k"], inp["master_v"], kl, vl, cfg.siblings, cfg.block_tokens,
+                                       entries=ent)
+    kvfix().check_status()
+    assert torch.equal(ok.view(torch.int16), inp["sib_k"].view(torch.int16))
+    assert torch.equal(ov.view(torch.int16), inp["sib_v"].view(torch.int16))
+    return kl, vl, ent
+
+
+@pytest.mark.parametrize("cfg", SMALL_DIFF, ids=lambda c: c.name)
+def test_split_diff_bit_exact(cfg):
+    inp = synth.diff_inputs(cfg, DEV)
+    kl, vl, _ = _split_check(cfg, inp)
+    # the generator dirties K and V in the same blocks: the two lists coincide
+    assert torch.equal(kl[0], vl[0]) and torch.equal(kl[1], vl[1])
+    _planes_differ(inp, cfg, 5)
+    kl, vl, ent = _split_check(cfg, inp)
+    assert not torch.equal(kl[0], vl[0])
+
+
+@pytest.mark.slow
+def test_full_size_split_diff():
+    cfg = synth.SIBLINGS_8B
+    inp = synth.diff_inputs(cfg, DEV)
+    _planes_differ(inp, cfg, 6)
+    kl, vl, ent = kvfix().diff_encode_split(inp["master_k"], inp["master_v"], inp["sib_k"], inp["sib_v"],
+                                            cfg.block_tokens)
+    mask, offsets, payload, entries = kvfix().diff_encode(inp["master_k"], inp["master_v"], inp["sib_k"],
+                                                          inp["sib_v"], cfg.block_tokens)
+    kvfix().check_status()
+    assert torch.equal(kl[0] | vl[0], mask)
+    assert max(ent) <= entries <= ent[0] + ent[1]
+    ok, ov = kvfix().diff_gather_split(inp["master_k"], inp["master_v"], kl, vl, cfg.siblings, cfg.block_tokens,
+                                       entries=ent)
+    kvfix().check_status()
+    assert torch.equal(ok.view(torch.int16), inp["sib_k"].view(torch.int16))
+    assert torch.equal(ov.view(torch.int16), inp["sib_v"].view(torch.int16))
+
+
+def test_master_select_matches_oracle():
+    rng = np.random.default_rng(80)
+    for A, R, n in ((8, 8, 512), (3, 1, 4096), (16, 2, 1000)):
+        dk = rng.random((A * R, n)).astype(np.float32)
+        dv = rng.random((A * R, n)).astype(np.float32)
+        m, tot = kvfix().master_select(torch.as_tensor(dk, device=DEV), torch.as_tensor(dv, device=DEV), A)
+        rm, rtot = oracle.master_select(dk, dv, A)
+        np.testing.assert_allclose(tot.cpu().numpy(), rtot, rtol=1e-12)
+        srt = np.sort(rtot)
+        if (srt[1] - srt[0]) / srt[1] > 1e-12:
+            assert int(m.item()) == rm
+        mk, _ = kvfix().master_select(torch.as_tensor(dk, device=DEV), None, A)
+        assert int(mk.item()) == oracle.master_select(dk, None, A)[0]
+    same = torch.as_tensor(np.tile(dk[:2], (16, 1)), device=DEV)
+    assert int(kvfix().master_select(same, same, 16)[0].item()) == 0
