@@ -763,6 +763,9 @@ PROFILE_CASES = {
     "diff": lambda: synth.SIBLINGS_8B.with_(layers=4),
     "lowrank": lambda: synth.LOWRANK_70B.with_(chunks=1, layers=8),
     "anchor": lambda: synth.ANCHOR_8B.with_(layers=8),
+    "diff_split": lambda: synth.SIBLINGS_8B.with_(layers=4),
+    "layout": lambda: synth.LOWRANK_70B.with_(layers=8),
+    "master": lambda: synth.ROUND_QWEN14B.with_(layers=8),
 }
 
 
@@ -796,6 +799,37 @@ def run_profile_case(name: str, iters: int = 3):
             kvfix.diff_restore(inp["master_k"], inp["master_v"], m, o, pl, cfg.siblings, cfg.block_tokens,
                                tgt["delta"], cfg.rope_base, tgt["slot_mapping"], pk, pv,
                                payload_entries=entries)
+    elif name == "diff_split":
+        inp = synth.diff_inputs(cfg, "cuda")
+        _, _, ent = kvfix.diff_encode_split(inp["master_k"], inp["master_v"], inp["sib_k"], inp["sib_v"],
+                                            cfg.block_tokens)
+        def step():
+            kl, vl, _ = kvfix.diff_encode_split(inp["master_k"], inp["master_v"], inp["sib_k"], inp["sib_v"],
+                                                cfg.block_tokens, capacity=ent, sync=False)
+            kvfix.diff_gather_split(inp["master_k"], inp["master_v"], kl, vl, cfg.siblings, cfg.block_tokens,
+                                    entries=ent)
+    elif name == "layout":
+        # heavy-tailed row scores like the draft's (seeded), then both layouts and their repair
+        g = torch.Generator(device="cuda").manual_seed(cfg.seed)
+        scores = torch.exp(2.0 * torch.randn((cfg.chunks, cfg.tokens), generator=g, device="cuda",
+                                             dtype=torch.float64))
+        shape = (cfg.chunks, cfg.layers, cfg.tokens, cfg.kv_heads, cfg.head_dim)
+        kio = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+        vio = torch.zeros_like(kio)
+        kf = torch.ones_like(kio)
+        vf = torch.ones_like(kio)
+        def step():
+            for lay in (kvfix.LAYOUT_CHUNK, kvfix.LAYOUT_GROW):
+                idx, cnt = kvfix.repair_layout(scores, lay, 64, (cfg.budget_num, cfg.budget_den), 0.25, True)
+                kvfix.repair_rows(kio, vio, kf, vf, idx, cnt)
+    elif name == "master":
+        reuse = synth.repair_reuse(cfg, "cuda")
+        fk, fv = compose_fresh_gpu(kvfix, cfg, reuse, range(cfg.units))
+        cl = cfg.check_layer
+        def step():
+            sel = kvfix.score_topk(reuse["k_reuse"][:, cl:cl + 1], reuse["v_reuse"][:, cl:cl + 1], fk[:, cl:cl + 1],
+                                   fv[:, cl:cl + 1], cfg.agents, reuse["delta"], cfg.rope_base, cfg.b)
+            kvfix.master_select(sel["d_k"], sel["d_v"], cfg.agents)
     elif name == "anchor":
         inp = synth.anchor_inputs(cfg, "cuda")
         src = compose_anchor_sources(cfg, inp)
