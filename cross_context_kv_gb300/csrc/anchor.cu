@@ -68,6 +68,7 @@ constexpr int kAdThreads = 320;       // warp 0 TMA, warp 1 MMA, warps 2..9 epil
 constexpr int kAdCols = 128;          // features per chunk (MMA N)
 constexpr int kAdSlots = 4;           // tensor-memory accumulators of 128 columns
 constexpr int kAdMaxB = 16;           // Bt ring entries (one anchor's chunk each)
+constexpr int kAdMaxX = 4;            // x chunk buffers
 constexpr int kAdXBytes = kAnRows * kAdCols * 2;  // x chunk: two 64-feature boxes, 128-byte swizzle
 
 enum { kAdWeights = 0, kAdGate = 1 };
@@ -76,7 +77,7 @@ struct AdArgs {
     int V, L, n, F, C;
     int rows;            // rows of the tile range: n (weights) or the gate prefix k
     int tiles;           // ceil(rows / 128)
-    int nb;              // Bt ring entries
+    int nb, nx;          // Bt ring entries, x chunk buffers
     float inv_T;
     float* w[2];         // weights mode: [C][L][n][V] per plane
     float* partial;      // gate mode: [C][L][tiles][V]
@@ -106,7 +107,7 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
                    AdArgs args) {
     using K = AdCfg<R>;
     extern __shared__ unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t xfull[2], xempty[2], bfull[kAdMaxB], bempty[kAdMaxB], tfull[kAdSlots],
+    __shared__ __align__(8) uint64_t xfull[kAdMaxX], xempty[kAdMaxX], bfull[kAdMaxB], bempty[kAdMaxB], tfull[kAdSlots],
         tempty[kAdSlots], afull;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
@@ -117,10 +118,10 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
     const int c = (int)blockIdx.z % args.C;
     if (MODE == kAdWeights && args.accept && args.accept[c] == 0) return;
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int V = args.V, NB = args.nb;
+    const int V = args.V, NB = args.nb, NX = args.nx;
     unsigned char* asm_ = smem;                             // V A tiles
-    unsigned char* xs = smem + V * K::kABytes;              // two x chunks
-    unsigned char* bs = xs + 2 * kAdXBytes;                 // Bt ring
+    unsigned char* xs = smem + V * K::kABytes;              // NX x chunks
+    unsigned char* bs = xs + NX * kAdXBytes;                // Bt ring
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const CUtensorMap* mx = plane ? &tm_x1 : &tm_x0;
     const CUtensorMap* ma = plane ? &tm_a1 : &tm_a0;
@@ -130,7 +131,7 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
     const int total = chunks * V;                           // (chunk, anchor) steps
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NX; ++i) {
             mbar_init(&xfull[i], 1);
             mbar_init(&xempty[i], 8);   // the eight epilogue warps
         }
@@ -166,8 +167,8 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
             for (int v = 0; v < V; ++v)
                 tma_load_2d(asm_ + v * K::kABytes, ma, 0, ((c * V + v) * args.L + l) * args.n + t0, &afull);
             for (int j = 0; j < chunks && !anchor_vload(&abort_flag); ++j) {
-                const int xi = j & 1;
-                if (j >= 2 && !mbar_wait(&xempty[xi], (unsigned)(j / 2 - 1) & 1u)) {
+                const int xi = j % NX;
+                if (j >= NX && !mbar_wait(&xempty[xi], (unsigned)(j / NX - 1) & 1u)) {
                     atomicOr(&abort_flag, 1);
                     break;
                 }
@@ -224,8 +225,8 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
         for (int v = 0; v < kAnMaxAnchors; ++v) acc[v] = 0.f;
         bool ok = true;
         for (int j = 0; ok && j < chunks; ++j) {
-            const int xi = j & 1;
-            if (anchor_vload(&abort_flag) || !mbar_wait(&xfull[xi], (unsigned)(j / 2) & 1u)) {
+            const int xi = j % NX;
+            if (anchor_vload(&abort_flag) || !mbar_wait(&xfull[xi], (unsigned)(j / NX) & 1u)) {
                 ok = false;
                 break;
             }
@@ -686,16 +687,20 @@ constexpr int kAdStaticBytes = 10 * 1024;
 constexpr int kApStaticBytes = 2 * 1024;
 
 struct AdShape {
-    int nb, smem;
+    int nb, nx, smem;
 };
 
+// As many x buffers (up to 4) as leave room for at least 4 Bt entries (or 2, with 2 x
+// buffers), then the Bt ring takes the rest (up to 16 entries).
 static bool ad_shape(int V, int r, AdShape* s) {
     const int row = 2 * r;
     const int abytes = kAnRows * row, bbytes = kAdCols * row;
-    const int budget = kAnSmemLimit - kAdStaticBytes - 1024 - V * abytes - 2 * kAdXBytes;
-    s->nb = budget / bbytes;
+    const int room = kAnSmemLimit - kAdStaticBytes - 1024 - V * abytes;
+    for (s->nx = kAdMaxX; s->nx > 2 && room - s->nx * kAdXBytes < 4 * bbytes; --s->nx) {
+    }
+    s->nb = (room - s->nx * kAdXBytes) / bbytes;
     if (s->nb > kAdMaxB) s->nb = kAdMaxB;
-    s->smem = 1024 + V * abytes + 2 * kAdXBytes + s->nb * bbytes;
+    s->smem = 1024 + V * abytes + s->nx * kAdXBytes + s->nb * bbytes;
     return V >= 1 && V <= kAnMaxAnchors && s->nb >= 2;
 }
 
@@ -734,6 +739,7 @@ static cudaError_t launch_dist(const CUtensorMap* mx, const CUtensorMap* ma, con
     AdShape sh;
     if (!ad_shape(args.V, R, &sh)) return cudaErrorInvalidValue;
     args.nb = sh.nb;
+    args.nx = sh.nx;
     cudaError_t e = cudaFuncSetAttribute(anchor_dist_kernel<R, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, sh.smem);
     if (e != cudaSuccess) return e;
     dim3 grid(args.tiles, args.L, planes * args.C);
