@@ -370,6 +370,8 @@ cudaError_t launch_diff_pack(const uint16_t* sk, const uint16_t* sv, const kvfix
 
 // ----------------------------------------------------------------------- gather
 
+constexpr int kGatherSibChunk = 64;  // siblings whose payload entries a CTA stages at once
+
 // The V plane's list when K and V keep separate ones (null mask: one list for both).
 struct SplitList {
     const uint32_t* mask;
@@ -383,7 +385,7 @@ __device__ __forceinline__ long long diff_entry(const uint32_t* mask, const int6
                                                long long i) {
     long long e = mask_bit(mask, i) ? offsets[i] : -1;
     if (e >= entries) {
-        if (threadIdx.x == 0) atomicOr(&g_status_diff, FLAG_NOSPACE);
+        atomicOr(&g_status_diff, FLAG_NOSPACE);
         e = -1;
     }
     return e;
@@ -398,6 +400,7 @@ diff_gather_kernel(const uint16_t* __restrict__ mk, const uint16_t* __restrict__
                    const uint32_t* __restrict__ mask, const int64_t* __restrict__ offsets,
                    const uint16_t* __restrict__ payload, long long payload_entries, int S, int bt,
                    uint16_t* ok, uint16_t* ov, Plane op, SplitList vl) {
+    __shared__ long long ent_k[kGatherSibChunk], ent_v[kGatherSibChunk];
     const int blk = blockIdx.x, l = blockIdx.y;
     const int nblk = mp.tokens / bt, L = mp.layers;
     BlockMap bm{bt, mp.heads * mp.dim / 8, (long long)bt * (mp.heads * mp.dim / 8)};
@@ -419,23 +422,34 @@ diff_gather_kernel(const uint16_t* __restrict__ mk, const uint16_t* __restrict__
         }
         const bool split = vl.mask != nullptr;
         const long long vpp = bm.vecs_per_plane, estride = split ? vpp : total;
-        for (int s = 0; s < S; ++s) {
-            const long long i = ((long long)s * L + l) * nblk + blk;
-            const long long e = diff_entry(mask, offsets, payload_entries, i);
-            const uint4* src = e >= 0 ? reinterpret_cast<const uint4*>(payload + e * estride * 8) : nullptr;
-            const uint4* srcv = src;  // joint entry: V vectors follow its K vectors
-            if (split) {
-                const long long ev = diff_entry(vl.mask, vl.offsets, vl.entries, i);
-                srcv = ev >= 0 ? reinterpret_cast<const uint4*>(vl.payload + ev * vpp * 8) : nullptr;
+        // the payload entries of a chunk of siblings, looked up once per CTA
+        for (int s0 = 0; s0 < S; s0 += kGatherSibChunk) {
+            const int sc = min(kGatherSibChunk, S - s0);
+            __syncthreads();  // the previous chunk's entries are no longer read
+            if (threadIdx.x < sc) {
+                const long long i = ((long long)(s0 + threadIdx.x) * L + l) * nblk + blk;
+                ent_k[threadIdx.x] = diff_entry(mask, offsets, payload_entries, i);
+                ent_v[threadIdx.x] = split ? diff_entry(vl.mask, vl.offsets, vl.entries, i) : -1;
             }
+            __syncthreads();
+            for (int ss = 0; ss < sc; ++ss) {
+                const int s = s0 + ss;
+                const long long e = ent_k[ss];
+                const uint4* src = e >= 0 ? reinterpret_cast<const uint4*>(payload + e * estride * 8) : nullptr;
+                const uint4* srcv = src;  // joint entry: V vectors follow its K vectors
+                if (split) {
+                    const long long ev = ent_v[ss];
+                    srcv = ev >= 0 ? reinterpret_cast<const uint4*>(vl.payload + ev * vpp * 8) : nullptr;
+                }
 #pragma unroll
-            for (int k = 0; k < kDiffVec; ++k) {
-                if (pl[k] < 0) continue;
-                const long long q = q0 + (long long)k * kDiffThreads + threadIdx.x;
-                const uint4* sp = pl[k] ? srcv : src;
-                uint4 v = sp ? ld_stream(sp + (split && pl[k] ? q - vpp : q)) : m[k];
-                uint16_t* base = (pl[k] ? ov : ok) + (long long)s * op.sc;
-                st_stream(reinterpret_cast<uint4*>(base + off[k]), v);
+                for (int k = 0; k < kDiffVec; ++k) {
+                    if (pl[k] < 0) continue;
+                    const long long q = q0 + (long long)k * kDiffThreads + threadIdx.x;
+                    const uint4* sp = pl[k] ? srcv : src;
+                    uint4 v = sp ? ld_stream(sp + (split && pl[k] ? q - vpp : q)) : m[k];
+                    uint16_t* base = (pl[k] ? ov : ok) + (long long)s * op.sc;
+                    st_stream(reinterpret_cast<uint4*>(base + off[k]), v);
+                }
             }
         }
     }
