@@ -33,7 +33,6 @@ unsigned read_status_layout(cudaStream_t stream) {
 }
 
 constexpr int kLayThreads = 1024;
-constexpr int kLayMaxTokens = 16384;
 
 struct LayoutArgs {
     int n, layout, B;
