@@ -98,6 +98,22 @@ def test_host_validation_rejects_bad_arguments(lib):
                                 pool, None) == lib.EINVAL
     assert L.kvfix_diff_restore(fake, fake, dm, fake, fake, None, 0, 2, 16, fake, 1.0, fake, far, far_v,
                                 pool, None) == lib.EINVAL
+    # repair layouts: tokens beyond 16384, an unknown layout, a budget above 1, max_rows too small
+    assert L.kvfix_repair_layout(fake, 1, 16385, 0, 64, 1, 5, 0.25, 1, fake, 4000, fake, None) == lib.EINVAL
+    assert L.kvfix_repair_layout(fake, 1, 1000, 3, 64, 1, 5, 0.25, 1, fake, 1000, fake, None) == lib.EINVAL
+    assert L.kvfix_repair_layout(fake, 1, 1000, 2, 64, 6, 5, 0.25, 1, fake, 1000, fake, None) == lib.EINVAL
+    assert L.kvfix_repair_layout(fake, 1, 1000, 2, 64, 1, 5, 0.25, 1, fake, 199, fake, None) == lib.EINVAL
+    assert b"max_rows" in L.kvfix_last_error()
+    assert L.kvfix_repair_layout(fake, 1, 1000, 1, 64, 1, 5, 0.25, 1, fake, 191, fake, None) == lib.EINVAL
+    # row repair: a plane with io but no fresh pointer
+    assert L.kvfix_repair_rows(fake, None, d, None, None, d, fake, 4, fake, None) == lib.EINVAL
+    # master selection: no score plane
+    assert L.kvfix_master_select(None, None, 4, 2, 16, fake, fake, None) == lib.EINVAL
+    # per-plane diffs: a missing V mask
+    assert L.kvfix_diff_encode_split(fake, fake, dm, fake, fake, dm, 16, fake, None, fake, fake, None, None, 0, 0,
+                                     None, None) == lib.EINVAL
+    assert L.kvfix_diff_gather_split(fake, fake, dm, fake, None, fake, fake, None, None, 0, 0, 1, 16, far, far_v,
+                                     dm, None) == lib.EINVAL
 
 
 def test_version(lib):
