@@ -6,8 +6,8 @@
  * calls it, and it shares no source with the CUDA library.
  *
  * Every function is the plain definition written out: loops over the tensors in
- * index order, all arithmetic in double, library routines (pow, cos, sin, exp,
- * sqrt, qsort) as single steps.  bf16 inputs are decoded exactly; bf16 outputs are
+ * index order, all arithmetic in double, library routines (pow, cos, sin, exp, log2,
+ * fabs, sqrt, qsort, memcmp) as single steps.  bf16 inputs are decoded exactly; bf16 outputs are
  * rounded double -> float (round to nearest even, the C conversion) -> bf16 (round
  * to nearest even on the float bit pattern, from the IEEE-754 definition).
  *
@@ -16,11 +16,14 @@
  *   low-rank A       [chunk][layer][head][token][rank]
  *   low-rank B       [chunk][layer][head][rank][dim]
  *   draft queries    [chunk][layer][step][q_head][dim]
+ *   anchor factors   A [segment][anchor][layer][token][r], Bt [segment][anchor][layer][feature][r]
+ *   paged pool       [layer][slot][head][dim]
  *
  * Parity status per function (what pins it, other than itself, is listed in the
  * test files):
  *   bf16 rounding, rerope, scores, top-b, mean correction, low-rank apply, draft
- *   scores, top-k, diff encode/gather: pinned.
+ *   scores, top-k, diff encode/gather, diff restore, anchor gate / weights /
+ *   correction, repair layouts, master selection, per-plane diffs: pinned.
  *   mean correction at the synthetic configs beyond the pinned invariants: the pages
  *   print no worked tensor, so those outputs rest on the definition alone.
  */
