@@ -158,3 +158,19 @@ def test_full_size_anchor_sampled():
         ro = oracle.anchor_correct(x, synth.bits(inp[f"a_d_{p}"][:, :, :, ts]), synth.bits(inp[f"b_dt_{p}"]), rw,
                                    cfg.kv_heads, inp["delta"].cpu().numpy(), cfg.rope_base, rot)
         assert_close_kv(flat(got_o[:, :, ts]), ro, f"sampled out_{p}")
+
+
+def test_single_anchor_gate_rejects_and_weights_are_one():
+    cfg = SMALL[0].with_(anchors=1, seed=63)
+    inp = synth.anchor_inputs(cfg, DEV)
+    src = compose(cfg, inp)
+    d, g, hbar, acc = kvfix().anchor_gate(src["v"], inp["a_c_v"], inp["b_ct_v"], cfg.tokens, tau=1.0)
+    kvfix().check_status()
+    assert not acc.any() and torch.isnan(hbar).all() and (g == 1.0).all()
+    ok, ov, wk, wv = kvfix().anchor_correct(src["k"], src["v"], factors(inp), inp["delta"], cfg.rope_base)
+    kvfix().check_status()
+    assert (wk == 1.0).all() and (wv == 1.0).all()
+    ro = oracle.anchor_correct(flat(src["v"]), synth.bits(inp["a_d_v"]), synth.bits(inp["b_dt_v"]),
+                               np.ones((cfg.segments, cfg.layers, cfg.tokens, 1)), cfg.kv_heads,
+                               inp["delta"].cpu().numpy(), cfg.rope_base, False)
+    assert_close_kv(flat(ov), ro, "single anchor out_v")

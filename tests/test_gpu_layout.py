@@ -101,3 +101,14 @@ def test_full_size_layouts():
     s = draft_like(rng, 4, 16384)
     for case in CASES + [(1, 64, (1, 20), 0.25, True), (2, 1, (1, 20), 0.25, True)]:
         check(s, *case)
+
+
+def test_layout_edges():
+    rng = np.random.default_rng(74)
+    one = draft_like(rng, 2, 1)
+    for case in ((0, 1, (1, 1), 0.25, True), (2, 1, (1, 1), 0.25, True), (1, 64, (1, 1), 0.25, False)):
+        check(one, *case)
+    s = draft_like(rng, 3, 700)
+    for case in ((0, 1, (0, 1), 0.25, True), (2, 1, (0, 1), 0.25, True), (1, 1024, (1, 5), 0.25, False),
+                 (1, 1024, (1, 5), 0.25, True), (2, 1, (1, 1), 0.5, True), (1, 1, (1, 1), 0.25, True)):
+        check(s, *case)
