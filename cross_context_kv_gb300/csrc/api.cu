@@ -105,7 +105,7 @@ kvfix_status kvfix_check_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "kvfix_check_status: stream synchronize");
     unsigned bits = read_status_repair(s) | read_status_diff(s) | read_status_draft(s) | read_status_lowrank(s) |
-                    read_status_anchor(s) | read_status_layout(s);
+                    read_status_anchor(s) | read_status_layout(s) | read_status_selftest(s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kvfix_check_status: status read");
     if (bits & 4u) return fail(KVFIX_ETIMEOUT, "a bounded device wait gave up");
@@ -707,6 +707,12 @@ kvfix_status kvfix_diff_gather_split(const kvfix_bf16* master_k, const kvfix_bf1
                                        block_tokens, out_k, out_v, out, (cudaStream_t)stream, mask_v, offsets_v,
                                        payload_v, entries_v),
                     fn);
+}
+
+kvfix_status kvfix_selftest_wait(int64_t limit_cycles, const int32_t* flag, void* stream) {
+    if (limit_cycles < 1 || limit_cycles > 4000000000ll)
+        return fail(KVFIX_EINVAL, "kvfix_selftest_wait: limit_cycles must be in [1, 4e9]");
+    return launched(launch_selftest_wait(limit_cycles, flag, (cudaStream_t)stream), "kvfix_selftest_wait");
 }
 
 }  // extern "C"

@@ -131,4 +131,8 @@ cudaError_t launch_anchor_correct(const AnchorPlanes& pl, const kvfix_kv_desc& d
                                   const int32_t* delta, const RopeTheta& th, const int32_t* accept,
                                   cudaStream_t s);
 
+// Bounded-wait self test.
+unsigned read_status_selftest(cudaStream_t stream);
+cudaError_t launch_selftest_wait(long long limit_cycles, const int* flag, cudaStream_t s);
+
 }  // namespace kvfix

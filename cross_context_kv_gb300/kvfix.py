@@ -53,6 +53,7 @@ SIGNATURES = {
     "kvfix_diff_restore": (ctypes.c_int, [P, P, D, P, P, P, I64, I32, I32, P, F64, P, P, P, D, P]),
     "kvfix_repair_layout": (ctypes.c_int, [P, I32, I32, I32, I32, I32, I32, F64, I32, P, I32, P, P]),
     "kvfix_master_select": (ctypes.c_int, [P, P, I32, I32, I32, P, P, P]),
+    "kvfix_selftest_wait": (ctypes.c_int, [I64, P, P]),
     "kvfix_diff_encode_split": (ctypes.c_int, [P, P, D, P, P, D, I32, P, P, P, P, P, P, I64, I64, P, P]),
     "kvfix_diff_gather_split": (ctypes.c_int, [P, P, D, P, P, P, P, P, P, I64, I64, I32, I32, P, P, D, P]),
     "kvfix_repair_rows": (ctypes.c_int, [P, P, D, P, P, D, P, I32, P, P]),
@@ -469,3 +470,11 @@ def diff_gather_split(master_k, master_v, k_list, v_list, siblings: int, block_t
                                        int(siblings), int(block_tokens), _ptr(out_k), _ptr(out_v), plane_desc(out_k),
                                        _stream(mk)))
     return out_k, out_v
+
+
+def selftest_wait(limit_cycles: int, flag=None):
+    """Launch the bounded-wait self test on the current stream (see kvfix_selftest_wait)."""
+    if flag is not None:
+        _i32(flag, "flag")
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    _check(lib.kvfix_selftest_wait(int(limit_cycles), _ptr(flag), s))

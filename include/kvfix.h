@@ -496,6 +496,16 @@ KVFIX_API kvfix_status kvfix_diff_gather_split(
     int64_t entries_k, int64_t entries_v, int32_t siblings, int32_t block_tokens,
     kvfix_bf16* out_k, kvfix_bf16* out_v, kvfix_kv_desc out, void* stream);
 
+/*
+ * kvfix_selftest_wait -- exercise the bounded wait that every pipelined kernel uses, with
+ * no hang: one warp waits on a barrier phase that never completes and then on the device
+ * int32 *flag (optional; 0 = not set), each for at most limit_cycles SM clocks, and records
+ * a timeout in the device status word, which kvfix_check_status reports as KVFIX_ETIMEOUT
+ * (and clears).  The kernel returns in about 2 * limit_cycles clocks; the context stays
+ * usable.  limit_cycles in [1, 4e9].
+ */
+KVFIX_API kvfix_status kvfix_selftest_wait(int64_t limit_cycles, const int32_t* flag, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -312,3 +312,20 @@ def test_master_select_matches_oracle():
         assert int(mk.item()) == oracle.master_select(dk, None, A)[0]
     same = torch.as_tensor(np.tile(dk[:2], (16, 1)), device=DEV)
     assert int(kvfix().master_select(same, same, 16)[0].item()) == 0
+
+
+def test_bounded_wait_times_out_and_the_context_survives():
+    """The pipelines' bounded wait, run out on purpose (a barrier phase nothing completes,
+    a flag nothing sets): the status word reports a timeout, reading it clears it, and
+    the next calls run normally."""
+    kvfix().check_status()
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kvfix().selftest_wait(2_000_000, flag)
+    with pytest.raises(kvfix().KvfixError) as e:
+        kvfix().check_status()
+    assert e.value.status == kvfix().ETIMEOUT
+    kvfix().check_status()                       # cleared
+    k = torch.randn((1, 2, 64, 2, 64), device=DEV).to(torch.bfloat16)
+    out = kvfix().rerope(k, torch.zeros(1, dtype=torch.int32, device=DEV), 1e4)
+    kvfix().check_status()
+    assert torch.equal(out.view(torch.int16), k.view(torch.int16))
