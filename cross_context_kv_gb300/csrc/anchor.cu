@@ -71,7 +71,7 @@ constexpr int kAdMaxB = 16;           // Bt ring entries (one anchor's chunk eac
 constexpr int kAdMaxX = 4;            // x chunk buffers
 constexpr int kAdXBytes = kAnRows * kAdCols * 2;  // x chunk: two 64-feature boxes, 128-byte swizzle
 
-enum { kAdWeights = 0, kAdGate = 1 };
+enum { kAdWeights = 0, kAdGate = 1, kAdBoth = 2 };
 
 struct AdArgs {
     int V, L, n, F, C;
@@ -80,7 +80,8 @@ struct AdArgs {
     int nb, nx;          // Bt ring entries, x chunk buffers
     float inv_T;
     float* w[2];         // weights mode: [C][L][n][V] per plane
-    float* partial;      // gate mode: [C][L][tiles][V]
+    float* partial;      // gate mode, and both mode's value plane: [C][L][tiles][V]
+    int gate_rows;       // both mode: the gate's prefix k
     const int32_t* accept;  // weights mode: [C] or null; rejected segments are skipped
 };
 
@@ -98,7 +99,9 @@ struct AdCfg {
 // thread holds in registers (its row, 64 of the chunk's features) for all anchors.
 // MODE kAdWeights: both planes (z = plane * C + c), every row; writes the softmax of
 // -mean|x - rec_v| / T per row.  MODE kAdGate: the value plane, rows < k; writes per-tile
-// sums of (x - rec_v)^2.
+// sums of (x - rec_v)^2.  MODE kAdBoth: the weights of both planes and, on the value
+// plane, the gate's per-tile sums from the same reconstructions (warp partials folded in
+// a fixed order).
 template <int R, int MODE>
 __global__ void __launch_bounds__(kAdThreads, 1)
 anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CUtensorMap tm_x1,
@@ -113,10 +116,11 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
     __shared__ int abort_flag;
     __shared__ float red[kAnRows][kAnMaxAnchors + 1];
     __shared__ float gsum[4][kAnMaxAnchors];
+    __shared__ float gsq[8][kAnMaxAnchors];  // both mode: per epilogue warp, per anchor
     const int tile = blockIdx.x, l = blockIdx.y;
     const int plane = MODE == kAdGate ? 0 : (int)blockIdx.z / args.C;
     const int c = (int)blockIdx.z % args.C;
-    if (MODE == kAdWeights && args.accept && args.accept[c] == 0) return;
+    if (MODE != kAdGate && args.accept && args.accept[c] == 0) return;
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int V = args.V, NB = args.nb, NX = args.nx;
     unsigned char* asm_ = smem;                             // V A tiles
@@ -223,6 +227,10 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
         float acc[kAnMaxAnchors];
 #pragma unroll
         for (int v = 0; v < kAnMaxAnchors; ++v) acc[v] = 0.f;
+        const bool gate_too = MODE == kAdBoth && plane == 1;
+        const bool gate_row = t0 + m < args.gate_rows;
+        if (gate_too && lane < kAnMaxAnchors) gsq[ew][lane] = 0.f;
+        __syncwarp();
         bool ok = true;
         for (int j = 0; ok && j < chunks; ++j) {
             const int xi = j % NX;
@@ -277,19 +285,28 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
                     acc[v] += s2.x + s2.y;
                 } else {
                     float s0 = 0.f, s1 = 0.f;
+                    float2 q2 = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const float2 d = __ffma2_rn(make_float2(__uint_as_float(r0[2 * e]), __uint_as_float(r0[2 * e + 1])),
                                                     neg, x2[e]);
                         s0 += fabsf(d.x) + fabsf(d.y);
+                        if (MODE == kAdBoth && gate_too) q2 = __ffma2_rn(d, d, q2);
                     }
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const float2 d = __ffma2_rn(make_float2(__uint_as_float(r1[2 * e]), __uint_as_float(r1[2 * e + 1])),
                                                     neg, x2[16 + e]);
                         s1 += fabsf(d.x) + fabsf(d.y);
+                        if (MODE == kAdBoth && gate_too) q2 = __ffma2_rn(d, d, q2);
                     }
                     acc[v] += s0 + s1;
+                    if (MODE == kAdBoth && gate_too) {
+                        float q = gate_row ? q2.x + q2.y : 0.f;
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+                        if (lane == 0) gsq[ew][v] += q;
+                    }
                 }
             }
         }
@@ -302,11 +319,16 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
                 if (v < V) red[m][v] = acc[v];
         }
         asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (MODE == kAdBoth && gate_too && ew == 0 && lane < V && !anchor_vload(&abort_flag)) {
+            float x = 0.f;
+            for (int w = 0; w < 8; ++w) x += gsq[w][lane];
+            args.partial[(((long long)c * args.L + l) * args.tiles + tile) * V + lane] = x;
+        }
         if (half == 0 && !anchor_vload(&abort_flag)) {
 #pragma unroll
             for (int v = 0; v < kAnMaxAnchors; ++v)
                 if (v < V) acc[v] += red[m][v];
-            if (MODE == kAdWeights) {
+            if (MODE != kAdGate) {
                 if (row_ok) {
                     const float invF = 1.f / (float)args.F;
                     float mmin = acc[0] * invF;
@@ -818,7 +840,7 @@ static cudaError_t launch_apply(const uint16_t* const* x, const Plane& p, uint16
 
 cudaError_t launch_anchor_correct(const AnchorPlanes& pl, const kvfix_kv_desc& d, const kvfix_kv_desc& od, int V,
                                   int r, double T, const int32_t* delta, const RopeTheta& th,
-                                  const int32_t* accept, cudaStream_t s) {
+                                  const int32_t* accept, cudaStream_t s, const AnchorGateOut* gate) {
     Plane p = plane_of(d), op = plane_of(od);
     if (p.chunks == 0 || p.layers == 0 || p.tokens == 0) return cudaSuccess;
     AdArgs args = {};
@@ -834,10 +856,25 @@ cudaError_t launch_anchor_correct(const AnchorPlanes& pl, const kvfix_kv_desc& d
     args.w[1] = pl.w[1];
     args.accept = accept;
     cudaError_t e;
-    if (r == 16) e = dist_maps_and_launch<16, kAdWeights>(pl.src, p, pl.ac, pl.bct, args, 2, s);
-    else if (r == 32) e = dist_maps_and_launch<32, kAdWeights>(pl.src, p, pl.ac, pl.bct, args, 2, s);
-    else e = dist_maps_and_launch<64, kAdWeights>(pl.src, p, pl.ac, pl.bct, args, 2, s);
-    if (e != cudaSuccess) return e;
+    if (gate) {
+        // the gate from the value plane's reconstructions of the same pass
+        args.partial = static_cast<float*>(gate->workspace);
+        args.gate_rows = gate->k;
+        if (r == 16) e = dist_maps_and_launch<16, kAdBoth>(pl.src, p, pl.ac, pl.bct, args, 2, s);
+        else if (r == 32) e = dist_maps_and_launch<32, kAdBoth>(pl.src, p, pl.ac, pl.bct, args, 2, s);
+        else e = dist_maps_and_launch<64, kAdBoth>(pl.src, p, pl.ac, pl.bct, args, 2, s);
+        if (e != cudaSuccess) return e;
+        anchor_gate_kernel<<<p.chunks, 32 * kAnMaxAnchors, 0, s>>>(args.partial, V, p.layers, args.tiles, gate->T,
+                                                                    gate->tau, gate->d, gate->g, gate->hbar,
+                                                                    gate->accept);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        accept = gate->accept;
+    } else {
+        if (r == 16) e = dist_maps_and_launch<16, kAdWeights>(pl.src, p, pl.ac, pl.bct, args, 2, s);
+        else if (r == 32) e = dist_maps_and_launch<32, kAdWeights>(pl.src, p, pl.ac, pl.bct, args, 2, s);
+        else e = dist_maps_and_launch<64, kAdWeights>(pl.src, p, pl.ac, pl.bct, args, 2, s);
+        if (e != cudaSuccess) return e;
+    }
     ApArgs ap = {};
     ap.V = V;
     ap.L = p.layers;

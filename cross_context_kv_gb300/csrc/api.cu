@@ -486,19 +486,19 @@ kvfix_status kvfix_anchor_gate(const kvfix_bf16* v_src, kvfix_kv_desc src, const
                     fn);
 }
 
-kvfix_status kvfix_anchor_correct(const kvfix_bf16* k_src, const kvfix_bf16* v_src, kvfix_kv_desc src,
-                                  const kvfix_bf16* a_c_k, const kvfix_bf16* b_ct_k, const kvfix_bf16* a_c_v,
-                                  const kvfix_bf16* b_ct_v, const kvfix_bf16* a_d_k, const kvfix_bf16* b_dt_k,
-                                  const kvfix_bf16* a_d_v, const kvfix_bf16* b_dt_v, int32_t anchors,
-                                  int32_t rank, double temperature, const int32_t* delta, double rope_base,
-                                  const int32_t* accept, float* w_k, float* w_v, kvfix_bf16* k_out,
-                                  kvfix_bf16* v_out, kvfix_kv_desc out, void* stream) {
-    const char* fn = "kvfix_anchor_correct";
+static kvfix_status anchor_correct_impl(const char* fn, const kvfix_bf16* k_src, const kvfix_bf16* v_src,
+                                        kvfix_kv_desc src, const kvfix_bf16* a_c_k, const kvfix_bf16* b_ct_k,
+                                        const kvfix_bf16* a_c_v, const kvfix_bf16* b_ct_v, const kvfix_bf16* a_d_k,
+                                        const kvfix_bf16* b_dt_k, const kvfix_bf16* a_d_v, const kvfix_bf16* b_dt_v,
+                                        int32_t anchors, int32_t rank, double temperature, const int32_t* delta,
+                                        double rope_base, const int32_t* accept, float* w_k, float* w_v,
+                                        kvfix_bf16* k_out, kvfix_bf16* v_out, kvfix_kv_desc out, void* stream,
+                                        const AnchorGateOut* gate) {
     kvfix_status st;
-    if ((st = check_plane(k_src, src, "kvfix_anchor_correct: k_src")) != KVFIX_OK) return st;
-    if ((st = check_plane(v_src, src, "kvfix_anchor_correct: v_src")) != KVFIX_OK) return st;
-    if ((st = check_plane(k_out, out, "kvfix_anchor_correct: k_out")) != KVFIX_OK) return st;
-    if ((st = check_plane(v_out, out, "kvfix_anchor_correct: v_out")) != KVFIX_OK) return st;
+    if ((st = check_plane(k_src, src, "anchor correction: k_src")) != KVFIX_OK) return st;
+    if ((st = check_plane(v_src, src, "anchor correction: v_src")) != KVFIX_OK) return st;
+    if ((st = check_plane(k_out, out, "anchor correction: k_out")) != KVFIX_OK) return st;
+    if ((st = check_plane(v_out, out, "anchor correction: v_out")) != KVFIX_OK) return st;
     if (!same_shape(src, out) || src.chunks != out.chunks)
         return fail(KVFIX_EINVAL, "%s: out must have the shape of src", fn);
     if (src.head_dim != 64 && src.head_dim != 128) return fail(KVFIX_EINVAL, "%s: head_dim must be 64 or 128", fn);
@@ -535,8 +535,52 @@ kvfix_status kvfix_anchor_correct(const kvfix_bf16* k_src, const kvfix_bf16* v_s
     pl.out[1] = v_out;
     RopeTheta th = make_theta(rope_base, src.head_dim);
     return launched(launch_anchor_correct(pl, src, out, anchors, rank, temperature, delta, th, accept,
-                                          (cudaStream_t)stream),
+                                          (cudaStream_t)stream, gate),
                     fn);
+}
+
+kvfix_status kvfix_anchor_correct(const kvfix_bf16* k_src, const kvfix_bf16* v_src, kvfix_kv_desc src,
+                                  const kvfix_bf16* a_c_k, const kvfix_bf16* b_ct_k, const kvfix_bf16* a_c_v,
+                                  const kvfix_bf16* b_ct_v, const kvfix_bf16* a_d_k, const kvfix_bf16* b_dt_k,
+                                  const kvfix_bf16* a_d_v, const kvfix_bf16* b_dt_v, int32_t anchors,
+                                  int32_t rank, double temperature, const int32_t* delta, double rope_base,
+                                  const int32_t* accept, float* w_k, float* w_v, kvfix_bf16* k_out,
+                                  kvfix_bf16* v_out, kvfix_kv_desc out, void* stream) {
+    return anchor_correct_impl("kvfix_anchor_correct", k_src, v_src, src, a_c_k, b_ct_k, a_c_v, b_ct_v, a_d_k, b_dt_k,
+                               a_d_v, b_dt_v, anchors, rank, temperature, delta, rope_base, accept, w_k, w_v, k_out,
+                               v_out, out, stream, nullptr);
+}
+
+kvfix_status kvfix_anchor_gate_correct(const kvfix_bf16* k_src, const kvfix_bf16* v_src, kvfix_kv_desc src,
+                                       const kvfix_bf16* a_c_k, const kvfix_bf16* b_ct_k, const kvfix_bf16* a_c_v,
+                                       const kvfix_bf16* b_ct_v, const kvfix_bf16* a_d_k, const kvfix_bf16* b_dt_k,
+                                       const kvfix_bf16* a_d_v, const kvfix_bf16* b_dt_v, int32_t anchors,
+                                       int32_t rank, int32_t prefix, double temperature, double tau,
+                                       const int32_t* delta, double rope_base, double* d, double* g, double* hbar,
+                                       int32_t* accept, float* w_k, float* w_v, kvfix_bf16* k_out, kvfix_bf16* v_out,
+                                       kvfix_kv_desc out, void* workspace, size_t workspace_bytes, void* stream) {
+    const char* fn = "kvfix_anchor_gate_correct";
+    if (prefix < 1 || prefix > src.tokens) return fail(KVFIX_EINVAL, "%s: prefix must be in [1, tokens]", fn);
+    if (isnan(tau)) return fail(KVFIX_EINVAL, "%s: tau must be a number", fn);
+    if (src.chunks > 0 && (!d || !g || !hbar || !accept))
+        return fail(KVFIX_EINVAL, "%s: d, g, hbar and accept are required", fn);
+    if (src.chunks > 0 && src.layers > 0) {
+        if (!workspace || workspace_bytes < anchor_gate_workspace_bytes(src, anchors, src.tokens))
+            return fail(KVFIX_EINVAL, "%s: workspace smaller than kvfix_anchor_gate_workspace_bytes(src, anchors, tokens)", fn);
+        if (!aligned16(workspace)) return fail(KVFIX_EINVAL, "%s: workspace not 16-byte aligned", fn);
+    }
+    AnchorGateOut gate;
+    gate.k = prefix;
+    gate.T = temperature;
+    gate.tau = tau;
+    gate.d = d;
+    gate.g = g;
+    gate.hbar = hbar;
+    gate.accept = accept;
+    gate.workspace = workspace;
+    return anchor_correct_impl(fn, k_src, v_src, src, a_c_k, b_ct_k, a_c_v, b_ct_v, a_d_k, b_dt_k, a_d_v, b_dt_v,
+                               anchors, rank, temperature, delta, rope_base, nullptr, w_k, w_v, k_out, v_out, out,
+                               stream, &gate);
 }
 
 // p / q rounded to the nearest integer, halves to even (p >= 0, q > 0).

@@ -126,10 +126,21 @@ cudaError_t launch_anchor_gate(const uint16_t* v_src, const kvfix_kv_desc& d, co
                                const uint16_t* bct, int V, int r, int k, double T, double tau,
                                double* dist, double* g, double* hbar, int32_t* accept,
                                void* workspace, cudaStream_t s);
+// With gate non-null, the gate is computed in the same pass (value plane, prefix k) and
+// its accept flags decide which segments are corrected.
+struct AnchorGateOut {
+    int k;
+    double T, tau;
+    double* d;
+    double* g;
+    double* hbar;
+    int32_t* accept;
+    void* workspace;  // anchor_gate_workspace_bytes(d, V, tokens)
+};
 cudaError_t launch_anchor_correct(const AnchorPlanes& pl, const kvfix_kv_desc& d,
                                   const kvfix_kv_desc& od, int V, int r, double T,
                                   const int32_t* delta, const RopeTheta& th, const int32_t* accept,
-                                  cudaStream_t s);
+                                  cudaStream_t s, const AnchorGateOut* gate = nullptr);
 
 // Bounded-wait self test.
 unsigned read_status_selftest(cudaStream_t stream);

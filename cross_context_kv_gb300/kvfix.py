@@ -54,6 +54,8 @@ SIGNATURES = {
     "kvfix_repair_layout": (ctypes.c_int, [P, I32, I32, I32, I32, I32, I32, F64, I32, P, I32, P, P]),
     "kvfix_master_select": (ctypes.c_int, [P, P, I32, I32, I32, P, P, P]),
     "kvfix_selftest_wait": (ctypes.c_int, [I64, P, P]),
+    "kvfix_anchor_gate_correct": (ctypes.c_int, [P, P, D, P, P, P, P, P, P, P, P, I32, I32, I32, F64, F64, P, F64, P,
+                                                 P, P, P, P, P, P, P, D, P, SZ, P]),
     "kvfix_diff_encode_split": (ctypes.c_int, [P, P, D, P, P, D, I32, P, P, P, P, P, P, I64, I64, P, P]),
     "kvfix_diff_gather_split": (ctypes.c_int, [P, P, D, P, P, P, P, P, P, I64, I64, I32, I32, P, P, D, P]),
     "kvfix_repair_rows": (ctypes.c_int, [P, P, D, P, P, D, P, I32, P, P]),
@@ -478,3 +480,34 @@ def selftest_wait(limit_cycles: int, flag=None):
         _i32(flag, "flag")
     s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     _check(lib.kvfix_selftest_wait(int(limit_cycles), _ptr(flag), s))
+
+
+def anchor_gate_correct(k_src, v_src, factors: dict, prefix: int, delta, rope_base: float,
+                        temperature: float = 1.0, tau: float = 0.5, out_k=None, out_v=None):
+    """The gate and the correction in one pass (see kvfix_anchor_gate_correct).  Returns
+    (out_k, out_v, w_k, w_v, d, g, hbar, accept)."""
+    _bf16(k_src, "k_src")
+    _bf16(v_src, "v_src")
+    _i32(delta, "delta")
+    C, L, n, H, Dh = k_src.shape
+    V, r = factors["a_c_k"].shape[1], factors["a_c_k"].shape[-1]
+    names = ("a_c_k", "b_ct_k", "a_c_v", "b_ct_v", "a_d_k", "b_dt_k", "a_d_v", "b_dt_v")
+    for nm in names:
+        _factor(factors[nm], nm, (C, V, L, n, r) if nm.startswith("a_") else (C, V, L, H * Dh, r))
+    dev = k_src.device
+    out_k = torch.empty_like(k_src) if out_k is None else out_k
+    out_v = torch.empty_like(v_src) if out_v is None else out_v
+    w_k = torch.empty((C, L, n, V), dtype=torch.float32, device=dev)
+    w_v = torch.empty_like(w_k)
+    d = torch.empty((C, V), dtype=torch.float64, device=dev)
+    g = torch.empty_like(d)
+    hbar = torch.empty(C, dtype=torch.float64, device=dev)
+    acc = torch.empty(C, dtype=torch.int32, device=dev)
+    desc = plane_desc(k_src)
+    nbytes = lib.kvfix_anchor_gate_workspace_bytes(desc, V, n)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    _check(lib.kvfix_anchor_gate_correct(_ptr(k_src), _ptr(v_src), desc, *[_ptr(factors[nm]) for nm in names], V, r,
+                                         int(prefix), float(temperature), float(tau), _ptr(delta), float(rope_base),
+                                         _ptr(d), _ptr(g), _ptr(hbar), _ptr(acc), _ptr(w_k), _ptr(w_v), _ptr(out_k),
+                                         _ptr(out_v), plane_desc(out_k), _ptr(ws), ws.numel(), _stream(k_src)))
+    return out_k, out_v, w_k, w_v, d, g, hbar, acc

@@ -497,6 +497,26 @@ KVFIX_API kvfix_status kvfix_diff_gather_split(
     kvfix_bf16* out_k, kvfix_bf16* out_v, kvfix_kv_desc out, void* stream);
 
 /*
+ * kvfix_anchor_gate_correct -- kvfix_anchor_gate and kvfix_anchor_correct in one pass over
+ * the sources: the gate's value-plane distances (prefix k) come from the same
+ * reconstructions as the value plane's token weights, the gate is decided on the device,
+ * and only accepted segments are corrected (rejected ones keep their outputs; their
+ * weights are still written).  Arguments as for the two calls; `accept` is an output here.
+ * The gate's per-tile sums are folded per warp and then over the warps in a fixed order,
+ * so d differs from kvfix_anchor_gate's in the last bits (and is deterministic).
+ * workspace: at least kvfix_anchor_gate_workspace_bytes(src, anchors, src.tokens).
+ * head_dim 64 or 128.
+ */
+KVFIX_API kvfix_status kvfix_anchor_gate_correct(
+    const kvfix_bf16* k_src, const kvfix_bf16* v_src, kvfix_kv_desc src, const kvfix_bf16* a_c_k,
+    const kvfix_bf16* b_ct_k, const kvfix_bf16* a_c_v, const kvfix_bf16* b_ct_v,
+    const kvfix_bf16* a_d_k, const kvfix_bf16* b_dt_k, const kvfix_bf16* a_d_v,
+    const kvfix_bf16* b_dt_v, int32_t anchors, int32_t rank, int32_t prefix, double temperature,
+    double tau, const int32_t* delta, double rope_base, double* d, double* g, double* hbar,
+    int32_t* accept, float* w_k, float* w_v, kvfix_bf16* k_out, kvfix_bf16* v_out,
+    kvfix_kv_desc out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * kvfix_selftest_wait -- exercise the bounded wait that every pipelined kernel uses, with
  * no hang: one warp waits on a barrier phase that never completes and then on the device
  * int32 *flag (optional; 0 = not set), each for at most limit_cycles SM clocks, and records

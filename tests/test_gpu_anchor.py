@@ -174,3 +174,31 @@ def test_single_anchor_gate_rejects_and_weights_are_one():
                                np.ones((cfg.segments, cfg.layers, cfg.tokens, 1)), cfg.kv_heads,
                                inp["delta"].cpu().numpy(), cfg.rope_base, False)
     assert_close_kv(flat(ov), ro, "single anchor out_v")
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+def test_gate_correct_in_one_pass(cfg):
+    """The fused call gives the gate of kvfix_anchor_gate (to rounding, against the oracle)
+    and the outputs of kvfix_anchor_correct for accepted segments, untouched ones for the
+    rejected."""
+    inp = synth.anchor_inputs(cfg, DEV)
+    src = compose(cfg, inp)
+    for k, tau in ((cfg.tokens, cfg.tau), (77, cfg.tau), (cfg.tokens, -1.0)):
+        ok0 = torch.full_like(src["k"], 3.0)
+        ov0 = torch.full_like(src["v"], 3.0)
+        ok, ov, wk, wv, d, g, hbar, acc = kvfix().anchor_gate_correct(
+            src["k"], src["v"], factors(inp), k, inp["delta"], cfg.rope_base, tau=tau, out_k=ok0, out_v=ov0)
+        kvfix().check_status()
+        ref = oracle.anchor_gate(flat(src["v"]), synth.bits(inp["a_c_v"]), synth.bits(inp["b_ct_v"]), k, tau=tau)
+        check_gate((d, g, hbar, acc), ref, tau, f"{cfg.name} k={k}")
+        rk, rv, rwk, rwv = kvfix().anchor_correct(src["k"], src["v"], factors(inp), inp["delta"], cfg.rope_base)
+        assert torch.equal(wk, rwk) and torch.equal(wv, rwv)
+        for c in range(cfg.segments):
+            if acc[c]:
+                assert torch.equal(ok[c].view(torch.int16), rk[c].view(torch.int16))
+                assert torch.equal(ov[c].view(torch.int16), rv[c].view(torch.int16))
+            else:
+                assert (ok[c] == 3.0).all() and (ov[c] == 3.0).all()
+    g1 = kvfix().anchor_gate_correct(src["k"], src["v"], factors(inp), cfg.tokens, inp["delta"], cfg.rope_base)
+    g2 = kvfix().anchor_gate_correct(src["k"], src["v"], factors(inp), cfg.tokens, inp["delta"], cfg.rope_base)
+    assert torch.equal(g1[4], g2[4])                 # deterministic distances
