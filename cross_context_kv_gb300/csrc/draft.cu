@@ -3,8 +3,8 @@
 //
 // Method: Budgeted Cache Repair, section 3 ("The repair": row score a_j summed over
 // layers after the first, steps and heads of softmax(Q K~^T / sqrt(d_head))), App. B
-// Algorithm 2 (grouped-query keys expanded to query heads) and Algorithm 1 step 6
-// (the selected rows' K and V are overwritten before use); KVCMAS Eq. 3.
+// Algorithm 2 (grouped-query keys expanded to query heads) and Algorithm 1 (the
+// selected rows' K and V are overwritten before use); KVCMAS Eq. 3.
 //
 // Pipeline (one unit = chunk, layer >= layer_begin, KV head; its G = steps x
 // q_heads/kv_heads <= 16 query rows share the unit's keys):

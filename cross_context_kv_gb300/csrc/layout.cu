@@ -5,9 +5,9 @@
 // Method: Budgeted Cache Repair, section 3 "The layouts" (BCR-single: the best rows;
 // BCR-chunk: fixed 64-token chunks, the best rho of them; BCR-grow: a span seeded on the
 // best row, extended while a neighbour scores at least tau of the seed); App. A.2 "The
-// policy" step 2 (a chunk is scored by the mean of its rows, a short trailing chunk by its
-// own mean) and Table 8 (max(1, round(rho n_chunks)) chunks); App. B, Algorithm 1 lines
-// 1-2 (skip when M < 2B or rho M < B; round(rho M / B) chunks) and Algorithm 2 line 5.
+// policy" (a chunk is scored by the mean of its rows, a short trailing chunk by its own
+// mean) and Table 8 (max(1, round(rho n_chunks)) chunks); App. B, Algorithm 1 (skip when
+// M < 2B or rho M < B; round(rho M / B) chunks) and Algorithm 2 (chunk scores).
 //
 // One CTA per unit: the keys (row scores, or chunk means summed row by row in index
 // order) sit in shared memory; an 8-bit radix search marks the best rows or chunks

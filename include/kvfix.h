@@ -196,8 +196,8 @@ KVFIX_API kvfix_status kvfix_lowrank_apply(const kvfix_bf16* x, kvfix_kv_desc de
  * kvfix_draft_rank -- rank cached rows by the attention mass of draft queries, keep
  * the best k_rows, and optionally repair them.
  * [BCR] section 3 ("The repair": the row score a_j), App. B Algorithm 2 (draft
- * scoring with grouped-query keys expanded to query heads) and Algorithm 1 step 6
- * (selected rows' K and V overwritten with exact ones); [KVCMAS] Eq. 3.
+ * scoring with grouped-query keys expanded to query heads) and Algorithm 1 (the
+ * selected rows' K and V overwritten with exact ones); [KVCMAS] Eq. 3.
  *
  *     scores[c][j] = sum_{l >= layer_begin} sum_{t < draft_steps} sum_{h < q_heads}
  *                    softmax_j( q[c][l][t][h] . k[c][l][j][h / (q_heads/kv_heads)] / sqrt(D) )
@@ -404,8 +404,8 @@ KVFIX_API kvfix_status kvfix_anchor_correct(
 
 /*
  * kvfix_repair_layout -- the rows a draft-scored repair recomputes, in one of the layouts
- * of [BCR] section 3 "The layouts", App. A.2 ("The policy" step 2, Table 8) and App. B
- * (Algorithm 1 lines 1-2, Algorithm 2 line 5).  For each unit u of scores [units][tokens]
+ * of [BCR] section 3 "The layouts", App. A.2 ("The policy", Table 8) and App. B
+ * (Algorithms 1 and 2).  For each unit u of scores [units][tokens]
  * (e.g. kvfix_draft_rank's), with rho = budget_num / budget_den and rounding of halves
  * to even:
  *   KVFIX_LAYOUT_SINGLE: the round(rho n) rows with the largest scores;
@@ -413,7 +413,7 @@ KVFIX_API kvfix_status kvfix_anchor_correct(
  *                        the mean of its rows' scores (summed in index order, in double);
  *                        the max(1, round(rho n / chunk_tokens)) best chunks, all their
  *                        rows.  skip_rule != 0: no rows when n < 2 chunk_tokens or
- *                        rho n < chunk_tokens (Algorithm 1 line 1);
+ *                        rho n < chunk_tokens (Algorithm 1's skip rule);
  *   KVFIX_LAYOUT_GROW  : round(rho n) rows: the best unselected row seeds a span, which
  *                        takes the better of its two unselected neighbours (left on a tie)
  *                        while that one scores at least tau times the seed, until neither
@@ -434,8 +434,8 @@ KVFIX_API kvfix_status kvfix_repair_layout(const double* scores, int32_t units, 
                                            void* stream);
 
 /*
- * kvfix_repair_rows -- overwrite the chosen rows with exact ones ([BCR] App. B Algorithm 1
- * line 6; [KVCMAS] Eq. 3): for every chunk c of `desc`, layer and KV head, rows
+ * kvfix_repair_rows -- overwrite the chosen rows with exact ones ([BCR] App. B Algorithm 1;
+ * [KVCMAS] Eq. 3): for every chunk c of `desc`, layer and KV head, rows
  * idx[c][0 .. counts[c]) of k_io / v_io get the same rows of k_fresh / v_fresh
  * (`fresh_desc`, the shape of desc).  idx holds max_rows entries per chunk; rows out of
  * range are skipped and flagged (KVFIX_EDEVICE in kvfix_check_status).  Either plane may

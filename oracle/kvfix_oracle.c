@@ -193,8 +193,8 @@ EXPORT void oracle_compose_fresh(const uint16_t* reuse, const float* mu, const f
 /* ---------------------------------------------------- divergence scores */
 
 /*
- * Check-layer divergence (AgentKVShift, "Core idea and method", step 1 and the
- * displayed d_{K,j} = || K_fresh,j - K_reuse,j ||_2; TokenDance section 4.2: the rotated
+ * Check-layer divergence (AgentKVShift, "Core idea and method": the score of each
+ * token and the displayed d_{K,j} = || K_fresh,j - K_reuse,j ||_2; TokenDance section 4.2: the rotated
  * keys are compared with the cached ones at one check layer):
  *   d[a][r][j] = sqrt( sum over heads h, dims e of (fresh[a][r][j][h][e] - rot(reuse[r][j][h])[e])^2 )
  * The norm runs over the whole token row (all KV heads), since probes are tokens.
@@ -252,7 +252,7 @@ static int int_asc(const void* pa, const void* pb)
 
 /*
  * The b indices with the largest key, ties to the lower index, returned in
- * ascending index order (AgentKVShift, step 2: the b tokens with the largest score,
+ * ascending index order (AgentKVShift, "Core idea and method": the b tokens with the largest score,
  * one set per score; Budgeted Cache Repair section 3: the best-scoring rows up to the
  * budget).  keys_as_float != 0 rounds each key to binary32 first, so that the
  * ranking decision is taken in the same precision as a float32 score.
@@ -384,7 +384,7 @@ EXPORT void oracle_lowrank_apply(const uint16_t* x, const uint16_t* A, const uin
 /*
  * Draft-attention row scores (Budgeted Cache Repair, section 3 "The repair": a_j is the
  * softmax(Q K~^T / sqrt(d_head)) mass the draft queries put on row j, over layers after
- * the first; App. B, Algorithm 2 step 5, grouped-query keys expanded to query heads):
+ * the first; App. B, Algorithm 2, grouped-query keys expanded to query heads):
  *   a[c][j] = sum_{l >= layer_begin} sum_{t < T} sum_{h < Hq}
  *               exp(z_j - max z) / sum_i exp(z_i - max z),
  *   z_i = q[c][l][t][h] . k[c][l][i][h / (Hq/Hkv)] / sqrt(D).
@@ -435,8 +435,8 @@ EXPORT void oracle_draft_scores(const uint16_t* k, const uint16_t* q, int C, int
 }
 
 /*
- * Budgeted repair of the selected rows (Budgeted Cache Repair, App. B, Algorithm 1
- * step 6: the selected rows' keys and values are overwritten with exact ones; KVCMAS
+ * Budgeted repair of the selected rows (Budgeted Cache Repair, App. B, Algorithm 1:
+ * the selected rows' keys and values are overwritten with exact ones; KVCMAS
  * Eq. 3 selective recomputation): for every layer and head,
  *   kv[c][l][j] = fresh[c][l][j] for j in idx[c][0..k-1].
  */
@@ -733,8 +733,8 @@ static int64_t round_half_even(int64_t p, int64_t q)
 
 /*
  * Rows to repair from per-row draft scores, in the three layouts of Budgeted Cache
- * Repair (section 3 "The layouts"; App. A.2 "The policy" step 2 and Table 8; App. B,
- * Algorithm 1 lines 1-2 and Algorithm 2 line 5), for each unit u of scores [U][n]:
+ * Repair (section 3 "The layouts"; App. A.2 "The policy" and Table 8; App. B,
+ * Algorithms 1 and 2), for each unit u of scores [U][n]:
  *   layout 0 (single): the round(rho n) rows with the largest scores;
  *   layout 1 (chunk):  B-token chunks (the last one may be short), each scored by the mean
  *                      of its rows' scores; the max(1, round(rho n / B)) best chunks, all
