@@ -431,7 +431,7 @@ def stage_diff(kvfix, peak, steps=5, warmup=2):
     gat_bytes = 2 * plane + entries * blk + 2 * plane * cfg.siblings + E // 8 + 8 * (E + 1)
     # per-plane lists of the same siblings (the generator dirties K and V in the same
     # blocks, so both lists equal the joint one): encode and gather
-    sp_enc, sp_gat = [], []
+    sp_enc, sp_gat, sp_res = [], [], []
     kl, vl, sent = kvfix.diff_encode_split(inp["master_k"], inp["master_v"], inp["sib_k"], inp["sib_v"],
                                            cfg.block_tokens)
     for s in range(warmup + steps):
@@ -449,10 +449,18 @@ def stage_diff(kvfix, peak, steps=5, warmup=2):
         kvfix.diff_gather_split(inp["master_k"], inp["master_v"], kl, vl, cfg.siblings, cfg.block_tokens, out_k,
                                 out_v, entries=sent)
         e3.record(stream)
+        flush.zero_()
+        host_lead()
+        e4, e5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e4.record(stream)
+        kvfix.diff_restore_split(inp["master_k"], inp["master_v"], kl, vl, cfg.siblings, cfg.block_tokens,
+                                 tgt["delta"], cfg.rope_base, tgt["slot_mapping"], pool_k, pool_v, entries=sent)
+        e5.record(stream)
         torch.cuda.synchronize()
         if s >= warmup:
             sp_enc.append(e0.elapsed_time(e1))
             sp_gat.append(e2.elapsed_time(e3))
+            sp_res.append(e4.elapsed_time(e5))
     kvfix.check_status()
     del kl, vl
     res_bytes = gat_bytes + cfg.siblings * (cfg.tokens + 1) * 4
@@ -468,7 +476,9 @@ def stage_diff(kvfix, peak, steps=5, warmup=2):
            "split_lists": {"entries": list(sent), "encode_ms": round(statistics.mean(sp_enc), 4),
                            "encode_frac": round((enc_bytes + 8 * (E + 1) + E // 8) / statistics.mean(sp_enc) / 1e6 / peak, 4),
                            "gather_ms": round(statistics.mean(sp_gat), 4),
-                           "gather_frac": round((gat_bytes + 8 * (E + 1) + E // 8) / statistics.mean(sp_gat) / 1e6 / peak, 4)},
+                           "gather_frac": round((gat_bytes + 8 * (E + 1) + E // 8) / statistics.mean(sp_gat) / 1e6 / peak, 4),
+                           "restore_ms": round(statistics.mean(sp_res), 4),
+                           "restore_frac": round((res_bytes + 8 * (E + 1) + E // 8) / statistics.mean(sp_res) / 1e6 / peak, 4)},
            "restore": {"ms": round(rst, 4), "algorithmic_bytes": res_bytes,
                        "GBps": round(res_bytes / rst / 1e6, 1), "frac": round(res_bytes / rst / 1e6 / peak, 4),
                        "pool": f"{tgt['slots']} slots of 16-token pages, keys re-aligned per sibling"}}
@@ -819,6 +829,10 @@ def run_profile_case(name: str, iters: int = 3):
                                payload_entries=entries)
     elif name == "diff_split":
         inp = synth.diff_inputs(cfg, "cuda")
+        tgt = synth.restore_inputs(cfg, "cuda")
+        pk = torch.empty((cfg.layers, tgt["slots"], cfg.kv_heads, cfg.head_dim), dtype=torch.bfloat16,
+                         device="cuda")
+        pv = torch.empty_like(pk)
         _, _, ent = kvfix.diff_encode_split(inp["master_k"], inp["master_v"], inp["sib_k"], inp["sib_v"],
                                             cfg.block_tokens)
         def step():
@@ -826,6 +840,8 @@ def run_profile_case(name: str, iters: int = 3):
                                                 cfg.block_tokens, capacity=ent, sync=False)
             kvfix.diff_gather_split(inp["master_k"], inp["master_v"], kl, vl, cfg.siblings, cfg.block_tokens,
                                     entries=ent)
+            kvfix.diff_restore_split(inp["master_k"], inp["master_v"], kl, vl, cfg.siblings, cfg.block_tokens,
+                                     tgt["delta"], cfg.rope_base, tgt["slot_mapping"], pk, pv, entries=ent)
     elif name == "layout":
         # heavy-tailed row scores like the draft's (seeded), then both layouts and their repair
         g = torch.Generator(device="cuda").manual_seed(cfg.seed)

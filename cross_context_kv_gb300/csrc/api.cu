@@ -394,19 +394,24 @@ kvfix_status kvfix_diff_gather(const kvfix_bf16* master_k, const kvfix_bf16* mas
                                        (cudaStream_t)stream), fn);
 }
 
-kvfix_status kvfix_diff_restore(const kvfix_bf16* master_k, const kvfix_bf16* master_v,
-                                kvfix_kv_desc master, const uint32_t* mask,
-                                const int64_t* offsets, const kvfix_bf16* payload,
-                                int64_t payload_entries, int32_t siblings, int32_t block_tokens,
-                                const int32_t* delta, double rope_base,
-                                const int32_t* slot_mapping, kvfix_bf16* pool_k,
-                                kvfix_bf16* pool_v, kvfix_kv_desc pool, void* stream) {
-    const char* fn = "kvfix_diff_restore";
+// Shared by the joint and the per-plane restore: with mask_v set, (mask, offsets, payload,
+// payload_entries) is the key plane's list and (mask_v, offsets_v, payload_v, entries_v) the
+// value plane's; otherwise one list holds both planes.
+static kvfix_status restore_impl(const char* fn, const kvfix_bf16* master_k, const kvfix_bf16* master_v,
+                                 kvfix_kv_desc master, const uint32_t* mask, const int64_t* offsets,
+                                 const kvfix_bf16* payload, int64_t payload_entries, const uint32_t* mask_v,
+                                 const int64_t* offsets_v, const kvfix_bf16* payload_v, int64_t entries_v,
+                                 bool split, int32_t siblings, int32_t block_tokens, const int32_t* delta,
+                                 double rope_base, const int32_t* slot_mapping, kvfix_bf16* pool_k,
+                                 kvfix_bf16* pool_v, kvfix_kv_desc pool, void* stream) {
     kvfix_status st;
-    if ((st = check_plane(master_k, master, "kvfix_diff_restore: master_k")) != KVFIX_OK) return st;
-    if ((st = check_plane(master_v, master, "kvfix_diff_restore: master_v")) != KVFIX_OK) return st;
-    if ((st = check_plane(pool_k, pool, "kvfix_diff_restore: pool_k")) != KVFIX_OK) return st;
-    if ((st = check_plane(pool_v, pool, "kvfix_diff_restore: pool_v")) != KVFIX_OK) return st;
+    char what[64];
+    const void* planes[4] = {master_k, master_v, pool_k, pool_v};
+    const char* names[4] = {"master_k", "master_v", "pool_k", "pool_v"};
+    for (int i = 0; i < 4; ++i) {
+        snprintf(what, sizeof what, "%s: %s", fn, names[i]);
+        if ((st = check_plane(planes[i], i < 2 ? master : pool, what)) != KVFIX_OK) return st;
+    }
     if (master.chunks != 1 || pool.chunks != 1)
         return fail(KVFIX_EINVAL, "%s: master.chunks and pool.chunks must be 1", fn);
     if (pool.layers != master.layers || pool.kv_heads != master.kv_heads ||
@@ -416,23 +421,50 @@ kvfix_status kvfix_diff_restore(const kvfix_bf16* master_k, const kvfix_bf16* ma
         return fail(KVFIX_EINVAL, "%s: block_tokens must divide tokens", fn);
     if (siblings < 0 || siblings > 65535 || master.layers > 65535)
         return fail(KVFIX_EINVAL, "%s: siblings and layers must be <= 65535", fn);
-    if (!mask || !offsets) return fail(KVFIX_EINVAL, "%s: mask and offsets are required", fn);
+    if (!mask || !offsets || (split && (!mask_v || !offsets_v)))
+        return fail(KVFIX_EINVAL, "%s: every mask and offset array is required", fn);
     if (siblings > 0 && (!delta || (master.tokens > 0 && !slot_mapping)))
         return fail(KVFIX_EINVAL, "%s: delta and slot_mapping are required", fn);
     if (!(rope_base > 1.0) || !isfinite(rope_base))
         return fail(KVFIX_EINVAL, "%s: rope_base must be finite and > 1", fn);
-    if (payload_entries < 0) return fail(KVFIX_EINVAL, "%s: negative payload_entries", fn);
-    if (payload_entries > 0 && (!payload || !aligned16(payload)))
-        return fail(KVFIX_EINVAL, "%s: payload must be a 16-byte aligned device pointer", fn);
+    if (payload_entries < 0 || entries_v < 0) return fail(KVFIX_EINVAL, "%s: negative payload entries", fn);
+    if ((payload_entries > 0 && (!payload || !aligned16(payload))) ||
+        (split && entries_v > 0 && (!payload_v || !aligned16(payload_v))))
+        return fail(KVFIX_EINVAL, "%s: payloads must be 16-byte aligned device pointers", fn);
     if (overlaps(pool_k, pool, master_k, master) || overlaps(pool_v, pool, master_v, master) ||
         overlaps(pool_k, pool, master_v, master) || overlaps(pool_v, pool, master_k, master) ||
         overlaps(pool_k, pool, pool_v, pool))
         return fail(KVFIX_EINVAL, "%s: pool planes overlap the master or each other", fn);
     RopeTheta th = make_theta(rope_base, master.head_dim);
-    return launched(launch_diff_restore(master_k, master_v, master, mask, offsets, payload,
-                                        payload_entries, siblings, block_tokens, delta, th,
-                                        slot_mapping, pool_k, pool_v, pool, (cudaStream_t)stream),
+    return launched(launch_diff_restore(master_k, master_v, master, mask, offsets, payload, payload_entries,
+                                        siblings, block_tokens, delta, th, slot_mapping, pool_k, pool_v, pool,
+                                        (cudaStream_t)stream, split ? mask_v : nullptr, offsets_v, payload_v,
+                                        split ? entries_v : 0),
                     fn);
+}
+
+kvfix_status kvfix_diff_restore(const kvfix_bf16* master_k, const kvfix_bf16* master_v,
+                                kvfix_kv_desc master, const uint32_t* mask,
+                                const int64_t* offsets, const kvfix_bf16* payload,
+                                int64_t payload_entries, int32_t siblings, int32_t block_tokens,
+                                const int32_t* delta, double rope_base,
+                                const int32_t* slot_mapping, kvfix_bf16* pool_k,
+                                kvfix_bf16* pool_v, kvfix_kv_desc pool, void* stream) {
+    return restore_impl("kvfix_diff_restore", master_k, master_v, master, mask, offsets, payload, payload_entries,
+                        nullptr, nullptr, nullptr, 0, false, siblings, block_tokens, delta, rope_base,
+                        slot_mapping, pool_k, pool_v, pool, stream);
+}
+
+kvfix_status kvfix_diff_restore_split(const kvfix_bf16* master_k, const kvfix_bf16* master_v,
+                                      kvfix_kv_desc master, const uint32_t* mask_k, const uint32_t* mask_v,
+                                      const int64_t* offsets_k, const int64_t* offsets_v,
+                                      const kvfix_bf16* payload_k, const kvfix_bf16* payload_v, int64_t entries_k,
+                                      int64_t entries_v, int32_t siblings, int32_t block_tokens,
+                                      const int32_t* delta, double rope_base, const int32_t* slot_mapping,
+                                      kvfix_bf16* pool_k, kvfix_bf16* pool_v, kvfix_kv_desc pool, void* stream) {
+    return restore_impl("kvfix_diff_restore_split", master_k, master_v, master, mask_k, offsets_k, payload_k,
+                        entries_k, mask_v, offsets_v, payload_v, entries_v, true, siblings, block_tokens, delta,
+                        rope_base, slot_mapping, pool_k, pool_v, pool, stream);
 }
 
 static kvfix_status check_factor(const void* p, const char* fn, const char* name) {

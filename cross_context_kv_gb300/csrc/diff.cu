@@ -552,18 +552,21 @@ __device__ __forceinline__ void restore_rotate8(uint4& lo, uint4& hi, const floa
 // (cos, sin, -sin) of the column's 8 angles are read once for both rows.  Siblings go in
 // chunks of up to 16: per chunk the CTA stages in shared memory each sibling's payload
 // entry (or -1), its angle tables and the pool slots of the pass's rows, so the
-// per-sibling loop issues its stores without waiting on global memory.
+// per-sibling loop issues its stores without waiting on global memory.  With per-plane
+// lists (vl.mask set) each sibling has a K entry in the first list and a V entry in vl,
+// each holding one plane's block.
 __global__ void __launch_bounds__(kRestoreThreads, 1)
 diff_restore_kernel(const uint16_t* __restrict__ mk, const uint16_t* __restrict__ mv, Plane mp,
                     const uint32_t* __restrict__ mask, const int64_t* __restrict__ offsets,
                     const uint16_t* __restrict__ payload, long long payload_entries, int S, int bt,
                     const int32_t* __restrict__ delta, RopeTheta th,
-                    const int32_t* __restrict__ slot_map, uint16_t* pk, uint16_t* pv, Plane pp) {
+                    const int32_t* __restrict__ slot_map, uint16_t* pk, uint16_t* pv, Plane pp, SplitList vl) {
     __shared__ __align__(16) float cos_s[kRestoreSibChunk][kMaxHeadDim / 2];
     __shared__ __align__(16) float sin_s[kRestoreSibChunk][kMaxHeadDim / 2];
     __shared__ __align__(16) float nsin_s[kRestoreSibChunk][kMaxHeadDim / 2];
     __shared__ int slot_s[kRestoreSlotStage];
-    __shared__ long long ent_s[kRestoreSibChunk];
+    __shared__ long long ent_s[kRestoreSibChunk], entv_s[kRestoreSibChunk];
+    const bool split = vl.mask != nullptr;  // per-plane lists: each payload entry holds one plane
     __shared__ int rot_s[kRestoreSibChunk];
     const int blk = blockIdx.x, l = blockIdx.y;
     const int n = mp.tokens, nblk = n / bt, L = mp.layers;
@@ -634,18 +637,21 @@ diff_restore_kernel(const uint16_t* __restrict__ mk, const uint16_t* __restrict_
                 if (threadIdx.x < sc) {
                     const int s = s0 + threadIdx.x;
                     const long long i = ((long long)s * L + l) * nblk + blk;
-                    long long e = mask_bit(mask, i) ? offsets[i] : -1;
-                    if (e >= payload_entries) {
-                        atomicOr(&g_status_diff, FLAG_NOSPACE);
-                        e = -1;
-                    }
-                    ent_s[threadIdx.x] = e;
+                    ent_s[threadIdx.x] = diff_entry(mask, offsets, payload_entries, i);
+                    entv_s[threadIdx.x] = split ? diff_entry(vl.mask, vl.offsets, vl.entries, i) : -1;
                     rot_s[threadIdx.x] = delta[s] != 0;
                 }
                 __syncthreads();
                 for (int ss = 0; ss < sc; ++ss) {
                     const long long e = ent_s[ss];
-                    const uint16_t* src = e >= 0 ? payload + e * 2 * blk_elems : nullptr;
+                    const uint16_t* src = e >= 0 ? payload + e * (split ? 1 : 2) * blk_elems : nullptr;
+                    const uint16_t* srcv;  // the V block: after the K block, or its own list's entry
+                    if (split) {
+                        const long long ev = entv_s[ss];
+                        srcv = ev >= 0 ? vl.payload + ev * blk_elems : nullptr;
+                    } else {
+                        srcv = src ? src + blk_elems : nullptr;
+                    }
                     const bool rotate = rot_s[ss] != 0 && k_ok;
                     float2 cc[4], sn[4], ns[4];
                     if (rotate) {
@@ -677,8 +683,7 @@ diff_restore_kernel(const uint16_t* __restrict__ mk, const uint16_t* __restrict_
                         for (int y = 0; y < 2; ++y) {
                             if (!v_ok[y]) continue;
                             uint4 v = vv[x][y];
-                            if (src)
-                                v = ld_stream(reinterpret_cast<const uint4*>(src + blk_elems + srow + vo[y]));
+                            if (srcv) v = ld_stream(reinterpret_cast<const uint4*>(srcv + srow + vo[y]));
                             st_stream(reinterpret_cast<uint4*>(pvl + prow + vo[y]), v);
                         }
                     }
@@ -693,13 +698,15 @@ cudaError_t launch_diff_restore(const uint16_t* mk, const uint16_t* mv, const kv
                                 const uint16_t* payload, long long payload_entries, int siblings,
                                 int bt, const int32_t* delta, const RopeTheta& th,
                                 const int32_t* slot_map, uint16_t* pk, uint16_t* pv,
-                                const kvfix_kv_desc& pd, cudaStream_t s) {
+                                const kvfix_kv_desc& pd, cudaStream_t s, const uint32_t* mask_v,
+                                const int64_t* offsets_v, const uint16_t* payload_v, long long entries_v) {
     Plane mp = plane_of(md), pp = plane_of(pd);
+    SplitList vl{mask_v, offsets_v, payload_v, entries_v};
     if (mp.layers == 0 || mp.tokens == 0 || siblings == 0) return cudaSuccess;
     dim3 grid(mp.tokens / bt, mp.layers);
     diff_restore_kernel<<<grid, kRestoreThreads, 0, s>>>(mk, mv, mp, mask, offsets, payload,
                                                          payload_entries, siblings, bt, delta, th,
-                                                         slot_map, pk, pv, pp);
+                                                         slot_map, pk, pv, pp, vl);
     return cudaGetLastError();
 }
 

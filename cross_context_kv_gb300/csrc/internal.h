@@ -107,7 +107,9 @@ cudaError_t launch_diff_restore(const uint16_t* mk, const uint16_t* mv, const kv
                                 const uint16_t* payload, long long payload_entries, int siblings,
                                 int bt, const int32_t* delta, const RopeTheta& th,
                                 const int32_t* slot_map, uint16_t* pk, uint16_t* pv,
-                                const kvfix_kv_desc& pd, cudaStream_t s);
+                                const kvfix_kv_desc& pd, cudaStream_t s, const uint32_t* mask_v = nullptr,
+                                const int64_t* offsets_v = nullptr, const uint16_t* payload_v = nullptr,
+                                long long entries_v = 0);
 
 // Anchor-pool correction (both planes: index 0 = keys, rotated; 1 = values).
 struct AnchorPlanes {

@@ -58,6 +58,8 @@ SIGNATURES = {
                                                  P, P, P, P, P, P, P, D, P, SZ, P]),
     "kvfix_diff_encode_split": (ctypes.c_int, [P, P, D, P, P, D, I32, P, P, P, P, P, P, I64, I64, P, P]),
     "kvfix_diff_gather_split": (ctypes.c_int, [P, P, D, P, P, P, P, P, P, I64, I64, I32, I32, P, P, D, P]),
+    "kvfix_diff_restore_split": (ctypes.c_int, [P, P, D, P, P, P, P, P, P, I64, I64, I32, I32, P, F64, P, P, P, D,
+                                                P]),
     "kvfix_repair_rows": (ctypes.c_int, [P, P, D, P, P, D, P, I32, P, P]),
     "kvfix_anchor_gate_workspace_bytes": (SZ, [D, I32, I32]),
     "kvfix_anchor_gate": (ctypes.c_int, [P, D, P, P, I32, I32, I32, F64, F64, P, P, P, P, P, SZ, P]),
@@ -472,6 +474,29 @@ def diff_gather_split(master_k, master_v, k_list, v_list, siblings: int, block_t
                                        int(siblings), int(block_tokens), _ptr(out_k), _ptr(out_v), plane_desc(out_k),
                                        _stream(mk)))
     return out_k, out_v
+
+
+def diff_restore_split(master_k, master_v, k_list, v_list, siblings: int, block_tokens: int, delta,
+                       rope_base: float, slot_mapping, pool_k, pool_v, entries=None):
+    """diff_restore from the per-plane lists of diff_encode_split (written in place)."""
+    for t, name in ((master_k, "master_k"), (master_v, "master_v"), (pool_k, "pool_k"), (pool_v, "pool_v")):
+        _bf16(t, name)
+    _i32(delta, "delta")
+    _i32(slot_mapping, "slot_mapping")
+    mk = master_k.unsqueeze(0) if master_k.dim() == 4 else master_k
+    mv = master_v.unsqueeze(0) if master_v.dim() == 4 else master_v
+    if pool_k.dim() != 4 or pool_v.shape != pool_k.shape:
+        raise ValueError("pool_k and pool_v must both be [layers][slots][heads][dim]")
+    if delta.numel() != int(siblings) or slot_mapping.numel() != int(siblings) * mk.shape[2]:
+        raise ValueError("delta must hold one shift per sibling and slot_mapping one slot per "
+                         "(sibling, token)")
+    ek, ev = (k_list[2].shape[0], v_list[2].shape[0]) if entries is None else entries
+    _check(lib.kvfix_diff_restore_split(_ptr(mk), _ptr(mv), plane_desc(mk), _ptr(k_list[0]), _ptr(v_list[0]),
+                                        _ptr(k_list[1]), _ptr(v_list[1]), _ptr(k_list[2]), _ptr(v_list[2]),
+                                        int(ek), int(ev), int(siblings), int(block_tokens), _ptr(delta),
+                                        float(rope_base), _ptr(slot_mapping), _ptr(pool_k), _ptr(pool_v),
+                                        plane_desc(pool_k.unsqueeze(0)), _stream(mk)))
+    return pool_k, pool_v
 
 
 def selftest_wait(limit_cycles: int, flag=None):

@@ -497,6 +497,23 @@ KVFIX_API kvfix_status kvfix_diff_gather_split(
     kvfix_bf16* out_k, kvfix_bf16* out_v, kvfix_kv_desc out, void* stream);
 
 /*
+ * kvfix_diff_restore_split -- kvfix_diff_restore from per-plane diffs (the lists
+ * kvfix_diff_encode_split writes): the restored K block of a sibling comes from
+ * (mask_k, offsets_k, payload_k), its V block from (mask_v, offsets_v, payload_v); a
+ * plane whose block is clean is read from the master.  entries_* are the payloads' sizes
+ * (an offset beyond them is not read and is flagged).  Re-alignment, slot mapping, pool
+ * layout, validation and errors as for kvfix_diff_restore; the output is the same bits
+ * as kvfix_diff_restore's on the joint lists of the same siblings.
+ */
+KVFIX_API kvfix_status kvfix_diff_restore_split(
+    const kvfix_bf16* master_k, const kvfix_bf16* master_v, kvfix_kv_desc master,
+    const uint32_t* mask_k, const uint32_t* mask_v, const int64_t* offsets_k,
+    const int64_t* offsets_v, const kvfix_bf16* payload_k, const kvfix_bf16* payload_v,
+    int64_t entries_k, int64_t entries_v, int32_t siblings, int32_t block_tokens,
+    const int32_t* delta, double rope_base, const int32_t* slot_mapping, kvfix_bf16* pool_k,
+    kvfix_bf16* pool_v, kvfix_kv_desc pool, void* stream);
+
+/*
  * kvfix_anchor_gate_correct -- kvfix_anchor_gate and kvfix_anchor_correct in one pass over
  * the sources: the gate's value-plane distances (prefix k) come from the same
  * reconstructions as the value plane's token weights, the gate is decided on the device,

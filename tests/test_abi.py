@@ -98,6 +98,15 @@ def test_host_validation_rejects_bad_arguments(lib):
                                 pool, None) == lib.EINVAL
     assert L.kvfix_diff_restore(fake, fake, dm, fake, fake, None, 0, 2, 16, fake, 1.0, fake, far, far_v,
                                 pool, None) == lib.EINVAL
+    # the per-plane restore wants both lists and a valid pool like the joint one
+    assert L.kvfix_diff_restore_split(fake, fake, dm, fake, None, fake, fake, None, None, 0, 0, 2, 16, fake, 1e4,
+                                      fake, far, far_v, pool, None) == lib.EINVAL
+    assert b"mask" in L.kvfix_last_error()
+    assert L.kvfix_diff_restore_split(fake, fake, dm, fake, fake, fake, fake, None, None, 0, 3, 2, 16, fake, 1e4,
+                                      fake, far, far_v, pool, None) == lib.EINVAL
+    assert b"payload" in L.kvfix_last_error()
+    assert L.kvfix_diff_restore_split(fake, fake, dm, fake, fake, fake, fake, None, None, 0, 0, 2, 16, fake, 1e4,
+                                      fake, far, far_v, _desc(lib, L=3, n=100), None) == lib.EINVAL
     # repair layouts: tokens beyond 16384, an unknown layout, a budget above 1, max_rows too small
     assert L.kvfix_repair_layout(fake, 1, 16385, 0, 64, 1, 5, 0.25, 1, fake, 4000, fake, None) == lib.EINVAL
     assert L.kvfix_repair_layout(fake, 1, 1000, 3, 64, 1, 5, 0.25, 1, fake, 1000, fake, None) == lib.EINVAL

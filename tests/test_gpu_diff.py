@@ -278,6 +278,37 @@ def test_split_diff_bit_exact(cfg):
     assert not torch.equal(kl[0], vl[0])
 
 
+@pytest.mark.parametrize("cfg", SMALL_DIFF, ids=lambda c: c.name)
+def test_split_restore_equals_joint_restore(cfg):
+    """The restore from per-plane lists writes the joint restore's words, also where the K
+    and V planes of a sibling are dirty in different blocks; V rows equal the oracle's."""
+    inp = synth.diff_inputs(cfg, DEV)
+    _planes_differ(inp, cfg, 8)
+    kl, vl, ent = _split_check(cfg, inp)
+    mask, offsets, payload, entries = kvfix().diff_encode(inp["master_k"], inp["master_v"], inp["sib_k"],
+                                                          inp["sib_v"], cfg.block_tokens)
+    tgt = synth.restore_inputs(cfg, DEV, skip=0.1, spare_pages=3)
+    shape = (cfg.layers, tgt["slots"], cfg.kv_heads, cfg.head_dim)
+    g = torch.Generator(device=DEV).manual_seed(cfg.seed + 9)
+    pool0 = torch.randn(shape, generator=g, device=DEV).to(torch.bfloat16)
+    jk, jv = pool0.clone(), pool0.clone()
+    kvfix().diff_restore(inp["master_k"], inp["master_v"], mask, offsets, payload, cfg.siblings,
+                         cfg.block_tokens, tgt["delta"], cfg.rope_base, tgt["slot_mapping"], jk, jv,
+                         payload_entries=entries)
+    sk, sv = pool0.clone(), pool0.clone()
+    kvfix().diff_restore_split(inp["master_k"], inp["master_v"], kl, vl, cfg.siblings, cfg.block_tokens,
+                               tgt["delta"], cfg.rope_base, tgt["slot_mapping"], sk, sv, entries=ent)
+    kvfix().check_status()
+    assert torch.equal(sk.view(torch.int16), jk.view(torch.int16))
+    assert torch.equal(sv.view(torch.int16), jv.view(torch.int16))
+    _, ov = oracle.diff_restore(synth.bits(inp["master_k"]), synth.bits(inp["master_v"]),
+                                mask.cpu().numpy().view(np.uint32), offsets.cpu().numpy(),
+                                synth.bits(payload[:max(entries, 1)]), cfg.siblings, cfg.block_tokens,
+                                tgt["delta"].cpu().numpy(), cfg.rope_base,
+                                tgt["slot_mapping"].cpu().numpy(), synth.bits(pool0), synth.bits(pool0))
+    assert np.array_equal(synth.bits(sv), ov)
+
+
 @pytest.mark.slow
 def test_full_size_split_diff():
     cfg = synth.SIBLINGS_8B
@@ -295,6 +326,19 @@ def test_full_size_split_diff():
     kvfix().check_status()
     assert torch.equal(ok.view(torch.int16), inp["sib_k"].view(torch.int16))
     assert torch.equal(ov.view(torch.int16), inp["sib_v"].view(torch.int16))
+    del ok, ov
+    tgt = synth.restore_inputs(cfg, DEV)
+    shape = (cfg.layers, tgt["slots"], cfg.kv_heads, cfg.head_dim)
+    jk = torch.zeros(shape, dtype=torch.bfloat16, device=DEV)
+    jv, sk, sv = torch.zeros_like(jk), torch.zeros_like(jk), torch.zeros_like(jk)
+    kvfix().diff_restore(inp["master_k"], inp["master_v"], mask, offsets, payload, cfg.siblings,
+                         cfg.block_tokens, tgt["delta"], cfg.rope_base, tgt["slot_mapping"], jk, jv,
+                         payload_entries=entries)
+    kvfix().diff_restore_split(inp["master_k"], inp["master_v"], kl, vl, cfg.siblings, cfg.block_tokens,
+                               tgt["delta"], cfg.rope_base, tgt["slot_mapping"], sk, sv, entries=ent)
+    kvfix().check_status()
+    assert torch.equal(sk.view(torch.int16), jk.view(torch.int16))
+    assert torch.equal(sv.view(torch.int16), jv.view(torch.int16))
 
 
 def test_master_select_matches_oracle():
