@@ -791,6 +791,7 @@ PROFILE_CASES = {
     "diff": lambda: synth.SIBLINGS_8B.with_(layers=4),
     "lowrank": lambda: synth.LOWRANK_70B.with_(chunks=1, layers=8),
     "anchor": lambda: synth.ANCHOR_8B.with_(layers=8),
+    "anchor_fused": lambda: synth.ANCHOR_8B.with_(layers=8),
     "diff_split": lambda: synth.SIBLINGS_8B.with_(layers=4),
     "layout": lambda: synth.LOWRANK_70B.with_(layers=8),
     "master": lambda: synth.ROUND_QWEN14B.with_(layers=8),
@@ -871,6 +872,12 @@ def run_profile_case(name: str, iters: int = 3):
         def step():
             _, _, _, acc = kvfix.anchor_gate(src["v"], inp["a_c_v"], inp["b_ct_v"], cfg.tokens, tau=cfg.tau)
             kvfix.anchor_correct(src["k"], src["v"], fac, inp["delta"], cfg.rope_base, accept=acc)
+    elif name == "anchor_fused":
+        inp = synth.anchor_inputs(cfg, "cuda")
+        src = compose_anchor_sources(cfg, inp)
+        fac = {k: inp[k] for k in ANCHOR_FACTORS}
+        def step():
+            kvfix.anchor_gate_correct(src["k"], src["v"], fac, cfg.tokens, inp["delta"], cfg.rope_base, tau=cfg.tau)
     else:
         inp = synth.lowrank_inputs(cfg, "cuda")
         kt = torch.empty_like(inp["x_k"])
