@@ -309,6 +309,41 @@ def test_split_restore_equals_joint_restore(cfg):
     assert np.array_equal(synth.bits(sv), ov)
 
 
+def test_split_restore_with_empty_lists_and_one_dirty_plane():
+    """Siblings equal to the master give two empty lists: every restored row is the master's
+    (keys re-aligned).  Then one value word changes in one sibling: only the value list
+    holds an entry, and the restore still equals the joint one."""
+    cfg = SMALL_DIFF[0]
+    inp = synth.diff_inputs(cfg, DEV)
+    S = cfg.siblings
+    sk = inp["master_k"].unsqueeze(0).repeat(S, 1, 1, 1, 1)
+    sv = inp["master_v"].unsqueeze(0).repeat(S, 1, 1, 1, 1)
+    tgt = synth.restore_inputs(cfg, DEV, skip=0.0, spare_pages=2)
+    shape = (cfg.layers, tgt["slots"], cfg.kv_heads, cfg.head_dim)
+    for step in range(2):
+        if step == 1:
+            sv[2, 1, 40, 0, 3] = sv[2, 1, 40, 0, 3] + 1.0
+        kl, vl, ent = kvfix().diff_encode_split(inp["master_k"], inp["master_v"], sk, sv, cfg.block_tokens)
+        mask, offsets, payload, entries = kvfix().diff_encode(inp["master_k"], inp["master_v"], sk, sv,
+                                                              cfg.block_tokens)
+        kvfix().check_status()
+        assert ent == ((0, 0) if step == 0 else (0, 1)) and entries == step
+        jk, jv = torch.zeros(shape, dtype=torch.bfloat16, device=DEV), torch.zeros(shape, dtype=torch.bfloat16, device=DEV)
+        pk, pv = torch.zeros_like(jk), torch.zeros_like(jv)
+        kvfix().diff_restore(inp["master_k"], inp["master_v"], mask, offsets, payload, S, cfg.block_tokens,
+                             tgt["delta"], cfg.rope_base, tgt["slot_mapping"], jk, jv, payload_entries=entries)
+        kvfix().diff_restore_split(inp["master_k"], inp["master_v"], kl, vl, S, cfg.block_tokens, tgt["delta"],
+                                   cfg.rope_base, tgt["slot_mapping"], pk, pv, entries=ent)
+        kvfix().check_status()
+        assert torch.equal(pk.view(torch.int16), jk.view(torch.int16))
+        assert torch.equal(pv.view(torch.int16), jv.view(torch.int16))
+        slot = tgt["slot_mapping"].long()
+        for s in range(S):
+            rk = kvfix().rerope(inp["master_k"].unsqueeze(0), tgt["delta"][s:s + 1], cfg.rope_base)
+            assert torch.equal(pk[:, slot[s]].view(torch.int16), rk[0].view(torch.int16))
+            assert torch.equal(pv[:, slot[s]].view(torch.int16), sv[s].view(torch.int16))
+
+
 @pytest.mark.slow
 def test_full_size_split_diff():
     cfg = synth.SIBLINGS_8B
