@@ -35,7 +35,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from cross_context_kv_gb300 import synth  # noqa: E402
+from cross_context_kv_gb300 import accounting, synth  # noqa: E402
 
 METRIC = "corrected KV GB/s & tokens/s on 1 GB300; fraction of HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
@@ -465,10 +465,13 @@ def stage_diff(kvfix, peak, steps=5, warmup=2):
     del kl, vl
     res_bytes = gat_bytes + cfg.siblings * (cfg.tokens + 1) * 4
     enc, gat, rst = statistics.mean(enc_ms), statistics.mean(gat_ms), statistics.mean(res_ms)
-    full = 2 * plane * cfg.siblings
-    stored = entries * blk + E // 8 + 8 * (E + 1)
+    compression = accounting.diff_compression(cfg.siblings, cfg.layers, cfg.tokens, cfg.kv_heads, cfg.head_dim,
+                                              cfg.block_tokens, int(entries))
+    copies = accounting.mirror_round_copies(cfg.siblings + 1, compression)
     res = {"workload": "siblings_8b: 16 siblings of a 32-layer 8192-token 8x128 cache, 16-token blocks",
-           "dirty_entries": int(entries), "compression_x": round(full / stored, 2),
+           "dirty_entries": int(entries), "compression_x": round(compression, 2),
+           "round_copies": round(copies, 3),
+           "memory_reduction_x": round((cfg.siblings + 1) / copies, 2),
            "encode": {"ms": round(enc, 4), "algorithmic_bytes": enc_bytes,
                       "GBps": round(enc_bytes / enc / 1e6, 1), "frac": round(enc_bytes / enc / 1e6 / peak, 4)},
            "gather": {"ms": round(gat, 4), "algorithmic_bytes": gat_bytes,
