@@ -93,9 +93,12 @@ struct AdCfg {
     static constexpr int kBBytes = kAdCols * kRowBytes;           // one anchor's Bt chunk
 };
 
-// grid = (tiles, L, planes * C).  For each 128-feature chunk the x tile is staged once;
-// the anchors' base rows of the chunk (M = 128 rows, N = 128 features, K = r) go through
-// four tensor-memory accumulators while the epilogue folds them against x, which each
+// Persistent: CTA i takes the units (128-row tile, layer, plane and segment) i, i + grid,
+// ...; the x, Bt and tensor-memory rings run on from one unit to the next, and a unit's A
+// tiles are loaded once the previous unit's MMAs have committed ("adone"), so the next
+// unit's loads overlap the previous one's epilogue.  Per unit, for each 128-feature chunk
+// the x tile is staged once; the anchors' base rows of the chunk (M = 128 rows, N = 128
+// features, K = r) go through four tensor-memory accumulators while the epilogue folds them against x, which each
 // thread holds in registers (its row, 64 of the chunk's features) for all anchors.
 // MODE kAdWeights: both planes (z = plane * C + c), every row; writes the softmax of
 // -mean|x - rec_v| / T per row.  MODE kAdGate: the value plane, rows < k; writes per-tile
@@ -111,28 +114,32 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
     using K = AdCfg<R>;
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t xfull[kAdMaxX], xempty[kAdMaxX], bfull[kAdMaxB], bempty[kAdMaxB], tfull[kAdSlots],
-        tempty[kAdSlots], afull;
+        tempty[kAdSlots], afull, adone;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ float red[kAnRows][kAnMaxAnchors + 1];
     __shared__ float gsum[4][kAnMaxAnchors];
     __shared__ float gsq[8][kAnMaxAnchors];  // both mode: per epilogue warp, per anchor
-    const int tile = blockIdx.x, l = blockIdx.y;
-    const int plane = MODE == kAdGate ? 0 : (int)blockIdx.z / args.C;
-    const int c = (int)blockIdx.z % args.C;
-    if (MODE != kAdGate && args.accept && args.accept[c] == 0) return;
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int V = args.V, NB = args.nb, NX = args.nx;
     unsigned char* asm_ = smem;                             // V A tiles
     unsigned char* xs = smem + V * K::kABytes;              // NX x chunks
     unsigned char* bs = xs + NX * kAdXBytes;                // Bt ring
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const CUtensorMap* mx = plane ? &tm_x1 : &tm_x0;
-    const CUtensorMap* ma = plane ? &tm_a1 : &tm_a0;
-    const CUtensorMap* mb = plane ? &tm_b1 : &tm_b0;
-    const int t0 = tile * kAnRows;
     const int chunks = args.F / kAdCols;
-    const int total = chunks * V;                           // (chunk, anchor) steps
+    const int total = chunks * V;                           // (chunk, anchor) steps of a tile
+    const int zdim = MODE == kAdGate ? args.C : 2 * args.C;
+    const int units = args.tiles * args.L * zdim;           // (tile, layer, plane and segment) units
+    // a unit is skipped (by every role alike) when its segment was rejected
+    auto unit_of = [&](int w, int& tile, int& l, int& plane, int& c) {
+        tile = w % args.tiles;
+        const int rest = w / args.tiles;
+        l = rest % args.L;
+        const int z = rest / args.L;
+        plane = MODE == kAdGate ? 0 : z / args.C;
+        c = z % args.C;
+        return !(MODE != kAdGate && args.accept && args.accept[c] == 0);
+    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NX; ++i) {
@@ -148,6 +155,7 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
             mbar_init(&tempty[a], 8);
         }
         mbar_init(&afull, 1);
+        mbar_init(&adone, 1);
         fence_mbar_init();
         abort_flag = 0;
     }
@@ -162,58 +170,106 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // lane 0 streams A and the x chunks, lane 1 the Bt ring (independent waits)
+        // lane 0 streams A and the x chunks, lane 1 the Bt ring (independent waits); the
+        // rings run on across the units of this CTA
         if (lane == 0) {
-            prefetch_tensormap(mx);
-            prefetch_tensormap(ma);
-            prefetch_tensormap(mb);
-            mbar_arrive_expect_tx(&afull, (unsigned)(V * K::kABytes));
-            for (int v = 0; v < V; ++v)
-                tma_load_2d(asm_ + v * K::kABytes, ma, 0, ((c * V + v) * args.L + l) * args.n + t0, &afull);
-            for (int j = 0; j < chunks && !anchor_vload(&abort_flag); ++j) {
-                const int xi = j % NX;
-                if (j >= NX && !mbar_wait(&xempty[xi], (unsigned)(j / NX - 1) & 1u)) {
+            prefetch_tensormap(&tm_x0);
+            prefetch_tensormap(&tm_x1);
+            prefetch_tensormap(&tm_a0);
+            prefetch_tensormap(&tm_a1);
+            prefetch_tensormap(&tm_b0);
+            prefetch_tensormap(&tm_b1);
+            int it = 0;
+            for (int w = blockIdx.x; w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
+                int tile, l, plane, c;
+                if (!unit_of(w, tile, l, plane, c)) continue;
+                const CUtensorMap* mx = plane ? &tm_x1 : &tm_x0;
+                const CUtensorMap* ma = plane ? &tm_a1 : &tm_a0;
+                const int t0 = tile * kAnRows;
+                // the previous unit's MMAs have read their A tiles
+                if (it > 0 && !mbar_wait(&adone, (unsigned)(it - 1) & 1u)) {
                     atomicOr(&abort_flag, 1);
                     break;
                 }
-                mbar_arrive_expect_tx(&xfull[xi], (unsigned)kAdXBytes);
-                for (int b = 0; b < 2; ++b)
-                    tma_load_4d(xs + xi * kAdXBytes + b * (kAnRows * 128), mx, j * kAdCols + 64 * b, t0, l, c,
-                                &xfull[xi]);
+                mbar_arrive_expect_tx(&afull, (unsigned)(V * K::kABytes));
+                for (int v = 0; v < V; ++v)
+                    tma_load_2d(asm_ + v * K::kABytes, ma, 0, ((c * V + v) * args.L + l) * args.n + t0, &afull);
+                bool ok = true;
+                for (int j = 0; j < chunks; ++j) {
+                    const int jg = it * chunks + j, xi = jg % NX;
+                    if (jg >= NX && !mbar_wait(&xempty[xi], (unsigned)(jg / NX - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&xfull[xi], (unsigned)kAdXBytes);
+                    for (int b = 0; b < 2; ++b)
+                        tma_load_4d(xs + xi * kAdXBytes + b * (kAnRows * 128), mx, j * kAdCols + 64 * b, t0, l, c,
+                                    &xfull[xi]);
+                }
+                if (!ok) {
+                    atomicOr(&abort_flag, 1);
+                    break;
+                }
+                ++it;
             }
         } else if (lane == 1) {
-            for (int q = 0; q < total && !anchor_vload(&abort_flag); ++q) {
-                const int j = q / V, v = q % V, e = q % NB;
-                if (q >= NB && !mbar_wait(&bempty[e], (unsigned)(q / NB - 1) & 1u)) {
+            int it = 0;
+            for (int w = blockIdx.x; w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
+                int tile, l, plane, c;
+                if (!unit_of(w, tile, l, plane, c)) continue;
+                const CUtensorMap* mb = plane ? &tm_b1 : &tm_b0;
+                bool ok = true;
+                for (int q = 0; q < total && !anchor_vload(&abort_flag); ++q) {
+                    const int qg = it * total + q;
+                    const int j = q / V, v = q % V, e = qg % NB;
+                    if (qg >= NB && !mbar_wait(&bempty[e], (unsigned)(qg / NB - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bfull[e], (unsigned)K::kBBytes);
+                    tma_load_2d(bs + e * K::kBBytes, mb, 0, ((c * V + v) * args.L + l) * args.F + j * kAdCols, &bfull[e]);
+                }
+                if (!ok) {
                     atomicOr(&abort_flag, 1);
                     break;
                 }
-                mbar_arrive_expect_tx(&bfull[e], (unsigned)K::kBBytes);
-                tma_load_2d(bs + e * K::kBBytes, mb, 0, ((c * V + v) * args.L + l) * args.F + j * kAdCols, &bfull[e]);
+                ++it;
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = tc_idesc_bf16(kAnRows, kAdCols);
-            bool ok = mbar_wait(&afull, 0u);
-            tc_fence_after();
-            for (int q = 0; ok && q < total && !anchor_vload(&abort_flag); ++q) {
-                const int v = q % V, e = q % NB, a = q % kAdSlots;
-                if ((q >= kAdSlots && !mbar_wait(&tempty[a], (unsigned)(q / kAdSlots - 1) & 1u)) ||
-                    !mbar_wait(&bfull[e], (unsigned)(q / NB) & 1u)) {
+            int it = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; ok && w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
+                int tile, l, plane, c;
+                if (!unit_of(w, tile, l, plane, c)) continue;
+                if (!mbar_wait(&afull, (unsigned)it & 1u)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                for (int q = 0; q < total && !anchor_vload(&abort_flag); ++q) {
+                    const int qg = it * total + q;
+                    const int v = q % V, e = qg % NB, a = qg % kAdSlots;
+                    if ((qg >= kAdSlots && !mbar_wait(&tempty[a], (unsigned)(qg / kAdSlots - 1) & 1u)) ||
+                        !mbar_wait(&bfull[e], (unsigned)(qg / NB) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < R / 16; ++kk) {
-                    const uint64_t adesc = tc_smem_desc(asm_ + v * K::kABytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
-                    const uint64_t bdesc = tc_smem_desc(bs + e * K::kBBytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
-                    tc_mma_bf16(tmem + a * kAdCols, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < R / 16; ++kk) {
+                        const uint64_t adesc = tc_smem_desc(asm_ + v * K::kABytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
+                        const uint64_t bdesc = tc_smem_desc(bs + e * K::kBBytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
+                        tc_mma_bf16(tmem + a * kAdCols, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(&bempty[e]);
+                    tc_commit(&tfull[a]);
                 }
-                tc_commit(&bempty[e]);
-                tc_commit(&tfull[a]);
+                tc_commit(&adone);  // this unit's MMAs are done with the A tiles
+                ++it;
             }
             if (!ok) atomicOr(&abort_flag, 1);
         }
@@ -223,150 +279,159 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
         const int wq = warp & 3;              // TMEM lane quarter this warp may read
         const int half = ew >> 2;             // which 64 of the chunk's 128 features
         const int m = 32 * wq + lane;         // tile row of this thread
-        const bool row_ok = t0 + m < args.rows;
-        float acc[kAnMaxAnchors];
-#pragma unroll
-        for (int v = 0; v < kAnMaxAnchors; ++v) acc[v] = 0.f;
-        const bool gate_too = MODE == kAdBoth && plane == 1;
-        const bool gate_row = t0 + m < args.gate_rows;
-        if (gate_too && lane < kAnMaxAnchors) gsq[ew][lane] = 0.f;
-        __syncwarp();
         bool ok = true;
-        for (int j = 0; ok && j < chunks; ++j) {
-            const int xi = j % NX;
-            if (anchor_vload(&abort_flag) || !mbar_wait(&xfull[xi], (unsigned)(j / NX) & 1u)) {
-                ok = false;
-                break;
-            }
-            // this row's 64 features of the chunk, as float pairs
-            float2 x2[32];
-            const unsigned char* xrow = xs + xi * kAdXBytes + half * (kAnRows * 128) + m * 128;
+        int it = 0;
+        for (int w = blockIdx.x; w < units; w += gridDim.x) {
+            int tile, l, plane, c;
+            if (!unit_of(w, tile, l, plane, c)) continue;
+            // the previous unit's reads of red, gsum and gsq are done; leave together on abort
+            if (bar_any<1, 256>(!ok || anchor_vload(&abort_flag))) break;
+            const int t0 = tile * kAnRows;
+            const bool row_ok = t0 + m < args.rows;
+            float acc[kAnMaxAnchors];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint4 u = *reinterpret_cast<const uint4*>(xrow + ((q ^ (m & 7)) << 4));
-                const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) x2[4 * q + e] = __bfloat1622float2(h2[e]);
-            }
+            for (int v = 0; v < kAnMaxAnchors; ++v) acc[v] = 0.f;
+            const bool gate_too = MODE == kAdBoth && plane == 1;
+            const bool gate_row = t0 + m < args.gate_rows;
+            if (gate_too && lane < kAnMaxAnchors) gsq[ew][lane] = 0.f;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&xempty[xi]);  // x is in registers now
-#pragma unroll
-            for (int v = 0; v < kAnMaxAnchors; ++v) {
-                if (v >= V) break;
-                const int q = j * V + v, a = q % kAdSlots;
-                if (!mbar_wait(&tfull[a], (unsigned)(q / kAdSlots) & 1u)) {
+            for (int j = 0; ok && j < chunks; ++j) {
+                const int jg = it * chunks + j, xi = jg % NX;
+                if (anchor_vload(&abort_flag) || !mbar_wait(&xfull[xi], (unsigned)(jg / NX) & 1u)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                uint32_t r0[32], r1[32];
-                const uint32_t tb = tmem + ((uint32_t)(32 * wq) << 16) + a * kAdCols + 64 * half;
-                tmem_ld32(tb, r0);
-                tmem_ld32(tb + 32, r1);
-                tmem_wait_ld();
-                tc_fence_before();
+                // this row's 64 features of the chunk, as float pairs
+                float2 x2[32];
+                const unsigned char* xrow = xs + xi * kAdXBytes + half * (kAnRows * 128) + m * 128;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(xrow + ((q ^ (m & 7)) << 4));
+                    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) x2[4 * q + e] = __bfloat1622float2(h2[e]);
+                }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[a]);
-                const float2 neg = make_float2(-1.f, -1.f);
-                if (MODE == kAdGate) {
-                    float2 s2 = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float2 d = __ffma2_rn(make_float2(__uint_as_float(r0[2 * e]), __uint_as_float(r0[2 * e + 1])),
-                                                    neg, x2[e]);
-                        s2 = __ffma2_rn(d, d, s2);
-                    }
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float2 d = __ffma2_rn(make_float2(__uint_as_float(r1[2 * e]), __uint_as_float(r1[2 * e + 1])),
-                                                    neg, x2[16 + e]);
-                        s2 = __ffma2_rn(d, d, s2);
-                    }
-                    acc[v] += s2.x + s2.y;
-                } else {
-                    float s0 = 0.f, s1 = 0.f;
-                    float2 q2 = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float2 d = __ffma2_rn(make_float2(__uint_as_float(r0[2 * e]), __uint_as_float(r0[2 * e + 1])),
-                                                    neg, x2[e]);
-                        s0 += fabsf(d.x) + fabsf(d.y);
-                        if (MODE == kAdBoth && gate_too) q2 = __ffma2_rn(d, d, q2);
-                    }
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float2 d = __ffma2_rn(make_float2(__uint_as_float(r1[2 * e]), __uint_as_float(r1[2 * e + 1])),
-                                                    neg, x2[16 + e]);
-                        s1 += fabsf(d.x) + fabsf(d.y);
-                        if (MODE == kAdBoth && gate_too) q2 = __ffma2_rn(d, d, q2);
-                    }
-                    acc[v] += s0 + s1;
-                    if (MODE == kAdBoth && gate_too) {
-                        float q = gate_row ? q2.x + q2.y : 0.f;
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
-                        if (lane == 0) gsq[ew][v] += q;
-                    }
-                }
-            }
-        }
-        if (!ok) atomicOr(&abort_flag, 1);
-        // both halves of a row: the second half adds its sums into the first's (the loops
-        // run to the fixed bound so that the sums stay in registers)
-        if (half == 1) {
-#pragma unroll
-            for (int v = 0; v < kAnMaxAnchors; ++v)
-                if (v < V) red[m][v] = acc[v];
-        }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        if (MODE == kAdBoth && gate_too && ew == 0 && lane < V && !anchor_vload(&abort_flag)) {
-            float x = 0.f;
-            for (int w = 0; w < 8; ++w) x += gsq[w][lane];
-            args.partial[(((long long)c * args.L + l) * args.tiles + tile) * V + lane] = x;
-        }
-        if (half == 0 && !anchor_vload(&abort_flag)) {
-#pragma unroll
-            for (int v = 0; v < kAnMaxAnchors; ++v)
-                if (v < V) acc[v] += red[m][v];
-            if (MODE != kAdGate) {
-                if (row_ok) {
-                    const float invF = 1.f / (float)args.F;
-                    float mmin = acc[0] * invF;
-#pragma unroll
-                    for (int v = 1; v < kAnMaxAnchors; ++v)
-                        if (v < V) mmin = fminf(mmin, acc[v] * invF);
-                    float z = 0.f;
-#pragma unroll
-                    for (int v = 0; v < kAnMaxAnchors; ++v)
-                        if (v < V) {
-                            acc[v] = expf(-(acc[v] * invF - mmin) * args.inv_T);
-                            z += acc[v];
-                        }
-                    const float iz = 1.f / z;
-                    float* wr = (plane ? args.w[1] : args.w[0]) + (((long long)c * args.L + l) * args.n + t0 + m) * V;
-#pragma unroll
-                    for (int v = 0; v < kAnMaxAnchors; ++v)
-                        if (v < V) wr[v] = acc[v] * iz;
-                }
-            } else {
-                // per-tile sums over the rows, in a fixed order: lanes, then the four warps
+                if (lane == 0) mbar_arrive(&xempty[xi]);  // x is in registers now
 #pragma unroll
                 for (int v = 0; v < kAnMaxAnchors; ++v) {
-                    if (v < V) {
-                        float x = row_ok ? acc[v] : 0.f;
+                    if (v >= V) break;
+                    const int qg = it * total + j * V + v, a = qg % kAdSlots;
+                    if (!mbar_wait(&tfull[a], (unsigned)(qg / kAdSlots) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t r0[32], r1[32];
+                    const uint32_t tb = tmem + ((uint32_t)(32 * wq) << 16) + a * kAdCols + 64 * half;
+                    tmem_ld32(tb, r0);
+                    tmem_ld32(tb + 32, r1);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[a]);
+                    const float2 neg = make_float2(-1.f, -1.f);
+                    if (MODE == kAdGate) {
+                        float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-                        if (lane == 0) gsum[wq][v] = x;
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(r0[2 * e]), __uint_as_float(r0[2 * e + 1])),
+                                                        neg, x2[e]);
+                            s2 = __ffma2_rn(d, d, s2);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(r1[2 * e]), __uint_as_float(r1[2 * e + 1])),
+                                                        neg, x2[16 + e]);
+                            s2 = __ffma2_rn(d, d, s2);
+                        }
+                        acc[v] += s2.x + s2.y;
+                    } else {
+                        float s0 = 0.f, s1 = 0.f;
+                        float2 q2 = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(r0[2 * e]), __uint_as_float(r0[2 * e + 1])),
+                                                        neg, x2[e]);
+                            s0 += fabsf(d.x) + fabsf(d.y);
+                            if (MODE == kAdBoth && gate_too) q2 = __ffma2_rn(d, d, q2);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(r1[2 * e]), __uint_as_float(r1[2 * e + 1])),
+                                                        neg, x2[16 + e]);
+                            s1 += fabsf(d.x) + fabsf(d.y);
+                            if (MODE == kAdBoth && gate_too) q2 = __ffma2_rn(d, d, q2);
+                        }
+                        acc[v] += s0 + s1;
+                        if (MODE == kAdBoth && gate_too) {
+                            float q = gate_row ? q2.x + q2.y : 0.f;
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+                            if (lane == 0) gsq[ew][v] += q;
+                        }
                     }
                 }
             }
-        }
-        if (MODE == kAdGate) {
+            if (!ok) atomicOr(&abort_flag, 1);
+            // both halves of a row: the second half adds its sums into the first's (the loops
+            // run to the fixed bound so that the sums stay in registers)
+            if (half == 1) {
+#pragma unroll
+                for (int v = 0; v < kAnMaxAnchors; ++v)
+                    if (v < V) red[m][v] = acc[v];
+            }
             asm volatile("bar.sync 1, 256;" ::: "memory");
-            if (ew == 0 && lane < V && !anchor_vload(&abort_flag)) {
-                const float x = ((gsum[0][lane] + gsum[1][lane]) + gsum[2][lane]) + gsum[3][lane];
+            if (MODE == kAdBoth && gate_too && ew == 0 && lane < V && !anchor_vload(&abort_flag)) {
+                float x = 0.f;
+                for (int w2 = 0; w2 < 8; ++w2) x += gsq[w2][lane];
                 args.partial[(((long long)c * args.L + l) * args.tiles + tile) * V + lane] = x;
             }
+            if (half == 0 && !anchor_vload(&abort_flag)) {
+#pragma unroll
+                for (int v = 0; v < kAnMaxAnchors; ++v)
+                    if (v < V) acc[v] += red[m][v];
+                if (MODE != kAdGate) {
+                    if (row_ok) {
+                        const float invF = 1.f / (float)args.F;
+                        float mmin = acc[0] * invF;
+#pragma unroll
+                        for (int v = 1; v < kAnMaxAnchors; ++v)
+                            if (v < V) mmin = fminf(mmin, acc[v] * invF);
+                        float z = 0.f;
+#pragma unroll
+                        for (int v = 0; v < kAnMaxAnchors; ++v)
+                            if (v < V) {
+                                acc[v] = expf(-(acc[v] * invF - mmin) * args.inv_T);
+                                z += acc[v];
+                            }
+                        const float iz = 1.f / z;
+                        float* wr = (plane ? args.w[1] : args.w[0]) + (((long long)c * args.L + l) * args.n + t0 + m) * V;
+#pragma unroll
+                        for (int v = 0; v < kAnMaxAnchors; ++v)
+                            if (v < V) wr[v] = acc[v] * iz;
+                    }
+                } else {
+                    // per-tile sums over the rows, in a fixed order: lanes, then the four warps
+#pragma unroll
+                    for (int v = 0; v < kAnMaxAnchors; ++v) {
+                        if (v < V) {
+                            float x = row_ok ? acc[v] : 0.f;
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                            if (lane == 0) gsum[wq][v] = x;
+                        }
+                    }
+                }
+            }
+            if (MODE == kAdGate) {
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                if (ew == 0 && lane < V && !anchor_vload(&abort_flag)) {
+                    const float x = ((gsum[0][lane] + gsum[1][lane]) + gsum[2][lane]) + gsum[3][lane];
+                    args.partial[(((long long)c * args.L + l) * args.tiles + tile) * V + lane] = x;
+                }
+            }
+            ++it;
         }
     }
     __syncthreads();
@@ -764,7 +829,13 @@ static cudaError_t launch_dist(const CUtensorMap* mx, const CUtensorMap* ma, con
     args.nx = sh.nx;
     cudaError_t e = cudaFuncSetAttribute(anchor_dist_kernel<R, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, sh.smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(args.tiles, args.L, planes * args.C);
+    // persistent: one CTA per SM (the shared-memory rings allow no second) walks the units
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const long long units = (long long)args.tiles * args.L * planes * args.C;
+    if (units == 0) return cudaSuccess;
+    dim3 grid((unsigned)(units < nsm ? units : (nsm > 0 ? nsm : 1)));
     anchor_dist_kernel<R, MODE><<<grid, kAdThreads, sh.smem, s>>>(mx[0], mx[1], ma[0], ma[1], mb[0], mb[1], args);
     return cudaGetLastError();
 }
