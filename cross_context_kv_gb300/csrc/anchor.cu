@@ -507,7 +507,10 @@ struct ApCfg {
     static constexpr int kBSlot = kBBytes < 1024 ? 1024 : kBBytes;
 };
 
-// grid = (tiles, L, 2 * C), z = plane * C + c (plane 0 keys, rotated; 1 values).
+// Persistent like the distance kernel: CTA i takes the units (tile, layer, plane and
+// segment) i, i + grid, ... (plane 0 keys, rotated; 1 values); the x slabs, Bt ring and
+// tensor-memory slots run on across units, and a unit's A tiles load once the previous
+// unit's MMAs have committed.
 template <int D, int R>
 __global__ void __launch_bounds__(kApThreads, 1)
 anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CUtensorMap tm_x1,
@@ -517,31 +520,37 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
                     ApArgs args, RopeTheta th) {
     using K = ApCfg<D, R>;
     extern __shared__ unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t afull, ascaled, xfull[kApMaxX], xempty[kApMaxX], bfull[kApMaxB], bempty[kApMaxB],
-        tfull[2], tempty[2];
+    __shared__ __align__(8) uint64_t afull, ascaled, adone, xfull[kApMaxX], xempty[kApMaxX], bfull[kApMaxB],
+        bempty[kApMaxB], tfull[2], tempty[2];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ float2 tab[D / 2];
-    const int tile = blockIdx.x, l = blockIdx.y;
-    const int plane = (int)blockIdx.z / args.C, c = (int)blockIdx.z % args.C;
-    if ((plane ? args.out[1] : args.out[0]) == nullptr) return;
-    if (args.accept && args.accept[c] == 0) return;  // rejected segment: left to a dense prefill
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int V = args.V, H = args.H, NB = args.nb, NX = args.nx;
     unsigned char* asm_ = smem;                                  // V scaled A tiles
     unsigned char* xs = asm_ + V * K::kABytes;                   // NX head slabs of x
     unsigned char* bs = xs + NX * K::kXBytes;                    // Bt ring
-    const CUtensorMap* mx = plane ? &tm_x1 : &tm_x0;
-    const CUtensorMap* mo = plane ? &tm_o1 : &tm_o0;
-    const CUtensorMap* ma = plane ? &tm_a1 : &tm_a0;
-    const CUtensorMap* mb = plane ? &tm_b1 : &tm_b0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t0 = tile * kAnRows;
     const int F = H * D;
+    const int tiles = (args.n + kAnRows - 1) / kAnRows;
+    const int units = tiles * args.L * 2 * args.C;
+    // unit w = ((plane * C + c) * L + l) * tiles + tile; missing planes and rejected segments
+    // are skipped by every role alike
+    auto unit_of = [&](int w, int& tile, int& l, int& plane, int& c) {
+        tile = w % tiles;
+        const int rest = w / tiles;
+        l = rest % args.L;
+        const int z = rest / args.L;
+        plane = z / args.C;
+        c = z % args.C;
+        if ((plane ? args.out[1] : args.out[0]) == nullptr) return false;
+        return !(args.accept && args.accept[c] == 0);  // rejected segment: left to a dense prefill
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(&afull, 1);
         mbar_init(&ascaled, 4);
+        mbar_init(&adone, 1);
         for (int i = 0; i < NX; ++i) {
             mbar_init(&xfull[i], 1);
             mbar_init(&xempty[i], 1);
@@ -568,64 +577,112 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // lane 0 streams A and the x slabs, lane 1 the Bt ring (independent waits)
+        // lane 0 streams A and the x slabs, lane 1 the Bt ring (independent waits); the
+        // rings run on across the units of this CTA
         if (lane == 0) {
-            prefetch_tensormap(mx);
-            prefetch_tensormap(mo);
-            prefetch_tensormap(ma);
-            prefetch_tensormap(mb);
-            mbar_arrive_expect_tx(&afull, (unsigned)(V * K::kABytes));
-            for (int v = 0; v < V; ++v)
-                tma_load_2d(asm_ + v * K::kABytes, ma, 0, ((c * V + v) * args.L + l) * args.n + t0, &afull);
-            for (int h = 0; h < H && !anchor_vload(&abort_flag); ++h) {
-                const int xi = h % NX;
-                if (h >= NX && !mbar_wait(&xempty[xi], (unsigned)(h / NX - 1) & 1u)) {
+            prefetch_tensormap(&tm_x0);
+            prefetch_tensormap(&tm_x1);
+            prefetch_tensormap(&tm_o0);
+            prefetch_tensormap(&tm_o1);
+            prefetch_tensormap(&tm_a0);
+            prefetch_tensormap(&tm_a1);
+            prefetch_tensormap(&tm_b0);
+            prefetch_tensormap(&tm_b1);
+            int it = 0;
+            for (int w = blockIdx.x; w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
+                int tile, l, plane, c;
+                if (!unit_of(w, tile, l, plane, c)) continue;
+                const CUtensorMap* mx = plane ? &tm_x1 : &tm_x0;
+                const CUtensorMap* ma = plane ? &tm_a1 : &tm_a0;
+                const int t0 = tile * kAnRows;
+                // the previous unit's MMAs have read its (scaled) A tiles
+                if (it > 0 && !mbar_wait(&adone, (unsigned)(it - 1) & 1u)) {
                     atomicOr(&abort_flag, 1);
                     break;
                 }
-                mbar_arrive_expect_tx(&xfull[xi], (unsigned)K::kXBytes);
-                for (int b = 0; b < D / 64; ++b)
-                    tma_load_4d(xs + xi * K::kXBytes + b * (kAnRows * 128), mx, h * D + 64 * b, t0, l, c, &xfull[xi]);
+                mbar_arrive_expect_tx(&afull, (unsigned)(V * K::kABytes));
+                for (int v = 0; v < V; ++v)
+                    tma_load_2d(asm_ + v * K::kABytes, ma, 0, ((c * V + v) * args.L + l) * args.n + t0, &afull);
+                bool ok = true;
+                for (int h = 0; h < H; ++h) {
+                    const int hg = it * H + h, xi = hg % NX;
+                    if (hg >= NX && !mbar_wait(&xempty[xi], (unsigned)(hg / NX - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&xfull[xi], (unsigned)K::kXBytes);
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_load_4d(xs + xi * K::kXBytes + b * (kAnRows * 128), mx, h * D + 64 * b, t0, l, c, &xfull[xi]);
+                }
+                if (!ok) {
+                    atomicOr(&abort_flag, 1);
+                    break;
+                }
+                ++it;
             }
         } else if (lane == 1) {
-            for (int q = 0; q < H * V && !anchor_vload(&abort_flag); ++q) {
-                const int h = q / V, v = q % V, e = q % NB;
-                if (q >= NB && !mbar_wait(&bempty[e], (unsigned)(q / NB - 1) & 1u)) {
+            int it = 0;
+            for (int w = blockIdx.x; w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
+                int tile, l, plane, c;
+                if (!unit_of(w, tile, l, plane, c)) continue;
+                const CUtensorMap* mb = plane ? &tm_b1 : &tm_b0;
+                bool ok = true;
+                for (int q = 0; q < H * V && !anchor_vload(&abort_flag); ++q) {
+                    const int qg = it * H * V + q;
+                    const int h = q / V, v = q % V, e = qg % NB;
+                    if (qg >= NB && !mbar_wait(&bempty[e], (unsigned)(qg / NB - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bfull[e], (unsigned)K::kBBytes);
+                    tma_load_2d(bs + e * K::kBSlot, mb, 0, ((c * V + v) * args.L + l) * F + h * D, &bfull[e]);
+                }
+                if (!ok) {
                     atomicOr(&abort_flag, 1);
                     break;
                 }
-                mbar_arrive_expect_tx(&bfull[e], (unsigned)K::kBBytes);
-                tma_load_2d(bs + e * K::kBSlot, mb, 0, ((c * V + v) * args.L + l) * F + h * D, &bfull[e]);
+                ++it;
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = tc_idesc_bf16(kAnRows, D);
-            bool ok = mbar_wait(&ascaled, 0u);
-            for (int h = 0; ok && h < H && !anchor_vload(&abort_flag); ++h) {
-                const int a = h & 1;
-                if (h >= 2 && !mbar_wait(&tempty[a], (unsigned)(h / 2 - 1) & 1u)) {
+            bool ok = true;
+            int it = 0;
+            for (int w = blockIdx.x; ok && w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
+                int tile, l, plane, c;
+                if (!unit_of(w, tile, l, plane, c)) continue;
+                if (!mbar_wait(&ascaled, (unsigned)it & 1u)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                for (int v = 0; v < V; ++v) {
-                    const int q = h * V + v, e = q % NB;
-                    if (!mbar_wait(&bfull[e], (unsigned)(q / NB) & 1u)) {
+                for (int h = 0; ok && h < H && !anchor_vload(&abort_flag); ++h) {
+                    const int hg = it * H + h, a = hg & 1;
+                    if (hg >= 2 && !mbar_wait(&tempty[a], (unsigned)(hg / 2 - 1) & 1u)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    for (int v = 0; v < V; ++v) {
+                        const int qg = hg * V + v, e = qg % NB;
+                        if (!mbar_wait(&bfull[e], (unsigned)(qg / NB) & 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < R / 16; ++kk) {
-                        const uint64_t adesc = tc_smem_desc(asm_ + v * K::kABytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
-                        const uint64_t bdesc = tc_smem_desc(bs + e * K::kBSlot + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
-                        tc_mma_bf16(tmem + a * D, adesc, bdesc, idesc, (v > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < R / 16; ++kk) {
+                            const uint64_t adesc = tc_smem_desc(asm_ + v * K::kABytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
+                            const uint64_t bdesc = tc_smem_desc(bs + e * K::kBSlot + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
+                            tc_mma_bf16(tmem + a * D, adesc, bdesc, idesc, (v > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc_commit(&bempty[e]);
                     }
-                    tc_commit(&bempty[e]);
+                    if (ok) tc_commit(&tfull[a]);
                 }
-                if (ok) tc_commit(&tfull[a]);
+                tc_commit(&adone);  // this unit's MMAs are done with its A tiles
+                ++it;
             }
             if (!ok) atomicOr(&abort_flag, 1);
         }
@@ -634,93 +691,105 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
         const int wq = warp & 3;
         const int m = 32 * wq + lane;        // tile row
         const int et = threadIdx.x - 64;     // 0..127
-        const bool row_ok = t0 + m < args.n;
-        if (plane == 0)
-            for (int i = et; i < D / 2; i += 128) {
-                float cs, sn;
-                rope_cos_sin(args.delta[c], th.theta[i], &cs, &sn);
-                tab[i] = make_float2(cs, sn);
-            }
-        // scale row m of every anchor's A tile by the token's weight (bf16, in place: the
-        // swizzle only permutes 16-byte pieces within the row)
-        bool ok = mbar_wait(&afull, 0u);
-        if (ok) {
-            const float* wr = (plane ? args.w[1] : args.w[0]) + (((long long)c * args.L + l) * args.n + (row_ok ? t0 + m : 0)) * V;
-            for (int v = 0; v < V; ++v) {
-                const float wv = row_ok ? wr[v] : 0.f;
-                uint4* p = reinterpret_cast<uint4*>(asm_ + v * K::kABytes + m * K::kRowBytes);
-#pragma unroll
-                for (int q = 0; q < K::kRowBytes / 16; ++q) {
-                    float f[8];
-                    unpack8(p[q], f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] *= wv;
-                    p[q] = pack8(f);
+        bool ok = true;
+        int it = 0;
+        for (int w = blockIdx.x; w < units; w += gridDim.x) {
+            int tile, l, plane, c;
+            if (!unit_of(w, tile, l, plane, c)) continue;
+            // the previous unit is done with the angle table; leave together on abort
+            if (bar_any<1, 128>(!ok || anchor_vload(&abort_flag))) break;
+            const CUtensorMap* mo = plane ? &tm_o1 : &tm_o0;
+            const int t0 = tile * kAnRows;
+            const bool row_ok = t0 + m < args.n;
+            if (plane == 0)
+                for (int i = et; i < D / 2; i += 128) {
+                    float cs, sn;
+                    rope_cos_sin(args.delta[c], th.theta[i], &cs, &sn);
+                    tab[i] = make_float2(cs, sn);
                 }
-            }
-        } else {
-            atomicOr(&abort_flag, 1);
-        }
-        fence_proxy_async_smem();  // generic writes of A -> read by the tensor core
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ascaled);
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // the angle table is complete
-        for (int h = 0; h < H; ++h) {
-            const int a = h & 1, xi = h % NX;
-            ok = ok && !anchor_vload(&abort_flag) && mbar_wait(&tfull[a], (unsigned)(h / 2) & 1u) &&
-                 mbar_wait(&xfull[xi], (unsigned)(h / NX) & 1u);
-            if (!ok) atomicOr(&abort_flag, 1);
-            tc_fence_after();
-            unsigned char* slab = xs + xi * K::kXBytes;
-            if (ok) {
-                const uint32_t tb = tmem + ((uint32_t)(32 * wq) << 16) + a * D;
+            // scale row m of every anchor's A tile by the token's weight (bf16, in place: the
+            // swizzle only permutes 16-byte pieces within the row)
+            if (mbar_wait(&afull, (unsigned)it & 1u)) {
+                const float* wr = (plane ? args.w[1] : args.w[0]) + (((long long)c * args.L + l) * args.n + (row_ok ? t0 + m : 0)) * V;
+                for (int v = 0; v < V; ++v) {
+                    const float wv = row_ok ? wr[v] : 0.f;
+                    uint4* p = reinterpret_cast<uint4*>(asm_ + v * K::kABytes + m * K::kRowBytes);
 #pragma unroll
-                for (int j = 0; j < D / 64; ++j) {
-                    // dims [32j, 32j + 32) and their partners [D/2 + 32j, D/2 + 32j + 32)
-                    uint32_t lo[32], hi[32];
-                    tmem_ld32(tb + 32 * j, lo);
-                    tmem_ld32(tb + D / 2 + 32 * j, hi);
-                    tmem_wait_ld();
+                    for (int q = 0; q < K::kRowBytes / 16; ++q) {
+                        float f[8];
+                        unpack8(p[q], f);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int f0 = 32 * j + 8 * q, f1 = D / 2 + f0;  // first dims of the two pieces
-                        uint4* p0 = reinterpret_cast<uint4*>(slab + (f0 / 64) * (kAnRows * 128) + m * 128 +
-                                                             ((((f0 % 64) / 8) ^ (m & 7)) << 4));
-                        uint4* p1 = reinterpret_cast<uint4*>(slab + (f1 / 64) * (kAnRows * 128) + m * 128 +
-                                                             ((((f1 % 64) / 8) ^ (m & 7)) << 4));
-                        float x0[8], x1[8];
-                        unpack8(*p0, x0);
-                        unpack8(*p1, x1);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            float y0 = x0[e], y1 = x1[e];
-                            if (plane == 0) {
-                                const float2 cs = tab[f0 + e];
-                                y0 = __fmaf_rn(x0[e], cs.x, __fmul_rn(x1[e], -cs.y));
-                                y1 = __fmaf_rn(x1[e], cs.x, __fmul_rn(x0[e], cs.y));
-                            }
-                            x0[e] = y0 + __uint_as_float(lo[8 * q + e]);
-                            x1[e] = y1 + __uint_as_float(hi[8 * q + e]);
-                        }
-                        *p0 = pack8(x0);
-                        *p1 = pack8(x1);
+                        for (int e = 0; e < 8; ++e) f[e] *= wv;
+                        p[q] = pack8(f);
                     }
                 }
+            } else {
+                ok = false;
+                atomicOr(&abort_flag, 1);
             }
-            tc_fence_before();
+            fence_proxy_async_smem();  // generic writes of A -> read by the tensor core
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[a]);
-            fence_proxy_async_smem();  // epilogue writes -> TMA store reads
-            if (bar_any<1, 128>(!ok || anchor_vload(&abort_flag))) ok = false;  // same verdict in all
-            if (et == 0) {
-                if (ok)
-                    for (int b = 0; b < D / 64; ++b)
-                        tma_store_4d(mo, slab + b * (kAnRows * 128), h * D + 64 * b, t0, l, c);
-                bulk_commit();
-                bulk_wait_read<1>();  // the previous head's store has read its slab
-                if (h >= 1) mbar_arrive(&xempty[(h - 1) % NX]);
+            if (lane == 0) mbar_arrive(&ascaled);
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // the angle table is complete
+            for (int h = 0; h < H; ++h) {
+                const int hg = it * H + h, a = hg & 1, xi = hg % NX;
+                ok = ok && !anchor_vload(&abort_flag) && mbar_wait(&tfull[a], (unsigned)(hg / 2) & 1u) &&
+                     mbar_wait(&xfull[xi], (unsigned)(hg / NX) & 1u);
+                if (!ok) atomicOr(&abort_flag, 1);
+                tc_fence_after();
+                unsigned char* slab = xs + xi * K::kXBytes;
+                if (ok) {
+                    const uint32_t tb = tmem + ((uint32_t)(32 * wq) << 16) + a * D;
+#pragma unroll
+                    for (int j = 0; j < D / 64; ++j) {
+                        // dims [32j, 32j + 32) and their partners [D/2 + 32j, D/2 + 32j + 32)
+                        uint32_t lo[32], hi[32];
+                        tmem_ld32(tb + 32 * j, lo);
+                        tmem_ld32(tb + D / 2 + 32 * j, hi);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int f0 = 32 * j + 8 * q, f1 = D / 2 + f0;  // first dims of the two pieces
+                            uint4* p0 = reinterpret_cast<uint4*>(slab + (f0 / 64) * (kAnRows * 128) + m * 128 +
+                                                                 ((((f0 % 64) / 8) ^ (m & 7)) << 4));
+                            uint4* p1 = reinterpret_cast<uint4*>(slab + (f1 / 64) * (kAnRows * 128) + m * 128 +
+                                                                 ((((f1 % 64) / 8) ^ (m & 7)) << 4));
+                            float x0[8], x1[8];
+                            unpack8(*p0, x0);
+                            unpack8(*p1, x1);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                float y0 = x0[e], y1 = x1[e];
+                                if (plane == 0) {
+                                    const float2 cs = tab[f0 + e];
+                                    y0 = __fmaf_rn(x0[e], cs.x, __fmul_rn(x1[e], -cs.y));
+                                    y1 = __fmaf_rn(x1[e], cs.x, __fmul_rn(x0[e], cs.y));
+                                }
+                                x0[e] = y0 + __uint_as_float(lo[8 * q + e]);
+                                x1[e] = y1 + __uint_as_float(hi[8 * q + e]);
+                            }
+                            *p0 = pack8(x0);
+                            *p1 = pack8(x1);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[a]);
+                fence_proxy_async_smem();  // epilogue writes -> TMA store reads
+                if (bar_any<1, 128>(!ok || anchor_vload(&abort_flag))) ok = false;  // same verdict in all
+                if (et == 0) {
+                    if (ok)
+                        for (int b = 0; b < D / 64; ++b)
+                            tma_store_4d(mo, slab + b * (kAnRows * 128), h * D + 64 * b, t0, l, c);
+                    bulk_commit();
+                    bulk_wait_read<1>();  // the previous head's store has read its slab
+                    if (hg >= 1) mbar_arrive(&xempty[(hg - 1) % NX]);
+                }
+                if (!ok) break;
             }
             if (!ok) break;
+            ++it;
         }
         if (et == 0) bulk_wait<0>();
     }
@@ -903,7 +972,15 @@ static cudaError_t launch_apply(const uint16_t* const* x, const Plane& p, uint16
     }
     e = cudaFuncSetAttribute(anchor_apply_kernel<D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, sh.smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((p.tokens + kAnRows - 1) / kAnRows, p.layers, 2 * p.chunks);
+    int dev = 0, nsm = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, anchor_apply_kernel<D, R>, kApThreads, sh.smem)) != cudaSuccess)
+        return e;
+    const long long units = (long long)((args.n + kAnRows - 1) / kAnRows) * args.L * 2 * args.C;
+    if (units == 0) return cudaSuccess;
+    const long long slots = (long long)(nsm > 0 ? nsm : 1) * (per_sm > 0 ? per_sm : 1);
+    dim3 grid((unsigned)(units < slots ? units : slots));
     anchor_apply_kernel<D, R><<<grid, kApThreads, sh.smem, s>>>(mx[0], mx[1], mo[0], mo[1], ma[0], ma[1], mb[0],
                                                                  mb[1], args, th);
     return cudaGetLastError();
