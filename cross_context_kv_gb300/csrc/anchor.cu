@@ -12,15 +12,17 @@
 // stored transposed, Bt [segment][anchor][layer][feature][r] (feature = head*D + dim),
 // so that both MMA operands are K-major with K = r.
 //
-// Blackwell path, three kernels:
-//   anchor_dist_kernel   per (128-row tile, layer, plane and segment): the anchors' base
+// Blackwell path, three kernels; the two big ones are persistent (one CTA per SM slot
+// walks the (128-row tile, layer, plane and segment) units, its rings running on from
+// one unit to the next):
+//   anchor_dist_kernel   per unit: the anchors' base
 //                        rows A_v B_v are built 128 features at a time by tcgen05.mma
 //                        (M = 128 rows, N = 128, K = r) into four tensor-memory buffers,
 //                        while eight epilogue warps fold |x - rec| (token weights) or
 //                        (x - rec)^2 (gate) into per-row, per-anchor sums; x chunks and Bt
 //                        stream through TMA rings fed by two producer lanes.
 //   anchor_gate_kernel   per segment: the gate's distances, softmax, normalised entropy.
-//   anchor_apply_kernel  per (tile, layer, plane and segment): the anchors' delta factors
+//   anchor_apply_kernel  per unit: the anchors' delta factors
 //                        are scaled by the token weights in shared memory and multiplied by
 //                        the stacked Bt (K = V*r) head by head into tensor memory; the
 //                        epilogue adds the aligned source (keys rotated) and stores by TMA.
