@@ -127,3 +127,68 @@ def test_host_validation_rejects_bad_arguments(lib):
 
 def test_version(lib):
     assert lib.version() == 100
+
+
+def test_anchor_and_mean_correct_validation(lib):
+    """The anchor and probe-mean calls reject bad arguments on the host, before any
+    device work (no GPU needed: every case fails a check)."""
+    L = lib.lib
+    fake = ctypes.c_void_p(1 << 20)
+    fake2 = ctypes.c_void_p(1 << 23)
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    far, far_v = ctypes.c_void_p(1 << 30), ctypes.c_void_p((1 << 30) + (1 << 26))
+    src = _desc(lib, C=2, L=2, n=256, H=8, D=128)
+    f8 = [fake] * 8
+
+    def correct(**kw):
+        a = dict(k_src=fake, v_src=fake2, src=src, f=f8, anchors=10, rank=32, T=1.0, delta=fake, base=1e4,
+                 accept=None, w_k=fake, w_v=fake2, k_out=far, v_out=far_v, out=src)
+        a.update(kw)
+        return L.kvfix_anchor_correct(a["k_src"], a["v_src"], a["src"], *a["f"], a["anchors"], a["rank"], a["T"],
+                                      a["delta"], a["base"], a["accept"], a["w_k"], a["w_v"], a["k_out"],
+                                      a["v_out"], a["out"], None)
+
+    assert correct(rank=24) == lib.EINVAL and b"rank" in L.kvfix_last_error()
+    assert correct(anchors=0) == lib.EINVAL and correct(anchors=17) == lib.EINVAL
+    hd96 = _desc(lib, C=2, L=2, n=256, H=4, D=96)
+    assert correct(src=hd96, out=hd96) == lib.EINVAL and b"head_dim" in L.kvfix_last_error()
+    narrow = _desc(lib, C=2, L=2, n=256, H=1, D=64)   # a row of 64 features: not a whole chunk
+    assert correct(src=narrow, out=narrow) == lib.EINVAL and b"multiple of 128" in L.kvfix_last_error()
+    assert correct(base=1.0) == lib.EINVAL
+    assert correct(T=0.0) == lib.EINVAL
+    assert correct(w_k=None) == lib.EINVAL and b"required" in L.kvfix_last_error()
+    assert correct(f=[fake] * 7 + [odd]) == lib.EINVAL and b"b_dt_v" in L.kvfix_last_error()
+    # exactly in place is allowed; an output straddling the other plane's source is not
+    assert correct(k_out=fake, v_out=ctypes.c_void_p((1 << 20) + 4096)) == lib.EINVAL
+    assert b"overlap" in L.kvfix_last_error()
+
+    need = L.kvfix_anchor_gate_workspace_bytes(src, 10, 256)
+    assert need > 0 and L.kvfix_anchor_gate_workspace_bytes(src, 10, 128) <= need
+    assert L.kvfix_anchor_gate_workspace_bytes(src, 0, 256) == 0
+
+    def gate(**kw):
+        a = dict(src=src, anchors=10, rank=32, prefix=256, T=1.0, tau=0.5, ws=far, ws_bytes=need)
+        a.update(kw)
+        return L.kvfix_anchor_gate(fake, a["src"], fake, fake, a["anchors"], a["rank"], a["prefix"], a["T"], a["tau"],
+                                   fake, fake, fake, fake, a["ws"], a["ws_bytes"], None)
+
+    assert gate(prefix=0) == lib.EINVAL and gate(prefix=257) == lib.EINVAL
+    assert gate(tau=float("nan")) == lib.EINVAL
+    assert gate(ws=None) == lib.EINVAL and b"workspace" in L.kvfix_last_error()
+    assert gate(ws_bytes=need - 1) == lib.EINVAL
+    assert gate(ws=ctypes.c_void_p((1 << 30) + 4)) == lib.EINVAL and b"aligned" in L.kvfix_last_error()
+
+    # the one-pass call checks the gate's arguments too
+    assert L.kvfix_anchor_gate_correct(fake, fake2, src, *f8, 10, 32, 256, 1.0, 0.5, fake, 1e4, fake, fake, fake,
+                                       fake, fake, fake2, far, far_v, src, far, 0, None) == lib.EINVAL
+    assert b"workspace" in L.kvfix_last_error()
+
+    # probe-mean correction: b beyond the tokens, no agents, a plane without weights
+    r = _desc(lib, C=1, L=2, n=64, H=2, D=64)
+    args = [fake, fake2, r, far, far_v, r, ctypes.c_void_p(1 << 31), ctypes.c_void_p((1 << 31) + (1 << 26)), r]
+    assert L.kvfix_mean_correct(*args, 1, fake, 1e4, fake, fake, 65, fake, fake, fake, fake, None) == lib.EINVAL
+    assert L.kvfix_mean_correct(*args, 0, fake, 1e4, fake, fake, 8, fake, fake, fake, fake, None) == lib.EINVAL
+    assert L.kvfix_mean_correct(*args, 1, fake, 1e4, fake, fake, 8, None, fake, fake, fake, None) == lib.EINVAL
+    assert b"needs w" in L.kvfix_last_error()
+    # the bounded-wait self test: a limit outside [1, 4e9]
+    assert L.kvfix_selftest_wait(0, None, None) == lib.EINVAL
