@@ -673,6 +673,31 @@ def test_anchor_correct_is_weighted_sum_of_anchor_deltas():
     np.testing.assert_allclose(oracle.bf16_decode(out), ref, rtol=2.0 ** -8, atol=1e-6)
 
 
+def test_anchor_order_does_not_matter():
+    """Relabelling the anchors permutes d, g and the weights the same way and leaves the
+    entropy, the verdict and (up to the order of a double sum) the correction unchanged:
+    catches an anchor index crossed between A and B or between weights and deltas."""
+    rng = np.random.default_rng(46)
+    C, V, L, n, H, D, r = 2, 5, 2, 6, 2, 16, 4
+    x, a, b = _anchor_case(rng, C=C, V=V, L=L, n=n, F=H * D, r=r, a_std=0.3)
+    ad = _bf16_bits(0.2 * rng.standard_normal((C, V, L, n, r)))
+    bd = _bf16_bits(rng.standard_normal((C, V, L, H * D, r)))
+    perm = np.array([3, 0, 4, 1, 2])
+    d, g, hbar, acc = oracle.anchor_gate(x, a, b, 4, tau=0.7)
+    dp, gp, hp, ap = oracle.anchor_gate(x, a[:, perm], b[:, perm], 4, tau=0.7)
+    np.testing.assert_array_equal(dp, d[:, perm])
+    np.testing.assert_allclose(gp, g[:, perm], rtol=1e-14)
+    np.testing.assert_allclose(hp, hbar, rtol=1e-13)
+    assert np.array_equal(ap, acc)
+    w = oracle.anchor_weights(x, a, b)
+    wp = oracle.anchor_weights(x, a[:, perm], b[:, perm])
+    np.testing.assert_allclose(wp, w[..., perm], rtol=1e-14)
+    out = oracle.anchor_correct(x, ad, bd, w, H, [9, 400], 1e4, rotate=True)
+    outp = oracle.anchor_correct(x, ad[:, perm], bd[:, perm], wp, H, [9, 400], 1e4, rotate=True)
+    assert np.mean(out == outp) > 0.999
+    np.testing.assert_allclose(oracle.bf16_decode(outp), oracle.bf16_decode(out), rtol=2.0 ** -8, atol=1e-6)
+
+
 # ------------------------------------------------------------ repair layouts
 
 def test_chunk_budgets_reproduce_table8():
