@@ -636,10 +636,7 @@ def run_ours(args, world, rank, local):
         "step_ms_spread": [round(min(step_ms), 5), round(statistics.median(step_ms), 5), round(max(step_ms), 5)],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded draws: reuse ~ N(0,1); fresh = rerope(reuse) + mu + xi)",
-        "config": {"workload": "repair_llama8b: one 4096-token chunk, 32 layers, 8 KV heads x 128, bf16, "
-                               "r=0.15 (b=615), check layer 1, RoPE base 5e5, re-rope by U[500,8000]",
-                   "chunks_per_gpu": 1, "global_chunks": world, "parallelism": f"replicas x{world} (weak)",
-                   "l2": "flushed between timed steps (512 MiB write); working set 1.6 GB > L2"},
+        "config": repair_config(world),
         "tokens_per_s": round(world * by["tokens"] / ms * 1e3, 1),
         "algorithmic_bytes_per_step": by["step"],
         "roofline": {"bound": "hbm", "kernel": "mean_correct_kernel (kvfix_mean_correct: probe means + correction, K and V, one launch)",
@@ -672,6 +669,14 @@ def run_ours(args, world, rank, local):
     return line
 
 
+def repair_config(world: int) -> dict:
+    """The workload both arms report (the reference arm times a bounded sample of it)."""
+    return {"workload": "repair_llama8b: one 4096-token chunk, 32 layers, 8 KV heads x 128, bf16, "
+                        "r=0.15 (b=615), check layer 1, RoPE base 5e5, re-rope by U[500,8000]",
+            "chunks_per_gpu": 1, "global_chunks": world, "parallelism": f"replicas x{world} (weak)",
+            "l2": "flushed between timed steps (512 MiB write); working set 1.6 GB > L2"}
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return None
@@ -691,7 +696,7 @@ def run_reference(args, world, rank):
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": f"repair_llama8b sample: layers 0..{layers - 1} of one chunk"},
+            "data": "synthetic", "config": repair_config(world),
             "tokens_per_s": round(by["tokens"] / sec, 2),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cb["cores"], "kind": "oracle",
                              "sample": cb["sample"]},
