@@ -108,6 +108,7 @@ kvfix_status kvfix_check_status(void* stream) {
                     read_status_anchor(s) | read_status_layout(s) | read_status_selftest(s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kvfix_check_status: status read");
+    if (bits & 8u) return fail(KVFIX_EDEVICE, "a kernel's shared-memory layout check failed; its work was skipped");
     if (bits & 4u) return fail(KVFIX_ETIMEOUT, "a bounded device wait gave up");
     if (bits & 2u) return fail(KVFIX_ENOSPACE, "diff payload entries beyond the capacity were skipped");
     if (bits & 1u) return fail(KVFIX_EDEVICE, "an index in caller data was out of range and skipped");
@@ -227,6 +228,10 @@ kvfix_status kvfix_mean_correct(const kvfix_bf16* k_reuse, const kvfix_bf16* v_r
         const size_t mu_bytes = sizeof(float) * (size_t)units * reuse.layers * reuse.kv_heads * reuse.head_dim;
         if (overlaps_bytes(p.mu, mu_bytes, p.w, sizeof(float) * (size_t)units * reuse.tokens))
             return fail(KVFIX_EINVAL, "%s: %s mu overlaps w", fn, p.name);
+        uintptr_t o0, o1;
+        extent(p.out, out, &o0, &o1);
+        if (overlaps_bytes(p.mu, mu_bytes, (const void*)o0, o1 - o0))
+            return fail(KVFIX_EINVAL, "%s: %s mu overlaps out", fn, p.name);
     }
     if (!active) return fail(KVFIX_EINVAL, "%s: no plane given", fn);
     cudaStream_t s = (cudaStream_t)stream;

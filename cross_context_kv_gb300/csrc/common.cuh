@@ -17,6 +17,7 @@ enum : unsigned {
     FLAG_BOUNDS = 1u,   // an index in caller data was out of range and skipped
     FLAG_NOSPACE = 2u,  // a payload entry beyond the capacity was skipped
     FLAG_TIMEOUT = 4u,  // a bounded wait gave up
+    FLAG_INTERNAL = 8u, // a kernel's own layout check failed; it skipped its work
 };
 
 // ------------------------------------------------------------- addressing

@@ -218,23 +218,6 @@ lowrank_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constan
     if (warp == 1) tmem_dealloc(tmem, C::kCols);
 }
 
-// Strides (bytes) of a plane view for a 4-D tensor map (dims: row elements, tokens,
-// layers, chunks); the stride of a dimension of size 1 is irrelevant and is replaced
-// by a consistent one.
-static void plane_map_strides(const Plane& p, cuuint64_t* dims, cuuint64_t* strides) {
-    const long long row = (long long)p.heads * p.dim;
-    dims[0] = (cuuint64_t)row;
-    dims[1] = (cuuint64_t)p.tokens;
-    dims[2] = (cuuint64_t)p.layers;
-    dims[3] = (cuuint64_t)p.chunks;
-    long long st = p.tokens > 1 ? p.st : row;
-    long long sl = p.layers > 1 ? p.sl : st * p.tokens;
-    long long sc = p.chunks > 1 ? p.sc : sl * p.layers;
-    strides[0] = (cuuint64_t)(2 * st);
-    strides[1] = (cuuint64_t)(2 * sl);
-    strides[2] = (cuuint64_t)(2 * sc);
-}
-
 static cudaError_t encode_plane(CUtensorMap* map, const void* base, const Plane& p) {
     auto enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;

@@ -12,10 +12,11 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
-#include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace kvfix {
 
@@ -491,40 +492,43 @@ cudaError_t launch_select_f32(const float* d_k, const float* d_v, int units, int
 }
 
 // =====================================================================================
-// Probe-mean correction, one launch for both planes.  One thread-block cluster of 8
-// CTAs per (reused chunk, layer, plane):
-//   phase 1, per agent: the 32 slot sums P_s (s = probe index mod 32, each summed in
-//     probe-list order) are spread over the cluster, 4 per CTA; the fresh probe rows are
-//     copied to the output on the way.  The rotation is linear, so a slot sums fresh and
-//     reused rows separately and rotates the reused sum once: P_s = sum(fresh) -
-//     rot(sum(reuse)).  Cluster barrier; CTA k reads, for the row elements e with
-//     e % 4 == k % 4 in its half, the 32 partials through distributed shared memory,
-//     adds the group sums Q_g = ((P_4g + P_4g+1) + P_4g+2) + P_4g+3 in order g = 0..7
-//     and divides by b.  Cluster barrier; every CTA gathers
-//     the full mean.  Cluster barrier (the buffers are reused by the next agent).
-//   phase 2: CTA k streams 1/8 of the layer's rows through a 3-stage ring of 16 KB
-//     shared-memory tiles filled by bulk asynchronous copies (TMA, completion counted
-//     in bytes on a "full" mbarrier, release by every warp on an "empty" mbarrier).
-//     The first tiles are requested at kernel start, so they arrive during phase 1.
+// Probe-mean correction: two kernels chained by programmatic dependent launch.  Both
+// work on column slices of the token row: `cw` consecutive row elements made of whole
+// heads (128 elements unless a head is wider), so an 8 x 128 row has eight slices.
+//   probe_mean_kernel: one CTA per (unit, layer, plane, slice).  Thread (s, quad pair)
+//     sums the probes i = s, s + 32, ... of slot s in probe-list order, the loads of
+//     four rows in flight at a time; fresh and reused rows are summed separately and
+//     the reused sum is rotated once, P_s = sum(fresh) - rot(sum(reuse)) (the rotation
+//     is linear).  The fresh probe rows are copied to the output on the way.  The CTA
+//     then adds the group sums Q_g = ((P_4g + P_4g+1) + P_4g+2) + P_4g+3 in order
+//     g = 0..7 and divides by b: the mean, written to the mean output.
+//   mean_stream_kernel: one CTA per (row block, layer, plane, slice, reused chunk,
+//     agent group) streams the block's reused rows through a 3-stage ring of 16 KB
+//     shared-memory tiles, each one TMA tensor copy of (cw columns x TR rows) completed
+//     in bytes on a "full" mbarrier and released by every warp on an "empty" mbarrier.
 //     Each reused row is read once and the corrected row of every agent of the group is
-//     written from it; probe rows are skipped (phase 1 wrote them).
+//     written from it; probe rows are skipped (the mean kernel wrote them).  The
+//     barriers, the rotation table and the first tiles are set up before the wait on
+//     the mean kernel.
 // Work unit of a thread: a "quad pair" -- dims [4v, 4v+4) of one head and their rotation
-// partners [D/2+4v, D/2+4v+4).  A thread keeps the same quad pair through phase 2, so
-// its cos/sin and mean values stay in registers.  Shared-memory vectors read 4 at a
-// time are stored by residue: element e sits at (e % 4) * (HD / 4) + e / 4.
-// The summation order (slots, then groups of four, then the eight groups) is fixed, and
-// the multi-agent kernels below follow it too: one call for N agents is bit-identical
-// to N calls.
+// partners [D/2+4v, D/2+4v+4) -- so the rotation never leaves the thread.  The summation
+// order is fixed per element and shared with the multi-agent kernels below: one call
+// for N agents is bit-identical to N calls, whatever the slicing.
 // =====================================================================================
-namespace cg = cooperative_groups;
+constexpr int kGroups = 8;         // the 32 probe slots fold in 8 groups of 4
+constexpr int kSlotsPerGroup = 4;
+constexpr int kSlots = kGroups * kSlotsPerGroup;
+constexpr int kMcSliceCols = 128;  // width of a column slice in elements (whole heads)
+constexpr int kPmBatch = 2;        // probe rows of a slot whose loads are in flight together
+constexpr int kMsThreads = 256;
+constexpr int kMsWarps = kMsThreads / 32;
+constexpr int kMsStages = 3;
+constexpr int kMsTileBytes = 16384;
+constexpr int kMsRows = 512;       // rows per CTA of the stream kernel
 
-constexpr int kMcCluster = 8;
-constexpr int kMcThreads = 256;
-constexpr int kMcWarps = kMcThreads / 32;
-constexpr int kMcSlotsPerCta = 32 / kMcCluster;
-constexpr int kMcLanesPerSlot = kMcThreads / kMcSlotsPerCta;  // 64
-constexpr int kMcStages = 3;
-constexpr int kMcTileBytes = 16384;
+struct McMaps {  // TMA maps of the two reused planes (dims: row elements, tokens, layers, chunks)
+    CUtensorMap reuse[2];
+};
 
 struct McArgs {
     const uint16_t* reuse[2];
@@ -534,353 +538,349 @@ struct McArgs {
     const float* w[2];
     float* mu[2];
     Plane rp, fp, op;
-    int agents, b, rows_per_cta, tile_rows;
+    int agents, b, rows_per_cta, tile_rows, cw, slices;
     const int32_t* delta;
     RopeTheta th;
 };
 
-struct McLayout {  // byte offsets into the dynamic shared memory
-    int ps, slice, ring, mu_all, cs, member, wts, total, words_member;
-    int ps_alias;  // the phase-1 partials share the last ring stage
-};
-
-__host__ __device__ inline int align128(int x) { return (x + 127) / 128 * 128; }
-__host__ __device__ inline bool mc_stage_weights(int ag, int rows_per_cta) { return ag * rows_per_cta <= 2048; }
-
-__host__ __device__ inline McLayout mc_layout(int HD, int half, int ag, int rows_per_cta, int tile_rows) {
-    McLayout m;
-    // The partial sums of phase 1 are dead during phase 2: when they fit in one ring
-    // stage they live in the last one, which takes tiles only after phase 1.
-    const int stage = tile_rows * HD * 2, ps_bytes = 4 * kMcSlotsPerCta * HD;
-    m.ring = 0;
-    m.ps_alias = ps_bytes <= stage;
-    m.ps = m.ps_alias ? m.ring + (kMcStages - 1) * stage : m.ring + kMcStages * stage;
-    m.slice = align128(m.ps_alias ? m.ring + kMcStages * stage : m.ps + ps_bytes);
-    m.mu_all = align128(m.slice + 4 * (HD / kMcCluster));
-    m.cs = m.mu_all + 4 * ag * HD;
-    m.member = m.cs + 4 * 2 * ag * half;
-    m.words_member = (rows_per_cta + 31) / 32;
-    m.wts = m.member + 4 * ag * m.words_member;
-    // weights of this CTA's rows, per agent, when they fit in 8 KB
-    m.total = m.wts + (mc_stage_weights(ag, rows_per_cta) ? 4 * ag * rows_per_cta : 0);
-    return m;
-}
-
-__global__ void __cluster_dims__(kMcCluster, 1, 1) __launch_bounds__(kMcThreads, 4)
-mean_correct_kernel(McArgs args) {
+__global__ void __launch_bounds__(1024, 1) probe_mean_kernel(McArgs args) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(8) uint64_t full[kMcStages];
-    __shared__ __align__(8) uint64_t empty[kMcStages];
-    __shared__ int rot_on[kAgentGroup];
-    __shared__ int abort_flag;
-    cg::cluster_group cluster = cg::this_cluster();
-    const int rank = (int)cluster.block_rank();
-    const int plane = blockIdx.y & 1, l = blockIdx.y >> 1, r = blockIdx.z;
+    __shared__ float2 tab[kMaxHeadDim / 2];
+    const int slice = blockIdx.x, plane = blockIdx.y & 1, l = blockIdx.y >> 1, u = blockIdx.z;
     const uint16_t* reuse = args.reuse[plane];
-    if (reuse == nullptr) return;  // plane not requested: the whole cluster leaves
+    if (reuse == nullptr) return;
     const uint16_t* fresh = args.fresh[plane];
     uint16_t* out = args.out[plane];
-    const int32_t* idx = args.idx[plane];
-    const float* wgt = args.w[plane];
-    float* mu = args.mu[plane];
     const Plane& rp = args.rp;
     const Plane& fp = args.fp;
     const Plane& op = args.op;
-    const int R = rp.chunks, n = rp.tokens, L = rp.layers;
-    const int D = rp.dim, half = D / 2, v8 = D / 8;       // quads per half-head
-    const int HD = rp.heads * D, P = rp.heads * v8, G = HD / 4;
-    const int SL = HD / kMcCluster;                       // mean elements reduced per CTA
+    const int R = rp.chunks, r = u % R, n = rp.tokens, L = rp.layers;
+    const int D = rp.dim, half = D / 2, v8 = D / 8;
+    const int HD = rp.heads * D, CW = args.cw, c0 = slice * CW, P = CW / 8;
     const int b = args.b;
-    const bool keys = plane == 0;
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int t_lo = min(n, rank * args.rows_per_cta), t_hi = min(n, t_lo + args.rows_per_cta);
-    const int TR = args.tile_rows;
-    const int ag_max = min(args.agents, kAgentGroup);
-    const McLayout lay = mc_layout(HD, half, ag_max, args.rows_per_cta, TR);
-    float* ps = reinterpret_cast<float*>(smem + lay.ps);                // [4 slots][HD] by residue
-    float* mu_slice = reinterpret_cast<float*>(smem + lay.slice);      // [SL]
-    uint16_t* ring = reinterpret_cast<uint16_t*>(smem + lay.ring);
-    float* mu_all = reinterpret_cast<float*>(smem + lay.mu_all);      // [ag][HD] by residue
-    float* cos_t = reinterpret_cast<float*>(smem + lay.cs);           // [ag][4][D/8]
-    float* sin_t = cos_t + ag_max * half;                             // [ag][4][D/8]
-    uint32_t* member = reinterpret_cast<uint32_t*>(smem + lay.member);
-    float* wts = reinterpret_cast<float*>(smem + lay.wts);              // [ag][rows_per_cta]
-    const bool rows_contig = rp.st == HD;
-    const unsigned row_bytes = (unsigned)HD * 2u;
-    const int groups = (args.agents + kAgentGroup - 1) / kAgentGroup;
-    const int tiles = (t_hi - t_lo + TR - 1) / TR;   // per agent group
-    const int total_tiles = groups * tiles;
-    int issued = 0;                                  // thread 0 only
-
-    auto issue = [&](int k) {  // thread 0: bulk-copy global tile k into its stage
-        const int slot = k % kMcStages;
-        const int t0 = t_lo + (k % tiles) * TR;
-        const int tt = min(TR, t_hi - t0);
-        uint16_t* dst = ring + (size_t)slot * TR * HD;
-        mbar_arrive_expect_tx(&full[slot], row_bytes * tt);
-        if (rows_contig) {
-            bulk_g2s(dst, reuse + rp.row(r, l, t0), row_bytes * tt, &full[slot]);
-        } else {
-            for (int q = 0; q < tt; ++q) bulk_g2s(dst + q * HD, reuse + rp.row(r, l, t0 + q), row_bytes, &full[slot]);
+    const int tid = threadIdx.x, nthreads = blockDim.x;  // kSlots * P threads
+    float* Ps = reinterpret_cast<float*>(smem);  // [32 slots][CW], natural element order
+    const int dl = args.delta[u];
+    const bool rot = plane == 0 && dl != 0;
+    if (rot)  // independent of the selection: before the wait
+        for (int e = tid; e < half; e += nthreads) {
+            float c, s;
+            rope_cos_sin(dl, args.th.theta[e], &c, &s);
+            tab[e] = make_float2(c, s);
         }
+    // The stream kernel may launch now: it sets up its ring and first tiles while this
+    // grid runs, and waits for this grid's completion before it reads the means.
+    pdl_trigger();
+    pdl_wait();  // probe sets of the selection kernel
+    float* mu_g = args.mu[plane] + ((long long)u * L + l) * HD + c0;
+    if (b == 0) {
+        for (int e = tid; e < CW; e += nthreads) mu_g[e] = 0.f;
+        return;
+    }
+    const int s = tid / P, pq = tid % P;
+    const int h = pq / v8, v = pq % v8;
+    const int eo = c0 + h * D + 4 * v;
+    const int32_t* S = args.idx[plane] + (long long)u * b;
+    float fs0[4], fs1[4], xs0[4], xs1[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) fs0[k] = fs1[k] = xs0[k] = xs1[k] = 0.f;
+    auto probe = [&](int i) {  // row index of list position i, or -1 (past the end or out of range)
+        if (i >= b) return -1;
+        const int j = __ldg(S + i);
+        if (j < 0 || j >= n) {
+            atomicOr(&g_status_repair, FLAG_BOUNDS);
+            return -1;
+        }
+        return j;
     };
-
-    if (tid == 0) {
-        for (int q = 0; q < kMcStages; ++q) {
-            mbar_init(&full[q], 1);
-            mbar_init(&empty[q], kMcWarps);
+    int jn[kPmBatch];
+#pragma unroll
+    for (int q = 0; q < kPmBatch; ++q) jn[q] = probe(s + kSlots * q);
+    for (int i0 = s; i0 < b; i0 += kSlots * kPmBatch) {
+        int jj[kPmBatch];
+        uint2 xv[kPmBatch][2], fv[kPmBatch][2];
+#pragma unroll
+        for (int q = 0; q < kPmBatch; ++q) {
+            jj[q] = jn[q];
+            if (jj[q] >= 0) {
+                const long long ro = rp.row(r, l, jj[q]) + eo;
+                const long long fo = fp.row(u, l, jj[q]) + eo;
+                xv[q][0] = __ldg(reinterpret_cast<const uint2*>(reuse + ro));
+                xv[q][1] = __ldg(reinterpret_cast<const uint2*>(reuse + ro + half));
+                fv[q][0] = __ldcs(reinterpret_cast<const uint2*>(fresh + fo));
+                fv[q][1] = __ldcs(reinterpret_cast<const uint2*>(fresh + fo + half));
+            }
         }
-        fence_mbar_init();
-        abort_flag = 0;
+#pragma unroll
+        for (int q = 0; q < kPmBatch; ++q) jn[q] = probe(i0 + kSlots * (kPmBatch + q));  // the next batch
+#pragma unroll
+        for (int q = 0; q < kPmBatch; ++q) {  // in list order
+            if (jj[q] < 0) continue;
+            const long long oo = op.row(u, l, jj[q]) + eo;
+            __stcs(reinterpret_cast<uint2*>(out + oo), fv[q][0]);
+            __stcs(reinterpret_cast<uint2*>(out + oo + half), fv[q][1]);
+            add4(xv[q][0], xs0);
+            add4(xv[q][1], xs1);
+            add4(fv[q][0], fs0);
+            add4(fv[q][1], fs1);
+        }
     }
+    __syncthreads();  // the angle table
+    if (rot) {
+        float c[4], sn[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 cs = tab[4 * v + k];
+            c[k] = cs.x;
+            sn[k] = cs.y;
+        }
+        rotate4(xs0, xs1, c, sn);
+    }
+    float* mine = Ps + s * CW + (eo - c0);
+    *reinterpret_cast<float4*>(mine) =
+        make_float4(fs0[0] - xs0[0], fs0[1] - xs0[1], fs0[2] - xs0[2], fs0[3] - xs0[3]);
+    *reinterpret_cast<float4*>(mine + half) =
+        make_float4(fs1[0] - xs1[0], fs1[1] - xs1[1], fs1[2] - xs1[2], fs1[3] - xs1[3]);
     __syncthreads();
-    // the first tiles stream in while phase 1 runs (not into the stage holding the partials)
-    const int ahead0 = lay.ps_alias ? kMcStages - 1 : kMcStages;
-    if (tid == 0)
-        for (; issued < min(ahead0, total_tiles); ++issued) issue(issued);
-    pdl_wait();  // probe sets and weights of the selection kernel
-
-    for (int grp = 0; grp < groups; ++grp) {
-        const int a0 = grp * kAgentGroup;
-        const int ag = min(kAgentGroup, args.agents - a0);
-        __syncthreads();
-        for (int i = tid; i < ag * half; i += kMcThreads) {
-            const int a = i / half, e = i % half;  // angle index e = 4 * vq + k
-            float c = 1.f, s = 0.f;
-            if (keys) rope_cos_sin(args.delta[(a0 + a) * R + r], args.th.theta[e], &c, &s);
-            const int o = (a * 4 + (e % 4)) * v8 + e / 4;
-            cos_t[o] = c;
-            sin_t[o] = s;
+    for (int e = tid; e < CW; e += nthreads) {
+        float sum = 0.f;
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+            const float* q = Ps + (kSlotsPerGroup * g) * CW + e;
+            sum += ((q[0] + q[CW]) + q[2 * CW]) + q[3 * CW];
         }
-        if (tid < ag) rot_on[tid] = keys && args.delta[(a0 + tid) * R + r] != 0;
-        for (int i = tid; i < ag * lay.words_member; i += kMcThreads) member[i] = 0u;
-        __syncthreads();
-
-        // ---------------- phase 1: probe means, one agent at a time
-        for (int a = 0; a < ag; ++a) {
-            const long long u = (long long)(a0 + a) * R + r;
-            float* mu_g = mu + (u * L + l) * (long long)HD;
-            if (b == 0) {
-                for (int e = tid; e < HD; e += kMcThreads) mu_all[a * HD + e] = 0.f;
-                for (int e = tid; e < SL; e += kMcThreads) {
-                    const int ri = rank * SL + e;  // residue-major index
-                    mu_g[4 * (ri % G) + ri / G] = 0.f;
-                }
-                continue;
-            }
-            const int32_t* S = idx + u * b;
-            const int ls = tid / kMcLanesPerSlot;
-            const int s = rank * kMcSlotsPerCta + ls;
-            for (int pq = tid % kMcLanesPerSlot; pq < P; pq += kMcLanesPerSlot) {
-                const int h = pq / v8, v = pq % v8;
-                const long long eo = (long long)h * D + 4 * v;
-                const int g_lo = h * (D / 4) + v, g_hi = g_lo + v8;
-                float fs0[4], fs1[4], xs0[4], xs1[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) fs0[k] = fs1[k] = xs0[k] = xs1[k] = 0.f;
-                for (int i = s; i < b; i += 32) {
-                    const int j = S[i];
-                    if (j < 0 || j >= n) {
-                        atomicOr(&g_status_repair, FLAG_BOUNDS);
-                        continue;
-                    }
-                    const long long ro = rp.row(r, l, j) + eo;
-                    const long long fo = fp.row((int)u, l, j) + eo;
-                    const uint2 x0v = *reinterpret_cast<const uint2*>(reuse + ro);
-                    const uint2 x1v = *reinterpret_cast<const uint2*>(reuse + ro + half);
-                    const uint2 f0v = *reinterpret_cast<const uint2*>(fresh + fo);
-                    const uint2 f1v = *reinterpret_cast<const uint2*>(fresh + fo + half);
-                    const long long oo = op.row((int)u, l, j) + eo;
-                    st_stream2(reinterpret_cast<uint2*>(out + oo), f0v);
-                    st_stream2(reinterpret_cast<uint2*>(out + oo + half), f1v);
-                    add4(x0v, xs0);
-                    add4(x1v, xs1);
-                    add4(f0v, fs0);
-                    add4(f1v, fs1);
-                }
-                if (rot_on[a]) {
-                    float c[4], sn[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        c[k] = cos_t[(a * 4 + k) * v8 + v];
-                        sn[k] = sin_t[(a * 4 + k) * v8 + v];
-                    }
-                    rotate4(xs0, xs1, c, sn);
-                }
-                float* mine = ps + ls * HD;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    mine[k * G + g_lo] = fs0[k] - xs0[k];
-                    mine[k * G + g_hi] = fs1[k] - xs1[k];
-                }
-            }
-            fence_proxy_async_smem();  // the partials' stage is refilled by bulk copies later
-            cluster.sync();
-            // residue-major elements [rank*SL, rank*SL + SL): the group sums
-            // Q_g = ((P_4g + P_4g+1) + P_4g+2) + P_4g+3 added in order g = 0..7
-            for (int e = tid; e < SL; e += kMcThreads) {
-                const int ri = rank * SL + e;
-                float part[32];
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const float* rps = cluster.map_shared_rank(ps, q / kMcSlotsPerCta);
-                    part[q] = rps[(q % kMcSlotsPerCta) * HD + ri];
-                }
-                float sum = 0.f;
-#pragma unroll
-                for (int g = 0; g < kMcCluster; ++g)
-                    sum += ((part[4 * g] + part[4 * g + 1]) + part[4 * g + 2]) + part[4 * g + 3];
-                const float m = sum / (float)b;
-                mu_slice[e] = m;
-                mu_g[4 * (ri % G) + ri / G] = m;
-            }
-            cluster.sync();
-            for (int i = tid; i < HD; i += kMcThreads) {
-                const float* rsl = cluster.map_shared_rank(mu_slice, i / SL);
-                mu_all[a * HD + i] = rsl[i % SL];
-            }
-            cluster.sync();
-        }
-
-        // ---------------- phase 2: stream this CTA's rows for every agent of the group
-        if (b > 0) {
-            for (int i = tid; i < ag * b; i += kMcThreads) {
-                const int a = i / b;
-                const long long u = (long long)(a0 + a) * R + r;
-                const int j = idx[u * b + (i % b)];
-                if (j >= t_lo && j < t_hi)
-                    atomicOr(&member[a * lay.words_member + ((j - t_lo) >> 5)], 1u << ((j - t_lo) & 31));
-            }
-            const int rows = mc_stage_weights(ag_max, args.rows_per_cta) ? t_hi - t_lo : 0;
-            for (int i = tid; i < ag * rows; i += kMcThreads) {
-                const int a = i / rows, t = i % rows;
-                const long long u = (long long)(a0 + a) * R + r;
-                wts[a * args.rows_per_cta + t] = wgt[u * n + t_lo + t];
-            }
-        }
-        __syncthreads();
-        // Top the ring up to kMcStages tiles of this group.  When the partials share a
-        // stage, tiles of the next group wait for its phase 1: the ring is drained at
-        // each group's end.
-        const int tile_end = lay.ps_alias ? min(total_tiles, (grp + 1) * tiles) : total_tiles;
-        if (tid == 0 && !abort_flag) {
-            fence_proxy_async_smem();
-            for (; issued < min(grp * tiles + kMcStages, tile_end); ++issued) issue(issued);
-        }
-        const int rpp = kMcThreads / P;  // rows per pass (P <= 256 quad pairs per row)
-        const bool active = tid < rpp * P;
-        const int pq = tid % P, row_off = tid / P;
-        const int h = pq / v8, v = pq % v8;
-        const int eo = h * D + 4 * v;
-        const int g_lo = h * (D / 4) + v, g_hi = g_lo + v8;
-        // per-agent constants as float pairs (packed f32x2 arithmetic): cos, sin, -sin, mean
-        float2 c2[2], s2[2], ns2[2], m0[2], m1[2];
-        int cached = -1;  // agent whose constants sit in these registers
-        for (int kl = 0; kl < tiles; ++kl) {
-            const int k = grp * tiles + kl;
-            const int slot = k % kMcStages;
-            const unsigned parity = (unsigned)(k / kMcStages) & 1u;
-            if (abort_flag) break;
-            if (!mbar_wait(&full[slot], parity)) {
-                atomicOr(&g_status_repair, FLAG_TIMEOUT);
-                abort_flag = 1;
-                break;
-            }
-            const uint16_t* tb = ring + (size_t)slot * TR * HD + eo;
-            const int t0 = t_lo + kl * TR;
-            const int tt = min(TR, t_hi - t0);
-            if (active) {
-                for (int a = 0; a < ag; ++a) {
-                    const bool rot = rot_on[a];
-                    if (a != cached) {
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const float* ct = cos_t + (a * 4 + 2 * q) * v8 + v;
-                            const float* st = sin_t + (a * 4 + 2 * q) * v8 + v;
-                            c2[q] = make_float2(ct[0], ct[v8]);
-                            s2[q] = make_float2(st[0], st[v8]);
-                            ns2[q] = make_float2(-s2[q].x, -s2[q].y);
-                            const float* mm = mu_all + a * HD + (2 * q) * G;
-                            m0[q] = make_float2(mm[g_lo], mm[G + g_lo]);
-                            m1[q] = make_float2(mm[g_hi], mm[G + g_hi]);
-                        }
-                        cached = a;
-                    }
-                    const long long u = (long long)(a0 + a) * R + r;
-                    uint16_t* ob = out + op.row((int)u, l, 0) + eo;
-                    const bool staged = mc_stage_weights(ag_max, args.rows_per_cta);
-                    const float* wb = staged ? wts + a * args.rows_per_cta - t_lo : wgt + u * n;
-                    const uint32_t* mem = member + a * lay.words_member;
-                    // probe bits of the tile's rows (TR <= 32 here: at most two bitmap words)
-                    const int tl0 = t0 - t_lo;
-                    uint64_t pbits = mem[tl0 >> 5];
-                    if ((tl0 & 31) + tt > 32) pbits |= (uint64_t)mem[(tl0 >> 5) + 1] << 32;
-                    pbits >>= (tl0 & 31);
-                    for (int row = row_off; row < tt; row += rpp) {
-                        const int t = t0 + row;
-                        if ((pbits >> row) & 1u) continue;
-                        const uint2 lo_raw = *reinterpret_cast<const uint2*>(tb + row * HD);
-                        const uint2 hi_raw = *reinterpret_cast<const uint2*>(tb + row * HD + half);
-                        float2 x0[2], x1[2];
-                        x0[0] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo_raw.x));
-                        x0[1] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo_raw.y));
-                        x1[0] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi_raw.x));
-                        x1[1] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi_raw.y));
-                        if (rot) {
-#pragma unroll
-                            for (int q = 0; q < 2; ++q) {
-                                const float2 lo = __ffma2_rn(x0[q], c2[q], __fmul2_rn(x1[q], ns2[q]));
-                                const float2 hi = __ffma2_rn(x1[q], c2[q], __fmul2_rn(x0[q], s2[q]));
-                                x0[q] = lo;
-                                x1[q] = hi;
-                            }
-                        }
-                        if (b > 0) {
-                            const float wt = wb[t];
-                            const float2 w2 = make_float2(wt, wt);
-#pragma unroll
-                            for (int q = 0; q < 2; ++q) {
-                                x0[q] = __ffma2_rn(w2, m0[q], x0[q]);
-                                x1[q] = __ffma2_rn(w2, m1[q], x1[q]);
-                            }
-                        }
-                        uint2 lo_out, hi_out;
-                        *reinterpret_cast<__nv_bfloat162*>(&lo_out.x) = __float22bfloat162_rn(x0[0]);
-                        *reinterpret_cast<__nv_bfloat162*>(&lo_out.y) = __float22bfloat162_rn(x0[1]);
-                        *reinterpret_cast<__nv_bfloat162*>(&hi_out.x) = __float22bfloat162_rn(x1[0]);
-                        *reinterpret_cast<__nv_bfloat162*>(&hi_out.y) = __float22bfloat162_rn(x1[1]);
-                        uint16_t* o = ob + (long long)t * op.st;
-                        st_stream2(reinterpret_cast<uint2*>(o), lo_out);
-                        st_stream2(reinterpret_cast<uint2*>(o + half), hi_out);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-            if (tid == 0 && issued < tile_end && !abort_flag) {
-                // the stage is free once every warp released it; then refill it
-                if (!mbar_wait(&empty[slot], parity)) {
-                    atomicOr(&g_status_repair, FLAG_TIMEOUT);
-                    abort_flag = 1;
-                } else {
-                    issue(issued);
-                    ++issued;
-                }
-            }
-        }
-        __syncthreads();
-    }
-    if (abort_flag) {
-        // A wait ran out (the status word says so).  From then on the tile loops skipped
-        // every wait while the CTA still passed each cluster barrier, so the other CTAs of
-        // the cluster were not held; copies still in flight are waited for (bounded).
-        if (tid == 0)
-            for (int k = max(0, issued - kMcStages); k < issued; ++k)
-                mbar_wait(&full[k % kMcStages], (unsigned)(k / kMcStages) & 1u);
-        __syncthreads();
+        mu_g[e] = sum / (float)b;
     }
 }
 
+// One quad pair of one non-probe row: rotate (keys, delta != 0), add w * mean, round to
+// bf16 and store.  The same packed f32x2 arithmetic as the multi-agent stream kernel.
+struct McConst {  // per-agent constants of a quad pair: cos, sin, -sin, mean (lo, hi)
+    float2 c2[2], s2[2], ns2[2], m0[2], m1[2];
+};
+
+__device__ __forceinline__ void correct_quad_pair(const uint16_t* tr, uint16_t* o, int half, bool rot, bool add,
+                                                  float wt, const McConst& k) {
+    const uint2 lo_raw = *reinterpret_cast<const uint2*>(tr);
+    const uint2 hi_raw = *reinterpret_cast<const uint2*>(tr + half);
+    float2 x0[2], x1[2];
+    x0[0] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo_raw.x));
+    x0[1] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo_raw.y));
+    x1[0] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi_raw.x));
+    x1[1] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi_raw.y));
+    if (rot) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const float2 lo = __ffma2_rn(x0[q], k.c2[q], __fmul2_rn(x1[q], k.ns2[q]));
+            const float2 hi = __ffma2_rn(x1[q], k.c2[q], __fmul2_rn(x0[q], k.s2[q]));
+            x0[q] = lo;
+            x1[q] = hi;
+        }
+    }
+    if (add) {
+        const float2 w2 = make_float2(wt, wt);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            x0[q] = __ffma2_rn(w2, k.m0[q], x0[q]);
+            x1[q] = __ffma2_rn(w2, k.m1[q], x1[q]);
+        }
+    }
+    uint2 lo_out, hi_out;
+    *reinterpret_cast<__nv_bfloat162*>(&lo_out.x) = __float22bfloat162_rn(x0[0]);
+    *reinterpret_cast<__nv_bfloat162*>(&lo_out.y) = __float22bfloat162_rn(x0[1]);
+    *reinterpret_cast<__nv_bfloat162*>(&hi_out.x) = __float22bfloat162_rn(x1[0]);
+    *reinterpret_cast<__nv_bfloat162*>(&hi_out.y) = __float22bfloat162_rn(x1[1]);
+    st_stream2(reinterpret_cast<uint2*>(o), lo_out);
+    st_stream2(reinterpret_cast<uint2*>(o + half), hi_out);
+}
+
+struct MsLayout {  // byte offsets into the stream kernel's dynamic shared memory
+    int ring, mu, cs, member, wts, total, words;
+};
+
+__host__ __device__ inline MsLayout ms_layout(int CW, int half, int ag, int rows, int tile_rows) {
+    MsLayout m;
+    m.ring = 0;
+    m.mu = kMsStages * tile_rows * CW * 2;  // [ag][CW] means, natural order
+    m.cs = m.mu + 4 * ag * CW;               // [ag][half] (cos, sin)
+    m.member = m.cs + 8 * ag * half;          // [ag][words] probe bits of the block's rows
+    m.words = (rows + 31) / 32;
+    m.wts = m.member + 4 * ag * m.words;      // [ag][rows] weights
+    m.total = m.wts + 4 * ag * rows;
+    return m;
+}
+
+// kCW: the slice width when it is known at compile time (the row loop then unrolls), else 0.
+template <int kCW>
+__global__ void __launch_bounds__(kMsThreads, 4)
+mean_stream_kernel(const __grid_constant__ McMaps maps, McArgs args) {
+    // TMA tile copies need a 128-byte aligned destination: the ring gets a symbol of its own
+    extern __shared__ __align__(1024) unsigned char ms_smem[];
+    unsigned char* smem = ms_smem;
+    __shared__ __align__(8) uint64_t full[kMsStages];
+    __shared__ __align__(8) uint64_t empty[kMsStages];
+    __shared__ int rot_on[kAgentGroup];
+    __shared__ int abort_flag;
+    const int slice = (int)blockIdx.y % args.slices, lp = (int)blockIdx.y / args.slices;
+    const int plane = lp & 1, l = lp >> 1;
+    const uint16_t* reuse = args.reuse[plane];
+    if (reuse == nullptr) return;
+    const CUtensorMap* map = &maps.reuse[plane];
+    uint16_t* out = args.out[plane];
+    const Plane& rp = args.rp;
+    const Plane& op = args.op;
+    const int R = rp.chunks, n = rp.tokens, L = rp.layers;
+    const int r = blockIdx.z % R, a0 = (blockIdx.z / R) * kAgentGroup;
+    const int ag = min(kAgentGroup, args.agents - a0);
+    const int D = rp.dim, half = D / 2, v8 = D / 8;
+    const int HD = rp.heads * D, CW = kCW ? kCW : args.cw, c0 = slice * CW, P = CW / 8;
+    const int b = args.b;
+    const bool keys = plane == 0;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int rows = args.rows_per_cta;
+    const int t_lo = blockIdx.x * rows, t_hi = min(n, t_lo + rows);
+    const int TR = args.tile_rows;
+    const MsLayout lay = ms_layout(CW, half, min(args.agents, kAgentGroup), rows, TR);
+    uint16_t* ring = reinterpret_cast<uint16_t*>(smem + lay.ring);  // [stages][TR][CW]
+    float* mu_s = reinterpret_cast<float*>(smem + lay.mu);
+    float2* cs = reinterpret_cast<float2*>(smem + lay.cs);
+    uint32_t* member = reinterpret_cast<uint32_t*>(smem + lay.member);
+    float* wts = reinterpret_cast<float*>(smem + lay.wts);
+    const unsigned tile_bytes = (unsigned)TR * CW * 2u;  // a box is always copied whole
+    const int tiles = (t_hi - t_lo + TR - 1) / TR;
+    int issued = 0;  // thread 0 only
+    auto issue = [&](int k) {
+        const int slot = k % kMsStages;
+        mbar_arrive_expect_tx(&full[slot], tile_bytes);
+        tma_load_4d(ring + (size_t)slot * TR * CW, map, c0, t_lo + k * TR, l, r, &full[slot]);
+    };
+    if (smem_u32(ring) & 127u) {  // never expected: report it instead of copying
+        if (tid == 0) atomicOr(&g_status_repair, FLAG_INTERNAL);
+        return;
+    }
+    if (tid == 0) {
+        prefetch_tensormap(map);
+        for (int q = 0; q < kMsStages; ++q) {
+            mbar_init(&full[q], 1);
+            mbar_init(&empty[q], kMsWarps);
+        }
+        fence_mbar_init();
+        abort_flag = 0;
+        // reused rows depend on no kernel of the chain: the first tiles go out at once
+        for (; issued < min(kMsStages, tiles); ++issued) issue(issued);
+    }
+    for (int i = tid; i < ag * half; i += kMsThreads) {
+        const int a = i / half, e = i % half;
+        float c = 1.f, s = 0.f;
+        if (keys) rope_cos_sin(args.delta[(a0 + a) * R + r], args.th.theta[e], &c, &s);
+        cs[a * half + e] = make_float2(c, s);
+    }
+    if (tid < ag) rot_on[tid] = keys && args.delta[(a0 + tid) * R + r] != 0;
+    for (int i = tid; i < ag * lay.words; i += kMsThreads) member[i] = 0u;
+    pdl_wait();  // means (and, before them, probe sets and weights)
+    __syncthreads();
+    for (int i = tid; i < ag * CW; i += kMsThreads) {
+        const int a = i / CW, e = i % CW;
+        const long long u = (long long)(a0 + a) * R + r;
+        mu_s[i] = args.mu[plane][(u * L + l) * HD + c0 + e];
+    }
+    if (b > 0) {
+        for (int i = tid; i < ag * b; i += kMsThreads) {
+            const int a = i / b;
+            const long long u = (long long)(a0 + a) * R + r;
+            const int j = args.idx[plane][u * b + (i % b)];
+            if (j >= t_lo && j < t_hi) atomicOr(&member[a * lay.words + ((j - t_lo) >> 5)], 1u << ((j - t_lo) & 31));
+        }
+        for (int i = tid; i < ag * (t_hi - t_lo); i += kMsThreads) {
+            const int a = i / (t_hi - t_lo), t = i % (t_hi - t_lo);
+            const long long u = (long long)(a0 + a) * R + r;
+            wts[a * rows + t] = args.w[plane][u * n + t_lo + t];
+        }
+    }
+    __syncthreads();
+    const int rpp = kMsThreads / P;  // rows per pass (P = cw / 8 divides the block)
+    const int pq = tid % P, row_off = tid / P;
+    const int h = pq / v8, v = pq % v8;
+    const int eo = h * D + 4 * v;  // within the slice
+    const long long pass_st = (long long)rpp * op.st;
+    McConst kc;
+    int cached = -1;  // agent whose constants sit in kc
+    for (int k = 0; k < tiles; ++k) {
+        const int slot = k % kMsStages;
+        const unsigned parity = (unsigned)(k / kMsStages) & 1u;
+        if (!mbar_wait(&full[slot], parity)) {
+            atomicOr(&g_status_repair, FLAG_TIMEOUT);
+            abort_flag = 1;
+        }
+        if (abort_flag) break;
+        const uint16_t* tb = ring + (size_t)slot * TR * CW + eo;
+        const int t0 = t_lo + k * TR;
+        const int tt = min(TR, t_hi - t0);
+        for (int a = 0; a < ag; ++a) {
+            const bool rot = rot_on[a];
+            if (a != cached) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const float2 ca = cs[a * half + 4 * v + 2 * q], cb = cs[a * half + 4 * v + 2 * q + 1];
+                    kc.c2[q] = make_float2(ca.x, cb.x);
+                    kc.s2[q] = make_float2(ca.y, cb.y);
+                    kc.ns2[q] = make_float2(-ca.y, -cb.y);
+                    const float* mm = mu_s + a * CW + eo + 2 * q;
+                    kc.m0[q] = make_float2(mm[0], mm[1]);
+                    kc.m1[q] = make_float2(mm[half], mm[half + 1]);
+                }
+                cached = a;
+            }
+            const long long u = (long long)(a0 + a) * R + r;
+            const float* wb = wts + a * rows - t_lo;
+            const uint32_t* mem = member + a * lay.words;
+            uint16_t* o = out + op.row((int)u, l, t0 + row_off) + c0 + eo;
+            if (kCW != 0 && kMsTileBytes / (2 * kCW) <= 64) {
+                // TR <= 64 and tiles start at multiples of TR: the tile's probe bits are one
+                // 64-bit window, and the row loop unrolls over the passes
+                constexpr int kPasses = kCW ? (kMsTileBytes / (2 * kCW)) / (kMsThreads / (kCW / 8)) : 1;
+                const int tl0 = t0 - t_lo;
+                uint64_t pbits = 0;
+                if (b > 0) {
+                    const int w0 = tl0 >> 5, sh = tl0 & 31;
+                    const uint64_t lo = mem[w0];
+                    const uint64_t hi = (w0 + 1 < lay.words) ? mem[w0 + 1] : 0u;
+                    const uint64_t x2 = (sh && w0 + 2 < lay.words) ? mem[w0 + 2] : 0u;
+                    pbits = ((lo | (hi << 32)) >> sh) | (sh ? (x2 << (64 - sh)) : 0u);
+                }
+#pragma unroll
+                for (int ps = 0; ps < kPasses; ++ps) {
+                    const int row = row_off + ps * (kMsThreads / (kCW / 8));
+                    if (row < tt && !((pbits >> row) & 1u))
+                        correct_quad_pair(tb + row * kCW, o, half, rot, b > 0, b > 0 ? wb[t0 + row] : 0.f, kc);
+                    o += pass_st;
+                }
+            } else {
+                for (int row = row_off; row < tt; row += rpp, o += pass_st) {
+                    const int tl = t0 + row - t_lo;
+                    if (b > 0 && ((mem[tl >> 5] >> (tl & 31)) & 1u)) continue;  // probe row: written already
+                    correct_quad_pair(tb + row * CW, o, half, rot, b > 0, b > 0 ? wb[t0 + row] : 0.f, kc);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (tid == 0 && issued < tiles && !abort_flag) {
+            // the stage is free once every warp released it; then refill it
+            if (!mbar_wait(&empty[slot], parity)) {
+                atomicOr(&g_status_repair, FLAG_TIMEOUT);
+                abort_flag = 1;
+            } else {
+                issue(issued);
+                ++issued;
+            }
+        }
+    }
+    __syncthreads();
+    if (abort_flag && tid == 0)  // a wait ran out: copies still in flight are waited for (bounded)
+        for (int k = max(0, issued - kMsStages); k < issued; ++k)
+            mbar_wait(&full[k % kMsStages], (unsigned)(k / kMsStages) & 1u);
+}
 // =====================================================================================
 // Rounds of several agents: two kernels instead of the per-agent phases above.
 //   round_mean_kernel: one CTA per (unit, layer, plane) computes that unit's probe mean
@@ -898,7 +898,7 @@ constexpr int kRsRows = 128;  // rows per CTA of the stream kernel
 constexpr int kRsStages = 3;  // tiles of reused rows in flight per CTA
 
 __global__ void __launch_bounds__(kRmThreads, 4) round_mean_kernel(McArgs args) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float ct[kMaxHeadDim / 2], st[kMaxHeadDim / 2];
     const int u = blockIdx.x, plane = blockIdx.y & 1, l = blockIdx.y >> 1;
     const uint16_t* reuse = args.reuse[plane];
@@ -933,8 +933,8 @@ __global__ void __launch_bounds__(kRmThreads, 4) round_mean_kernel(McArgs args) 
         const long long eo = (long long)h * D + 4 * v;
         float q0[4], q1[4];
 #pragma unroll
-        for (int j4 = 0; j4 < kMcSlotsPerCta; ++j4) {
-            const int s = warp * kMcSlotsPerCta + j4;
+        for (int j4 = 0; j4 < kSlotsPerGroup; ++j4) {
+            const int s = warp * kSlotsPerGroup + j4;
             float fs0[4], fs1[4], xs0[4], xs1[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) fs0[k] = fs1[k] = xs0[k] = xs1[k] = 0.f;
@@ -996,14 +996,14 @@ __global__ void __launch_bounds__(kRmThreads, 4) round_mean_kernel(McArgs args) 
     for (int e = tid; e < HD; e += kRmThreads) {
         float sum = 0.f;
 #pragma unroll
-        for (int g = 0; g < kMcCluster; ++g) sum += Qs[g * HD + e];
+        for (int g = 0; g < kGroups; ++g) sum += Qs[g * HD + e];
         mu_g[e] = sum / (float)b;
     }
     pdl_trigger();
 }
 
 __global__ void __launch_bounds__(kRsThreads) round_stream_kernel(McArgs args, int tile_rows) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     const int plane = blockIdx.y & 1, l = blockIdx.y >> 1;
     const uint16_t* reuse = args.reuse[plane];
     if (reuse == nullptr) return;
@@ -1173,7 +1173,7 @@ cudaError_t launch_mean_correct(const McPlanes& pl, const kvfix_kv_desc& rd, con
     const int HD = a.rp.heads * a.rp.dim;
     if (agents > 1 && kAgentGroup * (HD / 8) <= kRsThreads) {
         // a round of several agents: all probe means at once, then one fan-out stream
-        const size_t mean_smem = (size_t)kMcCluster * HD * sizeof(float);
+        const size_t mean_smem = (size_t)kGroups * HD * sizeof(float);
         cudaError_t e = cudaFuncSetAttribute(round_mean_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)mean_smem);
         if (e != cudaSuccess) return e;
@@ -1181,7 +1181,7 @@ cudaError_t launch_mean_correct(const McPlanes& pl, const kvfix_kv_desc& rd, con
                            mean_smem, s, a);
         if (e != cudaSuccess) return e;
         const int half = a.rp.dim / 2;
-        const int tile_rows = max(1, min(32, kMcTileBytes / (2 * HD)));
+        const int tile_rows = max(1, min(32, kMsTileBytes / (2 * HD)));
         const size_t stream_smem = (size_t)kRsStages * tile_rows * HD * 2 +
                                    sizeof(float) * (2 * kAgentGroup * half + kAgentGroup * kRsRows) +
                                    sizeof(uint32_t) * kAgentGroup * (kRsRows / 32);
@@ -1192,18 +1192,54 @@ cudaError_t launch_mean_correct(const McPlanes& pl, const kvfix_kv_desc& rd, con
                                                         a.rp.chunks * groups),
                               dim3(kRsThreads), stream_smem, s, a, tile_rows);
     }
-    a.rows_per_cta = (n + kMcCluster - 1) / kMcCluster;
-    // at most 32 rows a tile: a tile's probe bits then fit one 64-bit window
-    a.tile_rows = max(1, min(32, kMcTileBytes / (2 * HD)));
+    // column slices of whole heads, kMcSliceCols elements wide unless one head is wider
+    int hs = 1;
+    for (int d = a.rp.heads; d >= 1; --d)
+        if (a.rp.heads % d == 0 && d * a.rp.dim <= kMcSliceCols) {
+            hs = d;
+            break;
+        }
+    a.cw = hs * a.rp.dim;
+    a.slices = a.rp.heads / hs;
+    const int groups = (agents + kAgentGroup - 1) / kAgentGroup;
+    const long long units = (long long)agents * a.rp.chunks;
+    if (2ll * a.rp.layers * a.slices > 65535 || (long long)a.rp.chunks * groups > 65535 || units > 65535)
+        return cudaErrorInvalidConfiguration;
+    // the means: one CTA per (unit, layer, plane, slice), a thread per (slot, quad pair)
+    const int pm_threads = kSlots * (a.cw / 8);
+    const size_t pm_smem = (size_t)kSlots * a.cw * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(probe_mean_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pm_smem);
+    if (e != cudaSuccess) return e;
+    e = launch_chained(probe_mean_kernel, dim3(a.slices, 2 * a.rp.layers, (unsigned)units), dim3(pm_threads), pm_smem,
+                       s, a);
+    if (e != cudaSuccess) return e;
+    // the stream: tiles of (cw x tile_rows) elements, 16 KB or the block's rows
+    a.rows_per_cta = min(kMsRows, n);
+    a.tile_rows = min(kMsTileBytes / (2 * a.cw), (a.rows_per_cta + 7) / 8 * 8);
     const int ag = agents < kAgentGroup ? agents : kAgentGroup;
-    const McLayout lay = mc_layout(HD, a.rp.dim / 2, ag, a.rows_per_cta, a.tile_rows);
+    const MsLayout lay = ms_layout(a.cw, a.rp.dim / 2, ag, a.rows_per_cta, a.tile_rows);
     const size_t smem = (size_t)lay.total;
     if (smem > 220 * 1024) return cudaErrorInvalidValue;  // shape beyond the kernel's shared memory
-    cudaError_t e = cudaFuncSetAttribute(mean_correct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    McMaps maps;
+    memset(&maps, 0, sizeof maps);
+    auto enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    for (int q = 0; q < 2; ++q) {
+        if (!a.reuse[q]) continue;
+        cuuint64_t dims[4], strides[3];
+        plane_map_strides(a.rp, dims, strides);
+        cuuint32_t box[4] = {(cuuint32_t)a.cw, (cuuint32_t)a.tile_rows, 1, 1};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (enc(&maps.reuse[q], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(a.reuse[q]), dims,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    auto kernel = a.cw == 128 ? mean_stream_kernel<128> : mean_stream_kernel<0>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(kMcCluster, 2 * a.rp.layers, a.rp.chunks);
-    return launch_chained(mean_correct_kernel, grid, dim3(kMcThreads), smem, s, a);
+    dim3 grid((n + a.rows_per_cta - 1) / a.rows_per_cta, 2 * a.rp.layers * a.slices, a.rp.chunks * groups);
+    return launch_chained(kernel, grid, dim3(kMsThreads), smem, s, maps, a);
 }
 
 }  // namespace kvfix

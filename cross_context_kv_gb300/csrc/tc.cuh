@@ -17,6 +17,23 @@ namespace kvfix {
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
+// Dims and strides (bytes) of a plane view for a 4-D tensor map (dims: row elements,
+// tokens, layers, chunks); the stride of a dimension of size 1 is irrelevant and is
+// replaced by a consistent one.
+inline void plane_map_strides(const Plane& p, cuuint64_t* dims, cuuint64_t* strides) {
+    const long long row = (long long)p.heads * p.dim;
+    dims[0] = (cuuint64_t)row;
+    dims[1] = (cuuint64_t)p.tokens;
+    dims[2] = (cuuint64_t)p.layers;
+    dims[3] = (cuuint64_t)p.chunks;
+    long long st = p.tokens > 1 ? p.st : row;
+    long long sl = p.layers > 1 ? p.sl : st * p.tokens;
+    long long sc = p.chunks > 1 ? p.sc : sl * p.layers;
+    strides[0] = (cuuint64_t)(2 * st);
+    strides[1] = (cuuint64_t)(2 * sl);
+    strides[2] = (cuuint64_t)(2 * sc);
+}
+
 // Shared-memory swizzle of a TMA box whose inner extent is `inner_bytes` (32, 64, 128).
 inline CUtensorMapSwizzle swizzle_for(int inner_bytes) {
     return inner_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B

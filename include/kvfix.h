@@ -163,7 +163,8 @@ KVFIX_API kvfix_status kvfix_score_topk(const kvfix_bf16* k_reuse, const kvfix_b
  * idx_k, idx_v      : device int32[agents*R][b] (ascending not required; each entry
  *                     must lie in [0, tokens) -- others are skipped and flagged).
  * w_k, w_v          : device float[agents*R][tokens].
- * mu_k, mu_v        : device float[agents*R][layers][kv_heads*head_dim], written.
+ * mu_k, mu_v        : device float[agents*R][layers][kv_heads*head_dim], written (and
+ *                     read back by the call's second kernel); must not overlap w or out.
  * Each reused row is read once for all agents of the call.
  */
 KVFIX_API kvfix_status kvfix_mean_correct(const kvfix_bf16* k_reuse, const kvfix_bf16* v_reuse,

@@ -67,6 +67,11 @@ SMALL_REPAIR = [
     # a token row wider than 1024 elements: probe rows are read straight from memory
     synth.REPAIR_TINY.with_(name="wide_rows", tokens=90, kv_heads=9, head_dim=128, layers=2,
                             r_num=1, r_den=3, seed=11),
+    # three row blocks of the stream kernel, the last one ragged, over 8 head slices
+    synth.REPAIR_TINY.with_(name="row_blocks", tokens=1100, kv_heads=8, head_dim=128, layers=2,
+                            r_num=3, r_den=20, seed=12, rope_base=5e5, delta_kind="fixed", delta_fixed=4321),
+    # one 256-wide head: the widest slice (1024 threads per probe-mean CTA)
+    synth.REPAIR_TINY.with_(name="head256", tokens=200, kv_heads=1, head_dim=256, layers=2, seed=13),
 ]
 
 
