@@ -172,6 +172,87 @@ def barrier(world: int):
         dist.barrier()
 
 
+# ------------------------------------------------------- oracle-side helpers
+# (the cpu_baseline legs only: none of this runs inside a timed GPU region)
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine() or "unknown"
+
+
+def timed_reps(fn, min_seconds: float, max_reps: int = 1 << 30):
+    """Repeat fn until min_seconds have passed (at least once); (seconds per rep, reps)."""
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        fn()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            return el / reps, reps
+
+
+def with_threads(oracle, n: int, fn):
+    """Run fn with the oracle's OpenMP team set to n threads, then restore it."""
+    old = oracle.num_threads()
+    oracle.set_num_threads(n)
+    try:
+        return fn()
+    finally:
+        oracle.set_num_threads(old)
+
+
+def baseline_obj(oracle, value, unit, sample, **extra):
+    """The cpu_baseline object of a line or stage: the oracle as it stands on the host."""
+    d = {"value": value, "unit": unit, "cores": oracle.num_threads(), "nproc": os.cpu_count(),
+         "cpu_model": cpu_model(), "kind": "oracle", "sample": sample}
+    d.update(extra)
+    return d
+
+
+def selection_agreement(gpu_idx, scores, b: int, keys_as_float: bool):
+    """Compare GPU index sets [units][b] with the oracle's top-b of `scores` [units][n]
+    (the ranking keys: float32 of the score when keys_as_float).  Returns the number of
+    swapped pairs that are near ties (< 1e-5 relative), the number that are not, and the
+    smallest relative gap between the b-th and (b+1)-th key over the units."""
+    import oracle
+    gpu_idx = np.asarray(gpu_idx).reshape(len(scores), -1)
+    near, far, gaps = 0, 0, []
+    for u in range(len(scores)):
+        keys = np.asarray(scores[u], dtype=np.float64)
+        if keys_as_float:
+            keys = keys.astype(np.float32).astype(np.float64)
+        ref = oracle.topk(keys, b, keys_as_float)
+        sg, sr = set(gpu_idx[u].tolist()), set(ref.tolist())
+        for i, j in zip(sorted(sg - sr), sorted(sr - sg)):
+            rel = abs(keys[i] - keys[j]) / max(abs(keys[i]), abs(keys[j]), 1e-300)
+            if rel < 1e-5:
+                near += 1
+            else:
+                far += 1
+        if 0 < b < keys.size:
+            srt = np.sort(keys)[::-1]
+            gaps.append(float((srt[b - 1] - srt[b]) / max(abs(srt[b - 1]), 1e-300)))
+    return {"near_tie_swaps": near, "non_tie_mismatches": far,
+            "boundary_gap": min(gaps) if gaps else None,
+            "units_checked": len(scores)}
+
+
 # ------------------------------------------------------------ workload sizes
 
 def repair_bytes(cfg: synth.RepairConfig):
@@ -233,7 +314,7 @@ def time_repair(kvfix, cfg, inp, steps, warmup, flush):
     flushed (untimed) between steps.  Then `steps` launches of mean_correct alone, each
     bracketed by events, for the correction kernel's own duration (an event between the
     two calls would break the launch chaining, so the step loop has none).
-    Returns (step times ms, mean_correct times ms)."""
+    Returns (step times ms, mean_correct times ms, the last step's selection)."""
     stream = torch.cuda.current_stream()
     out = {"k": torch.empty_like(inp["k_fresh"]), "v": torch.empty_like(inp["v_fresh"]),
            "mu_k": torch.empty(cfg.units, cfg.layers, cfg.kv_heads * cfg.head_dim, device="cuda"),
@@ -265,7 +346,36 @@ def time_repair(kvfix, cfg, inp, steps, warmup, flush):
     torch.cuda.synchronize()
     mc_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     kvfix.check_status()
-    return step_ms, mc_ms
+    return step_ms, mc_ms, sel
+
+
+def time_steady(kvfix, cfg, inp, seconds: float, flush):
+    """The same step back to back for at least `seconds` of wall time, L2 flushed (untimed)
+    between steps, each step bracketed by events: the spread of a long run, and a window
+    long enough for the clock sampler."""
+    stream = torch.cuda.current_stream()
+    out = {"k": torch.empty_like(inp["k_fresh"]), "v": torch.empty_like(inp["v_fresh"]),
+           "mu_k": torch.empty(cfg.units, cfg.layers, cfg.kv_heads * cfg.head_dim, device="cuda"),
+           "mu_v": torch.empty(cfg.units, cfg.layers, cfg.kv_heads * cfg.head_dim, device="cuda")}
+    ms = []
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        evs = []
+        for _ in range(50):
+            flush.zero_()
+            host_lead()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run_repair_step(kvfix, cfg, inp, out)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        ms.extend(a.elapsed_time(b) for a, b in evs)
+    kvfix.check_status()
+    ms.sort()
+    q = lambda f: round(ms[min(len(ms) - 1, int(f * len(ms)))], 5)  # noqa: E731
+    return {"steps": len(ms), "wall_s": round(time.perf_counter() - t0, 2), "median_ms": q(0.5),
+            "p10_ms": q(0.1), "p90_ms": q(0.9), "min_ms": round(ms[0], 5), "max_ms": round(ms[-1], 5)}
 
 
 def time_score(kvfix, cfg, inp, steps, flush):
@@ -337,7 +447,83 @@ def time_e2e(kvfix, cfg, inp, steps, warmup):
     return t0.elapsed_time(t1) / steps, h2d, d2h
 
 
-def stage_round(kvfix, peak, steps=5, warmup=2):
+ORACLE_STAGE_SECONDS = 5.0   # per stage oracle leg (siblings are timed until this is spent)
+ORACLE_ROUND_AGENTS = 2      # agents of the round the oracle leg repairs (host memory)
+
+
+def stage_tiny(kvfix, peak, steps=20, warmup=5, oracle_leg=True):
+    """The tiny single-chunk repair (2 layers, 4 x 64, 256 tokens): L2-resident and
+    launch-bound, reported but exempt from the roofline target."""
+    cfg = synth.REPAIR_TINY
+    reuse = synth.repair_reuse(cfg, "cuda")
+    fk, fv = compose_fresh_gpu(kvfix, cfg, reuse, range(cfg.units))
+    inp = {"k_reuse": reuse["k_reuse"], "v_reuse": reuse["v_reuse"], "delta": reuse["delta"],
+           "k_fresh": fk, "v_fresh": fv}
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    step_ms, mc_ms, sel = time_repair(kvfix, cfg, inp, steps, warmup, flush)
+    by = repair_bytes(cfg)
+    ms, mc = statistics.median(step_ms), statistics.median(mc_ms)
+    res = {"workload": "repair_tiny: one 256-token chunk, 2 layers, 4 KV heads x 64, b = 26, delta 137, base 1e4",
+           "ms_per_step": round(ms, 5), "corrected_GBps": round(by["corrected"] / ms / 1e6, 2),
+           "tokens_per_s": round(by["tokens"] / ms * 1e3, 1),
+           "step_frac": round(by["step"] / ms / 1e6 / peak, 4),
+           "mean_correct": {"ms": round(mc, 5), "algorithmic_bytes": by["mean_correct"],
+                            "frac": round(by["mean_correct"] / mc / 1e6 / peak, 4)},
+           "note": "L2-resident and launch-bound (1.1 MB): reported, exempt from the roofline target"}
+    if oracle_leg:
+        import oracle
+        oracle.build()
+        h = host_repair_inputs(inp)
+        cl = cfg.check_layer
+        dk = oracle.scores(h["rk"][:, cl], h["fk"][:, cl], h["delta"], 1, cfg.rope_base, True)
+        dv = oracle.scores(h["rv"][:, cl], h["fv"][:, cl], h["delta"], 1, cfg.rope_base, False)
+        res["selection"] = repair_selection_report(cfg, sel, dk, dv)
+        res["cpu_baseline"] = repair_cpu_baseline(cfg, h, 2.0, True, "repair_tiny, the timed chunk")
+    del inp, fk, fv, reuse, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def stage_rerope(kvfix, peak, steps=10, warmup=3, oracle_leg=True):
+    """kvfix_rerope alone on the 8B chunk's key plane (32 layers x 4096 x 8 x 128)."""
+    cfg = synth.REPAIR_LLAMA8B
+    reuse = synth.repair_reuse(cfg, "cuda")
+    k, delta = reuse["k_reuse"], reuse["delta"]
+    out = torch.empty_like(k)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    ms = []
+    for s_ in range(warmup + steps):
+        flush.zero_()
+        host_lead()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        kvfix.rerope(k, delta, cfg.rope_base, out=out)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if s_ >= warmup:
+            ms.append(e0.elapsed_time(e1))
+    kvfix.check_status()
+    t = statistics.median(ms)
+    nbytes = 2 * k.numel() * 2
+    res = {"workload": "rerope of the repair_llama8b key plane: 32 layers x 4096 tokens x 8 x 128, "
+                       "delta U[500,8000], base 5e5",
+           "ms": round(t, 5), "algorithmic_bytes": nbytes, "GBps": round(nbytes / t / 1e6, 1),
+           "frac": round(nbytes / t / 1e6 / peak, 4)}
+    if oracle_leg:
+        import oracle
+        oracle.build()
+        kb, dn = synth.bits(k), delta.cpu().numpy()
+        sec, reps = timed_reps(lambda: oracle.rerope(kb, dn, cfg.rope_base), 2.0)
+        res["cpu_baseline"] = baseline_obj(oracle, round(nbytes / sec / 1e9, 4), "GB/s",
+                                           f"the same key plane, {reps} repetition(s) of {sec:.4f} s")
+        del kb
+    del reuse, k, out, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def stage_round(kvfix, peak, steps=5, warmup=2, oracle_leg=True):
     """Collective 8-agent round (Qwen2.5-14B shape): one score + one correct call covers
     all 8 agents x 8 shared blocks; each shared block's reused rows are read once."""
     cfg = synth.ROUND_QWEN14B
@@ -346,7 +532,7 @@ def stage_round(kvfix, peak, steps=5, warmup=2):
     inp = {"k_reuse": reuse["k_reuse"], "v_reuse": reuse["v_reuse"], "delta": reuse["delta"],
            "k_fresh": fk, "v_fresh": fv}
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    step_ms, mc_ms = time_repair(kvfix, cfg, inp, steps, warmup, flush)
+    step_ms, mc_ms, sel_t = time_repair(kvfix, cfg, inp, steps, warmup, flush)
     by = repair_bytes(cfg)
     ms = statistics.mean(step_ms)
     mc = statistics.mean(mc_ms)
@@ -375,12 +561,34 @@ def stage_round(kvfix, peak, steps=5, warmup=2):
                             "GBps": round(by["mean_correct"] / mc / 1e6, 1),
                             "frac": round(by["mean_correct"] / mc / 1e6 / peak, 4)},
            "reuse_reads_saved_vs_per_agent_bytes": per_agent_extra}
+    if oracle_leg:
+        import oracle
+        oracle.build()
+        # probe sets of all 64 (agent, block) units against the oracle's check-layer scores
+        cl = cfg.check_layer
+        hk = {"rk": synth.bits(inp["k_reuse"][:, cl]), "rv": synth.bits(inp["v_reuse"][:, cl]),
+              "fk": synth.bits(inp["k_fresh"][:, cl]), "fv": synth.bits(inp["v_fresh"][:, cl])}
+        dn = inp["delta"].cpu().numpy()
+        dk = oracle.scores(hk["rk"], hk["fk"], dn, cfg.agents, cfg.rope_base, True)
+        dv = oracle.scores(hk["rv"], hk["fv"], dn, cfg.agents, cfg.rope_base, False)
+        res["selection"] = repair_selection_report(cfg, sel_t, dk, dv)
+        # the oracle's whole round on a sample of the agents (host memory), all 48 layers
+        A = ORACLE_ROUND_AGENTS
+        scfg = cfg.with_(agents=A)
+        R = cfg.chunks
+        h = {"rk": synth.bits(inp["k_reuse"]), "rv": synth.bits(inp["v_reuse"]),
+             "fk": synth.bits(inp["k_fresh"][:A * R]), "fv": synth.bits(inp["v_fresh"][:A * R]),
+             "delta": dn[:A * R]}
+        res["cpu_baseline"] = repair_cpu_baseline(scfg, h, 0.0, False,
+                                                  f"round_qwen14b agents 0..{A - 1} of {cfg.agents} "
+                                                  f"({A * R} of {cfg.units} units, all 48 layers)")
+        del h
     del inp, fk, fv, reuse, flush
     torch.cuda.empty_cache()
     return res
 
 
-def stage_diff(kvfix, peak, steps=5, warmup=2):
+def stage_diff(kvfix, peak, steps=5, warmup=2, oracle_leg=True):
     cfg = synth.SIBLINGS_8B
     inp = synth.diff_inputs(cfg, "cuda")
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -485,12 +693,38 @@ def stage_diff(kvfix, peak, steps=5, warmup=2):
            "restore": {"ms": round(rst, 4), "algorithmic_bytes": res_bytes,
                        "GBps": round(res_bytes / rst / 1e6, 1), "frac": round(res_bytes / rst / 1e6 / peak, 4),
                        "pool": f"{tgt['slots']} slots of 16-token pages, keys re-aligned per sibling"}}
+    if oracle_leg:
+        # the oracle's encode + gather, one sibling at a time (host memory), until the
+        # time budget is spent; its rate is per sibling, the same for all sixteen
+        import oracle
+        oracle.build()
+        mk, mv = synth.bits(inp["master_k"]), synth.bits(inp["master_v"])
+        te = tg = 0.0
+        done = 0
+        t_start = time.perf_counter()
+        while done < cfg.siblings and (done == 0 or time.perf_counter() - t_start < ORACLE_STAGE_SECONDS):
+            sk, sv = synth.bits(inp["sib_k"][done:done + 1]), synth.bits(inp["sib_v"][done:done + 1])
+            t0 = time.perf_counter()
+            m_, o_, p_, e_ = oracle.diff_encode(mk, mv, sk, sv, cfg.block_tokens)
+            t1 = time.perf_counter()
+            oracle.diff_gather(mk, mv, m_, o_, p_, 1, cfg.block_tokens)
+            t2 = time.perf_counter()
+            te += t1 - t0
+            tg += t2 - t1
+            done += 1
+            del sk, sv, m_, o_, p_
+        per_s = (enc_bytes + gat_bytes) / cfg.siblings
+        res["cpu_baseline"] = baseline_obj(
+            oracle, round(per_s * done / (te + tg) / 1e9, 4), "GB/s",
+            f"siblings_8b siblings 0..{done - 1} of {cfg.siblings}, one at a time: encode then gather",
+            encode_s_per_sibling=round(te / done, 4), gather_s_per_sibling=round(tg / done, 4))
+        del mk, mv
     del inp, mask, offsets, payload, out_k, out_v, flush, pool_k, pool_v, tgt
     torch.cuda.empty_cache()
     return res
 
 
-def stage_lowrank(kvfix, peak, steps=3, warmup=2):
+def stage_lowrank(kvfix, peak, steps=3, warmup=2, oracle_leg=True):
     cfg = synth.LOWRANK_70B
     inp = synth.lowrank_inputs(cfg, "cuda")
     stream = torch.cuda.current_stream()
@@ -560,50 +794,104 @@ def stage_lowrank(kvfix, peak, steps=3, warmup=2):
            "draft_rank": {"ms": round(dr, 4), "algorithmic_bytes": dr_bytes,
                           "GBps": round(dr_bytes / dr / 1e6, 1), "frac": round(dr_bytes / dr / 1e6 / peak, 4)},
            "layouts": lay}
+    if oracle_leg:
+        import oracle
+        oracle.build()
+        # the draft top-k of every chunk against the oracle's scores of the same keys
+        kvfix.lowrank_apply(inp["x_k"], inp["a_k"], inp["b_k"], out=kt)
+        gidx, _ = kvfix.draft_rank(kt, inp["q"], cfg.layer_begin, cfg.k_rows, workspace=ws)
+        gidx = gidx.cpu().numpy()
+        near, far, gaps = 0, 0, []
+        for c in range(cfg.chunks):
+            sc = oracle.draft_scores(synth.bits(kt[c:c + 1]), synth.bits(inp["q"][c:c + 1]), cfg.layer_begin)
+            rep = selection_agreement(gidx[c:c + 1], sc, cfg.k_rows, False)
+            near += rep["near_tie_swaps"]
+            far += rep["non_tie_mismatches"]
+            if rep["boundary_gap"] is not None:
+                gaps.append(rep["boundary_gap"])
+        res["selection"] = {"near_ties": near, "non_tie_mismatches": far, "boundary_gap": min(gaps) if gaps else None,
+                            "sets_checked": cfg.chunks,
+                            "rule": "oracle draft scores of the GPU's low-rank keys; swaps accepted only below "
+                                    "1e-5 relative; boundary_gap = smallest relative gap between the k-th and "
+                                    "(k+1)-th oracle score"}
+        # the oracle's whole stage for chunk 0 (host memory): low-rank K and V, draft scores,
+        # top-k, row overwrite of both planes
+        t_or = 0.0
+        keep = {}
+        for pl in ("k", "v"):
+            x = synth.bits(inp[f"x_{pl}"][0:1])
+            a_, b_ = synth.bits(inp[f"a_{pl}"][0:1]), synth.bits(inp[f"b_{pl}"][0:1])
+            t0 = time.perf_counter()
+            keep[pl] = oracle.lowrank_apply(x, a_, b_)
+            t_or += time.perf_counter() - t0
+            del x, a_, b_
+        t0 = time.perf_counter()
+        sc = oracle.draft_scores(keep["k"], synth.bits(inp["q"][0:1]), cfg.layer_begin)
+        oidx = oracle.topk(sc[0], cfg.k_rows, False)
+        t_or += time.perf_counter() - t0
+        for pl in ("k", "v"):
+            fr = synth.bits(inp[f"fresh_{pl}"][0:1])
+            t0 = time.perf_counter()
+            oracle.row_overwrite(keep[pl], fr, oidx[None])
+            t_or += time.perf_counter() - t0
+            del fr
+        del keep
+        res["cpu_baseline"] = baseline_obj(
+            oracle, round(2 * plane / C / t_or / 1e9, 4), "GB/s",
+            f"lowrank_70b chunk 0 of {C}: low-rank K and V, draft scores, top-{cfg.k_rows}, row overwrite "
+            f"(value = corrected K+V bytes of the chunk / time)", seconds_per_chunk=round(t_or, 3))
     del inp, kt, vt, ws, flush
     torch.cuda.empty_cache()
     return res
 
 
-def cpu_baseline(cfg, rank_seed_unit=0, min_seconds=10.0, max_layers=None):
-    """The oracle as it stands on the host cores: score + top-b + mean correction of a
-    sample of the workload (layers [0, max_layers) of one chunk), repeated until
-    min_seconds of CPU work.  Returns the line's cpu_baseline object."""
+def host_repair_inputs(inp) -> dict:
+    """Host copies (bf16 bit patterns) of a repair workload's device inputs."""
+    return {"rk": synth.bits(inp["k_reuse"]), "rv": synth.bits(inp["v_reuse"]),
+            "fk": synth.bits(inp["k_fresh"]), "fv": synth.bits(inp["v_fresh"]),
+            "delta": inp["delta"].cpu().numpy()}
+
+
+def oracle_repair(oracle, cfg, h):
+    """The oracle's whole repair of every unit, K and V: check-layer scores, top-b probe
+    sets, probe means and correction of every layer.  Returns the scores (dk, dv)."""
+    cl = cfg.check_layer
+    dk = oracle.scores(h["rk"][:, cl], h["fk"][:, cl], h["delta"], cfg.agents, cfg.rope_base, True)
+    dv = oracle.scores(h["rv"][:, cl], h["fv"][:, cl], h["delta"], cfg.agents, cfg.rope_base, False)
+    ik = np.stack([oracle.topk(dk[u], cfg.b, True) for u in range(cfg.units)])
+    iv = np.stack([oracle.topk(dv[u], cfg.b, True) for u in range(cfg.units)])
+    oracle.mean_correct(h["rk"], h["fk"], h["delta"], cfg.agents, cfg.rope_base, True, ik, np.minimum(dk, 1.0))
+    oracle.mean_correct(h["rv"], h["fv"], h["delta"], cfg.agents, cfg.rope_base, False, iv, np.minimum(dv, 1.0))
+    return dk, dv
+
+
+def repair_cpu_baseline(cfg, h, min_seconds: float, one_thread: bool, what: str):
+    """The oracle on the host cores over the same host buffers: all threads, repeated for at
+    least min_seconds, plus (one_thread) a single-thread pass."""
     import oracle
     oracle.build()
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
-    L = cfg.layers if max_layers is None else min(cfg.layers, max_layers)
-    scfg = cfg.with_(layers=L)
-    reuse = synth.repair_reuse(scfg, dev)
-    rk, rv = synth.bits(reuse["k_reuse"]), synth.bits(reuse["v_reuse"])
-    delta = reuse["delta"].cpu().numpy()
-    res = synth.repair_residual(scfg, 0, dev)
-    fk = oracle.compose_fresh(rk, res["mu_k"][None].cpu().numpy(), res["xi_k"][None].cpu().numpy(), delta, 1,
-                              scfg.rope_base, True)
-    fv = oracle.compose_fresh(rv, res["mu_v"][None].cpu().numpy(), res["xi_v"][None].cpu().numpy(), delta, 1,
-                              scfg.rope_base, False)
-    del res, reuse
-    cl = scfg.check_layer
-    reps = 0
-    t0 = time.perf_counter()
-    while True:
-        dk = oracle.scores(rk[:, cl], fk[:, cl], delta, 1, scfg.rope_base, True)
-        dv = oracle.scores(rv[:, cl], fv[:, cl], delta, 1, scfg.rope_base, False)
-        ik = oracle.topk(dk[0], scfg.b, True)[None]
-        iv = oracle.topk(dv[0], scfg.b, True)[None]
-        oracle.mean_correct(rk, fk, delta, 1, scfg.rope_base, True, ik, np.minimum(dk, 1.0))
-        oracle.mean_correct(rv, fv, delta, 1, scfg.rope_base, False, iv, np.minimum(dv, 1.0))
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= min_seconds:
-            break
-    by = repair_bytes(scfg)
-    sec = el / reps
-    return {"value": round(by["corrected"] / sec / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": f"{cfg.name} chunk 0, layers 0..{L - 1} of {cfg.layers} (score + top-b + mean correction, "
-                      f"K and V), {reps} repetition(s), {sec:.3f} s each",
-            "seconds_per_step": round(sec, 4), "tokens_per_s": round(by["tokens"] / sec, 2)}
+    sec, reps = timed_reps(lambda: oracle_repair(oracle, cfg, h), min_seconds)
+    by = repair_bytes(cfg)
+    extra = {"seconds_per_step": round(sec, 5), "tokens_per_s": round(by["tokens"] / sec, 2)}
+    if one_thread:
+        sec1, _ = with_threads(oracle, 1, lambda: timed_reps(lambda: oracle_repair(oracle, cfg, h), 0.0, 1))
+        extra["one_thread"] = {"value": round(by["corrected"] / sec1 / 1e9, 4), "unit": "GB/s",
+                               "seconds_per_step": round(sec1, 4)}
+    return baseline_obj(oracle, round(by["corrected"] / sec / 1e9, 4), "GB/s",
+                        f"{what}: score + top-b + mean correction of every unit and layer, K and V, "
+                        f"{reps} repetition(s) of {sec:.4f} s", **extra)
+
+
+def repair_selection_report(cfg, sel, dk, dv):
+    """Probe sets of the GPU (sel) against the oracle's scores of the same inputs."""
+    rk = selection_agreement(sel["idx_k"].cpu().numpy(), dk, cfg.b, True)
+    rv = selection_agreement(sel["idx_v"].cpu().numpy(), dv, cfg.b, True)
+    gaps = [g for g in (rk["boundary_gap"], rv["boundary_gap"]) if g is not None]
+    return {"near_ties": rk["near_tie_swaps"] + rv["near_tie_swaps"],
+            "non_tie_mismatches": rk["non_tie_mismatches"] + rv["non_tie_mismatches"],
+            "boundary_gap": min(gaps) if gaps else None,
+            "sets_checked": 2 * cfg.units, "rule": "swaps accepted only below 1e-5 relative; "
+            "boundary_gap = smallest relative gap between the b-th and (b+1)-th oracle key"}
 
 
 def run_ours(args, world, rank, local):
@@ -619,10 +907,13 @@ def run_ours(args, world, rank, local):
     barrier(world)
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
-        step_ms, mc_ms = time_repair(kvfix, cfg, inp, args.steps, args.warmup, flush)
+        step_ms, mc_ms, sel = time_repair(kvfix, cfg, inp, args.steps, args.warmup, flush)
         torch.cuda.synchronize()
-    barrier(world)
+        barrier(world)
+        # after the timed region: the same step for >= 1 s, for the spread and the clocks
+        steady = time_steady(kvfix, cfg, inp, args.steady_seconds, flush)
     clocks = clk.summary()
+    clocks["window"] = "the timed steps, then the steady loop of the same step"
     ms = barrier_max(statistics.mean(step_ms), world)
     mc = barrier_max(statistics.mean(mc_ms), world)
     score_ms = statistics.mean(time_score(kvfix, cfg, inp, max(3, args.steps // 4), flush))
@@ -634,6 +925,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "step_ms_spread": [round(min(step_ms), 5), round(statistics.median(step_ms), 5), round(max(step_ms), 5)],
+        "steady": steady,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded draws: reuse ~ N(0,1); fresh = rerope(reuse) + mu + xi)",
         "config": repair_config(world),
@@ -653,19 +945,29 @@ def run_ours(args, world, rank, local):
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
+    host = host_repair_inputs(inp) if rank == 0 and world == 1 and not args.no_oracle else None
     del inp, fk, fv, reuse, flush
     torch.cuda.empty_cache()
     if not args.no_stages and rank == 0:
         stages = {}
-        for name, fn in (("collective_round", stage_round), ("diff", stage_diff), ("lowrank_draft", stage_lowrank),
-                         ("anchor", stage_anchor)):
+        for name, fn in (("tiny", stage_tiny), ("rerope", stage_rerope), ("collective_round", stage_round),
+                         ("diff", stage_diff), ("lowrank_draft", stage_lowrank), ("anchor", stage_anchor)):
             try:
-                stages[name] = fn(kvfix, peak)
+                stages[name] = fn(kvfix, peak, oracle_leg=not args.no_oracle)
             except Exception as exc:  # report, do not hide
                 stages[name] = {"error": f"{type(exc).__name__}: {exc}"}
         line["stages"] = stages
-    if rank == 0 and world == 1:
-        line["cpu_baseline"] = cpu_baseline(synth.REPAIR_LLAMA8B, min_seconds=10.0)
+    if host is not None:
+        # the oracle on host copies of the timed inputs: near ties of the probe sets, then
+        # its time on the host cores (all threads, and one thread)
+        import oracle
+        oracle.build()
+        cl = cfg.check_layer
+        dk = oracle.scores(host["rk"][:, cl], host["fk"][:, cl], host["delta"], cfg.agents, cfg.rope_base, True)
+        dv = oracle.scores(host["rv"][:, cl], host["fv"][:, cl], host["delta"], cfg.agents, cfg.rope_base, False)
+        line["selection"] = repair_selection_report(cfg, sel, dk, dv)
+        line["cpu_baseline"] = repair_cpu_baseline(cfg, host, args.oracle_seconds, True,
+                                                   f"{cfg.name}, the timed chunk (all 32 layers)")
     return line
 
 
@@ -678,28 +980,42 @@ def repair_config(world: int) -> dict:
 
 
 def run_reference(args, world, rank):
+    """The oracle as it stands, on the host cores: each step is its whole repair of the
+    benchmark's chunk (all 32 layers, K and V), on inputs drawn the way the GPU arm draws
+    them (fresh keys composed by the oracle itself, not by the library)."""
     if rank != 0:
         return None
+    import oracle
+    oracle.build()
     cfg = synth.REPAIR_LLAMA8B
-    # each step: the oracle on a bounded sample (4 of the 32 layers)
-    layers = 4
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    reuse = synth.repair_reuse(cfg, dev)
+    h = {"rk": synth.bits(reuse["k_reuse"]), "rv": synth.bits(reuse["v_reuse"]),
+         "delta": reuse["delta"].cpu().numpy()}
+    res = synth.repair_residual(cfg, 0, dev)
+    h["fk"] = oracle.compose_fresh(h["rk"], res["mu_k"][None].cpu().numpy(), res["xi_k"][None].cpu().numpy(),
+                                   h["delta"], 1, cfg.rope_base, True)
+    h["fv"] = oracle.compose_fresh(h["rv"], res["mu_v"][None].cpu().numpy(), res["xi_v"][None].cpu().numpy(),
+                                   h["delta"], 1, cfg.rope_base, False)
+    del res, reuse
     times = []
-    cb = None
     for s in range(args.warmup + args.steps):
-        cb = cpu_baseline(cfg, min_seconds=0.0, max_layers=layers)
+        t0 = time.perf_counter()
+        oracle_repair(oracle, cfg, h)
         if s >= args.warmup:
-            times.append(cb["seconds_per_step"])
+            times.append(time.perf_counter() - t0)
     sec = statistics.mean(times)
-    scfg = cfg.with_(layers=layers)
-    by = repair_bytes(scfg)
+    by = repair_bytes(cfg)
     value = by["corrected"] / sec / 1e9
+    cb = baseline_obj(oracle, round(value, 4), "GB/s",
+                      f"{cfg.name}: the whole chunk (32 layers, K and V), score + top-b + mean correction, "
+                      f"one step per repair, {args.steps} timed steps")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": repair_config(world),
+            "data": "synthetic", "config": repair_config(1),
             "tokens_per_s": round(by["tokens"] / sec, 2),
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cb["cores"], "kind": "oracle",
-                             "sample": cb["sample"]},
+            "cpu_baseline": cb,
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -721,7 +1037,7 @@ def compose_anchor_sources(cfg, inp):
 ANCHOR_FACTORS = ("a_c_k", "b_ct_k", "a_c_v", "b_ct_v", "a_d_k", "b_dt_k", "a_d_v", "b_dt_v")
 
 
-def stage_anchor(kvfix, peak, steps=5, warmup=3):
+def stage_anchor(kvfix, peak, steps=5, warmup=3, oracle_leg=True):
     cfg = synth.ANCHOR_8B
     inp = synth.anchor_inputs(cfg, "cuda")
     src = compose_anchor_sources(cfg, inp)
@@ -787,6 +1103,28 @@ def stage_anchor(kvfix, peak, steps=5, warmup=3):
            "correct": {"ms": round(cor, 4), "algorithmic_bytes": cor_bytes,
                        "GBps": round(cor_bytes / cor / 1e6, 1), "frac": round(cor_bytes / cor / 1e6 / peak, 4),
                        "tflops": round(4 * 2 * mac / cor / 1e9, 1)}}
+    if oracle_leg:
+        # the oracle's gate + weights + correction on segment 0, layers 0..1 (its double
+        # loops over V anchors x rank x features take minutes for the whole workload)
+        import oracle
+        oracle.build()
+        Ls = 2
+        xs = {p: synth.bits(src[p][0:1, :Ls]).reshape(1, Ls, n, F) for p in ("k", "v")}  # [C][L][n][F]
+        fs = {k_: synth.bits(inp[k_][0:1, :, :Ls]) for k_ in ANCHOR_FACTORS}  # [C][V][L]...
+        dn = inp["delta"][0:1].cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.anchor_gate(xs["v"], fs["a_c_v"], fs["b_ct_v"], n, tau=cfg.tau)
+        for p, rot in (("k", True), ("v", False)):
+            w_ = oracle.anchor_weights(xs[p], fs[f"a_c_{p}"], fs[f"b_ct_{p}"])
+            oracle.anchor_correct(xs[p], fs[f"a_d_{p}"], fs[f"b_dt_{p}"], w_, cfg.kv_heads, dn, cfg.rope_base, rot)
+        t_or = time.perf_counter() - t0
+        sample_bytes = cor_bytes * Ls / (L * C)
+        res["cpu_baseline"] = baseline_obj(
+            oracle, round(sample_bytes / t_or / 1e9, 4), "GB/s",
+            f"anchor_8b segment 0, layers 0..{Ls - 1} of {L}: gate, weights and correction of K and V "
+            f"(value = the one-pass call's algorithmic bytes, scaled to the sample, / time)",
+            seconds=round(t_or, 3))
+        del xs, fs
     del inp, src, fac, ok, ov, wk, wv, flush
     torch.cuda.empty_cache()
     return res
@@ -910,6 +1248,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-stages", action="store_true")
+    ap.add_argument("--no-oracle", action="store_true", help="skip the oracle legs (cpu_baseline, near ties)")
+    ap.add_argument("--oracle-seconds", type=float, default=5.0,
+                    help="minimum host time of the headline oracle baseline")
+    ap.add_argument("--steady-seconds", type=float, default=1.0,
+                    help="length of the untimed-for-value steady loop that follows the timed steps")
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
                     help="run a few launches of one stage on a reduced workload (for ncu) and exit")
     args = ap.parse_args()

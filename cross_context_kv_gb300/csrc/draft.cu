@@ -49,7 +49,8 @@ unsigned read_status_draft(cudaStream_t stream) {
 //               from TMEM), combined over the cluster through distributed shared memory
 //               in rank order; then each key's mass sum_q exp(z - max_q) / sum_q.
 // The per-key masses go to the workspace [unit][n]; a second kernel adds them over the
-// units of a chunk (layer-major, then head) in double and in a fixed order.
+// units of a chunk (layer-major, then head) in a fixed order as compensated float pairs
+// (about 48 significant bits), returned as doubles.
 constexpr int kDcCluster = 8;
 constexpr int kDcThreads = 192;
 constexpr int kDcStages = 3;

@@ -20,6 +20,8 @@
 //  - the first call on a device looks up the buffer's device address (with that device
 //    current), so make that first call before any stream capture begins.
 #include <cuda_runtime.h>
+#include <stdio.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -78,6 +80,12 @@ extern "C" kvfix_status kvfix_draft_rank_noalloc(const kvfix_bf16* k, kvfix_kv_d
     void* ws = nullptr;
     kvfix_status st = scratch_for_current_device(&ws);
     if (st != KVFIX_OK) return st;
-    return kvfix_draft_rank(k, desc, q, draft_steps, q_heads, layer_begin, k_rows, idx, scores,
-                            k_fresh, v_fresh, fresh_desc, k_io, v_io, ws, have, stream);
+    st = kvfix_draft_rank(k, desc, q, draft_steps, q_heads, layer_begin, k_rows, idx, scores, k_fresh,
+                          v_fresh, fresh_desc, k_io, v_io, ws, have, stream);
+    if (st != KVFIX_OK) {  // name this entry point in the message of the inner call's error
+        char inner[400];
+        snprintf(inner, sizeof inner, "%s", kvfix_last_error());
+        return fail(st, "kvfix_draft_rank_noalloc: %s", inner);
+    }
+    return KVFIX_OK;
 }

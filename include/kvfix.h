@@ -219,7 +219,9 @@ KVFIX_API kvfix_status kvfix_lowrank_apply(const kvfix_bf16* x, kvfix_kv_desc de
  * kv_heads <= 65535, 0 <= k_rows <= tokens.
  * Arithmetic: the logits are a bf16 tensor-core contraction (tcgen05) with float
  * accumulation kept in tensor memory; softmax statistics in float; per-unit masses in
- * float, summed over units in double.
+ * float, summed over the units of a chunk in a fixed order (layer-major, then head) as
+ * a compensated float pair (running sum plus its accumulated rounding errors, about 48
+ * significant bits), returned as the double hi + lo.
  */
 KVFIX_API size_t kvfix_draft_rank_workspace_bytes(kvfix_kv_desc desc, int32_t layer_begin);
 KVFIX_API kvfix_status kvfix_draft_rank(const kvfix_bf16* k, kvfix_kv_desc desc, const kvfix_bf16* q,

@@ -1,6 +1,8 @@
 """The benchmark's reference arm (the oracle timed on the host cores) keeps its JSON
 contract: the GPU arm's metric, unit and workload config, a cpu_baseline describing the
-run, and an end-to-end block with no host-device traffic."""
+run, and an end-to-end block with no host-device traffic.  Each of its steps is the
+oracle's repair of the whole declared chunk, so its time and token rate describe that
+workload."""
 import json
 import os
 import subprocess
@@ -22,3 +24,11 @@ def test_reference_arm_json_line():
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert cb["cpu_model"] and cb["nproc"] >= 1
+    # the value, the step time and the token rate all describe the whole 32-layer chunk
+    cfg = bench.synth.REPAIR_LLAMA8B
+    by = bench.repair_bytes(cfg)
+    sec = line["ms_per_step"] / 1e3
+    assert abs(line["tokens_per_s"] - cfg.tokens / sec) <= 1e-3 * line["tokens_per_s"] + 1.0
+    assert abs(line["value"] - by["corrected"] / sec / 1e9) <= 1e-3 * line["value"] + 1e-3
+    assert "32 layers" in cb["sample"]

@@ -202,3 +202,47 @@ def test_gate_correct_in_one_pass(cfg):
     g1 = kvfix().anchor_gate_correct(src["k"], src["v"], factors(inp), cfg.tokens, inp["delta"], cfg.rope_base)
     g2 = kvfix().anchor_gate_correct(src["k"], src["v"], factors(inp), cfg.tokens, inp["delta"], cfg.rope_base)
     assert torch.equal(g1[4], g2[4])                 # deterministic distances
+
+
+def test_persistent_kernels_walk_many_units():
+    """More (row tile, layer, plane, segment) units than SMs, so every CTA of the
+    persistent distance and apply kernels walks several units and skips rejected
+    segments: the outputs of the accepted segment equal a call on that segment alone,
+    bit for bit, and the rejected segment's outputs and weights keep their fill."""
+    cfg = synth.ANCHOR_8B.with_(name="anchor_many", segments=2, anchors=4, layers=4, tokens=4096, kv_heads=2,
+                                head_dim=128, rank=16, seed=64)
+    inp = synth.anchor_inputs(cfg, DEV)
+    src = compose(cfg, inp)
+    fac = factors(inp)
+    ref = [kvfix().anchor_correct(src["k"][c:c + 1], src["v"][c:c + 1], {k: v[c:c + 1] for k, v in fac.items()},
+                                  inp["delta"][c:c + 1], cfg.rope_base) for c in range(cfg.segments)]
+    ok = torch.full_like(src["k"], 7.0)
+    ov = torch.full_like(src["v"], 7.0)
+    wk = torch.full((cfg.segments, cfg.layers, cfg.tokens, cfg.anchors), -1.0, device=DEV)
+    wv = wk.clone()
+    accept = torch.tensor([1, 0], dtype=torch.int32, device=DEV)
+    kvfix().anchor_correct(src["k"], src["v"], fac, inp["delta"], cfg.rope_base, accept=accept, out_k=ok, out_v=ov,
+                           w_k=wk, w_v=wv)
+    kvfix().check_status()
+    assert torch.equal(ok[0].view(torch.int16), ref[0][0][0].view(torch.int16))
+    assert torch.equal(ov[0].view(torch.int16), ref[0][1][0].view(torch.int16))
+    assert torch.equal(wk[0], ref[0][2][0]) and torch.equal(wv[0], ref[0][3][0])
+    assert (ok[1] == 7.0).all() and (ov[1] == 7.0).all() and (wk[1] == -1.0).all() and (wv[1] == -1.0).all()
+    # the one-pass call with a threshold between the two segments' entropies: one passes
+    _, _, hbar, _ = kvfix().anchor_gate(src["v"], inp["a_c_v"], inp["b_ct_v"], cfg.tokens, tau=cfg.tau)
+    h = hbar.cpu().numpy()
+    assert h[0] != h[1]
+    tau = float((h[0] + h[1]) / 2)
+    ok2 = torch.full_like(src["k"], 3.0)
+    ov2 = torch.full_like(src["v"], 3.0)
+    res = kvfix().anchor_gate_correct(src["k"], src["v"], fac, cfg.tokens, inp["delta"], cfg.rope_base, tau=tau,
+                                      out_k=ok2, out_v=ov2)
+    kvfix().check_status()
+    acc = res[7].cpu().numpy().astype(bool)
+    assert acc.sum() == 1
+    for c in range(cfg.segments):
+        if acc[c]:
+            assert torch.equal(ok2[c].view(torch.int16), ref[c][0][0].view(torch.int16))
+            assert torch.equal(ov2[c].view(torch.int16), ref[c][1][0].view(torch.int16))
+        else:
+            assert (ok2[c] == 3.0).all() and (ov2[c] == 3.0).all()

@@ -53,6 +53,51 @@ def test_noalloc_matches_draft_rank_on_consecutive_calls():
         assert torch.equal(got_v.view(torch.int16), ref_v.view(torch.int16))
 
 
+def test_noalloc_allocates_nothing():
+    """Once the outputs exist and a first call has looked up the buffer (and loaded the
+    kernels), a further call changes neither the device's free memory nor the memory
+    torch's allocator holds."""
+    from cross_context_kv_gb300 import kvfix
+    cfg = CASES[1]
+    inp = synth.lowrank_inputs(cfg, DEV)
+    k_io, v_io = inp["x_k"].clone(), inp["x_v"].clone()
+    d = kvfix.plane_desc(inp["x_k"])
+    idx = torch.empty((d.chunks, cfg.k_rows), dtype=torch.int32, device=DEV)
+    scores = torch.empty((d.chunks, d.tokens), dtype=torch.float64, device=DEV)
+    p = kvfix._ptr
+
+    def call():
+        return kvfix.lib.kvfix_draft_rank_noalloc(p(inp["x_k"]), d, p(inp["q"]), int(inp["q"].shape[2]),
+                                                  int(inp["q"].shape[3]), cfg.layer_begin, cfg.k_rows, p(idx),
+                                                  p(scores), p(inp["fresh_k"]), p(inp["fresh_v"]), d, p(k_io),
+                                                  p(v_io), kvfix._stream(k_io))
+    assert call() == kvfix.OK, kvfix.lib.kvfix_last_error()
+    torch.cuda.synchronize()
+    free0, reserved0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_reserved()
+    for _ in range(2):
+        assert call() == kvfix.OK, kvfix.lib.kvfix_last_error()
+    torch.cuda.synchronize()
+    kvfix.check_status()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_reserved() == reserved0
+
+
+def test_noalloc_errors_name_the_entry_point():
+    """An argument error found by the draft-rank checks is reported under this entry
+    point's name."""
+    from cross_context_kv_gb300 import kvfix
+    cfg = CASES[0]
+    inp = synth.lowrank_inputs(cfg, DEV)
+    d = kvfix.plane_desc(inp["x_k"])
+    idx = torch.empty((d.chunks, 1), dtype=torch.int32, device=DEV)
+    scores = torch.empty((d.chunks, d.tokens), dtype=torch.float64, device=DEV)
+    p = kvfix._ptr
+    st = kvfix.lib.kvfix_draft_rank_noalloc(p(inp["x_k"]), d, p(inp["q"]), int(inp["q"].shape[2]), 7, 1, 1,
+                                            p(idx), p(scores), None, None, d, None, None, kvfix._stream(idx))
+    assert st == kvfix.EINVAL  # 7 query heads is no multiple of the KV heads
+    assert kvfix.lib.kvfix_last_error().startswith(b"kvfix_draft_rank_noalloc: ")
+
+
 def test_noalloc_rejects_problems_beyond_the_buffer():
     """A problem whose scratch exceeds the fixed buffer is refused before anything is
     read or launched, so the descriptor may describe more rows than the buffers hold."""
