@@ -353,6 +353,8 @@ def time_steady(kvfix, cfg, inp, seconds: float, flush):
     """The same step back to back for at least `seconds` of wall time, L2 flushed (untimed)
     between steps, each step bracketed by events: the spread of a long run, and a window
     long enough for the clock sampler."""
+    if seconds <= 0:
+        return None
     stream = torch.cuda.current_stream()
     out = {"k": torch.empty_like(inp["k_fresh"]), "v": torch.empty_like(inp["v_fresh"]),
            "mu_k": torch.empty(cfg.units, cfg.layers, cfg.kv_heads * cfg.head_dim, device="cuda"),
@@ -931,10 +933,10 @@ def run_ours(args, world, rank, local):
         "config": repair_config(world),
         "tokens_per_s": round(world * by["tokens"] / ms * 1e3, 1),
         "algorithmic_bytes_per_step": by["step"],
-        "roofline": {"bound": "hbm", "kernel": "mean_correct_kernel (kvfix_mean_correct: probe means + correction, K and V, one launch)",
+        "roofline": {"bound": "hbm", "kernel": "kvfix_mean_correct: probe_mean_kernel + mean_stream_kernel (probe means, then correction), K and V, one call",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": profiled_traffic("mean_correct_kernel_repair_llama8b.md"),
+                     "traffic": profiled_traffic("mean_correct_repair_llama8b.md"),
                      "peak_kind": peak_kind + " (copy bandwidth)",
                      "launch_ms": round(mc, 5), "algorithmic_bytes_per_launch": by["mean_correct"]},
         "step_roofline_frac": round(by["step"] / ms / 1e6 / peak, 4),
