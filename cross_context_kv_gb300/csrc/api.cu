@@ -105,7 +105,8 @@ kvfix_status kvfix_check_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "kvfix_check_status: stream synchronize");
     unsigned bits = read_status_repair(s) | read_status_diff(s) | read_status_draft(s) | read_status_lowrank(s) |
-                    read_status_anchor(s) | read_status_layout(s) | read_status_selftest(s);
+                    read_status_anchor(s) | read_status_layout(s) | read_status_selftest(s) |
+                    read_status_lowrank_draft(s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kvfix_check_status: status read");
     if (bits & 8u) return fail(KVFIX_EDEVICE, "a kernel's shared-memory layout check failed; its work was skipped");
@@ -321,6 +322,74 @@ kvfix_status kvfix_draft_rank(const kvfix_bf16* k, kvfix_kv_desc desc, const kvf
     if (v_io) {
         if ((e = launch_row_repair(v_io, desc, v_fresh, fresh_desc, idx, k_rows, s)) != cudaSuccess) return cuda_fail(e, fn);
     }
+    return KVFIX_OK;
+}
+
+size_t kvfix_lowrank_draft_workspace_bytes(kvfix_kv_desc desc, int32_t layer_begin) {
+    return lowrank_draft_workspace_bytes(desc, layer_begin);
+}
+
+kvfix_status kvfix_lowrank_draft(const kvfix_bf16* x, kvfix_kv_desc desc, const kvfix_bf16* A, const kvfix_bf16* B,
+                                 int32_t rank, kvfix_bf16* out, kvfix_kv_desc out_desc, const kvfix_bf16* q,
+                                 int32_t draft_steps, int32_t q_heads, int32_t layer_begin, int32_t k_rows,
+                                 int32_t* idx, double* scores, const kvfix_bf16* k_fresh, const kvfix_bf16* v_fresh,
+                                 kvfix_kv_desc fresh_desc, kvfix_bf16* v_io, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+    const char* fn = "kvfix_lowrank_draft";
+    kvfix_status st;
+    // the low-rank part: the checks of kvfix_lowrank_apply
+    if ((st = check_plane(x, desc, "kvfix_lowrank_draft: x")) != KVFIX_OK) return st;
+    if ((st = check_plane(out, out_desc, "kvfix_lowrank_draft: out")) != KVFIX_OK) return st;
+    if (!same_shape(desc, out_desc) || desc.chunks != out_desc.chunks)
+        return fail(KVFIX_EINVAL, "%s: x and out shapes differ", fn);
+    if (!A || !B) return fail(KVFIX_EINVAL, "%s: A and B are required", fn);
+    if (!aligned16(A) || !aligned16(B)) return fail(KVFIX_EINVAL, "%s: A and B must be 16-byte aligned", fn);
+    if (rank != 16 && rank != 32 && rank != 64) return fail(KVFIX_EINVAL, "%s: rank must be 16, 32 or 64", fn);
+    if (desc.tokens > 0 && ((long long)desc.chunks * desc.layers * desc.kv_heads * desc.tokens >= (1ll << 31)))
+        return fail(KVFIX_EINVAL, "%s: at most 2^31 factor rows", fn);
+    if (desc.head_dim != 64 && desc.head_dim != 128) return fail(KVFIX_EINVAL, "%s: head_dim must be 64 or 128", fn);
+    const bool in_place = (const void*)x == (const void*)out && same_desc(desc, out_desc);
+    if (!in_place && overlaps(x, desc, out, out_desc))
+        return fail(KVFIX_EINVAL, "%s: out overlaps x (only an exact in-place call is allowed)", fn);
+    const size_t na = 2 * (size_t)desc.chunks * desc.layers * desc.kv_heads * desc.tokens * rank;
+    const size_t nb = 2 * (size_t)desc.chunks * desc.layers * desc.kv_heads * rank * desc.head_dim;
+    uintptr_t o0, o1;
+    extent(out, out_desc, &o0, &o1);
+    if (overlaps_bytes((const void*)o0, o1 - o0, A, na) || overlaps_bytes((const void*)o0, o1 - o0, B, nb))
+        return fail(KVFIX_EINVAL, "%s: out overlaps A or B", fn);
+    // the draft part: the checks of kvfix_draft_rank, on the corrected plane
+    if (!q || !aligned16(q)) return fail(KVFIX_EINVAL, "%s: q must be a 16-byte aligned device pointer", fn);
+    if (draft_steps < 1 || q_heads < 1 || q_heads % desc.kv_heads)
+        return fail(KVFIX_EINVAL, "%s: q_heads must be a positive multiple of kv_heads, draft_steps >= 1", fn);
+    if ((q_heads / desc.kv_heads) * draft_steps > 16)
+        return fail(KVFIX_EINVAL, "%s: (q_heads/kv_heads)*draft_steps must be <= 16", fn);
+    if (layer_begin < 0 || layer_begin > desc.layers) return fail(KVFIX_EINVAL, "%s: layer_begin out of range", fn);
+    if (desc.tokens > 16384 || desc.chunks > 65535) return fail(KVFIX_EINVAL, "%s: tokens <= 16384, chunks <= 65535", fn);
+    if (k_rows < 0 || k_rows > desc.tokens) return fail(KVFIX_EINVAL, "%s: k_rows must lie in [0, tokens]", fn);
+    if (!scores || (k_rows > 0 && !idx)) return fail(KVFIX_EINVAL, "%s: scores and idx are required", fn);
+    if (!workspace || workspace_bytes < lowrank_draft_workspace_bytes(desc, layer_begin))
+        return fail(KVFIX_EINVAL, "%s: workspace smaller than kvfix_lowrank_draft_workspace_bytes()", fn);
+    if (!aligned16(workspace)) return fail(KVFIX_EINVAL, "%s: workspace not 16-byte aligned", fn);
+    if (k_fresh || v_io || v_fresh) {
+        if (v_io && !v_fresh) return fail(KVFIX_EINVAL, "%s: v_io needs v_fresh", fn);
+        if (k_fresh && (st = check_plane(k_fresh, fresh_desc, "kvfix_lowrank_draft: k_fresh")) != KVFIX_OK) return st;
+        if (v_fresh && (st = check_plane(v_fresh, fresh_desc, "kvfix_lowrank_draft: v_fresh")) != KVFIX_OK) return st;
+        if (v_io && (st = check_plane(v_io, out_desc, "kvfix_lowrank_draft: v_io")) != KVFIX_OK) return st;
+        if (!same_shape(desc, fresh_desc) || fresh_desc.chunks != desc.chunks)
+            return fail(KVFIX_EINVAL, "%s: fresh_desc must match desc", fn);
+        if (k_fresh && overlaps(out, out_desc, k_fresh, fresh_desc)) return fail(KVFIX_EINVAL, "%s: out overlaps k_fresh", fn);
+        if (v_io && overlaps(out, out_desc, v_io, out_desc)) return fail(KVFIX_EINVAL, "%s: v_io overlaps out", fn);
+    }
+    if (workspace && overlaps_bytes(workspace, workspace_bytes, (const void*)o0, o1 - o0))
+        return fail(KVFIX_EINVAL, "%s: workspace overlaps out", fn);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_lowrank_draft(x, desc, A, B, rank, out, out_desc, q, draft_steps, q_heads, layer_begin,
+                                         k_rows, idx, scores, workspace, s);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    if (k_fresh && (e = launch_row_repair(out, out_desc, k_fresh, fresh_desc, idx, k_rows, s)) != cudaSuccess)
+        return cuda_fail(e, fn);
+    if (v_io && (e = launch_row_repair(v_io, out_desc, v_fresh, fresh_desc, idx, k_rows, s)) != cudaSuccess)
+        return cuda_fail(e, fn);
     return KVFIX_OK;
 }
 

@@ -22,6 +22,7 @@
 
 #include <cooperative_groups.h>
 
+#include "softmax.cuh"
 #include "tc.cuh"
 
 namespace cg = cooperative_groups;
@@ -195,16 +196,20 @@ draft_cluster_kernel(const __grid_constant__ CUtensorMap tm_k, DcArgs args) {
         }
     } else {
         // ------------------------------------------------------------ softmax
+        // one pass over the CTA's logits, tile by tile: per query row the running maximum
+        // and rescaled sum (softmax.cuh); then the warp's and the CTA's pairs
         const int wq = warp & 3, ew = warp - 2;
         const int key_in_tile = 32 * wq + lane;
         const float scale = rsqrtf((float)D) * kLog2e;  // logits in base-2 units
         const bool ok = mbar_wait(&done, 0u);
         if (!ok) atomicOr(&abort_flag, 1);
         tc_fence_after();
-        const int G = args.G;
-        float mx[kDcQ];
+        float mx[kDcQ], sm[kDcQ];
 #pragma unroll
-        for (int q = 0; q < kDcQ; ++q) mx[q] = -INFINITY;
+        for (int q = 0; q < kDcQ; ++q) {
+            mx[q] = -INFINITY;
+            sm[q] = 0.f;
+        }
         for (int i = 0; i < ntiles && ok; ++i) {
             const int key = (tile0 + i) * kDcRows + key_in_tile;
             uint32_t v[16];
@@ -212,50 +217,24 @@ draft_cluster_kernel(const __grid_constant__ CUtensorMap tm_k, DcArgs args) {
             tmem_wait_ld();
             if (key < n) {
 #pragma unroll
-                for (int q = 0; q < kDcQ; ++q) mx[q] = fmaxf(mx[q], __uint_as_float(v[q]) * scale);
+                for (int q = 0; q < kDcQ; ++q) online_add(mx[q], sm[q], __uint_as_float(v[q]) * scale);
             }
         }
 #pragma unroll
-        for (int q = 0; q < kDcQ; ++q) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], o));
-        }
+        for (int q = 0; q < kDcQ; ++q) warp_combine(mx[q], sm[q]);
         if (lane == 0)
 #pragma unroll
-            for (int q = 0; q < kDcQ; ++q) red_m[ew][q] = mx[q];
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (threadIdx.x - 64 < kDcQ) {
-            const int q = threadIdx.x - 64;
-            cta_m[q] = fmaxf(fmaxf(red_m[0][q], red_m[1][q]), fmaxf(red_m[2][q], red_m[3][q]));
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        float sm[kDcQ];
-#pragma unroll
-        for (int q = 0; q < kDcQ; ++q) sm[q] = 0.f;
-        for (int i = 0; i < ntiles && ok; ++i) {
-            const int key = (tile0 + i) * kDcRows + key_in_tile;
-            uint32_t v[16];
-            tmem_ld16(tmem + ((uint32_t)(32 * wq) << 16) + kDcQ * i, v);
-            tmem_wait_ld();
-            if (key < n) {
-#pragma unroll
-                for (int q = 0; q < kDcQ; ++q) sm[q] += exp2f(__uint_as_float(v[q]) * scale - cta_m[q]);
+            for (int q = 0; q < kDcQ; ++q) {
+                red_m[ew][q] = mx[q];
+                red_s[ew][q] = sm[q];
             }
-        }
-#pragma unroll
-        for (int q = 0; q < kDcQ; ++q) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) sm[q] += __shfl_xor_sync(0xffffffffu, sm[q], o);
-        }
-        if (lane == 0)
-#pragma unroll
-            for (int q = 0; q < kDcQ; ++q) red_s[ew][q] = sm[q];
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (threadIdx.x - 64 < kDcQ) {
             const int q = threadIdx.x - 64;
-            cta_s[q] = ((red_s[0][q] + red_s[1][q]) + red_s[2][q]) + red_s[3][q];
+            const float m4[4] = {red_m[0][q], red_m[1][q], red_m[2][q], red_m[3][q]};
+            const float s4[4] = {red_s[0][q], red_s[1][q], red_s[2][q], red_s[3][q]};
+            combine4(m4, s4, cta_m[q], cta_s[q]);
         }
-        (void)G;
     }
     // ---------------- cluster: combine the 8 CTAs' (max, sum) in rank order
     cluster.sync();
@@ -479,6 +458,29 @@ static cudaError_t encode_keys(CUtensorMap* map, const uint16_t* base, const Pla
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t launch_draft_finish(const float* contrib, int chunks, int n, long long units_per_chunk, int k_rows,
+                                int32_t* idx, double* scores, cudaStream_t s) {
+    cudaError_t e;
+    if (chunks == 0 || n == 0) return cudaSuccess;
+    if (units_per_chunk == 0) {
+        e = cudaMemsetAsync(scores, 0, sizeof(double) * (size_t)chunks * n, s);
+        if (e != cudaSuccess) return e;
+    } else {
+        dim3 g3((n + kAccThreads - 1) / kAccThreads, chunks);
+        draft_accum_kernel<<<g3, kAccThreads, 0, s>>>(contrib, n, units_per_chunk, scores);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (k_rows > 0) {
+        const int words = (n + 31) / 32;
+        size_t smem = ((sizeof(uint32_t) * words + 15) / 16) * 16 + (n <= kSelSmemKeys2 ? sizeof(unsigned long long) * n : 0);
+        e = cudaFuncSetAttribute(select_f64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        select_f64_kernel<<<chunks, kSelThreads2, smem, s>>>(scores, n, k_rows, idx);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_draft(const uint16_t* k, const kvfix_kv_desc& d, const uint16_t* q, int steps,
                          int q_heads, int layer_begin, int k_rows, int32_t* idx, double* scores,
                          void* ws_ptr, cudaStream_t s) {
@@ -489,10 +491,7 @@ cudaError_t launch_draft(const uint16_t* k, const kvfix_kv_desc& d, const uint16
     const long long units = units_per_chunk * p.chunks;
     cudaError_t e;
     if (p.chunks == 0 || n == 0) return cudaSuccess;
-    if (units == 0) {
-        e = cudaMemsetAsync(scores, 0, sizeof(double) * (size_t)p.chunks * n, s);
-        if (e != cudaSuccess) return e;
-    } else {
+    if (units > 0) {
         if (units > 65535) return cudaErrorInvalidValue;
         CUtensorMap tk;
         if ((e = encode_keys(&tk, k, p)) != cudaSuccess) return e;
@@ -522,19 +521,8 @@ cudaError_t launch_draft(const uint16_t* k, const kvfix_kv_desc& d, const uint16
             draft_cluster_kernel<64><<<grid, kDcThreads, DcCfg<64>::kSmem, s>>>(tk, a);
         }
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        dim3 g3((n + kAccThreads - 1) / kAccThreads, p.chunks);
-        draft_accum_kernel<<<g3, kAccThreads, 0, s>>>(a.contrib, n, units_per_chunk, scores);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if (k_rows > 0) {
-        const int words = (n + 31) / 32;
-        size_t smem = ((sizeof(uint32_t) * words + 15) / 16) * 16 + (n <= kSelSmemKeys2 ? sizeof(unsigned long long) * n : 0);
-        e = cudaFuncSetAttribute(select_f64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        select_f64_kernel<<<p.chunks, kSelThreads2, smem, s>>>(scores, n, k_rows, idx);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    return launch_draft_finish(static_cast<const float*>(ws_ptr), p.chunks, n, units_per_chunk, k_rows, idx, scores, s);
 }
 
 // ---- 4. row repair: grid = (ceil(k/16), L, C) ----------------------------------------

@@ -27,6 +27,7 @@ unsigned read_status_repair(cudaStream_t stream);
 unsigned read_status_diff(cudaStream_t stream);
 unsigned read_status_draft(cudaStream_t stream);
 unsigned read_status_lowrank(cudaStream_t stream);
+unsigned read_status_lowrank_draft(cudaStream_t stream);
 
 // ---- launchers (enqueue only; arguments already validated) -----------------------
 
@@ -68,6 +69,20 @@ size_t draft_workspace_bytes(const kvfix_kv_desc& d, int layer_begin);
 cudaError_t launch_draft(const uint16_t* k, const kvfix_kv_desc& d, const uint16_t* q,
                          int steps, int q_heads, int layer_begin, int k_rows, int32_t* idx,
                          double* scores, void* ws, cudaStream_t s);
+// The draft-rank tail shared by the fused low-rank call: the per-key masses of each
+// chunk's units (contrib [chunks][units_per_chunk][n]) summed into scores, then the top
+// k_rows of each chunk.
+cudaError_t launch_draft_finish(const float* contrib, int chunks, int n, long long units_per_chunk, int k_rows,
+                                int32_t* idx, double* scores, cudaStream_t s);
+// Low-rank delta of the key plane fused with the draft scoring of the corrected keys:
+// out = x + A B (every layer), and for layers >= layer_begin the per-key attention
+// masses of the draft queries into contrib (as launch_draft's first stage); then the
+// draft-rank tail.
+size_t lowrank_draft_workspace_bytes(const kvfix_kv_desc& d, int layer_begin);
+cudaError_t launch_lowrank_draft(const uint16_t* x, const kvfix_kv_desc& d, const uint16_t* A, const uint16_t* B,
+                                 int rank, uint16_t* out, const kvfix_kv_desc& od, const uint16_t* q, int steps,
+                                 int q_heads, int layer_begin, int k_rows, int32_t* idx, double* scores, void* ws,
+                                 cudaStream_t s);
 // Rows idx[c][0 .. k_rows) (or the first counts[c] of them, counts non-null) of io are
 // overwritten with the same rows of fresh, every layer and head.
 cudaError_t launch_row_repair(uint16_t* io, const kvfix_kv_desc& d, const uint16_t* fresh,

@@ -48,6 +48,8 @@ SIGNATURES = {
     "kvfix_draft_rank_workspace_bytes": (SZ, [D, I32]),
     "kvfix_draft_rank": (ctypes.c_int, [P, D, P, I32, I32, I32, I32, P, P, P, P, D, P, P, P, SZ, P]),
     "kvfix_draft_rank_noalloc": (ctypes.c_int, [P, D, P, I32, I32, I32, I32, P, P, P, P, D, P, P, P]),
+    "kvfix_lowrank_draft_workspace_bytes": (SZ, [D, I32]),
+    "kvfix_lowrank_draft": (ctypes.c_int, [P, D, P, P, I32, P, D, P, I32, I32, I32, I32, P, P, P, P, D, P, P, SZ, P]),
     "kvfix_diff_encode": (ctypes.c_int, [P, P, D, P, P, D, I32, P, P, P, I64, P, P]),
     "kvfix_diff_gather": (ctypes.c_int, [P, P, D, P, P, P, I64, I32, I32, P, P, D, P]),
     "kvfix_diff_restore": (ctypes.c_int, [P, P, D, P, P, P, I64, I32, I32, P, F64, P, P, P, D, P]),
@@ -243,6 +245,37 @@ def draft_rank(k, q, layer_begin: int, k_rows: int, k_fresh=None, v_fresh=None, 
                                 int(k_rows), _ptr(idx), _ptr(scores), _ptr(k_fresh), _ptr(v_fresh), fd,
                                 _ptr(k_io), _ptr(v_io), _ptr(workspace), workspace.numel(), _stream(k)))
     return idx, scores
+
+
+def lowrank_draft_workspace_bytes(k, layer_begin: int) -> int:
+    return int(lib.kvfix_lowrank_draft_workspace_bytes(plane_desc(k), int(layer_begin)))
+
+
+def lowrank_draft(x, A, B, q, layer_begin: int, k_rows: int, out=None, k_fresh=None, v_fresh=None, v_io=None,
+                  workspace=None):
+    """out = x + A B (the key plane) and the draft ranking of out in one pass; with k_fresh
+    the selected rows of out, with v_fresh/v_io those of v_io, are overwritten.  x, out
+    [C][L][n][Hkv][D]; A [C][L][Hkv][n][r]; B [C][L][Hkv][r][D]; q [C][L][T][Hq][D].
+    Returns (out, idx, scores)."""
+    for t, nm in ((x, "x"), (A, "A"), (B, "B"), (q, "q")):
+        _bf16(t, nm)
+    if not (A.is_contiguous() and B.is_contiguous() and q.is_contiguous()):
+        raise ValueError("A, B and q must be contiguous")
+    out = torch.empty_like(x) if out is None else out
+    _bf16(out, "out")
+    d, od = plane_desc(x), plane_desc(out)
+    C, n = d.chunks, d.tokens
+    ws_bytes = lowrank_draft_workspace_bytes(out, layer_begin)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=x.device)
+    idx = torch.empty(C, max(k_rows, 0), dtype=torch.int32, device=x.device)
+    scores = torch.empty(C, n, dtype=torch.float64, device=x.device)
+    fd = plane_desc(k_fresh) if k_fresh is not None else (plane_desc(v_fresh) if v_fresh is not None else d)
+    _check(lib.kvfix_lowrank_draft(_ptr(x), d, _ptr(A), _ptr(B), int(A.shape[-1]), _ptr(out), od, _ptr(q),
+                                   int(q.shape[2]), int(q.shape[3]), int(layer_begin), int(k_rows), _ptr(idx),
+                                   _ptr(scores), _ptr(k_fresh), _ptr(v_fresh), fd, _ptr(v_io), _ptr(workspace),
+                                   workspace.numel(), _stream(x)))
+    return out, idx, scores
 
 
 def diff_encode(master_k, master_v, sib_k, sib_v, block_tokens: int, capacity: int | None = None,

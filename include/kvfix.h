@@ -232,6 +232,42 @@ KVFIX_API kvfix_status kvfix_draft_rank(const kvfix_bf16* k, kvfix_kv_desc desc,
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * kvfix_lowrank_draft -- kvfix_lowrank_apply of the key plane and kvfix_draft_rank of the
+ * corrected keys in one pass: each corrected key tile is scored while it is still on chip,
+ * so the corrected keys are read from memory by neither step.
+ * [KVCMAS] Eq. 4, 7, 8 (corrected keys = reference keys + A B); [BCR] section 3 ("The
+ * repair": rows ranked by the draft queries' attention mass over the predicted keys) and
+ * App. B Algorithms 1 and 2.
+ *
+ * Computes exactly what these calls compute, in this order:
+ *     kvfix_lowrank_apply(x, desc, A, B, rank, out, out_desc)
+ *     kvfix_draft_rank(out, out_desc, q, draft_steps, q_heads, layer_begin, k_rows, idx,
+ *                      scores, k_fresh, v_fresh, fresh_desc, k_fresh ? out : NULL, v_io)
+ * with the same bits: out, idx and scores equal the two-call sequence's.  The value
+ * plane's low-rank delta is a separate kvfix_lowrank_apply (give its output as v_io to
+ * repair its rows here).
+ * Arguments are those of the two calls: x/out/A/B/rank as for kvfix_lowrank_apply (out may
+ * be x itself, in place); q, draft_steps, q_heads, layer_begin, k_rows, idx and scores as
+ * for kvfix_draft_rank.  workspace: device buffer of
+ * kvfix_lowrank_draft_workspace_bytes(desc, layer_begin) bytes (16-byte aligned; the
+ * draft workspace plus a fixed 132 KB exchange area), contents irrelevant on entry.  k_fresh (optional): the selected rows of out are overwritten with it;
+ * v_fresh with v_io (optional): the selected rows of v_io (shaped like out) are
+ * overwritten with it.  Limits: head_dim 64 or 128, rank 16/32/64, tokens <= 16384,
+ * (q_heads/kv_heads)*draft_steps <= 16.
+ * Runs as one persistent cooperative kernel (one CTA per SM, all of its tensor memory;
+ * it fails with KVFIX_ECUDA if the device cannot hold one CTA on each SM it uses), then
+ * the per-key sums, the top-k and the row repair.
+ */
+KVFIX_API size_t kvfix_lowrank_draft_workspace_bytes(kvfix_kv_desc desc, int32_t layer_begin);
+KVFIX_API kvfix_status kvfix_lowrank_draft(const kvfix_bf16* x, kvfix_kv_desc desc, const kvfix_bf16* A,
+                                           const kvfix_bf16* B, int32_t rank, kvfix_bf16* out,
+                                           kvfix_kv_desc out_desc, const kvfix_bf16* q, int32_t draft_steps,
+                                           int32_t q_heads, int32_t layer_begin, int32_t k_rows, int32_t* idx,
+                                           double* scores, const kvfix_bf16* k_fresh, const kvfix_bf16* v_fresh,
+                                           kvfix_kv_desc fresh_desc, kvfix_bf16* v_io, void* workspace,
+                                           size_t workspace_bytes, void* stream);
+
+/*
  * kvfix_draft_rank_noalloc -- kvfix_draft_rank for callers that cannot allocate device
  * memory.  The pages have no counterpart: this is a service of this library only.
  *

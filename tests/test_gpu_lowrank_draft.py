@@ -126,3 +126,76 @@ def test_full_size_lowrank_draft_parity():
         a = synth.bits(inp["a_k"][c:c + 1][:, :, :, rows])
         ref = oracle.lowrank_apply(xs, a, synth.bits(inp["b_k"][c:c + 1]))
         assert_close_kv(synth.bits(kt[c:c + 1, :, rows]), ref, f"K~ chunk {c} sampled rows")
+
+
+# ------------------------------------------------------------------ fused low-rank + draft
+
+FUSED = SMALL_LR + [
+    # more (chunk, layer, head) units than resident clusters: each cluster walks several,
+    # with the B/query buffers and the logits columns reused
+    synth.LOWRANK_70B.with_(name="fused_many_units", chunks=2, layers=6, tokens=2100, kv_heads=4, q_heads=32,
+                            seed=43),
+    synth.LOWRANK_70B.with_(name="fused_layer_begin0", chunks=1, layers=3, tokens=640, kv_heads=2, q_heads=16,
+                            layer_begin=0, seed=44),
+]
+
+
+@pytest.mark.parametrize("cfg", FUSED, ids=lambda c: c.name)
+def test_lowrank_draft_equals_the_two_calls(cfg):
+    """kvfix_lowrank_draft gives the bits of kvfix_lowrank_apply followed by
+    kvfix_draft_rank: corrected keys, scores, selection and repaired planes."""
+    inp = synth.lowrank_inputs(cfg, DEV)
+    kt = kvfix().lowrank_apply(inp["x_k"], inp["a_k"], inp["b_k"])
+    vt = kvfix().lowrank_apply(inp["x_v"], inp["a_v"], inp["b_v"])
+    plain = kt.clone()
+    ref_idx, ref_scores = kvfix().draft_rank(kt, inp["q"], cfg.layer_begin, cfg.k_rows, inp["fresh_k"],
+                                             inp["fresh_v"], kt, vt)
+    vt2 = kvfix().lowrank_apply(inp["x_v"], inp["a_v"], inp["b_v"])
+    out, idx, scores = kvfix().lowrank_draft(inp["x_k"], inp["a_k"], inp["b_k"], inp["q"], cfg.layer_begin,
+                                             cfg.k_rows, k_fresh=inp["fresh_k"], v_fresh=inp["fresh_v"], v_io=vt2)
+    kvfix().check_status()
+    assert torch.equal(scores, ref_scores)
+    assert torch.equal(idx, ref_idx)
+    assert torch.equal(out.view(torch.int16), kt.view(torch.int16))
+    assert torch.equal(vt2.view(torch.int16), vt.view(torch.int16))
+    # without the repair the output is the low-rank result itself; in place too
+    out2, idx2, scores2 = kvfix().lowrank_draft(inp["x_k"], inp["a_k"], inp["b_k"], inp["q"], cfg.layer_begin,
+                                                cfg.k_rows)
+    x3 = inp["x_k"].clone()
+    kvfix().lowrank_draft(x3, inp["a_k"], inp["b_k"], inp["q"], cfg.layer_begin, cfg.k_rows, out=x3)
+    kvfix().check_status()
+    assert torch.equal(out2.view(torch.int16), plain.view(torch.int16))
+    assert torch.equal(x3.view(torch.int16), plain.view(torch.int16))
+    assert torch.equal(scores2, ref_scores) and torch.equal(idx2, ref_idx)
+    # against the oracle: the scores of the fused call's keys and the selection
+    ref = oracle.draft_scores(synth.bits(out2), synth.bits(inp["q"]), cfg.layer_begin)
+    np.testing.assert_allclose(scores2.cpu().numpy(), ref, rtol=1e-5, atol=1e-9)
+    for c in range(cfg.chunks):
+        check_index_set(idx2[c].cpu().numpy(), oracle.topk(ref[c], cfg.k_rows, False), ref[c], f"{cfg.name} {c}")
+
+
+@pytest.mark.slow
+def test_full_size_lowrank_draft_fused_equals_two_calls():
+    """The 70B-shaped workload: the fused call equals the two-call sequence bit for bit
+    (both planes repaired), and chunk 0's scores and selection match the oracle's."""
+    cfg = synth.LOWRANK_70B
+    inp = synth.lowrank_inputs(cfg, DEV)
+    kt = kvfix().lowrank_apply(inp["x_k"], inp["a_k"], inp["b_k"])
+    vt = kvfix().lowrank_apply(inp["x_v"], inp["a_v"], inp["b_v"])
+    ref_idx, ref_scores = kvfix().draft_rank(kt, inp["q"], cfg.layer_begin, cfg.k_rows, inp["fresh_k"],
+                                             inp["fresh_v"], kt, vt)
+    kt2 = torch.empty_like(kt)
+    vt2 = kvfix().lowrank_apply(inp["x_v"], inp["a_v"], inp["b_v"])
+    _, idx, scores = kvfix().lowrank_draft(inp["x_k"], inp["a_k"], inp["b_k"], inp["q"], cfg.layer_begin, cfg.k_rows,
+                                           out=kt2, k_fresh=inp["fresh_k"], v_fresh=inp["fresh_v"], v_io=vt2)
+    kvfix().check_status()
+    assert torch.equal(scores, ref_scores) and torch.equal(idx, ref_idx)
+    assert torch.equal(kt2.view(torch.int16), kt.view(torch.int16))
+    assert torch.equal(vt2.view(torch.int16), vt.view(torch.int16))
+    del kt, vt, vt2, kt2
+    c = 0
+    ref_kt = oracle.lowrank_apply(synth.bits(inp["x_k"][c:c + 1]), synth.bits(inp["a_k"][c:c + 1]),
+                                  synth.bits(inp["b_k"][c:c + 1]))
+    ref_sc = oracle.draft_scores(ref_kt, synth.bits(inp["q"][c:c + 1]), cfg.layer_begin)[0]
+    np.testing.assert_allclose(scores[c].cpu().numpy(), ref_sc, rtol=1e-4)
+    check_index_set(idx[c].cpu().numpy(), oracle.topk(ref_sc, cfg.k_rows, False), ref_sc, "fused chunk 0")
