@@ -882,20 +882,23 @@ mean_stream_kernel(const __grid_constant__ McMaps maps, McArgs args) {
             mbar_wait(&full[k % kMsStages], (unsigned)(k / kMsStages) & 1u);
 }
 // =====================================================================================
-// Rounds of several agents: two kernels instead of the per-agent phases above.
+// Rounds of several agents: the same two steps with a fan-out stream.
 //   round_mean_kernel: one CTA per (unit, layer, plane) computes that unit's probe mean
 //     into the mean output, all units at once.  Warp g takes slots 4g..4g+3 and folds
 //     them into the group sum Q_g; the CTA adds Q_0..Q_7 in order -- the arithmetic of
-//     the cluster kernel, element for element.  Fresh probe rows are copied to the output.
+//     the one-agent probe-mean kernel, element for element.  Fresh probe rows are copied
+//     to the output.
 //   round_stream_kernel: one CTA per (row block, layer, plane, reused chunk, agent group)
-//     reads each reused row once and writes the corrected row of every agent of the
-//     group.  A thread is one (agent, quad pair): its rotation and mean stay in
-//     registers for the whole row block.
+//     reads each reused row once, through a 3-stage ring of bulk-copied 32 KB tiles with
+//     full/empty mbarriers, and writes the corrected row of every agent of the group.  A
+//     thread is one (agent, quad pair): its rotation and mean stay in registers for the
+//     whole row block.
 // =====================================================================================
 constexpr int kRmThreads = 256;
 constexpr int kRsThreads = 1024;
 constexpr int kRsRows = 128;  // rows per CTA of the stream kernel
 constexpr int kRsStages = 3;  // tiles of reused rows in flight per CTA
+constexpr int kRsTileBytes = 32768;  // a stage: 16 rows of an 8 x 128 row
 
 __global__ void __launch_bounds__(kRmThreads, 4) round_mean_kernel(McArgs args) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -928,13 +931,14 @@ __global__ void __launch_bounds__(kRmThreads, 4) round_mean_kernel(McArgs args) 
     }
     __syncthreads();
     const int32_t* S = args.idx[plane] + (long long)u * b;
+    const int grp = warp;  // warp g folds slots 4g..4g+3
     for (int pq = lane; pq < P; pq += 32) {
         const int h = pq / v8, v = pq % v8;
         const long long eo = (long long)h * D + 4 * v;
         float q0[4], q1[4];
 #pragma unroll
         for (int j4 = 0; j4 < kSlotsPerGroup; ++j4) {
-            const int s = warp * kSlotsPerGroup + j4;
+            const int s = grp * kSlotsPerGroup + j4;
             float fs0[4], fs1[4], xs0[4], xs1[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) fs0[k] = fs1[k] = xs0[k] = xs1[k] = 0.f;
@@ -985,7 +989,7 @@ __global__ void __launch_bounds__(kRmThreads, 4) round_mean_kernel(McArgs args) 
                 q1[k] = j4 == 0 ? p1 : q1[k] + p1;
             }
         }
-        float* Q = Qs + warp * HD + h * D + 4 * v;
+        float* Q = Qs + grp * HD + h * D + 4 * v;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             Q[k] = q0[k];
@@ -1004,6 +1008,8 @@ __global__ void __launch_bounds__(kRmThreads, 4) round_mean_kernel(McArgs args) 
 
 __global__ void __launch_bounds__(kRsThreads) round_stream_kernel(McArgs args, int tile_rows) {
     extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full[kRsStages], empty[kRsStages];
+    __shared__ int abort_flag;
     const int plane = blockIdx.y & 1, l = blockIdx.y >> 1;
     const uint16_t* reuse = args.reuse[plane];
     if (reuse == nullptr) return;
@@ -1016,7 +1022,7 @@ __global__ void __launch_bounds__(kRsThreads) round_stream_kernel(McArgs args, i
     const int D = rp.dim, half = D / 2, v8 = D / 8;
     const int HD = rp.heads * D, P = rp.heads * v8;
     const int b = args.b;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int t_lo = blockIdx.x * kRsRows, t_hi = min(n, t_lo + kRsRows);
     const int words = kRsRows / 32;
     const int TR = tile_rows;
@@ -1026,20 +1032,31 @@ __global__ void __launch_bounds__(kRsThreads) round_stream_kernel(McArgs args, i
     float* wts = reinterpret_cast<float*>(member + kAgentGroup * words);        // [ag][kRsRows]
     const bool keys = plane == 0;
     const int tiles = (t_hi - t_lo + TR - 1) / TR;
-    const int chunks_row = HD / 8;  // 16-byte pieces of a row
-    // every thread copies its 16-byte pieces of a tile; one commit group per tile
-    auto fetch = [&](int k) {
-        if (k < tiles) {
-            uint16_t* dst = ring + (size_t)(k % kRsStages) * TR * HD;
-            const int t0 = t_lo + k * TR, tt = min(TR, t_hi - t0);
-            for (int c = tid; c < tt * chunks_row; c += kRsThreads) {
-                const int q = c / chunks_row, o = (c % chunks_row) * 8;
-                cp_async16(dst + q * HD + o, reuse + rp.row(r, l, t0 + q) + o);
-            }
+    const bool rows_contig = rp.st == HD;
+    const unsigned row_bytes = (unsigned)HD * 2u;
+    int issued = 0;  // thread 0 only
+    // thread 0: bulk copies of tile k's reused rows into its stage, counted in bytes
+    auto issue = [&](int k) {
+        const int slot = k % kRsStages;
+        const int t0 = t_lo + k * TR, tt = min(TR, t_hi - t0);
+        uint16_t* dst = ring + (size_t)slot * TR * HD;
+        mbar_arrive_expect_tx(&full[slot], row_bytes * tt);
+        if (rows_contig) {
+            bulk_g2s(dst, reuse + rp.row(r, l, t0), row_bytes * tt, &full[slot]);
+        } else {
+            for (int q = 0; q < tt; ++q) bulk_g2s(dst + q * HD, reuse + rp.row(r, l, t0 + q), row_bytes, &full[slot]);
         }
-        cp_async_commit();
     };
-    for (int k = 0; k < kRsStages - 1; ++k) fetch(k);  // reused rows do not depend on the means
+    if (tid == 0) {
+        for (int q = 0; q < kRsStages; ++q) {
+            mbar_init(&full[q], 1);
+            mbar_init(&empty[q], kRsThreads / 32);
+        }
+        fence_mbar_init();
+        abort_flag = 0;
+        // reused rows depend on no kernel of the chain: the first tiles go out at once
+        for (; issued < min(kRsStages, tiles); ++issued) issue(issued);
+    }
     for (int i = tid; i < ag * half; i += kRsThreads) {
         const int a = i / half, e = i % half;
         const int dlt = args.delta[(a0 + a) * R + r];
@@ -1073,29 +1090,33 @@ __global__ void __launch_bounds__(kRsThreads) round_stream_kernel(McArgs args, i
     const int h = pq / v8, v = pq % v8;
     const int eo = h * D + 4 * v;
     const bool rot = keys && args.delta[min(u, args.agents * R - 1)] != 0;
-    // the same float-pair constants and arithmetic as the cluster kernel's phase 2
-    float2 c2[2], s2[2], ns2[2], m0[2], m1[2];
+    // the same float-pair constants and arithmetic as the one-agent stream kernel
+    McConst kc;
     if (active) {
         const float* mu_g = args.mu[plane] + ((long long)u * L + l) * HD + eo;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const float* ct = cs + a * half + 4 * v + 2 * q;
             const float* st = cs + (kAgentGroup + a) * half + 4 * v + 2 * q;
-            c2[q] = make_float2(ct[0], ct[1]);
-            s2[q] = make_float2(st[0], st[1]);
-            ns2[q] = make_float2(-s2[q].x, -s2[q].y);
-            m0[q] = make_float2(mu_g[2 * q], mu_g[2 * q + 1]);
-            m1[q] = make_float2(mu_g[half + 2 * q], mu_g[half + 2 * q + 1]);
+            kc.c2[q] = make_float2(ct[0], ct[1]);
+            kc.s2[q] = make_float2(st[0], st[1]);
+            kc.ns2[q] = make_float2(-st[0], -st[1]);
+            kc.m0[q] = make_float2(mu_g[2 * q], mu_g[2 * q + 1]);
+            kc.m1[q] = make_float2(mu_g[half + 2 * q], mu_g[half + 2 * q + 1]);
         }
     }
     const uint32_t* mem = member + a * words;
     const float* wb = wts + a * kRsRows;
     uint16_t* ob = out + op.row(u, l, 0) + eo;
     for (int k = 0; k < tiles; ++k) {
-        fetch(k + kRsStages - 1);
-        cp_async_wait<kRsStages - 1>();  // this thread's pieces of tile k have landed
-        __syncthreads();                 // ... and everyone's
-        const uint16_t* tb = ring + (size_t)(k % kRsStages) * TR * HD + eo;
+        const int slot = k % kRsStages;
+        const unsigned parity = (unsigned)(k / kRsStages) & 1u;
+        if (!mbar_wait(&full[slot], parity)) {
+            atomicOr(&g_status_repair, FLAG_TIMEOUT);
+            abort_flag = 1;
+        }
+        if (abort_flag) break;
+        const uint16_t* tb = ring + (size_t)slot * TR * HD + eo;
         const int t0 = t_lo + k * TR, tt = min(TR, t_hi - t0);
         if (active) {
             // probe bits of the tile's rows (TR <= 32: at most two bitmap words)
@@ -1106,47 +1127,30 @@ __global__ void __launch_bounds__(kRsThreads) round_stream_kernel(McArgs args, i
                 if ((tl0 & 31) + TR > 32) pbits |= (uint64_t)mem[(tl0 >> 5) + 1] << 32;
                 pbits >>= (tl0 & 31);
             }
-            const long long ostep = (long long)rpp * op.st;
             uint16_t* o = ob + (long long)(t0 + row_off) * op.st;
+            const long long ostep = (long long)rpp * op.st;
             for (int row = row_off; row < tt; row += rpp, o += ostep) {
                 if ((pbits >> row) & 1u) continue;  // probe row: written already
-                const uint2 lo_raw = *reinterpret_cast<const uint2*>(tb + row * HD);
-                const uint2 hi_raw = *reinterpret_cast<const uint2*>(tb + row * HD + half);
-                float2 x0[2], x1[2];
-                x0[0] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo_raw.x));
-                x0[1] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo_raw.y));
-                x1[0] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi_raw.x));
-                x1[1] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi_raw.y));
-                if (rot) {
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const float2 lo = __ffma2_rn(x0[q], c2[q], __fmul2_rn(x1[q], ns2[q]));
-                        const float2 hi = __ffma2_rn(x1[q], c2[q], __fmul2_rn(x0[q], s2[q]));
-                        x0[q] = lo;
-                        x1[q] = hi;
-                    }
-                }
-                if (b > 0) {
-                    const float wt = wb[tl0 + row];
-                    const float2 w2 = make_float2(wt, wt);
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        x0[q] = __ffma2_rn(w2, m0[q], x0[q]);
-                        x1[q] = __ffma2_rn(w2, m1[q], x1[q]);
-                    }
-                }
-                uint2 lo_out, hi_out;
-                *reinterpret_cast<__nv_bfloat162*>(&lo_out.x) = __float22bfloat162_rn(x0[0]);
-                *reinterpret_cast<__nv_bfloat162*>(&lo_out.y) = __float22bfloat162_rn(x0[1]);
-                *reinterpret_cast<__nv_bfloat162*>(&hi_out.x) = __float22bfloat162_rn(x1[0]);
-                *reinterpret_cast<__nv_bfloat162*>(&hi_out.y) = __float22bfloat162_rn(x1[1]);
-                st_stream2(reinterpret_cast<uint2*>(o), lo_out);
-                st_stream2(reinterpret_cast<uint2*>(o + half), hi_out);
+                correct_quad_pair(tb + row * HD, o, half, rot, b > 0, b > 0 ? wb[tl0 + row] : 0.f, kc);
             }
         }
-        __syncthreads();  // tile k's stage is refilled by the next iteration's fetch
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (tid == 0 && issued < tiles && !abort_flag) {
+            // the stage is free once every warp released it; then refill it
+            if (!mbar_wait(&empty[slot], parity)) {
+                atomicOr(&g_status_repair, FLAG_TIMEOUT);
+                abort_flag = 1;
+            } else {
+                issue(issued);
+                ++issued;
+            }
+        }
     }
-    cp_async_wait<0>();
+    __syncthreads();
+    if (abort_flag && tid == 0)  // a wait ran out: copies still in flight are waited for (bounded)
+        for (int k = max(0, issued - kRsStages); k < issued; ++k)
+            mbar_wait(&full[k % kRsStages], (unsigned)(k / kRsStages) & 1u);
 }
 
 cudaError_t launch_mean_correct(const McPlanes& pl, const kvfix_kv_desc& rd, const kvfix_kv_desc& fd,
@@ -1181,7 +1185,7 @@ cudaError_t launch_mean_correct(const McPlanes& pl, const kvfix_kv_desc& rd, con
                            mean_smem, s, a);
         if (e != cudaSuccess) return e;
         const int half = a.rp.dim / 2;
-        const int tile_rows = max(1, min(32, kMsTileBytes / (2 * HD)));
+        const int tile_rows = max(1, min(32, kRsTileBytes / (2 * HD)));
         const size_t stream_smem = (size_t)kRsStages * tile_rows * HD * 2 +
                                    sizeof(float) * (2 * kAgentGroup * half + kAgentGroup * kRsRows) +
                                    sizeof(uint32_t) * kAgentGroup * (kRsRows / 32);
