@@ -72,6 +72,7 @@ constexpr int kAdSlots = 4;           // tensor-memory accumulators of 128 colum
 constexpr int kAdMaxB = 16;           // Bt ring entries (one anchor's chunk each)
 constexpr int kAdMaxX = 4;            // x chunk buffers
 constexpr int kAdXBytes = kAnRows * kAdCols * 2;  // x chunk: two 64-feature boxes, 128-byte swizzle
+constexpr int kAdEpi = 256;           // epilogue threads
 
 enum { kAdWeights = 0, kAdGate = 1, kAdBoth = 2 };
 
@@ -107,6 +108,14 @@ struct AdCfg {
 // sums of (x - rec_v)^2.  MODE kAdBoth: the weights of both planes and, on the value
 // plane, the gate's per-tile sums from the same reconstructions (warp partials folded in
 // a fixed order).
+//
+// After an abort a producer waits (bounded) for the copies it armed last on each barrier
+// of a ring, so that no bulk copy is still writing shared memory when the CTA leaves;
+// item i of a ring of n one-arrival barriers is phase i / n of barrier i % n.
+__device__ __forceinline__ void drain_ring(uint64_t* ring, int n, int armed) {
+    for (int i = armed > n ? armed - n : 0; i < armed; ++i) mbar_wait(&ring[i % n], (unsigned)(i / n) & 1u);
+}
+
 template <int R, int MODE>
 __global__ void __launch_bounds__(kAdThreads, 1)
 anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CUtensorMap tm_x1,
@@ -116,10 +125,9 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
     using K = AdCfg<R>;
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t xfull[kAdMaxX], xempty[kAdMaxX], bfull[kAdMaxB], bempty[kAdMaxB], tfull[kAdSlots],
-        tempty[kAdSlots], afull, adone;
+        tempty[kAdSlots], afull, adone, mdrain;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
-    __shared__ float red[kAnRows][kAnMaxAnchors + 1];
     __shared__ float gsum[4][kAnMaxAnchors];
     __shared__ float gsq[8][kAnMaxAnchors];  // both mode: per epilogue warp, per anchor
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -127,6 +135,8 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
     unsigned char* asm_ = smem;                             // V A tiles
     unsigned char* xs = smem + V * K::kABytes;              // NX x chunks
     unsigned char* bs = xs + NX * kAdXBytes;                // Bt ring
+    float* accs = reinterpret_cast<float*>(bs + NB * K::kBBytes);  // [V][kAdEpi] row sums
+    float* gacc = accs + V * kAdEpi;  // both mode: [V][kAdEpi] row sums of squares (gate)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chunks = args.F / kAdCols;
     const int total = chunks * V;                           // (chunk, anchor) steps of a tile
@@ -158,6 +168,7 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
         }
         mbar_init(&afull, 1);
         mbar_init(&adone, 1);
+        mbar_init(&mdrain, 1);
         fence_mbar_init();
         abort_flag = 0;
     }
@@ -181,7 +192,7 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
             prefetch_tensormap(&tm_a1);
             prefetch_tensormap(&tm_b0);
             prefetch_tensormap(&tm_b1);
-            int it = 0;
+            int it = 0, an = 0, xn = 0;  // units and x chunks armed
             for (int w = blockIdx.x; w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
                 int tile, l, plane, c;
                 if (!unit_of(w, tile, l, plane, c)) continue;
@@ -196,6 +207,7 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
                 mbar_arrive_expect_tx(&afull, (unsigned)(V * K::kABytes));
                 for (int v = 0; v < V; ++v)
                     tma_load_2d(asm_ + v * K::kABytes, ma, 0, ((c * V + v) * args.L + l) * args.n + t0, &afull);
+                ++an;
                 bool ok = true;
                 for (int j = 0; j < chunks; ++j) {
                     const int jg = it * chunks + j, xi = jg % NX;
@@ -207,6 +219,7 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
                     for (int b = 0; b < 2; ++b)
                         tma_load_4d(xs + xi * kAdXBytes + b * (kAnRows * 128), mx, j * kAdCols + 64 * b, t0, l, c,
                                     &xfull[xi]);
+                    ++xn;
                 }
                 if (!ok) {
                     atomicOr(&abort_flag, 1);
@@ -214,35 +227,44 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
                 }
                 ++it;
             }
+            if (anchor_vload(&abort_flag)) {
+                drain_ring(&afull, 1, an);
+                drain_ring(xfull, NX, xn);
+            }
         } else if (lane == 1) {
-            int it = 0;
+            int bn = 0, e = 0;  // Bt tiles armed; ring slot of the next
+            unsigned ph = 0;     // phase parity of that slot's next fill
             for (int w = blockIdx.x; w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
                 int tile, l, plane, c;
                 if (!unit_of(w, tile, l, plane, c)) continue;
                 const CUtensorMap* mb = plane ? &tm_b1 : &tm_b0;
                 bool ok = true;
+                int j = 0, v = 0;
                 for (int q = 0; q < total && !anchor_vload(&abort_flag); ++q) {
-                    const int qg = it * total + q;
-                    const int j = q / V, v = q % V, e = qg % NB;
-                    if (qg >= NB && !mbar_wait(&bempty[e], (unsigned)(qg / NB - 1) & 1u)) {
+                    if (bn >= NB && !mbar_wait(&bempty[e], ph ^ 1u)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(&bfull[e], (unsigned)K::kBBytes);
                     tma_load_2d(bs + e * K::kBBytes, mb, 0, ((c * V + v) * args.L + l) * args.F + j * kAdCols, &bfull[e]);
+                    ++bn;
+                    if (++e == NB) e = 0, ph ^= 1u;
+                    if (++v == V) v = 0, ++j;
                 }
                 if (!ok) {
                     atomicOr(&abort_flag, 1);
                     break;
                 }
-                ++it;
             }
+            if (anchor_vload(&abort_flag)) drain_ring(bfull, NB, bn);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // (running ring slots and parities: no division in the per-step path)
         if (lane == 0) {
             constexpr uint32_t idesc = tc_idesc_bf16(kAnRows, kAdCols);
-            int it = 0;
+            int it = 0, qg = 0, e = 0;  // steps issued; Bt ring slot of the next
+            unsigned bph = 0;           // its fill's phase parity
             bool ok = true;
             for (int w = blockIdx.x; ok && w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
                 int tile, l, plane, c;
@@ -252,11 +274,11 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
                     break;
                 }
                 tc_fence_after();
-                for (int q = 0; q < total && !anchor_vload(&abort_flag); ++q) {
-                    const int qg = it * total + q;
-                    const int v = q % V, e = qg % NB, a = qg % kAdSlots;
-                    if ((qg >= kAdSlots && !mbar_wait(&tempty[a], (unsigned)(qg / kAdSlots - 1) & 1u)) ||
-                        !mbar_wait(&bfull[e], (unsigned)(qg / NB) & 1u)) {
+                int v = 0;
+                for (int q = 0; q < total && !anchor_vload(&abort_flag); ++q, ++qg) {
+                    const int a = qg & (kAdSlots - 1);
+                    if ((qg >= kAdSlots && !mbar_wait(&tempty[a], (unsigned)((qg / kAdSlots) & 1) ^ 1u)) ||
+                        !mbar_wait(&bfull[e], bph)) {
                         ok = false;
                         break;
                     }
@@ -269,37 +291,58 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
                     }
                     tc_commit(&bempty[e]);
                     tc_commit(&tfull[a]);
+                    if (++e == NB) e = 0, bph ^= 1u;
+                    if (++v == V) v = 0;
                 }
                 tc_commit(&adone);  // this unit's MMAs are done with the A tiles
                 ++it;
             }
             if (!ok) atomicOr(&abort_flag, 1);
+            // every MMA issued has completed before the tensor memory is released
+            tc_commit(&mdrain);
+            mbar_wait(&mdrain, 0u);
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        // Thread et holds row m's 64 features of the chunk in registers and accumulates its
+        // per-anchor sums in shared memory (accs[v][et], so that the anchor loop stays
+        // rolled: the unrolled form overflowed the instruction cache).  Each step is read
+        // from tensor memory in two 32-column halves: the second half is loaded while the
+        // first is folded, and the next step's first half while the second is folded.  The
+        // waits are made warp-uniform (the loads are warp-collective).
         const int ew = warp - 2;              // 0..7
         const int wq = warp & 3;              // TMEM lane quarter this warp may read
         const int half = ew >> 2;             // which 64 of the chunk's 128 features
         const int m = 32 * wq + lane;         // tile row of this thread
+        const int et = threadIdx.x - 64;      // 0..255; row m's other half is et ^ 128
+        const uint32_t tcol = tmem + ((uint32_t)(32 * wq) << 16) + 64 * half;
         bool ok = true;
         int it = 0;
         for (int w = blockIdx.x; w < units; w += gridDim.x) {
             int tile, l, plane, c;
             if (!unit_of(w, tile, l, plane, c)) continue;
-            // the previous unit's reads of red, gsum and gsq are done; leave together on abort
+            // the previous unit's reads of accs, gsum and gsq are done; leave together on abort
             if (bar_any<1, 256>(!ok || anchor_vload(&abort_flag))) break;
             const int t0 = tile * kAnRows;
             const bool row_ok = t0 + m < args.rows;
-            float acc[kAnMaxAnchors];
-#pragma unroll
-            for (int v = 0; v < kAnMaxAnchors; ++v) acc[v] = 0.f;
             const bool gate_too = MODE == kAdBoth && plane == 1;
             const bool gate_row = t0 + m < args.gate_rows;
-            if (gate_too && lane < kAnMaxAnchors) gsq[ew][lane] = 0.f;
-            __syncwarp();
+            for (int v = 0; v < V; ++v) accs[v * kAdEpi + et] = 0.f;
+            if (gate_too)
+                for (int v = 0; v < V; ++v) gacc[v * kAdEpi + et] = 0.f;
+            const int qbase = it * total;
+            uint32_t p[32], r[32];
+            if (__all_sync(0xffffffffu, mbar_wait(&tfull[qbase & (kAdSlots - 1)], (unsigned)(qbase / kAdSlots) & 1u))) {
+                tc_fence_after();
+                tmem_ld32(tcol + (qbase & (kAdSlots - 1)) * kAdCols, p);
+            } else {
+                ok = false;
+            }
+            const float2 neg = make_float2(-1.f, -1.f);
+            int qg = qbase;
             for (int j = 0; ok && j < chunks; ++j) {
                 const int jg = it * chunks + j, xi = jg % NX;
-                if (anchor_vload(&abort_flag) || !mbar_wait(&xfull[xi], (unsigned)(jg / NX) & 1u)) {
+                if (!__all_sync(0xffffffffu, !anchor_vload(&abort_flag) && mbar_wait(&xfull[xi], (unsigned)(jg / NX) & 1u))) {
                     ok = false;
                     break;
                 }
@@ -315,114 +358,133 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&xempty[xi]);  // x is in registers now
+#pragma unroll 1
+                for (int v = 0; v < V; ++v, ++qg) {
+                    const int a = qg & (kAdSlots - 1);
+                    tmem_wait_ld32(p);
+                    tmem_ld32(tcol + a * kAdCols + 32, r);
+                    // first half: features [0, 32) of this thread's 64
+                    float s0 = 0.f, s1 = 0.f;
+                    float2 q2 = make_float2(0.f, 0.f);
+                    if (MODE == kAdGate) {
 #pragma unroll
-                for (int v = 0; v < kAnMaxAnchors; ++v) {
-                    if (v >= V) break;
-                    const int qg = it * total + j * V + v, a = qg % kAdSlots;
-                    if (!mbar_wait(&tfull[a], (unsigned)(qg / kAdSlots) & 1u)) {
-                        ok = false;
-                        break;
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])),
+                                                        neg, x2[e]);
+                            q2 = __ffma2_rn(d, d, q2);
+                        }
+                    } else if (gate_too) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])),
+                                                        neg, x2[e]);
+                            s0 += fabsf(d.x) + fabsf(d.y);
+                            q2 = __ffma2_rn(d, d, q2);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])),
+                                                        neg, x2[e]);
+                            s0 += fabsf(d.x) + fabsf(d.y);
+                        }
                     }
-                    tc_fence_after();
-                    uint32_t r0[32], r1[32];
-                    const uint32_t tb = tmem + ((uint32_t)(32 * wq) << 16) + a * kAdCols + 64 * half;
-                    tmem_ld32(tb, r0);
-                    tmem_ld32(tb + 32, r1);
-                    tmem_wait_ld();
+                    tmem_wait_ld32(r);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&tempty[a]);
-                    const float2 neg = make_float2(-1.f, -1.f);
+                    // the next step's first half (also across the chunk boundary); p is zeroed
+                    // when there is none, so that its old value is dead here
+                    {
+                        const int qn = qg + 1, an = qn & (kAdSlots - 1);
+                        const bool more = qn < qbase + total;
+                        const bool got =
+                            more && __all_sync(0xffffffffu, mbar_wait(&tfull[an], (unsigned)(qn / kAdSlots) & 1u));
+                        if (got) {
+                            tc_fence_after();
+                            tmem_ld32(tcol + an * kAdCols, p);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) p[i] = 0u;
+                        }
+                        if (more && !got) ok = false;
+                    }
+                    // second half: features [32, 64)
+                    float* acc = accs + v * kAdEpi + et;
                     if (MODE == kAdGate) {
-                        float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
-                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(r0[2 * e]), __uint_as_float(r0[2 * e + 1])),
-                                                        neg, x2[e]);
-                            s2 = __ffma2_rn(d, d, s2);
-                        }
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(r1[2 * e]), __uint_as_float(r1[2 * e + 1])),
+                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])),
                                                         neg, x2[16 + e]);
-                            s2 = __ffma2_rn(d, d, s2);
+                            q2 = __ffma2_rn(d, d, q2);
                         }
-                        acc[v] += s2.x + s2.y;
-                    } else {
-                        float s0 = 0.f, s1 = 0.f;
-                        float2 q2 = make_float2(0.f, 0.f);
+                        *acc += q2.x + q2.y;
+                    } else if (gate_too) {
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
-                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(r0[2 * e]), __uint_as_float(r0[2 * e + 1])),
-                                                        neg, x2[e]);
-                            s0 += fabsf(d.x) + fabsf(d.y);
-                            if (MODE == kAdBoth && gate_too) q2 = __ffma2_rn(d, d, q2);
-                        }
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(r1[2 * e]), __uint_as_float(r1[2 * e + 1])),
+                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])),
                                                         neg, x2[16 + e]);
                             s1 += fabsf(d.x) + fabsf(d.y);
-                            if (MODE == kAdBoth && gate_too) q2 = __ffma2_rn(d, d, q2);
+                            q2 = __ffma2_rn(d, d, q2);
                         }
-                        acc[v] += s0 + s1;
-                        if (MODE == kAdBoth && gate_too) {
-                            float q = gate_row ? q2.x + q2.y : 0.f;
+                        *acc += s0 + s1;
+                        gacc[v * kAdEpi + et] += q2.x + q2.y;
+                    } else {
 #pragma unroll
-                            for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
-                            if (lane == 0) gsq[ew][v] += q;
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])),
+                                                        neg, x2[16 + e]);
+                            s1 += fabsf(d.x) + fabsf(d.y);
                         }
+                        *acc += s0 + s1;
                     }
+                    if (!ok) break;
                 }
             }
+            tmem_wait_ld();  // no load left in flight (an abort may leave one)
             if (!ok) atomicOr(&abort_flag, 1);
-            // both halves of a row: the second half adds its sums into the first's (the loops
-            // run to the fixed bound so that the sums stay in registers)
-            if (half == 1) {
+            // the gate's partial of this warp per anchor: its rows below the gate prefix,
+            // lanes folded by a fixed tree
+            if (MODE == kAdBoth && gate_too) {
+                for (int v = 0; v < V; ++v) {
+                    float g = gate_row ? gacc[v * kAdEpi + et] : 0.f;
 #pragma unroll
-                for (int v = 0; v < kAnMaxAnchors; ++v)
-                    if (v < V) red[m][v] = acc[v];
+                    for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
+                    if (lane == 0) gsq[ew][v] = g;
+                }
             }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
+            asm volatile("bar.sync 1, 256;" ::: "memory");  // both halves' sums are in accs
             if (MODE == kAdBoth && gate_too && ew == 0 && lane < V && !anchor_vload(&abort_flag)) {
                 float x = 0.f;
                 for (int w2 = 0; w2 < 8; ++w2) x += gsq[w2][lane];
                 args.partial[(((long long)c * args.L + l) * args.tiles + tile) * V + lane] = x;
             }
             if (half == 0 && !anchor_vload(&abort_flag)) {
-#pragma unroll
-                for (int v = 0; v < kAnMaxAnchors; ++v)
-                    if (v < V) acc[v] += red[m][v];
+                // row m's sum per anchor: the first half's plus the second half's
+                float* mine = accs + et;
+                const float* other = accs + (et ^ 128);
                 if (MODE != kAdGate) {
                     if (row_ok) {
                         const float invF = 1.f / (float)args.F;
-                        float mmin = acc[0] * invF;
-#pragma unroll
-                        for (int v = 1; v < kAnMaxAnchors; ++v)
-                            if (v < V) mmin = fminf(mmin, acc[v] * invF);
+                        float mmin = (mine[0] + other[0]) * invF;
+                        for (int v = 1; v < V; ++v) mmin = fminf(mmin, (mine[v * kAdEpi] + other[v * kAdEpi]) * invF);
                         float z = 0.f;
-#pragma unroll
-                        for (int v = 0; v < kAnMaxAnchors; ++v)
-                            if (v < V) {
-                                acc[v] = expf(-(acc[v] * invF - mmin) * args.inv_T);
-                                z += acc[v];
-                            }
+                        for (int v = 0; v < V; ++v) {
+                            const float ev = expf(-((mine[v * kAdEpi] + other[v * kAdEpi]) * invF - mmin) * args.inv_T);
+                            mine[v * kAdEpi] = ev;
+                            z += ev;
+                        }
                         const float iz = 1.f / z;
                         float* wr = (plane ? args.w[1] : args.w[0]) + (((long long)c * args.L + l) * args.n + t0 + m) * V;
-#pragma unroll
-                        for (int v = 0; v < kAnMaxAnchors; ++v)
-                            if (v < V) wr[v] = acc[v] * iz;
+                        for (int v = 0; v < V; ++v) wr[v] = mine[v * kAdEpi] * iz;
                     }
                 } else {
                     // per-tile sums over the rows, in a fixed order: lanes, then the four warps
+                    for (int v = 0; v < V; ++v) {
+                        float x = row_ok ? mine[v * kAdEpi] + other[v * kAdEpi] : 0.f;
 #pragma unroll
-                    for (int v = 0; v < kAnMaxAnchors; ++v) {
-                        if (v < V) {
-                            float x = row_ok ? acc[v] : 0.f;
-#pragma unroll
-                            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-                            if (lane == 0) gsum[wq][v] = x;
-                        }
+                        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                        if (lane == 0) gsum[wq][v] = x;
                     }
                 }
             }
@@ -486,13 +548,15 @@ anchor_gate_kernel(const float* __restrict__ partial, int V, int L, int tiles, d
 
 // ------------------------------------------------------------------ apply
 
-constexpr int kApThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kApMaxB = 16;           // Bt ring entries (one anchor's head slab each)
+constexpr int kApThreads = 320;       // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kApEpi = 256;           // epilogue threads: two per tile row
+constexpr int kApMaxB = 16;           // Bt ring entries (one anchor's rows of one head group)
 constexpr int kApMaxX = 2;            // x head slabs
 
 struct ApArgs {
     int V, L, n, H, C;
     int nb, nx;                       // Bt ring entries and x slabs in use
+    int G;                            // heads per MMA group (G * D accumulator columns)
     const float* w[2];                // [C][L][n][V] per plane
     const int32_t* accept;            // [C] or null
     const int32_t* delta;             // [C]
@@ -505,14 +569,16 @@ struct ApCfg {
     static constexpr uint32_t kLayout = R == 16 ? 6u : R == 32 ? 4u : 2u;
     static constexpr int kABytes = kAnRows * kRowBytes;   // one anchor's A tile
     static constexpr int kXBytes = kAnRows * D * 2;       // one head slab of x (64-feature boxes)
-    static constexpr int kBBytes = D * kRowBytes;         // one anchor's Bt rows of one head
-    static constexpr int kBSlot = kBBytes < 1024 ? 1024 : kBBytes;
+    static constexpr int kPairs = D / 4;                  // rotation pairs per epilogue thread and head
 };
 
 // Persistent like the distance kernel: CTA i takes the units (tile, layer, plane and
 // segment) i, i + grid, ... (plane 0 keys, rotated; 1 values); the x slabs, Bt ring and
 // tensor-memory slots run on across units, and a unit's A tiles load once the previous
-// unit's MMAs have committed.
+// unit's MMAs have committed.  The heads go through the tensor core G at a time: one
+// MMA chain of N = G * D columns per group (K = V * r), into one of two accumulator
+// slots, so that the epilogue of a group overlaps the MMAs of the next.  Each tile row
+// is finished by two epilogue threads, each taking half of a head's rotation pairs.
 template <int D, int R>
 __global__ void __launch_bounds__(kApThreads, 1)
 anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CUtensorMap tm_x1,
@@ -522,13 +588,16 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
                     ApArgs args, RopeTheta th) {
     using K = ApCfg<D, R>;
     extern __shared__ unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t afull, ascaled, adone, xfull[kApMaxX], xempty[kApMaxX], bfull[kApMaxB],
+    __shared__ __align__(8) uint64_t afull, ascaled, adone, mdrain, xfull[kApMaxX], xempty[kApMaxX], bfull[kApMaxB],
         bempty[kApMaxB], tfull[2], tempty[2];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ float2 tab[D / 2];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int V = args.V, H = args.H, NB = args.nb, NX = args.nx;
+    const int V = args.V, H = args.H, NB = args.nb, NX = args.nx, G = args.G;
+    const int GD = G * D;                                        // accumulator columns of a group
+    const int groups = (H + G - 1) / G;
+    const int bslot = GD * K::kRowBytes;                         // one anchor's Bt rows of a group
     unsigned char* asm_ = smem;                                  // V scaled A tiles
     unsigned char* xs = asm_ + V * K::kABytes;                   // NX head slabs of x
     unsigned char* bs = xs + NX * K::kXBytes;                    // Bt ring
@@ -551,15 +620,16 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
 
     if (threadIdx.x == 0) {
         mbar_init(&afull, 1);
-        mbar_init(&ascaled, 4);
+        mbar_init(&ascaled, kApEpi / 32);
         mbar_init(&adone, 1);
+        mbar_init(&mdrain, 1);
         for (int i = 0; i < NX; ++i) {
             mbar_init(&xfull[i], 1);
             mbar_init(&xempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 4);
+            mbar_init(&tempty[i], kApEpi / 32);
         }
         for (int i = 0; i < NB; ++i) {
             mbar_init(&bfull[i], 1);
@@ -569,7 +639,7 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
         abort_flag = 0;
     }
     if (warp == 1) {
-        tmem_alloc(&tmem_slot, 2 * D);
+        tmem_alloc(&tmem_slot, 2 * GD);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -590,7 +660,7 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
             prefetch_tensormap(&tm_a1);
             prefetch_tensormap(&tm_b0);
             prefetch_tensormap(&tm_b1);
-            int it = 0;
+            int it = 0, an = 0, xn = 0;  // units and x slabs armed
             for (int w = blockIdx.x; w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
                 int tile, l, plane, c;
                 if (!unit_of(w, tile, l, plane, c)) continue;
@@ -605,6 +675,7 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
                 mbar_arrive_expect_tx(&afull, (unsigned)(V * K::kABytes));
                 for (int v = 0; v < V; ++v)
                     tma_load_2d(asm_ + v * K::kABytes, ma, 0, ((c * V + v) * args.L + l) * args.n + t0, &afull);
+                ++an;
                 bool ok = true;
                 for (int h = 0; h < H; ++h) {
                     const int hg = it * H + h, xi = hg % NX;
@@ -615,6 +686,7 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
                     mbar_arrive_expect_tx(&xfull[xi], (unsigned)K::kXBytes);
                     for (int b = 0; b < D / 64; ++b)
                         tma_load_4d(xs + xi * K::kXBytes + b * (kAnRows * 128), mx, h * D + 64 * b, t0, l, c, &xfull[xi]);
+                    ++xn;
                 }
                 if (!ok) {
                     atomicOr(&abort_flag, 1);
@@ -622,36 +694,46 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
                 }
                 ++it;
             }
+            if (anchor_vload(&abort_flag)) {
+                drain_ring(&afull, 1, an);
+                drain_ring(xfull, NX, xn);
+            }
         } else if (lane == 1) {
-            int it = 0;
+            int bn = 0, e = 0;  // Bt tiles armed; ring slot of the next
+            unsigned ph = 0;     // phase parity of that slot's next fill
             for (int w = blockIdx.x; w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
                 int tile, l, plane, c;
                 if (!unit_of(w, tile, l, plane, c)) continue;
                 const CUtensorMap* mb = plane ? &tm_b1 : &tm_b0;
                 bool ok = true;
-                for (int q = 0; q < H * V && !anchor_vload(&abort_flag); ++q) {
-                    const int qg = it * H * V + q;
-                    const int h = q / V, v = q % V, e = qg % NB;
-                    if (qg >= NB && !mbar_wait(&bempty[e], (unsigned)(qg / NB - 1) & 1u)) {
-                        ok = false;
-                        break;
+                // rows g * GD .. of each anchor's Bt (a short last group reads rows it does
+                // not use: the next anchor's, or zero fill past the end)
+                for (int g = 0; ok && g < groups && !anchor_vload(&abort_flag); ++g)
+                    for (int v = 0; v < V; ++v) {
+                        if (bn >= NB && !mbar_wait(&bempty[e], ph ^ 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&bfull[e], (unsigned)bslot);
+                        tma_load_2d(bs + e * bslot, mb, 0, ((c * V + v) * args.L + l) * F + g * GD, &bfull[e]);
+                        ++bn;
+                        if (++e == NB) e = 0, ph ^= 1u;
                     }
-                    mbar_arrive_expect_tx(&bfull[e], (unsigned)K::kBBytes);
-                    tma_load_2d(bs + e * K::kBSlot, mb, 0, ((c * V + v) * args.L + l) * F + h * D, &bfull[e]);
-                }
                 if (!ok) {
                     atomicOr(&abort_flag, 1);
                     break;
                 }
-                ++it;
             }
+            if (anchor_vload(&abort_flag)) drain_ring(bfull, NB, bn);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = tc_idesc_bf16(kAnRows, D);
             bool ok = true;
-            int it = 0;
+            int it = 0, gg = 0, e = 0;  // units; groups issued; Bt ring slot of the next
+            unsigned bph = 0;           // its fill's phase parity
+            const uint64_t a_first = tc_smem_desc(asm_, 16, 8 * K::kRowBytes, K::kLayout);
+            const uint64_t b_first = tc_smem_desc(bs, 16, 8 * K::kRowBytes, K::kLayout);
             for (int w = blockIdx.x; ok && w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
                 int tile, l, plane, c;
                 if (!unit_of(w, tile, l, plane, c)) continue;
@@ -659,27 +741,30 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
                     ok = false;
                     break;
                 }
-                for (int h = 0; ok && h < H && !anchor_vload(&abort_flag); ++h) {
-                    const int hg = it * H + h, a = hg & 1;
-                    if (hg >= 2 && !mbar_wait(&tempty[a], (unsigned)(hg / 2 - 1) & 1u)) {
+                for (int g = 0; ok && g < groups && !anchor_vload(&abort_flag); ++g, ++gg) {
+                    const int a = gg & 1;
+                    const int hn = H - g * G < G ? H - g * G : G;  // heads of this group
+                    const uint32_t idesc = tc_idesc_bf16(kAnRows, hn * D);
+                    if (gg >= 2 && !mbar_wait(&tempty[a], (unsigned)((gg >> 1) & 1) ^ 1u)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    // descriptors advance by 16-byte units (shared addresses stay below 256 KB)
+                    uint64_t a_desc = a_first;
                     for (int v = 0; v < V; ++v) {
-                        const int qg = hg * V + v, e = qg % NB;
-                        if (!mbar_wait(&bfull[e], (unsigned)(qg / NB) & 1u)) {
+                        if (!mbar_wait(&bfull[e], bph)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
+                        const uint64_t b_desc = b_first + (uint64_t)((e * bslot) >> 4);
 #pragma unroll
-                        for (int kk = 0; kk < R / 16; ++kk) {
-                            const uint64_t adesc = tc_smem_desc(asm_ + v * K::kABytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
-                            const uint64_t bdesc = tc_smem_desc(bs + e * K::kBSlot + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
-                            tc_mma_bf16(tmem + a * D, adesc, bdesc, idesc, (v > 0 || kk > 0) ? 1u : 0u);
-                        }
+                        for (int kk = 0; kk < R / 16; ++kk)
+                            tc_mma_bf16(tmem + a * GD, a_desc + 2 * kk, b_desc + 2 * kk, idesc, (v > 0 || kk > 0) ? 1u : 0u);
                         tc_commit(&bempty[e]);
+                        if (++e == NB) e = 0, bph ^= 1u;
+                        a_desc += (uint64_t)(K::kABytes >> 4);
                     }
                     if (ok) tc_commit(&tfull[a]);
                 }
@@ -687,42 +772,60 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
                 ++it;
             }
             if (!ok) atomicOr(&abort_flag, 1);
+            // every MMA issued has completed before the tensor memory is released
+            tc_commit(&mdrain);
+            mbar_wait(&mdrain, 0u);
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int wq = warp & 3;
+        const int ew = warp - 2;             // 0..7
+        const int wq = warp & 3;             // TMEM lane quarter of this warp
+        const int half = ew >> 2;            // which half of a head's rotation pairs
         const int m = 32 * wq + lane;        // tile row
-        const int et = threadIdx.x - 64;     // 0..127
+        const int et = threadIdx.x - 64;     // 0..255
+        const int i0 = half * K::kPairs;     // first rotation pair (dims i0.., D/2 + i0..)
         bool ok = true;
-        int it = 0;
+        int it = 0, gg = 0;
         for (int w = blockIdx.x; w < units; w += gridDim.x) {
             int tile, l, plane, c;
             if (!unit_of(w, tile, l, plane, c)) continue;
             // the previous unit is done with the angle table; leave together on abort
-            if (bar_any<1, 128>(!ok || anchor_vload(&abort_flag))) break;
+            if (bar_any<1, kApEpi>(!ok || anchor_vload(&abort_flag))) break;
             const CUtensorMap* mo = plane ? &tm_o1 : &tm_o0;
             const int t0 = tile * kAnRows;
             const bool row_ok = t0 + m < args.n;
             if (plane == 0)
-                for (int i = et; i < D / 2; i += 128) {
+                for (int i = et; i < D / 2; i += kApEpi) {
                     float cs, sn;
                     rope_cos_sin(args.delta[c], th.theta[i], &cs, &sn);
                     tab[i] = make_float2(cs, sn);
                 }
-            // scale row m of every anchor's A tile by the token's weight (bf16, in place: the
-            // swizzle only permutes 16-byte pieces within the row)
-            if (mbar_wait(&afull, (unsigned)it & 1u)) {
+            // scale each anchor's A tile row by the token's weight (bf16, in place: the swizzle
+            // only permutes 16-byte pieces within the row).  Lane i of the warp holds the
+            // weights of row 32 wq + i; in step k the warp scales the 32 consecutive 16-byte
+            // pieces [32 k, 32 k + 32) of its 32 rows (conflict-free), taking each piece's
+            // weight from its row's lane; the two warps of a lane quarter take alternate
+            // steps.  The wait's outcome is made warp-uniform for the shuffles.
+            if (__all_sync(0xffffffffu, mbar_wait(&afull, (unsigned)it & 1u))) {
                 const float* wr = (plane ? args.w[1] : args.w[0]) + (((long long)c * args.L + l) * args.n + (row_ok ? t0 + m : 0)) * V;
-                for (int v = 0; v < V; ++v) {
-                    const float wv = row_ok ? wr[v] : 0.f;
-                    uint4* p = reinterpret_cast<uint4*>(asm_ + v * K::kABytes + m * K::kRowBytes);
+                float wmine[kAnMaxAnchors];
 #pragma unroll
-                    for (int q = 0; q < K::kRowBytes / 16; ++q) {
+                for (int v = 0; v < kAnMaxAnchors; ++v) wmine[v] = (v < V && row_ok) ? wr[v] : 0.f;
+                constexpr int kPieces = K::kRowBytes / 16;  // 16-byte pieces per row (2, 4 or 8)
+#pragma unroll
+                for (int v = 0; v < kAnMaxAnchors; ++v) {
+                    if (v >= V) break;
+                    unsigned char* at = asm_ + v * K::kABytes + (32 * wq) * K::kRowBytes;
+#pragma unroll
+                    for (int k = half; k < kPieces; k += 2) {
+                        const int pc = 32 * k + lane, row = pc / kPieces;  // row within the warp's 32
+                        const float wv = __shfl_sync(0xffffffffu, wmine[v], row);
+                        uint4* pp = reinterpret_cast<uint4*>(at + pc * 16);
                         float f[8];
-                        unpack8(p[q], f);
+                        unpack8(*pp, f);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] *= wv;
-                        p[q] = pack8(f);
+                        for (int q = 0; q < 8; ++q) f[q] *= wv;
+                        *pp = pack8(f);
                     }
                 }
             } else {
@@ -732,26 +835,42 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
             fence_proxy_async_smem();  // generic writes of A -> read by the tensor core
             __syncwarp();
             if (lane == 0) mbar_arrive(&ascaled);
-            asm volatile("bar.sync 1, 128;" ::: "memory");  // the angle table is complete
-            for (int h = 0; h < H; ++h) {
-                const int hg = it * H + h, a = hg & 1, xi = hg % NX;
-                ok = ok && !anchor_vload(&abort_flag) && mbar_wait(&tfull[a], (unsigned)(hg / 2) & 1u) &&
-                     mbar_wait(&xfull[xi], (unsigned)(hg / NX) & 1u);
+            asm volatile("bar.sync 1, 256;" ::: "memory");  // the angle table is complete
+            for (int g = 0; ok && g < groups; ++g, ++gg) {
+                const int a = gg & 1;
+                const int hn = H - g * G < G ? H - g * G : G;
+                ok = ok && !anchor_vload(&abort_flag) &&
+                     __all_sync(0xffffffffu, mbar_wait(&tfull[a], (unsigned)(gg >> 1) & 1u));
                 if (!ok) atomicOr(&abort_flag, 1);
                 tc_fence_after();
-                unsigned char* slab = xs + xi * K::kXBytes;
-                if (ok) {
-                    const uint32_t tb = tmem + ((uint32_t)(32 * wq) << 16) + a * D;
-#pragma unroll
-                    for (int j = 0; j < D / 64; ++j) {
-                        // dims [32j, 32j + 32) and their partners [D/2 + 32j, D/2 + 32j + 32)
-                        uint32_t lo[32], hi[32];
-                        tmem_ld32(tb + 32 * j, lo);
-                        tmem_ld32(tb + D / 2 + 32 * j, hi);
+                for (int hl = 0; hl < hn; ++hl) {
+                    const int h = g * G + hl, hx = it * H + h, xi = hx % NX;
+                    ok = ok && !anchor_vload(&abort_flag) &&
+                         __all_sync(0xffffffffu, mbar_wait(&xfull[xi], (unsigned)(hx / NX) & 1u));
+                    if (!ok) atomicOr(&abort_flag, 1);
+                    unsigned char* slab = xs + xi * K::kXBytes;
+                    if (ok) {
+                        // this thread's rotation pairs of head h: dims i0 .. i0 + kPairs and their
+                        // partners D/2 + i0 ..
+                        const uint32_t tb = tmem + ((uint32_t)(32 * wq) << 16) + a * GD + hl * D;
+                        uint32_t lo[K::kPairs], hi[K::kPairs];
+                        if constexpr (K::kPairs == 32) {
+                            tmem_ld32(tb + i0, lo);
+                            tmem_ld32(tb + D / 2 + i0, hi);
+                        } else {
+                            tmem_ld16(tb + i0, lo);
+                            tmem_ld16(tb + D / 2 + i0, hi);
+                        }
                         tmem_wait_ld();
+                        if (hl == hn - 1) {
+                            // the group's accumulators are all in registers: free the slot
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&tempty[a]);
+                        }
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int f0 = 32 * j + 8 * q, f1 = D / 2 + f0;  // first dims of the two pieces
+                        for (int q = 0; q < K::kPairs / 8; ++q) {
+                            const int f0 = i0 + 8 * q, f1 = D / 2 + f0;  // first dims of the two pieces
                             uint4* p0 = reinterpret_cast<uint4*>(slab + (f0 / 64) * (kAnRows * 128) + m * 128 +
                                                                  ((((f0 % 64) / 8) ^ (m & 7)) << 4));
                             uint4* p1 = reinterpret_cast<uint4*>(slab + (f1 / 64) * (kAnRows * 128) + m * 128 +
@@ -773,22 +892,23 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
                             *p0 = pack8(x0);
                             *p1 = pack8(x1);
                         }
+                    } else if (hl == hn - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tempty[a]);
                     }
+                    fence_proxy_async_smem();  // epilogue writes -> TMA store reads
+                    if (bar_any<1, kApEpi>(!ok || anchor_vload(&abort_flag))) ok = false;  // same verdict in all
+                    if (et == 0) {
+                        if (ok)
+                            for (int b = 0; b < D / 64; ++b)
+                                tma_store_4d(mo, slab + b * (kAnRows * 128), h * D + 64 * b, t0, l, c);
+                        bulk_commit();
+                        bulk_wait_read<1>();  // the previous head's store has read its slab
+                        if (hx >= 1) mbar_arrive(&xempty[(hx - 1) % NX]);
+                    }
+                    if (!ok) break;
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[a]);
-                fence_proxy_async_smem();  // epilogue writes -> TMA store reads
-                if (bar_any<1, 128>(!ok || anchor_vload(&abort_flag))) ok = false;  // same verdict in all
-                if (et == 0) {
-                    if (ok)
-                        for (int b = 0; b < D / 64; ++b)
-                            tma_store_4d(mo, slab + b * (kAnRows * 128), h * D + 64 * b, t0, l, c);
-                    bulk_commit();
-                    bulk_wait_read<1>();  // the previous head's store has read its slab
-                    if (hg >= 1) mbar_arrive(&xempty[(hg - 1) % NX]);
-                }
-                if (!ok) break;
             }
             if (!ok) break;
             ++it;
@@ -798,7 +918,7 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
     __syncthreads();
     if (abort_flag && threadIdx.x == 0) atomicOr(&g_status_anchor, FLAG_TIMEOUT);
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, 2 * D);
+    if (warp == 1) tmem_dealloc(tmem, 2 * GD);
 }
 
 // ------------------------------------------------------------------ host side
@@ -838,52 +958,55 @@ static cudaError_t anchor_factor_map(CUtensorMap* map, const void* base, long lo
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-static int round_up(int x, int a) { return (x + a - 1) / a * a; }
-
 // Static shared memory of the kernels, kept out of the dynamic budget.
-constexpr int kAdStaticBytes = 10 * 1024;
+constexpr int kAdStaticBytes = 2 * 1024;
 constexpr int kApStaticBytes = 2 * 1024;
 
 struct AdShape {
     int nb, nx, smem;
 };
 
-// As many x buffers (up to 4) as leave room for at least 4 Bt entries (or 2, with 2 x
-// buffers), then the Bt ring takes the rest (up to 16 entries).
-static bool ad_shape(int V, int r, AdShape* s) {
+// After the A tiles and the row sums (one array, or two with the gate's): as many x
+// buffers (up to 4) as leave room for at least 8 Bt entries (or 2 x buffers, or 1 when
+// 2 leave no room for 2 entries), then the Bt ring takes the rest (up to 16).
+static bool ad_shape(int V, int r, AdShape* s, int sum_arrays = 1) {
     const int row = 2 * r;
-    const int abytes = kAnRows * row, bbytes = kAdCols * row;
-    const int room = kAnSmemLimit - kAdStaticBytes - 1024 - V * abytes;
-    for (s->nx = kAdMaxX; s->nx > 2 && room - s->nx * kAdXBytes < 4 * bbytes; --s->nx) {
+    const int abytes = kAnRows * row, bbytes = kAdCols * row, sums = sum_arrays * V * kAdEpi * (int)sizeof(float);
+    const int room = kAnSmemLimit - kAdStaticBytes - 1024 - V * abytes - sums;
+    for (s->nx = kAdMaxX; s->nx > 2 && room - s->nx * kAdXBytes < 8 * bbytes; --s->nx) {
     }
+    if (room - s->nx * kAdXBytes < 2 * bbytes) s->nx = 1;
     s->nb = (room - s->nx * kAdXBytes) / bbytes;
     if (s->nb > kAdMaxB) s->nb = kAdMaxB;
-    s->smem = 1024 + V * abytes + s->nx * kAdXBytes + s->nb * bbytes;
+    s->smem = 1024 + V * abytes + s->nx * kAdXBytes + s->nb * bbytes + sums;
     return V >= 1 && V <= kAnMaxAnchors && s->nb >= 2;
 }
 
 struct ApShape {
-    int nb, nx, smem;
+    int nb, nx, g, smem;
 };
 
-static bool ap_shape(int V, int r, int D, ApShape* s) {
+// Two x slabs; heads per MMA group 256 / D (N = 256 accumulator columns), halved while
+// there are fewer heads or the Bt ring would hold fewer than 4 entries (one head per
+// group takes 2).
+static bool ap_shape(int V, int r, int D, int H, ApShape* s) {
     const int row = 2 * r;
     const int abytes = kAnRows * row, xbytes = kAnRows * D * 2;
-    const int bslot = D * row < 1024 ? 1024 : D * row;
-    for (s->nx = kApMaxX; s->nx >= 2; --s->nx) {
-        const int budget = kAnSmemLimit - kApStaticBytes - 1024 - V * abytes - s->nx * xbytes;
-        s->nb = budget / bslot;
+    s->nx = kApMaxX;
+    const int budget = kAnSmemLimit - kApStaticBytes - 1024 - V * abytes - s->nx * xbytes;
+    for (s->g = 256 / D;; s->g /= 2) {
+        s->nb = budget > 0 ? budget / (s->g * D * row) : 0;
         if (s->nb > kApMaxB) s->nb = kApMaxB;
-        if (s->nb >= 2) break;
+        if (s->g == 1 || (s->g <= H && s->nb >= 4)) break;
     }
-    s->smem = 1024 + V * abytes + s->nx * xbytes + s->nb * bslot;
-    return V >= 1 && V <= kAnMaxAnchors && s->nx >= 2 && s->nb >= 2;
+    s->smem = 1024 + V * abytes + s->nx * xbytes + s->nb * s->g * D * row;
+    return V >= 1 && V <= kAnMaxAnchors && s->nb >= 2;
 }
 
 bool anchor_shape_ok(int anchors, int rank, int head_dim) {
     AdShape a;
     ApShape b;
-    return ad_shape(anchors, rank, &a) && (head_dim <= 0 || ap_shape(anchors, rank, head_dim, &b));
+    return ad_shape(anchors, rank, &a, 2) && (head_dim <= 0 || ap_shape(anchors, rank, head_dim, 1, &b));
 }
 
 size_t anchor_gate_workspace_bytes(const kvfix_kv_desc& d, int anchors, int prefix) {
@@ -895,7 +1018,7 @@ template <int R, int MODE>
 static cudaError_t launch_dist(const CUtensorMap* mx, const CUtensorMap* ma, const CUtensorMap* mb, AdArgs& args,
                                int planes, cudaStream_t s) {
     AdShape sh;
-    if (!ad_shape(args.V, R, &sh)) return cudaErrorInvalidValue;
+    if (!ad_shape(args.V, R, &sh, MODE == kAdBoth ? 2 : 1)) return cudaErrorInvalidValue;
     args.nb = sh.nb;
     args.nx = sh.nx;
     cudaError_t e = cudaFuncSetAttribute(anchor_dist_kernel<R, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, sh.smem);
@@ -959,9 +1082,10 @@ static cudaError_t launch_apply(const uint16_t* const* x, const Plane& p, uint16
                                 const uint16_t* const* ad, const uint16_t* const* bdt, ApArgs& args,
                                 const RopeTheta& th, cudaStream_t s) {
     ApShape sh;
-    if (!ap_shape(args.V, R, D, &sh)) return cudaErrorInvalidValue;
+    if (!ap_shape(args.V, R, D, args.H, &sh)) return cudaErrorInvalidValue;
     args.nb = sh.nb;
     args.nx = sh.nx;
+    args.G = sh.g;
     CUtensorMap mx[2], mo[2], ma[2], mb[2];
     cudaError_t e;
     const long long arows = (long long)args.C * args.V * args.L * args.n;
@@ -970,7 +1094,7 @@ static cudaError_t launch_apply(const uint16_t* const* x, const Plane& p, uint16
         if ((e = anchor_plane_map(&mx[q], x[q], p, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
         if ((e = anchor_plane_map(&mo[q], out[q], op, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
         if ((e = anchor_factor_map(&ma[q], ad[q], arows, R, kAnRows)) != cudaSuccess) return e;
-        if ((e = anchor_factor_map(&mb[q], bdt[q], brows, R, D)) != cudaSuccess) return e;
+        if ((e = anchor_factor_map(&mb[q], bdt[q], brows, R, (uint32_t)(sh.g * D))) != cudaSuccess) return e;
     }
     e = cudaFuncSetAttribute(anchor_apply_kernel<D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, sh.smem);
     if (e != cudaSuccess) return e;

@@ -24,6 +24,15 @@ SMALL = [
                           head_dim=128, rank=32, seed=61),
     synth.ANCHOR_8B.with_(name="anchor_sixteen", segments=2, anchors=16, layers=1, tokens=130, kv_heads=4,
                           head_dim=64, rank=16, seed=62),
+    # three heads: the correction's last head group is short (two heads per MMA, then one)
+    synth.ANCHOR_8B.with_(name="anchor_ragged_heads", segments=1, anchors=5, layers=2, tokens=200, kv_heads=3,
+                          head_dim=128, rank=32, seed=64),
+    # rank 64, six heads of 64: groups of four heads, then two
+    synth.ANCHOR_8B.with_(name="anchor_rank64", segments=2, anchors=4, layers=1, tokens=150, kv_heads=6,
+                          head_dim=64, rank=64, seed=65),
+    # rank 64, head 128, seven anchors: one head per MMA group (shared memory)
+    synth.ANCHOR_8B.with_(name="anchor_rank64_wide", segments=1, anchors=7, layers=1, tokens=140, kv_heads=2,
+                          head_dim=128, rank=64, seed=66),
 ]
 
 
@@ -214,29 +223,35 @@ def test_persistent_kernels_walk_many_units():
     inp = synth.anchor_inputs(cfg, DEV)
     src = compose(cfg, inp)
     fac = factors(inp)
+    # a temperature on the scale of the gate's distances, so that the entropies of the two
+    # segments lie strictly between 0 and 1 (at T = 1 each segment matches one anchor so
+    # closely that both entropies are 0)
+    d0, _, _, _ = kvfix().anchor_gate(src["v"], inp["a_c_v"], inp["b_ct_v"], cfg.tokens, tau=cfg.tau)
+    T = float(d0.mean().item())
     ref = [kvfix().anchor_correct(src["k"][c:c + 1], src["v"][c:c + 1], {k: v[c:c + 1] for k, v in fac.items()},
-                                  inp["delta"][c:c + 1], cfg.rope_base) for c in range(cfg.segments)]
+                                  inp["delta"][c:c + 1], cfg.rope_base, temperature=T) for c in range(cfg.segments)]
     ok = torch.full_like(src["k"], 7.0)
     ov = torch.full_like(src["v"], 7.0)
     wk = torch.full((cfg.segments, cfg.layers, cfg.tokens, cfg.anchors), -1.0, device=DEV)
     wv = wk.clone()
     accept = torch.tensor([1, 0], dtype=torch.int32, device=DEV)
-    kvfix().anchor_correct(src["k"], src["v"], fac, inp["delta"], cfg.rope_base, accept=accept, out_k=ok, out_v=ov,
-                           w_k=wk, w_v=wv)
+    kvfix().anchor_correct(src["k"], src["v"], fac, inp["delta"], cfg.rope_base, temperature=T, accept=accept,
+                           out_k=ok, out_v=ov, w_k=wk, w_v=wv)
     kvfix().check_status()
     assert torch.equal(ok[0].view(torch.int16), ref[0][0][0].view(torch.int16))
     assert torch.equal(ov[0].view(torch.int16), ref[0][1][0].view(torch.int16))
     assert torch.equal(wk[0], ref[0][2][0]) and torch.equal(wv[0], ref[0][3][0])
     assert (ok[1] == 7.0).all() and (ov[1] == 7.0).all() and (wk[1] == -1.0).all() and (wv[1] == -1.0).all()
     # the one-pass call with a threshold between the two segments' entropies: one passes
-    _, _, hbar, _ = kvfix().anchor_gate(src["v"], inp["a_c_v"], inp["b_ct_v"], cfg.tokens, tau=cfg.tau)
+    _, _, hbar, _ = kvfix().anchor_gate(src["v"], inp["a_c_v"], inp["b_ct_v"], cfg.tokens, temperature=T,
+                                        tau=cfg.tau)
     h = hbar.cpu().numpy()
-    assert h[0] != h[1]
+    assert 0.0 < h.min() < h.max() < 1.0
     tau = float((h[0] + h[1]) / 2)
     ok2 = torch.full_like(src["k"], 3.0)
     ov2 = torch.full_like(src["v"], 3.0)
-    res = kvfix().anchor_gate_correct(src["k"], src["v"], fac, cfg.tokens, inp["delta"], cfg.rope_base, tau=tau,
-                                      out_k=ok2, out_v=ov2)
+    res = kvfix().anchor_gate_correct(src["k"], src["v"], fac, cfg.tokens, inp["delta"], cfg.rope_base, temperature=T,
+                                      tau=tau, out_k=ok2, out_v=ov2)
     kvfix().check_status()
     acc = res[7].cpu().numpy().astype(bool)
     assert acc.sum() == 1
