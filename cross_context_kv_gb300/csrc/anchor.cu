@@ -66,7 +66,7 @@ constexpr int kAnSmemLimit = 227 * 1024;
 
 // ------------------------------------------------------------------ distances
 
-constexpr int kAdThreads = 320;       // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kAdThreads = 352;       // warp 0 TMA, warps 1 and 10 MMA, warps 2..9 epilogue
 constexpr int kAdCols = 128;          // features per chunk (MMA N)
 constexpr int kAdSlots = 4;           // tensor-memory accumulators of 128 columns
 constexpr int kAdMaxB = 16;           // Bt ring entries (one anchor's chunk each)
@@ -125,7 +125,7 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
     using K = AdCfg<R>;
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t xfull[kAdMaxX], xempty[kAdMaxX], bfull[kAdMaxB], bempty[kAdMaxB], tfull[kAdSlots],
-        tempty[kAdSlots], afull, adone, mdrain;
+        tinit[kAdSlots], afull, adone, mdrain;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ float gsum[4][kAnMaxAnchors];
@@ -164,11 +164,11 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
         }
         for (int a = 0; a < kAdSlots; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 8);
+            mbar_init(&tinit[a], 8);   // the eight epilogue warps: slot holds -x, ready for the MMA
         }
         mbar_init(&afull, 1);
-        mbar_init(&adone, 1);
-        mbar_init(&mdrain, 1);
+        mbar_init(&adone, 2);    // both MMA issuers
+        mbar_init(&mdrain, 2);
         fence_mbar_init();
         abort_flag = 0;
     }
@@ -258,13 +258,17 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
             }
             if (anchor_vload(&abort_flag)) drain_ring(bfull, NB, bn);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // (running ring slots and parities: no division in the per-step path)
+    } else if (warp == 1 || warp == kAdThreads / 32 - 1) {
+        // ------------------------------------------------------------ MMA issuers
+        // Two threads in two warps issue alternate steps (even and odd step numbers: slots
+        // 0, 2 and 1, 3); each commits its own steps.  Ring slots and parities are derived
+        // once per unit and then advance without division.
         if (lane == 0) {
+            const int par = warp == 1 ? 0 : 1;
             constexpr uint32_t idesc = tc_idesc_bf16(kAnRows, kAdCols);
-            int it = 0, qg = 0, e = 0;  // steps issued; Bt ring slot of the next
-            unsigned bph = 0;           // its fill's phase parity
+            const uint64_t a_first = tc_smem_desc(asm_, 16, 8 * K::kRowBytes, K::kLayout);
+            const uint64_t b_first = tc_smem_desc(bs, 16, 8 * K::kRowBytes, K::kLayout);
+            int it = 0;
             bool ok = true;
             for (int w = blockIdx.x; ok && w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
                 int tile, l, plane, c;
@@ -274,27 +278,30 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
                     break;
                 }
                 tc_fence_after();
-                int v = 0;
-                for (int q = 0; q < total && !anchor_vload(&abort_flag); ++q, ++qg) {
+                const int qb = it * total, q0 = (par ^ qb) & 1;
+                int qg = qb + q0, e = qg % NB, v = q0 % V;
+                unsigned bph = (unsigned)(qg / NB) & 1u;
+                for (int q = q0; q < total && !anchor_vload(&abort_flag); q += 2, qg += 2) {
                     const int a = qg & (kAdSlots - 1);
-                    if ((qg >= kAdSlots && !mbar_wait(&tempty[a], (unsigned)((qg / kAdSlots) & 1) ^ 1u)) ||
-                        !mbar_wait(&bfull[e], bph)) {
+                    if (!mbar_wait(&tinit[a], (unsigned)(qg / kAdSlots) & 1u) || !mbar_wait(&bfull[e], bph)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    // descriptors advance by 16-byte units (shared addresses stay below 256 KB)
+                    const uint64_t ad = a_first + (uint64_t)(v * (K::kABytes >> 4));
+                    const uint64_t bd = b_first + (uint64_t)(e * (K::kBBytes >> 4));
 #pragma unroll
-                    for (int kk = 0; kk < R / 16; ++kk) {
-                        const uint64_t adesc = tc_smem_desc(asm_ + v * K::kABytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
-                        const uint64_t bdesc = tc_smem_desc(bs + e * K::kBBytes + 32 * kk, 16, 8 * K::kRowBytes, K::kLayout);
-                        tc_mma_bf16(tmem + a * kAdCols, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < R / 16; ++kk)
+                        tc_mma_bf16(tmem + a * kAdCols, ad + 2 * kk, bd + 2 * kk, idesc, 1u);  // onto -x
                     tc_commit(&bempty[e]);
                     tc_commit(&tfull[a]);
-                    if (++e == NB) e = 0, bph ^= 1u;
-                    if (++v == V) v = 0;
+                    e += 2;
+                    if (e >= NB) e -= NB, bph ^= 1u;
+                    v += 2;
+                    while (v >= V) v -= V;
                 }
-                tc_commit(&adone);  // this unit's MMAs are done with the A tiles
+                tc_commit(&adone);  // this issuer's MMAs of the unit are done with the A tiles
                 ++it;
             }
             if (!ok) atomicOr(&abort_flag, 1);
@@ -304,12 +311,13 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // Thread et holds row m's 64 features of the chunk in registers and accumulates its
-        // per-anchor sums in shared memory (accs[v][et], so that the anchor loop stays
-        // rolled: the unrolled form overflowed the instruction cache).  Each step is read
-        // from tensor memory in two 32-column halves: the second half is loaded while the
-        // first is folded, and the next step's first half while the second is folded.  The
-        // waits are made warp-uniform (the loads are warp-collective).
+        // Thread et owns row m's 64 features of the chunk.  Before each step's MMA the warps
+        // write -x into the step's accumulator slot (tcgen05.st), so that the tensor core
+        // leaves rec - x there; the epilogue then folds |rec - x| (and its square for the
+        // gate) and accumulates its per-anchor sums in shared memory (accs[v][et]; the
+        // anchor loop stays rolled).  A slot is written again right after its values are
+        // loaded when its next step lies in the same chunk, else at the start of the next
+        // chunk, once that chunk's x is in registers.
         const int ew = warp - 2;              // 0..7
         const int wq = warp & 3;              // TMEM lane quarter this warp may read
         const int half = ew >> 2;             // which 64 of the chunk's 128 features
@@ -330,115 +338,105 @@ anchor_dist_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_const
             for (int v = 0; v < V; ++v) accs[v * kAdEpi + et] = 0.f;
             if (gate_too)
                 for (int v = 0; v < V; ++v) gacc[v * kAdEpi + et] = 0.f;
-            const int qbase = it * total;
-            uint32_t p[32], r[32];
-            if (__all_sync(0xffffffffu, mbar_wait(&tfull[qbase & (kAdSlots - 1)], (unsigned)(qbase / kAdSlots) & 1u))) {
-                tc_fence_after();
-                tmem_ld32(tcol + (qbase & (kAdSlots - 1)) * kAdCols, p);
-            } else {
-                ok = false;
-            }
-            const float2 neg = make_float2(-1.f, -1.f);
-            int qg = qbase;
+            int qg = it * total;
             for (int j = 0; ok && j < chunks; ++j) {
                 const int jg = it * chunks + j, xi = jg % NX;
                 if (!__all_sync(0xffffffffu, !anchor_vload(&abort_flag) && mbar_wait(&xfull[xi], (unsigned)(jg / NX) & 1u))) {
                     ok = false;
                     break;
                 }
-                // this row's 64 features of the chunk, as float pairs
-                float2 x2[32];
+                // -x of this row's 64 features of the chunk, as float bit patterns
+                uint32_t nx[64];
                 const unsigned char* xrow = xs + xi * kAdXBytes + half * (kAnRows * 128) + m * 128;
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const uint4 u = *reinterpret_cast<const uint4*>(xrow + ((q ^ (m & 7)) << 4));
-                    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+                    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) x2[4 * q + e] = __bfloat1622float2(h2[e]);
+                    for (int k = 0; k < 4; ++k) {
+                        nx[8 * q + 2 * k] = (wd[k] << 16) ^ 0x80000000u;
+                        nx[8 * q + 2 * k + 1] = (wd[k] & 0xffff0000u) ^ 0x80000000u;
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&xempty[xi]);  // x is in registers now
+                // the slots of the chunk's first steps (their previous steps were in earlier chunks)
+                for (int v = 0; v < V && v < kAdSlots; ++v) {
+                    const uint32_t ts = tcol + ((qg + v) & (kAdSlots - 1)) * kAdCols;
+                    tmem_st32(ts, nx);
+                    tmem_st32(ts + 32, nx + 32);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tinit[(qg + v) & (kAdSlots - 1)]);
+                }
 #pragma unroll 1
                 for (int v = 0; v < V; ++v, ++qg) {
                     const int a = qg & (kAdSlots - 1);
-                    tmem_wait_ld32(p);
+                    if (!__all_sync(0xffffffffu, mbar_wait(&tfull[a], (unsigned)(qg / kAdSlots) & 1u))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t p[32], r[32];
+                    tmem_ld32(tcol + a * kAdCols, p);
                     tmem_ld32(tcol + a * kAdCols + 32, r);
-                    // first half: features [0, 32) of this thread's 64
-                    float s0 = 0.f, s1 = 0.f;
-                    float2 q2 = make_float2(0.f, 0.f);
-                    if (MODE == kAdGate) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])),
-                                                        neg, x2[e]);
-                            q2 = __ffma2_rn(d, d, q2);
-                        }
-                    } else if (gate_too) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])),
-                                                        neg, x2[e]);
-                            s0 += fabsf(d.x) + fabsf(d.y);
-                            q2 = __ffma2_rn(d, d, q2);
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])),
-                                                        neg, x2[e]);
-                            s0 += fabsf(d.x) + fabsf(d.y);
-                        }
-                    }
+                    tmem_wait_ld32(p);
                     tmem_wait_ld32(r);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[a]);
-                    // the next step's first half (also across the chunk boundary); p is zeroed
-                    // when there is none, so that its old value is dead here
-                    {
-                        const int qn = qg + 1, an = qn & (kAdSlots - 1);
-                        const bool more = qn < qbase + total;
-                        const bool got =
-                            more && __all_sync(0xffffffffu, mbar_wait(&tfull[an], (unsigned)(qn / kAdSlots) & 1u));
-                        if (got) {
-                            tc_fence_after();
-                            tmem_ld32(tcol + an * kAdCols, p);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) p[i] = 0u;
-                        }
-                        if (more && !got) ok = false;
+                    if (v + kAdSlots < V) {
+                        // the slot's next step is in this chunk: write -x again now
+                        tmem_st32(tcol + a * kAdCols, nx);
+                        tmem_st32(tcol + a * kAdCols + 32, nx + 32);
+                        tmem_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tinit[a]);
                     }
-                    // second half: features [32, 64)
+                    // d = rec - x for features [0, 32) (p) and [32, 64) (r) of this thread's 64
                     float* acc = accs + v * kAdEpi + et;
                     if (MODE == kAdGate) {
+                        float2 q2 = make_float2(0.f, 0.f), q2o = make_float2(0.f, 0.f);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])),
-                                                        neg, x2[16 + e]);
+                        for (int e = 0; e < 16; e += 2) {
+                            const float2 d = make_float2(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1]));
+                            const float2 f = make_float2(__uint_as_float(p[2 * e + 2]), __uint_as_float(p[2 * e + 3]));
                             q2 = __ffma2_rn(d, d, q2);
+                            q2o = __ffma2_rn(f, f, q2o);
                         }
-                        *acc += q2.x + q2.y;
-                    } else if (gate_too) {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])),
-                                                        neg, x2[16 + e]);
-                            s1 += fabsf(d.x) + fabsf(d.y);
+                        for (int e = 0; e < 16; e += 2) {
+                            const float2 d = make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                            const float2 f = make_float2(__uint_as_float(r[2 * e + 2]), __uint_as_float(r[2 * e + 3]));
                             q2 = __ffma2_rn(d, d, q2);
+                            q2o = __ffma2_rn(f, f, q2o);
                         }
-                        *acc += s0 + s1;
-                        gacc[v * kAdEpi + et] += q2.x + q2.y;
+                        *acc += (q2.x + q2.y) + (q2o.x + q2o.y);
                     } else {
+                        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float2 d = __ffma2_rn(make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])),
-                                                        neg, x2[16 + e]);
-                            s1 += fabsf(d.x) + fabsf(d.y);
+                        for (int e = 0; e < 32; e += 4) {
+                            s0 += fabsf(__uint_as_float(p[e])) + fabsf(__uint_as_float(p[e + 1]));
+                            s1 += fabsf(__uint_as_float(p[e + 2])) + fabsf(__uint_as_float(p[e + 3]));
+                            s2 += fabsf(__uint_as_float(r[e])) + fabsf(__uint_as_float(r[e + 1]));
+                            s3 += fabsf(__uint_as_float(r[e + 2])) + fabsf(__uint_as_float(r[e + 3]));
                         }
-                        *acc += s0 + s1;
+                        *acc += (s0 + s1) + (s2 + s3);
+                        if (gate_too) {
+                            float2 q2 = make_float2(0.f, 0.f), q2o = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4) {
+                                q2 = __ffma2_rn(make_float2(__uint_as_float(p[e]), __uint_as_float(p[e + 1])),
+                                                make_float2(__uint_as_float(p[e]), __uint_as_float(p[e + 1])), q2);
+                                q2o = __ffma2_rn(make_float2(__uint_as_float(p[e + 2]), __uint_as_float(p[e + 3])),
+                                                 make_float2(__uint_as_float(p[e + 2]), __uint_as_float(p[e + 3])), q2o);
+                                q2 = __ffma2_rn(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                                                make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), q2);
+                                q2o = __ffma2_rn(make_float2(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])),
+                                                 make_float2(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])), q2o);
+                            }
+                            gacc[v * kAdEpi + et] += (q2.x + q2.y) + (q2o.x + q2o.y);
+                        }
                     }
-                    if (!ok) break;
                 }
             }
             tmem_wait_ld();  // no load left in flight (an abort may leave one)
@@ -548,7 +546,7 @@ anchor_gate_kernel(const float* __restrict__ partial, int V, int L, int tiles, d
 
 // ------------------------------------------------------------------ apply
 
-constexpr int kApThreads = 320;       // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kApThreads = 352;       // warp 0 TMA loads, warp 1 MMA, warps 2..9 epilogue, warp 10 TMA stores
 constexpr int kApEpi = 256;           // epilogue threads: two per tile row
 constexpr int kApMaxB = 16;           // Bt ring entries (one anchor's rows of one head group)
 constexpr int kApMaxX = 2;            // x head slabs
@@ -578,7 +576,9 @@ struct ApCfg {
 // unit's MMAs have committed.  The heads go through the tensor core G at a time: one
 // MMA chain of N = G * D columns per group (K = V * r), into one of two accumulator
 // slots, so that the epilogue of a group overlaps the MMAs of the next.  Each tile row
-// is finished by two epilogue threads, each taking half of a head's rotation pairs.
+// is finished by two epilogue threads, each taking half of a head's rotation pairs; a
+// head's slab, corrected in place, is stored by the store warp, which frees the slab for
+// the next load as soon as the store has read it.
 template <int D, int R>
 __global__ void __launch_bounds__(kApThreads, 1)
 anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CUtensorMap tm_x1,
@@ -588,8 +588,8 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
                     ApArgs args, RopeTheta th) {
     using K = ApCfg<D, R>;
     extern __shared__ unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t afull, ascaled, adone, mdrain, xfull[kApMaxX], xempty[kApMaxX], bfull[kApMaxB],
-        bempty[kApMaxB], tfull[2], tempty[2];
+    __shared__ __align__(8) uint64_t afull, ascaled, adone, mdrain, xfull[kApMaxX], xdone[kApMaxX], xempty[kApMaxX],
+        bfull[kApMaxB], bempty[kApMaxB], tfull[2], tempty[2];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ float2 tab[D / 2];
@@ -625,6 +625,7 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
         mbar_init(&mdrain, 1);
         for (int i = 0; i < NX; ++i) {
             mbar_init(&xfull[i], 1);
+            mbar_init(&xdone[i], kApEpi / 32);
             mbar_init(&xempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -776,8 +777,42 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
             tc_commit(&mdrain);
             mbar_wait(&mdrain, 0u);
         }
+    } else if (warp == kApThreads / 32 - 1) {
+        // ------------------------------------------------------------ TMA stores
+        // each finished slab goes out, and is freed for the next load once read
+        if (lane == 0) {
+            int it = 0;
+            for (int w = blockIdx.x; w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
+                int tile, l, plane, c;
+                if (!unit_of(w, tile, l, plane, c)) continue;
+                const CUtensorMap* mo = plane ? &tm_o1 : &tm_o0;
+                const int t0 = tile * kAnRows;
+                bool ok = true;
+                for (int h = 0; h < H; ++h) {
+                    const int hx = it * H + h, xi = hx % NX;
+                    if (anchor_vload(&abort_flag) || !mbar_wait(&xdone[xi], (unsigned)(hx / NX) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    unsigned char* slab = xs + xi * K::kXBytes;
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_store_4d(mo, slab + b * (kAnRows * 128), h * D + 64 * b, t0, l, c);
+                    bulk_commit();
+                    bulk_wait_read<0>();
+                    mbar_arrive(&xempty[xi]);
+                }
+                if (!ok) {
+                    atomicOr(&abort_flag, 1);
+                    break;
+                }
+                ++it;
+            }
+            bulk_wait<0>();
+        }
     } else {
         // ------------------------------------------------------------ epilogue
+        // A warp that meets a failed wait skips the rest of the unit; all 256 threads meet
+        // once per unit at the barrier that decides whether to go on.
         const int ew = warp - 2;             // 0..7
         const int wq = warp & 3;             // TMEM lane quarter of this warp
         const int half = ew >> 2;            // which half of a head's rotation pairs
@@ -791,7 +826,6 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
             if (!unit_of(w, tile, l, plane, c)) continue;
             // the previous unit is done with the angle table; leave together on abort
             if (bar_any<1, kApEpi>(!ok || anchor_vload(&abort_flag))) break;
-            const CUtensorMap* mo = plane ? &tm_o1 : &tm_o0;
             const int t0 = tile * kAnRows;
             const bool row_ok = t0 + m < args.n;
             if (plane == 0)
@@ -839,81 +873,70 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
             for (int g = 0; ok && g < groups; ++g, ++gg) {
                 const int a = gg & 1;
                 const int hn = H - g * G < G ? H - g * G : G;
-                ok = ok && !anchor_vload(&abort_flag) &&
-                     __all_sync(0xffffffffu, mbar_wait(&tfull[a], (unsigned)(gg >> 1) & 1u));
-                if (!ok) atomicOr(&abort_flag, 1);
+                if (anchor_vload(&abort_flag) || !__all_sync(0xffffffffu, mbar_wait(&tfull[a], (unsigned)(gg >> 1) & 1u))) {
+                    ok = false;
+                    atomicOr(&abort_flag, 1);
+                    break;
+                }
                 tc_fence_after();
                 for (int hl = 0; hl < hn; ++hl) {
                     const int h = g * G + hl, hx = it * H + h, xi = hx % NX;
-                    ok = ok && !anchor_vload(&abort_flag) &&
-                         __all_sync(0xffffffffu, mbar_wait(&xfull[xi], (unsigned)(hx / NX) & 1u));
-                    if (!ok) atomicOr(&abort_flag, 1);
+                    if (anchor_vload(&abort_flag) ||
+                        !__all_sync(0xffffffffu, mbar_wait(&xfull[xi], (unsigned)(hx / NX) & 1u))) {
+                        ok = false;
+                        atomicOr(&abort_flag, 1);
+                        break;
+                    }
                     unsigned char* slab = xs + xi * K::kXBytes;
-                    if (ok) {
-                        // this thread's rotation pairs of head h: dims i0 .. i0 + kPairs and their
-                        // partners D/2 + i0 ..
-                        const uint32_t tb = tmem + ((uint32_t)(32 * wq) << 16) + a * GD + hl * D;
-                        uint32_t lo[K::kPairs], hi[K::kPairs];
-                        if constexpr (K::kPairs == 32) {
-                            tmem_ld32(tb + i0, lo);
-                            tmem_ld32(tb + D / 2 + i0, hi);
-                        } else {
-                            tmem_ld16(tb + i0, lo);
-                            tmem_ld16(tb + D / 2 + i0, hi);
-                        }
-                        tmem_wait_ld();
-                        if (hl == hn - 1) {
-                            // the group's accumulators are all in registers: free the slot
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&tempty[a]);
-                        }
-#pragma unroll
-                        for (int q = 0; q < K::kPairs / 8; ++q) {
-                            const int f0 = i0 + 8 * q, f1 = D / 2 + f0;  // first dims of the two pieces
-                            uint4* p0 = reinterpret_cast<uint4*>(slab + (f0 / 64) * (kAnRows * 128) + m * 128 +
-                                                                 ((((f0 % 64) / 8) ^ (m & 7)) << 4));
-                            uint4* p1 = reinterpret_cast<uint4*>(slab + (f1 / 64) * (kAnRows * 128) + m * 128 +
-                                                                 ((((f1 % 64) / 8) ^ (m & 7)) << 4));
-                            float x0[8], x1[8];
-                            unpack8(*p0, x0);
-                            unpack8(*p1, x1);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                float y0 = x0[e], y1 = x1[e];
-                                if (plane == 0) {
-                                    const float2 cs = tab[f0 + e];
-                                    y0 = __fmaf_rn(x0[e], cs.x, __fmul_rn(x1[e], -cs.y));
-                                    y1 = __fmaf_rn(x1[e], cs.x, __fmul_rn(x0[e], cs.y));
-                                }
-                                x0[e] = y0 + __uint_as_float(lo[8 * q + e]);
-                                x1[e] = y1 + __uint_as_float(hi[8 * q + e]);
-                            }
-                            *p0 = pack8(x0);
-                            *p1 = pack8(x1);
-                        }
-                    } else if (hl == hn - 1) {
+                    // this thread's rotation pairs of head h: dims i0 .. i0 + kPairs and their
+                    // partners D/2 + i0 ..
+                    const uint32_t tb = tmem + ((uint32_t)(32 * wq) << 16) + a * GD + hl * D;
+                    uint32_t lo[K::kPairs], hi[K::kPairs];
+                    if constexpr (K::kPairs == 32) {
+                        tmem_ld32(tb + i0, lo);
+                        tmem_ld32(tb + D / 2 + i0, hi);
+                    } else {
+                        tmem_ld16(tb + i0, lo);
+                        tmem_ld16(tb + D / 2 + i0, hi);
+                    }
+                    tmem_wait_ld();
+                    if (hl == hn - 1) {
+                        // the group's accumulators are all in registers: free the slot
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&tempty[a]);
                     }
-                    fence_proxy_async_smem();  // epilogue writes -> TMA store reads
-                    if (bar_any<1, kApEpi>(!ok || anchor_vload(&abort_flag))) ok = false;  // same verdict in all
-                    if (et == 0) {
-                        if (ok)
-                            for (int b = 0; b < D / 64; ++b)
-                                tma_store_4d(mo, slab + b * (kAnRows * 128), h * D + 64 * b, t0, l, c);
-                        bulk_commit();
-                        bulk_wait_read<1>();  // the previous head's store has read its slab
-                        if (hx >= 1) mbar_arrive(&xempty[(hx - 1) % NX]);
+#pragma unroll
+                    for (int q = 0; q < K::kPairs / 8; ++q) {
+                        const int f0 = i0 + 8 * q, f1 = D / 2 + f0;  // first dims of the two pieces
+                        uint4* p0 = reinterpret_cast<uint4*>(slab + (f0 / 64) * (kAnRows * 128) + m * 128 +
+                                                             ((((f0 % 64) / 8) ^ (m & 7)) << 4));
+                        uint4* p1 = reinterpret_cast<uint4*>(slab + (f1 / 64) * (kAnRows * 128) + m * 128 +
+                                                             ((((f1 % 64) / 8) ^ (m & 7)) << 4));
+                        float x0[8], x1[8];
+                        unpack8(*p0, x0);
+                        unpack8(*p1, x1);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            float y0 = x0[e], y1 = x1[e];
+                            if (plane == 0) {
+                                const float2 cs = tab[f0 + e];
+                                y0 = __fmaf_rn(x0[e], cs.x, __fmul_rn(x1[e], -cs.y));
+                                y1 = __fmaf_rn(x1[e], cs.x, __fmul_rn(x0[e], cs.y));
+                            }
+                            x0[e] = y0 + __uint_as_float(lo[8 * q + e]);
+                            x1[e] = y1 + __uint_as_float(hi[8 * q + e]);
+                        }
+                        *p0 = pack8(x0);
+                        *p1 = pack8(x1);
                     }
-                    if (!ok) break;
+                    fence_proxy_async_smem();  // epilogue writes -> TMA store reads
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&xdone[xi]);
                 }
             }
-            if (!ok) break;
             ++it;
         }
-        if (et == 0) bulk_wait<0>();
     }
     __syncthreads();
     if (abort_flag && threadIdx.x == 0) atomicOr(&g_status_anchor, FLAG_TIMEOUT);
@@ -986,18 +1009,30 @@ struct ApShape {
     int nb, nx, g, smem;
 };
 
-// Two x slabs; heads per MMA group 256 / D (N = 256 accumulator columns), halved while
-// there are fewer heads or the Bt ring would hold fewer than 4 entries (one head per
-// group takes 2).
+// Heads per MMA group 256 / D (N = 256 accumulator columns), halved while there are
+// fewer heads or the rings do not fit; x slabs 3 with at least 3 Bt entries, else 2
+// with at least 4 (one head per group: 2 slabs and 2 entries at least).
 static bool ap_shape(int V, int r, int D, int H, ApShape* s) {
     const int row = 2 * r;
     const int abytes = kAnRows * row, xbytes = kAnRows * D * 2;
-    s->nx = kApMaxX;
-    const int budget = kAnSmemLimit - kApStaticBytes - 1024 - V * abytes - s->nx * xbytes;
+    const int base = kAnSmemLimit - kApStaticBytes - 1024 - V * abytes;
     for (s->g = 256 / D;; s->g /= 2) {
-        s->nb = budget > 0 ? budget / (s->g * D * row) : 0;
-        if (s->nb > kApMaxB) s->nb = kApMaxB;
-        if (s->g == 1 || (s->g <= H && s->nb >= 4)) break;
+        const int bslot = s->g * D * row;
+        bool fit = false;
+        for (s->nx = kApMaxX; s->nx >= 2 && !fit; --s->nx) {
+            const int budget = base - s->nx * xbytes;
+            s->nb = budget > 0 ? budget / bslot : 0;
+            if (s->nb > kApMaxB) s->nb = kApMaxB;
+            fit = s->nb >= (s->nx == 3 ? 3 : 4);
+            if (fit) break;
+        }
+        if (fit && s->g <= H) break;
+        if (s->g == 1) {
+            s->nx = 2;
+            s->nb = base - 2 * xbytes > 0 ? (base - 2 * xbytes) / bslot : 0;
+            if (s->nb > kApMaxB) s->nb = kApMaxB;
+            break;
+        }
     }
     s->smem = 1024 + V * abytes + s->nx * xbytes + s->nb * s->g * D * row;
     return V >= 1 && V <= kAnMaxAnchors && s->nb >= 2;
