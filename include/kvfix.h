@@ -558,8 +558,9 @@ KVFIX_API kvfix_status kvfix_diff_restore_split(
  * reconstructions as the value plane's token weights, the gate is decided on the device,
  * and only accepted segments are corrected (rejected ones keep their outputs; their
  * weights are still written).  Arguments as for the two calls; `accept` is an output here.
- * The gate's per-tile sums are folded per warp and then over the warps in a fixed order,
- * so d differs from kvfix_anchor_gate's in the last bits (and is deterministic).
+ * The gate's squares are summed per thread over the features, folded per warp by a fixed
+ * tree and then over the warps in a fixed order, so d differs from kvfix_anchor_gate's in
+ * the last bits (and is deterministic).
  * workspace: at least kvfix_anchor_gate_workspace_bytes(src, anchors, src.tokens).
  * head_dim 64 or 128.
  */
