@@ -100,14 +100,15 @@ struct AdCfg {
 // ...; the x, Bt and tensor-memory rings run on from one unit to the next, and a unit's A
 // tiles are loaded once the previous unit's MMAs have committed ("adone"), so the next
 // unit's loads overlap the previous one's epilogue.  Per unit, for each 128-feature chunk
-// the x tile is staged once; the anchors' base rows of the chunk (M = 128 rows, N = 128
-// features, K = r) go through four tensor-memory accumulators while the epilogue folds them against x, which each
-// thread holds in registers (its row, 64 of the chunk's features) for all anchors.
+// the x tile is staged once; each thread takes its row's 64 of the chunk's features into
+// registers as -x and writes them into the tensor-memory slot of each (chunk, anchor) step
+// before the step's MMA (M = 128 rows, N = 128 features, K = r) accumulates the anchor's
+// reconstruction onto them, so the epilogue reads rec - x from four rotating slots.
 // MODE kAdWeights: both planes (z = plane * C + c), every row; writes the softmax of
 // -mean|x - rec_v| / T per row.  MODE kAdGate: the value plane, rows < k; writes per-tile
 // sums of (x - rec_v)^2.  MODE kAdBoth: the weights of both planes and, on the value
-// plane, the gate's per-tile sums from the same reconstructions (warp partials folded in
-// a fixed order).
+// plane, the gate's per-tile sums from the same reconstructions (per-thread sums folded
+// per warp and then over the warps in a fixed order).
 //
 // After an abort a producer waits (bounded) for the copies it armed last on each barrier
 // of a ring, so that no bulk copy is still writing shared memory when the CTA leaves;
