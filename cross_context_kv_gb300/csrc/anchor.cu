@@ -662,22 +662,12 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
             prefetch_tensormap(&tm_a1);
             prefetch_tensormap(&tm_b0);
             prefetch_tensormap(&tm_b1);
-            int it = 0, an = 0, xn = 0;  // units and x slabs armed
+            int it = 0, xn = 0;  // units; x slabs armed
             for (int w = blockIdx.x; w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
                 int tile, l, plane, c;
                 if (!unit_of(w, tile, l, plane, c)) continue;
                 const CUtensorMap* mx = plane ? &tm_x1 : &tm_x0;
-                const CUtensorMap* ma = plane ? &tm_a1 : &tm_a0;
                 const int t0 = tile * kAnRows;
-                // the previous unit's MMAs have read its (scaled) A tiles
-                if (it > 0 && !mbar_wait(&adone, (unsigned)(it - 1) & 1u)) {
-                    atomicOr(&abort_flag, 1);
-                    break;
-                }
-                mbar_arrive_expect_tx(&afull, (unsigned)(V * K::kABytes));
-                for (int v = 0; v < V; ++v)
-                    tma_load_2d(asm_ + v * K::kABytes, ma, 0, ((c * V + v) * args.L + l) * args.n + t0, &afull);
-                ++an;
                 bool ok = true;
                 for (int h = 0; h < H; ++h) {
                     const int hg = it * H + h, xi = hg % NX;
@@ -696,10 +686,26 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
                 }
                 ++it;
             }
-            if (anchor_vload(&abort_flag)) {
-                drain_ring(&afull, 1, an);
-                drain_ring(xfull, NX, xn);
+            if (anchor_vload(&abort_flag)) drain_ring(xfull, NX, xn);
+        } else if (lane == 2) {
+            // the A tiles of each unit, as soon as the previous unit's MMAs have read theirs
+            int it = 0, an = 0;  // units; A loads armed
+            for (int w = blockIdx.x; w < units && !anchor_vload(&abort_flag); w += gridDim.x) {
+                int tile, l, plane, c;
+                if (!unit_of(w, tile, l, plane, c)) continue;
+                const CUtensorMap* ma = plane ? &tm_a1 : &tm_a0;
+                const int t0 = tile * kAnRows;
+                if (it > 0 && !mbar_wait(&adone, (unsigned)(it - 1) & 1u)) {
+                    atomicOr(&abort_flag, 1);
+                    break;
+                }
+                mbar_arrive_expect_tx(&afull, (unsigned)(V * K::kABytes));
+                for (int v = 0; v < V; ++v)
+                    tma_load_2d(asm_ + v * K::kABytes, ma, 0, ((c * V + v) * args.L + l) * args.n + t0, &afull);
+                ++an;
+                ++it;
             }
+            if (anchor_vload(&abort_flag)) drain_ring(&afull, 1, an);
         } else if (lane == 1) {
             int bn = 0, e = 0;  // Bt tiles armed; ring slot of the next
             unsigned ph = 0;     // phase parity of that slot's next fill
@@ -841,11 +847,12 @@ anchor_apply_kernel(const __grid_constant__ CUtensorMap tm_x0, const __grid_cons
             // pieces [32 k, 32 k + 32) of its 32 rows (conflict-free), taking each piece's
             // weight from its row's lane; the two warps of a lane quarter take alternate
             // steps.  The wait's outcome is made warp-uniform for the shuffles.
-            if (__all_sync(0xffffffffu, mbar_wait(&afull, (unsigned)it & 1u))) {
-                const float* wr = (plane ? args.w[1] : args.w[0]) + (((long long)c * args.L + l) * args.n + (row_ok ? t0 + m : 0)) * V;
-                float wmine[kAnMaxAnchors];
+            // the row's weights, loaded while the A tiles are still on their way
+            const float* wr = (plane ? args.w[1] : args.w[0]) + (((long long)c * args.L + l) * args.n + (row_ok ? t0 + m : 0)) * V;
+            float wmine[kAnMaxAnchors];
 #pragma unroll
-                for (int v = 0; v < kAnMaxAnchors; ++v) wmine[v] = (v < V && row_ok) ? wr[v] : 0.f;
+            for (int v = 0; v < kAnMaxAnchors; ++v) wmine[v] = (v < V && row_ok) ? wr[v] : 0.f;
+            if (__all_sync(0xffffffffu, mbar_wait(&afull, (unsigned)it & 1u))) {
                 constexpr int kPieces = K::kRowBytes / 16;  // 16-byte pieces per row (2, 4 or 8)
 #pragma unroll
                 for (int v = 0; v < kAnMaxAnchors; ++v) {
