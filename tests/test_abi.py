@@ -125,6 +125,33 @@ def test_host_validation_rejects_bad_arguments(lib):
                                      dm, None) == lib.EINVAL
 
 
+def test_anchor_shared_memory_admission(lib):
+    """Which (anchors, rank) the anchor kernels take: the resident first-factor tiles,
+    row sums and rings must fit one SM's shared memory.  Ranks 16 and 32 take all 16
+    anchors, rank 64 at most 8, for head_dim 64 and 128 alike.  A shape that fits gets
+    past the shape check and fails the next host check instead (no GPU involved)."""
+    L = lib.lib
+    fake = ctypes.c_void_p(1 << 20)
+    fake2 = ctypes.c_void_p(1 << 23)
+    far, far_v = ctypes.c_void_p(1 << 30), ctypes.c_void_p((1 << 30) + (1 << 26))
+    for H, D in ((8, 128), (2, 64)):
+        src = _desc(lib, C=1, L=1, n=256, H=H, D=D)
+        for rank in (16, 32, 64):
+            for anchors in range(1, 17):
+                fits = rank < 64 or anchors <= 8
+                st = L.kvfix_anchor_correct(fake, fake2, src, *([fake] * 8), anchors, rank, 0.0, fake, 1e4, None,
+                                            fake, fake2, far, far_v, src, None)
+                msg = L.kvfix_last_error()
+                assert st == lib.EINVAL
+                assert (b"temperature" in msg) == fits and (b"shared memory" in msg) == (not fits), \
+                    (H, D, rank, anchors, msg)
+                st = L.kvfix_anchor_gate(fake, src, fake, fake, anchors, rank, 0, 1.0, 0.5, fake, fake, fake, fake,
+                                         far, 1 << 20, None)
+                msg = L.kvfix_last_error()
+                assert st == lib.EINVAL
+                assert (b"prefix" in msg) == fits and (b"shared memory" in msg) == (not fits), (rank, anchors, msg)
+
+
 def test_version(lib):
     assert lib.version() == 100
 
