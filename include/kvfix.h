@@ -389,8 +389,9 @@ KVFIX_API kvfix_status kvfix_diff_restore(const kvfix_bf16* master_k, const kvfi
  *     A  : device bf16 [C][V][L][n][r]        (first factor, row t of the segment)
  *     Bt : device bf16 [C][V][L][F][r]        (second factor, stored transposed)
  * so that anchor v's state of layer l is A[c][v][l] * Bt[c][v][l]^T ([n x F]).
- * anchors: 1..16; rank: 16, 32 or 64 (anchors * rank limited by shared memory: the call
- * returns KVFIX_EINVAL for shapes that do not fit); F must be a multiple of 128.
+ * anchors: 1..16; rank: 16, 32 or 64 (the first-factor tiles of all anchors stay in
+ * shared memory: ranks 16 and 32 take up to 16 anchors, rank 64 up to 8; the calls return
+ * KVFIX_EINVAL for shapes that do not fit); F must be a multiple of 128.
  */
 
 /* Bytes of device workspace kvfix_anchor_gate needs for `src`, `anchors` and `prefix`. */
