@@ -1159,6 +1159,7 @@ PROFILE_CASES = {
     "round": lambda: synth.ROUND_QWEN14B.with_(layers=8),
     "diff": lambda: synth.SIBLINGS_8B.with_(layers=4),
     "lowrank": lambda: synth.LOWRANK_70B.with_(chunks=1, layers=8),
+    "draft": lambda: synth.LOWRANK_70B.with_(chunks=1, layers=8),
     "anchor": lambda: synth.ANCHOR_8B.with_(layers=8),
     "anchor_fused": lambda: synth.ANCHOR_8B.with_(layers=8),
     "diff_split": lambda: synth.SIBLINGS_8B.with_(layers=4),
@@ -1247,6 +1248,12 @@ def run_profile_case(name: str, iters: int = 3):
         fac = {k: inp[k] for k in ANCHOR_FACTORS}
         def step():
             kvfix.anchor_gate_correct(src["k"], src["v"], fac, cfg.tokens, inp["delta"], cfg.rope_base, tau=cfg.tau)
+    elif name == "draft":
+        # the unfused ranking (kvfix_draft_rank) on keys already corrected
+        inp = synth.lowrank_inputs(cfg, "cuda")
+        kt = kvfix.lowrank_apply(inp["x_k"], inp["a_k"], inp["b_k"])
+        def step():
+            kvfix.draft_rank(kt, inp["q"], cfg.layer_begin, cfg.k_rows)
     else:
         inp = synth.lowrank_inputs(cfg, "cuda")
         kt = torch.empty_like(inp["x_k"])
